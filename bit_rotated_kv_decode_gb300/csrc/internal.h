@@ -1,0 +1,123 @@
+// Internal declarations shared by the host library and the CUDA kernels.
+// Layout constants follow the record format documented in include/oscar.h.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace oscar {
+
+constexpr int D = 128;            // head_dim = quantisation group = Hadamard order
+constexpr int PAGE = 64;          // tokens per page
+constexpr int SINK = 64;          // BF16 sink tokens
+constexpr int RECENT = 256;       // BF16 recent window
+constexpr int RING_PAGES = RECENT / PAGE;
+constexpr int BF16_PAGES_PER_REQ = 1 + RING_PAGES;
+constexpr int CODE_BYTES = D / 4;              // 32
+constexpr int META_BYTES = 4;                  // fp16 s, fp16 z
+constexpr int K_CODES_OFF = 0;
+constexpr int V_CODES_OFF = PAGE * CODE_BYTES;             // 2048
+constexpr int K_META_OFF = 2 * PAGE * CODE_BYTES;          // 4096
+constexpr int V_META_OFF = K_META_OFF + PAGE * META_BYTES; // 4352
+constexpr int RECORD = V_META_OFF + PAGE * META_BYTES;     // 4608
+constexpr int BF16_RECORD_ELEMS = 2 * PAGE * D;            // K rows then V rows
+constexpr int MAX_G = 8;
+// decode partial per (work item, query head): o[128], m, l, 2 floats of padding
+// (a multiple of 16 bytes so o can be moved with 16-byte vector accesses)
+constexpr int PARTIAL_FLOATS = D + 4;
+constexpr int PARTIAL_M = D;
+constexpr int PARTIAL_L = D + 1;
+
+// sticky device error bits
+constexpr int ERR_INT2_PAGE = 1;
+constexpr int ERR_BF16_PAGE = 2;
+constexpr int ERR_LENGTH = 4;
+
+// Plain pointers into the cache's device memory.
+struct DevCache {
+  uint8_t* int2;
+  size_t int2_layer_stride;      // bytes
+  uint16_t* bf16;
+  size_t bf16_layer_stride;      // elements
+  const float* rot_k;            // [L][Hkv][D][D], x_rot = x R
+  const float* rot_v;
+  const float* rot_kt;           // transposes
+  const float* rot_vt;
+  const float* tau_k;            // [L][Hkv]
+  const float* tau_v;
+  int32_t* hist_pt;              // [max_requests][max_pages]
+  int32_t* bf16_pt;              // [max_requests][5]
+  int32_t* err;
+  int32_t L, Hq, Hkv, G, max_pages;
+  int64_t n_int2_pages, n_bf16_pages;
+  float scale;
+};
+
+// ---- page-table updates ---------------------------------------------------
+struct PtEntry {
+  int32_t table;   // 0 = hist_pt, 1 = bf16_pt
+  int32_t index;   // flat index into that table
+  int32_t value;
+};
+constexpr int PT_ENTRIES_PER_LAUNCH = 300;
+
+cudaError_t launch_pt_update(const DevCache& c, const PtEntry* entries, int n, cudaStream_t s);
+
+// ---- rotation set-up --------------------------------------------------------
+cudaError_t launch_rotation_setup(const DevCache& c, const float* rot_k_src, const float* rot_v_src,
+                                  float* rot_k, float* rot_v, float* rot_kt, float* rot_vt, cudaStream_t s);
+
+// ---- prefill ------------------------------------------------------------------
+// Copy input rows of positions [p0, p1) that fall in the sink or the recent ring.
+struct BF16Dest {
+  int32_t sink_page;
+  int32_t ring_page[RING_PAGES];
+};
+cudaError_t launch_prefill_bf16(const DevCache& c, int layer, const uint16_t* k, const uint16_t* v,
+                                int64_t in_base, int64_t p0, int64_t p1, BF16Dest dst, cudaStream_t s);
+// Rotate / clip / quantise / pack input positions [h0, h1) into history pages
+// read from the device page table row of `slot`.
+cudaError_t launch_prefill_hist(const DevCache& c, int layer, int slot, const uint16_t* k, const uint16_t* v,
+                                int64_t in_base, int64_t h0, int64_t h1, cudaStream_t s);
+
+// ---- append / demote ----------------------------------------------------------
+struct AppendReq {
+  int32_t slot;
+  int32_t in_row;          // row of the batch's k / v input (-1: demote only)
+  int32_t dst_page;        // BF16 page of the new token
+  int32_t dst_row;         // row inside it
+  int32_t demote_slot;     // history slot (0..63) of the demoted token, -1: none
+  int32_t hist_page;       // physical INT2 page receiving it
+  int32_t src_page;        // BF16 ring page holding the demoted token
+  int32_t src_row;
+  int32_t pt_index;        // >= 0: write hist_pt[slot][pt_index] = hist_page
+};
+constexpr int APPEND_PER_LAUNCH = 48;
+cudaError_t launch_append(const DevCache& c, int layer, const AppendReq* reqs, int n, const uint16_t* k,
+                          const uint16_t* v, cudaStream_t s);
+
+// ---- decode ---------------------------------------------------------------------
+struct DecodeReq {
+  int32_t slot;
+  int32_t batch_row;       // row of q / out
+  int32_t tokens;          // T
+  int32_t hist_end;
+  int32_t sink_page;
+  int32_t ring_page[RING_PAGES];
+  int32_t item_start;      // first work item of this request
+  int32_t chunks;          // INT2 chunks per kv head
+};
+constexpr int DECODE_PER_LAUNCH = 64;
+struct DecodePlan {
+  int n;
+  int pages_per_chunk;
+  int total_items;
+  size_t counter_bytes;
+  size_t partial_bytes;
+};
+cudaError_t launch_decode(const DevCache& c, int layer, const DecodeReq* reqs, const DecodePlan& plan,
+                          const uint16_t* q, float* out, void* workspace, cudaStream_t s);
+
+}  // namespace oscar

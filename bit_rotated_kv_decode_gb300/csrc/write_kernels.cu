@@ -1,0 +1,271 @@
+// Write path: page-table updates, rotation set-up, prefill-quantize and the
+// fused append + demote kernel.
+//
+// "Together AI Open-Sources OSCAR" (MarkTechPost), section "The Serving
+// System: Mixed-Precision Cache Layout": each history token is rotated by
+// R_K / R_V, clipped to the calibration threshold and quantised to per-token
+// asymmetric INT2; "TogetherAI开源OSCAR" (ModelScope), section "OSCAR的设计":
+// new tokens enter the BF16 recent window and the oldest recent token is
+// rotated, clipped, quantised and packed (4 codes per byte) into INT2 history.
+//
+// The rotated value of channel c of a token is the fp32 FMA chain
+//   acc_0 = 0, acc_{i+1} = fma(k_i, R[i][c], acc_i), i = 0..127,
+// in every kernel here, so prefill and sequential appends write identical bytes.
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "quant_device.cuh"
+
+namespace oscar {
+namespace {
+
+struct PtArgs {
+  int n;
+  PtEntry e[PT_ENTRIES_PER_LAUNCH];
+};
+
+__global__ void pt_update_kernel(int32_t* hist_pt, int32_t* bf16_pt, PtArgs a) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < a.n) {
+    int32_t* t = a.e[i].table == 0 ? hist_pt : bf16_pt;
+    t[a.e[i].index] = a.e[i].value;
+  }
+}
+
+__global__ void rotation_setup_kernel(const float* __restrict__ src_k, const float* __restrict__ src_v,
+                                      float* rk, float* rv, float* rkt, float* rvt, size_t mats) {
+  const size_t total = mats * D * D;
+  for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (size_t)gridDim.x * blockDim.x) {
+    const size_t m = idx / (D * D);
+    const int i = static_cast<int>((idx / D) % D);
+    const int j = static_cast<int>(idx % D);
+    const float a = src_k[idx];
+    const float b = src_v[idx];
+    rk[idx] = a;
+    rv[idx] = b;
+    rkt[m * D * D + (size_t)j * D + i] = a;
+    rvt[m * D * D + (size_t)j * D + i] = b;
+  }
+}
+
+__device__ __forceinline__ uint16_t* bf16_row(const DevCache& c, int layer, int page, int head, int which,
+                                              int row) {
+  return c.bf16 + layer * c.bf16_layer_stride + ((size_t)page * c.Hkv + head) * BF16_RECORD_ELEMS +
+         (size_t)which * PAGE * D + (size_t)row * D;
+}
+
+__device__ __forceinline__ uint8_t* int2_record(const DevCache& c, int layer, int page, int head) {
+  return c.int2 + layer * c.int2_layer_stride + ((size_t)page * c.Hkv + head) * RECORD;
+}
+
+// One position of the sink or the recent ring per block (x), K or V (y).
+__global__ void __launch_bounds__(128) prefill_bf16_kernel(DevCache c, int layer, const uint16_t* __restrict__ k,
+                                                           const uint16_t* __restrict__ v, int64_t in_base,
+                                                           int64_t p0, BF16Dest dst) {
+  const int64_t p = p0 + blockIdx.x;
+  const int which = blockIdx.y;
+  const uint16_t* src = (which ? v : k) + (size_t)(p - in_base) * c.Hkv * D;
+  int page, row;
+  if (p < SINK) {
+    page = dst.sink_page;
+    row = static_cast<int>(p);
+  } else {
+    const int slot = static_cast<int>((p - SINK) % RECENT);
+    page = dst.ring_page[slot / PAGE];
+    row = slot % PAGE;
+  }
+  if (page < 0 || page >= c.n_bf16_pages) {
+    if (threadIdx.x == 0) atomicOr(c.err, ERR_BF16_PAGE);
+    return;
+  }
+  for (int idx = threadIdx.x; idx < c.Hkv * (D / 8); idx += blockDim.x) {
+    const int head = idx / (D / 8);
+    const int part = idx % (D / 8);
+    const uint4 val = reinterpret_cast<const uint4*>(src + (size_t)head * D)[part];
+    reinterpret_cast<uint4*>(bf16_row(c, layer, page, head, which, row))[part] = val;
+  }
+}
+
+constexpr int KT_STRIDE = PAGE + 4;   // floats per row of the transposed input tile
+
+// Tile of up to 64 history positions (x) of one kv head (y), K or V (z).
+__global__ void __launch_bounds__(128) prefill_hist_kernel(DevCache c, int layer, int slot,
+                                                           const uint16_t* __restrict__ k,
+                                                           const uint16_t* __restrict__ v, int64_t in_base,
+                                                           int64_t h0, int64_t h1) {
+  extern __shared__ float4 smem4[];
+  float* sm = reinterpret_cast<float*>(smem4);
+  const int head = blockIdx.y;
+  const int which = blockIdx.z;
+  const int64_t t0 = h0 + (int64_t)blockIdx.x * PAGE;
+  const int ntok = static_cast<int>(h1 - t0 < PAGE ? h1 - t0 : PAGE);
+  const uint16_t* src = which ? v : k;
+  const size_t lh = (size_t)layer * c.Hkv + head;
+  const float* __restrict__ R = (which ? c.rot_v : c.rot_k) + lh * D * D;
+  const float tau = (which ? c.tau_v : c.tau_k)[lh];
+
+  for (int idx = threadIdx.x; idx < PAGE * D; idx += blockDim.x) {
+    const int j = idx / D;
+    const int i = idx % D;
+    float val = 0.0f;
+    if (j < ntok) val = bf16_bits_to_float(src[((size_t)(t0 + j - in_base) * c.Hkv + head) * D + i]);
+    sm[i * KT_STRIDE + j] = val;
+  }
+  __syncthreads();
+
+  const int co = threadIdx.x;
+  float acc[PAGE];
+#pragma unroll
+  for (int j = 0; j < PAGE; ++j) acc[j] = 0.0f;
+  for (int i = 0; i < D; ++i) {
+    const float r = __ldg(R + i * D + co);
+    const float4* kr = reinterpret_cast<const float4*>(sm + i * KT_STRIDE);
+#pragma unroll
+    for (int j4 = 0; j4 < PAGE / 4; ++j4) {
+      const float4 kk = kr[j4];
+      acc[4 * j4 + 0] = fmaf(kk.x, r, acc[4 * j4 + 0]);
+      acc[4 * j4 + 1] = fmaf(kk.y, r, acc[4 * j4 + 1]);
+      acc[4 * j4 + 2] = fmaf(kk.z, r, acc[4 * j4 + 2]);
+      acc[4 * j4 + 3] = fmaf(kk.w, r, acc[4 * j4 + 3]);
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < PAGE; ++j) sm[j * D + co] = acc[j];
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int32_t* pt = c.hist_pt + (size_t)slot * c.max_pages;
+  for (int j = warp; j < ntok; j += 4) {
+    const float4 x = *reinterpret_cast<const float4*>(sm + j * D + 4 * lane);
+    const GroupCode g = quantize_group_warp(x, tau);
+    const int64_t h = t0 + j - SINK;
+    const int32_t page = pt[h / PAGE];
+    const int row = static_cast<int>(h % PAGE);
+    if (page < 0 || page >= c.n_int2_pages) {
+      if (lane == 0) atomicOr(c.err, ERR_INT2_PAGE);
+      continue;
+    }
+    uint8_t* rec = int2_record(c, layer, page, head);
+    rec[(which ? V_CODES_OFF : K_CODES_OFF) + row * CODE_BYTES + lane] = static_cast<uint8_t>(g.byte);
+    if (lane == 0) {
+      *reinterpret_cast<uint32_t*>(rec + (which ? V_META_OFF : K_META_OFF) + row * META_BYTES) =
+          static_cast<uint32_t>(g.s_bits) | (static_cast<uint32_t>(g.z_bits) << 16);
+    }
+  }
+}
+
+struct AppendArgs {
+  int n;
+  AppendReq r[APPEND_PER_LAUNCH];
+};
+
+// One request (x), kv head (y), K or V (z) per block of 128 threads: demote the
+// token in the ring slot (if any), then write the new token into its slot.
+__global__ void __launch_bounds__(128) append_kernel(DevCache c, int layer, const uint16_t* __restrict__ k,
+                                                     const uint16_t* __restrict__ v, AppendArgs a) {
+  __shared__ float xin[D];
+  __shared__ float xrot[D];
+  const AppendReq q = a.r[blockIdx.x];
+  const int head = blockIdx.y;
+  const int which = blockIdx.z;
+  const int t = threadIdx.x;
+  const size_t lh = (size_t)layer * c.Hkv + head;
+
+  if (q.demote_slot >= 0) {
+    const bool ok_src = q.src_page >= 0 && q.src_page < c.n_bf16_pages;
+    const bool ok_dst = q.hist_page >= 0 && q.hist_page < c.n_int2_pages;
+    if (!ok_src || !ok_dst) {
+      if (t == 0) atomicOr(c.err, ok_src ? ERR_INT2_PAGE : ERR_BF16_PAGE);
+    } else {
+      xin[t] = bf16_bits_to_float(bf16_row(c, layer, q.src_page, head, which, q.src_row)[t]);
+      __syncthreads();
+      const float* __restrict__ R = (which ? c.rot_v : c.rot_k) + lh * D * D;
+      float acc = 0.0f;
+#pragma unroll 8
+      for (int i = 0; i < D; ++i) acc = fmaf(xin[i], __ldg(R + i * D + t), acc);
+      xrot[t] = acc;
+      __syncthreads();
+      if (t < 32) {
+        const float tau = (which ? c.tau_v : c.tau_k)[lh];
+        const float4 x = *reinterpret_cast<const float4*>(xrot + 4 * t);
+        const GroupCode g = quantize_group_warp(x, tau);
+        uint8_t* rec = int2_record(c, layer, q.hist_page, head);
+        rec[(which ? V_CODES_OFF : K_CODES_OFF) + q.demote_slot * CODE_BYTES + t] = static_cast<uint8_t>(g.byte);
+        if (t == 0) {
+          *reinterpret_cast<uint32_t*>(rec + (which ? V_META_OFF : K_META_OFF) + q.demote_slot * META_BYTES) =
+              static_cast<uint32_t>(g.s_bits) | (static_cast<uint32_t>(g.z_bits) << 16);
+        }
+      }
+      if (q.pt_index >= 0 && head == 0 && which == 0 && t == 0) {
+        c.hist_pt[(size_t)q.slot * c.max_pages + q.pt_index] = q.hist_page;
+      }
+    }
+  }
+  __syncthreads();   // the demoted row has been read before its slot is overwritten
+  if (q.in_row >= 0) {
+    if (q.dst_page < 0 || q.dst_page >= c.n_bf16_pages) {
+      if (t == 0) atomicOr(c.err, ERR_BF16_PAGE);
+      return;
+    }
+    const uint16_t* src = (which ? v : k) + ((size_t)q.in_row * c.Hkv + head) * D;
+    bf16_row(c, layer, q.dst_page, head, which, q.dst_row)[t] = src[t];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_pt_update(const DevCache& c, const PtEntry* entries, int n, cudaStream_t s) {
+  for (int base = 0; base < n; base += PT_ENTRIES_PER_LAUNCH) {
+    PtArgs a;
+    a.n = n - base < PT_ENTRIES_PER_LAUNCH ? n - base : PT_ENTRIES_PER_LAUNCH;
+    for (int i = 0; i < a.n; ++i) a.e[i] = entries[base + i];
+    pt_update_kernel<<<(a.n + 127) / 128, 128, 0, s>>>(c.hist_pt, c.bf16_pt, a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_rotation_setup(const DevCache& c, const float* rot_k_src, const float* rot_v_src, float* rot_k,
+                                  float* rot_v, float* rot_kt, float* rot_vt, cudaStream_t s) {
+  const size_t mats = (size_t)c.L * c.Hkv;
+  rotation_setup_kernel<<<1024, 256, 0, s>>>(rot_k_src, rot_v_src, rot_k, rot_v, rot_kt, rot_vt, mats);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_bf16(const DevCache& c, int layer, const uint16_t* k, const uint16_t* v, int64_t in_base,
+                                int64_t p0, int64_t p1, BF16Dest dst, cudaStream_t s) {
+  if (p1 <= p0) return cudaSuccess;
+  dim3 grid(static_cast<unsigned>(p1 - p0), 2);
+  prefill_bf16_kernel<<<grid, 128, 0, s>>>(c, layer, k, v, in_base, p0, dst);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_hist(const DevCache& c, int layer, int slot, const uint16_t* k, const uint16_t* v,
+                                int64_t in_base, int64_t h0, int64_t h1, cudaStream_t s) {
+  if (h1 <= h0) return cudaSuccess;
+  const size_t smem = (size_t)D * KT_STRIDE * sizeof(float);
+  static_assert(D * KT_STRIDE >= PAGE * D, "tile buffer reused for the rotated values");
+  dim3 grid(static_cast<unsigned>((h1 - h0 + PAGE - 1) / PAGE), c.Hkv, 2);
+  prefill_hist_kernel<<<grid, 128, smem, s>>>(c, layer, slot, k, v, in_base, h0, h1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append(const DevCache& c, int layer, const AppendReq* reqs, int n, const uint16_t* k,
+                          const uint16_t* v, cudaStream_t s) {
+  for (int base = 0; base < n; base += APPEND_PER_LAUNCH) {
+    AppendArgs a;
+    a.n = n - base < APPEND_PER_LAUNCH ? n - base : APPEND_PER_LAUNCH;
+    for (int i = 0; i < a.n; ++i) a.r[i] = reqs[base + i];
+    dim3 grid(a.n, c.Hkv, 2);
+    append_kernel<<<grid, 128, 0, s>>>(c, layer, k, v, a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace oscar

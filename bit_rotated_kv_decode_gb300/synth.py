@@ -145,7 +145,7 @@ def queries(cfg: int, layer: int, num_q_heads: int, n: int, step: int, device="c
     g = _gen(device, seed_for(cfg, layer, 0, purpose, step=step + 1))
     z = torch.randn((n, num_q_heads, HEAD_DIM), generator=g, device=device, dtype=torch.float32)
     q = torch.einsum("nhi,hoi->nho", z, mix) / np.sqrt(HEAD_DIM)
-    return q.to(torch.bfloat16)
+    return q.to(torch.bfloat16).contiguous()
 
 
 def calibration_set(cfg: int, layer: int, num_q_heads: int, num_kv_heads: int, n: int = 512,

@@ -10,7 +10,8 @@ Readings (the pages give no formula):
   * x = k . R evaluated exactly, then rounded once to fp32 -- fp32 is the
     precision the kernels take every quantisation decision in, so the oracle
     takes them in fp32 too;
-  * clip: x <- min(max(x, -tau), tau) with the stored fp32 tau;
+  * clip: x <- min(max(x, -tau), tau) with the stored fp32 tau, then + 0 so a
+    signed zero becomes +0 (IEEE: -0 + +0 = +0) and min/max are unambiguous;
   * z = fp16_rn(min x), s = fp16_rn(fl32(fl32(max x - min x) / 3));
   * code = clamp(rint_half_even(fl32(fl32(x - z) / s)), 0, 3), code = 0 when
     s == 0;
@@ -84,7 +85,7 @@ def quantize_groups(x32: np.ndarray, tau: np.float32):
     """
     x32 = np.asarray(x32, dtype=np.float32)
     tau = np.float32(tau)
-    xc = np.minimum(np.maximum(x32, -tau), tau)
+    xc = (np.minimum(np.maximum(x32, -tau), tau) + np.float32(0.0)).astype(np.float32)
     mn = xc.min(axis=-1)
     mx = xc.max(axis=-1)
     z = mn.astype(np.float16)
@@ -102,7 +103,7 @@ def quantize_groups(x32: np.ndarray, tau: np.float32):
 def t_values(x32: np.ndarray, tau: np.float32, s: np.ndarray, z: np.ndarray) -> np.ndarray:
     """The fp32 t = (clip(x) - z) / s each code was rounded from (for exemption bands)."""
     tau = np.float32(tau)
-    xc = np.minimum(np.maximum(np.asarray(x32, np.float32), -tau), tau)
+    xc = (np.minimum(np.maximum(np.asarray(x32, np.float32), -tau), tau) + np.float32(0.0)).astype(np.float32)
     zf = z.astype(np.float32)[..., None]
     sf = s.astype(np.float32)[..., None]
     with np.errstate(divide="ignore", invalid="ignore"):

@@ -54,6 +54,13 @@ def test_constant_group_gives_zero_scale():
     assert float(z[0]) == float(np.float16(0.3))
 
 
+def test_signed_zero_is_canonical():
+    x = np.zeros(128, dtype=np.float32)
+    x[:64] = -0.0
+    c, s, z = quant.quantize_groups(x[None], np.float32(1.0))
+    assert z.view(np.uint16)[0] == 0 and s.view(np.uint16)[0] == 0
+
+
 def test_fp16_round_to_nearest_even():
     # 1 + 2^-11 is halfway between 1 and 1 + 2^-10: ties go to the even mantissa
     assert float(np.float32(1 + 2 ** -11).astype(np.float16)) == 1.0
