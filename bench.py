@@ -1,0 +1,487 @@
+"""Benchmark of the three-segment INT2 KV-cache hot path on GB300.
+
+Default workload (N = 1): Qwen3-8B attention shape, 32 layers, 32 query / 8 KV
+heads, head_dim 128, batch 1, 100,000-token context (64 BF16 sink + 99,680
+INT2 history + 256 BF16 recent), 64-token pages in a seeded random physical
+order.  One step = for every layer: append one token (demoting the oldest
+recent token into INT2 history) and run decode attention over the whole
+cache.  Inputs are synthetic (seeded generator), resident in HBM before the
+timed region; the step's data (1.9 GB) is far larger than the 129 MB L2.
+
+Prints one JSON line.  ``--impl reference`` times the float64 oracle on the
+host cores instead (a bounded sample of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention µs/step & KV HBM GB/s (frac of 8 TB/s) at 100K ctx; demote tok/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+INT2_BYTES_PER_TOKEN_HEAD = 72          # 2 x (32 code bytes + 4 meta bytes)
+BF16_BYTES_PER_TOKEN_HEAD = 512         # K and V rows of 128 bf16
+
+WORKLOADS = {
+    2: dict(name="qwen3-8b-100k-decode", layers=32, q_heads=32, kv_heads=8, batch=1, context=100000),
+    4: dict(name="qwen3-32b-128k-b8-decode", layers=64, q_heads=64, kv_heads=8, batch=8, context=131072),
+}
+
+
+# ----------------------------------------------------------------------------------------------
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Max of a float over all ranks (identity on one rank)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def measured_peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def committed_traffic(kernel: str):
+    """Per-launch DRAM bytes of a kernel from the committed ncu summary, if current."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            entry = json.load(f)[kernel]
+    except Exception:
+        return None
+    src = os.path.join(ROOT, "bit_rotated_kv_decode_gb300", "csrc", entry["source"])
+    import hashlib
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return entry["bytes_per_launch"] if digest == entry.get("source_sha256_16") else None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------------------------
+def pages_for(hist_end: int) -> int:
+    return (hist_end - 64 + 63) // 64 if hist_end > 64 else 0
+
+
+def algorithmic_bytes(tokens: int, hist_end: int, kv_heads: int) -> int:
+    """Bytes one decode of one request must read: INT2 codes + fp16 meta + BF16 segments."""
+    n_hist = max(0, hist_end - 64)
+    n_bf16 = min(tokens, 64) + (tokens - hist_end if tokens > 64 else 0)
+    return kv_heads * (n_hist * INT2_BYTES_PER_TOKEN_HEAD + n_bf16 * BF16_BYTES_PER_TOKEN_HEAD)
+
+
+class Workload:
+    """The cache, its rotations and every input of the timed steps, resident on the GPU."""
+
+    def __init__(self, cfg_id: int, steps_total: int, log):
+        import torch
+        from bit_rotated_kv_decode_gb300 import binding, build, calibrate, synth
+        build.build()
+        self.torch = torch
+        self.b = binding
+        self.synth = synth
+        w = WORKLOADS[cfg_id]
+        self.cfg_id = cfg_id
+        self.w = w
+        self.L, self.hq, self.hkv, self.batch, self.T0 = (w["layers"], w["q_heads"], w["kv_heads"], w["batch"],
+                                                        w["context"])
+        self.drift = cfg_id == 4
+        t = time.time()
+        fit = None if self.L <= 32 else list(range(0, self.L, 8))
+        self.rk, self.rv, self.tk, self.tv = calibrate.calibrate_model(cfg_id, self.L, self.hq, self.hkv,
+                                                                       drift=self.drift, layers=fit)
+        log(f"calibration {time.time() - t:.1f}s")
+        max_pages = pages_for(self.T0 + steps_total + 64) + 1
+        seed = synth.seed_for(cfg_id, 0, 0, 99) or 1
+        cfg = binding.make_config(self.L, self.hq, self.hkv, self.batch, max_pages, self.batch * max_pages + 8,
+                                  0, 0.0, seed)
+        self.cache = binding.OscarCache(cfg, torch.from_numpy(self.rk).cuda(), torch.from_numpy(self.rv).cuda(),
+                                        self.tk, self.tv)
+        self.reqs = [self.cache.open() for _ in range(self.batch)]
+        t = time.time()
+        for layer in range(self.L):
+            for i, r in enumerate(self.reqs):
+                k = synth.kv_tokens(cfg_id, layer, self.hkv, "k", range(0, self.T0), total_len=self.T0,
+                                    drift=self.drift, device="cuda", stream_id=i)
+                v = synth.kv_tokens(cfg_id, layer, self.hkv, "v", range(0, self.T0), total_len=self.T0,
+                                    drift=self.drift, device="cuda", stream_id=i)
+                self.cache.prefill(r, layer, k, v)
+                del k, v
+        torch.cuda.synchronize()
+        self.cache.check()
+        log(f"prefill {time.time() - t:.1f}s")
+        # inputs of every step: new k / v per layer, q per layer
+        n = steps_total
+        self.k_new = torch.empty((n, self.L, self.batch, self.hkv, 128), dtype=torch.bfloat16, device="cuda")
+        self.v_new = torch.empty_like(self.k_new)
+        self.q = torch.empty((n, self.L, self.batch, self.hq, 128), dtype=torch.bfloat16, device="cuda")
+        for layer in range(self.L):
+            mix = synth.query_mix(cfg_id, layer, self.hq, device="cuda")
+            for i in range(self.batch):
+                self.k_new[:, layer, i] = synth.kv_tokens(cfg_id, layer, self.hkv, "k", range(self.T0, self.T0 + n),
+                                                          total_len=self.T0, drift=self.drift, device="cuda",
+                                                          stream_id=i)
+                self.v_new[:, layer, i] = synth.kv_tokens(cfg_id, layer, self.hkv, "v", range(self.T0, self.T0 + n),
+                                                          total_len=self.T0, drift=self.drift, device="cuda",
+                                                          stream_id=i)
+            for s in range(n):
+                self.q[s, layer] = synth.queries(cfg_id, layer, self.hq, self.batch, s, device="cuda", mix=mix)
+        self.out = torch.empty((self.L, self.batch, self.hq, 128), dtype=torch.float32, device="cuda")
+        ws_bytes = self.cache.workspace_bytes(self.reqs) + (1 << 20)
+        self.ws = binding.new_workspace(ws_bytes)
+        self.step_index = 0
+        # raw C entry points with pre-marshalled arguments (the binding's own calls, minus re-marshalling)
+        self.lib = self.cache.lib
+        self.h = self.cache.h
+        self.reqs_arr = (ctypes.c_int32 * self.batch)(*self.reqs)
+        self.ws_ptr = self.ws.data_ptr()
+        self.ws_len = self.ws.numel()
+
+    def stream_ptr(self):
+        return self.torch.cuda.current_stream().cuda_stream
+
+    def run_step(self, s: int, stream, dec_events=None, app_events=None):
+        """One step: every layer appends (with demotion) and decodes."""
+        lib, h, n, ra = self.lib, self.h, self.batch, self.reqs_arr
+        kn, vn, q, out = self.k_new[s], self.v_new[s], self.q[s], self.out
+        for layer in range(self.L):
+            if app_events is not None:
+                app_events[layer][0].record()
+            st = lib.oscar_append(h, layer, n, ra, kn[layer].data_ptr(), vn[layer].data_ptr(), stream)
+            if app_events is not None:
+                app_events[layer][1].record()
+            if st:
+                raise RuntimeError(f"append failed: {lib.oscar_last_error(h).decode()}")
+            if dec_events is not None:
+                dec_events[layer][0].record()
+            st = lib.oscar_decode_attention(h, layer, n, ra, q[layer].data_ptr(), out[layer].data_ptr(),
+                                            self.ws_ptr, self.ws_len, stream)
+            if dec_events is not None:
+                dec_events[layer][1].record()
+            if st:
+                raise RuntimeError(f"decode failed: {lib.oscar_last_error(h).decode()}")
+
+    def decode_bytes(self, layer: int) -> int:
+        tot = 0
+        for r in self.reqs:
+            t, he = self.cache.length(r, layer)
+            tot += algorithmic_bytes(t, he, self.hkv)
+        return tot
+
+
+def run_gpu(args, log):
+    import torch
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    W, K = args.warmup, args.steps
+    ew, ek = 2, max(3, K // 2)
+    wl = Workload(args.config, W + K + ew + ek, log)
+    stream = wl.stream_ptr()
+    L = wl.L
+    # --- device-resident timing ---------------------------------------------------------------
+    for s in range(W):
+        wl.run_step(s, stream)
+    torch.cuda.synchronize()
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    dec = [[(mk(), mk()) for _ in range(L)] for _ in range(K)]
+    app = [[(mk(), mk()) for _ in range(L)] for _ in range(K)]
+    bytes_per_launch = []
+    start, end = mk(), mk()
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        start.record()
+        for i in range(K):
+            wl.run_step(W + i, stream, dec[i], app[i])
+            bytes_per_launch.append(np.mean([wl.decode_bytes(layer) for layer in (0, L - 1)]))
+        end.record()
+        torch.cuda.synchronize()
+        barrier(world)
+    wl.cache.check()
+    total_ms = start.elapsed_time(end)
+    total_ms = max_over_ranks(total_ms, world)
+    us_step = 1000.0 * total_ms / K
+    dec_us = [1000.0 * a.elapsed_time(b) for row in dec for (a, b) in row]
+    app_us = [1000.0 * a.elapsed_time(b) for row in app for (a, b) in row]
+    dec_avg = float(np.mean(dec_us))
+    app_avg = float(np.mean(app_us))
+    bpl = float(np.mean(bytes_per_launch))
+    # --- end to end: host (pinned) inputs copied in and outputs copied out inside the timed region
+    kh = wl.k_new[W + K:].cpu().pin_memory()
+    vh = wl.v_new[W + K:].cpu().pin_memory()
+    qh = wl.q[W + K:].cpu().pin_memory()
+    oh = torch.empty((ew + ek,) + tuple(wl.out.shape), dtype=torch.float32).pin_memory()
+    base = W + K
+    for i in range(ew + ek):
+        if i == ew:
+            torch.cuda.synchronize()
+            barrier(world)
+            e0 = mk()
+            e0.record()
+        wl.k_new[base + i].copy_(kh[i], non_blocking=True)
+        wl.v_new[base + i].copy_(vh[i], non_blocking=True)
+        wl.q[base + i].copy_(qh[i], non_blocking=True)
+        wl.run_step(base + i, stream)
+        oh[i].copy_(wl.out, non_blocking=True)
+    e1 = mk()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e_us = 1000.0 * e2e_ms / ek
+    h2d = (kh[0].numel() + vh[0].numel() + qh[0].numel()) * 2
+    d2h = oh[0].numel() * 4
+    peak, peak_kind = measured_peak_hbm()
+    achieved = bpl / (dec_avg * 1e-6) / 1e9
+    res = {
+        "us_step": us_step, "dec_avg_us": dec_avg, "app_avg_us": app_avg, "bytes_per_launch": bpl,
+        "achieved_gbs": achieved, "peak": peak, "peak_kind": peak_kind, "e2e_us": e2e_us, "h2d": h2d, "d2h": d2h,
+        "clocks": clk.summary(), "launches": K * L * 2, "world": world, "rank": rank,
+    }
+    return wl, res
+
+
+# ----------------------------------------------------------------------------------------------
+def oracle_inputs(wl, layer: int):
+    """Host float64 K / V of request 0 of one layer at the cache's current state."""
+    import torch
+    hkv = wl.hkv
+    r = wl.reqs[0]
+    t, he = wl.cache.length(r, layer)
+    n_new = t - wl.T0
+    k0 = wl.synth.kv_tokens(wl.cfg_id, layer, hkv, "k", range(0, wl.T0), total_len=wl.T0, drift=wl.drift,
+                            device="cuda", stream_id=0)
+    v0 = wl.synth.kv_tokens(wl.cfg_id, layer, hkv, "v", range(0, wl.T0), total_len=wl.T0, drift=wl.drift,
+                            device="cuda", stream_id=0)
+    k = torch.cat([k0, wl.k_new[:n_new, layer, 0]]).float().cpu().numpy().astype(np.float64)
+    v = torch.cat([v0, wl.v_new[:n_new, layer, 0]]).float().cpu().numpy().astype(np.float64)
+    del k0, v0
+    return k, v, t, he
+
+
+def cpu_baseline(wl, res, log):
+    """Time the oracle on the host cores for layer 0 of request 0 and check the GPU output there."""
+    import torch
+    from oracle import attention
+    from tests import parity
+    layer = 0
+    k, v, t, he = oracle_inputs(wl, layer)
+    # recompute layer 0's decode on the GPU at this exact state and compare
+    q = wl.q[0, layer].contiguous()
+    out = torch.empty((wl.batch, wl.hq, 128), dtype=torch.float32, device="cuda")
+    wl.cache.decode(layer, wl.reqs, q, out, wl.ws)
+    wl.cache.check()
+    qf = q[0].float().cpu().numpy().astype(np.float64)
+    cores = len(os.sched_getaffinity(0))
+    t0 = time.time()
+    ref = attention.decode(qf, k, v, he, wl.rk[layer].astype(np.float64), wl.rv[layer].astype(np.float64),
+                           wl.tk[layer], wl.tv[layer])
+    secs = time.time() - t0
+    par = parity.check_output(out[0].cpu().numpy(), ref)
+    return {
+        "value": secs * 1e6 * wl.L,
+        "unit": "us/step",
+        "cores": cores,
+        "kind": "oracle",
+        "sample": f"layer {layer} of {wl.L}, request 0, all {wl.hq} query heads over {t} tokens "
+                  f"(oracle quantises the history itself), extrapolated x{wl.L} layers; "
+                  f"measured {secs:.2f} s for the sample",
+    }, {"layer": layer, "tokens": t, "hist_end": he, **par,
+        "thresholds": {"max_abs": parity.OUT_MAX_ABS, "rel_fro": parity.OUT_REL_FRO}}
+
+
+# ----------------------------------------------------------------------------------------------
+def run_reference(args, log):
+    """The oracle as it stands, timed on the host cores on a bounded sample per step."""
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return None
+    import torch
+    from bit_rotated_kv_decode_gb300 import calibrate, synth
+    from oracle import attention
+    w = WORKLOADS[args.config]
+    L, hq, hkv, T = w["layers"], w["q_heads"], w["kv_heads"], w["context"]
+    g = hq // hkv
+    rk, rv, tk, tv = calibrate.calibrate_model(args.config, 1, hq, hkv)
+    # one kv head (its GQA group of query heads) of layer 0 per step, drawn on the host
+    k = synth.kv_tokens(args.config, 0, hkv, "k", range(0, T), total_len=T).to(torch.float64).numpy()[:, :1]
+    v = synth.kv_tokens(args.config, 0, hkv, "v", range(0, T), total_len=T).to(torch.float64).numpy()[:, :1]
+    cores = len(os.sched_getaffinity(0))
+    times = []
+    for s in range(args.warmup + args.steps):
+        q = synth.queries(args.config, 0, hq, 1, s).to(torch.float64).numpy()[0, :g]
+        t0 = time.time()
+        attention.decode(q, k, v, T - 256, rk[0, :1].astype(np.float64), rv[0, :1].astype(np.float64),
+                         tk[0, :1], tv[0, :1])
+        if s >= args.warmup:
+            times.append(time.time() - t0)
+    per_step_us = float(np.mean(times)) * 1e6 * hkv * L
+    sample = (f"layer 0, kv head 0 and its {g} query heads over {T} tokens per step, "
+              f"extrapolated x{hkv} kv heads x{L} layers")
+    return {
+        "metric": METRIC, "impl": "reference", "value": per_step_us, "unit": "us/step", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step_us / 1000.0, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w["name"], "layers": L, "q_heads": hq, "kv_heads": hkv, "batch": w["batch"],
+                   "context": T},
+        "cpu_baseline": {"value": per_step_us, "unit": "us/step", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": per_step_us, "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------------------------------------
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--config", type=int, default=2, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, _ = dist_info()
+    log = (lambda m: print(f"[bench] {m}", file=sys.stderr, flush=True)) if rank == 0 else (lambda m: None)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "gb300" else "gloo")
+    if args.impl == "reference":
+        line = run_reference(args, log)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    wl, r = run_gpu(args, log)
+    w = WORKLOADS[args.config]
+    cpu = par = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu, par = cpu_baseline(wl, r, log)
+    traffic = committed_traffic("decode_kernel")
+    kv_gbs = r["bytes_per_launch"] * wl.L / (r["us_step"] * 1e-6) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": r["us_step"],
+        "unit": "us/step",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": r["us_step"] / 1000.0,
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp32",
+        "data": "synthetic",
+        "config": {"workload": w["name"], "layers": wl.L, "q_heads": wl.hq, "kv_heads": wl.hkv, "head_dim": 128,
+                   "batch": wl.batch, "context": wl.T0, "page_tokens": 64, "page_order": "seeded shuffle",
+                   "storage": "INT2 codes + fp16 scale/zero history, BF16 sink/recent",
+                   "step": "per layer: append (fused demote) + decode attention",
+                   "l2": "inputs larger than L2 (%.2f GB of KV per step vs 129 MB L2)" % (
+                       r["bytes_per_launch"] * wl.L / 1e9),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "kv_gbs_step": kv_gbs,
+        "kv_frac_of_8tbs_step": kv_gbs / NOMINAL_HBM_GBS,
+        "decode_us_per_layer": r["dec_avg_us"],
+        "append_us_per_layer": r["app_avg_us"],
+        "demote_tok_s": wl.batch * 1e6 / r["app_avg_us"],
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": r["achieved_gbs"], "peak": r["peak"],
+                     "unit": "GB/s", "frac": r["achieved_gbs"] / r["peak"], "peak_source": r["peak_kind"],
+                     "traffic": traffic, "algorithmic_bytes_per_launch": r["bytes_per_launch"]},
+        "e2e": {"value": r["e2e_us"], "unit": "us/step", "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+        line["parity"] = par
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

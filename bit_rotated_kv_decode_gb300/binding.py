@@ -43,7 +43,8 @@ class oscar_cache_layout(ctypes.Structure):
     _fields_ = [(name, c_size_t) for name in (
         "total_bytes", "int2_pool_offset", "int2_layer_stride", "int2_page_stride", "int2_record_bytes",
         "bf16_pool_offset", "bf16_layer_stride", "bf16_page_stride", "bf16_record_bytes",
-        "rot_k_offset", "rot_v_offset", "rot_kt_offset", "rot_vt_offset", "tau_k_offset", "tau_v_offset",
+        "rot_k_offset", "rot_v_offset", "rot_kt_offset", "rot_vt_offset", "rot_colnorm_offset",
+        "tau_k_offset", "tau_v_offset",
         "hist_pt_offset", "bf16_pt_offset", "error_word_offset")]
 
 

@@ -156,6 +156,8 @@ oscar_cache_layout make_layout(const oscar_cache_config& c) {
   off += rot;
   l.rot_vt_offset = off;
   off += rot;
+  l.rot_colnorm_offset = off;
+  off += align256(2 * L * H * sizeof(float));
   const size_t tau = align256(L * H * sizeof(float));
   l.tau_k_offset = off;
   off += tau;
@@ -237,6 +239,8 @@ oscar_status oscar_cache_create(const oscar_cache_config* cfg, void* device_mem,
   d.rot_v = rv;
   d.rot_kt = rkt;
   d.rot_vt = rvt;
+  float* rcn = reinterpret_cast<float*>(base + c->lay.rot_colnorm_offset);
+  d.rot_cn = rcn;
   d.tau_k = reinterpret_cast<float*>(base + c->lay.tau_k_offset);
   d.tau_v = reinterpret_cast<float*>(base + c->lay.tau_v_offset);
   d.hist_pt = reinterpret_cast<int32_t*>(base + c->lay.hist_pt_offset);
@@ -255,7 +259,7 @@ oscar_status oscar_cache_create(const oscar_cache_config* cfg, void* device_mem,
     e = cudaMemsetAsync(d.hist_pt, 0xff, (size_t)c->cfg.max_requests * c->cfg.max_pages_per_request * 4, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(d.bf16_pt, 0xff, (size_t)c->cfg.max_requests * BF16_PAGES_PER_REQ * 4, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(d.err, 0, 4, s);
-  if (e == cudaSuccess) e = launch_rotation_setup(d, rot_k, rot_v, rk, rv, rkt, rvt, s);
+  if (e == cudaSuccess) e = launch_rotation_setup(d, rot_k, rot_v, rk, rv, rkt, rvt, rcn, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) {
     delete c;

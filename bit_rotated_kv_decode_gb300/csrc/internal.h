@@ -45,6 +45,7 @@ struct DevCache {
   const float* rot_v;
   const float* rot_kt;           // transposes
   const float* rot_vt;
+  const float* rot_cn;           // [2][L][Hkv]: max column norm of R_K, then R_V (rounded up)
   const float* tau_k;            // [L][Hkv]
   const float* tau_v;
   int32_t* hist_pt;              // [max_requests][max_pages]
@@ -67,7 +68,8 @@ cudaError_t launch_pt_update(const DevCache& c, const PtEntry* entries, int n, c
 
 // ---- rotation set-up --------------------------------------------------------
 cudaError_t launch_rotation_setup(const DevCache& c, const float* rot_k_src, const float* rot_v_src,
-                                  float* rot_k, float* rot_v, float* rot_kt, float* rot_vt, cudaStream_t s);
+                                  float* rot_k, float* rot_v, float* rot_kt, float* rot_vt, float* rot_cn,
+                                  cudaStream_t s);
 
 // ---- prefill ------------------------------------------------------------------
 // Copy input rows of positions [p0, p1) that fall in the sink or the recent ring.

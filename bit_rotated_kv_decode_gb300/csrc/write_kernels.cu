@@ -49,6 +49,24 @@ __global__ void rotation_setup_kernel(const float* __restrict__ src_k, const flo
   }
 }
 
+// Largest column norm of each matrix (K matrices, then V), rounded up so it
+// bounds the exact norm: one block per matrix, one thread per column.
+__global__ void __launch_bounds__(D) colnorm_kernel(const float* __restrict__ src_k, const float* __restrict__ src_v,
+                                                    float* out, int mats) {
+  __shared__ float red[D];
+  const int m = blockIdx.x;
+  const float* R = (m < mats ? src_k : src_v) + (size_t)(m % mats) * D * D;
+  float acc = 0.0f;
+  for (int i = 0; i < D; ++i) acc = __fmaf_ru(R[i * D + threadIdx.x], R[i * D + threadIdx.x], acc);
+  red[threadIdx.x] = __fsqrt_ru(__fmul_ru(acc, 1.0001f));
+  __syncthreads();
+  for (int w = D / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) red[threadIdx.x] = fmaxf(red[threadIdx.x], red[threadIdx.x + w]);
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) out[m] = red[0];
+}
+
 __device__ __forceinline__ uint16_t* bf16_row(const DevCache& c, int layer, int page, int head, int which,
                                               int row) {
   return c.bf16 + layer * c.bf16_layer_stride + ((size_t)page * c.Hkv + head) * BF16_RECORD_ELEMS +
@@ -88,6 +106,7 @@ __global__ void __launch_bounds__(128) prefill_bf16_kernel(DevCache c, int layer
 }
 
 constexpr int KT_STRIDE = PAGE + 4;   // floats per row of the transposed input tile
+constexpr size_t PREFILL_SMEM = (size_t)(D * KT_STRIDE + PAGE * D) * sizeof(float);
 
 // Tile of up to 64 history positions (x) of one kv head (y), K or V (z).
 __global__ void __launch_bounds__(128) prefill_hist_kernel(DevCache c, int layer, int slot,
@@ -95,7 +114,8 @@ __global__ void __launch_bounds__(128) prefill_hist_kernel(DevCache c, int layer
                                                            const uint16_t* __restrict__ v, int64_t in_base,
                                                            int64_t h0, int64_t h1) {
   extern __shared__ float4 smem4[];
-  float* sm = reinterpret_cast<float*>(smem4);
+  float* kt = reinterpret_cast<float*>(smem4);     // [D][KT_STRIDE] input tile, transposed
+  float* xs = kt + D * KT_STRIDE;                  // [PAGE][D] rotated values
   const int head = blockIdx.y;
   const int which = blockIdx.z;
   const int64_t t0 = h0 + (int64_t)blockIdx.x * PAGE;
@@ -103,14 +123,16 @@ __global__ void __launch_bounds__(128) prefill_hist_kernel(DevCache c, int layer
   const uint16_t* src = which ? v : k;
   const size_t lh = (size_t)layer * c.Hkv + head;
   const float* __restrict__ R = (which ? c.rot_v : c.rot_k) + lh * D * D;
+  const float* __restrict__ Rt = (which ? c.rot_vt : c.rot_kt) + lh * D * D;
   const float tau = (which ? c.tau_v : c.tau_k)[lh];
+  const float colnorm = c.rot_cn[(size_t)which * c.L * c.Hkv + lh];
 
   for (int idx = threadIdx.x; idx < PAGE * D; idx += blockDim.x) {
     const int j = idx / D;
     const int i = idx % D;
     float val = 0.0f;
     if (j < ntok) val = bf16_bits_to_float(src[((size_t)(t0 + j - in_base) * c.Hkv + head) * D + i]);
-    sm[i * KT_STRIDE + j] = val;
+    kt[i * KT_STRIDE + j] = val;
   }
   __syncthreads();
 
@@ -120,7 +142,7 @@ __global__ void __launch_bounds__(128) prefill_hist_kernel(DevCache c, int layer
   for (int j = 0; j < PAGE; ++j) acc[j] = 0.0f;
   for (int i = 0; i < D; ++i) {
     const float r = __ldg(R + i * D + co);
-    const float4* kr = reinterpret_cast<const float4*>(sm + i * KT_STRIDE);
+    const float4* kr = reinterpret_cast<const float4*>(kt + i * KT_STRIDE);
 #pragma unroll
     for (int j4 = 0; j4 < PAGE / 4; ++j4) {
       const float4 kk = kr[j4];
@@ -130,17 +152,23 @@ __global__ void __launch_bounds__(128) prefill_hist_kernel(DevCache c, int layer
       acc[4 * j4 + 3] = fmaf(kk.w, r, acc[4 * j4 + 3]);
     }
   }
-  __syncthreads();
 #pragma unroll
-  for (int j = 0; j < PAGE; ++j) sm[j * D + co] = acc[j];
+  for (int j = 0; j < PAGE; ++j) xs[j * D + co] = acc[j];
   __syncthreads();
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int32_t* pt = c.hist_pt + (size_t)slot * c.max_pages;
   for (int j = warp; j < ntok; j += 4) {
-    const float4 x = *reinterpret_cast<const float4*>(sm + j * D + 4 * lane);
-    const GroupCode g = quantize_group_warp(x, tau);
+    const float4 x = *reinterpret_cast<const float4*>(xs + j * D + 4 * lane);
+    float kn = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) kn = __fmaf_ru(kt[(4 * lane + i) * KT_STRIDE + j], kt[(4 * lane + i) * KT_STRIDE + j], kn);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) kn += __shfl_xor_sync(0xffffffffu, kn, off);
+    const float err = chain_error_bound(kn, colnorm);
+    const float* kcol = kt + j;
+    const GroupCode g = quantize_group_warp(x, err, tau, [&](int ch) { return exact_dot_fp32(kcol, KT_STRIDE, Rt + ch * D); });
     const int64_t h = t0 + j - SINK;
     const int32_t page = pt[h / PAGE];
     const int row = static_cast<int>(h % PAGE);
@@ -190,8 +218,16 @@ __global__ void __launch_bounds__(128) append_kernel(DevCache c, int layer, cons
       __syncthreads();
       if (t < 32) {
         const float tau = (which ? c.tau_v : c.tau_k)[lh];
+        const float colnorm = c.rot_cn[(size_t)which * c.L * c.Hkv + lh];
+        const float* __restrict__ Rt = (which ? c.rot_vt : c.rot_kt) + lh * D * D;
         const float4 x = *reinterpret_cast<const float4*>(xrot + 4 * t);
-        const GroupCode g = quantize_group_warp(x, tau);
+        float kn = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) kn = __fmaf_ru(xin[4 * t + i], xin[4 * t + i], kn);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) kn += __shfl_xor_sync(0xffffffffu, kn, off);
+        const GroupCode g = quantize_group_warp(x, chain_error_bound(kn, colnorm), tau,
+                                                [&](int ch) { return exact_dot_fp32(xin, 1, Rt + ch * D); });
         uint8_t* rec = int2_record(c, layer, q.hist_page, head);
         rec[(which ? V_CODES_OFF : K_CODES_OFF) + q.demote_slot * CODE_BYTES + t] = static_cast<uint8_t>(g.byte);
         if (t == 0) {
@@ -230,9 +266,12 @@ cudaError_t launch_pt_update(const DevCache& c, const PtEntry* entries, int n, c
 }
 
 cudaError_t launch_rotation_setup(const DevCache& c, const float* rot_k_src, const float* rot_v_src, float* rot_k,
-                                  float* rot_v, float* rot_kt, float* rot_vt, cudaStream_t s) {
+                                  float* rot_v, float* rot_kt, float* rot_vt, float* rot_cn, cudaStream_t s) {
   const size_t mats = (size_t)c.L * c.Hkv;
   rotation_setup_kernel<<<1024, 256, 0, s>>>(rot_k_src, rot_v_src, rot_k, rot_v, rot_kt, rot_vt, mats);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  colnorm_kernel<<<static_cast<unsigned>(2 * mats), D, 0, s>>>(rot_k_src, rot_v_src, rot_cn, static_cast<int>(mats));
   return cudaGetLastError();
 }
 
@@ -247,8 +286,14 @@ cudaError_t launch_prefill_bf16(const DevCache& c, int layer, const uint16_t* k,
 cudaError_t launch_prefill_hist(const DevCache& c, int layer, int slot, const uint16_t* k, const uint16_t* v,
                                 int64_t in_base, int64_t h0, int64_t h1, cudaStream_t s) {
   if (h1 <= h0) return cudaSuccess;
-  const size_t smem = (size_t)D * KT_STRIDE * sizeof(float);
-  static_assert(D * KT_STRIDE >= PAGE * D, "tile buffer reused for the rotated values");
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(PREFILL_SMEM));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const size_t smem = PREFILL_SMEM;
   dim3 grid(static_cast<unsigned>((h1 - h0 + PAGE - 1) / PAGE), c.Hkv, 2);
   prefill_hist_kernel<<<grid, 128, smem, s>>>(c, layer, slot, k, v, in_base, h0, h1);
   return cudaGetLastError();

@@ -95,6 +95,7 @@ typedef struct {
   size_t int2_pool_offset, int2_layer_stride, int2_page_stride, int2_record_bytes;
   size_t bf16_pool_offset, bf16_layer_stride, bf16_page_stride, bf16_record_bytes;
   size_t rot_k_offset, rot_v_offset, rot_kt_offset, rot_vt_offset; /* fp32 [L][Hkv][128][128] */
+  size_t rot_colnorm_offset;                                       /* fp32 [2][L][Hkv] */
   size_t tau_k_offset, tau_v_offset;                               /* fp32 [L][Hkv] */
   size_t hist_pt_offset, bf16_pt_offset, error_word_offset;
 } oscar_cache_layout;
