@@ -156,7 +156,7 @@ def algorithmic_bytes(tokens: int, hist_end: int, kv_heads: int) -> int:
 class Workload:
     """The cache, its rotations and every input of the timed steps, resident on the GPU."""
 
-    def __init__(self, cfg_id: int, steps_total: int, log):
+    def __init__(self, cfg_id: int, steps_total: int, log, layers: int = 0):
         import torch
         from bit_rotated_kv_decode_gb300 import binding, build, calibrate, synth
         build.build()
@@ -168,6 +168,8 @@ class Workload:
         self.w = w
         self.L, self.hq, self.hkv, self.batch, self.T0 = (w["layers"], w["q_heads"], w["kv_heads"], w["batch"],
                                                         w["context"])
+        if layers:
+            self.L = layers
         self.drift = cfg_id == 4
         t = time.time()
         fit = None if self.L <= 32 else list(range(0, self.L, 8))
@@ -258,7 +260,7 @@ def run_gpu(args, log):
     torch.cuda.set_device(local)
     W, K = args.warmup, args.steps
     ew, ek = 2, max(3, K // 2)
-    wl = Workload(args.config, W + K + ew + ek, log)
+    wl = Workload(args.config, W + K + ew + ek, log, args.layers)
     stream = wl.stream_ptr()
     L = wl.L
     # --- device-resident timing ---------------------------------------------------------------
@@ -318,7 +320,7 @@ def run_gpu(args, log):
     res = {
         "us_step": us_step, "dec_avg_us": dec_avg, "app_avg_us": app_avg, "bytes_per_launch": bpl,
         "achieved_gbs": achieved, "peak": peak, "peak_kind": peak_kind, "e2e_us": e2e_us, "h2d": h2d, "d2h": d2h,
-        "clocks": clk.summary(), "launches": K * L * 2, "world": world, "rank": rank,
+        "clocks": clk.summary(), "launches": K * L * 3, "world": world, "rank": rank,
     }
     return wl, res
 
@@ -420,6 +422,7 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--config", type=int, default=2, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0, help="fewer layers (small profiling cases only)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -7,16 +7,28 @@
 // "Together AI Open-Sources OSCAR" (MarkTechPost), section "The Serving
 // System": the value path is inverse-rotated.
 //
-// One launch per layer.  Work items, per (request, kv head):
-//   item 0      the BF16 sink + recent tokens, with the unrotated q;
-//   items 1..C  chunks of INT2 history pages, in the rotated basis: q is
-//               rotated by R_K, and for token j with codes c_j, scale s_j,
-//               zero z_j the logit is scale * (s_j (q_rot . c_j) + z_j sum(q_rot))
-//               and the value contribution is p_j (s_j c_j + z_j 1).
-// Every item writes an (m, l, o[128]) partial per query head of the GQA group
-// (log2-domain max m).  The last item of a (request, kv head) to finish --
-// decided by an atomic ticket, no waiting -- merges the partials, applies R_V^T
-// to the history part and writes out = (O_bf16 + O_hist R_V^T) / L.
+// One launch per layer.  Work items per (request, kv head):
+//   items 0..4   BF16 sink page and the four recent-ring pages, unrotated q;
+//   items 5..    chunks of INT2 history pages in the rotated basis.
+// For an INT2 token j with codes c_j and fp16 scale / zero (s_j, z_j):
+//   logit_j = scale * (s_j (q_rot . c_j) + z_j sum(q_rot)),
+//   value   = s_j c_j + z_j 1   (accumulated as p_j s_j c_j plus sum p_j z_j).
+// The two contractions over a 64-token page -- q_rot . c (64 tokens x G heads x
+// 128 channels) and sum_j (p_j s_j) c_j (128 channels x G heads x 64 tokens) --
+// run on the tensor cores (mma.sync m16n8k16, fp16 operands, fp32 accumulate):
+//   * a 2-bit field masked out of a packed byte word, with every other bit
+//     zero, is the fp16 subnormal code * 2^(2e-24) -- exact, one LOP3 per two
+//     codes; the factor 4^e of its bit position is folded into the other operand;
+//   * q_rot and p s are split into fp16 hi + lo parts (22 significant bits),
+//     occupying the N columns as (head, part) pairs;
+//   * every product is exact in fp32; accumulation is fp32.
+// Pages are staged HBM -> shared memory by TMA bulk copies (cp.async.bulk, one
+// 4608-byte record per page and kv head) into a per-warp ring, completion on
+// mbarriers; every wait is bounded and reports ERR_TIMEOUT instead of hanging.
+// Each item writes an (o[128], m, l) partial per query head (log2-domain max m).
+// The last item of a (request, kv head) to finish -- an atomic ticket, no
+// waiting -- merges the partials, applies R_V^T to the history part and writes
+// out = (O_bf16 + O_hist R_V^T) / L.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -27,316 +39,765 @@ namespace {
 
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr int PART = PARTIAL_FLOATS;
+constexpr int WARPS = 4;                 // warps per CTA
+constexpr int THREADS = 32 * WARPS;
+constexpr int STAGES = 3;                // TMA ring depth per warp
+constexpr int BF16_ITEMS = DECODE_BF16_ITEMS;
+constexpr uint32_t WAIT_LIMIT = 1u << 22;
+constexpr int ERR_TIMEOUT_BIT = 8;
 
 struct DecodeArgs {
   int n;
   int pages_per_chunk;
+  int group_stride;          // group partial slots per (request, kv head)
   DecodeReq r[DECODE_PER_LAUNCH];
 };
 
-__device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-__device__ __forceinline__ float warp_max(float x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-  return x;
-}
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-struct Online {
-  float m;          // running max (log2 domain)
-  float l;          // this lane's part of the running sum
-  float o[4];       // this lane's 4 output channels
-  float u;          // running sum of p_j z_j (INT2 items only)
-};
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
 
-// Rescale the running state to a new maximum; returns the new max.
-__device__ __forceinline__ float online_rescale(Online& st, float page_max) {
-  const float m_new = fmaxf(st.m, page_max);
-  const float corr = (st.m == -INFINITY) ? 0.0f : exp2f(st.m - m_new);
-  st.l *= corr;
-  st.u *= corr;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) st.o[i] *= corr;
-  st.m = m_new;
-  return m_new;
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+// 1-D TMA bulk copy global -> shared; completion counted on bar.
+__device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Bounded wait for the phase with the given parity; false if it gave up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t addr = smem_u32(bar);
+  for (uint32_t it = 0; it < WAIT_LIMIT; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Pair of 2-bit codes m of each 16-bit half of w (m = 0..7) as an fp16x2 of
+// subnormals code * 2^(2 e(m) - 24), e(m) = m for m <= 4, m - 5 otherwise.
+template <int M>
+__device__ __forceinline__ uint32_t code_pair(uint32_t w) {
+  if constexpr (M <= 4) {
+    return w & (0x00030003u << (2 * M));
+  } else {
+    return (w >> 10) & (0x00030003u << (2 * (M - 5)));
+  }
+}
+__device__ __forceinline__ uint32_t code_pair_rt(uint32_t w, int m) {
+  return m <= 4 ? (w & (0x00030003u << (2 * m))) : ((w >> 10) & (0x00030003u << (2 * (m - 5))));
+}
+__host__ __device__ constexpr int code_exp(int m) { return m <= 4 ? m : m - 5; }
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// fp16 hi / lo split of x: hi = fp16_rn(x), lo = fp16_rn(x - hi).
+__device__ __forceinline__ void split_half(float x, float& hi, float& lo) {
+  hi = __half2float(__float2half_rn(x));
+  lo = x - hi;
 }
 
 template <int G>
 struct Smem {
-  float q[G][D];
-  float qsum[G];
-  float w[G][PAGE];
-  float u[G][PAGE];
-  float oh[G][D];
-  int ticket;
+  // INT2: per-warp TMA rings; BF16 items: the page's K rows (16-byte chunks
+  // XOR-swizzled by row) and V rows; after the page loop: per-warp states.
   union {
-    __align__(16) uint8_t rec[RECORD];
+    __align__(128) uint8_t ring[WARPS][STAGES][RECORD];
     struct {
       __align__(16) uint16_t k[PAGE][D];
       __align__(16) uint16_t v[PAGE][D];
     } bf;
+    float state[WARPS][G][PART];
   } buf;
+  __align__(8) uint64_t bar[WARPS][STAGES];
+  float q[G][D];             // q (BF16 items) or q_rot (INT2 chunks)
+  float qsum[G];             // sum of q_rot over channels
+  float qscale[G];           // power-of-two prescale of q_rot into fp16 range
+  __align__(16) float pw[WARPS][G][PAGE];  // p * s_v of the current page, per warp
+  float red[WARPS][G];
+  int ticket;
 };
 
+constexpr int QROT_THREADS = 256;
+constexpr int QROT_GROUPS = QROT_THREADS / 32;   // row groups
+constexpr int QROT_ROWS = D / QROT_GROUPS;       // rows per group
+
+// q_rot = q R_K for the G query heads of every (request, kv head) of the launch
+// (block x = request * Hkv + kv head), with per-head sums and the power-of-two
+// prescale that keeps the fp16 tensor-core operands finite.  Thread (group g,
+// lane l) accumulates channels 4l .. 4l+3 over rows 16g .. 16g+15 with 16
+// independent float4 loads of R_K.  The decode kernel is launched as its
+// programmatic dependent and waits for this grid before reading q_rot.
 template <int G>
-__global__ void __launch_bounds__(32 * G) decode_kernel(DevCache c, int layer, DecodeArgs a,
-                                                        const uint16_t* __restrict__ q, float* __restrict__ out,
-                                                        int32_t* counters, float* partials) {
-  __shared__ Smem<G> sm;
+__global__ void __launch_bounds__(QROT_THREADS) qrot_kernel(DevCache c, int layer, DecodeArgs a,
+                                                            const uint16_t* __restrict__ q, float* qrot) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __shared__ float qs[G][D];
+  __shared__ __align__(16) float part[QROT_GROUPS][G][D];
+  __shared__ float red[4][G][2];
+  const int ri = blockIdx.x / c.Hkv, head = blockIdx.x % c.Hkv;
+  const int t = threadIdx.x, lane = t & 31, grp = t >> 5;
+  const float* __restrict__ RK = c.rot_k + ((size_t)layer * c.Hkv + head) * D * D;
+  float4 r[QROT_ROWS];
+#pragma unroll
+  for (int i = 0; i < QROT_ROWS; ++i)
+    r[i] = __ldg(reinterpret_cast<const float4*>(RK + (size_t)(QROT_ROWS * grp + i) * D) + lane);
+  const uint16_t* qrow = q + ((size_t)a.r[ri].batch_row * c.Hq + (size_t)head * G) * D;
+  for (int i = t; i < G * D; i += QROT_THREADS) qs[i / D][i % D] = __uint_as_float(static_cast<uint32_t>(qrow[i]) << 16);
+  __syncthreads();
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+    for (int i = 0; i < QROT_ROWS; ++i) {
+      const float qv = qs[h][QROT_ROWS * grp + i];
+      acc.x = fmaf(qv, r[i].x, acc.x);
+      acc.y = fmaf(qv, r[i].y, acc.y);
+      acc.z = fmaf(qv, r[i].z, acc.z);
+      acc.w = fmaf(qv, r[i].w, acc.w);
+    }
+    reinterpret_cast<float4*>(part[grp][h])[lane] = acc;
+  }
+  __syncthreads();
+  if (t < D) {
+    float* out = qrot + (size_t)blockIdx.x * G * QROT_FLOATS;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float v = 0.0f;
+#pragma unroll
+      for (int g2 = 0; g2 < QROT_GROUPS; ++g2) v += part[g2][h][t];
+      out[h * QROT_FLOATS + t] = v;
+      float sum = v, mx = fabsf(v);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      }
+      if (lane == 0) {
+        red[grp][h][0] = sum;
+        red[grp][h][1] = mx;
+      }
+    }
+  }
+  __syncthreads();
+  if (t < G) {
+    float sum = 0.0f, mx = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      sum += red[w][t][0];
+      mx = fmaxf(mx, red[w][t][1]);
+    }
+    // |q_rot| * 2^24 * prescale <= 2^15
+    int e = 0;
+    if (mx > 0.0f) e = static_cast<int>(floorf(log2f(32768.0f / mx))) - 24;
+    e = max(-60, min(e, 60));
+    float* out = qrot + (size_t)blockIdx.x * G * QROT_FLOATS + t * QROT_FLOATS;
+    out[QROT_SUM] = sum;
+    out[QROT_SCALE] = ldexpf(1.0f, e);
+  }
+}
+
+// One chunk of INT2 history pages of one (request, kv head); leaves the CTA's
+// partial (rotated basis) for every query head of the group in part_out.
+template <int G>
+__device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const DecodeReq& R, int ri, int head,
+                                           int chunk, int ppc, const float* qrot, Smem<G>& sm, float* part_out) {
+  constexpr int NT = (G + 3) / 4;       // n-tiles of 8 columns = 4 heads x (hi, lo)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tid = lane & 3;
+  const float scale2 = c.scale * LOG2E;
+  const int nhist = R.hist_end - SINK;
+  const int npages = (nhist + PAGE - 1) / PAGE;
+  const int pc0 = chunk * ppc;
+  const int pc1 = min(npages, pc0 + ppc);
+  const int my_n = (pc1 - pc0 > warp) ? (pc1 - pc0 - warp + WARPS - 1) / WARPS : 0;
+  const int32_t* pt = c.hist_pt + (size_t)R.slot * c.max_pages;
+  const uint8_t* base = c.int2 + layer * c.int2_layer_stride + (size_t)head * RECORD;
+  const size_t pstride = (size_t)c.Hkv * RECORD;
+  bool timed_out = false;
+  int issued = 0;   // copies issued by this warp (lane 0's count)
+
+  auto page_src = [&](int j) -> const uint8_t* {
+    int32_t page = pt[pc0 + warp + WARPS * j];
+    if (page < 0 || page >= c.n_int2_pages) {
+      atomicOr(c.err, ERR_INT2_PAGE);
+      page = 0;
+    }
+    return base + (size_t)page * pstride;
+  };
+  if (lane == 0) {
+#pragma unroll
+    for (int st = 0; st < STAGES; ++st) mbar_init(&sm.bar[warp][st], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    for (int j = 0; j < STAGES && j < my_n; ++j) {
+      mbar_expect_tx(&sm.bar[warp][j], RECORD);
+      tma_load_1d(sm.buf.ring[warp][j], page_src(j), RECORD, &sm.bar[warp][j]);
+      ++issued;
+    }
+  }
+  // the copies are in flight while this grid waits for the q rotation grid
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  {
+    const float* qr = qrot + (size_t)(ri * c.Hkv + head) * G * QROT_FLOATS;
+    for (int i = threadIdx.x; i < G * D; i += THREADS) sm.q[i / D][i % D] = __ldcg(qr + (i / D) * QROT_FLOATS + i % D);
+    if (threadIdx.x < G) {
+      sm.qsum[threadIdx.x] = __ldcg(qr + threadIdx.x * QROT_FLOATS + QROT_SUM);
+      sm.qscale[threadIdx.x] = __ldcg(qr + threadIdx.x * QROT_FLOATS + QROT_SCALE);
+    }
+    __syncthreads();
+  }
+  // weights p * s_v are prescaled by 2^ew so the smallest ones stay representable in
+  // fp16: s_v <= fp16(2 tau_V / 3) and p <= 1, so p s_v 2^ew <= 2^15
+  int ew;
+  {
+    const float smax = c.tau_v[(size_t)layer * c.Hkv + head] * (2.0f / 3.0f) * 1.002f;
+    ew = max(-60, min(60, static_cast<int>(floorf(log2f(32768.0f / smax)))));
+  }
+  const float wscale = ldexpf(1.0f, ew);
+
+  // B operands of q_rot . c: per n-tile, k-step s, two registers (hi or lo part)
+  uint32_t bq[NT][8][2];
+  float invp[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int h = 4 * nt + (gid >> 1);
+    const bool lo_part = gid & 1;
+    const bool hv = h < G;
+    const float p = hv ? sm.qscale[h] : 1.0f;
+    invp[nt] = (4 * nt + tid < G) ? 1.0f / sm.qscale[4 * nt + tid] : 0.0f;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      const int ch0 = 32 * tid + 16 * (s >> 2) + 2 * (s & 3);
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int m = 2 * (s & 3) + r;
+        const int cha = ch0 + r;
+        const float f = ldexpf(p, 24 - 2 * code_exp(m));
+        float va = hv ? sm.q[h][cha] * f : 0.0f;
+        float vb = hv ? sm.q[h][cha + 8] * f : 0.0f;
+        float ha, la, hb, lb;
+        split_half(va, ha, la);
+        split_half(vb, hb, lb);
+        bq[nt][s][r] = lo_part ? pack_half2(la, lb) : pack_half2(ha, hb);
+      }
+    }
+  }
+  float qs[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) qs[nt] = (4 * nt + tid < G) ? sm.qsum[4 * nt + tid] : 0.0f;
+
+  float o[NT][8][4];
+  float m_run[NT], l_run[NT], u_run[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    m_run[nt] = -INFINITY;
+    l_run[nt] = 0.0f;
+    u_run[nt] = 0.0f;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[nt][mt][e] = 0.0f;
+  }
+
+  for (int j = 0; j < my_n; ++j) {
+    const int stg = j % STAGES;
+    if (!timed_out && !mbar_wait(&sm.bar[warp][stg], (j / STAGES) & 1)) {
+      timed_out = true;
+      if (lane == 0) atomicOr(c.err, ERR_TIMEOUT_BIT);
+    }
+    if (timed_out) break;
+    const uint8_t* rec = sm.buf.ring[warp][stg];
+    const int pi = pc0 + warp + WARPS * j;
+    const int valid = min(PAGE, nhist - pi * PAGE);
+
+    // ---- logits: 4 m-tiles of 16 tokens x NT n-tiles, K = 128 channels
+    float acc[NT][4][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][mt][e] = 0.0f;
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      const uint2 ka = *reinterpret_cast<const uint2*>(rec + K_CODES_OFF + (16 * mt + gid) * CODE_BYTES + 8 * tid);
+      const uint2 kb = *reinterpret_cast<const uint2*>(rec + K_CODES_OFF + (16 * mt + gid + 8) * CODE_BYTES + 8 * tid);
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t wa = s < 4 ? ka.x : ka.y;
+        const uint32_t wb = s < 4 ? kb.x : kb.y;
+        const int m0 = 2 * (s & 3);
+        const uint32_t a0 = code_pair_rt(wa, m0), a1 = code_pair_rt(wb, m0);
+        const uint32_t a2 = code_pair_rt(wa, m0 + 1), a3 = code_pair_rt(wb, m0 + 1);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt][mt], a0, a1, a2, a3, bq[nt][s][0], bq[nt][s][1]);
+      }
+    }
+    // token meta of this lane's 8 tokens: 16 mt + gid + 8 rr
+    float lg[NT][8], sv[8], zv[8];
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int tok = 16 * mt + gid + 8 * rr;
+        const __half2 km = *reinterpret_cast<const __half2*>(rec + K_META_OFF + tok * META_BYTES);
+        const __half2 vm = *reinterpret_cast<const __half2*>(rec + V_META_OFF + tok * META_BYTES);
+        const bool ok = tok < valid;
+        sv[2 * mt + rr] = ok ? __low2float(vm) : 0.0f;
+        zv[2 * mt + rr] = ok ? __high2float(vm) : 0.0f;
+        const float sk = __low2float(km), zk = __high2float(km);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const float d = (acc[nt][mt][2 * rr] + acc[nt][mt][2 * rr + 1]) * invp[nt];
+          lg[nt][2 * mt + rr] = (ok && 4 * nt + tid < G) ? scale2 * fmaf(sk, d, zk * qs[nt]) : -INFINITY;
+        }
+      }
+    // ---- online softmax per head (lanes with equal tid share a head)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float pm = lg[nt][0];
+#pragma unroll
+      for (int i = 1; i < 8; ++i) pm = fmaxf(pm, lg[nt][i]);
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+      const float m_new = fmaxf(m_run[nt], pm);
+      const float corr = (m_run[nt] == -INFINITY) ? 0.0f : exp2f(m_run[nt] - m_new);
+      m_run[nt] = m_new;
+      l_run[nt] *= corr;
+      u_run[nt] *= corr;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[nt][mt][e] *= corr;
+      const int h = 4 * nt + tid;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float p = (lg[nt][i] == -INFINITY) ? 0.0f : exp2f(lg[nt][i] - m_new);
+        l_run[nt] += p;
+        u_run[nt] = fmaf(p, zv[i], u_run[nt]);
+        if (h < G) sm.pw[warp][h][16 * (i >> 1) + gid + 8 * (i & 1)] = p * sv[i] * wscale;
+      }
+    }
+    __syncwarp();
+    // ---- values: 8 m-tiles of 16 channels x NT n-tiles, K = 64 tokens
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int ta = 16 * s + 2 * tid;
+      uint32_t bw[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int h = 4 * nt + (gid >> 1);
+        if (h < G) {
+          const float2 w01 = *reinterpret_cast<const float2*>(&sm.pw[warp][h][ta]);
+          const float2 w89 = *reinterpret_cast<const float2*>(&sm.pw[warp][h][ta + 8]);
+          float h0, l0, h1, l1, h8, l8, h9, l9;
+          split_half(w01.x, h0, l0);
+          split_half(w01.y, h1, l1);
+          split_half(w89.x, h8, l8);
+          split_half(w89.y, h9, l9);
+          bw[nt][0] = (gid & 1) ? pack_half2(l0, l1) : pack_half2(h0, h1);
+          bw[nt][1] = (gid & 1) ? pack_half2(l8, l9) : pack_half2(h8, h9);
+        } else {
+          bw[nt][0] = bw[nt][1] = 0u;
+        }
+      }
+      const uint32_t* vrow = reinterpret_cast<const uint32_t*>(rec + V_CODES_OFF) + gid;
+      const uint32_t wa = vrow[ta * (CODE_BYTES / 4)], wb = vrow[(ta + 1) * (CODE_BYTES / 4)];
+      const uint32_t wc = vrow[(ta + 8) * (CODE_BYTES / 4)], wd = vrow[(ta + 9) * (CODE_BYTES / 4)];
+      const uint32_t x1 = __byte_perm(wa, wb, 0x5410), y1 = __byte_perm(wa, wb, 0x7632);
+      const uint32_t x2 = __byte_perm(wc, wd, 0x5410), y2 = __byte_perm(wc, wd, 0x7632);
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const uint32_t a0 = code_pair_rt(x1, mt), a1 = code_pair_rt(y1, mt);
+        const uint32_t a2 = code_pair_rt(x2, mt), a3 = code_pair_rt(y2, mt);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma16816(o[nt][mt], a0, a1, a2, a3, bw[nt][0], bw[nt][1]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && j + STAGES < my_n) {
+      mbar_expect_tx(&sm.bar[warp][stg], RECORD);
+      tma_load_1d(sm.buf.ring[warp][stg], page_src(j + STAGES), RECORD, &sm.bar[warp][stg]);
+      ++issued;
+    }
+  }
+  if (timed_out && lane == 0) {
+    // let every copy this warp issued land (bounded) before the buffers are reused:
+    // stage st received ceil((issued - st) / STAGES) copies; wait for the last phase
+    for (int st = 0; st < STAGES && st < issued; ++st) {
+      const int count = (issued - st + STAGES - 1) / STAGES;
+      mbar_wait(&sm.bar[warp][st], (count - 1) & 1);
+    }
+  }
+  __syncthreads();   // every warp is done with every ring before states overwrite them
+
+  // ---- this warp's state -> shared memory (rotated basis, unscaled, z term added)
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    float l = l_run[nt], u = u_run[nt];
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l += __shfl_xor_sync(0xffffffffu, l, off);
+      u += __shfl_xor_sync(0xffffffffu, u, off);
+    }
+    const int h = 4 * nt + tid;
+    if (h < G) {
+      float* st = sm.buf.state[warp][h];
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const float f = ldexpf(1.0f, 24 - 2 * code_exp(mt) - ew);
+        st[16 * gid + mt] = fmaf(o[nt][mt][0] + o[nt][mt][1], f, u);
+        st[16 * gid + 8 + mt] = fmaf(o[nt][mt][2] + o[nt][mt][3], f, u);
+      }
+      if (gid == 0) {
+        st[PARTIAL_M] = m_run[nt];
+        st[PARTIAL_L] = l;
+      }
+    }
+  }
+  __syncthreads();
+  // ---- merge the warps: thread t owns channel t
+  const int t = threadIdx.x;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) M = fmaxf(M, sm.buf.state[w][h][PARTIAL_M]);
+    float acc_o = 0.0f, acc_l = 0.0f;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) {
+      const float mw = sm.buf.state[w][h][PARTIAL_M];
+      if (mw == -INFINITY) continue;
+      const float f = exp2f(mw - M);
+      acc_o = fmaf(sm.buf.state[w][h][t], f, acc_o);
+      acc_l = fmaf(sm.buf.state[w][h][PARTIAL_L], f, acc_l);
+    }
+    part_out[h * PART + t] = acc_o;
+    if (t == 0) {
+      part_out[h * PART + PARTIAL_M] = M;
+      part_out[h * PART + PARTIAL_L] = acc_l;
+    }
+  }
+}
+
+// One BF16 page (the sink page, or one of the four recent-ring pages) of one
+// (request, kv head), with the unrotated q; partial for every query head.
+template <int G>
+__device__ __forceinline__ void bf16_item(const DevCache& c, int layer, const DecodeReq& R, int head, int which,
+                                          Smem<G>& sm, float* part_out) {
+  const int t = threadIdx.x;
+  const int warp = t >> 5, lane = t & 31;
+  const float scale2 = c.scale * LOG2E;
+  const int T = R.tokens, he = R.hist_end;
+  int page = which == 0 ? R.sink_page : R.ring_page[which - 1];
+  if (page < 0 || page >= c.n_bf16_pages) {
+    if (t == 0) atomicOr(c.err, ERR_BF16_PAGE);
+    page = 0;
+  }
+  // validity of row r: sink rows [0, min(T, 64)); ring slot s = 64 (which-1) + r holds
+  // position he + ((s - (he - 64)) mod 256), valid when below T
+  auto row_valid = [&](int r) -> bool {
+    if (which == 0) return r < min(T, SINK);
+    if (T <= SINK) return false;
+    const int s = PAGE * (which - 1) + r;
+    const int p = he + ((s - (he - SINK)) % RECENT + RECENT) % RECENT;
+    return p < T;
+  };
+  const uint16_t* src = c.bf16 + layer * c.bf16_layer_stride + ((size_t)page * c.Hkv + head) * BF16_RECORD_ELEMS;
+  constexpr int LOADS = PAGE * (D / 8) / THREADS;
+  uint4 kk[LOADS], vv[LOADS];
+#pragma unroll
+  for (int it = 0; it < LOADS; ++it) {
+    const int idx = t + THREADS * it, r = idx / (D / 8), part = idx % (D / 8);
+    kk[it] = reinterpret_cast<const uint4*>(src + (size_t)r * D)[part];
+    vv[it] = reinterpret_cast<const uint4*>(src + (size_t)(PAGE + r) * D)[part];
+  }
+#pragma unroll
+  for (int it = 0; it < LOADS; ++it) {
+    const int idx = t + THREADS * it, r = idx / (D / 8), part = idx % (D / 8);
+    reinterpret_cast<uint4*>(&sm.buf.bf.k[r][0])[part ^ (r & 15)] = kk[it];
+    reinterpret_cast<uint4*>(&sm.buf.bf.v[r][0])[part] = vv[it];
+  }
+  __syncthreads();
+  // logits: thread t -> token t/2, channel half t%2, all G heads
+  {
+    const int r = t >> 1, half = t & 1;
+    float acc[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) acc[h] = 0.0f;
+    const uint4* kr = reinterpret_cast<const uint4*>(&sm.buf.bf.k[r][0]);
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const int chunk = 8 * half + b;
+      const uint4 w = kr[chunk ^ (r & 15)];
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float k0 = bf16lo(ww[e]), k1 = bf16hi(ww[e]);
+        const int ch = 8 * chunk + 2 * e;
+#pragma unroll
+        for (int h = 0; h < G; ++h) acc[h] = fmaf(sm.q[h][ch + 1], k1, fmaf(sm.q[h][ch], k0, acc[h]));
+      }
+    }
+    const bool ok = row_valid(r);
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], 1);
+      if (half == 0) sm.pw[0][h][r] = ok ? acc[h] * scale2 : -INFINITY;
+    }
+  }
+  __syncthreads();
+  // softmax and values: warp w handles heads w, w + 4; lane owns channels 4 lane .. 4 lane + 3
+  for (int h = warp; h < G; h += WARPS) {
+    const float x0 = sm.pw[0][h][lane], x1 = sm.pw[0][h][lane + 32];
+    float m = fmaxf(x0, x1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float p0 = (x0 == -INFINITY) ? 0.0f : exp2f(x0 - m);
+    const float p1 = (x1 == -INFINITY) ? 0.0f : exp2f(x1 - m);
+    float l = p0 + p1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    __syncwarp();
+    sm.pw[0][h][lane] = p0;
+    sm.pw[0][h][lane + 32] = p1;
+    __syncwarp();
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (m != -INFINITY) {
+      for (int r = 0; r < PAGE; ++r) {
+        const float p = sm.pw[0][h][r];
+        const uint2 vv = reinterpret_cast<const uint2*>(&sm.buf.bf.v[r][0])[lane];
+        acc[0] = fmaf(p, bf16lo(vv.x), acc[0]);
+        acc[1] = fmaf(p, bf16hi(vv.x), acc[1]);
+        acc[2] = fmaf(p, bf16lo(vv.y), acc[2]);
+        acc[3] = fmaf(p, bf16hi(vv.y), acc[3]);
+      }
+    }
+    reinterpret_cast<float4*>(part_out + h * PART)[lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    if (lane == 0) {
+      part_out[h * PART + PARTIAL_M] = m;
+      part_out[h * PART + PARTIAL_L] = l;
+    }
+  }
+}
+
+// Online-softmax merge of `count` consecutive partials (stride G * PART floats)
+// into one: thread t owns channel t of every query head.
+template <int G>
+__device__ __forceinline__ void merge_partials(const float* src, int count, float* dst) {
+  const int t = threadIdx.x;
+#pragma unroll 1
+  for (int h = 0; h < G; ++h) {
+    float M = -INFINITY;
+#pragma unroll 8
+    for (int k = 0; k < count; ++k) M = fmaxf(M, __ldcg(src + ((size_t)k * G + h) * PART + PARTIAL_M));
+    float L = 0.0f, o = 0.0f;
+#pragma unroll 8
+    for (int k = 0; k < count; ++k) {
+      const float* pk = src + ((size_t)k * G + h) * PART;
+      const float mk = __ldcg(pk + PARTIAL_M);
+      const float f = (mk == -INFINITY) ? 0.0f : exp2f(mk - M);
+      L = fmaf(__ldcg(pk + PARTIAL_L), f, L);
+      o = fmaf(__ldcg(pk + t), f, o);
+    }
+    dst[h * PART + t] = o;
+    if (t == 0) {
+      dst[h * PART + PARTIAL_M] = M;
+      dst[h * PART + PARTIAL_L] = L;
+    }
+  }
+}
+
+template <int G>
+__global__ void __launch_bounds__(THREADS, DECODE_CTAS_PER_SM) decode_kernel(DevCache c, int layer, DecodeArgs a,
+                                                         const uint16_t* __restrict__ q, float* __restrict__ out,
+                                                         int32_t* counters, const float* qrot, float* partials,
+                                                         float* gpart) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  Smem<G>& sm = *reinterpret_cast<Smem<G>*>(smem_raw);
   const int item = blockIdx.x;
   int ri = 0;
   while (ri + 1 < a.n && a.r[ri + 1].item_start <= item) ++ri;
   const DecodeReq R = a.r[ri];
+  const int per_head = BF16_ITEMS + R.chunks;
   const int local = item - R.item_start;
-  const int per_head = 1 + R.chunks;
   const int head = local / per_head;
   const int sub = local % per_head;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int qh = head * G + warp;
+  const int t = threadIdx.x;
   const size_t lh = (size_t)layer * c.Hkv + head;
-  const float scale2 = c.scale * LOG2E;
-
-  // q of this warp's head (bf16 -> fp32)
-  const uint16_t* qrow = q + ((size_t)R.batch_row * c.Hq + qh) * D;
-  for (int i = lane; i < D; i += 32) sm.q[warp][i] = bf16f(qrow[i]);
-  __syncwarp();
-
-  Online st;
-  st.m = -INFINITY;
-  st.l = 0.0f;
-  st.u = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) st.o[i] = 0.0f;
+  const float* __restrict__ RVt = c.rot_vt + lh * D * D;
 
   if (sub == 0) {
-    // ---- BF16 sink + recent window, unrotated basis ------------------------
-    const int T = R.tokens;
-    const int nsink = T < SINK ? T : SINK;
-    const int rec_lo = T > SINK ? R.hist_end : T;   // recent = [hist_end, T)
-    const int nrec = T - rec_lo;
-    const int ntot = nsink + nrec;
-    for (int base = 0; base < ntot; base += PAGE) {
-      const int cnt = min(PAGE, ntot - base);
-      __syncthreads();
-      for (int idx = threadIdx.x; idx < cnt * (D / 8); idx += blockDim.x) {
-        const int j = idx / (D / 8);
-        const int part = idx % (D / 8);
-        const int t = base + j;
-        int page, row;
-        if (t < nsink) {
-          page = R.sink_page;
-          row = t;
-        } else {
-          const int p = rec_lo + (t - nsink);
-          const int slot = (p - SINK) % RECENT;
-          page = R.ring_page[slot / PAGE];
-          row = slot % PAGE;
-        }
-        if (page < 0 || page >= c.n_bf16_pages) {
-          atomicOr(c.err, ERR_BF16_PAGE);
-          page = 0;
-        }
-        const uint16_t* src = c.bf16 + layer * c.bf16_layer_stride + ((size_t)page * c.Hkv + head) * BF16_RECORD_ELEMS;
-        const uint4 kk = reinterpret_cast<const uint4*>(src + (size_t)row * D)[part];
-        const uint4 vv = reinterpret_cast<const uint4*>(src + (size_t)(PAGE + row) * D)[part];
-        // K rows are stored with their 16-byte chunks XOR-swizzled by the row
-        reinterpret_cast<uint4*>(&sm.buf.bf.k[j][0])[part ^ (j & 15)] = kk;
-        reinterpret_cast<uint4*>(&sm.buf.bf.v[j][0])[part] = vv;
-      }
-      __syncthreads();
-      float lg[2];
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const int j = lane + 32 * h2;
-        float dot = 0.0f;
-        if (j < cnt) {
-          const uint4* kr = reinterpret_cast<const uint4*>(&sm.buf.bf.k[j][0]);
-#pragma unroll
-          for (int b = 0; b < D / 8; ++b) {
-            const uint4 w = kr[b ^ (j & 15)];
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              dot = fmaf(sm.q[warp][8 * b + 2 * e], __uint_as_float(ww[e] << 16), dot);
-              dot = fmaf(sm.q[warp][8 * b + 2 * e + 1], __uint_as_float(ww[e] & 0xffff0000u), dot);
-            }
-          }
-          lg[h2] = dot * scale2;
-        } else {
-          lg[h2] = -INFINITY;
-        }
-      }
-      const float m_new = online_rescale(st, warp_max(fmaxf(lg[0], lg[1])));
-      const float p0 = exp2f(lg[0] - m_new);
-      const float p1 = exp2f(lg[1] - m_new);
-      st.l += p0 + p1;
-      sm.w[warp][lane] = p0;
-      sm.w[warp][lane + 32] = p1;
-      __syncwarp();
-      for (int j = 0; j < cnt; ++j) {
-        const float p = sm.w[warp][j];
-        const uint2 vv = reinterpret_cast<const uint2*>(&sm.buf.bf.v[j][0])[lane];
-        st.o[0] = fmaf(p, __uint_as_float(vv.x << 16), st.o[0]);
-        st.o[1] = fmaf(p, __uint_as_float(vv.x & 0xffff0000u), st.o[1]);
-        st.o[2] = fmaf(p, __uint_as_float(vv.y << 16), st.o[2]);
-        st.o[3] = fmaf(p, __uint_as_float(vv.y & 0xffff0000u), st.o[3]);
-      }
-      __syncwarp();
-    }
+    // warm L2 with R_V^T for whichever item of this head merges last
+    for (int line = t; line < D * D / 32; line += THREADS)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(RVt + (size_t)line * 32));
+  }
+  const uint16_t* qrow = q + ((size_t)R.batch_row * c.Hq + (size_t)head * G) * D;
+  for (int i = t; i < G * D; i += THREADS) sm.q[i / D][i % D] = __uint_as_float(static_cast<uint32_t>(qrow[i]) << 16);
+  __syncthreads();
+
+  float* part = partials + (size_t)item * G * PART;
+  if (sub < BF16_ITEMS) {
+    bf16_item<G>(c, layer, R, head, sub, sm, part);
   } else {
-    // ---- INT2 history chunk, rotated basis ----------------------------------
-    // q_rot = q R_K: lane computes channels 4 lane .. 4 lane + 3
-    const float* __restrict__ RK = c.rot_k + lh * D * D;
-    float qr[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    for (int i = 0; i < D; ++i) {
-      const float qi = sm.q[warp][i];
-      const float4 r = __ldg(reinterpret_cast<const float4*>(RK + (size_t)i * D) + lane);
-      qr[0] = fmaf(qi, r.x, qr[0]);
-      qr[1] = fmaf(qi, r.y, qr[1]);
-      qr[2] = fmaf(qi, r.z, qr[2]);
-      qr[3] = fmaf(qi, r.w, qr[3]);
+    int2_chunk<G>(c, layer, R, ri, head, sub - BF16_ITEMS, a.pages_per_chunk, qrot, sm, part);
+  }
+
+  // ---- two-level merge by atomic tickets (nobody waits) -----------------------------
+  // group 0 = the BF16 items, group g >= 1 = INT2 chunks (g-1)*MERGE_GROUP .. +MERGE_GROUP-1
+  const int g = sub < BF16_ITEMS ? 0 : 1 + (sub - BF16_ITEMS) / MERGE_GROUP;
+  const int gfirst = g == 0 ? 0 : BF16_ITEMS + (g - 1) * MERGE_GROUP;
+  const int gcount = g == 0 ? BF16_ITEMS : min(MERGE_GROUP, R.chunks - (g - 1) * MERGE_GROUP);
+  const int ngroups = 1 + (R.chunks + MERGE_GROUP - 1) / MERGE_GROUP;
+  int32_t* cnt = counters + (size_t)(ri * c.Hkv + head) * MERGE_COUNTERS;
+  float* gbase = gpart + (size_t)(ri * c.Hkv + head) * a.group_stride * G * PART;
+  __threadfence();
+  __syncthreads();
+  if (t == 0) sm.ticket = atomicAdd(cnt + 1 + g, 1);
+  __syncthreads();
+  if (sm.ticket != gcount - 1) return;
+  __threadfence();
+  merge_partials<G>(partials + (size_t)(R.item_start + head * per_head + gfirst) * G * PART, gcount,
+                    gbase + (size_t)g * G * PART);
+  if (t == 0) cnt[1 + g] = 0;
+  __threadfence();
+  __syncthreads();
+  if (t == 0) sm.ticket = atomicAdd(cnt, 1);
+  __syncthreads();
+  if (sm.ticket != ngroups - 1) return;
+  __threadfence();
+
+  // ---- last group of this (request, kv head): BF16 part + R_V^T (history part) ----
+  float* oh = &sm.pw[0][0][0];   // [G][D] history part (rotated basis)
+#pragma unroll 1
+  for (int h = 0; h < G; ++h) {
+    float M = -INFINITY;
+#pragma unroll 8
+    for (int k = 0; k < ngroups; ++k) M = fmaxf(M, __ldcg(gbase + ((size_t)k * G + h) * PART + PARTIAL_M));
+    float L = 0.0f, ob = 0.0f, ohist = 0.0f;
+#pragma unroll 8
+    for (int k = 0; k < ngroups; ++k) {
+      const float* pk = gbase + ((size_t)k * G + h) * PART;
+      const float mk = __ldcg(pk + PARTIAL_M);
+      const float f = (mk == -INFINITY) ? 0.0f : exp2f(mk - M);
+      L = fmaf(__ldcg(pk + PARTIAL_L), f, L);
+      const float ok = __ldcg(pk + t) * f;
+      if (k == 0)
+        ob += ok;
+      else
+        ohist += ok;
     }
-    const float qs = warp_sum(qr[0] + qr[1] + qr[2] + qr[3]);
-    __syncwarp();
+    oh[h * D + t] = ohist;
+    if (t == 0) sm.qsum[h] = L;
+    sm.q[h][t] = ob;
+  }
+  __syncthreads();
+  // out_c = (O_bf16_c + sum_j O_hist_j R_V[c][j]) / L with rot_vt[j][c] = R_V[c][j]:
+  // thread (group gr, lane l) sums rows 32 gr .. 32 gr + 31 for channels 4l .. 4l+3
+  {
+    const int lane = t & 31, grp = t >> 5;
+    float4 acc[G];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) sm.q[warp][4 * lane + i] = qr[i];
-    __syncwarp();
-
-    const int nhist = R.hist_end - SINK;
-    const int npages = (nhist + PAGE - 1) / PAGE;
-    const int pc0 = (sub - 1) * a.pages_per_chunk;
-    const int pc1 = min(npages, pc0 + a.pages_per_chunk);
-    const int32_t* pt = c.hist_pt + (size_t)R.slot * c.max_pages;
-    for (int pi = pc0; pi < pc1; ++pi) {
-      const int valid = min(PAGE, nhist - pi * PAGE);
-      int32_t page = pt[pi];
-      __syncthreads();
-      if (page < 0 || page >= c.n_int2_pages) {
-        if (threadIdx.x == 0) atomicOr(c.err, ERR_INT2_PAGE);
-        page = 0;
-      }
-      const uint4* src = reinterpret_cast<const uint4*>(c.int2 + layer * c.int2_layer_stride +
-                                                        ((size_t)page * c.Hkv + head) * RECORD);
-      for (int idx = threadIdx.x; idx < RECORD / 16; idx += blockDim.x)
-        reinterpret_cast<uint4*>(sm.buf.rec)[idx] = src[idx];
-      __syncthreads();
-
-      float lg[2];
-      float sv[2], zv[2];
+    for (int h = 0; h < G; ++h) acc[h] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    constexpr int BATCH = G <= 4 ? 16 : 8;   // R_V rows in flight per thread
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const int j = lane + 32 * h2;
-        const uint32_t km = *reinterpret_cast<const uint32_t*>(sm.buf.rec + K_META_OFF + j * META_BYTES);
-        const uint32_t vm = *reinterpret_cast<const uint32_t*>(sm.buf.rec + V_META_OFF + j * META_BYTES);
-        sv[h2] = 0.0f;
-        zv[h2] = 0.0f;
-        if (j < valid) {
-          // slots past the last demoted token hold stale bytes: never read them
-          sv[h2] = __half2float(__ushort_as_half(static_cast<uint16_t>(vm & 0xffff)));
-          zv[h2] = __half2float(__ushort_as_half(static_cast<uint16_t>(vm >> 16)));
-          const float sk = __half2float(__ushort_as_half(static_cast<uint16_t>(km & 0xffff)));
-          const float zk = __half2float(__ushort_as_half(static_cast<uint16_t>(km >> 16)));
-          const uint4* cr = reinterpret_cast<const uint4*>(sm.buf.rec + K_CODES_OFF + j * CODE_BYTES);
-          float dot = 0.0f;
+    for (int half = 0; half < 32 / BATCH; ++half) {
+      float4 r[BATCH];
 #pragma unroll
-          for (int half16 = 0; half16 < 2; ++half16) {
-            const uint4 w = cr[half16];
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+      for (int i = 0; i < BATCH; ++i)
+        r[i] = __ldg(reinterpret_cast<const float4*>(RVt + (size_t)(32 * grp + BATCH * half + i) * D) + lane);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
+      for (int i = 0; i < BATCH; ++i) {
+        const int j = 32 * grp + BATCH * half + i;
 #pragma unroll
-              for (int bit = 0; bit < 16; ++bit) {
-                const int ch = 64 * half16 + 16 * e + bit;
-                dot = fmaf(sm.q[warp][ch], static_cast<float>((ww[e] >> (2 * bit)) & 3u), dot);
-              }
-            }
-          }
-          lg[h2] = scale2 * fmaf(sk, dot, zk * qs);
-        } else {
-          lg[h2] = -INFINITY;
+        for (int h = 0; h < G; ++h) {
+          const float oj = oh[h * D + j];
+          acc[h].x = fmaf(oj, r[i].x, acc[h].x);
+          acc[h].y = fmaf(oj, r[i].y, acc[h].y);
+          acc[h].z = fmaf(oj, r[i].z, acc[h].z);
+          acc[h].w = fmaf(oj, r[i].w, acc[h].w);
         }
       }
-      const float m_new = online_rescale(st, warp_max(fmaxf(lg[0], lg[1])));
-      const float p0 = exp2f(lg[0] - m_new);
-      const float p1 = exp2f(lg[1] - m_new);
-      st.l += p0 + p1;
-      sm.w[warp][lane] = p0 * sv[0];
-      sm.w[warp][lane + 32] = p1 * sv[1];
-      st.u += p0 * zv[0] + p1 * zv[1];     // summed over lanes at the end
-      __syncwarp();
-      for (int j = 0; j < valid; ++j) {
-        const float w = sm.w[warp][j];
-        const uint32_t byte = sm.buf.rec[V_CODES_OFF + j * CODE_BYTES + lane];
-        st.o[0] = fmaf(w, static_cast<float>(byte & 3u), st.o[0]);
-        st.o[1] = fmaf(w, static_cast<float>((byte >> 2) & 3u), st.o[1]);
-        st.o[2] = fmaf(w, static_cast<float>((byte >> 4) & 3u), st.o[2]);
-        st.o[3] = fmaf(w, static_cast<float>((byte >> 6) & 3u), st.o[3]);
-      }
-      __syncwarp();
     }
-    const float usum = warp_sum(st.u);
+    float* mp = &sm.buf.state[0][0][0];   // [4][G][D]
 #pragma unroll
-    for (int i = 0; i < 4; ++i) st.o[i] += usum;
+    for (int h = 0; h < G; ++h) reinterpret_cast<float4*>(mp + ((size_t)grp * G + h) * D)[lane] = acc[h];
   }
-
-  // ---- write this item's partial for the warp's query head ----------------------
-  const float lsum = warp_sum(st.l);
-  float* part = partials + ((size_t)item * G + warp) * PART;
-  if (lane == 0) {
-    part[PARTIAL_M] = st.m;
-    part[PARTIAL_L] = lsum;
-  }
-  reinterpret_cast<float4*>(part)[lane] = make_float4(st.o[0], st.o[1], st.o[2], st.o[3]);
-  __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) sm.ticket = atomicAdd(counters + ri * c.Hkv + head, 1);
-  __syncthreads();
-  if (sm.ticket != per_head - 1) return;
-  __threadfence();
-
-  // ---- last item of this (request, kv head): merge --------------------------------
-  const int first = R.item_start + head * per_head;
-  float M = -INFINITY;
-  for (int k = 0; k < per_head; ++k) M = fmaxf(M, __ldcg(partials + ((size_t)(first + k) * G + warp) * PART + PARTIAL_M));
-  float L = 0.0f;
-  float ob[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  float ohist[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  for (int k = 0; k < per_head; ++k) {
-    const float* pk = partials + ((size_t)(first + k) * G + warp) * PART;
-    const float mk = __ldcg(pk + PARTIAL_M);
-    if (mk == -INFINITY) continue;
-    const float f = exp2f(mk - M);
-    L = fmaf(__ldcg(pk + PARTIAL_L), f, L);
-    const float4 ok = __ldcg(reinterpret_cast<const float4*>(pk) + lane);
-    float* dst = (k == 0) ? ob : ohist;
-    dst[0] = fmaf(ok.x, f, dst[0]);
-    dst[1] = fmaf(ok.y, f, dst[1]);
-    dst[2] = fmaf(ok.z, f, dst[2]);
-    dst[3] = fmaf(ok.w, f, dst[3]);
-  }
+  {
+    const float* mp = &sm.buf.state[0][0][0];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) sm.oh[warp][4 * lane + i] = ohist[i];
-  __syncwarp();
-  // out_c = O_bf16_c + sum_j O_hist_j R_V[c][j]; rot_vt[j][c] = R_V[c][j]
-  const float* __restrict__ RVt = c.rot_vt + lh * D * D;
-  for (int j = 0; j < D; ++j) {
-    const float oj = sm.oh[warp][j];
-    const float4 r = __ldg(reinterpret_cast<const float4*>(RVt + (size_t)j * D) + lane);
-    ob[0] = fmaf(oj, r.x, ob[0]);
-    ob[1] = fmaf(oj, r.y, ob[1]);
-    ob[2] = fmaf(oj, r.z, ob[2]);
-    ob[3] = fmaf(oj, r.w, ob[3]);
+    for (int h = 0; h < G; ++h) {
+      float v = sm.q[h][t];
+#pragma unroll
+      for (int g2 = 0; g2 < WARPS; ++g2) v += mp[((size_t)g2 * G + h) * D + t];
+      out[((size_t)R.batch_row * c.Hq + (size_t)head * G + h) * D + t] = v / sm.qsum[h];
+    }
   }
-  const float inv = 1.0f / L;
-  float* orow = out + ((size_t)R.batch_row * c.Hq + qh) * D;
-  reinterpret_cast<float4*>(orow)[lane] = make_float4(ob[0] * inv, ob[1] * inv, ob[2] * inv, ob[3] * inv);
-  if (threadIdx.x == 0) counters[ri * c.Hkv + head] = 0;
+  if (t == 0) cnt[0] = 0;
+}
+
+template <int G>
+cudaError_t launch_g(const DevCache& c, int layer, const DecodeArgs& a, int items, const uint16_t* q, float* out,
+                     int32_t* counters, float* qrot, float* partials, float* gpart, cudaStream_t s) {
+  static bool attr = false;
+  const size_t smem = sizeof(Smem<G>);
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  qrot_kernel<G><<<a.n * c.Hkv, QROT_THREADS, 0, s>>>(c, layer, a, q, qrot);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // programmatic dependent launch: decode CTAs start their page copies while
+  // the q rotation finishes, and wait for it (griddepcontrol.wait) before use
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(items));
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<G>, c, layer, a, q, out, counters, static_cast<const float*>(qrot),
+                            partials, gpart);
 }
 
 }  // namespace
@@ -346,17 +807,20 @@ cudaError_t launch_decode(const DevCache& c, int layer, const DecodeReq* reqs, c
   DecodeArgs a;
   a.n = plan.n;
   a.pages_per_chunk = plan.pages_per_chunk;
+  a.group_stride = plan.group_stride;
   for (int i = 0; i < plan.n; ++i) a.r[i] = reqs[i];
   int32_t* counters = static_cast<int32_t*>(workspace);
-  float* partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.counter_bytes);
+  float* qrot = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.counter_bytes);
+  float* partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.counter_bytes + plan.qrot_bytes);
+  float* gpart = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.counter_bytes + plan.qrot_bytes +
+                                          plan.partial_bytes);
   switch (c.G) {
-    case 1: decode_kernel<1><<<plan.total_items, 32, 0, s>>>(c, layer, a, q, out, counters, partials); break;
-    case 2: decode_kernel<2><<<plan.total_items, 64, 0, s>>>(c, layer, a, q, out, counters, partials); break;
-    case 4: decode_kernel<4><<<plan.total_items, 128, 0, s>>>(c, layer, a, q, out, counters, partials); break;
-    case 8: decode_kernel<8><<<plan.total_items, 256, 0, s>>>(c, layer, a, q, out, counters, partials); break;
+    case 1: return launch_g<1>(c, layer, a, plan.total_items, q, out, counters, qrot, partials, gpart, s);
+    case 2: return launch_g<2>(c, layer, a, plan.total_items, q, out, counters, qrot, partials, gpart, s);
+    case 4: return launch_g<4>(c, layer, a, plan.total_items, q, out, counters, qrot, partials, gpart, s);
+    case 8: return launch_g<8>(c, layer, a, plan.total_items, q, out, counters, qrot, partials, gpart, s);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace oscar

@@ -22,7 +22,6 @@ using namespace oscar;
 
 namespace {
 
-constexpr int CTAS_PER_SM_TARGET = 4;
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -500,12 +499,18 @@ DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int
   const int64_t H = c->cfg.num_kv_heads;
   int64_t total_pages = 0;
   for (int32_t i = 0; i < n; ++i) total_pages += H * pages_for(c->reqs[reqs[i]].he[layer]);
-  const int64_t target = std::max<int64_t>(1, (int64_t)c->num_sms * CTAS_PER_SM_TARGET);
-  const int64_t ppc = std::max<int64_t>({ppc_min, 2, (total_pages + target - 1) / target});
+  // one wave of resident CTAs: the BF16 items plus about as many INT2 chunks as fit beside them
+  const int64_t target = std::max<int64_t>(1, (int64_t)c->num_sms * DECODE_CTAS_PER_SM);
+  const int64_t budget = std::max<int64_t>(n * H, target - (int64_t)DECODE_BF16_ITEMS * n * H);
+  int64_t max_np = 0;
+  for (int32_t i = 0; i < n; ++i) max_np = std::max<int64_t>(max_np, pages_for(c->reqs[reqs[i]].he[layer]));
+  const int64_t ppc = std::max<int64_t>({ppc_min, 2, (total_pages + budget - 1) / budget,
+                                         (max_np + MAX_CHUNKS_PER_HEAD - 1) / MAX_CHUNKS_PER_HEAD});
   DecodePlan p{};
   p.n = n;
   p.pages_per_chunk = static_cast<int>(std::min<int64_t>(ppc, INT32_MAX));
   int64_t items = 0;
+  int64_t groups = 1;
   for (int32_t i = 0; i < n; ++i) {
     const Request& r = c->reqs[reqs[i]];
     const int64_t np = pages_for(r.he[layer]);
@@ -521,11 +526,15 @@ DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int
       d.item_start = static_cast<int32_t>(items);
       d.chunks = static_cast<int32_t>(chunks);
     }
-    items += H * (1 + chunks);
+    items += H * (DECODE_BF16_ITEMS + chunks);
+    groups = std::max<int64_t>(groups, 1 + (chunks + MERGE_GROUP - 1) / MERGE_GROUP);
   }
   p.total_items = static_cast<int>(items);
-  p.counter_bytes = 256 * (size_t)((n * H + 63) / 64);
+  p.group_stride = static_cast<int>(groups);
+  p.counter_bytes = align256((size_t)n * H * MERGE_COUNTERS * sizeof(int32_t));
+  p.qrot_bytes = align256((size_t)n * H * c->G() * QROT_FLOATS * sizeof(float));
   p.partial_bytes = align256((size_t)items * c->G() * PARTIAL_FLOATS * sizeof(float));
+  p.group_bytes = align256((size_t)n * H * groups * c->G() * PARTIAL_FLOATS * sizeof(float));
   return p;
 }
 
@@ -534,7 +543,7 @@ size_t decode_bytes_needed(const oscar_cache* c, int32_t layer, int32_t n, const
   for (int32_t b = 0; b < n; b += DECODE_PER_LAUNCH) {
     const int32_t m = std::min<int32_t>(DECODE_PER_LAUNCH, n - b);
     const DecodePlan p = plan_decode(c, layer, m, reqs + b, b, ppc_min, nullptr);
-    need = std::max(need, p.counter_bytes + p.partial_bytes);
+    need = std::max(need, p.counter_bytes + p.qrot_bytes + p.partial_bytes + p.group_bytes);
   }
   return need;
 }

@@ -112,12 +112,26 @@ struct DecodeReq {
   int32_t chunks;          // INT2 chunks per kv head
 };
 constexpr int DECODE_PER_LAUNCH = 64;
+constexpr int DECODE_BF16_ITEMS = 1 + RING_PAGES;   // BF16 work items per (request, kv head)
+constexpr int DECODE_CTAS_PER_SM = 3;               // resident decode CTAs per SM
+// rotated query record per (request, kv head, query head): q_rot[128], sum, prescale, pad
+constexpr int QROT_FLOATS = D + 4;
+constexpr int QROT_SUM = D;
+constexpr int QROT_SCALE = D + 1;
+// two-level merge: INT2 chunks are merged in groups of MERGE_GROUP; each
+// (request, kv head) owns MERGE_COUNTERS int32 tickets (head + groups)
+constexpr int MERGE_GROUP = 8;
+constexpr int MERGE_COUNTERS = 64;
+constexpr int MAX_CHUNKS_PER_HEAD = (MERGE_COUNTERS - 2) * MERGE_GROUP;
 struct DecodePlan {
   int n;
   int pages_per_chunk;
   int total_items;
+  int group_stride;
   size_t counter_bytes;
+  size_t qrot_bytes;
   size_t partial_bytes;
+  size_t group_bytes;
 };
 cudaError_t launch_decode(const DevCache& c, int layer, const DecodeReq* reqs, const DecodePlan& plan,
                           const uint16_t* q, float* out, void* workspace, cudaStream_t s);

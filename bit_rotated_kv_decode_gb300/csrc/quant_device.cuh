@@ -57,19 +57,34 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
-// fp32_rn of sum_i k_i * rt_i, k given as fp32 values that are exactly bf16.
-__device__ __forceinline__ float exact_dot_fp32(const float* k, int k_stride, const float* __restrict__ rt) {
-  double s = 0.0, c = 0.0;
-  for (int i = 0; i < D; ++i) {
-    const double p = static_cast<double>(k[i * k_stride]) * static_cast<double>(__ldg(rt + i));
-    const double t = s + p;
-    const double bp = t - s;
-    c += (s - (t - bp)) + (p - bp);
-    s = t;
+__device__ __forceinline__ void two_sum(double a, double b, double& s, double& e) {
+  s = a + b;
+  const double bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+
+// fp32_rn of sum_i k_i * r_i over 128 terms held by a whole warp, lane l holding
+// terms 4l .. 4l+3 (k exactly bf16-valued, r fp32).  Every product is exact in
+// double; the terms are added with TwoSum in a butterfly, so every lane ends
+// with the same (s, c), s + c within ~2^-100 * sum |k_i r_i| of the exact sum.
+__device__ __forceinline__ float warp_exact_dot(float4 k, float4 r) {
+  double s = static_cast<double>(k.x) * static_cast<double>(r.x);
+  double c = 0.0, e;
+  two_sum(s, static_cast<double>(k.y) * static_cast<double>(r.y), s, e);
+  c += e;
+  two_sum(s, static_cast<double>(k.z) * static_cast<double>(r.z), s, e);
+  c += e;
+  two_sum(s, static_cast<double>(k.w) * static_cast<double>(r.w), s, e);
+  c += e;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const double s2 = __shfl_xor_sync(0xffffffffu, s, off);
+    const double c2 = __shfl_xor_sync(0xffffffffu, c, off);
+    two_sum(s, s2, s, e);
+    c = (c + c2) + e;
   }
-  const double hi = s + c;
-  const double bh = hi - s;
-  const double lo = (s - (hi - bh)) + (c - bh);   // hi + lo == s + c exactly
+  double hi, lo;
+  two_sum(s, c, hi, lo);   // hi + lo == s + c exactly
   float f = __double2float_rn(hi);
   const double fd = static_cast<double>(f);
   if (hi != fd && lo != 0.0) {
@@ -81,19 +96,21 @@ __device__ __forceinline__ float exact_dot_fp32(const float* k, int k_stride, co
   return f;
 }
 
-// A full warp holds the group: lane l owns channels 4l .. 4l+3 (rotated by the
-// FMA chain, not yet clipped); err bounds the chain's error for this token.
-// exact(ch) returns fp32_rn(k . R_:ch) for channel ch.
-template <class Exact>
-__device__ __forceinline__ GroupCode quantize_group_warp(float4 xv, float err, float tau, Exact exact) {
+// A full warp holds the group: lane l owns channels 4l .. 4l+3 with rotated
+// values x (fast path) and error bounds err; k holds the token's input
+// channels 4l .. 4l+3 and rt points at R^T (row ch = column ch of R), so the
+// exact value of channel ch is warp_exact_dot(k, rt[ch][4l .. 4l+3]).
+__device__ __forceinline__ GroupCode quantize_group_warp(float4 xv, float4 ev, float tau, float4 k,
+                                                         const float* __restrict__ rt) {
   const int lane = threadIdx.x & 31;
-  float x[4] = {xv.x, xv.y, xv.z, xv.w};
+  const float x[4] = {xv.x, xv.y, xv.z, xv.w};
+  const float er[4] = {ev.x, ev.y, ev.z, ev.w};
   float lo[4], hi[4];
   GroupCode g;
   g.exact_calls = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float e = __fmaf_ru(fabsf(x[i]), 0x1.0001p-24f, err);
+    const float e = __fmaf_ru(fabsf(x[i]), 0x1.0001p-24f, er[i]);
     lo[i] = clip_canon(__fsub_rd(x[i], e), tau);
     hi[i] = clip_canon(__fadd_ru(x[i], e), tau);
   }
@@ -107,6 +124,10 @@ __device__ __forceinline__ GroupCode quantize_group_warp(float4 xv, float err, f
     for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
     return v;
   };
+  auto exact = [&](int ch) {
+    const float4 r = __ldg(reinterpret_cast<const float4*>(rt + (size_t)ch * D) + lane);
+    return warp_exact_dot(k, r);
+  };
   float mn_lo = reduce_min(fminf(fminf(lo[0], lo[1]), fminf(lo[2], lo[3])));
   float mn_hi = reduce_min(fminf(fminf(hi[0], hi[1]), fminf(hi[2], hi[3])));
   float mx_lo = reduce_max(fmaxf(fmaxf(lo[0], lo[1]), fmaxf(lo[2], lo[3])));
@@ -114,38 +135,68 @@ __device__ __forceinline__ GroupCode quantize_group_warp(float4 xv, float err, f
   const bool meta_sure = __half_as_ushort(__float2half_rn(mn_lo)) == __half_as_ushort(__float2half_rn(mn_hi)) &&
                          scale_of(mx_lo, mn_hi) == scale_of(mx_hi, mn_lo);
   if (!meta_sure) {
-    // (warp-uniform) the group's min or max is too close to an fp16 boundary: exact values
+    // (warp-uniform, rare) the group's min or max is too close to an fp16
+    // rounding boundary: take exactly every value that could be the min (its
+    // interval reaches below mn_hi) or the max (reaches above mx_lo).  The
+    // others lie strictly inside, so the extremes become exact.
+    uint32_t cand = 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float xe = clip_canon(exact(4 * lane + i), tau);
-      lo[i] = hi[i] = xe;
+    for (int i = 0; i < 4; ++i)
+      if (lo[i] <= mn_hi || hi[i] >= mx_lo) cand |= 1u << i;
+    uint32_t todo = __ballot_sync(0xffffffffu, cand != 0);
+    while (todo) {
+      const int src = __ffs(todo) - 1;
+      const int i = __ffs(__shfl_sync(0xffffffffu, cand, src)) - 1;
+      const float xe = clip_canon(exact(4 * src + i), tau);
+      if (lane == src) {
+        lo[i] = hi[i] = xe;
+        cand &= ~(1u << i);
+        g.exact_calls += 1;
+      }
+      todo = __ballot_sync(0xffffffffu, cand != 0);
     }
-    g.exact_calls += 4;
-    mn_lo = mn_hi = reduce_min(fminf(fminf(lo[0], lo[1]), fminf(lo[2], lo[3])));
-    mx_lo = mx_hi = reduce_max(fmaxf(fmaxf(lo[0], lo[1]), fmaxf(lo[2], lo[3])));
+    mn_lo = reduce_min(fminf(fminf(lo[0], lo[1]), fminf(lo[2], lo[3])));
+    mx_lo = reduce_max(fmaxf(fmaxf(lo[0], lo[1]), fmaxf(lo[2], lo[3])));
   }
   const __half zh = __float2half_rn(mn_lo);
   const float z = __half2float(zh);
-  const float sr = __fdiv_rn(__fsub_rn(mx_lo, mn_lo), 3.0f);
-  const __half sh = __float2half_rn(sr);
+  const __half sh = __float2half_rn(__fdiv_rn(__fsub_rn(mx_lo, mn_lo), 3.0f));
   const float s = __half2float(sh);
-  g.byte = 0;
+  uint32_t code[4];
+  uint32_t unsure = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    uint32_t c = code_of(lo[i], z, s);
-    if (c != code_of(hi[i], z, s)) {
-      c = code_of(clip_canon(exact(4 * lane + i), tau), z, s);
+    code[i] = code_of(lo[i], z, s);
+    if (code[i] != code_of(hi[i], z, s)) unsure |= 1u << i;
+  }
+  // resolve the undecided codes one at a time, the whole warp computing each
+  uint32_t pending = __ballot_sync(0xffffffffu, unsure != 0);
+  while (pending) {
+    const int src = __ffs(pending) - 1;
+    const uint32_t bits = __shfl_sync(0xffffffffu, unsure, src);
+    const int i = __ffs(bits) - 1;
+    const float xe = clip_canon(exact(4 * src + i), tau);
+    if (lane == src) {
+      code[i] = code_of(xe, z, s);
+      unsure &= ~(1u << i);
       g.exact_calls += 1;
     }
-    g.byte |= c << (2 * i);
+    pending = __ballot_sync(0xffffffffu, unsure != 0);
   }
+  g.byte = code[0] | (code[1] << 2) | (code[2] << 4) | (code[3] << 6);
   g.s_bits = __half_as_ushort(sh);
   g.z_bits = __half_as_ushort(zh);
   return g;
 }
 
-// Error bound of the FMA chain for a token with |k|_2^2 = knorm2 and a matrix
-// whose columns have norm at most colnorm.
+// gamma_n bound of an FMA chain / sum with n roundings, rounded up with margin.
+__device__ __forceinline__ float gamma_n(int n) {
+  const float u = 0x1p-24f;
+  return __fdiv_ru(n * u, 1.0f - n * u) * 1.0001f;
+}
+
+// Cauchy-Schwarz form of the chain bound for a token with |k|_2^2 = knorm2
+// and a matrix whose columns have norm at most colnorm.
 __device__ __forceinline__ float chain_error_bound(float knorm2, float colnorm) {
   return GAMMA_128 * 1.0001f * sqrtf(knorm2 * 1.0001f) * colnorm;
 }

@@ -167,8 +167,9 @@ __global__ void __launch_bounds__(128) prefill_hist_kernel(DevCache c, int layer
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) kn += __shfl_xor_sync(0xffffffffu, kn, off);
     const float err = chain_error_bound(kn, colnorm);
-    const float* kcol = kt + j;
-    const GroupCode g = quantize_group_warp(x, err, tau, [&](int ch) { return exact_dot_fp32(kcol, KT_STRIDE, Rt + ch * D); });
+    const float4 k4 = make_float4(kt[(4 * lane + 0) * KT_STRIDE + j], kt[(4 * lane + 1) * KT_STRIDE + j],
+                                  kt[(4 * lane + 2) * KT_STRIDE + j], kt[(4 * lane + 3) * KT_STRIDE + j]);
+    const GroupCode g = quantize_group_warp(x, make_float4(err, err, err, err), tau, k4, Rt);
     const int64_t h = t0 + j - SINK;
     const int32_t page = pt[h / PAGE];
     const int row = static_cast<int>(h % PAGE);
@@ -190,16 +191,28 @@ struct AppendArgs {
   AppendReq r[APPEND_PER_LAUNCH];
 };
 
-// One request (x), kv head (y), K or V (z) per block of 128 threads: demote the
-// token in the ring slot (if any), then write the new token into its slot.
-__global__ void __launch_bounds__(128) append_kernel(DevCache c, int layer, const uint16_t* __restrict__ k,
-                                                     const uint16_t* __restrict__ v, AppendArgs a) {
+constexpr int APPEND_THREADS = 256;
+constexpr int APPEND_GROUPS = APPEND_THREADS / 32;    // row groups of the rotation
+constexpr int APPEND_ROWS = D / APPEND_GROUPS;        // rows per group
+
+// One request (x), kv head (y), K or V (z) per block: demote the token in the
+// ring slot (if any), then write the new token into its slot.
+//
+// Rotation: thread (row group g, lane l) accumulates channels 4l .. 4l+3 over
+// rows 16g .. 16g+15 with 16 independent float4 loads of R; the 8 partial sums
+// are added in order.  Each value has at most 16 + 8 roundings, so its error
+// is below gamma_24 * sum_i |k_i R_ic|, which is accumulated alongside.
+__global__ void __launch_bounds__(APPEND_THREADS) append_kernel(DevCache c, int layer,
+                                                                const uint16_t* __restrict__ k,
+                                                                const uint16_t* __restrict__ v, AppendArgs a) {
   __shared__ float xin[D];
-  __shared__ float xrot[D];
+  __shared__ __align__(16) float part[APPEND_GROUPS][D];
+  __shared__ __align__(16) float apart[APPEND_GROUPS][D];
   const AppendReq q = a.r[blockIdx.x];
   const int head = blockIdx.y;
   const int which = blockIdx.z;
   const int t = threadIdx.x;
+  const int lane = t & 31, grp = t >> 5;
   const size_t lh = (size_t)layer * c.Hkv + head;
 
   if (q.demote_slot >= 0) {
@@ -208,29 +221,51 @@ __global__ void __launch_bounds__(128) append_kernel(DevCache c, int layer, cons
     if (!ok_src || !ok_dst) {
       if (t == 0) atomicOr(c.err, ok_src ? ERR_INT2_PAGE : ERR_BF16_PAGE);
     } else {
-      xin[t] = bf16_bits_to_float(bf16_row(c, layer, q.src_page, head, which, q.src_row)[t]);
-      __syncthreads();
       const float* __restrict__ R = (which ? c.rot_v : c.rot_k) + lh * D * D;
-      float acc = 0.0f;
-#pragma unroll 8
-      for (int i = 0; i < D; ++i) acc = fmaf(xin[i], __ldg(R + i * D + t), acc);
-      xrot[t] = acc;
+      float4 r[APPEND_ROWS];
+#pragma unroll
+      for (int i = 0; i < APPEND_ROWS; ++i)
+        r[i] = __ldg(reinterpret_cast<const float4*>(R + (size_t)(APPEND_ROWS * grp + i) * D) + lane);
+      if (t < D) xin[t] = bf16_bits_to_float(bf16_row(c, layer, q.src_page, head, which, q.src_row)[t]);
       __syncthreads();
-      if (t < 32) {
+      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f}, aac[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int i = 0; i < APPEND_ROWS; ++i) {
+        const float kv = xin[APPEND_ROWS * grp + i];
+        const float ka = fabsf(kv);
+        acc[0] = fmaf(kv, r[i].x, acc[0]);
+        acc[1] = fmaf(kv, r[i].y, acc[1]);
+        acc[2] = fmaf(kv, r[i].z, acc[2]);
+        acc[3] = fmaf(kv, r[i].w, acc[3]);
+        aac[0] = __fmaf_ru(ka, fabsf(r[i].x), aac[0]);
+        aac[1] = __fmaf_ru(ka, fabsf(r[i].y), aac[1]);
+        aac[2] = __fmaf_ru(ka, fabsf(r[i].z), aac[2]);
+        aac[3] = __fmaf_ru(ka, fabsf(r[i].w), aac[3]);
+      }
+      reinterpret_cast<float4*>(part[grp])[lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      reinterpret_cast<float4*>(apart[grp])[lane] = make_float4(aac[0], aac[1], aac[2], aac[3]);
+      __syncthreads();
+      if (grp == 0) {
+        float x[4], e[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float sum = part[0][4 * lane + j], asum = apart[0][4 * lane + j];
+#pragma unroll
+          for (int g2 = 1; g2 < APPEND_GROUPS; ++g2) {
+            sum += part[g2][4 * lane + j];
+            asum = __fadd_ru(asum, apart[g2][4 * lane + j]);
+          }
+          x[j] = sum;
+          e[j] = __fmul_ru(gamma_n(APPEND_ROWS + APPEND_GROUPS), asum);
+        }
         const float tau = (which ? c.tau_v : c.tau_k)[lh];
-        const float colnorm = c.rot_cn[(size_t)which * c.L * c.Hkv + lh];
         const float* __restrict__ Rt = (which ? c.rot_vt : c.rot_kt) + lh * D * D;
-        const float4 x = *reinterpret_cast<const float4*>(xrot + 4 * t);
-        float kn = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) kn = __fmaf_ru(xin[4 * t + i], xin[4 * t + i], kn);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) kn += __shfl_xor_sync(0xffffffffu, kn, off);
-        const GroupCode g = quantize_group_warp(x, chain_error_bound(kn, colnorm), tau,
-                                                [&](int ch) { return exact_dot_fp32(xin, 1, Rt + ch * D); });
+        const float4 k4 = make_float4(xin[4 * lane], xin[4 * lane + 1], xin[4 * lane + 2], xin[4 * lane + 3]);
+        const GroupCode g = quantize_group_warp(make_float4(x[0], x[1], x[2], x[3]), make_float4(e[0], e[1], e[2], e[3]),
+                                                tau, k4, Rt);
         uint8_t* rec = int2_record(c, layer, q.hist_page, head);
-        rec[(which ? V_CODES_OFF : K_CODES_OFF) + q.demote_slot * CODE_BYTES + t] = static_cast<uint8_t>(g.byte);
-        if (t == 0) {
+        rec[(which ? V_CODES_OFF : K_CODES_OFF) + q.demote_slot * CODE_BYTES + lane] = static_cast<uint8_t>(g.byte);
+        if (lane == 0) {
           *reinterpret_cast<uint32_t*>(rec + (which ? V_META_OFF : K_META_OFF) + q.demote_slot * META_BYTES) =
               static_cast<uint32_t>(g.s_bits) | (static_cast<uint32_t>(g.z_bits) << 16);
         }
@@ -241,7 +276,7 @@ __global__ void __launch_bounds__(128) append_kernel(DevCache c, int layer, cons
     }
   }
   __syncthreads();   // the demoted row has been read before its slot is overwritten
-  if (q.in_row >= 0) {
+  if (q.in_row >= 0 && t < D) {
     if (q.dst_page < 0 || q.dst_page >= c.n_bf16_pages) {
       if (t == 0) atomicOr(c.err, ERR_BF16_PAGE);
       return;
@@ -306,7 +341,7 @@ cudaError_t launch_append(const DevCache& c, int layer, const AppendReq* reqs, i
     a.n = n - base < APPEND_PER_LAUNCH ? n - base : APPEND_PER_LAUNCH;
     for (int i = 0; i < a.n; ++i) a.r[i] = reqs[base + i];
     dim3 grid(a.n, c.Hkv, 2);
-    append_kernel<<<grid, 128, 0, s>>>(c, layer, k, v, a);
+    append_kernel<<<grid, APPEND_THREADS, 0, s>>>(c, layer, k, v, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

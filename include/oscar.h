@@ -187,9 +187,10 @@ oscar_status oscar_decode_workspace_bytes(const oscar_cache* cache, int32_t n, c
  *   q          device bf16 [n][Hq][128].
  *   out        device fp32 [n][Hq][128].
  *   workspace  device, >= oscar_decode_workspace_bytes(), 256-byte aligned.
- *              Its first 256 bytes * ceil(n*Hkv/64) must be zero before the
- *              first use; every call leaves them zero again.  Calls that
- *              share a workspace must not overlap on the GPU. */
+ *              Its first 256 * min(n, 64) * num_kv_heads bytes (merge
+ *              tickets) must be zero before the first use; every call leaves
+ *              them zero again.  Calls that share a workspace must not
+ *              overlap on the GPU. */
 oscar_status oscar_decode_attention(oscar_cache* cache, int32_t layer, int32_t n, const int32_t* reqs,
                                     const uint16_t* q, float* out, void* workspace, size_t workspace_bytes,
                                     void* stream);
