@@ -41,7 +41,12 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr int PART = PARTIAL_FLOATS;
 constexpr int WARPS = 4;                 // warps per CTA
 constexpr int THREADS = 32 * WARPS;
-constexpr int STAGES = 3;                // TMA ring depth per warp
+// TMA ring depth per warp and resident CTAs per SM: GQA <= 4 trades a stage for
+// a fourth resident CTA (16 warps per SM); GQA 8 keeps three stages
+template <int G> struct Tune {
+  static constexpr int STAGES = G <= 4 ? 2 : 3;
+  static constexpr int CTAS = G <= 4 ? 4 : 3;
+};
 constexpr int BF16_ITEMS = DECODE_BF16_ITEMS;
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
 constexpr int ERR_TIMEOUT_BIT = 8;
@@ -49,6 +54,7 @@ constexpr int ERR_TIMEOUT_BIT = 8;
 struct DecodeArgs {
   int n;
   int pages_per_chunk;
+  int int2_items;            // INT2 CTAs, before the BF16 CTAs
   int group_stride;          // group partial slots per (request, kv head)
   DecodeReq r[DECODE_PER_LAUNCH];
 };
@@ -133,107 +139,137 @@ struct Smem {
   // INT2: per-warp TMA rings; BF16 items: the page's K rows (16-byte chunks
   // XOR-swizzled by row) and V rows; after the page loop: per-warp states.
   union {
-    __align__(128) uint8_t ring[WARPS][STAGES][RECORD];
+    __align__(128) uint8_t ring[WARPS][Tune<G>::STAGES][RECORD];
     struct {
       __align__(16) uint16_t k[PAGE][D];
       __align__(16) uint16_t v[PAGE][D];
     } bf;
     float state[WARPS][G][PART];
   } buf;
-  __align__(8) uint64_t bar[WARPS][STAGES];
-  float q[G][D];             // q (BF16 items) or q_rot (INT2 chunks)
+  __align__(8) uint64_t bar[WARPS][Tune<G>::STAGES];
+  float qin[G][D];           // q of the group's query heads (unrotated)
+  float q[G][D];             // q_rot (INT2 chunks); merge scratch
   float qsum[G];             // sum of q_rot over channels
   float qscale[G];           // power-of-two prescale of q_rot into fp16 range
   __align__(16) float pw[WARPS][G][PAGE];  // p * s_v of the current page, per warp
   float red[WARPS][G];
+  float cred[DECODE_CLUSTER][G][2];   // per-CTA partial sums / maxima of q_rot
   int ticket;
 };
 
-constexpr int QROT_THREADS = 256;
-constexpr int QROT_GROUPS = QROT_THREADS / 32;   // row groups
-constexpr int QROT_ROWS = D / QROT_GROUPS;       // rows per group
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
 
-// q_rot = q R_K for the G query heads of every (request, kv head) of the launch
-// (block x = request * Hkv + kv head), with per-head sums and the power-of-two
-// prescale that keeps the fp16 tensor-core operands finite.  Thread (group g,
-// lane l) accumulates channels 4l .. 4l+3 over rows 16g .. 16g+15 with 16
-// independent float4 loads of R_K.  The decode kernel is launched as its
-// programmatic dependent and waits for this grid before reading q_rot.
+// Store to the same shared-memory variable in CTA `rank` of this cluster.
+__device__ __forceinline__ void st_cluster(float* local, uint32_t rank, float v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+
+// Execution-only cluster barrier: every CTA of the cluster has started (no
+// memory ordering, so outstanding loads are not waited for).
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// q_rot = q R_K for the G query heads, computed by the DECODE_CLUSTER CTAs of
+// one (request, kv head) together: CTA r of the cluster computes channels
+// 32 r .. 32 r + 31 (thread (group g, lane l): rows 32 g .. 32 g + 31 of column
+// 32 r + l, 32 independent loads of R_K) and stores them into every CTA's
+// sm.q through distributed shared memory, with its partial per-head sums and
+// maxima; a cluster barrier publishes them.  Leaves sm.q, sm.qsum and the
+// power-of-two prescale sm.qscale (|q_rot| 2^24 prescale <= 2^15).
+// q of the group (G x 128 bf16) into sm.qin, every load in flight at once.
 template <int G>
-__global__ void __launch_bounds__(QROT_THREADS) qrot_kernel(DevCache c, int layer, DecodeArgs a,
-                                                            const uint16_t* __restrict__ q, float* qrot) {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  __shared__ float qs[G][D];
-  __shared__ __align__(16) float part[QROT_GROUPS][G][D];
-  __shared__ float red[4][G][2];
-  const int ri = blockIdx.x / c.Hkv, head = blockIdx.x % c.Hkv;
-  const int t = threadIdx.x, lane = t & 31, grp = t >> 5;
-  const float* __restrict__ RK = c.rot_k + ((size_t)layer * c.Hkv + head) * D * D;
-  float4 r[QROT_ROWS];
+__device__ __forceinline__ void load_q(const uint16_t* qrow, Smem<G>& sm) {
+  const int t = threadIdx.x;
+  uint16_t qv[G * D / THREADS];
 #pragma unroll
-  for (int i = 0; i < QROT_ROWS; ++i)
-    r[i] = __ldg(reinterpret_cast<const float4*>(RK + (size_t)(QROT_ROWS * grp + i) * D) + lane);
-  const uint16_t* qrow = q + ((size_t)a.r[ri].batch_row * c.Hq + (size_t)head * G) * D;
-  for (int i = t; i < G * D; i += QROT_THREADS) qs[i / D][i % D] = __uint_as_float(static_cast<uint32_t>(qrow[i]) << 16);
-  __syncthreads();
+  for (int u = 0; u < G * D / THREADS; ++u) qv[u] = qrow[u * THREADS + t];
+#pragma unroll
+  for (int u = 0; u < G * D / THREADS; ++u) {
+    const int i = u * THREADS + t;
+    sm.qin[i / D][i % D] = __uint_as_float(static_cast<uint32_t>(qv[u]) << 16);
+  }
+}
+
+// This CTA's slab of R_K (column 32 rank + lane, rows 32 grp .. 32 grp + 31), loaded
+// before the page copies are queued so it is not served behind them.
+__device__ __forceinline__ void load_rk_slab(const DevCache& c, size_t lh, float (&r)[32]) {
+  const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
+  const float* __restrict__ RK = c.rot_k + lh * D * D + 32 * cluster_rank() + lane;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) r[i] = __ldg(RK + (size_t)(32 * grp + i) * D);
+}
+
+template <int G>
+__device__ __forceinline__ void cluster_rotate_q(const float (&r)[32], Smem<G>& sm) {
+  static_assert(DECODE_CLUSTER * 32 == D, "one 32-channel slab per cluster CTA");
+  const int t = threadIdx.x, lane = t & 31, grp = t >> 5;
+  const uint32_t rank = cluster_rank();
+  cluster_sync_relaxed();   // every CTA of the cluster runs before any remote store
+  float acc[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    acc[h] = 0.0f;
 #pragma unroll
-    for (int i = 0; i < QROT_ROWS; ++i) {
-      const float qv = qs[h][QROT_ROWS * grp + i];
-      acc.x = fmaf(qv, r[i].x, acc.x);
-      acc.y = fmaf(qv, r[i].y, acc.y);
-      acc.z = fmaf(qv, r[i].z, acc.z);
-      acc.w = fmaf(qv, r[i].w, acc.w);
-    }
-    reinterpret_cast<float4*>(part[grp][h])[lane] = acc;
+    for (int i = 0; i < 32; ++i) acc[h] = fmaf(sm.qin[h][32 * grp + i], r[i], acc[h]);
+    sm.pw[grp][h][lane] = acc[h];
   }
   __syncthreads();
-  if (t < D) {
-    float* out = qrot + (size_t)blockIdx.x * G * QROT_FLOATS;
+  for (int idx = t; idx < G * 32; idx += THREADS) {
+    const int h = idx >> 5, l = idx & 31;
+    float v = 0.0f;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float v = 0.0f;
+    for (int g2 = 0; g2 < WARPS; ++g2) v += sm.pw[g2][h][l];
 #pragma unroll
-      for (int g2 = 0; g2 < QROT_GROUPS; ++g2) v += part[g2][h][t];
-      out[h * QROT_FLOATS + t] = v;
-      float sum = v, mx = fabsf(v);
+    for (uint32_t dst = 0; dst < DECODE_CLUSTER; ++dst) st_cluster(&sm.q[h][32 * rank + l], dst, v);
+    float sum = v, mx = fabsf(v);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      }
-      if (lane == 0) {
-        red[grp][h][0] = sum;
-        red[grp][h][1] = mx;
+    for (int o = 16; o > 0; o >>= 1) {
+      sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if (l == 0) {
+#pragma unroll
+      for (uint32_t dst = 0; dst < DECODE_CLUSTER; ++dst) {
+        st_cluster(&sm.cred[rank][h][0], dst, sum);
+        st_cluster(&sm.cred[rank][h][1], dst, mx);
       }
     }
   }
-  __syncthreads();
+  cluster_sync();
   if (t < G) {
     float sum = 0.0f, mx = 0.0f;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      sum += red[w][t][0];
-      mx = fmaxf(mx, red[w][t][1]);
+    for (int k = 0; k < DECODE_CLUSTER; ++k) {
+      sum += sm.cred[k][t][0];
+      mx = fmaxf(mx, sm.cred[k][t][1]);
     }
-    // |q_rot| * 2^24 * prescale <= 2^15
     int e = 0;
     if (mx > 0.0f) e = static_cast<int>(floorf(log2f(32768.0f / mx))) - 24;
     e = max(-60, min(e, 60));
-    float* out = qrot + (size_t)blockIdx.x * G * QROT_FLOATS + t * QROT_FLOATS;
-    out[QROT_SUM] = sum;
-    out[QROT_SCALE] = ldexpf(1.0f, e);
+    sm.qsum[t] = sum;
+    sm.qscale[t] = ldexpf(1.0f, e);
   }
+  __syncthreads();
 }
 
 // One chunk of INT2 history pages of one (request, kv head); leaves the CTA's
 // partial (rotated basis) for every query head of the group in part_out.
 template <int G>
-__device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const DecodeReq& R, int ri, int head,
-                                           int chunk, int ppc, const float* qrot, Smem<G>& sm, float* part_out) {
+__device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const DecodeReq& R, int head, int chunk,
+                                           int ppc, const uint16_t* qrow, Smem<G>& sm, float* part_out) {
   constexpr int NT = (G + 3) / 4;       // n-tiles of 8 columns = 4 heads x (hi, lo)
+  constexpr int STAGES = Tune<G>::STAGES;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tid = lane & 3;
   const float scale2 = c.scale * LOG2E;
@@ -246,38 +282,53 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
   const uint8_t* base = c.int2 + layer * c.int2_layer_stride + (size_t)head * RECORD;
   const size_t pstride = (size_t)c.Hkv * RECORD;
   bool timed_out = false;
-  int issued = 0;   // copies issued by this warp (lane 0's count)
+  int issued = 0;
+  float rk_slab[32];   // copies issued by this warp (lane 0's count)
 
+  // page ids of this warp's pages, read 32 at a time (lane l holds page 32 b + l of
+  // batch b); page_src is called by the whole warp with increasing j
+  int32_t batch_pages = 0;
+  int batch_idx = -1;
   auto page_src = [&](int j) -> const uint8_t* {
-    int32_t page = pt[pc0 + warp + WARPS * j];
-    if (page < 0 || page >= c.n_int2_pages) {
-      atomicOr(c.err, ERR_INT2_PAGE);
-      page = 0;
+    const int b = j >> 5;
+    if (b != batch_idx) {
+      batch_idx = b;
+      const int jj = 32 * b + lane;
+      int32_t page = 0;
+      if (jj < my_n) {
+        page = pt[pc0 + warp + WARPS * jj];
+        if (page < 0 || page >= c.n_int2_pages) {
+          atomicOr(c.err, ERR_INT2_PAGE);
+          page = 0;
+        }
+      }
+      batch_pages = page;
     }
-    return base + (size_t)page * pstride;
+    return base + (size_t)__shfl_sync(0xffffffffu, batch_pages, j & 31) * pstride;
   };
+  // every global load the prologue needs, issued together before any page copy:
+  // the first batch of page ids, this CTA's R_K slab and q
+  (void)page_src(0);
+  load_rk_slab(c, (size_t)layer * c.Hkv + head, rk_slab);
+  load_q<G>(qrow, sm);
+  __syncthreads();
   if (lane == 0) {
 #pragma unroll
     for (int st = 0; st < STAGES; ++st) mbar_init(&sm.bar[warp][st], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    for (int j = 0; j < STAGES && j < my_n; ++j) {
+  }
+#pragma unroll
+  for (int j = 0; j < STAGES; ++j) {
+    const uint8_t* src = page_src(j);
+    if (lane == 0 && j < my_n) {
       mbar_expect_tx(&sm.bar[warp][j], RECORD);
-      tma_load_1d(sm.buf.ring[warp][j], page_src(j), RECORD, &sm.bar[warp][j]);
+      tma_load_1d(sm.buf.ring[warp][j], src, RECORD, &sm.bar[warp][j]);
       ++issued;
     }
   }
-  // the copies are in flight while this grid waits for the q rotation grid
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  {
-    const float* qr = qrot + (size_t)(ri * c.Hkv + head) * G * QROT_FLOATS;
-    for (int i = threadIdx.x; i < G * D; i += THREADS) sm.q[i / D][i % D] = __ldcg(qr + (i / D) * QROT_FLOATS + i % D);
-    if (threadIdx.x < G) {
-      sm.qsum[threadIdx.x] = __ldcg(qr + threadIdx.x * QROT_FLOATS + QROT_SUM);
-      sm.qscale[threadIdx.x] = __ldcg(qr + threadIdx.x * QROT_FLOATS + QROT_SCALE);
-    }
-    __syncthreads();
-  }
+  // the copies are in flight while the cluster rotates q
+  cluster_rotate_q<G>(rk_slab, sm);
   // weights p * s_v are prescaled by 2^ew so the smallest ones stay representable in
   // fp16: s_v <= fp16(2 tau_V / 3) and p <= 1, so p s_v 2^ew <= 2^15
   int ew;
@@ -394,14 +445,16 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
       pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
       pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
       const float m_new = fmaxf(m_run[nt], pm);
-      const float corr = (m_run[nt] == -INFINITY) ? 0.0f : exp2f(m_run[nt] - m_new);
-      m_run[nt] = m_new;
-      l_run[nt] *= corr;
-      u_run[nt] *= corr;
+      if (m_new > m_run[nt]) {   // rescale only when the running max grows
+        const float corr = (m_run[nt] == -INFINITY) ? 0.0f : exp2f(m_run[nt] - m_new);
+        m_run[nt] = m_new;
+        l_run[nt] *= corr;
+        u_run[nt] *= corr;
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt)
+        for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) o[nt][mt][e] *= corr;
+          for (int e = 0; e < 4; ++e) o[nt][mt][e] *= corr;
+      }
       const int h = 4 * nt + tid;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -448,10 +501,13 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
       }
     }
     __syncwarp();
-    if (lane == 0 && j + STAGES < my_n) {
-      mbar_expect_tx(&sm.bar[warp][stg], RECORD);
-      tma_load_1d(sm.buf.ring[warp][stg], page_src(j + STAGES), RECORD, &sm.bar[warp][stg]);
-      ++issued;
+    {
+      const uint8_t* src = page_src(j + STAGES);
+      if (lane == 0 && j + STAGES < my_n) {
+        mbar_expect_tx(&sm.bar[warp][stg], RECORD);
+        tma_load_1d(sm.buf.ring[warp][stg], src, RECORD, &sm.bar[warp][stg]);
+        ++issued;
+      }
     }
   }
   if (timed_out && lane == 0) {
@@ -569,7 +625,7 @@ __device__ __forceinline__ void bf16_item(const DevCache& c, int layer, const De
         const float k0 = bf16lo(ww[e]), k1 = bf16hi(ww[e]);
         const int ch = 8 * chunk + 2 * e;
 #pragma unroll
-        for (int h = 0; h < G; ++h) acc[h] = fmaf(sm.q[h][ch + 1], k1, fmaf(sm.q[h][ch], k0, acc[h]));
+        for (int h = 0; h < G; ++h) acc[h] = fmaf(sm.qin[h][ch + 1], k1, fmaf(sm.qin[h][ch], k0, acc[h]));
       }
     }
     const bool ok = row_valid(r);
@@ -614,48 +670,71 @@ __device__ __forceinline__ void bf16_item(const DevCache& c, int layer, const De
   }
 }
 
-// Online-softmax merge of `count` consecutive partials (stride G * PART floats)
-// into one: thread t owns channel t of every query head.
+// Online-softmax merge of `count` (<= MERGE_GROUP) consecutive partials
+// (stride G * PART floats) into one.  The (m, l) pairs are loaded by
+// different threads at once; then thread t owns channel t of every head and
+// issues all of its count * G loads before using them.
 template <int G>
-__device__ __forceinline__ void merge_partials(const float* src, int count, float* dst) {
+__device__ __forceinline__ void merge_partials(const float* src, int count, float* dst, Smem<G>& sm) {
   const int t = threadIdx.x;
-#pragma unroll 1
-  for (int h = 0; h < G; ++h) {
+  if (t < count * G) {
+    const int k = t / G, h = t % G;
+    sm.pw[0][h][k] = __ldcg(src + ((size_t)k * G + h) * PART + PARTIAL_M);
+    sm.pw[0][h][MERGE_GROUP + k] = __ldcg(src + ((size_t)k * G + h) * PART + PARTIAL_L);
+  }
+  float ov[MERGE_GROUP][G];
+#pragma unroll
+  for (int k = 0; k < MERGE_GROUP; ++k)
+#pragma unroll
+    for (int h = 0; h < G; ++h) ov[k][h] = k < count ? __ldcg(src + ((size_t)k * G + h) * PART + t) : 0.0f;
+  __syncthreads();
+  if (t < G) {
     float M = -INFINITY;
-#pragma unroll 8
-    for (int k = 0; k < count; ++k) M = fmaxf(M, __ldcg(src + ((size_t)k * G + h) * PART + PARTIAL_M));
-    float L = 0.0f, o = 0.0f;
-#pragma unroll 8
+    for (int k = 0; k < count; ++k) M = fmaxf(M, sm.pw[0][t][k]);
+    float L = 0.0f;
     for (int k = 0; k < count; ++k) {
-      const float* pk = src + ((size_t)k * G + h) * PART;
-      const float mk = __ldcg(pk + PARTIAL_M);
+      const float mk = sm.pw[0][t][k];
       const float f = (mk == -INFINITY) ? 0.0f : exp2f(mk - M);
-      L = fmaf(__ldcg(pk + PARTIAL_L), f, L);
-      o = fmaf(__ldcg(pk + t), f, o);
+      sm.pw[0][t][2 * MERGE_GROUP + k] = f;
+      L = fmaf(sm.pw[0][t][MERGE_GROUP + k], f, L);
     }
+    dst[t * PART + PARTIAL_M] = M;
+    dst[t * PART + PARTIAL_L] = L;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float o = 0.0f;
+#pragma unroll
+    for (int k = 0; k < MERGE_GROUP; ++k)
+      if (k < count) o = fmaf(ov[k][h], sm.pw[0][h][2 * MERGE_GROUP + k], o);
     dst[h * PART + t] = o;
-    if (t == 0) {
-      dst[h * PART + PARTIAL_M] = M;
-      dst[h * PART + PARTIAL_L] = L;
-    }
   }
 }
 
 template <int G>
-__global__ void __launch_bounds__(THREADS, DECODE_CTAS_PER_SM) decode_kernel(DevCache c, int layer, DecodeArgs a,
+__global__ void __launch_bounds__(THREADS, Tune<G>::CTAS) decode_kernel(DevCache c, int layer, DecodeArgs a,
                                                          const uint16_t* __restrict__ q, float* __restrict__ out,
-                                                         int32_t* counters, const float* qrot, float* partials,
-                                                         float* gpart) {
+                                                         int32_t* counters, float* partials, float* gpart) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem<G>& sm = *reinterpret_cast<Smem<G>*>(smem_raw);
   const int item = blockIdx.x;
-  int ri = 0;
-  while (ri + 1 < a.n && a.r[ri + 1].item_start <= item) ++ri;
+  int ri = 0, head, sub;
+  if (item < a.int2_items) {
+    // INT2 chunk: clusters of DECODE_CLUSTER consecutive CTAs share one (request, kv head)
+    while (ri + 1 < a.n && a.r[ri + 1].int2_start <= item) ++ri;
+    const int local = item - a.r[ri].int2_start;
+    head = local / a.r[ri].chunks;
+    sub = BF16_ITEMS + local % a.r[ri].chunks;
+  } else {
+    const int b = item - a.int2_items;
+    if (b >= a.n * c.Hkv * BF16_ITEMS) return;   // cluster padding
+    ri = b / (c.Hkv * BF16_ITEMS);
+    head = (b / BF16_ITEMS) % c.Hkv;
+    sub = b % BF16_ITEMS;
+  }
   const DecodeReq R = a.r[ri];
   const int per_head = BF16_ITEMS + R.chunks;
-  const int local = item - R.item_start;
-  const int head = local / per_head;
-  const int sub = local % per_head;
   const int t = threadIdx.x;
   const size_t lh = (size_t)layer * c.Hkv + head;
   const float* __restrict__ RVt = c.rot_vt + lh * D * D;
@@ -666,63 +745,106 @@ __global__ void __launch_bounds__(THREADS, DECODE_CTAS_PER_SM) decode_kernel(Dev
       asm volatile("prefetch.global.L2 [%0];" ::"l"(RVt + (size_t)line * 32));
   }
   const uint16_t* qrow = q + ((size_t)R.batch_row * c.Hq + (size_t)head * G) * D;
-  for (int i = t; i < G * D; i += THREADS) sm.q[i / D][i % D] = __uint_as_float(static_cast<uint32_t>(qrow[i]) << 16);
-  __syncthreads();
+  if (sub < BF16_ITEMS) {
+    load_q<G>(qrow, sm);
+    __syncthreads();
+  }
 
-  float* part = partials + (size_t)item * G * PART;
+  const size_t head_parts = (size_t)R.part_start + (size_t)head * per_head;
+  float* part = partials + (head_parts + sub) * G * PART;
   if (sub < BF16_ITEMS) {
     bf16_item<G>(c, layer, R, head, sub, sm, part);
   } else {
-    int2_chunk<G>(c, layer, R, ri, head, sub - BF16_ITEMS, a.pages_per_chunk, qrot, sm, part);
+    int2_chunk<G>(c, layer, R, head, sub - BF16_ITEMS, a.pages_per_chunk, qrow, sm, part);
   }
 
   // ---- two-level merge by atomic tickets (nobody waits) -----------------------------
-  // group 0 = the BF16 items, group g >= 1 = INT2 chunks (g-1)*MERGE_GROUP .. +MERGE_GROUP-1
+  // group 0 = the BF16 items, group g >= 1 = INT2 chunks (g-1)*MERGE_GROUP .. +MERGE_GROUP-1.
+  // Ticket protocol: block barrier, then one thread fences (cumulative over the
+  // block's writes) and takes the ticket; the winner fences before reading.
   const int g = sub < BF16_ITEMS ? 0 : 1 + (sub - BF16_ITEMS) / MERGE_GROUP;
   const int gfirst = g == 0 ? 0 : BF16_ITEMS + (g - 1) * MERGE_GROUP;
   const int gcount = g == 0 ? BF16_ITEMS : min(MERGE_GROUP, R.chunks - (g - 1) * MERGE_GROUP);
   const int ngroups = 1 + (R.chunks + MERGE_GROUP - 1) / MERGE_GROUP;
   int32_t* cnt = counters + (size_t)(ri * c.Hkv + head) * MERGE_COUNTERS;
   float* gbase = gpart + (size_t)(ri * c.Hkv + head) * a.group_stride * G * PART;
-  __threadfence();
   __syncthreads();
-  if (t == 0) sm.ticket = atomicAdd(cnt + 1 + g, 1);
+  if (t == 0) {
+    __threadfence();
+    sm.ticket = atomicAdd(cnt + 1 + g, 1);
+    if (sm.ticket == gcount - 1) __threadfence();
+  }
   __syncthreads();
   if (sm.ticket != gcount - 1) return;
-  __threadfence();
-  merge_partials<G>(partials + (size_t)(R.item_start + head * per_head + gfirst) * G * PART, gcount,
-                    gbase + (size_t)g * G * PART);
-  if (t == 0) cnt[1 + g] = 0;
-  __threadfence();
+  merge_partials<G>(partials + (head_parts + gfirst) * G * PART, gcount, gbase + (size_t)g * G * PART, sm);
   __syncthreads();
-  if (t == 0) sm.ticket = atomicAdd(cnt, 1);
+  if (t == 0) {
+    cnt[1 + g] = 0;
+    __threadfence();
+    sm.ticket = atomicAdd(cnt, 1);
+    if (sm.ticket == ngroups - 1) __threadfence();
+  }
   __syncthreads();
   if (sm.ticket != ngroups - 1) return;
-  __threadfence();
 
   // ---- last group of this (request, kv head): BF16 part + R_V^T (history part) ----
-  float* oh = &sm.pw[0][0][0];   // [G][D] history part (rotated basis)
-#pragma unroll 1
+  // stage every group partial in shared memory with one round of 16-byte loads
+  float* gs = &sm.buf.state[0][0][0];   // [ngroups][G][PART], staged in chunks of STAGE_GROUPS
+  constexpr int STAGE_GROUPS = (WARPS * Tune<G>::STAGES * RECORD) / (G * PART * 4);
+  float* oh = &sm.pw[0][0][0];           // [G][D] history part (rotated basis)
+  float M[G], L[G], ob[G], ohist[G];
+#pragma unroll
   for (int h = 0; h < G; ++h) {
-    float M = -INFINITY;
-#pragma unroll 8
-    for (int k = 0; k < ngroups; ++k) M = fmaxf(M, __ldcg(gbase + ((size_t)k * G + h) * PART + PARTIAL_M));
-    float L = 0.0f, ob = 0.0f, ohist = 0.0f;
-#pragma unroll 8
-    for (int k = 0; k < ngroups; ++k) {
-      const float* pk = gbase + ((size_t)k * G + h) * PART;
-      const float mk = __ldcg(pk + PARTIAL_M);
-      const float f = (mk == -INFINITY) ? 0.0f : exp2f(mk - M);
-      L = fmaf(__ldcg(pk + PARTIAL_L), f, L);
-      const float ok = __ldcg(pk + t) * f;
-      if (k == 0)
-        ob += ok;
-      else
-        ohist += ok;
+    M[h] = -INFINITY;
+    L[h] = 0.0f;
+    ob[h] = 0.0f;
+    ohist[h] = 0.0f;
+  }
+  for (int k0 = 0; k0 < ngroups; k0 += STAGE_GROUPS) {
+    const int kn = min(STAGE_GROUPS, ngroups - k0);
+    const int n4 = kn * G * PART / 4;
+    const float4* src4 = reinterpret_cast<const float4*>(gbase + (size_t)k0 * G * PART);
+    for (int i0 = 0; i0 < n4; i0 += 8 * THREADS) {
+      float4 v4[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * THREADS + t;
+        if (i < n4) v4[u] = __ldcg(src4 + i);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * THREADS + t;
+        if (i < n4) reinterpret_cast<float4*>(gs)[i] = v4[u];
+      }
     }
-    oh[h * D + t] = ohist;
-    if (t == 0) sm.qsum[h] = L;
-    sm.q[h][t] = ob;
+    __syncthreads();
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float Mn = M[h];
+      for (int k = 0; k < kn; ++k) Mn = fmaxf(Mn, gs[(k * G + h) * PART + PARTIAL_M]);
+      const float fo = (M[h] == -INFINITY) ? 0.0f : exp2f(M[h] - Mn);
+      L[h] *= fo;
+      ob[h] *= fo;
+      ohist[h] *= fo;
+      M[h] = Mn;
+      for (int k = 0; k < kn; ++k) {
+        const float* pk = gs + (k * G + h) * PART;
+        const float mk = pk[PARTIAL_M];
+        const float f = (mk == -INFINITY) ? 0.0f : exp2f(mk - Mn);
+        L[h] = fmaf(pk[PARTIAL_L], f, L[h]);
+        if (k0 + k == 0)
+          ob[h] = fmaf(pk[t], f, ob[h]);
+        else
+          ohist[h] = fmaf(pk[t], f, ohist[h]);
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    oh[h * D + t] = ohist[h];
+    if (t == 0) sm.qsum[h] = L[h];
+    sm.q[h][t] = ob[h];
   }
   __syncthreads();
   // out_c = (O_bf16_c + sum_j O_hist_j R_V[c][j]) / L with rot_vt[j][c] = R_V[c][j]:
@@ -772,32 +894,29 @@ __global__ void __launch_bounds__(THREADS, DECODE_CTAS_PER_SM) decode_kernel(Dev
 
 template <int G>
 cudaError_t launch_g(const DevCache& c, int layer, const DecodeArgs& a, int items, const uint16_t* q, float* out,
-                     int32_t* counters, float* qrot, float* partials, float* gpart, cudaStream_t s) {
+                     int32_t* counters, float* partials, float* gpart, cudaStream_t s) {
   static bool attr = false;
   const size_t smem = sizeof(Smem<G>);
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_kernel<G>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  qrot_kernel<G><<<a.n * c.Hkv, QROT_THREADS, 0, s>>>(c, layer, a, q, qrot);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  // programmatic dependent launch: decode CTAs start their page copies while
-  // the q rotation finishes, and wait for it (griddepcontrol.wait) before use
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(items));
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = DECODE_CLUSTER;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<G>, c, layer, a, q, out, counters, static_cast<const float*>(qrot),
-                            partials, gpart);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<G>, c, layer, a, q, out, counters, partials, gpart);
 }
 
 }  // namespace
@@ -808,19 +927,22 @@ cudaError_t launch_decode(const DevCache& c, int layer, const DecodeReq* reqs, c
   a.n = plan.n;
   a.pages_per_chunk = plan.pages_per_chunk;
   a.group_stride = plan.group_stride;
+  a.int2_items = plan.int2_items;
   for (int i = 0; i < plan.n; ++i) a.r[i] = reqs[i];
   int32_t* counters = static_cast<int32_t*>(workspace);
-  float* qrot = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.counter_bytes);
-  float* partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.counter_bytes + plan.qrot_bytes);
-  float* gpart = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.counter_bytes + plan.qrot_bytes +
-                                          plan.partial_bytes);
+  float* partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.counter_bytes);
+  float* gpart = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.counter_bytes + plan.partial_bytes);
   switch (c.G) {
-    case 1: return launch_g<1>(c, layer, a, plan.total_items, q, out, counters, qrot, partials, gpart, s);
-    case 2: return launch_g<2>(c, layer, a, plan.total_items, q, out, counters, qrot, partials, gpart, s);
-    case 4: return launch_g<4>(c, layer, a, plan.total_items, q, out, counters, qrot, partials, gpart, s);
-    case 8: return launch_g<8>(c, layer, a, plan.total_items, q, out, counters, qrot, partials, gpart, s);
+    case 1: return launch_g<1>(c, layer, a, plan.total_items, q, out, counters, partials, gpart, s);
+    case 2: return launch_g<2>(c, layer, a, plan.total_items, q, out, counters, partials, gpart, s);
+    case 4: return launch_g<4>(c, layer, a, plan.total_items, q, out, counters, partials, gpart, s);
+    case 8: return launch_g<8>(c, layer, a, plan.total_items, q, out, counters, partials, gpart, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
+}  // namespace oscar
+
+namespace oscar {
+int decode_ctas_per_sm(int g) { return g <= 4 ? Tune<4>::CTAS : Tune<8>::CTAS; }
 }  // namespace oscar

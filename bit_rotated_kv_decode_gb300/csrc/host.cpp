@@ -491,30 +491,44 @@ oscar_status write_batch(oscar_cache* c, int32_t layer, int32_t n, const int32_t
   return err == cudaSuccess ? OSCAR_OK : c->cuda_fail(err, append ? "append launch" : "demote launch");
 }
 
-// Work split of one decode launch over reqs[0..n), n <= DECODE_PER_LAUNCH:
-// per (request, kv head) one BF16 item plus ceil(pages / ppc) INT2 chunks,
-// with ppc chosen so the launch has about CTAS_PER_SM_TARGET items per SM.
+// Work split of one decode launch over reqs[0..n), n <= DECODE_PER_LAUNCH.
+// Per (request, kv head): five BF16 items (sink page, four ring pages) and
+// a multiple of DECODE_CLUSTER INT2 chunks of pages_per_chunk pages, sized so
+// the launch is about one wave of resident CTAs.
+int64_t chunks_for(int64_t np, int64_t ppc) {
+  if (np == 0) return 0;
+  const int64_t c = (np + ppc - 1) / ppc;
+  return (c + DECODE_CLUSTER - 1) / DECODE_CLUSTER * DECODE_CLUSTER;
+}
+
 DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int32_t* reqs, int32_t first_row,
                        int64_t ppc_min, DecodeReq* out) {
   const int64_t H = c->cfg.num_kv_heads;
-  int64_t total_pages = 0;
-  for (int32_t i = 0; i < n; ++i) total_pages += H * pages_for(c->reqs[reqs[i]].he[layer]);
-  // one wave of resident CTAs: the BF16 items plus about as many INT2 chunks as fit beside them
-  const int64_t target = std::max<int64_t>(1, (int64_t)c->num_sms * DECODE_CTAS_PER_SM);
-  const int64_t budget = std::max<int64_t>(n * H, target - (int64_t)DECODE_BF16_ITEMS * n * H);
-  int64_t max_np = 0;
-  for (int32_t i = 0; i < n; ++i) max_np = std::max<int64_t>(max_np, pages_for(c->reqs[reqs[i]].he[layer]));
-  const int64_t ppc = std::max<int64_t>({ppc_min, 2, (total_pages + budget - 1) / budget,
-                                         (max_np + MAX_CHUNKS_PER_HEAD - 1) / MAX_CHUNKS_PER_HEAD});
+  int64_t total_pages = 0, max_np = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const int64_t np = pages_for(c->reqs[reqs[i]].he[layer]);
+    total_pages += H * np;
+    max_np = std::max(max_np, np);
+  }
+  const int64_t target = std::max<int64_t>(1, (int64_t)c->num_sms * decode_ctas_per_sm(c->G()));
+  const int64_t bf16 = ((int64_t)DECODE_BF16_ITEMS * n * H + DECODE_CLUSTER - 1) / DECODE_CLUSTER * DECODE_CLUSTER;
+  const int64_t budget = std::max<int64_t>(n * H, target - bf16);
+  int64_t ppc = std::max<int64_t>({ppc_min, 2, (total_pages + budget - 1) / budget,
+                                   (max_np + MAX_CHUNKS_PER_HEAD - 1) / MAX_CHUNKS_PER_HEAD});
+  // chunk counts are rounded up to whole clusters: grow ppc until the launch fits the budget
+  for (;;) {
+    int64_t items = 0;
+    for (int32_t i = 0; i < n; ++i) items += H * chunks_for(pages_for(c->reqs[reqs[i]].he[layer]), ppc);
+    if (items <= budget || ppc >= max_np) break;
+    ++ppc;
+  }
   DecodePlan p{};
   p.n = n;
   p.pages_per_chunk = static_cast<int>(std::min<int64_t>(ppc, INT32_MAX));
-  int64_t items = 0;
-  int64_t groups = 1;
+  int64_t int2 = 0, parts = 0, groups = 1;
   for (int32_t i = 0; i < n; ++i) {
     const Request& r = c->reqs[reqs[i]];
-    const int64_t np = pages_for(r.he[layer]);
-    const int64_t chunks = (np + ppc - 1) / ppc;
+    const int64_t chunks = chunks_for(pages_for(r.he[layer]), ppc);
     if (out) {
       DecodeReq& d = out[i];
       d.slot = reqs[i];
@@ -523,17 +537,19 @@ DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int
       d.hist_end = static_cast<int32_t>(r.he[layer]);
       d.sink_page = r.bf16_pt[0];
       for (int k = 0; k < RING_PAGES; ++k) d.ring_page[k] = r.bf16_pt[1 + k];
-      d.item_start = static_cast<int32_t>(items);
+      d.int2_start = static_cast<int32_t>(int2);
       d.chunks = static_cast<int32_t>(chunks);
+      d.part_start = static_cast<int32_t>(parts);
     }
-    items += H * (DECODE_BF16_ITEMS + chunks);
+    int2 += H * chunks;
+    parts += H * (DECODE_BF16_ITEMS + chunks);
     groups = std::max<int64_t>(groups, 1 + (chunks + MERGE_GROUP - 1) / MERGE_GROUP);
   }
-  p.total_items = static_cast<int>(items);
+  p.int2_items = static_cast<int>(int2);
+  p.total_items = static_cast<int>(int2 + bf16);
   p.group_stride = static_cast<int>(groups);
   p.counter_bytes = align256((size_t)n * H * MERGE_COUNTERS * sizeof(int32_t));
-  p.qrot_bytes = align256((size_t)n * H * c->G() * QROT_FLOATS * sizeof(float));
-  p.partial_bytes = align256((size_t)items * c->G() * PARTIAL_FLOATS * sizeof(float));
+  p.partial_bytes = align256((size_t)parts * c->G() * PARTIAL_FLOATS * sizeof(float));
   p.group_bytes = align256((size_t)n * H * groups * c->G() * PARTIAL_FLOATS * sizeof(float));
   return p;
 }
@@ -543,7 +559,7 @@ size_t decode_bytes_needed(const oscar_cache* c, int32_t layer, int32_t n, const
   for (int32_t b = 0; b < n; b += DECODE_PER_LAUNCH) {
     const int32_t m = std::min<int32_t>(DECODE_PER_LAUNCH, n - b);
     const DecodePlan p = plan_decode(c, layer, m, reqs + b, b, ppc_min, nullptr);
-    need = std::max(need, p.counter_bytes + p.qrot_bytes + p.partial_bytes + p.group_bytes);
+    need = std::max(need, p.counter_bytes + p.partial_bytes + p.group_bytes);
   }
   return need;
 }

@@ -127,12 +127,26 @@ __global__ void __launch_bounds__(128) prefill_hist_kernel(DevCache c, int layer
   const float tau = (which ? c.tau_v : c.tau_k)[lh];
   const float colnorm = c.rot_cn[(size_t)which * c.L * c.Hkv + lh];
 
-  for (int idx = threadIdx.x; idx < PAGE * D; idx += blockDim.x) {
-    const int j = idx / D;
-    const int i = idx % D;
-    float val = 0.0f;
-    if (j < ntok) val = bf16_bits_to_float(src[((size_t)(t0 + j - in_base) * c.Hkv + head) * D + i]);
-    kt[i * KT_STRIDE + j] = val;
+  {
+    // 64 tokens x 128 channels of bf16 = 1024 16-byte chunks, 8 per thread, all in flight
+    constexpr int CHUNKS = PAGE * D / 8 / 128;
+    uint4 v[CHUNKS];
+#pragma unroll
+    for (int u = 0; u < CHUNKS; ++u) {
+      const int idx = u * 128 + threadIdx.x, j = idx / (D / 8), part = idx % (D / 8);
+      v[u] = j < ntok ? reinterpret_cast<const uint4*>(src + ((size_t)(t0 + j - in_base) * c.Hkv + head) * D)[part]
+                      : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < CHUNKS; ++u) {
+      const int idx = u * 128 + threadIdx.x, j = idx / (D / 8), part = idx % (D / 8);
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        kt[(8 * part + 2 * e) * KT_STRIDE + j] = __uint_as_float(w[e] << 16);
+        kt[(8 * part + 2 * e + 1) * KT_STRIDE + j] = __uint_as_float(w[e] & 0xffff0000u);
+      }
+    }
   }
   __syncthreads();
 
