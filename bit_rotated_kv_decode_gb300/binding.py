@@ -73,6 +73,7 @@ _SIGNATURES = {
     "oscar_demote": (c_int32, [_P, c_int32, c_int32, POINTER(c_int32), _P]),
     "oscar_decode_workspace_bytes": (c_int32, [_P, c_int32, POINTER(c_int32), POINTER(c_size_t)]),
     "oscar_decode_attention": (c_int32, [_P, c_int32, c_int32, POINTER(c_int32), _P, _P, _P, c_size_t, _P]),
+    "oscar_decode_attention_noalloc": (c_int32, [_P, c_int32, c_int32, POINTER(c_int32), _P, _P, _P]),
     "oscar_cache_check": (c_int32, [_P, _P]),
     "oscar_last_error": (c_char_p, [_P]),
 }
@@ -244,6 +245,13 @@ class OscarCache:
         self._check(self.lib.oscar_decode_attention(self.h, layer, len(reqs), arr, _ptr(q), _ptr(out),
                                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
                                                     _stream_ptr(stream)), "decode")
+
+    def decode_noalloc(self, layer: int, reqs, q, out, stream=None) -> None:
+        """Decode with the library's fixed static scratch (no workspace argument)."""
+        arr = self._reqs(reqs)
+        self._check(self.lib.oscar_decode_attention_noalloc(self.h, layer, len(reqs), arr, _ptr(q), _ptr(out),
+                                                            None if self.dry else _stream_ptr(stream)),
+                    "decode (fixed scratch)", allow_dry=True)
 
     def check(self, stream=None) -> None:
         self._check(self.lib.oscar_cache_check(self.h, None if self.dry else _stream_ptr(stream)), "device check")

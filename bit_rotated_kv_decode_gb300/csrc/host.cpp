@@ -625,6 +625,31 @@ oscar_status oscar_decode_attention(oscar_cache* c, int32_t layer, int32_t n, co
   return OSCAR_OK;
 }
 
+// Same decode, with the merge tickets and partials in the library's fixed
+// static scratch (decode_scratch.cu) instead of a caller workspace, for callers
+// that cannot allocate device memory around a step.
+oscar_status oscar_decode_attention_noalloc(oscar_cache* c, int32_t layer, int32_t n, const int32_t* reqs,
+                                            const uint16_t* q, float* out, void* stream) {
+  if (!c) return OSCAR_ERR_INVALID_ARG;
+  const oscar_status st = check_decode_batch(c, layer, n, reqs);
+  if (st != OSCAR_OK) return st;
+  // the smallest plan: one cluster of chunks per (request, kv head)
+  const size_t need = decode_bytes_needed(c, layer, n, reqs, INT32_MAX);
+  if (need > DECODE_SCRATCH_BYTES) {
+    char msg[192];
+    std::snprintf(msg, sizeof msg,
+                  "batch needs %zu bytes of decode scratch, above the fixed %zu; "
+                  "use oscar_decode_attention with a caller workspace",
+                  need, DECODE_SCRATCH_BYTES);
+    return c->fail(OSCAR_ERR_INVALID_ARG, msg);
+  }
+  if (c->dry) return OSCAR_ERR_DRY_RUN;
+  void* scratch = nullptr;
+  const cudaError_t e = decode_scratch_address(&scratch, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return c->cuda_fail(e, "decode scratch set-up");
+  return oscar_decode_attention(c, layer, n, reqs, q, out, scratch, DECODE_SCRATCH_BYTES, stream);
+}
+
 oscar_status oscar_cache_check(oscar_cache* c, void* stream) {
   if (!c) return OSCAR_ERR_INVALID_ARG;
   if (c->dry) return OSCAR_OK;

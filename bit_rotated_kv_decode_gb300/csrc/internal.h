@@ -134,4 +134,10 @@ struct DecodePlan {
 cudaError_t launch_decode(const DevCache& c, int layer, const DecodeReq* reqs, const DecodePlan& plan,
                           const uint16_t* q, float* out, void* workspace, cudaStream_t s);
 
+// Fixed decode scratch (one static device array per device) for callers that
+// cannot allocate.  The first call on a device, with that device current,
+// takes the array's address and zeroes it on stream s.
+constexpr size_t DECODE_SCRATCH_BYTES = size_t(8) << 20;
+cudaError_t decode_scratch_address(void** ptr, cudaStream_t s);
+
 }  // namespace oscar

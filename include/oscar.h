@@ -195,6 +195,28 @@ oscar_status oscar_decode_attention(oscar_cache* cache, int32_t layer, int32_t n
                                     const uint16_t* q, float* out, void* workspace, size_t workspace_bytes,
                                     void* stream);
 
+/* oscar_decode_attention without a workspace argument: the library allocates
+ * nothing.  The pages have no counterpart to this call; it exists for callers
+ * that cannot allocate device memory around a decode step (a serving engine
+ * that gives all free HBM to its KV pools at start-up and owns no per-step
+ * allocator, or a plain C host with no allocator to pass).  The merge tickets
+ * and partials live in one fixed static device array of 8 MiB per device
+ * inside the library.
+ *   Arguments, layouts and results are those of oscar_decode_attention.
+ *   Size limit: a batch whose smallest plan (one cluster of four INT2 chunks
+ *     per request and kv head, per launch of up to 64 requests) needs more
+ *     than 8 MiB is rejected with OSCAR_ERR_INVALID_ARG before any work; use
+ *     oscar_decode_attention with a caller workspace for it.
+ *   Set-up: the first call on each device, made with that device current,
+ *     takes the array's address and zeroes it on "stream" (an error there is
+ *     OSCAR_ERR_CUDA).  Make that first call before capturing any stream.
+ *     The ticket words must be zero when a call starts: set-up zeroes them
+ *     and every call leaves them zero again.
+ *   Overlap: the array is shared by every cache on the device; two calls
+ *     that overlap on the GPU (other streams, other caches) race. */
+oscar_status oscar_decode_attention_noalloc(oscar_cache* cache, int32_t layer, int32_t n, const int32_t* reqs,
+                                            const uint16_t* q, float* out, void* stream);
+
 /* Synchronise "stream" and report the sticky device error word (then clear it). */
 oscar_status oscar_cache_check(oscar_cache* cache, void* stream);
 
