@@ -333,7 +333,7 @@ def run_gpu(args, log):
     res = {
         "us_step": us_step, "kv_bytes_step": kv_bytes_step, "dec_avg_us": dec_avg, "app_avg_us": app_avg, "bytes_per_launch": bpl,
         "achieved_gbs": achieved, "peak": peak, "peak_kind": peak_kind, "e2e_us": e2e_us, "h2d": h2d, "d2h": d2h,
-        "clocks": clk.summary(), "launches": K * L * 2, "world": world, "rank": rank,
+        "clocks": clk.summary(), "launches": K * L * 4, "world": world, "rank": rank,
     }
     return wl, res
 
@@ -454,7 +454,7 @@ def main(argv=None):
     cpu = par = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu, par = cpu_baseline(wl, r, log)
-    traffic = committed_traffic("decode_kernel")
+    traffic = committed_traffic("decode_stream_kernel")
     kv_gbs = r["kv_bytes_step"] / (r["us_step"] * 1e-6) / 1e9
     line = {
         "metric": METRIC,
@@ -481,7 +481,7 @@ def main(argv=None):
         "decode_us_per_layer": r["dec_avg_us"],
         "append_us_per_layer": r["app_avg_us"],
         "demote_tok_s": wl.batch * 1e6 / r["app_avg_us"],
-        "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": r["achieved_gbs"], "peak": r["peak"],
+        "roofline": {"bound": "hbm", "kernel": "decode_stream_kernel", "achieved": r["achieved_gbs"], "peak": r["peak"],
                      "unit": "GB/s", "frac": r["achieved_gbs"] / r["peak"], "peak_source": r["peak_kind"],
                      "traffic": traffic, "algorithmic_bytes_per_launch": r["bytes_per_launch"]},
         "e2e": {"value": r["e2e_us"], "unit": "us/step", "h2d_bytes_per_step": r["h2d"],

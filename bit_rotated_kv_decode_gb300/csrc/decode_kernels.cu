@@ -7,9 +7,22 @@
 // "Together AI Open-Sources OSCAR" (MarkTechPost), section "The Serving
 // System": the value path is inverse-rotated.
 //
-// One launch per layer.  Work items per (request, kv head):
-//   items 0..4   BF16 sink page and the four recent-ring pages, unrotated q;
-//   items 5..    chunks of INT2 history pages in the rotated basis.
+// Three launches per layer (and per 64 requests), chained on the stream with
+// programmatic dependent launch so each one is resident and has issued its
+// independent loads before its producer finishes:
+//   1. rotate_q   q_rot = q R_K for every query head, written to the workspace
+//                 as the fp16 hi / lo tensor-core operands of step 2;
+//   2. stream     work items per (request, kv head):
+//                   items 0..4  BF16 sink page and the four recent-ring pages,
+//                               unrotated q;
+//                   items 5..   chunks of INT2 history pages, rotated basis;
+//                 each writes an (o[128], m, l) partial per query head
+//                 (log2-domain max m).  Page ids and the first page copies are
+//                 issued before q_rot is waited for;
+//   3. merge      one block per query head: online-softmax merge of the
+//                 partials, R_V^T applied to the history part,
+//                 out = (O_bf16 + O_hist R_V^T) / L.  R_V^T is loaded before
+//                 the partials are waited for.
 // For an INT2 token j with codes c_j and fp16 scale / zero (s_j, z_j):
 //   logit_j = scale * (s_j (q_rot . c_j) + z_j sum(q_rot)),
 //   value   = s_j c_j + z_j 1   (accumulated as p_j s_j c_j plus sum p_j z_j).
@@ -25,10 +38,6 @@
 // Pages are staged HBM -> shared memory by TMA bulk copies (cp.async.bulk, one
 // 4608-byte record per page and kv head) into a per-warp ring, completion on
 // mbarriers; every wait is bounded and reports ERR_TIMEOUT instead of hanging.
-// Each item writes an (o[128], m, l) partial per query head (log2-domain max m).
-// The last item of a (request, kv head) to finish -- an atomic ticket, no
-// waiting -- merges the partials, applies R_V^T to the history part and writes
-// out = (O_bf16 + O_hist R_V^T) / L.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -39,10 +48,10 @@ namespace {
 
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr int PART = PARTIAL_FLOATS;
-constexpr int WARPS = 4;                 // warps per CTA
+constexpr int WARPS = 4;                 // warps per stream block
 constexpr int THREADS = 32 * WARPS;
-// TMA ring depth per warp and resident CTAs per SM: GQA <= 4 trades a stage for
-// a fourth resident CTA (16 warps per SM); GQA 8 keeps three stages
+constexpr int MERGE_THREADS = 512;
+// TMA ring depth per warp and resident stream blocks per SM
 template <int G> struct Tune {
   static constexpr int STAGES = G <= 4 ? 2 : 3;
   static constexpr int CTAS = G <= 4 ? 4 : 3;
@@ -54,13 +63,17 @@ constexpr int ERR_TIMEOUT_BIT = 8;
 struct DecodeArgs {
   int n;
   int pages_per_chunk;
-  int int2_items;            // INT2 CTAs, before the BF16 CTAs
-  int group_stride;          // group partial slots per (request, kv head)
+  int int2_items;            // INT2 blocks, before the BF16 blocks
   DecodeReq r[DECODE_PER_LAUNCH];
 };
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Programmatic dependent launch: wait for the preceding grid (complete, its
+// writes visible); allow the next grid to be scheduled.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -110,14 +123,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 
 // Pair of 2-bit codes m of each 16-bit half of w (m = 0..7) as an fp16x2 of
 // subnormals code * 2^(2 e(m) - 24), e(m) = m for m <= 4, m - 5 otherwise.
-template <int M>
-__device__ __forceinline__ uint32_t code_pair(uint32_t w) {
-  if constexpr (M <= 4) {
-    return w & (0x00030003u << (2 * M));
-  } else {
-    return (w >> 10) & (0x00030003u << (2 * (M - 5)));
-  }
-}
 __device__ __forceinline__ uint32_t code_pair_rt(uint32_t w, int m) {
   return m <= 4 ? (w & (0x00030003u << (2 * m))) : ((w >> 10) & (0x00030003u << (2 * (m - 5))));
 }
@@ -134,6 +139,8 @@ __device__ __forceinline__ void split_half(float x, float& hi, float& lo) {
   lo = x - hi;
 }
 
+constexpr int WH_STRIDE = PAGE + 8;   // halves per weight row (bank spread)
+
 template <int G>
 struct Smem {
   // INT2: per-warp TMA rings; BF16 items: the page's K rows (16-byte chunks
@@ -147,132 +154,132 @@ struct Smem {
     float state[WARPS][G][PART];
   } buf;
   __align__(8) uint64_t bar[WARPS][Tune<G>::STAGES];
-  float qin[G][D];           // q of the group's query heads (unrotated)
-  float q[G][D];             // q_rot (INT2 chunks); merge scratch
-  float qsum[G];             // sum of q_rot over channels
-  float qscale[G];           // power-of-two prescale of q_rot into fp16 range
-  __align__(16) float pw[WARPS][G][PAGE];  // p * s_v of the current page, per warp
-  float red[WARPS][G];
-  float cred[DECODE_CLUSTER][G][2];   // per-CTA partial sums / maxima of q_rot
-  int ticket;
+  float q[G][D];             // q of the group (BF16 items)
+  union {
+    __align__(16) float pw[WARPS][G][PAGE];              // BF16 items: logits / weights
+    __align__(16) uint16_t wh[WARPS][G][2][WH_STRIDE];   // INT2: p s_v 2^ew as fp16 hi, lo
+  } ws;
 };
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Store to the same shared-memory variable in CTA `rank` of this cluster.
-__device__ __forceinline__ void st_cluster(float* local, uint32_t rank, float v) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
-}
-
-// Execution-only cluster barrier: every CTA of the cluster has started (no
-// memory ordering, so outstanding loads are not waited for).
-__device__ __forceinline__ void cluster_sync_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// q_rot = q R_K for the G query heads, computed by the DECODE_CLUSTER CTAs of
-// one (request, kv head) together: CTA r of the cluster computes channels
-// 32 r .. 32 r + 31 (thread (group g, lane l): rows 32 g .. 32 g + 31 of column
-// 32 r + l, 32 independent loads of R_K) and stores them into every CTA's
-// sm.q through distributed shared memory, with its partial per-head sums and
-// maxima; a cluster barrier publishes them.  Leaves sm.q, sm.qsum and the
-// power-of-two prescale sm.qscale (|q_rot| 2^24 prescale <= 2^15).
-// q of the group (G x 128 bf16) into sm.qin, every load in flight at once.
+// ---- 1. q_rot = q R_K, delivered as tensor-core operands --------------------------
+// Per (request, kv head) the workspace holds QFrag<G>::WORDS 32-bit words:
+//   frag[lane][nt][s][r]  fp16x2 B operands of the q_rot . c contraction
+//                         (n-tile nt of (head, hi / lo part) columns, k-step s,
+//                         register r), prescaled by qscale(h) 2^(24 - 2 e(m)) so
+//                         that the fp32 accumulator holds qscale(h) q_rot . c;
+//   kscale[8], kzero[8]   fp32 per query head h of the group:
+//                         logit (log2 domain) = kscale[h] s_k acc + kzero[h] z_k,
+//                         kscale = scale log2(e) / qscale(h),
+//                         kzero  = scale log2(e) sum_c q_rot[h][c].
+// Register r of k-step s for lane (gid, tid) pairs channel 32 tid + 16 (s >> 2) + m
+// (low half) with that channel + 8 (high half), m = 2 (s & 3) + r, as the code
+// registers of the A operand do.
 template <int G>
-__device__ __forceinline__ void load_q(const uint16_t* qrow, Smem<G>& sm) {
-  const int t = threadIdx.x;
-  uint16_t qv[G * D / THREADS];
-#pragma unroll
-  for (int u = 0; u < G * D / THREADS; ++u) qv[u] = qrow[u * THREADS + t];
-#pragma unroll
-  for (int u = 0; u < G * D / THREADS; ++u) {
-    const int i = u * THREADS + t;
-    sm.qin[i / D][i % D] = __uint_as_float(static_cast<uint32_t>(qv[u]) << 16);
-  }
-}
-
-// This CTA's slab of R_K (column 32 rank + lane, rows 32 grp .. 32 grp + 31), loaded
-// before the page copies are queued so it is not served behind them.
-__device__ __forceinline__ void load_rk_slab(const DevCache& c, size_t lh, float (&r)[32]) {
-  const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
-  const float* __restrict__ RK = c.rot_k + lh * D * D + 32 * cluster_rank() + lane;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) r[i] = __ldg(RK + (size_t)(32 * grp + i) * D);
-}
+struct QFrag {
+  static constexpr int NT = (G + 3) / 4;
+  static constexpr int REGS = NT * 16;              // fragment registers per lane
+  static constexpr int WORDS = 32 * REGS + 16;      // + kscale[8], kzero[8]
+};
+constexpr int ROT_THREADS = 512;
 
 template <int G>
-__device__ __forceinline__ void cluster_rotate_q(const float (&r)[32], Smem<G>& sm) {
-  static_assert(DECODE_CLUSTER * 32 == D, "one 32-channel slab per cluster CTA");
-  const int t = threadIdx.x, lane = t & 31, grp = t >> 5;
-  const uint32_t rank = cluster_rank();
-  cluster_sync_relaxed();   // every CTA of the cluster runs before any remote store
-  float acc[G];
+__global__ void __launch_bounds__(ROT_THREADS) rotate_q_kernel(DevCache c, int layer, DecodeArgs a,
+                                                               const uint16_t* __restrict__ q,
+                                                               uint32_t* __restrict__ qfrag) {
+  __shared__ float qs[G][D];
+  __shared__ float red[4][G][D];
+  __shared__ float qscale[G];
+  const int ri = blockIdx.x / c.Hkv, head = blockIdx.x % c.Hkv;
+  const int t = threadIdx.x, ch = t & (D - 1), rg = t >> 7;   // column, group of 32 rows
+  const int warp = t >> 5, lane = t & 31;
+  // the preceding grid (whatever wrote q or the cache) is complete before the next
+  // grid of this decode may start
+  grid_dep_wait();
+  grid_dep_launch();
+  const float* __restrict__ RK = c.rot_k + ((size_t)layer * c.Hkv + head) * D * D + ch;
+  float r[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) r[i] = __ldg(RK + (size_t)(32 * rg + i) * D);
+  const uint16_t* qrow = q + ((size_t)a.r[ri].batch_row * c.Hq + (size_t)head * G) * D;
+  for (int idx = t; idx < G * D; idx += ROT_THREADS)
+    qs[idx / D][idx % D] = __uint_as_float(static_cast<uint32_t>(__ldcg(qrow + idx)) << 16);
+  __syncthreads();
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    acc[h] = 0.0f;
+    float acc = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) acc[h] = fmaf(sm.qin[h][32 * grp + i], r[i], acc[h]);
-    sm.pw[grp][h][lane] = acc[h];
+    for (int i = 0; i < 32; ++i) acc = fmaf(qs[h][32 * rg + i], r[i], acc);
+    red[rg][h][ch] = acc;
   }
   __syncthreads();
-  for (int idx = t; idx < G * 32; idx += THREADS) {
-    const int h = idx >> 5, l = idx & 31;
-    float v = 0.0f;
-#pragma unroll
-    for (int g2 = 0; g2 < WARPS; ++g2) v += sm.pw[g2][h][l];
-#pragma unroll
-    for (uint32_t dst = 0; dst < DECODE_CLUSTER; ++dst) st_cluster(&sm.q[h][32 * rank + l], dst, v);
-    float sum = v, mx = fabsf(v);
+  for (int idx = t; idx < G * D; idx += ROT_THREADS) {
+    const int h = idx / D, cc = idx % D;
+    red[0][h][cc] = (red[0][h][cc] + red[1][h][cc]) + (red[2][h][cc] + red[3][h][cc]);
+  }
+  __syncthreads();
+  uint32_t* dst = qfrag + (size_t)blockIdx.x * QFrag<G>::WORDS;
+  float* consts = reinterpret_cast<float*>(dst + 32 * QFrag<G>::REGS);
+  if (warp < G) {
+    const float4 x = *reinterpret_cast<const float4*>(&red[0][warp][4 * lane]);
+    float sum = (x.x + x.y) + (x.z + x.w);
+    float mx = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       sum += __shfl_xor_sync(0xffffffffu, sum, o);
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     }
-    if (l == 0) {
-#pragma unroll
-      for (uint32_t dst = 0; dst < DECODE_CLUSTER; ++dst) {
-        st_cluster(&sm.cred[rank][h][0], dst, sum);
-        st_cluster(&sm.cred[rank][h][1], dst, mx);
-      }
+    if (lane == 0) {
+      // |q_rot| qscale 2^24 <= 2^15: the fp16 operands stay finite
+      int e = 0;
+      if (mx > 0.0f) e = static_cast<int>(floorf(log2f(32768.0f / mx))) - 24;
+      e = max(-60, min(e, 60));
+      qscale[warp] = ldexpf(1.0f, e);
+      const float scale2 = c.scale * LOG2E;
+      consts[warp] = ldexpf(scale2, -e);
+      consts[8 + warp] = scale2 * sum;
     }
-  }
-  cluster_sync();
-  if (t < G) {
-    float sum = 0.0f, mx = 0.0f;
-#pragma unroll
-    for (int k = 0; k < DECODE_CLUSTER; ++k) {
-      sum += sm.cred[k][t][0];
-      mx = fmaxf(mx, sm.cred[k][t][1]);
-    }
-    int e = 0;
-    if (mx > 0.0f) e = static_cast<int>(floorf(log2f(32768.0f / mx))) - 24;
-    e = max(-60, min(e, 60));
-    sm.qsum[t] = sum;
-    sm.qscale[t] = ldexpf(1.0f, e);
+  } else if (warp < 8 && lane == 0) {
+    consts[warp] = 0.0f;
+    consts[8 + warp] = 0.0f;
   }
   __syncthreads();
+  for (int wi = t; wi < 32 * QFrag<G>::REGS; wi += ROT_THREADS) {
+    const int ln = wi / QFrag<G>::REGS, k = wi % QFrag<G>::REGS;
+    const int nt = k >> 4, s = (k >> 1) & 7, rr = k & 1;
+    const int gid = ln >> 2, tid = ln & 3;
+    const int h = 4 * nt + (gid >> 1);
+    uint32_t word = 0u;
+    if (h < G) {
+      const int m = 2 * (s & 3) + rr;
+      const int cha = 32 * tid + 16 * (s >> 2) + m;
+      const float f = ldexpf(qscale[h], 24 - 2 * code_exp(m));
+      float ha, la, hb, lb;
+      split_half(red[0][h][cha] * f, ha, la);
+      split_half(red[0][h][cha + 8] * f, hb, lb);
+      word = (gid & 1) ? pack_half2(la, lb) : pack_half2(ha, hb);
+    }
+    dst[wi] = word;
+  }
 }
 
-// One chunk of INT2 history pages of one (request, kv head); leaves the CTA's
-// partial (rotated basis) for every query head of the group in part_out.
+// ---- 2. stream: INT2 chunks and BF16 pages ------------------------------------------
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// One chunk of INT2 history pages of one (request, kv head); qf points at the
+// (request, kv head)'s q operands.  Leaves the block's partial (rotated basis)
+// for every query head of the group in part_out.
 template <int G>
 __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const DecodeReq& R, int head, int chunk,
-                                           int ppc, const uint16_t* qrow, Smem<G>& sm, float* part_out) {
-  constexpr int NT = (G + 3) / 4;       // n-tiles of 8 columns = 4 heads x (hi, lo)
+                                           int ppc, const uint32_t* __restrict__ qf, Smem<G>& sm,
+                                           float* part_out) {
+  constexpr int NT = QFrag<G>::NT;       // n-tiles of 8 columns = 4 heads x (hi, lo)
   constexpr int STAGES = Tune<G>::STAGES;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tid = lane & 3;
-  const float scale2 = c.scale * LOG2E;
   const int nhist = R.hist_end - SINK;
   const int npages = (nhist + PAGE - 1) / PAGE;
   const int pc0 = chunk * ppc;
@@ -282,8 +289,7 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
   const uint8_t* base = c.int2 + layer * c.int2_layer_stride + (size_t)head * RECORD;
   const size_t pstride = (size_t)c.Hkv * RECORD;
   bool timed_out = false;
-  int issued = 0;
-  float rk_slab[32];   // copies issued by this warp (lane 0's count)
+  int issued = 0;   // copies issued by this warp (lane 0's count)
 
   // page ids of this warp's pages, read 32 at a time (lane l holds page 32 b + l of
   // batch b); page_src is called by the whole warp with increasing j
@@ -296,7 +302,7 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
       const int jj = 32 * b + lane;
       int32_t page = 0;
       if (jj < my_n) {
-        page = pt[pc0 + warp + WARPS * jj];
+        page = __ldcg(pt + pc0 + warp + WARPS * jj);
         if (page < 0 || page >= c.n_int2_pages) {
           atomicOr(c.err, ERR_INT2_PAGE);
           page = 0;
@@ -306,18 +312,15 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
     }
     return base + (size_t)__shfl_sync(0xffffffffu, batch_pages, j & 31) * pstride;
   };
-  // every global load the prologue needs, issued together before any page copy:
-  // the first batch of page ids, this CTA's R_K slab and q
-  (void)page_src(0);
-  load_rk_slab(c, (size_t)layer * c.Hkv + head, rk_slab);
-  load_q<G>(qrow, sm);
-  __syncthreads();
+  // the page copies do not depend on q_rot: queue the first STAGES of them, let the
+  // merge grid be scheduled, then wait for rotate_q
   if (lane == 0) {
 #pragma unroll
     for (int st = 0; st < STAGES; ++st) mbar_init(&sm.bar[warp][st], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
+  __syncwarp();
 #pragma unroll
   for (int j = 0; j < STAGES; ++j) {
     const uint8_t* src = page_src(j);
@@ -327,8 +330,6 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
       ++issued;
     }
   }
-  // the copies are in flight while the cluster rotates q
-  cluster_rotate_q<G>(rk_slab, sm);
   // weights p * s_v are prescaled by 2^ew so the smallest ones stay representable in
   // fp16: s_v <= fp16(2 tau_V / 3) and p <= 1, so p s_v 2^ew <= 2^15
   int ew;
@@ -337,37 +338,35 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
     ew = max(-60, min(60, static_cast<int>(floorf(log2f(32768.0f / smax)))));
   }
   const float wscale = ldexpf(1.0f, ew);
+  grid_dep_launch();
+  grid_dep_wait();
 
-  // B operands of q_rot . c: per n-tile, k-step s, two registers (hi or lo part)
+  // B operands of q_rot . c, and the per-head logit constants of this lane's head
   uint32_t bq[NT][8][2];
-  float invp[NT];
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(qf + (size_t)lane * QFrag<G>::REGS);
+    uint4 v[QFrag<G>::REGS / 4];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int h = 4 * nt + (gid >> 1);
-    const bool lo_part = gid & 1;
-    const bool hv = h < G;
-    const float p = hv ? sm.qscale[h] : 1.0f;
-    invp[nt] = (4 * nt + tid < G) ? 1.0f / sm.qscale[4 * nt + tid] : 0.0f;
+    for (int u = 0; u < QFrag<G>::REGS / 4; ++u) v[u] = __ldcg(src + u);
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const int ch0 = 32 * tid + 16 * (s >> 2) + 2 * (s & 3);
+    for (int u = 0; u < QFrag<G>::REGS / 4; ++u) {
+      const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int m = 2 * (s & 3) + r;
-        const int cha = ch0 + r;
-        const float f = ldexpf(p, 24 - 2 * code_exp(m));
-        float va = hv ? sm.q[h][cha] * f : 0.0f;
-        float vb = hv ? sm.q[h][cha + 8] * f : 0.0f;
-        float ha, la, hb, lb;
-        split_half(va, ha, la);
-        split_half(vb, hb, lb);
-        bq[nt][s][r] = lo_part ? pack_half2(la, lb) : pack_half2(ha, hb);
+      for (int e = 0; e < 4; ++e) {
+        const int k = 4 * u + e;
+        bq[k >> 4][(k >> 1) & 7][k & 1] = w4[e];
       }
     }
   }
-  float qs[NT];
+  float ks[NT], kz[NT];
+  {
+    const float* consts = reinterpret_cast<const float*>(qf + 32 * QFrag<G>::REGS);
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) qs[nt] = (4 * nt + tid < G) ? sm.qsum[4 * nt + tid] : 0.0f;
+    for (int nt = 0; nt < NT; ++nt) {
+      ks[nt] = __ldcg(consts + 4 * nt + tid);
+      kz[nt] = __ldcg(consts + 8 + 4 * nt + tid);
+    }
+  }
 
   float o[NT][8][4];
   float m_run[NT], l_run[NT], u_run[NT];
@@ -416,26 +415,30 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
         for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt][mt], a0, a1, a2, a3, bq[nt][s][0], bq[nt][s][1]);
       }
     }
-    // token meta of this lane's 8 tokens: 16 mt + gid + 8 rr
-    float lg[NT][8], sv[8], zv[8];
+    // token meta of this lane's 8 tokens: 16 mt + gid + 8 rr; a partial page (the
+    // last of the history) masks the rows past its end
+    float lg[NT][8], sw[8], zv[8];
+    const bool full = valid == PAGE;
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
+        const int i = 2 * mt + rr;
         const int tok = 16 * mt + gid + 8 * rr;
         const __half2 km = *reinterpret_cast<const __half2*>(rec + K_META_OFF + tok * META_BYTES);
         const __half2 vm = *reinterpret_cast<const __half2*>(rec + V_META_OFF + tok * META_BYTES);
-        const bool ok = tok < valid;
-        sv[2 * mt + rr] = ok ? __low2float(vm) : 0.0f;
-        zv[2 * mt + rr] = ok ? __high2float(vm) : 0.0f;
+        const bool ok = full || tok < valid;
+        sw[i] = ok ? __low2float(vm) * wscale : 0.0f;
+        zv[i] = ok ? __high2float(vm) : 0.0f;
         const float sk = __low2float(km), zk = __high2float(km);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const float d = (acc[nt][mt][2 * rr] + acc[nt][mt][2 * rr + 1]) * invp[nt];
-          lg[nt][2 * mt + rr] = (ok && 4 * nt + tid < G) ? scale2 * fmaf(sk, d, zk * qs[nt]) : -INFINITY;
+          const float v = fmaf(ks[nt] * sk, acc[nt][mt][2 * rr] + acc[nt][mt][2 * rr + 1], kz[nt] * zk);
+          lg[nt][i] = (ok && 4 * nt + tid < G) ? v : -INFINITY;
         }
       }
-    // ---- online softmax per head (lanes with equal tid share a head)
+    // ---- online softmax per head (lanes with equal tid share a head); the
+    // weights p s_v 2^ew go to shared memory as fp16 hi / lo halves
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       float pm = lg[nt][0];
@@ -446,7 +449,7 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
       pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
       const float m_new = fmaxf(m_run[nt], pm);
       if (m_new > m_run[nt]) {   // rescale only when the running max grows
-        const float corr = (m_run[nt] == -INFINITY) ? 0.0f : exp2f(m_run[nt] - m_new);
+        const float corr = ex2(m_run[nt] - m_new);
         m_run[nt] = m_new;
         l_run[nt] *= corr;
         u_run[nt] *= corr;
@@ -458,10 +461,16 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
       const int h = 4 * nt + tid;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float p = (lg[nt][i] == -INFINITY) ? 0.0f : exp2f(lg[nt][i] - m_new);
+        const float p = ex2(lg[nt][i] - m_new);
         l_run[nt] += p;
         u_run[nt] = fmaf(p, zv[i], u_run[nt]);
-        if (h < G) sm.pw[warp][h][16 * (i >> 1) + gid + 8 * (i & 1)] = p * sv[i] * wscale;
+        if (h < G) {
+          float hi, lo;
+          split_half(p * sw[i], hi, lo);
+          const int tok = 16 * (i >> 1) + gid + 8 * (i & 1);
+          sm.ws.wh[warp][h][0][tok] = __half_as_ushort(__float2half_rn(hi));
+          sm.ws.wh[warp][h][1][tok] = __half_as_ushort(__float2half_rn(lo));
+        }
       }
     }
     __syncwarp();
@@ -474,15 +483,9 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
       for (int nt = 0; nt < NT; ++nt) {
         const int h = 4 * nt + (gid >> 1);
         if (h < G) {
-          const float2 w01 = *reinterpret_cast<const float2*>(&sm.pw[warp][h][ta]);
-          const float2 w89 = *reinterpret_cast<const float2*>(&sm.pw[warp][h][ta + 8]);
-          float h0, l0, h1, l1, h8, l8, h9, l9;
-          split_half(w01.x, h0, l0);
-          split_half(w01.y, h1, l1);
-          split_half(w89.x, h8, l8);
-          split_half(w89.y, h9, l9);
-          bw[nt][0] = (gid & 1) ? pack_half2(l0, l1) : pack_half2(h0, h1);
-          bw[nt][1] = (gid & 1) ? pack_half2(l8, l9) : pack_half2(h8, h9);
+          const uint16_t* row = sm.ws.wh[warp][h][gid & 1];
+          bw[nt][0] = *reinterpret_cast<const uint32_t*>(row + ta);
+          bw[nt][1] = *reinterpret_cast<const uint32_t*>(row + ta + 8);
         } else {
           bw[nt][0] = bw[nt][1] = 0u;
         }
@@ -598,8 +601,8 @@ __device__ __forceinline__ void bf16_item(const DevCache& c, int layer, const De
 #pragma unroll
   for (int it = 0; it < LOADS; ++it) {
     const int idx = t + THREADS * it, r = idx / (D / 8), part = idx % (D / 8);
-    kk[it] = reinterpret_cast<const uint4*>(src + (size_t)r * D)[part];
-    vv[it] = reinterpret_cast<const uint4*>(src + (size_t)(PAGE + r) * D)[part];
+    kk[it] = __ldcg(reinterpret_cast<const uint4*>(src + (size_t)r * D) + part);
+    vv[it] = __ldcg(reinterpret_cast<const uint4*>(src + (size_t)(PAGE + r) * D) + part);
   }
 #pragma unroll
   for (int it = 0; it < LOADS; ++it) {
@@ -625,20 +628,20 @@ __device__ __forceinline__ void bf16_item(const DevCache& c, int layer, const De
         const float k0 = bf16lo(ww[e]), k1 = bf16hi(ww[e]);
         const int ch = 8 * chunk + 2 * e;
 #pragma unroll
-        for (int h = 0; h < G; ++h) acc[h] = fmaf(sm.qin[h][ch + 1], k1, fmaf(sm.qin[h][ch], k0, acc[h]));
+        for (int h = 0; h < G; ++h) acc[h] = fmaf(sm.q[h][ch + 1], k1, fmaf(sm.q[h][ch], k0, acc[h]));
       }
     }
     const bool ok = row_valid(r);
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], 1);
-      if (half == 0) sm.pw[0][h][r] = ok ? acc[h] * scale2 : -INFINITY;
+      if (half == 0) sm.ws.pw[0][h][r] = ok ? acc[h] * scale2 : -INFINITY;
     }
   }
   __syncthreads();
   // softmax and values: warp w handles heads w, w + 4; lane owns channels 4 lane .. 4 lane + 3
   for (int h = warp; h < G; h += WARPS) {
-    const float x0 = sm.pw[0][h][lane], x1 = sm.pw[0][h][lane + 32];
+    const float x0 = sm.ws.pw[0][h][lane], x1 = sm.ws.pw[0][h][lane + 32];
     float m = fmaxf(x0, x1);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -648,13 +651,13 @@ __device__ __forceinline__ void bf16_item(const DevCache& c, int layer, const De
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
     __syncwarp();
-    sm.pw[0][h][lane] = p0;
-    sm.pw[0][h][lane + 32] = p1;
+    sm.ws.pw[0][h][lane] = p0;
+    sm.ws.pw[0][h][lane + 32] = p1;
     __syncwarp();
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     if (m != -INFINITY) {
       for (int r = 0; r < PAGE; ++r) {
-        const float p = sm.pw[0][h][r];
+        const float p = sm.ws.pw[0][h][r];
         const uint2 vv = reinterpret_cast<const uint2*>(&sm.buf.bf.v[r][0])[lane];
         acc[0] = fmaf(p, bf16lo(vv.x), acc[0]);
         acc[1] = fmaf(p, bf16hi(vv.x), acc[1]);
@@ -670,253 +673,225 @@ __device__ __forceinline__ void bf16_item(const DevCache& c, int layer, const De
   }
 }
 
-// Online-softmax merge of `count` (<= MERGE_GROUP) consecutive partials
-// (stride G * PART floats) into one.  The (m, l) pairs are loaded by
-// different threads at once; then thread t owns channel t of every head and
-// issues all of its count * G loads before using them.
+// Work items: INT2 chunks first ((request, kv head) major, chunk minor), then the
+// BF16 pages ((request, kv head) major, item minor).  Partial slot of item k of
+// (request i, kv head h): part_start(i) + h * (5 + chunks(i)) + k, k < 5 the BF16
+// items, k >= 5 the chunks.
 template <int G>
-__device__ __forceinline__ void merge_partials(const float* src, int count, float* dst, Smem<G>& sm) {
-  const int t = threadIdx.x;
-  if (t < count * G) {
-    const int k = t / G, h = t % G;
-    sm.pw[0][h][k] = __ldcg(src + ((size_t)k * G + h) * PART + PARTIAL_M);
-    sm.pw[0][h][MERGE_GROUP + k] = __ldcg(src + ((size_t)k * G + h) * PART + PARTIAL_L);
-  }
-  float ov[MERGE_GROUP][G];
-#pragma unroll
-  for (int k = 0; k < MERGE_GROUP; ++k)
-#pragma unroll
-    for (int h = 0; h < G; ++h) ov[k][h] = k < count ? __ldcg(src + ((size_t)k * G + h) * PART + t) : 0.0f;
-  __syncthreads();
-  if (t < G) {
-    float M = -INFINITY;
-    for (int k = 0; k < count; ++k) M = fmaxf(M, sm.pw[0][t][k]);
-    float L = 0.0f;
-    for (int k = 0; k < count; ++k) {
-      const float mk = sm.pw[0][t][k];
-      const float f = (mk == -INFINITY) ? 0.0f : exp2f(mk - M);
-      sm.pw[0][t][2 * MERGE_GROUP + k] = f;
-      L = fmaf(sm.pw[0][t][MERGE_GROUP + k], f, L);
-    }
-    dst[t * PART + PARTIAL_M] = M;
-    dst[t * PART + PARTIAL_L] = L;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    float o = 0.0f;
-#pragma unroll
-    for (int k = 0; k < MERGE_GROUP; ++k)
-      if (k < count) o = fmaf(ov[k][h], sm.pw[0][h][2 * MERGE_GROUP + k], o);
-    dst[h * PART + t] = o;
-  }
-}
-
-template <int G>
-__global__ void __launch_bounds__(THREADS, Tune<G>::CTAS) decode_kernel(DevCache c, int layer, DecodeArgs a,
-                                                         const uint16_t* __restrict__ q, float* __restrict__ out,
-                                                         int32_t* counters, float* partials, float* gpart) {
+__global__ void __launch_bounds__(THREADS, Tune<G>::CTAS) decode_stream_kernel(DevCache c, int layer, DecodeArgs a,
+                                                                         const uint16_t* __restrict__ q,
+                                                                         const uint32_t* __restrict__ qfrag,
+                                                                         float* __restrict__ partials) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem<G>& sm = *reinterpret_cast<Smem<G>*>(smem_raw);
   const int item = blockIdx.x;
   int ri = 0, head, sub;
   if (item < a.int2_items) {
-    // INT2 chunk: clusters of DECODE_CLUSTER consecutive CTAs share one (request, kv head)
     while (ri + 1 < a.n && a.r[ri + 1].int2_start <= item) ++ri;
     const int local = item - a.r[ri].int2_start;
     head = local / a.r[ri].chunks;
     sub = BF16_ITEMS + local % a.r[ri].chunks;
   } else {
     const int b = item - a.int2_items;
-    if (b >= a.n * c.Hkv * BF16_ITEMS) return;   // cluster padding
     ri = b / (c.Hkv * BF16_ITEMS);
     head = (b / BF16_ITEMS) % c.Hkv;
     sub = b % BF16_ITEMS;
   }
   const DecodeReq R = a.r[ri];
   const int per_head = BF16_ITEMS + R.chunks;
-  const int t = threadIdx.x;
-  const size_t lh = (size_t)layer * c.Hkv + head;
-  const float* __restrict__ RVt = c.rot_vt + lh * D * D;
-
-  if (sub == 0) {
-    // warm L2 with R_V^T for whichever item of this head merges last
-    for (int line = t; line < D * D / 32; line += THREADS)
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(RVt + (size_t)line * 32));
-  }
-  const uint16_t* qrow = q + ((size_t)R.batch_row * c.Hq + (size_t)head * G) * D;
+  float* part = partials + ((size_t)R.part_start + (size_t)head * per_head + sub) * G * PART;
   if (sub < BF16_ITEMS) {
-    load_q<G>(qrow, sm);
+    // BF16 pages read q and the cache only, both complete before rotate_q ran
+    grid_dep_launch();
+    const uint16_t* qrow = q + ((size_t)R.batch_row * c.Hq + (size_t)head * G) * D;
+    const int t = threadIdx.x;
+    uint16_t qv[G];
+#pragma unroll
+    for (int u = 0; u < G; ++u) qv[u] = __ldcg(qrow + u * D + t);
+#pragma unroll
+    for (int u = 0; u < G; ++u) sm.q[u][t] = __uint_as_float(static_cast<uint32_t>(qv[u]) << 16);
     __syncthreads();
-  }
-
-  const size_t head_parts = (size_t)R.part_start + (size_t)head * per_head;
-  float* part = partials + (head_parts + sub) * G * PART;
-  if (sub < BF16_ITEMS) {
     bf16_item<G>(c, layer, R, head, sub, sm, part);
   } else {
-    int2_chunk<G>(c, layer, R, head, sub - BF16_ITEMS, a.pages_per_chunk, qrow, sm, part);
+    int2_chunk<G>(c, layer, R, head, sub - BF16_ITEMS, a.pages_per_chunk,
+                  qfrag + ((size_t)ri * c.Hkv + head) * QFrag<G>::WORDS, sm, part);
   }
+}
 
-  // ---- two-level merge by atomic tickets (nobody waits) -----------------------------
-  // group 0 = the BF16 items, group g >= 1 = INT2 chunks (g-1)*MERGE_GROUP .. +MERGE_GROUP-1.
-  // Ticket protocol: block barrier, then one thread fences (cumulative over the
-  // block's writes) and takes the ticket; the winner fences before reading.
-  const int g = sub < BF16_ITEMS ? 0 : 1 + (sub - BF16_ITEMS) / MERGE_GROUP;
-  const int gfirst = g == 0 ? 0 : BF16_ITEMS + (g - 1) * MERGE_GROUP;
-  const int gcount = g == 0 ? BF16_ITEMS : min(MERGE_GROUP, R.chunks - (g - 1) * MERGE_GROUP);
-  const int ngroups = 1 + (R.chunks + MERGE_GROUP - 1) / MERGE_GROUP;
-  int32_t* cnt = counters + (size_t)(ri * c.Hkv + head) * MERGE_COUNTERS;
-  float* gbase = gpart + (size_t)(ri * c.Hkv + head) * a.group_stride * G * PART;
-  __syncthreads();
-  if (t == 0) {
-    __threadfence();
-    sm.ticket = atomicAdd(cnt + 1 + g, 1);
-    if (sm.ticket == gcount - 1) __threadfence();
-  }
-  __syncthreads();
-  if (sm.ticket != gcount - 1) return;
-  merge_partials<G>(partials + (head_parts + gfirst) * G * PART, gcount, gbase + (size_t)g * G * PART, sm);
-  __syncthreads();
-  if (t == 0) {
-    cnt[1 + g] = 0;
-    __threadfence();
-    sm.ticket = atomicAdd(cnt, 1);
-    if (sm.ticket == ngroups - 1) __threadfence();
-  }
-  __syncthreads();
-  if (sm.ticket != ngroups - 1) return;
+// ---- 3. merge -------------------------------------------------------------------------
+// One block per (request, query head).  Warp w folds items w, w + 8, ... into a
+// running (M, L, O_bf16, O_hist) with lane l owning channels 4 l .. 4 l + 3; the
+// eight warp states are combined, O_hist is rotated back by R_V^T (staged in
+// shared memory before the partials are waited for) and the output row written.
+constexpr int MERGE_WARPS = MERGE_THREADS / 32;
+constexpr int MERGE_UNROLL = 8;
+struct MergeSmem {
+  float rvt[D][D];                     // R_V^T of the kv head: rvt[j][c] = R_V[c][j]
+  __align__(16) float ob[MERGE_WARPS][D];
+  __align__(16) float oh[MERGE_WARPS][D];
+  float m[MERGE_WARPS], l[MERGE_WARPS];
+  float hist[D], bf[D], part[MERGE_THREADS / D][D];
+  float L;
+};
 
-  // ---- last group of this (request, kv head): BF16 part + R_V^T (history part) ----
-  // stage every group partial in shared memory with one round of 16-byte loads
-  float* gs = &sm.buf.state[0][0][0];   // [ngroups][G][PART], staged in chunks of STAGE_GROUPS
-  constexpr int STAGE_GROUPS = (WARPS * Tune<G>::STAGES * RECORD) / (G * PART * 4);
-  float* oh = &sm.pw[0][0][0];           // [G][D] history part (rotated basis)
-  float M[G], L[G], ob[G], ohist[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    M[h] = -INFINITY;
-    L[h] = 0.0f;
-    ob[h] = 0.0f;
-    ohist[h] = 0.0f;
-  }
-  for (int k0 = 0; k0 < ngroups; k0 += STAGE_GROUPS) {
-    const int kn = min(STAGE_GROUPS, ngroups - k0);
-    const int n4 = kn * G * PART / 4;
-    const float4* src4 = reinterpret_cast<const float4*>(gbase + (size_t)k0 * G * PART);
-    for (int i0 = 0; i0 < n4; i0 += 8 * THREADS) {
-      float4 v4[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = i0 + u * THREADS + t;
-        if (i < n4) v4[u] = __ldcg(src4 + i);
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = i0 + u * THREADS + t;
-        if (i < n4) reinterpret_cast<float4*>(gs)[i] = v4[u];
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float Mn = M[h];
-      for (int k = 0; k < kn; ++k) Mn = fmaxf(Mn, gs[(k * G + h) * PART + PARTIAL_M]);
-      const float fo = (M[h] == -INFINITY) ? 0.0f : exp2f(M[h] - Mn);
-      L[h] *= fo;
-      ob[h] *= fo;
-      ohist[h] *= fo;
-      M[h] = Mn;
-      for (int k = 0; k < kn; ++k) {
-        const float* pk = gs + (k * G + h) * PART;
-        const float mk = pk[PARTIAL_M];
-        const float f = (mk == -INFINITY) ? 0.0f : exp2f(mk - Mn);
-        L[h] = fmaf(pk[PARTIAL_L], f, L[h]);
-        if (k0 + k == 0)
-          ob[h] = fmaf(pk[t], f, ob[h]);
-        else
-          ohist[h] = fmaf(pk[t], f, ohist[h]);
-      }
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    oh[h * D + t] = ohist[h];
-    if (t == 0) sm.qsum[h] = L[h];
-    sm.q[h][t] = ob[h];
-  }
-  __syncthreads();
-  // out_c = (O_bf16_c + sum_j O_hist_j R_V[c][j]) / L with rot_vt[j][c] = R_V[c][j]:
-  // thread (group gr, lane l) sums rows 32 gr .. 32 gr + 31 for channels 4l .. 4l+3
+template <int G>
+__global__ void __launch_bounds__(MERGE_THREADS) decode_merge_kernel(DevCache c, int layer, DecodeArgs a,
+                                                                     const float* __restrict__ partials,
+                                                                     float* __restrict__ out) {
+  extern __shared__ __align__(16) uint8_t merge_raw[];
+  MergeSmem& sm = *reinterpret_cast<MergeSmem*>(merge_raw);
+  const int ri = blockIdx.x / c.Hq, hq = blockIdx.x % c.Hq;
+  const int head = hq / G, g = hq % G;
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   {
-    const int lane = t & 31, grp = t >> 5;
-    float4 acc[G];
+    // R_V^T is written once at set-up: stage it while the stream grid runs
+    const float4* src = reinterpret_cast<const float4*>(c.rot_vt + ((size_t)layer * c.Hkv + head) * D * D);
+    float4* dst = reinterpret_cast<float4*>(&sm.rvt[0][0]);
+    constexpr int N4 = D * D / 4 / MERGE_THREADS;
+    float4 v[N4];
 #pragma unroll
-    for (int h = 0; h < G; ++h) acc[h] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    constexpr int BATCH = G <= 4 ? 16 : 8;   // R_V rows in flight per thread
+    for (int u = 0; u < N4; ++u) v[u] = __ldg(src + u * MERGE_THREADS + t);
 #pragma unroll
-    for (int half = 0; half < 32 / BATCH; ++half) {
-      float4 r[BATCH];
+    for (int u = 0; u < N4; ++u) dst[u * MERGE_THREADS + t] = v[u];
+  }
+  grid_dep_wait();
+  const DecodeReq& R = a.r[ri];
+  const int per_head = BF16_ITEMS + R.chunks;
+  const float* base = partials + ((size_t)R.part_start + (size_t)head * per_head) * G * PART + (size_t)g * PART;
+  float M = -INFINITY, L = 0.0f;
+  float4 ob = make_float4(0.0f, 0.0f, 0.0f, 0.0f), oh = ob;
+  for (int i0 = w; i0 < per_head; i0 += MERGE_WARPS * MERGE_UNROLL) {
+    float mv[MERGE_UNROLL], lv[MERGE_UNROLL];
+    float4 ov[MERGE_UNROLL];
 #pragma unroll
-      for (int i = 0; i < BATCH; ++i)
-        r[i] = __ldg(reinterpret_cast<const float4*>(RVt + (size_t)(32 * grp + BATCH * half + i) * D) + lane);
-#pragma unroll
-      for (int i = 0; i < BATCH; ++i) {
-        const int j = 32 * grp + BATCH * half + i;
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float oj = oh[h * D + j];
-          acc[h].x = fmaf(oj, r[i].x, acc[h].x);
-          acc[h].y = fmaf(oj, r[i].y, acc[h].y);
-          acc[h].z = fmaf(oj, r[i].z, acc[h].z);
-          acc[h].w = fmaf(oj, r[i].w, acc[h].w);
-        }
+    for (int u = 0; u < MERGE_UNROLL; ++u) {
+      const int i = i0 + MERGE_WARPS * u;
+      if (i < per_head) {
+        const float* p = base + (size_t)i * G * PART;
+        mv[u] = __ldcg(p + PARTIAL_M);
+        lv[u] = __ldcg(p + PARTIAL_L);
+        ov[u] = __ldcg(reinterpret_cast<const float4*>(p) + lane);
+      } else {
+        mv[u] = -INFINITY;
+        lv[u] = 0.0f;
+        ov[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       }
     }
-    float* mp = &sm.buf.state[0][0][0];   // [4][G][D]
+    float mn = M;
 #pragma unroll
-    for (int h = 0; h < G; ++h) reinterpret_cast<float4*>(mp + ((size_t)grp * G + h) * D)[lane] = acc[h];
+    for (int u = 0; u < MERGE_UNROLL; ++u) mn = fmaxf(mn, mv[u]);
+    if (mn > M) {
+      const float f = (M == -INFINITY) ? 0.0f : exp2f(M - mn);
+      L *= f;
+      ob.x *= f; ob.y *= f; ob.z *= f; ob.w *= f;
+      oh.x *= f; oh.y *= f; oh.z *= f; oh.w *= f;
+      M = mn;
+    }
+#pragma unroll
+    for (int u = 0; u < MERGE_UNROLL; ++u) {
+      const float f = (mv[u] == -INFINITY) ? 0.0f : exp2f(mv[u] - M);
+      L = fmaf(lv[u], f, L);
+      const bool is_bf = i0 + MERGE_WARPS * u < BF16_ITEMS;
+      const float fb = is_bf ? f : 0.0f, fh = is_bf ? 0.0f : f;
+      ob.x = fmaf(ov[u].x, fb, ob.x);
+      ob.y = fmaf(ov[u].y, fb, ob.y);
+      ob.z = fmaf(ov[u].z, fb, ob.z);
+      ob.w = fmaf(ov[u].w, fb, ob.w);
+      oh.x = fmaf(ov[u].x, fh, oh.x);
+      oh.y = fmaf(ov[u].y, fh, oh.y);
+      oh.z = fmaf(ov[u].z, fh, oh.z);
+      oh.w = fmaf(ov[u].w, fh, oh.w);
+    }
+  }
+  reinterpret_cast<float4*>(sm.ob[w])[lane] = ob;
+  reinterpret_cast<float4*>(sm.oh[w])[lane] = oh;
+  if (lane == 0) {
+    sm.m[w] = M;
+    sm.l[w] = L;
+  }
+  __syncthreads();
+  if (t < D) {
+    float Mt = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < MERGE_WARPS; ++k) Mt = fmaxf(Mt, sm.m[k]);
+    float Lt = 0.0f, b = 0.0f, h = 0.0f;
+#pragma unroll
+    for (int k = 0; k < MERGE_WARPS; ++k) {
+      const float f = (sm.m[k] == -INFINITY) ? 0.0f : exp2f(sm.m[k] - Mt);
+      Lt = fmaf(sm.l[k], f, Lt);
+      b = fmaf(sm.ob[k][t], f, b);
+      h = fmaf(sm.oh[k][t], f, h);
+    }
+    sm.bf[t] = b;
+    sm.hist[t] = h;
+    if (t == 0) sm.L = Lt;
   }
   __syncthreads();
   {
-    const float* mp = &sm.buf.state[0][0][0];
+    // out_c = O_bf16_c + sum_j O_hist_j R_V^T[j][c]; thread (quarter q, c) sums rows
+    // 32 q .. 32 q + 31
+    constexpr int ROWS = D * D / MERGE_THREADS;
+    const int ch = t & (D - 1), qr = t / D;
+    float acc = 0.0f;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float v = sm.q[h][t];
-#pragma unroll
-      for (int g2 = 0; g2 < WARPS; ++g2) v += mp[((size_t)g2 * G + h) * D + t];
-      out[((size_t)R.batch_row * c.Hq + (size_t)head * G + h) * D + t] = v / sm.qsum[h];
-    }
+    for (int j = ROWS * qr; j < ROWS * qr + ROWS; ++j) acc = fmaf(sm.hist[j], sm.rvt[j][ch], acc);
+    sm.part[qr][ch] = acc;
   }
-  if (t == 0) cnt[0] = 0;
+  __syncthreads();
+  if (t < D) {
+    float v = 0.0f;
+#pragma unroll
+    for (int k = 0; k < MERGE_THREADS / D; ++k) v += sm.part[k][t];
+    out[((size_t)R.batch_row * c.Hq + hq) * D + t] = (sm.bf[t] + v) / sm.L;
+  }
+}
+
+// Dynamic shared memory opt-in, once per device and kernel.
+template <typename K>
+cudaError_t set_smem(K kernel, size_t bytes, unsigned& done_mask) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned bit = 1u << (dev & 31);
+  if (dev < 32 && (done_mask & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess && dev < 32) done_mask |= bit;
+  return e;
 }
 
 template <int G>
 cudaError_t launch_g(const DevCache& c, int layer, const DecodeArgs& a, int items, const uint16_t* q, float* out,
-                     int32_t* counters, float* partials, float* gpart, cudaStream_t s) {
-  static bool attr = false;
+                     uint32_t* qfrag, float* partials, cudaStream_t s) {
+  static unsigned stream_set = 0, merge_set = 0;
   const size_t smem = sizeof(Smem<G>);
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_kernel<G>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  cudaError_t e = set_smem(decode_stream_kernel<G>, smem, stream_set);
+  if (e == cudaSuccess) e = set_smem(decode_merge_kernel<G>, sizeof(MergeSmem), merge_set);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
+  cfg.stream = s;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+
+  cfg.gridDim = dim3(static_cast<unsigned>(a.n * c.Hkv));
+  cfg.blockDim = dim3(ROT_THREADS);
+  cfg.dynamicSmemBytes = 0;
+  e = cudaLaunchKernelEx(&cfg, rotate_q_kernel<G>, c, layer, a, q, qfrag);
+  if (e != cudaSuccess) return e;
+
   cfg.gridDim = dim3(static_cast<unsigned>(items));
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = DECODE_CLUSTER;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<G>, c, layer, a, q, out, counters, partials, gpart);
+  e = cudaLaunchKernelEx(&cfg, decode_stream_kernel<G>, c, layer, a, q, static_cast<const uint32_t*>(qfrag),
+                         partials);
+  if (e != cudaSuccess) return e;
+
+  cfg.gridDim = dim3(static_cast<unsigned>(a.n * c.Hq));
+  cfg.blockDim = dim3(MERGE_THREADS);
+  cfg.dynamicSmemBytes = sizeof(MergeSmem);
+  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<G>, c, layer, a, static_cast<const float*>(partials), out);
 }
 
 }  // namespace
@@ -926,23 +901,23 @@ cudaError_t launch_decode(const DevCache& c, int layer, const DecodeReq* reqs, c
   DecodeArgs a;
   a.n = plan.n;
   a.pages_per_chunk = plan.pages_per_chunk;
-  a.group_stride = plan.group_stride;
   a.int2_items = plan.int2_items;
   for (int i = 0; i < plan.n; ++i) a.r[i] = reqs[i];
-  int32_t* counters = static_cast<int32_t*>(workspace);
-  float* partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.counter_bytes);
-  float* gpart = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.counter_bytes + plan.partial_bytes);
+  uint32_t* qfrag = static_cast<uint32_t*>(workspace);
+  float* partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.qrot_bytes);
   switch (c.G) {
-    case 1: return launch_g<1>(c, layer, a, plan.total_items, q, out, counters, partials, gpart, s);
-    case 2: return launch_g<2>(c, layer, a, plan.total_items, q, out, counters, partials, gpart, s);
-    case 4: return launch_g<4>(c, layer, a, plan.total_items, q, out, counters, partials, gpart, s);
-    case 8: return launch_g<8>(c, layer, a, plan.total_items, q, out, counters, partials, gpart, s);
+    case 1: return launch_g<1>(c, layer, a, plan.total_items, q, out, qfrag, partials, s);
+    case 2: return launch_g<2>(c, layer, a, plan.total_items, q, out, qfrag, partials, s);
+    case 4: return launch_g<4>(c, layer, a, plan.total_items, q, out, qfrag, partials, s);
+    case 8: return launch_g<8>(c, layer, a, plan.total_items, q, out, qfrag, partials, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
-}  // namespace oscar
-
-namespace oscar {
 int decode_ctas_per_sm(int g) { return g <= 4 ? Tune<4>::CTAS : Tune<8>::CTAS; }
+
+size_t decode_qfrag_bytes(int g) {
+  return (g <= 4 ? QFrag<4>::WORDS : QFrag<8>::WORDS) * sizeof(uint32_t);
+}
+
 }  // namespace oscar

@@ -1,19 +1,19 @@
-// Fixed, statically allocated decode scratch for oscar_decode_attention_noalloc.
+// Fixed, statically allocated decode scratch for oscar_decode_attention_noalloc:
+// q_rot and the partials of the decode kernels.
 //
 // Some callers cannot allocate device memory around a decode step: a serving
 // engine that hands all free HBM to its KV pools at start-up and owns no
 // allocator it may call per step, or a plain C host that has no allocator to
-// pass at all.  For them the merge tickets and partials of the decode kernel
+// pass at all.  For them q_rot and the partials of the decode kernels
 // live in one file-scope device array, loaded with the module, instead of a
 // caller-owned workspace.  Nothing here calls cudaMalloc, cudaFree or any
 // library routine that allocates.
 //
 // The array is one per device.  Set-up, once per device with that device
 // current, takes its address with cudaGetSymbolAddress and zeroes it on the
-// caller's stream; from then on every completed decode returns its ticket
-// words to zero, so the tickets stay zero between calls.  Partials need no
-// initial value.  Two calls that use the array at the same time on one
-// device -- on different streams, or from different caches -- race.
+// caller's stream (the decode itself needs no initial contents).  Two calls
+// that use the array at the same time on one device -- on different streams,
+// or from different caches -- race.
 #include <mutex>
 
 #include "internal.h"

@@ -493,13 +493,9 @@ oscar_status write_batch(oscar_cache* c, int32_t layer, int32_t n, const int32_t
 
 // Work split of one decode launch over reqs[0..n), n <= DECODE_PER_LAUNCH.
 // Per (request, kv head): five BF16 items (sink page, four ring pages) and
-// a multiple of DECODE_CLUSTER INT2 chunks of pages_per_chunk pages, sized so
-// the launch is about one wave of resident CTAs.
-int64_t chunks_for(int64_t np, int64_t ppc) {
-  if (np == 0) return 0;
-  const int64_t c = (np + ppc - 1) / ppc;
-  return (c + DECODE_CLUSTER - 1) / DECODE_CLUSTER * DECODE_CLUSTER;
-}
+// INT2 chunks of pages_per_chunk pages, sized so the stream launch is about one
+// wave of resident blocks.
+int64_t chunks_for(int64_t np, int64_t ppc) { return np == 0 ? 0 : (np + ppc - 1) / ppc; }
 
 DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int32_t* reqs, int32_t first_row,
                        int64_t ppc_min, DecodeReq* out) {
@@ -511,11 +507,10 @@ DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int
     max_np = std::max(max_np, np);
   }
   const int64_t target = std::max<int64_t>(1, (int64_t)c->num_sms * decode_ctas_per_sm(c->G()));
-  const int64_t bf16 = ((int64_t)DECODE_BF16_ITEMS * n * H + DECODE_CLUSTER - 1) / DECODE_CLUSTER * DECODE_CLUSTER;
+  const int64_t bf16 = (int64_t)DECODE_BF16_ITEMS * n * H;
   const int64_t budget = std::max<int64_t>(n * H, target - bf16);
   int64_t ppc = std::max<int64_t>({ppc_min, 2, (total_pages + budget - 1) / budget,
                                    (max_np + MAX_CHUNKS_PER_HEAD - 1) / MAX_CHUNKS_PER_HEAD});
-  // chunk counts are rounded up to whole clusters: grow ppc until the launch fits the budget
   for (;;) {
     int64_t items = 0;
     for (int32_t i = 0; i < n; ++i) items += H * chunks_for(pages_for(c->reqs[reqs[i]].he[layer]), ppc);
@@ -525,7 +520,7 @@ DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int
   DecodePlan p{};
   p.n = n;
   p.pages_per_chunk = static_cast<int>(std::min<int64_t>(ppc, INT32_MAX));
-  int64_t int2 = 0, parts = 0, groups = 1;
+  int64_t int2 = 0, parts = 0;
   for (int32_t i = 0; i < n; ++i) {
     const Request& r = c->reqs[reqs[i]];
     const int64_t chunks = chunks_for(pages_for(r.he[layer]), ppc);
@@ -543,14 +538,11 @@ DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int
     }
     int2 += H * chunks;
     parts += H * (DECODE_BF16_ITEMS + chunks);
-    groups = std::max<int64_t>(groups, 1 + (chunks + MERGE_GROUP - 1) / MERGE_GROUP);
   }
   p.int2_items = static_cast<int>(int2);
   p.total_items = static_cast<int>(int2 + bf16);
-  p.group_stride = static_cast<int>(groups);
-  p.counter_bytes = align256((size_t)n * H * MERGE_COUNTERS * sizeof(int32_t));
+  p.qrot_bytes = align256((size_t)n * H * decode_qfrag_bytes(c->G()));
   p.partial_bytes = align256((size_t)parts * c->G() * PARTIAL_FLOATS * sizeof(float));
-  p.group_bytes = align256((size_t)n * H * groups * c->G() * PARTIAL_FLOATS * sizeof(float));
   return p;
 }
 
@@ -559,7 +551,7 @@ size_t decode_bytes_needed(const oscar_cache* c, int32_t layer, int32_t n, const
   for (int32_t b = 0; b < n; b += DECODE_PER_LAUNCH) {
     const int32_t m = std::min<int32_t>(DECODE_PER_LAUNCH, n - b);
     const DecodePlan p = plan_decode(c, layer, m, reqs + b, b, ppc_min, nullptr);
-    need = std::max(need, p.counter_bytes + p.partial_bytes + p.group_bytes);
+    need = std::max(need, p.qrot_bytes + p.partial_bytes);
   }
   return need;
 }

@@ -108,28 +108,24 @@ struct DecodeReq {
   int32_t hist_end;
   int32_t sink_page;
   int32_t ring_page[RING_PAGES];
-  int32_t int2_start;      // first INT2 work item (CTA) of this request
-  int32_t chunks;          // INT2 chunks per kv head (a multiple of DECODE_CLUSTER)
+  int32_t int2_start;      // first INT2 work item (block) of this request
+  int32_t chunks;          // INT2 chunks per kv head
   int32_t part_start;      // first partial slot: per kv head, 5 BF16 items then the chunks
 };
 constexpr int DECODE_PER_LAUNCH = 64;
 constexpr int DECODE_BF16_ITEMS = 1 + RING_PAGES;   // BF16 work items per (request, kv head)
-int decode_ctas_per_sm(int g);                      // resident decode CTAs per SM
-constexpr int DECODE_CLUSTER = 4;                   // CTAs of one (request, kv head) sharing q_rot
-// two-level merge: INT2 chunks are merged in groups of MERGE_GROUP; each
-// (request, kv head) owns MERGE_COUNTERS int32 tickets (head + groups)
-constexpr int MERGE_GROUP = 8;
-constexpr int MERGE_COUNTERS = 64;
-constexpr int MAX_CHUNKS_PER_HEAD = (MERGE_COUNTERS - 2) * MERGE_GROUP;
+int decode_ctas_per_sm(int g);                      // resident stream blocks per SM
+constexpr int MAX_CHUNKS_PER_HEAD = 512;
+// Workspace of one decode launch: the q_rot operands, decode_qfrag_bytes(G) per
+// (request, kv head) in launch order, then the partials fp32 [slot][G][PARTIAL_FLOATS].
+size_t decode_qfrag_bytes(int g);
 struct DecodePlan {
   int n;
   int pages_per_chunk;
-  int int2_items;          // INT2 CTAs (a multiple of DECODE_CLUSTER)
-  int total_items;         // INT2 CTAs + BF16 CTAs (padded to a multiple of DECODE_CLUSTER)
-  int group_stride;
-  size_t counter_bytes;
+  int int2_items;          // INT2 blocks
+  int total_items;         // INT2 blocks + BF16 blocks
+  size_t qrot_bytes;
   size_t partial_bytes;
-  size_t group_bytes;
 };
 cudaError_t launch_decode(const DevCache& c, int layer, const DecodeReq* reqs, const DecodePlan& plan,
                           const uint16_t* q, float* out, void* workspace, cudaStream_t s);

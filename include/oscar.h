@@ -186,11 +186,11 @@ oscar_status oscar_decode_workspace_bytes(const oscar_cache* cache, int32_t n, c
  *   reqs       host int32 [n] request ids (each with T >= 1).
  *   q          device bf16 [n][Hq][128].
  *   out        device fp32 [n][Hq][128].
- *   workspace  device, >= oscar_decode_workspace_bytes(), 256-byte aligned.
- *              Its first 256 * min(n, 64) * num_kv_heads bytes (merge
- *              tickets) must be zero before the first use; every call leaves
- *              them zero again.  Calls that share a workspace must not
- *              overlap on the GPU. */
+ *   workspace  device, >= oscar_decode_workspace_bytes(), 256-byte aligned;
+ *              no initial contents are needed.  Calls that share a workspace
+ *              must not overlap on the GPU.
+ * The decode is three kernels chained with programmatic dependent launch; the
+ * first waits for everything before it on "stream", as any launch does. */
 oscar_status oscar_decode_attention(oscar_cache* cache, int32_t layer, int32_t n, const int32_t* reqs,
                                     const uint16_t* q, float* out, void* workspace, size_t workspace_bytes,
                                     void* stream);
@@ -210,8 +210,7 @@ oscar_status oscar_decode_attention(oscar_cache* cache, int32_t layer, int32_t n
  *   Set-up: the first call on each device, made with that device current,
  *     takes the array's address and zeroes it on "stream" (an error there is
  *     OSCAR_ERR_CUDA).  Make that first call before capturing any stream.
- *     The ticket words must be zero when a call starts: set-up zeroes them
- *     and every call leaves them zero again.
+ *     No part of the array needs particular contents when a call starts.
  *   Overlap: the array is shared by every cache on the device; two calls
  *     that overlap on the GPU (other streams, other caches) race. */
 oscar_status oscar_decode_attention_noalloc(oscar_cache* cache, int32_t layer, int32_t n, const int32_t* reqs,
