@@ -12,7 +12,8 @@
 // independent loads before its producer finishes:
 //   1. rotate_q   q_rot = q R_K for every query head, written to the workspace
 //                 as the fp16 hi / lo tensor-core operands of step 2;
-//   2. stream     work items per (request, kv head):
+//   2. stream     work items per (request, kv head), waiting (bounded) on
+//                 ready words rotate_q writes with the launch's epoch:
 //                   items 0..4  BF16 sink page and the four recent-ring pages,
 //                               unrotated q;
 //                   items 5..   chunks of INT2 history pages, rotated basis;
@@ -41,6 +42,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "internal.h"
 
 namespace oscar {
@@ -53,14 +56,16 @@ constexpr int THREADS = 32 * WARPS;
 constexpr int MERGE_THREADS = 512;
 // TMA ring depth per warp and resident stream blocks per SM
 template <int G> struct Tune {
-  static constexpr int STAGES = G <= 4 ? 2 : 3;
+  static constexpr int STAGES = 2;
   static constexpr int CTAS = G <= 4 ? 4 : 3;
 };
 constexpr int BF16_ITEMS = DECODE_BF16_ITEMS;
-constexpr uint32_t WAIT_LIMIT = 1u << 22;
+constexpr uint32_t WAIT_LIMIT = 1u << 22;        // mbarrier try_wait rounds
+constexpr uint32_t FLAG_WAIT_LIMIT = 1u << 20;   // polls of a ready word
 constexpr int ERR_TIMEOUT_BIT = 8;
 
 struct DecodeArgs {
+  unsigned long long epoch;  // unique per launch: marks the q operands as written
   int n;
   int pages_per_chunk;
   int int2_items;            // INT2 blocks, before the BF16 blocks
@@ -122,11 +127,13 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 }
 
 // Pair of 2-bit codes m of each 16-bit half of w (m = 0..7) as an fp16x2 of
-// subnormals code * 2^(2 e(m) - 24), e(m) = m for m <= 4, m - 5 otherwise.
-__device__ __forceinline__ uint32_t code_pair_rt(uint32_t w, int m) {
-  return m <= 4 ? (w & (0x00030003u << (2 * m))) : ((w >> 10) & (0x00030003u << (2 * (m - 5))));
-}
+// subnormals code * 2^(2 e(m) - 24), e(m) = m for m <= 4, m - 5 otherwise; the
+// caller supplies ws = w >> 10, so one shift serves three codes.
 __host__ __device__ constexpr int code_exp(int m) { return m <= 4 ? m : m - 5; }
+__device__ __forceinline__ uint32_t code_pair2(uint32_t w, uint32_t ws, int m) {
+  return m <= 4 ? (w & (0x00030003u << (2 * m))) : (ws & (0x00030003u << (2 * (m - 5))));
+}
+
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
@@ -140,25 +147,35 @@ __device__ __forceinline__ void split_half(float x, float& hi, float& lo) {
 }
 
 constexpr int WH_STRIDE = PAGE + 8;   // halves per weight row (bank spread)
+// Softmax weights of the page being processed, fp16 [G][hi, lo][WH_STRIDE] per warp.
+// Up to four heads they fit in the page's K-code region, dead once the logits are
+// formed; eight heads get rows of their own.
+template <int G>
+constexpr bool kWeightsInRing = G * 2 * WH_STRIDE * 2 <= PAGE * CODE_BYTES;
+template <int G, bool InRing = kWeightsInRing<G>>
+struct WeightRows {
+  __align__(16) uint16_t wh[WARPS][G][2][WH_STRIDE];
+};
+template <int G>
+struct WeightRows<G, true> {};
 
 template <int G>
 struct Smem {
   // INT2: per-warp TMA rings; BF16 items: the page's K rows (16-byte chunks
-  // XOR-swizzled by row) and V rows; after the page loop: per-warp states.
+  // XOR-swizzled by row), V rows, q and the logits; after the page loop:
+  // per-warp states.
   union {
     __align__(128) uint8_t ring[WARPS][Tune<G>::STAGES][RECORD];
     struct {
       __align__(16) uint16_t k[PAGE][D];
       __align__(16) uint16_t v[PAGE][D];
+      float q[G][D];
+      __align__(16) float pw[WARPS][G][PAGE];
     } bf;
     float state[WARPS][G][PART];
   } buf;
   __align__(8) uint64_t bar[WARPS][Tune<G>::STAGES];
-  float q[G][D];             // q of the group (BF16 items)
-  union {
-    __align__(16) float pw[WARPS][G][PAGE];              // BF16 items: logits / weights
-    __align__(16) uint16_t wh[WARPS][G][2][WH_STRIDE];   // INT2: p s_v 2^ew as fp16 hi, lo
-  } ws;
+  WeightRows<G> w;
 };
 
 // ---- 1. q_rot = q R_K, delivered as tensor-core operands --------------------------
@@ -167,98 +184,120 @@ struct Smem {
 //                         (n-tile nt of (head, hi / lo part) columns, k-step s,
 //                         register r), prescaled by qscale(h) 2^(24 - 2 e(m)) so
 //                         that the fp32 accumulator holds qscale(h) q_rot . c;
-//   kscale[8], kzero[8]   fp32 per query head h of the group:
-//                         logit (log2 domain) = kscale[h] s_k acc + kzero[h] z_k,
-//                         kscale = scale log2(e) / qscale(h),
-//                         kzero  = scale log2(e) sum_c q_rot[h][c].
+//   kscale[8]             fp32 per query head h: scale log2(e) / qscale(h);
+//   qsum[4][8]            fp32 per 32-channel slab and head: sum of q_rot;
+// followed by one 64-bit ready word per slab (the launch's epoch once that slab's
+// words are written).  The logit in the log2 domain is
+//   kscale[h] s_k acc + (scale log2(e) sum_slab qsum[slab][h]) z_k.
 // Register r of k-step s for lane (gid, tid) pairs channel 32 tid + 16 (s >> 2) + m
 // (low half) with that channel + 8 (high half), m = 2 (s & 3) + r, as the code
-// registers of the A operand do.
+// registers of the A operand do; so lanes with tid = t only need slab t.
+// qscale(h) = 2^e with |q_rot| 2^(e + 24) <= 2^15 taken from |q|_2 >= max |q_rot|
+// (R_K is orthogonal), so each slab block finds it alone.
 template <int G>
 struct QFrag {
   static constexpr int NT = (G + 3) / 4;
   static constexpr int REGS = NT * 16;              // fragment registers per lane
-  static constexpr int WORDS = 32 * REGS + 16;      // + kscale[8], kzero[8]
+  static constexpr int CONSTS = 32 * REGS;          // word offset of kscale[8], qsum[4][8]
+  static constexpr int READY = CONSTS + 40;         // word offset of the four 64-bit ready words
+  static constexpr int WORDS = READY + 8;
 };
-constexpr int ROT_THREADS = 512;
+constexpr int SLABS = D / 32;
+constexpr int ROT_THREADS = 128;
 
+__device__ __forceinline__ void st_release(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Block (request i, kv head h, slab s): channels 32 s .. 32 s + 31 of q_rot for the
+// G query heads; thread (row group g, lane l) sums rows 32 g .. 32 g + 31 of column
+// 32 s + l with 32 independent loads of R_K.
 template <int G>
 __global__ void __launch_bounds__(ROT_THREADS) rotate_q_kernel(DevCache c, int layer, DecodeArgs a,
                                                                const uint16_t* __restrict__ q,
                                                                uint32_t* __restrict__ qfrag) {
   __shared__ float qs[G][D];
-  __shared__ float red[4][G][D];
+  __shared__ float red[WARPS][G][32];
   __shared__ float qscale[G];
-  const int ri = blockIdx.x / c.Hkv, head = blockIdx.x % c.Hkv;
-  const int t = threadIdx.x, ch = t & (D - 1), rg = t >> 7;   // column, group of 32 rows
-  const int warp = t >> 5, lane = t & 31;
+  const int ri = blockIdx.x / c.Hkv, head = blockIdx.x % c.Hkv, slab = blockIdx.y;
+  const int t = threadIdx.x, lane = t & 31, grp = t >> 5;
   // the preceding grid (whatever wrote q or the cache) is complete before the next
   // grid of this decode may start
   grid_dep_wait();
   grid_dep_launch();
-  const float* __restrict__ RK = c.rot_k + ((size_t)layer * c.Hkv + head) * D * D + ch;
+  const float* __restrict__ RK = c.rot_k + ((size_t)layer * c.Hkv + head) * D * D + 32 * slab + lane;
   float r[32];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) r[i] = __ldg(RK + (size_t)(32 * rg + i) * D);
+  for (int i = 0; i < 32; ++i) r[i] = __ldg(RK + (size_t)(32 * grp + i) * D);
   const uint16_t* qrow = q + ((size_t)a.r[ri].batch_row * c.Hq + (size_t)head * G) * D;
-  for (int idx = t; idx < G * D; idx += ROT_THREADS)
-    qs[idx / D][idx % D] = __uint_as_float(static_cast<uint32_t>(__ldcg(qrow + idx)) << 16);
+  uint16_t qv[G];
+#pragma unroll
+  for (int u = 0; u < G; ++u) qv[u] = __ldcg(qrow + u * D + t);
+#pragma unroll
+  for (int u = 0; u < G; ++u) qs[u][t] = __uint_as_float(static_cast<uint32_t>(qv[u]) << 16);
   __syncthreads();
+  uint32_t* dst = qfrag + (size_t)blockIdx.x * QFrag<G>::WORDS;
+  float* consts = reinterpret_cast<float*>(dst + QFrag<G>::CONSTS);
+  for (int h = grp; h < G; h += WARPS) {
+    const float4 x = *reinterpret_cast<const float4*>(&qs[h][4 * lane]);
+    float n2 = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, x.w * x.w)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
+    if (lane == 0) {
+      int e = 0;
+      if (n2 > 0.0f) e = static_cast<int>(floorf(log2f(32768.0f / (sqrtf(n2) * 1.001f)))) - 24;
+      e = max(-60, min(e, 60));
+      qscale[h] = ldexpf(1.0f, e);
+      if (slab == 0) consts[h] = ldexpf(c.scale * LOG2E, -e);
+    }
+  }
+  if (slab == 0 && t >= G && t < 8) consts[t] = 0.0f;
 #pragma unroll
   for (int h = 0; h < G; ++h) {
     float acc = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) acc = fmaf(qs[h][32 * rg + i], r[i], acc);
-    red[rg][h][ch] = acc;
+    for (int i = 0; i < 32; ++i) acc = fmaf(qs[h][32 * grp + i], r[i], acc);
+    red[grp][h][lane] = acc;
   }
   __syncthreads();
-  for (int idx = t; idx < G * D; idx += ROT_THREADS) {
-    const int h = idx / D, cc = idx % D;
-    red[0][h][cc] = (red[0][h][cc] + red[1][h][cc]) + (red[2][h][cc] + red[3][h][cc]);
+  // q_rot of this slab into red[0]; per-head slab sums
+  for (int idx = t; idx < G * 32; idx += ROT_THREADS) {
+    const int h = idx >> 5, l = idx & 31;
+    red[0][h][l] = (red[0][h][l] + red[1][h][l]) + (red[2][h][l] + red[3][h][l]);
   }
   __syncthreads();
-  uint32_t* dst = qfrag + (size_t)blockIdx.x * QFrag<G>::WORDS;
-  float* consts = reinterpret_cast<float*>(dst + 32 * QFrag<G>::REGS);
-  if (warp < G) {
-    const float4 x = *reinterpret_cast<const float4*>(&red[0][warp][4 * lane]);
-    float sum = (x.x + x.y) + (x.z + x.w);
-    float mx = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+  for (int h = grp; h < 8; h += WARPS) {
+    float sum = h < G ? red[0][h][lane] : 0.0f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    }
-    if (lane == 0) {
-      // |q_rot| qscale 2^24 <= 2^15: the fp16 operands stay finite
-      int e = 0;
-      if (mx > 0.0f) e = static_cast<int>(floorf(log2f(32768.0f / mx))) - 24;
-      e = max(-60, min(e, 60));
-      qscale[warp] = ldexpf(1.0f, e);
-      const float scale2 = c.scale * LOG2E;
-      consts[warp] = ldexpf(scale2, -e);
-      consts[8 + warp] = scale2 * sum;
-    }
-  } else if (warp < 8 && lane == 0) {
-    consts[warp] = 0.0f;
-    consts[8 + warp] = 0.0f;
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) consts[8 + 8 * slab + h] = sum;
   }
-  __syncthreads();
-  for (int wi = t; wi < 32 * QFrag<G>::REGS; wi += ROT_THREADS) {
-    const int ln = wi / QFrag<G>::REGS, k = wi % QFrag<G>::REGS;
+  // fragment words of the lanes with tid == slab: lane 4 gid + slab, register k
+  for (int wi = t; wi < 8 * QFrag<G>::REGS; wi += ROT_THREADS) {
+    const int gid = wi / QFrag<G>::REGS, k = wi % QFrag<G>::REGS;
     const int nt = k >> 4, s = (k >> 1) & 7, rr = k & 1;
-    const int gid = ln >> 2, tid = ln & 3;
     const int h = 4 * nt + (gid >> 1);
     uint32_t word = 0u;
     if (h < G) {
       const int m = 2 * (s & 3) + rr;
-      const int cha = 32 * tid + 16 * (s >> 2) + m;
+      const int cl = 16 * (s >> 2) + m;     // channel within the slab
       const float f = ldexpf(qscale[h], 24 - 2 * code_exp(m));
       float ha, la, hb, lb;
-      split_half(red[0][h][cha] * f, ha, la);
-      split_half(red[0][h][cha + 8] * f, hb, lb);
+      split_half(red[0][h][cl] * f, ha, la);
+      split_half(red[0][h][cl + 8] * f, hb, lb);
       word = (gid & 1) ? pack_half2(la, lb) : pack_half2(ha, hb);
     }
-    dst[wi] = word;
+    dst[(size_t)(4 * gid + slab) * QFrag<G>::REGS + k] = word;
+  }
+  __syncthreads();
+  if (t == 0) {
+    __threadfence();
+    st_release(reinterpret_cast<unsigned long long*>(dst + QFrag<G>::READY) + slab, a.epoch);
   }
 }
 
@@ -270,12 +309,13 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // One chunk of INT2 history pages of one (request, kv head); qf points at the
-// (request, kv head)'s q operands.  Leaves the block's partial (rotated basis)
-// for every query head of the group in part_out.
+// (request, kv head)'s q operands.  Warp w of the block takes pages w, w + 4, ...
+// of the chunk.  Leaves the block's partial (rotated basis) for every query head
+// of the group in part_out.
 template <int G>
 __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const DecodeReq& R, int head, int chunk,
-                                           int ppc, const uint32_t* __restrict__ qf, Smem<G>& sm,
-                                           float* part_out) {
+                                           int ppc, const uint32_t* __restrict__ qf, unsigned long long epoch,
+                                           Smem<G>& sm, float* part_out) {
   constexpr int NT = QFrag<G>::NT;       // n-tiles of 8 columns = 4 heads x (hi, lo)
   constexpr int STAGES = Tune<G>::STAGES;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -339,7 +379,26 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
   }
   const float wscale = ldexpf(1.0f, ew);
   grid_dep_launch();
-  grid_dep_wait();
+  // wait (bounded) until the four slab blocks of rotate_q have written this
+  // (request, kv head)'s operands: lanes 0..3 each watch one ready word
+  {
+    bool ok = true;
+    if (lane < SLABS) {
+      const unsigned long long* ready = reinterpret_cast<const unsigned long long*>(qf + QFrag<G>::READY) + lane;
+      uint32_t it = 0;
+      while (ld_acquire(ready) != epoch) {
+        __nanosleep(64);
+        if (++it == FLAG_WAIT_LIMIT) {
+          ok = false;
+          break;
+        }
+      }
+    }
+    if (!__all_sync(0xffffffffu, ok)) {
+      if (lane == 0) atomicOr(c.err, ERR_TIMEOUT_BIT);
+      timed_out = true;
+    }
+  }
 
   // B operands of q_rot . c, and the per-head logit constants of this lane's head
   uint32_t bq[NT][8][2];
@@ -360,11 +419,14 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
   }
   float ks[NT], kz[NT];
   {
-    const float* consts = reinterpret_cast<const float*>(qf + 32 * QFrag<G>::REGS);
+    const float* consts = reinterpret_cast<const float*>(qf + QFrag<G>::CONSTS);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       ks[nt] = __ldcg(consts + 4 * nt + tid);
-      kz[nt] = __ldcg(consts + 8 + 4 * nt + tid);
+      float sum = 0.0f;
+#pragma unroll
+      for (int sl = 0; sl < SLABS; ++sl) sum += __ldcg(consts + 8 + 8 * sl + 4 * nt + tid);
+      kz[nt] = c.scale * LOG2E * sum;
     }
   }
 
@@ -383,13 +445,13 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
 
   for (int j = 0; j < my_n; ++j) {
     const int stg = j % STAGES;
+    const int pi = pc0 + warp + WARPS * j;
     if (!timed_out && !mbar_wait(&sm.bar[warp][stg], (j / STAGES) & 1)) {
       timed_out = true;
       if (lane == 0) atomicOr(c.err, ERR_TIMEOUT_BIT);
     }
     if (timed_out) break;
     const uint8_t* rec = sm.buf.ring[warp][stg];
-    const int pi = pc0 + warp + WARPS * j;
     const int valid = min(PAGE, nhist - pi * PAGE);
 
     // ---- logits: 4 m-tiles of 16 tokens x NT n-tiles, K = 128 channels
@@ -404,13 +466,15 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
     for (int mt = 0; mt < 4; ++mt) {
       const uint2 ka = *reinterpret_cast<const uint2*>(rec + K_CODES_OFF + (16 * mt + gid) * CODE_BYTES + 8 * tid);
       const uint2 kb = *reinterpret_cast<const uint2*>(rec + K_CODES_OFF + (16 * mt + gid + 8) * CODE_BYTES + 8 * tid);
+      const uint2 kas = make_uint2(ka.x >> 10, ka.y >> 10);
+      const uint2 kbs = make_uint2(kb.x >> 10, kb.y >> 10);
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        const uint32_t wa = s < 4 ? ka.x : ka.y;
-        const uint32_t wb = s < 4 ? kb.x : kb.y;
+        const uint32_t wa = s < 4 ? ka.x : ka.y, was = s < 4 ? kas.x : kas.y;
+        const uint32_t wb = s < 4 ? kb.x : kb.y, wbs = s < 4 ? kbs.x : kbs.y;
         const int m0 = 2 * (s & 3);
-        const uint32_t a0 = code_pair_rt(wa, m0), a1 = code_pair_rt(wb, m0);
-        const uint32_t a2 = code_pair_rt(wa, m0 + 1), a3 = code_pair_rt(wb, m0 + 1);
+        const uint32_t a0 = code_pair2(wa, was, m0), a1 = code_pair2(wb, wbs, m0);
+        const uint32_t a2 = code_pair2(wa, was, m0 + 1), a3 = code_pair2(wb, wbs, m0 + 1);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt][mt], a0, a1, a2, a3, bq[nt][s][0], bq[nt][s][1]);
       }
@@ -418,27 +482,40 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
     // token meta of this lane's 8 tokens: 16 mt + gid + 8 rr; a partial page (the
     // last of the history) masks the rows past its end
     float lg[NT][8], sw[8], zv[8];
-    const bool full = valid == PAGE;
+    auto epilogue = [&](auto full_page) {
+      constexpr bool FULL = decltype(full_page)::value;
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
+      for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int i = 2 * mt + rr;
-        const int tok = 16 * mt + gid + 8 * rr;
-        const __half2 km = *reinterpret_cast<const __half2*>(rec + K_META_OFF + tok * META_BYTES);
-        const __half2 vm = *reinterpret_cast<const __half2*>(rec + V_META_OFF + tok * META_BYTES);
-        const bool ok = full || tok < valid;
-        sw[i] = ok ? __low2float(vm) * wscale : 0.0f;
-        zv[i] = ok ? __high2float(vm) : 0.0f;
-        const float sk = __low2float(km), zk = __high2float(km);
+        for (int rr = 0; rr < 2; ++rr) {
+          const int i = 2 * mt + rr;
+          const int tok = 16 * mt + gid + 8 * rr;
+          const __half2 km = *reinterpret_cast<const __half2*>(rec + K_META_OFF + tok * META_BYTES);
+          const __half2 vm = *reinterpret_cast<const __half2*>(rec + V_META_OFF + tok * META_BYTES);
+          const bool ok = FULL || tok < valid;
+          sw[i] = ok ? __low2float(vm) * wscale : 0.0f;
+          zv[i] = ok ? __high2float(vm) : 0.0f;
+          const float sk = __low2float(km), zk = __high2float(km);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const float v = fmaf(ks[nt] * sk, acc[nt][mt][2 * rr] + acc[nt][mt][2 * rr + 1], kz[nt] * zk);
-          lg[nt][i] = (ok && 4 * nt + tid < G) ? v : -INFINITY;
+          for (int nt = 0; nt < NT; ++nt) {
+            const float v = fmaf(ks[nt] * sk, acc[nt][mt][2 * rr] + acc[nt][mt][2 * rr + 1], kz[nt] * zk);
+            lg[nt][i] = (ok && (4 * nt + 4 <= G || 4 * nt + tid < G)) ? v : -INFINITY;
+          }
         }
-      }
+    };
+    if (valid == PAGE)
+      epilogue(std::true_type{});
+    else
+      epilogue(std::false_type{});
     // ---- online softmax per head (lanes with equal tid share a head); the
     // weights p s_v 2^ew go to shared memory as fp16 hi / lo halves
+    uint16_t(*wh)[2][WH_STRIDE];
+    if constexpr (kWeightsInRing<G>) {
+      wh = reinterpret_cast<uint16_t(*)[2][WH_STRIDE]>(sm.buf.ring[warp][stg] + K_CODES_OFF);
+      __syncwarp();   // every lane is done reading this page's K codes
+    } else {
+      wh = sm.w.wh[warp];
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       float pm = lg[nt][0];
@@ -465,11 +542,12 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
         l_run[nt] += p;
         u_run[nt] = fmaf(p, zv[i], u_run[nt]);
         if (h < G) {
-          float hi, lo;
-          split_half(p * sw[i], hi, lo);
+          const float w = p * sw[i];
+          const __half hi = __float2half_rn(w);
+          const __half lo = __float2half_rn(w - __half2float(hi));
           const int tok = 16 * (i >> 1) + gid + 8 * (i & 1);
-          sm.ws.wh[warp][h][0][tok] = __half_as_ushort(__float2half_rn(hi));
-          sm.ws.wh[warp][h][1][tok] = __half_as_ushort(__float2half_rn(lo));
+          wh[h][0][tok] = __half_as_ushort(hi);
+          wh[h][1][tok] = __half_as_ushort(lo);
         }
       }
     }
@@ -483,7 +561,7 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
       for (int nt = 0; nt < NT; ++nt) {
         const int h = 4 * nt + (gid >> 1);
         if (h < G) {
-          const uint16_t* row = sm.ws.wh[warp][h][gid & 1];
+          const uint16_t* row = wh[h][gid & 1];
           bw[nt][0] = *reinterpret_cast<const uint32_t*>(row + ta);
           bw[nt][1] = *reinterpret_cast<const uint32_t*>(row + ta + 8);
         } else {
@@ -495,10 +573,12 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
       const uint32_t wc = vrow[(ta + 8) * (CODE_BYTES / 4)], wd = vrow[(ta + 9) * (CODE_BYTES / 4)];
       const uint32_t x1 = __byte_perm(wa, wb, 0x5410), y1 = __byte_perm(wa, wb, 0x7632);
       const uint32_t x2 = __byte_perm(wc, wd, 0x5410), y2 = __byte_perm(wc, wd, 0x7632);
+      const uint32_t x1s = x1 >> 10, y1s = y1 >> 10;
+      const uint32_t x2s = x2 >> 10, y2s = y2 >> 10;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
-        const uint32_t a0 = code_pair_rt(x1, mt), a1 = code_pair_rt(y1, mt);
-        const uint32_t a2 = code_pair_rt(x2, mt), a3 = code_pair_rt(y2, mt);
+        const uint32_t a0 = code_pair2(x1, x1s, mt), a1 = code_pair2(y1, y1s, mt);
+        const uint32_t a2 = code_pair2(x2, x2s, mt), a3 = code_pair2(y2, y2s, mt);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma16816(o[nt][mt], a0, a1, a2, a3, bw[nt][0], bw[nt][1]);
       }
@@ -507,6 +587,8 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
     {
       const uint8_t* src = page_src(j + STAGES);
       if (lane == 0 && j + STAGES < my_n) {
+        // the weights were written to this buffer through the generic proxy
+        if constexpr (kWeightsInRing<G>) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         mbar_expect_tx(&sm.bar[warp][stg], RECORD);
         tma_load_1d(sm.buf.ring[warp][stg], src, RECORD, &sm.bar[warp][stg]);
         ++issued;
@@ -628,20 +710,20 @@ __device__ __forceinline__ void bf16_item(const DevCache& c, int layer, const De
         const float k0 = bf16lo(ww[e]), k1 = bf16hi(ww[e]);
         const int ch = 8 * chunk + 2 * e;
 #pragma unroll
-        for (int h = 0; h < G; ++h) acc[h] = fmaf(sm.q[h][ch + 1], k1, fmaf(sm.q[h][ch], k0, acc[h]));
+        for (int h = 0; h < G; ++h) acc[h] = fmaf(sm.buf.bf.q[h][ch + 1], k1, fmaf(sm.buf.bf.q[h][ch], k0, acc[h]));
       }
     }
     const bool ok = row_valid(r);
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], 1);
-      if (half == 0) sm.ws.pw[0][h][r] = ok ? acc[h] * scale2 : -INFINITY;
+      if (half == 0) sm.buf.bf.pw[0][h][r] = ok ? acc[h] * scale2 : -INFINITY;
     }
   }
   __syncthreads();
   // softmax and values: warp w handles heads w, w + 4; lane owns channels 4 lane .. 4 lane + 3
   for (int h = warp; h < G; h += WARPS) {
-    const float x0 = sm.ws.pw[0][h][lane], x1 = sm.ws.pw[0][h][lane + 32];
+    const float x0 = sm.buf.bf.pw[0][h][lane], x1 = sm.buf.bf.pw[0][h][lane + 32];
     float m = fmaxf(x0, x1);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -651,13 +733,13 @@ __device__ __forceinline__ void bf16_item(const DevCache& c, int layer, const De
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
     __syncwarp();
-    sm.ws.pw[0][h][lane] = p0;
-    sm.ws.pw[0][h][lane + 32] = p1;
+    sm.buf.bf.pw[0][h][lane] = p0;
+    sm.buf.bf.pw[0][h][lane + 32] = p1;
     __syncwarp();
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     if (m != -INFINITY) {
       for (int r = 0; r < PAGE; ++r) {
-        const float p = sm.ws.pw[0][h][r];
+        const float p = sm.buf.bf.pw[0][h][r];
         const uint2 vv = reinterpret_cast<const uint2*>(&sm.buf.bf.v[r][0])[lane];
         acc[0] = fmaf(p, bf16lo(vv.x), acc[0]);
         acc[1] = fmaf(p, bf16hi(vv.x), acc[1]);
@@ -709,13 +791,15 @@ __global__ void __launch_bounds__(THREADS, Tune<G>::CTAS) decode_stream_kernel(D
 #pragma unroll
     for (int u = 0; u < G; ++u) qv[u] = __ldcg(qrow + u * D + t);
 #pragma unroll
-    for (int u = 0; u < G; ++u) sm.q[u][t] = __uint_as_float(static_cast<uint32_t>(qv[u]) << 16);
+    for (int u = 0; u < G; ++u) sm.buf.bf.q[u][t] = __uint_as_float(static_cast<uint32_t>(qv[u]) << 16);
     __syncthreads();
     bf16_item<G>(c, layer, R, head, sub, sm, part);
   } else {
     int2_chunk<G>(c, layer, R, head, sub - BF16_ITEMS, a.pages_per_chunk,
-                  qfrag + ((size_t)ri * c.Hkv + head) * QFrag<G>::WORDS, sm, part);
+                  qfrag + ((size_t)ri * c.Hkv + head) * QFrag<G>::WORDS, a.epoch, sm, part);
   }
+  // this grid completes only after rotate_q has (later launches rely on stream order)
+  grid_dep_wait();
 }
 
 // ---- 3. merge -------------------------------------------------------------------------
@@ -875,7 +959,7 @@ cudaError_t launch_g(const DevCache& c, int layer, const DecodeArgs& a, int item
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
 
-  cfg.gridDim = dim3(static_cast<unsigned>(a.n * c.Hkv));
+  cfg.gridDim = dim3(static_cast<unsigned>(a.n * c.Hkv), SLABS);
   cfg.blockDim = dim3(ROT_THREADS);
   cfg.dynamicSmemBytes = 0;
   e = cudaLaunchKernelEx(&cfg, rotate_q_kernel<G>, c, layer, a, q, qfrag);
@@ -897,8 +981,9 @@ cudaError_t launch_g(const DevCache& c, int layer, const DecodeArgs& a, int item
 }  // namespace
 
 cudaError_t launch_decode(const DevCache& c, int layer, const DecodeReq* reqs, const DecodePlan& plan,
-                          const uint16_t* q, float* out, void* workspace, cudaStream_t s) {
+                          const uint16_t* q, float* out, void* workspace, uint64_t epoch, cudaStream_t s) {
   DecodeArgs a;
+  a.epoch = epoch;
   a.n = plan.n;
   a.pages_per_chunk = plan.pages_per_chunk;
   a.int2_items = plan.int2_items;

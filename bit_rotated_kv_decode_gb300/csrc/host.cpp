@@ -9,6 +9,7 @@
 // prefix-cache compatibility the pages claim (same page, Visual Explainer step
 // 5; "TogetherAI开源OSCAR" (ModelScope), section "评估结果").
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -92,6 +93,10 @@ struct oscar_cache {
   std::vector<Request> reqs;
   std::string err;
   int num_sms = 152;
+  uint64_t uid = 0;               // process-unique cache id (high half of decode epochs)
+  uint32_t decode_launches = 0;
+
+  uint64_t next_epoch() { return (uid << 32) | ++decode_launches; }
 
   oscar_status fail(oscar_status s, const std::string& msg) {
     err = msg;
@@ -198,6 +203,8 @@ oscar_status oscar_cache_create(const oscar_cache_config* cfg, void* device_mem,
     }
   }
   oscar_cache* c = new oscar_cache();
+  static std::atomic<uint64_t> next_uid{1};
+  c->uid = next_uid.fetch_add(1);
   c->cfg = *cfg;
   if (c->cfg.num_bf16_pages == 0) c->cfg.num_bf16_pages = (int64_t)BF16_PAGES_PER_REQ * cfg->max_requests;
   if (c->cfg.softmax_scale == 0.0f) c->cfg.softmax_scale = 1.0f / std::sqrt(static_cast<float>(D));
@@ -611,7 +618,7 @@ oscar_status oscar_decode_attention(oscar_cache* c, int32_t layer, int32_t n, co
   for (int32_t b = 0; b < n; b += DECODE_PER_LAUNCH) {
     const int32_t m = std::min<int32_t>(DECODE_PER_LAUNCH, n - b);
     const DecodePlan p = plan_decode(c, layer, m, reqs + b, b, ppc_min, dr);
-    const cudaError_t err = launch_decode(c->dc, layer, dr, p, q, out, workspace, s);
+    const cudaError_t err = launch_decode(c->dc, layer, dr, p, q, out, workspace, c->next_epoch(), s);
     if (err != cudaSuccess) return c->cuda_fail(err, "decode launch");
   }
   return OSCAR_OK;

@@ -127,8 +127,9 @@ struct DecodePlan {
   size_t qrot_bytes;
   size_t partial_bytes;
 };
+// epoch: unique per launch (never repeated for any workspace the launch could use)
 cudaError_t launch_decode(const DevCache& c, int layer, const DecodeReq* reqs, const DecodePlan& plan,
-                          const uint16_t* q, float* out, void* workspace, cudaStream_t s);
+                          const uint16_t* q, float* out, void* workspace, uint64_t epoch, cudaStream_t s);
 
 // Fixed decode scratch (one static device array per device) for callers that
 // cannot allocate.  The first call on a device, with that device current,

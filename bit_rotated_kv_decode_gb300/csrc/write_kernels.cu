@@ -229,6 +229,18 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(DevCache c, int 
   const int lane = t & 31, grp = t >> 5;
   const size_t lh = (size_t)layer * c.Hkv + head;
 
+  // Launched with programmatic dependent launch: R is written once at set-up, so
+  // L2 is warmed with this thread's rows while the preceding grid (which may still
+  // be writing k / v or reading the cache) finishes; nothing is read before the wait.
+  if (q.demote_slot >= 0) {
+    const float* R = (which ? c.rot_v : c.rot_k) + lh * D * D;
+#pragma unroll
+    for (int i = 0; i < APPEND_ROWS; ++i)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(R + (size_t)(APPEND_ROWS * grp + i) * D + 4 * lane));
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   if (q.demote_slot >= 0) {
     const bool ok_src = q.src_page >= 0 && q.src_page < c.n_bf16_pages;
     const bool ok_dst = q.hist_page >= 0 && q.hist_page < c.n_int2_pages;
@@ -354,9 +366,16 @@ cudaError_t launch_append(const DevCache& c, int layer, const AppendReq* reqs, i
     AppendArgs a;
     a.n = n - base < APPEND_PER_LAUNCH ? n - base : APPEND_PER_LAUNCH;
     for (int i = 0; i < a.n; ++i) a.r[i] = reqs[base + i];
-    dim3 grid(a.n, c.Hkv, 2);
-    append_kernel<<<grid, APPEND_THREADS, 0, s>>>(c, layer, k, v, a);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.n), static_cast<unsigned>(c.Hkv), 2);
+    cfg.blockDim = dim3(APPEND_THREADS);
+    cfg.stream = s;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, append_kernel, c, layer, k, v, a);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
