@@ -215,6 +215,7 @@ class Workload:
         ws_bytes = self.cache.workspace_bytes(self.reqs) + (1 << 20)
         self.ws = binding.new_workspace(ws_bytes)
         self.step_index = 0
+        self.fused = True
         # raw C entry points with pre-marshalled arguments (the binding's own calls, minus re-marshalling)
         self.lib = self.cache.lib
         self.h = self.cache.h
@@ -233,10 +234,14 @@ class Workload:
     def run_step(self, ptrs, stream, dec_events=None, app_events=None):
         """One step: every layer appends (with demotion) and decodes."""
         lib, h, n, ra, ws, wl = self.lib, self.h, self.batch, self.reqs_arr, self.ws_ptr, self.ws_len
-        append, decode = lib.oscar_append, lib.oscar_decode_attention
+        append, decode, fused = lib.oscar_append, lib.oscar_decode_attention, lib.oscar_decode_step
         if dec_events is None:
             for layer, (kp, vp, qp, op) in enumerate(ptrs):
-                if append(h, layer, n, ra, kp, vp, stream) or decode(h, layer, n, ra, qp, op, ws, wl, stream):
+                if self.fused:
+                    st = fused(h, layer, n, ra, kp, vp, qp, op, ws, wl, stream)
+                else:
+                    st = append(h, layer, n, ra, kp, vp, stream) or decode(h, layer, n, ra, qp, op, ws, wl, stream)
+                if st:
                     raise RuntimeError(f"step failed: {lib.oscar_last_error(h).decode()}")
             return
         for layer, (kp, vp, qp, op) in enumerate(ptrs):
@@ -264,6 +269,7 @@ def run_gpu(args, log):
     W, K = args.warmup, args.steps
     ew, ek = 2, max(3, K // 2)
     wl = Workload(args.config, W + 2 * K + ew + ek, log, args.layers)
+    wl.fused = not args.separate_calls
     stream = wl.stream_ptr()
     L = wl.L
     ptrs = [wl.pointers(s) for s in range(W + 2 * K)]
@@ -333,7 +339,7 @@ def run_gpu(args, log):
     res = {
         "us_step": us_step, "kv_bytes_step": kv_bytes_step, "dec_avg_us": dec_avg, "app_avg_us": app_avg, "bytes_per_launch": bpl,
         "achieved_gbs": achieved, "peak": peak, "peak_kind": peak_kind, "e2e_us": e2e_us, "h2d": h2d, "d2h": d2h,
-        "clocks": clk.summary(), "launches": K * L * 4, "world": world, "rank": rank,
+        "clocks": clk.summary(), "launches": K * L * (3 if wl.fused else 4), "world": world, "rank": rank,
     }
     return wl, res
 
@@ -436,6 +442,8 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=2, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="fewer layers (small profiling cases only)")
+    ap.add_argument("--separate-calls", action="store_true",
+                    help="time oscar_append + oscar_decode_attention per layer instead of oscar_decode_step")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -472,7 +480,9 @@ def main(argv=None):
         "config": {"workload": w["name"], "layers": wl.L, "q_heads": wl.hq, "kv_heads": wl.hkv, "head_dim": 128,
                    "batch": wl.batch, "context": wl.T0, "page_tokens": 64, "page_order": "seeded shuffle",
                    "storage": "INT2 codes + fp16 scale/zero history, BF16 sink/recent",
-                   "step": "per layer: append (fused demote) + decode attention",
+                   "step": ("per layer: oscar_decode_step (append with fused demote, then decode attention)"
+                            if not args.separate_calls else
+                            "per layer: oscar_append (fused demote) then oscar_decode_attention"),
                    "l2": "inputs larger than L2 (%.2f GB of KV per step vs 129 MB L2)" % (
                        r["bytes_per_launch"] * wl.L / 1e9),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},

@@ -74,6 +74,7 @@ _SIGNATURES = {
     "oscar_decode_workspace_bytes": (c_int32, [_P, c_int32, POINTER(c_int32), POINTER(c_size_t)]),
     "oscar_decode_attention": (c_int32, [_P, c_int32, c_int32, POINTER(c_int32), _P, _P, _P, c_size_t, _P]),
     "oscar_decode_attention_noalloc": (c_int32, [_P, c_int32, c_int32, POINTER(c_int32), _P, _P, _P]),
+    "oscar_decode_step": (c_int32, [_P, c_int32, c_int32, POINTER(c_int32), _P, _P, _P, _P, _P, c_size_t, _P]),
     "oscar_cache_check": (c_int32, [_P, _P]),
     "oscar_last_error": (c_char_p, [_P]),
 }
@@ -245,6 +246,14 @@ class OscarCache:
         self._check(self.lib.oscar_decode_attention(self.h, layer, len(reqs), arr, _ptr(q), _ptr(out),
                                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
                                                     _stream_ptr(stream)), "decode")
+
+    def step(self, layer: int, reqs, k, v, q, out, workspace, stream=None) -> None:
+        """Append k / v of every request, then decode with q (one fused call)."""
+        arr = self._reqs(reqs)
+        nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        self._check(self.lib.oscar_decode_step(self.h, layer, len(reqs), arr, _ptr(k), _ptr(v), _ptr(q), _ptr(out),
+                                               _ptr(workspace), nbytes, None if self.dry else _stream_ptr(stream)),
+                    "decode step", allow_dry=True)
 
     def decode_noalloc(self, layer: int, reqs, q, out, stream=None) -> None:
         """Decode with the library's fixed static scratch (no workspace argument)."""

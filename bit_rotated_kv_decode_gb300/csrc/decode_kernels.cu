@@ -44,6 +44,7 @@
 
 #include <type_traits>
 
+#include "append_device.cuh"
 #include "internal.h"
 
 namespace oscar {
@@ -66,6 +67,7 @@ constexpr int ERR_TIMEOUT_BIT = 8;
 
 struct DecodeArgs {
   unsigned long long epoch;  // unique per launch: marks the q operands as written
+  int front_writes;          // the preceding grid writes the BF16 ring and the hot pages
   int n;
   int pages_per_chunk;
   int int2_items;            // INT2 blocks, before the BF16 blocks
@@ -214,37 +216,33 @@ __device__ __forceinline__ unsigned long long ld_acquire(const unsigned long lon
   return v;
 }
 
-// Block (request i, kv head h, slab s): channels 32 s .. 32 s + 31 of q_rot for the
-// G query heads; thread (row group g, lane l) sums rows 32 g .. 32 g + 31 of column
-// 32 s + l with 32 independent loads of R_K.
-template <int G>
-__global__ void __launch_bounds__(ROT_THREADS) rotate_q_kernel(DevCache c, int layer, DecodeArgs a,
-                                                               const uint16_t* __restrict__ q,
-                                                               uint32_t* __restrict__ qfrag) {
-  __shared__ float qs[G][D];
-  __shared__ float red[WARPS][G][32];
-  __shared__ float qscale[G];
-  const int ri = blockIdx.x / c.Hkv, head = blockIdx.x % c.Hkv, slab = blockIdx.y;
+// Block (request i, kv head h, slab s) of NTH threads: channels 32 s .. 32 s + 31
+// of q_rot for the G query heads; thread (row group g, lane l) sums the
+// D / (NTH / 32) rows of group g of column 32 s + l with independent loads of R_K.
+template <int G, int NTH>
+struct RotSmem {
+  float qs[G][D];
+  float red[NTH / 32][G][32];
+  float qscale[G];
+};
+
+template <int G, int NTH>
+__device__ __forceinline__ void rotate_block(const DevCache& c, int layer, unsigned long long epoch, int batch_row,
+                                             int head, int slab, const uint16_t* __restrict__ q,
+                                             uint32_t* __restrict__ dst, RotSmem<G, NTH>& sm) {
+  constexpr int RG = NTH / 32, ROWS = D / RG;
   const int t = threadIdx.x, lane = t & 31, grp = t >> 5;
-  // the preceding grid (whatever wrote q or the cache) is complete before the next
-  // grid of this decode may start
-  grid_dep_wait();
-  grid_dep_launch();
   const float* __restrict__ RK = c.rot_k + ((size_t)layer * c.Hkv + head) * D * D + 32 * slab + lane;
-  float r[32];
+  float r[ROWS];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) r[i] = __ldg(RK + (size_t)(32 * grp + i) * D);
-  const uint16_t* qrow = q + ((size_t)a.r[ri].batch_row * c.Hq + (size_t)head * G) * D;
-  uint16_t qv[G];
-#pragma unroll
-  for (int u = 0; u < G; ++u) qv[u] = __ldcg(qrow + u * D + t);
-#pragma unroll
-  for (int u = 0; u < G; ++u) qs[u][t] = __uint_as_float(static_cast<uint32_t>(qv[u]) << 16);
+  for (int i = 0; i < ROWS; ++i) r[i] = __ldg(RK + (size_t)(ROWS * grp + i) * D);
+  const uint16_t* qrow = q + ((size_t)batch_row * c.Hq + (size_t)head * G) * D;
+  for (int idx = t; idx < G * D; idx += NTH)
+    sm.qs[idx / D][idx % D] = __uint_as_float(static_cast<uint32_t>(__ldcg(qrow + idx)) << 16);
   __syncthreads();
-  uint32_t* dst = qfrag + (size_t)blockIdx.x * QFrag<G>::WORDS;
   float* consts = reinterpret_cast<float*>(dst + QFrag<G>::CONSTS);
-  for (int h = grp; h < G; h += WARPS) {
-    const float4 x = *reinterpret_cast<const float4*>(&qs[h][4 * lane]);
+  for (int h = grp; h < G; h += RG) {
+    const float4 x = *reinterpret_cast<const float4*>(&sm.qs[h][4 * lane]);
     float n2 = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, x.w * x.w)));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
@@ -252,7 +250,7 @@ __global__ void __launch_bounds__(ROT_THREADS) rotate_q_kernel(DevCache c, int l
       int e = 0;
       if (n2 > 0.0f) e = static_cast<int>(floorf(log2f(32768.0f / (sqrtf(n2) * 1.001f)))) - 24;
       e = max(-60, min(e, 60));
-      qscale[h] = ldexpf(1.0f, e);
+      sm.qscale[h] = ldexpf(1.0f, e);
       if (slab == 0) consts[h] = ldexpf(c.scale * LOG2E, -e);
     }
   }
@@ -261,24 +259,27 @@ __global__ void __launch_bounds__(ROT_THREADS) rotate_q_kernel(DevCache c, int l
   for (int h = 0; h < G; ++h) {
     float acc = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) acc = fmaf(qs[h][32 * grp + i], r[i], acc);
-    red[grp][h][lane] = acc;
+    for (int i = 0; i < ROWS; ++i) acc = fmaf(sm.qs[h][ROWS * grp + i], r[i], acc);
+    sm.red[grp][h][lane] = acc;
   }
   __syncthreads();
   // q_rot of this slab into red[0]; per-head slab sums
-  for (int idx = t; idx < G * 32; idx += ROT_THREADS) {
+  for (int idx = t; idx < G * 32; idx += NTH) {
     const int h = idx >> 5, l = idx & 31;
-    red[0][h][l] = (red[0][h][l] + red[1][h][l]) + (red[2][h][l] + red[3][h][l]);
+    float v = sm.red[0][h][l];
+#pragma unroll
+    for (int g2 = 1; g2 < RG; ++g2) v += sm.red[g2][h][l];
+    sm.red[0][h][l] = v;
   }
   __syncthreads();
-  for (int h = grp; h < 8; h += WARPS) {
-    float sum = h < G ? red[0][h][lane] : 0.0f;
+  for (int h = grp; h < 8; h += RG) {
+    float sum = h < G ? sm.red[0][h][lane] : 0.0f;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     if (lane == 0) consts[8 + 8 * slab + h] = sum;
   }
   // fragment words of the lanes with tid == slab: lane 4 gid + slab, register k
-  for (int wi = t; wi < 8 * QFrag<G>::REGS; wi += ROT_THREADS) {
+  for (int wi = t; wi < 8 * QFrag<G>::REGS; wi += NTH) {
     const int gid = wi / QFrag<G>::REGS, k = wi % QFrag<G>::REGS;
     const int nt = k >> 4, s = (k >> 1) & 7, rr = k & 1;
     const int h = 4 * nt + (gid >> 1);
@@ -286,10 +287,10 @@ __global__ void __launch_bounds__(ROT_THREADS) rotate_q_kernel(DevCache c, int l
     if (h < G) {
       const int m = 2 * (s & 3) + rr;
       const int cl = 16 * (s >> 2) + m;     // channel within the slab
-      const float f = ldexpf(qscale[h], 24 - 2 * code_exp(m));
+      const float f = ldexpf(sm.qscale[h], 24 - 2 * code_exp(m));
       float ha, la, hb, lb;
-      split_half(red[0][h][cl] * f, ha, la);
-      split_half(red[0][h][cl + 8] * f, hb, lb);
+      split_half(sm.red[0][h][cl] * f, ha, la);
+      split_half(sm.red[0][h][cl + 8] * f, hb, lb);
       word = (gid & 1) ? pack_half2(la, lb) : pack_half2(ha, hb);
     }
     dst[(size_t)(4 * gid + slab) * QFrag<G>::REGS + k] = word;
@@ -297,8 +298,22 @@ __global__ void __launch_bounds__(ROT_THREADS) rotate_q_kernel(DevCache c, int l
   __syncthreads();
   if (t == 0) {
     __threadfence();
-    st_release(reinterpret_cast<unsigned long long*>(dst + QFrag<G>::READY) + slab, a.epoch);
+    st_release(reinterpret_cast<unsigned long long*>(dst + QFrag<G>::READY) + slab, epoch);
   }
+}
+
+template <int G>
+__global__ void __launch_bounds__(ROT_THREADS) rotate_q_kernel(DevCache c, int layer, DecodeArgs a,
+                                                               const uint16_t* __restrict__ q,
+                                                               uint32_t* __restrict__ qfrag) {
+  __shared__ RotSmem<G, ROT_THREADS> sm;
+  const int ri = blockIdx.x / c.Hkv, head = blockIdx.x % c.Hkv, slab = blockIdx.y;
+  // the preceding grid (whatever wrote q or the cache) is complete before the next
+  // grid of this decode may start
+  grid_dep_wait();
+  grid_dep_launch();
+  rotate_block<G, ROT_THREADS>(c, layer, a.epoch, a.r[ri].batch_row, head, slab, q,
+                               qfrag + (size_t)blockIdx.x * QFrag<G>::WORDS, sm);
 }
 
 // ---- 2. stream: INT2 chunks and BF16 pages ------------------------------------------
@@ -335,22 +350,31 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
   // batch b); page_src is called by the whole warp with increasing j
   int32_t batch_pages = 0;
   int batch_idx = -1;
+  auto checked = [&](int32_t page) -> int32_t {
+    if (page < 0 || page >= c.n_int2_pages) {
+      atomicOr(c.err, ERR_INT2_PAGE);
+      page = 0;
+    }
+    return page;
+  };
+  // the hot page (written by a preceding fused append) is read only after that
+  // grid has completed: its id is fetched by lane 0 at copy time, after the wait
   auto page_src = [&](int j) -> const uint8_t* {
     const int b = j >> 5;
     if (b != batch_idx) {
       batch_idx = b;
       const int jj = 32 * b + lane;
+      const int pj = pc0 + warp + WARPS * jj;
       int32_t page = 0;
-      if (jj < my_n) {
-        page = __ldcg(pt + pc0 + warp + WARPS * jj);
-        if (page < 0 || page >= c.n_int2_pages) {
-          atomicOr(c.err, ERR_INT2_PAGE);
-          page = 0;
-        }
-      }
+      if (jj < my_n) page = pj == R.hot_page ? -1 : checked(__ldcg(pt + pj));
       batch_pages = page;
     }
-    return base + (size_t)__shfl_sync(0xffffffffu, batch_pages, j & 31) * pstride;
+    int32_t page = __shfl_sync(0xffffffffu, batch_pages, j & 31);
+    if (page < 0 && lane == 0) {
+      grid_dep_wait();
+      page = checked(__ldcg(pt + R.hot_page));
+    }
+    return base + (size_t)max(page, 0) * pstride;
   };
   // the page copies do not depend on q_rot: queue the first STAGES of them, let the
   // merge grid be scheduled, then wait for rotate_q
@@ -740,6 +764,8 @@ __device__ __forceinline__ void bf16_item(const DevCache& c, int layer, const De
     if (m != -INFINITY) {
       for (int r = 0; r < PAGE; ++r) {
         const float p = sm.buf.bf.pw[0][h][r];
+        // rows outside the window (p = 0) may hold anything, NaN included: skip them
+        if (p == 0.0f) continue;
         const uint2 vv = reinterpret_cast<const uint2*>(&sm.buf.bf.v[r][0])[lane];
         acc[0] = fmaf(p, bf16lo(vv.x), acc[0]);
         acc[1] = fmaf(p, bf16hi(vv.x), acc[1]);
@@ -783,8 +809,10 @@ __global__ void __launch_bounds__(THREADS, Tune<G>::CTAS) decode_stream_kernel(D
   const int per_head = BF16_ITEMS + R.chunks;
   float* part = partials + ((size_t)R.part_start + (size_t)head * per_head + sub) * G * PART;
   if (sub < BF16_ITEMS) {
-    // BF16 pages read q and the cache only, both complete before rotate_q ran
+    // BF16 pages read q and the cache only: complete before rotate_q ran, or once a
+    // preceding fused append has completed
     grid_dep_launch();
+    if (a.front_writes) grid_dep_wait();
     const uint16_t* qrow = q + ((size_t)R.batch_row * c.Hq + (size_t)head * G) * D;
     const int t = threadIdx.x;
     uint16_t qv[G];
@@ -930,6 +958,43 @@ __global__ void __launch_bounds__(MERGE_THREADS) decode_merge_kernel(DevCache c,
   }
 }
 
+// ---- fused step front: the append of every request and the q rotation -----------
+// Blocks [0, 2 Hkv n_app): append of (request, kv head, K or V); the rest: q
+// rotation slabs of (request, kv head).  Both parts wait for the preceding grid
+// first; the stream kernel that follows reads the q operands through the ready
+// words and the pages this grid writes only after it has completed.
+struct FrontArgs {
+  unsigned long long epoch;
+  int n_app;
+  AppendReq app[APPEND_PER_LAUNCH];
+  int batch_row[APPEND_PER_LAUNCH];
+};
+constexpr int FRONT_THREADS = APPEND_THREADS;
+
+template <int G>
+__global__ void __launch_bounds__(FRONT_THREADS) step_front_kernel(DevCache c, int layer, FrontArgs f,
+                                                                   const uint16_t* __restrict__ k,
+                                                                   const uint16_t* __restrict__ v,
+                                                                   const uint16_t* __restrict__ q,
+                                                                   uint32_t* __restrict__ qfrag) {
+  __shared__ union {
+    AppendSmem app;
+    RotSmem<G, FRONT_THREADS> rot;
+  } sm;
+  const int app_blocks = f.n_app * c.Hkv * 2;
+  if ((int)blockIdx.x < app_blocks) {
+    const int b = blockIdx.x;
+    append_block(c, layer, k, v, f.app[b / (2 * c.Hkv)], (b / 2) % c.Hkv, b % 2, sm.app);   // waits inside
+    return;
+  }
+  const int b = blockIdx.x - app_blocks;
+  const int ri = b / (c.Hkv * SLABS), head = (b / SLABS) % c.Hkv, slab = b % SLABS;
+  grid_dep_wait();
+  grid_dep_launch();
+  rotate_block<G, FRONT_THREADS>(c, layer, f.epoch, f.batch_row[ri], head, slab, q,
+                                 qfrag + ((size_t)ri * c.Hkv + head) * QFrag<G>::WORDS, sm.rot);
+}
+
 // Dynamic shared memory opt-in, once per device and kernel.
 template <typename K>
 cudaError_t set_smem(K kernel, size_t bytes, unsigned& done_mask) {
@@ -943,28 +1008,30 @@ cudaError_t set_smem(K kernel, size_t bytes, unsigned& done_mask) {
   return e;
 }
 
+// Launch configuration with programmatic dependent launch on stream s.
+struct PdlLaunch {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = {};
+  explicit PdlLaunch(cudaStream_t s) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+};
+
+// The stream and merge kernels (after rotate_q or the fused front).
 template <int G>
-cudaError_t launch_g(const DevCache& c, int layer, const DecodeArgs& a, int items, const uint16_t* q, float* out,
-                     uint32_t* qfrag, float* partials, cudaStream_t s) {
+cudaError_t launch_stream_merge(const DevCache& c, int layer, const DecodeArgs& a, int items, const uint16_t* q,
+                                float* out, uint32_t* qfrag, float* partials, cudaStream_t s) {
   static unsigned stream_set = 0, merge_set = 0;
   const size_t smem = sizeof(Smem<G>);
   cudaError_t e = set_smem(decode_stream_kernel<G>, smem, stream_set);
   if (e == cudaSuccess) e = set_smem(decode_merge_kernel<G>, sizeof(MergeSmem), merge_set);
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute pdl[1];
-  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  pdl[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.stream = s;
-  cfg.attrs = pdl;
-  cfg.numAttrs = 1;
-
-  cfg.gridDim = dim3(static_cast<unsigned>(a.n * c.Hkv), SLABS);
-  cfg.blockDim = dim3(ROT_THREADS);
-  cfg.dynamicSmemBytes = 0;
-  e = cudaLaunchKernelEx(&cfg, rotate_q_kernel<G>, c, layer, a, q, qfrag);
-  if (e != cudaSuccess) return e;
-
+  PdlLaunch L(s);
+  cudaLaunchConfig_t& cfg = L.cfg;
   cfg.gridDim = dim3(static_cast<unsigned>(items));
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = smem;
@@ -978,16 +1045,45 @@ cudaError_t launch_g(const DevCache& c, int layer, const DecodeArgs& a, int item
   return cudaLaunchKernelEx(&cfg, decode_merge_kernel<G>, c, layer, a, static_cast<const float*>(partials), out);
 }
 
-}  // namespace
+template <int G>
+cudaError_t launch_g(const DevCache& c, int layer, const DecodeArgs& a, int items, const uint16_t* q, float* out,
+                     uint32_t* qfrag, float* partials, cudaStream_t s) {
+  PdlLaunch L(s);
+  L.cfg.gridDim = dim3(static_cast<unsigned>(a.n * c.Hkv), SLABS);
+  L.cfg.blockDim = dim3(ROT_THREADS);
+  const cudaError_t e = cudaLaunchKernelEx(&L.cfg, rotate_q_kernel<G>, c, layer, a, q, qfrag);
+  if (e != cudaSuccess) return e;
+  return launch_stream_merge<G>(c, layer, a, items, q, out, qfrag, partials, s);
+}
 
-cudaError_t launch_decode(const DevCache& c, int layer, const DecodeReq* reqs, const DecodePlan& plan,
-                          const uint16_t* q, float* out, void* workspace, uint64_t epoch, cudaStream_t s) {
+template <int G>
+cudaError_t launch_step_g(const DevCache& c, int layer, const FrontArgs& f, const uint16_t* k, const uint16_t* v,
+                          const DecodeArgs& a, int items, const uint16_t* q, float* out, uint32_t* qfrag,
+                          float* partials, cudaStream_t s) {
+  PdlLaunch L(s);
+  L.cfg.gridDim = dim3(static_cast<unsigned>(f.n_app * c.Hkv * 2 + a.n * c.Hkv * SLABS));
+  L.cfg.blockDim = dim3(FRONT_THREADS);
+  const cudaError_t e = cudaLaunchKernelEx(&L.cfg, step_front_kernel<G>, c, layer, f, k, v, q, qfrag);
+  if (e != cudaSuccess) return e;
+  return launch_stream_merge<G>(c, layer, a, items, q, out, qfrag, partials, s);
+}
+
+DecodeArgs make_args(const DecodeReq* reqs, const DecodePlan& plan, uint64_t epoch, int front_writes) {
   DecodeArgs a;
   a.epoch = epoch;
+  a.front_writes = front_writes;
   a.n = plan.n;
   a.pages_per_chunk = plan.pages_per_chunk;
   a.int2_items = plan.int2_items;
   for (int i = 0; i < plan.n; ++i) a.r[i] = reqs[i];
+  return a;
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DevCache& c, int layer, const DecodeReq* reqs, const DecodePlan& plan,
+                          const uint16_t* q, float* out, void* workspace, uint64_t epoch, cudaStream_t s) {
+  const DecodeArgs a = make_args(reqs, plan, epoch, 0);
   uint32_t* qfrag = static_cast<uint32_t*>(workspace);
   float* partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.qrot_bytes);
   switch (c.G) {
@@ -995,6 +1091,27 @@ cudaError_t launch_decode(const DevCache& c, int layer, const DecodeReq* reqs, c
     case 2: return launch_g<2>(c, layer, a, plan.total_items, q, out, qfrag, partials, s);
     case 4: return launch_g<4>(c, layer, a, plan.total_items, q, out, qfrag, partials, s);
     case 8: return launch_g<8>(c, layer, a, plan.total_items, q, out, qfrag, partials, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_step(const DevCache& c, int layer, const AppendReq* app, int n_app, const uint16_t* k,
+                        const uint16_t* v, const DecodeReq* reqs, const DecodePlan& plan, const uint16_t* q,
+                        float* out, void* workspace, uint64_t epoch, cudaStream_t s) {
+  if (n_app > APPEND_PER_LAUNCH || plan.n > APPEND_PER_LAUNCH) return cudaErrorInvalidValue;
+  const DecodeArgs a = make_args(reqs, plan, epoch, 1);
+  FrontArgs f;
+  f.epoch = epoch;
+  f.n_app = n_app;
+  for (int i = 0; i < n_app; ++i) f.app[i] = app[i];
+  for (int i = 0; i < plan.n; ++i) f.batch_row[i] = reqs[i].batch_row;
+  uint32_t* qfrag = static_cast<uint32_t*>(workspace);
+  float* partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.qrot_bytes);
+  switch (c.G) {
+    case 1: return launch_step_g<1>(c, layer, f, k, v, a, plan.total_items, q, out, qfrag, partials, s);
+    case 2: return launch_step_g<2>(c, layer, f, k, v, a, plan.total_items, q, out, qfrag, partials, s);
+    case 4: return launch_step_g<4>(c, layer, f, k, v, a, plan.total_items, q, out, qfrag, partials, s);
+    case 8: return launch_step_g<8>(c, layer, f, k, v, a, plan.total_items, q, out, qfrag, partials, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -428,8 +428,10 @@ oscar_status oscar_prefill_quantize(oscar_cache* c, int32_t req, int32_t layer, 
 namespace {
 
 // Shared by append and demote: validate a batch, then apply it.
-oscar_status write_batch(oscar_cache* c, int32_t layer, int32_t n, const int32_t* reqs, const uint16_t* k,
-                         const uint16_t* v, bool append, void* stream) {
+// Append / demote of a batch in two halves: every check first (no side effect),
+// then the page allocation and state update, which cannot fail.
+oscar_status validate_write(oscar_cache* c, int32_t layer, int32_t n, const int32_t* reqs, const uint16_t* k,
+                            const uint16_t* v, bool append) {
   if (!c) return OSCAR_ERR_INVALID_ARG;
   if (!c->valid_layer(layer) || n < 1 || !reqs) return c->fail(OSCAR_ERR_INVALID_ARG, "bad layer or batch");
   if (append && !c->dry && (!k || !v || !aligned16(k) || !aligned16(v)))
@@ -457,6 +459,10 @@ oscar_status write_batch(oscar_cache* c, int32_t layer, int32_t n, const int32_t
     }
   }
   if (fresh > c->int2.free_count()) return c->fail(OSCAR_ERR_OUT_OF_PAGES, "out of INT2 pages");
+  return OSCAR_OK;
+}
+
+std::vector<AppendReq> apply_write(oscar_cache* c, int32_t layer, int32_t n, const int32_t* reqs, bool append) {
   std::vector<AppendReq> work(n);
   for (int32_t i = 0; i < n; ++i) {
     Request& r = c->reqs[reqs[i]];
@@ -493,6 +499,14 @@ oscar_status write_batch(oscar_cache* c, int32_t layer, int32_t n, const int32_t
       r.T[layer] = T + 1;
     }
   }
+  return work;
+}
+
+oscar_status write_batch(oscar_cache* c, int32_t layer, int32_t n, const int32_t* reqs, const uint16_t* k,
+                         const uint16_t* v, bool append, void* stream) {
+  const oscar_status st = validate_write(c, layer, n, reqs, k, v, append);
+  if (st != OSCAR_OK) return st;
+  const std::vector<AppendReq> work = apply_write(c, layer, n, reqs, append);
   if (c->dry) return OSCAR_ERR_DRY_RUN;
   cudaError_t err = launch_append(c->dc, layer, work.data(), n, k, v, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? OSCAR_OK : c->cuda_fail(err, append ? "append launch" : "demote launch");
@@ -542,6 +556,7 @@ DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int
       d.int2_start = static_cast<int32_t>(int2);
       d.chunks = static_cast<int32_t>(chunks);
       d.part_start = static_cast<int32_t>(parts);
+      d.hot_page = -1;
     }
     int2 += H * chunks;
     parts += H * (DECODE_BF16_ITEMS + chunks);
@@ -647,6 +662,56 @@ oscar_status oscar_decode_attention_noalloc(oscar_cache* c, int32_t layer, int32
   const cudaError_t e = decode_scratch_address(&scratch, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return c->cuda_fail(e, "decode scratch set-up");
   return oscar_decode_attention(c, layer, n, reqs, q, out, scratch, DECODE_SCRATCH_BYTES, stream);
+}
+
+oscar_status oscar_decode_step(oscar_cache* c, int32_t layer, int32_t n, const int32_t* reqs, const uint16_t* k,
+                               const uint16_t* v, const uint16_t* q, float* out, void* workspace, size_t ws_bytes,
+                               void* stream) {
+  if (!c) return OSCAR_ERR_INVALID_ARG;
+  if (!c->dry && (!q || !out || !workspace || !aligned16(q) || !aligned16(out) ||
+                  (reinterpret_cast<uintptr_t>(workspace) & 255) != 0))
+    return c->fail(OSCAR_ERR_INVALID_ARG, "null or misaligned q / out / workspace");
+  oscar_status st = validate_write(c, layer, n, reqs, k, v, true);
+  if (st != OSCAR_OK) return st;
+  // smallest workspace the decode can run in after the append (every request with
+  // history gets one chunk per kv head), checked before anything changes
+  {
+    const int64_t H = c->cfg.num_kv_heads;
+    size_t need = 0;
+    for (int32_t b = 0; b < n; b += APPEND_PER_LAUNCH) {
+      const int32_t m = std::min<int32_t>(APPEND_PER_LAUNCH, n - b);
+      int64_t parts = 0;
+      for (int32_t i = b; i < b + m; ++i) {
+        const Request& r = c->reqs[reqs[i]];
+        const int64_t T = r.T[layer], he = r.he[layer];
+        const int64_t he_after = (T >= SINK && T - he == RECENT) ? he + 1 : he;
+        parts += H * (DECODE_BF16_ITEMS + (pages_for(he_after) > 0 ? 1 : 0));
+      }
+      need = std::max(need, align256((size_t)m * H * decode_qfrag_bytes(c->G())) +
+                                align256((size_t)parts * c->G() * PARTIAL_FLOATS * sizeof(float)));
+    }
+    if (!c->dry && need > ws_bytes) return c->fail(OSCAR_ERR_INVALID_ARG, "workspace too small");
+  }
+  const std::vector<AppendReq> work = apply_write(c, layer, n, reqs, true);
+  if (c->dry) return OSCAR_ERR_DRY_RUN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DecodeReq dr[DECODE_PER_LAUNCH];
+  for (int32_t b = 0; b < n; b += APPEND_PER_LAUNCH) {
+    const int32_t m = std::min<int32_t>(APPEND_PER_LAUNCH, n - b);
+    int64_t ppc_min = 0, max_pages = 1;
+    for (int32_t i = b; i < b + m; ++i) max_pages = std::max<int64_t>(max_pages, pages_for(c->reqs[reqs[i]].he[layer]));
+    while (decode_bytes_needed(c, layer, m, reqs + b, ppc_min) > ws_bytes && ppc_min < max_pages)
+      ppc_min = ppc_min ? 2 * ppc_min : 4;
+    const DecodePlan p = plan_decode(c, layer, m, reqs + b, b, ppc_min, dr);
+    for (int32_t i = 0; i < m; ++i) {
+      const AppendReq& a = work[b + i];
+      dr[i].hot_page = a.demote_slot >= 0 ? static_cast<int32_t>((c->reqs[reqs[b + i]].he[layer] - 1 - SINK) / PAGE) : -1;
+    }
+    const cudaError_t err = launch_step(c->dc, layer, work.data() + b, m, k, v, dr, p, q, out, workspace,
+                                        c->next_epoch(), s);
+    if (err != cudaSuccess) return c->cuda_fail(err, "decode step launch");
+  }
+  return OSCAR_OK;
 }
 
 oscar_status oscar_cache_check(oscar_cache* c, void* stream) {

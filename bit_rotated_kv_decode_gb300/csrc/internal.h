@@ -111,6 +111,7 @@ struct DecodeReq {
   int32_t int2_start;      // first INT2 work item (block) of this request
   int32_t chunks;          // INT2 chunks per kv head
   int32_t part_start;      // first partial slot: per kv head, 5 BF16 items then the chunks
+  int32_t hot_page;        // history page the preceding fused append writes (-1: none)
 };
 constexpr int DECODE_PER_LAUNCH = 64;
 constexpr int DECODE_BF16_ITEMS = 1 + RING_PAGES;   // BF16 work items per (request, kv head)
@@ -130,6 +131,12 @@ struct DecodePlan {
 // epoch: unique per launch (never repeated for any workspace the launch could use)
 cudaError_t launch_decode(const DevCache& c, int layer, const DecodeReq* reqs, const DecodePlan& plan,
                           const uint16_t* q, float* out, void* workspace, uint64_t epoch, cudaStream_t s);
+// Fused step of up to APPEND_PER_LAUNCH requests: one kernel runs the append of
+// every request and the q rotation, then the decode's stream and merge kernels;
+// reqs[i].hot_page names the history page the append writes.
+cudaError_t launch_step(const DevCache& c, int layer, const AppendReq* app, int n_app, const uint16_t* k,
+                        const uint16_t* v, const DecodeReq* reqs, const DecodePlan& plan, const uint16_t* q,
+                        float* out, void* workspace, uint64_t epoch, cudaStream_t s);
 
 // Fixed decode scratch (one static device array per device) for callers that
 // cannot allocate.  The first call on a device, with that device current,

@@ -216,6 +216,22 @@ oscar_status oscar_decode_attention(oscar_cache* cache, int32_t layer, int32_t n
 oscar_status oscar_decode_attention_noalloc(oscar_cache* cache, int32_t layer, int32_t n, const int32_t* reqs,
                                             const uint16_t* q, float* out, void* stream);
 
+/* One decode step of one layer: oscar_append(layer, n, reqs, k, v) followed by
+ * oscar_decode_attention(layer, n, reqs, q, out, workspace), with identical
+ * results, as fewer and overlapping launches: the append and the rotation of q
+ * run as one kernel, and the decode streams every history page the append does
+ * not touch while that kernel is still running ([MTP] section "The Serving
+ * System": the write path and decode attention of a step).
+ *   k, v       device bf16 [n][Hkv][128], the new token of each request.
+ *   q, out     as oscar_decode_attention.
+ *   workspace  device, >= oscar_decode_workspace_bytes() taken before the step
+ *              (it covers the page the append may add), 256-byte aligned.
+ * Every argument and state check (those of both calls, and a workspace too
+ * small for the decode after the append) is made before any change. */
+oscar_status oscar_decode_step(oscar_cache* cache, int32_t layer, int32_t n, const int32_t* reqs,
+                               const uint16_t* k, const uint16_t* v, const uint16_t* q, float* out,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
 /* Synchronise "stream" and report the sticky device error word (then clear it). */
 oscar_status oscar_cache_check(oscar_cache* cache, void* stream);
 

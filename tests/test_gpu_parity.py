@@ -252,3 +252,20 @@ def test_device_check_is_clean_after_all_calls(b):
     s.prefill(r, 0, 500)
     s.decode([r], 0)
     s.cache.check()
+
+
+def test_unwritten_rows_holding_nan_do_not_leak(b):
+    """Rows outside a request's window are never written; whatever they hold (here
+    NaN bit patterns in every pool byte) must not reach the output."""
+    s = Setup(b, max_req=3)
+    s.cache.int2_pool(0).fill_(-1)      # codes 3, fp16 scale / zero 0xffff (NaN)
+    s.cache.bf16_pool(0).fill_(-1)      # bf16 0xffff (NaN)
+    reqs = [s.open() for _ in range(3)]
+    for r, t in zip(reqs, (40, 300, 1000)):
+        s.prefill(r, 0, t)
+    s.append(reqs, 0, 0)
+    q, out = s.decode(reqs, 0)
+    got = out.cpu().numpy()
+    assert np.isfinite(got).all()
+    for i, r in enumerate(reqs):
+        parity.check_output(got[i], s.oracle_decode(r, 0, q[i]))

@@ -91,10 +91,16 @@ def test_random_call_sequence_matches_mirror(b, seed):
                     for r, (t, he, pt) in zip(batch, snapshot):
                         mir.reqs[r].T[layer], mir.reqs[r].hist_end[layer], mir.reqs[r].hist_pt = t, he, pt
                     mir.int2.stack, mir.int2.refs = free0
+                    # the fused decode step makes exactly the append's state changes
+                    call = (lambda: lib.step(layer, batch, None, None, None, None, None)) if op == 7 else \
+                        (lambda: lib.append(layer, batch, None, None))
                     with pytest.raises(b.OscarError):
-                        lib.append(layer, batch, None, None)
+                        call()
                     continue
-                lib.append(layer, batch, None, None)
+                if op == 7:
+                    lib.step(layer, batch, None, None, None, None, None)
+                else:
+                    lib.append(layer, batch, None, None)
             elif op == 8 and live:
                 r = live[int(rng.integers(len(live)))]
                 layer = int(rng.integers(2))
