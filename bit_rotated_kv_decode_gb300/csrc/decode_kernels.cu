@@ -237,8 +237,15 @@ __device__ __forceinline__ void rotate_block(const DevCache& c, int layer, unsig
 #pragma unroll
   for (int i = 0; i < ROWS; ++i) r[i] = __ldg(RK + (size_t)(ROWS * grp + i) * D);
   const uint16_t* qrow = q + ((size_t)batch_row * c.Hq + (size_t)head * G) * D;
-  for (int idx = t; idx < G * D; idx += NTH)
-    sm.qs[idx / D][idx % D] = __uint_as_float(static_cast<uint32_t>(__ldcg(qrow + idx)) << 16);
+  constexpr int QN = (G * D + NTH - 1) / NTH;   // q values per thread, all loads in flight
+  uint16_t qv[QN];
+#pragma unroll
+  for (int u = 0; u < QN; ++u) qv[u] = (u * NTH + t < G * D) ? __ldcg(qrow + u * NTH + t) : uint16_t(0);
+#pragma unroll
+  for (int u = 0; u < QN; ++u) {
+    const int idx = u * NTH + t;
+    if (idx < G * D) sm.qs[idx / D][idx % D] = __uint_as_float(static_cast<uint32_t>(qv[u]) << 16);
+  }
   __syncthreads();
   float* consts = reinterpret_cast<float*>(dst + QFrag<G>::CONSTS);
   for (int h = grp; h < G; h += RG) {
