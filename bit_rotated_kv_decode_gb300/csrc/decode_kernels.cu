@@ -694,7 +694,12 @@ __device__ __forceinline__ void bf16_item(const DevCache& c, int layer, const De
   const int warp = t >> 5, lane = t & 31;
   const float scale2 = c.scale * LOG2E;
   const int T = R.tokens, he = R.hist_end;
-  int page = which == 0 ? R.sink_page : R.ring_page[which - 1];
+  // select chain, not an indexed load: a dynamic index would put R in local memory
+  int page = which == 0 ? R.sink_page
+           : which == 1 ? R.ring_page[0]
+           : which == 2 ? R.ring_page[1]
+           : which == 3 ? R.ring_page[2]
+                        : R.ring_page[3];
   if (page < 0 || page >= c.n_bf16_pages) {
     if (t == 0) atomicOr(c.err, ERR_BF16_PAGE);
     page = 0;

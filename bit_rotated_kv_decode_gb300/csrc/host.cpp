@@ -518,8 +518,9 @@ oscar_status write_batch(oscar_cache* c, int32_t layer, int32_t n, const int32_t
 // wave of resident blocks.
 int64_t chunks_for(int64_t np, int64_t ppc) { return np == 0 ? 0 : (np + ppc - 1) / ppc; }
 
+// reserve: resident stream-block slots taken by a kernel still running beside it
 DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int32_t* reqs, int32_t first_row,
-                       int64_t ppc_min, DecodeReq* out) {
+                       int64_t ppc_min, DecodeReq* out, int64_t reserve = 0) {
   const int64_t H = c->cfg.num_kv_heads;
   int64_t total_pages = 0, max_np = 0;
   for (int32_t i = 0; i < n; ++i) {
@@ -527,7 +528,7 @@ DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int
     total_pages += H * np;
     max_np = std::max(max_np, np);
   }
-  const int64_t target = std::max<int64_t>(1, (int64_t)c->num_sms * decode_ctas_per_sm(c->G()));
+  const int64_t target = std::max<int64_t>(1, (int64_t)c->num_sms * decode_ctas_per_sm(c->G()) - reserve);
   const int64_t bf16 = (int64_t)DECODE_BF16_ITEMS * n * H;
   const int64_t budget = std::max<int64_t>(n * H, target - bf16);
   int64_t ppc = std::max<int64_t>({ppc_min, 2, (total_pages + budget - 1) / budget,
@@ -702,7 +703,11 @@ oscar_status oscar_decode_step(oscar_cache* c, int32_t layer, int32_t n, const i
     for (int32_t i = b; i < b + m; ++i) max_pages = std::max<int64_t>(max_pages, pages_for(c->reqs[reqs[i]].he[layer]));
     while (decode_bytes_needed(c, layer, m, reqs + b, ppc_min) > ws_bytes && ppc_min < max_pages)
       ppc_min = ppc_min ? 2 * ppc_min : 4;
-    const DecodePlan p = plan_decode(c, layer, m, reqs + b, b, ppc_min, dr);
+    // each append block of the front kernel (256 threads) displaces two stream blocks
+    // until it ends; leaving their slots out keeps every stream block starting at once
+    const int64_t slots = (int64_t)c->num_sms * decode_ctas_per_sm(c->G());
+    const int64_t reserve = std::min<int64_t>(2 * (int64_t)m * c->cfg.num_kv_heads * 2, slots / 4);
+    const DecodePlan p = plan_decode(c, layer, m, reqs + b, b, ppc_min, dr, reserve);
     for (int32_t i = 0; i < m; ++i) {
       const AppendReq& a = work[b + i];
       dr[i].hot_page = a.demote_slot >= 0 ? static_cast<int32_t>((c->reqs[reqs[b + i]].he[layer] - 1 - SINK) / PAGE) : -1;
