@@ -38,10 +38,12 @@ def rotations(cfg_id, layers, hq, hkv, drift=False):
 
 
 class Setup:
-    def __init__(self, b, cfg_id=0, layers=1, hq=32, hkv=8, max_req=4, max_pages=64, pages=256, seed=0):
+    def __init__(self, b, cfg_id=0, layers=1, hq=32, hkv=8, max_req=4, max_pages=64, pages=256, seed=0,
+                 drift=False, total_len=0):
         self.b = b
         self.cfg_id, self.L, self.hq, self.hkv = cfg_id, layers, hq, hkv
-        self.rk, self.rv, self.tk, self.tv = rotations(cfg_id, layers, hq, hkv)
+        self.drift, self.total_len = drift, total_len
+        self.rk, self.rv, self.tk, self.tv = rotations(cfg_id, layers, hq, hkv, drift)
         cfg = b.make_config(layers, hq, hkv, max_req, max_pages, pages, 0, 0.0, seed)
         self.cache = b.OscarCache(cfg, torch.from_numpy(self.rk).cuda(), torch.from_numpy(self.rv).cuda(),
                                   self.tk, self.tv)
@@ -49,10 +51,10 @@ class Setup:
         self.tokens = {}   # (req, layer) -> (k, v) device bf16 [T][Hkv][128]
 
     def kv(self, layer, start, n, stream_id):
-        k = synth.kv_tokens(self.cfg_id, layer, self.hkv, "k", range(start, start + n), device="cuda",
-                            stream_id=stream_id)
-        v = synth.kv_tokens(self.cfg_id, layer, self.hkv, "v", range(start, start + n), device="cuda",
-                            stream_id=stream_id)
+        k = synth.kv_tokens(self.cfg_id, layer, self.hkv, "k", range(start, start + n), total_len=self.total_len,
+                            drift=self.drift, device="cuda", stream_id=stream_id)
+        v = synth.kv_tokens(self.cfg_id, layer, self.hkv, "v", range(start, start + n), total_len=self.total_len,
+                            drift=self.drift, device="cuda", stream_id=stream_id)
         return k, v
 
     def open(self):
