@@ -34,7 +34,11 @@ INT2_BYTES_PER_TOKEN_HEAD = 72          # 2 x (32 code bytes + 4 meta bytes)
 BF16_BYTES_PER_TOKEN_HEAD = 512         # K and V rows of 128 bf16
 
 WORKLOADS = {
+    1: dict(name="qwen3-8b-32k-prefill-and-demote", layers=32, q_heads=32, kv_heads=8, batch=1, context=32768,
+            write_path=True),
     2: dict(name="qwen3-8b-100k-decode", layers=32, q_heads=32, kv_heads=8, batch=1, context=100000),
+    3: dict(name="qwen3-4b-b32-16k-64k-shared-4k-prefix-decode", layers=36, q_heads=32, kv_heads=8, batch=32,
+            context=(16384, 65536), prefix=4096),
     4: dict(name="qwen3-32b-128k-b8-decode", layers=64, q_heads=64, kv_heads=8, batch=8, context=131072),
 }
 
@@ -166,8 +170,15 @@ class Workload:
         w = WORKLOADS[cfg_id]
         self.cfg_id = cfg_id
         self.w = w
-        self.L, self.hq, self.hkv, self.batch, self.T0 = (w["layers"], w["q_heads"], w["kv_heads"], w["batch"],
-                                                        w["context"])
+        self.L, self.hq, self.hkv, self.batch = w["layers"], w["q_heads"], w["kv_heads"], w["batch"]
+        if isinstance(w["context"], tuple):
+            self.lens = synth.request_lengths(cfg_id, self.batch, *w["context"])
+        else:
+            self.lens = [w["context"]] * self.batch
+        self.T0 = max(self.lens)
+        self.prefix = w.get("prefix", 0)
+        # generator stream of each request's own tokens (0 holds a shared prefix)
+        self.sid = [1 + i if self.prefix else i for i in range(self.batch)]
         if layers:
             self.L = layers
         self.drift = cfg_id == 4
@@ -177,21 +188,36 @@ class Workload:
                                                                        drift=self.drift, layers=fit)
         log(f"calibration {time.time() - t:.1f}s")
         max_pages = pages_for(self.T0 + steps_total + 64) + 1
+        n_pages = sum(pages_for(t + steps_total + 64) + 1 for t in self.lens) + 8
         seed = synth.seed_for(cfg_id, 0, 0, 99) or 1
-        cfg = binding.make_config(self.L, self.hq, self.hkv, self.batch, max_pages, self.batch * max_pages + 8,
-                                  0, 0.0, seed)
+        cfg = binding.make_config(self.L, self.hq, self.hkv, self.batch + (1 if self.prefix else 0), max_pages,
+                                  n_pages, 0, 0.0, seed)
         self.cache = binding.OscarCache(cfg, torch.from_numpy(self.rk).cuda(), torch.from_numpy(self.rv).cuda(),
                                         self.tk, self.tv)
-        self.reqs = [self.cache.open() for _ in range(self.batch)]
         t = time.time()
-        for layer in range(self.L):
-            for i, r in enumerate(self.reqs):
-                k = synth.kv_tokens(cfg_id, layer, self.hkv, "k", range(0, self.T0), total_len=self.T0,
-                                    drift=self.drift, device="cuda", stream_id=i)
-                v = synth.kv_tokens(cfg_id, layer, self.hkv, "v", range(0, self.T0), total_len=self.T0,
-                                    drift=self.drift, device="cuda", stream_id=i)
-                self.cache.prefill(r, layer, k, v)
-                del k, v
+
+        def fill(r, layer, p0, p1, sid, total):
+            k = synth.kv_tokens(cfg_id, layer, self.hkv, "k", range(p0, p1), total_len=total, drift=self.drift,
+                                device="cuda", stream_id=sid)
+            v = synth.kv_tokens(cfg_id, layer, self.hkv, "v", range(p0, p1), total_len=total, drift=self.drift,
+                                device="cuda", stream_id=sid)
+            self.cache.prefill(r, layer, k, v)
+
+        if self.prefix:
+            # one parent holds the shared prefix (demoted in every layer); each request forks it
+            parent = self.cache.open()
+            for layer in range(self.L):
+                fill(parent, layer, 0, self.prefix + 256, 0, self.prefix + 256)
+            self.reqs = [self.cache.fork(parent, self.prefix) for _ in range(self.batch)]
+            self.cache.close(parent)
+            for layer in range(self.L):
+                for i, r in enumerate(self.reqs):
+                    fill(r, layer, self.prefix, self.lens[i], self.sid[i], self.lens[i])
+        else:
+            self.reqs = [self.cache.open() for _ in range(self.batch)]
+            for layer in range(self.L):
+                for i, r in enumerate(self.reqs):
+                    fill(r, layer, 0, self.lens[i], self.sid[i], self.lens[i])
         torch.cuda.synchronize()
         self.cache.check()
         log(f"prefill {time.time() - t:.1f}s")
@@ -203,12 +229,13 @@ class Workload:
         for layer in range(self.L):
             mix = synth.query_mix(cfg_id, layer, self.hq, device="cuda")
             for i in range(self.batch):
-                self.k_new[:, layer, i] = synth.kv_tokens(cfg_id, layer, self.hkv, "k", range(self.T0, self.T0 + n),
-                                                          total_len=self.T0, drift=self.drift, device="cuda",
-                                                          stream_id=i)
-                self.v_new[:, layer, i] = synth.kv_tokens(cfg_id, layer, self.hkv, "v", range(self.T0, self.T0 + n),
-                                                          total_len=self.T0, drift=self.drift, device="cuda",
-                                                          stream_id=i)
+                t0 = self.lens[i]
+                self.k_new[:, layer, i] = synth.kv_tokens(cfg_id, layer, self.hkv, "k", range(t0, t0 + n),
+                                                          total_len=t0, drift=self.drift, device="cuda",
+                                                          stream_id=self.sid[i])
+                self.v_new[:, layer, i] = synth.kv_tokens(cfg_id, layer, self.hkv, "v", range(t0, t0 + n),
+                                                          total_len=t0, drift=self.drift, device="cuda",
+                                                          stream_id=self.sid[i])
             for s in range(n):
                 self.q[s, layer] = synth.queries(cfg_id, layer, self.hq, self.batch, s, device="cuda", mix=mix)
         self.out = torch.empty((self.L, self.batch, self.hq, 128), dtype=torch.float32, device="cuda")
@@ -254,11 +281,14 @@ class Workload:
             if st:
                 raise RuntimeError(f"step failed: {lib.oscar_last_error(h).decode()}")
 
-    def decode_bytes(self, layer: int) -> int:
+    def decode_bytes(self, layer: int, unique: bool = True) -> int:
+        """Algorithmic bytes of one layer's decode; history pages of a shared prefix count once."""
         tot = 0
         for r in self.reqs:
             t, he = self.cache.length(r, layer)
             tot += algorithmic_bytes(t, he, self.hkv)
+        if unique and self.prefix:
+            tot -= (self.batch - 1) * (self.prefix - 64) * self.hkv * INT2_BYTES_PER_TOKEN_HEAD
         return tot
 
 
@@ -345,20 +375,131 @@ def run_gpu(args, log):
 
 
 # ----------------------------------------------------------------------------------------------
+PREFILL_FLOP_PER_TOKEN_HEAD = 2 * 2 * 128 * 128      # K and V rotation, one FMA = 2 flops
+FP32_PEAK_TFLOPS_DERIVED = 152 * 128 * 2 * 2.07e9 / 1e12   # SMs x FP32 lanes x 2 flops x max SM clock
+
+
+def run_write(args, log):
+    """Qwen3-8B write path: prefill-quantize of a 32768-token prompt per layer, then
+    single-token appends (each demoting the oldest recent token) for every layer."""
+    import torch
+    from bit_rotated_kv_decode_gb300 import binding, build, calibrate, synth
+    build.build()
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    w = WORKLOADS[args.config]
+    L = args.layers or w["layers"]
+    hq, hkv, T = w["q_heads"], w["kv_heads"], w["context"]
+    W, K = args.warmup, args.steps
+    n_app = W + K + 4
+    rk, rv, tk, tv = calibrate.calibrate_model(args.config, L, hq, hkv)
+    max_pages = pages_for(T + n_app + 64) + 1
+    cfg = binding.make_config(L, hq, hkv, 1, max_pages, max_pages + 8, 0, 0.0, synth.seed_for(args.config, 0, 0, 99) or 1)
+    cache = binding.OscarCache(cfg, torch.from_numpy(rk).cuda(), torch.from_numpy(rv).cuda(), tk, tv)
+    r = cache.open()
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    pre_us = []
+    for layer in range(L):
+        k = synth.kv_tokens(args.config, layer, hkv, "k", range(0, T), device="cuda")
+        v = synth.kv_tokens(args.config, layer, hkv, "v", range(0, T), device="cuda")
+        torch.cuda.synchronize()
+        a, b = mk(), mk()
+        a.record()
+        cache.prefill(r, layer, k, v)
+        b.record()
+        torch.cuda.synchronize()
+        pre_us.append(1000.0 * a.elapsed_time(b))
+        del k, v
+    cache.check()
+    kn = torch.stack([synth.kv_tokens(args.config, l, hkv, "k", range(T, T + n_app), device="cuda", stream_id=7)
+                      for l in range(L)], 1)            # [step][layer][Hkv][128]
+    vn = torch.stack([synth.kv_tokens(args.config, l, hkv, "v", range(T, T + n_app), device="cuda", stream_id=7)
+                      for l in range(L)], 1)
+    lib, h = cache.lib, cache.h
+    ra = (ctypes.c_int32 * 1)(r)
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def step(s):
+        for layer in range(L):
+            if lib.oscar_append(h, layer, 1, ra, kn[s, layer].data_ptr(), vn[s, layer].data_ptr(), stream):
+                raise RuntimeError(lib.oscar_last_error(h).decode())
+
+    for s in range(W):
+        step(s)
+    torch.cuda.synchronize()
+    a, b = mk(), mk()
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        a.record()
+        for s in range(W, W + K):
+            step(s)
+        b.record()
+        torch.cuda.synchronize()
+        barrier(world)
+    cache.check()
+    ms = max_over_ranks(a.elapsed_time(b), world)
+    tok_s = world * K * L / (ms * 1e-3)
+    # end to end: each step's new k / v copied from pinned host memory, the error word read back
+    khost, vhost = kn[W + K:].cpu().pin_memory(), vn[W + K:].cpu().pin_memory()
+    e0, e1 = mk(), mk()
+    torch.cuda.synchronize()
+    e0.record()
+    for i in range(khost.shape[0]):
+        kn[W + K + i].copy_(khost[i], non_blocking=True)
+        vn[W + K + i].copy_(vhost[i], non_blocking=True)
+        step(W + K + i)
+    e1.record()
+    cache.check()
+    e2e_tok_s = khost.shape[0] * L / (e0.elapsed_time(e1) * 1e-3)
+    pre_avg = float(np.mean(pre_us[1:] if len(pre_us) > 1 else pre_us))
+    flops = (T - 320) * hkv * PREFILL_FLOP_PER_TOKEN_HEAD
+    achieved = flops / (pre_avg * 1e-6) / 1e12
+    pre_bytes = T * hkv * 512 + (T - 320) * hkv * INT2_BYTES_PER_TOKEN_HEAD + 320 * hkv * 512
+    return {
+        "metric": METRIC, "value": tok_s, "unit": "demoted tok/s (tokens x layers / s)", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
+        "config": {"workload": w["name"], "layers": L, "kv_heads": hkv, "head_dim": 128, "batch": 1, "context": T,
+                   "step": "one oscar_append per layer (each demotes the oldest recent token)",
+                   "l2": "prefill reads %.0f MB per layer from inputs larger than L2; appends touch a few KB"
+                         % (pre_bytes / 1e6)},
+        "prefill_us_per_layer": pre_avg,
+        "prefill_gbs": pre_bytes / (pre_avg * 1e-6) / 1e9,
+        "roofline": {"bound": "alu", "kernel": "prefill_hist_kernel (rotation as an fp32 FMA chain)",
+                     "achieved": achieved, "peak": FP32_PEAK_TFLOPS_DERIVED, "unit": "TFLOP/s",
+                     "frac": achieved / FP32_PEAK_TFLOPS_DERIVED,
+                     "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz", "traffic": None},
+        "e2e": {"value": e2e_tok_s, "unit": "demoted tok/s (tokens x layers / s)",
+                "h2d_bytes_per_step": (kn[0].numel() + vn[0].numel()) * 2, "d2h_bytes_per_step": 4},
+        "gpu_launches": K * L,
+        "clocks": clk.summary(),
+    }
+
+
+# ----------------------------------------------------------------------------------------------
 def oracle_inputs(wl, layer: int):
     """Host float64 K / V of request 0 of one layer at the cache's current state."""
     import torch
     hkv = wl.hkv
     r = wl.reqs[0]
     t, he = wl.cache.length(r, layer)
-    n_new = t - wl.T0
-    k0 = wl.synth.kv_tokens(wl.cfg_id, layer, hkv, "k", range(0, wl.T0), total_len=wl.T0, drift=wl.drift,
-                            device="cuda", stream_id=0)
-    v0 = wl.synth.kv_tokens(wl.cfg_id, layer, hkv, "v", range(0, wl.T0), total_len=wl.T0, drift=wl.drift,
-                            device="cuda", stream_id=0)
-    k = torch.cat([k0, wl.k_new[:n_new, layer, 0]]).float().cpu().numpy().astype(np.float64)
-    v = torch.cat([v0, wl.v_new[:n_new, layer, 0]]).float().cpu().numpy().astype(np.float64)
-    del k0, v0
+    t0 = wl.lens[0]
+    n_new = t - t0
+    parts_k, parts_v = [], []
+    if wl.prefix:
+        gen = lambda which: wl.synth.kv_tokens(wl.cfg_id, layer, hkv, which, range(0, wl.prefix + 256),  # noqa: E731
+                                               total_len=wl.prefix + 256, drift=wl.drift, device="cuda",
+                                               stream_id=0)[:wl.prefix]
+        parts_k.append(gen("k"))
+        parts_v.append(gen("v"))
+    p0 = wl.prefix
+    parts_k.append(wl.synth.kv_tokens(wl.cfg_id, layer, hkv, "k", range(p0, t0), total_len=t0, drift=wl.drift,
+                                      device="cuda", stream_id=wl.sid[0]))
+    parts_v.append(wl.synth.kv_tokens(wl.cfg_id, layer, hkv, "v", range(p0, t0), total_len=t0, drift=wl.drift,
+                                      device="cuda", stream_id=wl.sid[0]))
+    k = torch.cat(parts_k + [wl.k_new[:n_new, layer, 0]]).float().cpu().numpy().astype(np.float64)
+    v = torch.cat(parts_v + [wl.v_new[:n_new, layer, 0]]).float().cpu().numpy().astype(np.float64)
     return k, v, t, he
 
 
@@ -457,8 +598,13 @@ def main(argv=None):
         if line is not None:
             print(json.dumps(line), flush=True)
         return
-    wl, r = run_gpu(args, log)
     w = WORKLOADS[args.config]
+    if w.get("write_path"):
+        line = run_write(args, log)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
+    wl, r = run_gpu(args, log)
     cpu = par = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu, par = cpu_baseline(wl, r, log)
@@ -478,7 +624,10 @@ def main(argv=None):
         "dtype": "fp32",
         "data": "synthetic",
         "config": {"workload": w["name"], "layers": wl.L, "q_heads": wl.hq, "kv_heads": wl.hkv, "head_dim": 128,
-                   "batch": wl.batch, "context": wl.T0, "page_tokens": 64, "page_order": "seeded shuffle",
+                   "batch": wl.batch,
+                   "context": wl.T0 if len(set(wl.lens)) == 1 else "%d..%d (mean %d)" % (
+                       min(wl.lens), max(wl.lens), int(np.mean(wl.lens))),
+                   "shared_prefix_tokens": wl.prefix, "page_tokens": 64, "page_order": "seeded shuffle",
                    "storage": "INT2 codes + fp16 scale/zero history, BF16 sink/recent",
                    "step": ("per layer: oscar_decode_step (append with fused demote, then decode attention)"
                             if not args.separate_calls else
@@ -487,6 +636,7 @@ def main(argv=None):
                        r["bytes_per_launch"] * wl.L / 1e9),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "kv_gbs_step": kv_gbs,
+        "decode_bytes_per_layer_logical": wl.decode_bytes(0, unique=False),
         "kv_frac_of_8tbs_step": kv_gbs / NOMINAL_HBM_GBS,
         "decode_us_per_layer": r["dec_avg_us"],
         "append_us_per_layer": r["app_avg_us"],

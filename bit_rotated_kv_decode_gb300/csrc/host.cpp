@@ -530,7 +530,9 @@ DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int
   }
   const int64_t target = std::max<int64_t>(1, (int64_t)c->num_sms * decode_ctas_per_sm(c->G()) - reserve);
   const int64_t bf16 = (int64_t)DECODE_BF16_ITEMS * n * H;
-  const int64_t budget = std::max<int64_t>(n * H, target - bf16);
+  // the BF16 items are short: they share the first wave when few (one request), and
+  // otherwise follow the INT2 blocks rather than shrinking the INT2 split
+  const int64_t budget = std::max<int64_t>(n * H, target - std::min<int64_t>(bf16, target / 8));
   int64_t ppc = std::max<int64_t>({ppc_min, 2, (total_pages + budget - 1) / budget,
                                    (max_np + MAX_CHUNKS_PER_HEAD - 1) / MAX_CHUNKS_PER_HEAD});
   for (;;) {
@@ -705,8 +707,10 @@ oscar_status oscar_decode_step(oscar_cache* c, int32_t layer, int32_t n, const i
       ppc_min = ppc_min ? 2 * ppc_min : 4;
     // each append block of the front kernel (256 threads) displaces two stream blocks
     // until it ends; leaving their slots out keeps every stream block starting at once
+    // (a large batch's front kernel is over before it matters: no reservation)
     const int64_t slots = (int64_t)c->num_sms * decode_ctas_per_sm(c->G());
-    const int64_t reserve = std::min<int64_t>(2 * (int64_t)m * c->cfg.num_kv_heads * 2, slots / 4);
+    const int64_t app_blocks = (int64_t)m * c->cfg.num_kv_heads * 2;
+    const int64_t reserve = 2 * app_blocks <= slots / 8 ? 2 * app_blocks : 0;
     const DecodePlan p = plan_decode(c, layer, m, reqs + b, b, ppc_min, dr, reserve);
     for (int32_t i = 0; i < m; ++i) {
       const AppendReq& a = work[b + i];
