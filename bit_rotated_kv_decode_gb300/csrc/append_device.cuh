@@ -92,7 +92,7 @@ __device__ __forceinline__ void append_block(const DevCache& c, int layer, const
       reinterpret_cast<float4*>(apart[grp])[lane] = make_float4(aac[0], aac[1], aac[2], aac[3]);
       __syncthreads();
       if (grp == 0) {
-        float x[4], e[4];
+        float x[4], e[4], sabs[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           float sum = part[0][4 * lane + j], asum = apart[0][4 * lane + j];
@@ -103,12 +103,13 @@ __device__ __forceinline__ void append_block(const DevCache& c, int layer, const
           }
           x[j] = sum;
           e[j] = __fmul_ru(gamma_n(APPEND_ROWS + APPEND_GROUPS), asum);
+          sabs[j] = __fmul_ru(asum, 1.0001f);   // >= sum_i |k_i R_ic| (asum is accumulated rounding up)
         }
         const float tau = (which ? c.tau_v : c.tau_k)[lh];
         const float* __restrict__ Rt = (which ? c.rot_vt : c.rot_kt) + lh * D * D;
         const float4 k4 = make_float4(xin[4 * lane], xin[4 * lane + 1], xin[4 * lane + 2], xin[4 * lane + 3]);
         const GroupCode g = quantize_group_warp(make_float4(x[0], x[1], x[2], x[3]), make_float4(e[0], e[1], e[2], e[3]),
-                                                tau, k4, Rt);
+                                                make_float4(sabs[0], sabs[1], sabs[2], sabs[3]), tau, k4, Rt);
         uint8_t* rec = int2_record(c, layer, q.hist_page, head);
         rec[(which ? V_CODES_OFF : K_CODES_OFF) + q.demote_slot * CODE_BYTES + lane] = static_cast<uint8_t>(g.byte);
         if (lane == 0) {

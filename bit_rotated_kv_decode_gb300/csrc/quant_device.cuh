@@ -20,7 +20,9 @@
 // compensated (TwoSum) double-precision dot product -- each bf16 x fp32 product
 // is exact in double -- rounded once to fp32.  That result equals
 // fp32_rn(k . R) unless the exact value lies within ~2^-90 sum|k_i R_ij| of an
-// fp32 rounding midpoint.
+// fp32 rounding midpoint.  Before that, an undecided value is narrowed by a
+// compensated fp32 dot product (Dot2) with a rigorous bound; the fp64 path runs
+// only if the narrow interval still leaves the decision open.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -96,15 +98,58 @@ __device__ __forceinline__ float warp_exact_dot(float4 k, float4 r) {
   return f;
 }
 
+__device__ __forceinline__ void two_sum_f(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// Compensated fp32 dot product over the same 128 terms as warp_exact_dot
+// (Ogita, Rump and Oishi's Dot2): each product is split exactly into
+// p + q with an FMA, the p are added by error-free TwoSum steps (lane, then a
+// butterfly across the warp) and every error term is accumulated in c.  s + c
+// differs from the exact sum by at most gamma_16 * 9 u * S <= 144 u^2 S, with
+// S >= sum_i |k_i r_i| (16 = deepest chain of additions into c, 9 u S = bound on
+// the error terms' magnitudes).  Returns fp32 bounds lo <= exact <= hi, widened
+// by 2^-36 S (a 28x margin) and rounded outwards; fp32_rn(exact) lies in
+// [lo, hi] since rounding is monotone.
+__device__ __forceinline__ void warp_dot2(float4 k, float4 r, float S, float& lo, float& hi) {
+  const float kk[4] = {k.x, k.y, k.z, k.w}, rr[4] = {r.x, r.y, r.z, r.w};
+  float s = __fmul_rn(kk[0], rr[0]);
+  float c = __fmaf_rn(kk[0], rr[0], -s);
+#pragma unroll
+  for (int i = 1; i < 4; ++i) {
+    const float p = __fmul_rn(kk[i], rr[i]);
+    const float q = __fmaf_rn(kk[i], rr[i], -p);
+    float t;
+    two_sum_f(s, p, s, t);
+    c = __fadd_rn(c, __fadd_rn(t, q));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+    const float c2 = __shfl_xor_sync(0xffffffffu, c, off);
+    float t;
+    two_sum_f(s, s2, s, t);
+    c = __fadd_rn(c, __fadd_rn(c2, t));
+  }
+  const float E = __fmul_ru(S, 0x1p-36f);
+  lo = __fsub_rd(__fadd_rd(s, c), E);
+  hi = __fadd_ru(__fadd_ru(s, c), E);
+}
+
 // A full warp holds the group: lane l owns channels 4l .. 4l+3 with rotated
-// values x (fast path) and error bounds err; k holds the token's input
-// channels 4l .. 4l+3 and rt points at R^T (row ch = column ch of R), so the
-// exact value of channel ch is warp_exact_dot(k, rt[ch][4l .. 4l+3]).
-__device__ __forceinline__ GroupCode quantize_group_warp(float4 xv, float4 ev, float tau, float4 k,
+// values x (fast path), their error bounds ev and S >= sum_i |k_i R_i,ch| (sv);
+// k holds the token's input channels 4l .. 4l+3 and rt points at R^T (row ch =
+// column ch of R).  A value whose interval leaves a decision open is narrowed
+// first by warp_dot2 (cheap, fp32) and only then, if still open, computed
+// exactly by warp_exact_dot (fp64).
+__device__ __forceinline__ GroupCode quantize_group_warp(float4 xv, float4 ev, float4 sv, float tau, float4 k,
                                                          const float* __restrict__ rt) {
   const int lane = threadIdx.x & 31;
   const float x[4] = {xv.x, xv.y, xv.z, xv.w};
   const float er[4] = {ev.x, ev.y, ev.z, ev.w};
+  const float sb[4] = {sv.x, sv.y, sv.z, sv.w};
   float lo[4], hi[4];
   GroupCode g;
   g.exact_calls = 0;
@@ -128,28 +173,71 @@ __device__ __forceinline__ GroupCode quantize_group_warp(float4 xv, float4 ev, f
     const float4 r = __ldg(reinterpret_cast<const float4*>(rt + (size_t)ch * D) + lane);
     return warp_exact_dot(k, r);
   };
+  // value (src, i) narrowed by warp_dot2, clipped: every lane computes, lane src keeps
+  auto narrow = [&](int src, int i, float& nlo, float& nhi) {
+    const float4 r = __ldg(reinterpret_cast<const float4*>(rt + (size_t)(4 * src + i) * D) + lane);
+    // select, not an indexed load (which would put sb in local memory)
+    const float own = i == 0 ? sb[0] : i == 1 ? sb[1] : i == 2 ? sb[2] : sb[3];
+    const float S = __shfl_sync(0xffffffffu, own, src);
+    warp_dot2(k, r, S, nlo, nhi);
+    nlo = clip_canon(nlo, tau);
+    nhi = clip_canon(nhi, tau);
+  };
   float mn_lo = reduce_min(fminf(fminf(lo[0], lo[1]), fminf(lo[2], lo[3])));
   float mn_hi = reduce_min(fminf(fminf(hi[0], hi[1]), fminf(hi[2], hi[3])));
   float mx_lo = reduce_max(fmaxf(fmaxf(lo[0], lo[1]), fmaxf(lo[2], lo[3])));
   float mx_hi = reduce_max(fmaxf(fmaxf(hi[0], hi[1]), fmaxf(hi[2], hi[3])));
-  const bool meta_sure = __half_as_ushort(__float2half_rn(mn_lo)) == __half_as_ushort(__float2half_rn(mn_hi)) &&
-                         scale_of(mx_lo, mn_hi) == scale_of(mx_hi, mn_lo);
+  bool meta_sure = __half_as_ushort(__float2half_rn(mn_lo)) == __half_as_ushort(__float2half_rn(mn_hi)) &&
+                   scale_of(mx_lo, mn_hi) == scale_of(mx_hi, mn_lo);
   if (!meta_sure) {
-    // (warp-uniform, rare) the group's min or max is too close to an fp16
-    // rounding boundary: take exactly every value that could be the min (its
-    // interval reaches below mn_hi) or the max (reaches above mx_lo).  The
+    // (warp-uniform) the group's min or max is too close to an fp16 rounding
+    // boundary: narrow every value that could be the min (its interval reaches
+    // below mn_hi) or the max (reaches above mx_lo) and is not already a single
+    // point (a clipped value is); then decide again.
+    uint32_t cand = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (lo[i] != hi[i] && (lo[i] <= mn_hi || hi[i] >= mx_lo)) cand |= 1u << i;
+    uint32_t todo = __ballot_sync(0xffffffffu, cand != 0);
+    while (todo) {
+      const int src = __ffs(todo) - 1;
+      const int i = __ffs(__shfl_sync(0xffffffffu, cand, src)) - 1;
+      float nlo, nhi;
+      narrow(src, i, nlo, nhi);
+      if (lane == src) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (j == i) {
+            lo[j] = nlo;
+            hi[j] = nhi;
+          }
+        cand &= ~(1u << i);
+      }
+      todo = __ballot_sync(0xffffffffu, cand != 0);
+    }
+    mn_lo = reduce_min(fminf(fminf(lo[0], lo[1]), fminf(lo[2], lo[3])));
+    mn_hi = reduce_min(fminf(fminf(hi[0], hi[1]), fminf(hi[2], hi[3])));
+    mx_lo = reduce_max(fmaxf(fmaxf(lo[0], lo[1]), fmaxf(lo[2], lo[3])));
+    mx_hi = reduce_max(fmaxf(fmaxf(hi[0], hi[1]), fmaxf(hi[2], hi[3])));
+    meta_sure = __half_as_ushort(__float2half_rn(mn_lo)) == __half_as_ushort(__float2half_rn(mn_hi)) &&
+                scale_of(mx_lo, mn_hi) == scale_of(mx_hi, mn_lo);
+  }
+  if (!meta_sure) {
+    // (rare) still open: take exactly every candidate of the min or the max.  The
     // others lie strictly inside, so the extremes become exact.
     uint32_t cand = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      if (lo[i] <= mn_hi || hi[i] >= mx_lo) cand |= 1u << i;
+      if (lo[i] != hi[i] && (lo[i] <= mn_hi || hi[i] >= mx_lo)) cand |= 1u << i;
     uint32_t todo = __ballot_sync(0xffffffffu, cand != 0);
     while (todo) {
       const int src = __ffs(todo) - 1;
       const int i = __ffs(__shfl_sync(0xffffffffu, cand, src)) - 1;
       const float xe = clip_canon(exact(4 * src + i), tau);
       if (lane == src) {
-        lo[i] = hi[i] = xe;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (j == i) lo[j] = hi[j] = xe;
         cand &= ~(1u << i);
         g.exact_calls += 1;
       }
@@ -169,17 +257,27 @@ __device__ __forceinline__ GroupCode quantize_group_warp(float4 xv, float4 ev, f
     code[i] = code_of(lo[i], z, s);
     if (code[i] != code_of(hi[i], z, s)) unsure |= 1u << i;
   }
-  // resolve the undecided codes one at a time, the whole warp computing each
+  // resolve the undecided codes one at a time, the whole warp computing each:
+  // narrowed first, exactly only if the narrow interval still straddles a boundary
   uint32_t pending = __ballot_sync(0xffffffffu, unsure != 0);
   while (pending) {
     const int src = __ffs(pending) - 1;
     const uint32_t bits = __shfl_sync(0xffffffffu, unsure, src);
     const int i = __ffs(bits) - 1;
-    const float xe = clip_canon(exact(4 * src + i), tau);
+    float nlo, nhi;
+    narrow(src, i, nlo, nhi);
+    const uint32_t clo = code_of(nlo, z, s), chi = code_of(nhi, z, s);
+    const bool open = __shfl_sync(0xffffffffu, clo != chi ? 1 : 0, src) != 0;
+    uint32_t ce = clo;
+    if (open) {
+      ce = code_of(clip_canon(exact(4 * src + i), tau), z, s);
+      if (lane == src) g.exact_calls += 1;
+    }
     if (lane == src) {
-      code[i] = code_of(xe, z, s);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (j == i) code[j] = ce;
       unsure &= ~(1u << i);
-      g.exact_calls += 1;
     }
     pending = __ballot_sync(0xffffffffu, unsure != 0);
   }

@@ -172,9 +172,11 @@ __global__ void __launch_bounds__(128) prefill_hist_kernel(DevCache c, int layer
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) kn += __shfl_xor_sync(0xffffffffu, kn, off);
     const float err = chain_error_bound(kn, colnorm);
+    const float sbound = __fmul_ru(__fsqrt_ru(__fmul_ru(kn, 1.0001f)), colnorm);   // >= sum_i |k_i R_ic|
     const float4 k4 = make_float4(kt[(4 * lane + 0) * KT_STRIDE + j], kt[(4 * lane + 1) * KT_STRIDE + j],
                                   kt[(4 * lane + 2) * KT_STRIDE + j], kt[(4 * lane + 3) * KT_STRIDE + j]);
-    const GroupCode g = quantize_group_warp(x, make_float4(err, err, err, err), tau, k4, Rt);
+    const GroupCode g = quantize_group_warp(x, make_float4(err, err, err, err),
+                                            make_float4(sbound, sbound, sbound, sbound), tau, k4, Rt);
     const int64_t h = t0 + j - SINK;
     const int32_t page = pt[h / PAGE];
     const int row = static_cast<int>(h % PAGE);
