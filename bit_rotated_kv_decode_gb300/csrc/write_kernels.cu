@@ -8,9 +8,9 @@
 // new tokens enter the BF16 recent window and the oldest recent token is
 // rotated, clipped, quantised and packed (4 codes per byte) into INT2 history.
 //
-// The rotated value of channel c of a token is the fp32 FMA chain
-//   acc_0 = 0, acc_{i+1} = fma(k_i, R[i][c], acc_i), i = 0..127,
-// in every kernel here, so prefill and sequential appends write identical bytes.
+// Every quantisation decision is taken on fp32_rn(k . R) exactly (see
+// quant_device.cuh), whatever order a kernel's fp32 FMA chain takes, so prefill
+// and sequential appends write identical bytes.
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -96,17 +96,19 @@ __global__ void __launch_bounds__(128) prefill_bf16_kernel(DevCache c, int layer
   }
 }
 
-constexpr int KT_STRIDE = PAGE + 4;   // floats per row of the transposed input tile
-constexpr size_t PREFILL_SMEM = (size_t)(D * KT_STRIDE + PAGE * D) * sizeof(float);
+constexpr size_t PREFILL_SMEM = (size_t)(2 * PAGE * D + PAGE) * sizeof(float);
 
 // Tile of up to 64 history positions (x) of one kv head (y), K or V (z).
+// Shared memory: the input tile row-major ks[64][128] (fp32), the rotated
+// values xs[64][128] and |k|^2 of each token (rounded up).
 __global__ void __launch_bounds__(128) prefill_hist_kernel(DevCache c, int layer, int slot,
                                                            const uint16_t* __restrict__ k,
                                                            const uint16_t* __restrict__ v, int64_t in_base,
                                                            int64_t h0, int64_t h1) {
   extern __shared__ float4 smem4[];
-  float* kt = reinterpret_cast<float*>(smem4);     // [D][KT_STRIDE] input tile, transposed
-  float* xs = kt + D * KT_STRIDE;                  // [PAGE][D] rotated values
+  float* ks = reinterpret_cast<float*>(smem4);     // [PAGE][D] input tile
+  float* xs = ks + PAGE * D;                       // [PAGE][D] rotated values
+  float* kn = xs + PAGE * D;                       // [PAGE] |k|^2, rounded up
   const int head = blockIdx.y;
   const int which = blockIdx.z;
   const int64_t t0 = h0 + (int64_t)blockIdx.x * PAGE;
@@ -117,64 +119,75 @@ __global__ void __launch_bounds__(128) prefill_hist_kernel(DevCache c, int layer
   const float* __restrict__ Rt = (which ? c.rot_vt : c.rot_kt) + lh * D * D;
   const float tau = (which ? c.tau_v : c.tau_k)[lh];
   const float colnorm = c.rot_cn[(size_t)which * c.L * c.Hkv + lh];
+  const int t = threadIdx.x;
 
   {
-    // 64 tokens x 128 channels of bf16 = 1024 16-byte chunks, 8 per thread, all in flight
+    // 64 tokens x 128 channels of bf16 = 1024 16-byte chunks, 8 per thread, all in
+    // flight; 16 consecutive threads share a token and add up its |k|^2
     constexpr int CHUNKS = PAGE * D / 8 / 128;
     uint4 v[CHUNKS];
 #pragma unroll
     for (int u = 0; u < CHUNKS; ++u) {
-      const int idx = u * 128 + threadIdx.x, j = idx / (D / 8), part = idx % (D / 8);
+      const int idx = u * 128 + t, j = idx / (D / 8), part = idx % (D / 8);
       v[u] = j < ntok ? reinterpret_cast<const uint4*>(src + ((size_t)(t0 + j - in_base) * c.Hkv + head) * D)[part]
                       : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int u = 0; u < CHUNKS; ++u) {
-      const int idx = u * 128 + threadIdx.x, j = idx / (D / 8), part = idx % (D / 8);
+      const int idx = u * 128 + t, j = idx / (D / 8), part = idx % (D / 8);
       const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      float f[8];
+      float sq = 0.0f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        kt[(8 * part + 2 * e) * KT_STRIDE + j] = __uint_as_float(w[e] << 16);
-        kt[(8 * part + 2 * e + 1) * KT_STRIDE + j] = __uint_as_float(w[e] & 0xffff0000u);
+        f[2 * e] = __uint_as_float(w[e] << 16);
+        f[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+        sq = __fmaf_ru(f[2 * e], f[2 * e], sq);
+        sq = __fmaf_ru(f[2 * e + 1], f[2 * e + 1], sq);
       }
+      float4* row = reinterpret_cast<float4*>(ks + j * D + 8 * part);
+      row[0] = make_float4(f[0], f[1], f[2], f[3]);
+      row[1] = make_float4(f[4], f[5], f[6], f[7]);
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) sq = __fadd_ru(sq, __shfl_xor_sync(0xffffffffu, sq, off));
+      if (part == 0) kn[j] = sq;
     }
   }
   __syncthreads();
 
-  const int co = threadIdx.x;
+  // rotation: thread co keeps the 64 tokens' FMA chains over i = 0 .. 127 in order;
+  // a float4 of ks (4 channels of one token) is the same address across the warp
+  const int co = t;
   float acc[PAGE];
 #pragma unroll
   for (int j = 0; j < PAGE; ++j) acc[j] = 0.0f;
-  for (int i = 0; i < D; ++i) {
-    const float r = __ldg(R + i * D + co);
-    const float4* kr = reinterpret_cast<const float4*>(kt + i * KT_STRIDE);
+  for (int i4 = 0; i4 < D / 4; ++i4) {
+    const float r0 = __ldg(R + (4 * i4 + 0) * D + co);
+    const float r1 = __ldg(R + (4 * i4 + 1) * D + co);
+    const float r2 = __ldg(R + (4 * i4 + 2) * D + co);
+    const float r3 = __ldg(R + (4 * i4 + 3) * D + co);
 #pragma unroll
-    for (int j4 = 0; j4 < PAGE / 4; ++j4) {
-      const float4 kk = kr[j4];
-      acc[4 * j4 + 0] = fmaf(kk.x, r, acc[4 * j4 + 0]);
-      acc[4 * j4 + 1] = fmaf(kk.y, r, acc[4 * j4 + 1]);
-      acc[4 * j4 + 2] = fmaf(kk.z, r, acc[4 * j4 + 2]);
-      acc[4 * j4 + 3] = fmaf(kk.w, r, acc[4 * j4 + 3]);
+    for (int j = 0; j < PAGE; ++j) {
+      const float4 kk = *reinterpret_cast<const float4*>(ks + j * D + 4 * i4);
+      acc[j] = fmaf(kk.x, r0, acc[j]);
+      acc[j] = fmaf(kk.y, r1, acc[j]);
+      acc[j] = fmaf(kk.z, r2, acc[j]);
+      acc[j] = fmaf(kk.w, r3, acc[j]);
     }
   }
 #pragma unroll
   for (int j = 0; j < PAGE; ++j) xs[j * D + co] = acc[j];
   __syncthreads();
 
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
+  const int warp = t >> 5;
+  const int lane = t & 31;
   const int32_t* pt = c.hist_pt + (size_t)slot * c.max_pages;
   for (int j = warp; j < ntok; j += 4) {
     const float4 x = *reinterpret_cast<const float4*>(xs + j * D + 4 * lane);
-    float kn = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) kn = __fmaf_ru(kt[(4 * lane + i) * KT_STRIDE + j], kt[(4 * lane + i) * KT_STRIDE + j], kn);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) kn += __shfl_xor_sync(0xffffffffu, kn, off);
-    const float err = chain_error_bound(kn, colnorm);
-    const float sbound = __fmul_ru(__fsqrt_ru(__fmul_ru(kn, 1.0001f)), colnorm);   // >= sum_i |k_i R_ic|
-    const float4 k4 = make_float4(kt[(4 * lane + 0) * KT_STRIDE + j], kt[(4 * lane + 1) * KT_STRIDE + j],
-                                  kt[(4 * lane + 2) * KT_STRIDE + j], kt[(4 * lane + 3) * KT_STRIDE + j]);
+    const float4 k4 = *reinterpret_cast<const float4*>(ks + j * D + 4 * lane);
+    const float knj = kn[j];
+    const float err = chain_error_bound(knj, colnorm);
+    const float sbound = __fmul_ru(__fsqrt_ru(__fmul_ru(knj, 1.0001f)), colnorm);   // >= sum_i |k_i R_ic|
     const GroupCode g = quantize_group_warp(x, make_float4(err, err, err, err),
                                             make_float4(sbound, sbound, sbound, sbound), tau, k4, Rt);
     const int64_t h = t0 + j - SINK;
