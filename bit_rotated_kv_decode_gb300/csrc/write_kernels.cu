@@ -96,23 +96,24 @@ __global__ void __launch_bounds__(128) prefill_bf16_kernel(DevCache c, int layer
   }
 }
 
-constexpr size_t PREFILL_SMEM = (size_t)(2 * PAGE * D + PAGE) * sizeof(float);
+constexpr int PF_TILE = 32;   // history positions per block
+constexpr size_t PREFILL_SMEM = (size_t)(2 * PF_TILE * D + PF_TILE) * sizeof(float);
 
-// Tile of up to 64 history positions (x) of one kv head (y), K or V (z).
-// Shared memory: the input tile row-major ks[64][128] (fp32), the rotated
-// values xs[64][128] and |k|^2 of each token (rounded up).
+// Tile of up to PF_TILE history positions (x) of one kv head (y), K or V (z).
+// Shared memory: the input tile row-major ks[PF_TILE][128] (fp32), the rotated
+// values xs[PF_TILE][128] and |k|^2 of each token (rounded up).
 __global__ void __launch_bounds__(128) prefill_hist_kernel(DevCache c, int layer, int slot,
                                                            const uint16_t* __restrict__ k,
                                                            const uint16_t* __restrict__ v, int64_t in_base,
                                                            int64_t h0, int64_t h1) {
   extern __shared__ float4 smem4[];
-  float* ks = reinterpret_cast<float*>(smem4);     // [PAGE][D] input tile
-  float* xs = ks + PAGE * D;                       // [PAGE][D] rotated values
-  float* kn = xs + PAGE * D;                       // [PAGE] |k|^2, rounded up
+  float* ks = reinterpret_cast<float*>(smem4);     // [PF_TILE][D] input tile
+  float* xs = ks + PF_TILE * D;                    // [PF_TILE][D] rotated values
+  float* kn = xs + PF_TILE * D;                    // [PF_TILE] |k|^2, rounded up
   const int head = blockIdx.y;
   const int which = blockIdx.z;
-  const int64_t t0 = h0 + (int64_t)blockIdx.x * PAGE;
-  const int ntok = static_cast<int>(h1 - t0 < PAGE ? h1 - t0 : PAGE);
+  const int64_t t0 = h0 + (int64_t)blockIdx.x * PF_TILE;
+  const int ntok = static_cast<int>(h1 - t0 < PF_TILE ? h1 - t0 : PF_TILE);
   const uint16_t* src = which ? v : k;
   const size_t lh = (size_t)layer * c.Hkv + head;
   const float* __restrict__ R = (which ? c.rot_v : c.rot_k) + lh * D * D;
@@ -122,9 +123,9 @@ __global__ void __launch_bounds__(128) prefill_hist_kernel(DevCache c, int layer
   const int t = threadIdx.x;
 
   {
-    // 64 tokens x 128 channels of bf16 = 1024 16-byte chunks, 8 per thread, all in
-    // flight; 16 consecutive threads share a token and add up its |k|^2
-    constexpr int CHUNKS = PAGE * D / 8 / 128;
+    // PF_TILE tokens x 128 channels of bf16 in 16-byte chunks, all in flight;
+    // 16 consecutive threads share a token and add up its |k|^2
+    constexpr int CHUNKS = PF_TILE * D / 8 / 128;
     uint4 v[CHUNKS];
 #pragma unroll
     for (int u = 0; u < CHUNKS; ++u) {
@@ -155,19 +156,19 @@ __global__ void __launch_bounds__(128) prefill_hist_kernel(DevCache c, int layer
   }
   __syncthreads();
 
-  // rotation: thread co keeps the 64 tokens' FMA chains over i = 0 .. 127 in order;
+  // rotation: thread co keeps the tile's FMA chains over i = 0 .. 127 in order;
   // a float4 of ks (4 channels of one token) is the same address across the warp
   const int co = t;
-  float acc[PAGE];
+  float acc[PF_TILE];
 #pragma unroll
-  for (int j = 0; j < PAGE; ++j) acc[j] = 0.0f;
+  for (int j = 0; j < PF_TILE; ++j) acc[j] = 0.0f;
   for (int i4 = 0; i4 < D / 4; ++i4) {
     const float r0 = __ldg(R + (4 * i4 + 0) * D + co);
     const float r1 = __ldg(R + (4 * i4 + 1) * D + co);
     const float r2 = __ldg(R + (4 * i4 + 2) * D + co);
     const float r3 = __ldg(R + (4 * i4 + 3) * D + co);
 #pragma unroll
-    for (int j = 0; j < PAGE; ++j) {
+    for (int j = 0; j < PF_TILE; ++j) {
       const float4 kk = *reinterpret_cast<const float4*>(ks + j * D + 4 * i4);
       acc[j] = fmaf(kk.x, r0, acc[j]);
       acc[j] = fmaf(kk.y, r1, acc[j]);
@@ -176,7 +177,7 @@ __global__ void __launch_bounds__(128) prefill_hist_kernel(DevCache c, int layer
     }
   }
 #pragma unroll
-  for (int j = 0; j < PAGE; ++j) xs[j * D + co] = acc[j];
+  for (int j = 0; j < PF_TILE; ++j) xs[j * D + co] = acc[j];
   __syncthreads();
 
   const int warp = t >> 5;
@@ -261,7 +262,7 @@ cudaError_t launch_prefill_hist(const DevCache& c, int layer, int slot, const ui
     attr = true;
   }
   const size_t smem = PREFILL_SMEM;
-  dim3 grid(static_cast<unsigned>((h1 - h0 + PAGE - 1) / PAGE), c.Hkv, 2);
+  dim3 grid(static_cast<unsigned>((h1 - h0 + PF_TILE - 1) / PF_TILE), c.Hkv, 2);
   prefill_hist_kernel<<<grid, 128, smem, s>>>(c, layer, slot, k, v, in_base, h0, h1);
   return cudaGetLastError();
 }
