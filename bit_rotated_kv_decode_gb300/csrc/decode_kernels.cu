@@ -61,9 +61,12 @@ template <int G> struct Tune {
   static constexpr int CTAS = G <= 4 ? 4 : 3;
 };
 constexpr int BF16_ITEMS = DECODE_BF16_ITEMS;
-constexpr uint32_t WAIT_LIMIT = 1u << 22;        // mbarrier try_wait rounds
+constexpr uint32_t WAIT_LIMIT = 1u << 16;        // mbarrier try_wait rounds, each up to SUSPEND_NS
+constexpr uint32_t SUSPEND_NS = 20000;           // a waiting warp sleeps until the phase completes
 constexpr uint32_t FLAG_WAIT_LIMIT = 1u << 20;   // polls of a ready word
 constexpr int ERR_TIMEOUT_BIT = 8;
+constexpr int LAZY_MAX_INT = 8;                  // softmax reference max kept within 2^8 of the true one
+constexpr float LAZY_MAX = static_cast<float>(LAZY_MAX_INT);
 
 struct DecodeArgs {
   unsigned long long epoch;  // unique per launch: marks the q operands as written
@@ -110,9 +113,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   for (uint32_t it = 0; it < WAIT_LIMIT; ++it) {
     uint32_t done;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
         : "=r"(done)
-        : "r"(addr), "r"(parity)
+        : "r"(addr), "r"(parity), "r"(SUSPEND_NS)
         : "memory");
     if (done) return true;
   }
@@ -177,6 +180,7 @@ struct Smem {
     float state[WARPS][G][PART];
   } buf;
   __align__(8) uint64_t bar[WARPS][Tune<G>::STAGES];
+  __align__(16) float4 meta[WARPS][PAGE];   // INT2: per token {s_k, z_k, s_v 2^ew, z_v} of the page
   WeightRows<G> w;
 };
 
@@ -402,11 +406,11 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
     }
   }
   // weights p * s_v are prescaled by 2^ew so the smallest ones stay representable in
-  // fp16: s_v <= fp16(2 tau_V / 3) and p <= 1, so p s_v 2^ew <= 2^15
+  // fp16: s_v <= fp16(2 tau_V / 3) and p <= 2^LAZY_MAX, so p s_v 2^ew <= 2^15
   int ew;
   {
     const float smax = c.tau_v[(size_t)layer * c.Hkv + head] * (2.0f / 3.0f) * 1.002f;
-    ew = max(-60, min(60, static_cast<int>(floorf(log2f(32768.0f / smax)))));
+    ew = max(-60, min(60, static_cast<int>(floorf(log2f(32768.0f / smax))) - LAZY_MAX_INT));
   }
   const float wscale = ldexpf(1.0f, ew);
   grid_dep_launch();
@@ -512,6 +516,18 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
     }
     // token meta of this lane's 8 tokens: 16 mt + gid + 8 rr; a partial page (the
     // last of the history) masks the rows past its end
+    // the page's metadata converted once per token (lanes l and l + 32), not once
+    // per query head: {s_k, z_k, s_v 2^ew, z_v}, value terms zeroed past the end
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int tok = lane + 32 * hh;
+      const __half2 km = *reinterpret_cast<const __half2*>(rec + K_META_OFF + tok * META_BYTES);
+      const __half2 vm = *reinterpret_cast<const __half2*>(rec + V_META_OFF + tok * META_BYTES);
+      const bool ok = tok < valid;
+      sm.meta[warp][tok] = make_float4(__low2float(km), __high2float(km), ok ? __low2float(vm) * wscale : 0.0f,
+                                       ok ? __high2float(vm) : 0.0f);
+    }
+    __syncwarp();
     float lg[NT][8], sw[8], zv[8];
     auto epilogue = [&](auto full_page) {
       constexpr bool FULL = decltype(full_page)::value;
@@ -521,15 +537,13 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
         for (int rr = 0; rr < 2; ++rr) {
           const int i = 2 * mt + rr;
           const int tok = 16 * mt + gid + 8 * rr;
-          const __half2 km = *reinterpret_cast<const __half2*>(rec + K_META_OFF + tok * META_BYTES);
-          const __half2 vm = *reinterpret_cast<const __half2*>(rec + V_META_OFF + tok * META_BYTES);
+          const float4 mtv = sm.meta[warp][tok];
           const bool ok = FULL || tok < valid;
-          sw[i] = ok ? __low2float(vm) * wscale : 0.0f;
-          zv[i] = ok ? __high2float(vm) : 0.0f;
-          const float sk = __low2float(km), zk = __high2float(km);
+          sw[i] = mtv.z;
+          zv[i] = mtv.w;
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            const float v = fmaf(ks[nt] * sk, acc[nt][mt][2 * rr] + acc[nt][mt][2 * rr + 1], kz[nt] * zk);
+            const float v = fmaf(ks[nt] * mtv.x, acc[nt][mt][2 * rr] + acc[nt][mt][2 * rr + 1], kz[nt] * mtv.y);
             lg[nt][i] = (ok && (4 * nt + 4 <= G || 4 * nt + tid < G)) ? v : -INFINITY;
           }
         }
@@ -555,10 +569,12 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
       pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
       pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
       pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-      const float m_new = fmaxf(m_run[nt], pm);
-      if (m_new > m_run[nt]) {   // rescale only when the running max grows
-        const float corr = ex2(m_run[nt] - m_new);
-        m_run[nt] = m_new;
+      // the reference max m_run moves only when a page exceeds it by more than
+      // LAZY_MAX (log2 units): weights stay below 2^LAZY_MAX and the accumulators
+      // are rescaled on few pages
+      if (pm > m_run[nt] + LAZY_MAX) {
+        const float corr = ex2(m_run[nt] - pm);
+        m_run[nt] = pm;
         l_run[nt] *= corr;
         u_run[nt] *= corr;
 #pragma unroll
@@ -566,10 +582,11 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
 #pragma unroll
           for (int e = 0; e < 4; ++e) o[nt][mt][e] *= corr;
       }
+      const float m_ref = m_run[nt];
       const int h = 4 * nt + tid;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float p = ex2(lg[nt][i] - m_new);
+        const float p = ex2(lg[nt][i] - m_ref);
         l_run[nt] += p;
         u_run[nt] = fmaf(p, zv[i], u_run[nt]);
         if (h < G) {
