@@ -230,16 +230,30 @@ struct RotSmem {
   float qscale[G];
 };
 
-template <int G, int NTH>
-__device__ __forceinline__ void rotate_block(const DevCache& c, int layer, unsigned long long epoch, int batch_row,
-                                             int head, int slab, const uint16_t* __restrict__ q,
-                                             uint32_t* __restrict__ dst, RotSmem<G, NTH>& sm) {
-  constexpr int RG = NTH / 32, ROWS = D / RG;
+template <int NTH>
+struct RotRows {
+  static constexpr int RG = NTH / 32, ROWS = D / RG;
+  float r[ROWS];
+};
+
+// The R_K column slice a thread of the slab block sums with.  R_K is written once at
+// set-up, so the loads may be issued before the wait for the preceding grid.
+template <int NTH>
+__device__ __forceinline__ void rotate_load_r(const DevCache& c, int layer, int head, int slab, RotRows<NTH>& rr) {
   const int t = threadIdx.x, lane = t & 31, grp = t >> 5;
   const float* __restrict__ RK = c.rot_k + ((size_t)layer * c.Hkv + head) * D * D + 32 * slab + lane;
-  float r[ROWS];
 #pragma unroll
-  for (int i = 0; i < ROWS; ++i) r[i] = __ldg(RK + (size_t)(ROWS * grp + i) * D);
+  for (int i = 0; i < RotRows<NTH>::ROWS; ++i) rr.r[i] = __ldg(RK + (size_t)(RotRows<NTH>::ROWS * grp + i) * D);
+}
+
+template <int G, int NTH>
+__device__ __forceinline__ void rotate_block(const DevCache& c, unsigned long long epoch, int batch_row,
+                                             int head, int slab, const uint16_t* __restrict__ q,
+                                             uint32_t* __restrict__ dst, const RotRows<NTH>& rows,
+                                             RotSmem<G, NTH>& sm) {
+  constexpr int RG = NTH / 32, ROWS = D / RG;
+  const int t = threadIdx.x, lane = t & 31, grp = t >> 5;
+  const float (&r)[ROWS] = rows.r;
   const uint16_t* qrow = q + ((size_t)batch_row * c.Hq + (size_t)head * G) * D;
   constexpr int QN = (G * D + NTH - 1) / NTH;   // q values per thread, all loads in flight
   uint16_t qv[QN];
@@ -319,12 +333,14 @@ __global__ void __launch_bounds__(ROT_THREADS) rotate_q_kernel(DevCache c, int l
                                                                uint32_t* __restrict__ qfrag) {
   __shared__ RotSmem<G, ROT_THREADS> sm;
   const int ri = blockIdx.x / c.Hkv, head = blockIdx.x % c.Hkv, slab = blockIdx.y;
+  RotRows<ROT_THREADS> rows;
+  rotate_load_r(c, layer, head, slab, rows);
   // the preceding grid (whatever wrote q or the cache) is complete before the next
   // grid of this decode may start
   grid_dep_wait();
   grid_dep_launch();
-  rotate_block<G, ROT_THREADS>(c, layer, a.epoch, a.r[ri].batch_row, head, slab, q,
-                               qfrag + (size_t)blockIdx.x * QFrag<G>::WORDS, sm);
+  rotate_block<G, ROT_THREADS>(c, a.epoch, a.r[ri].batch_row, head, slab, q,
+                               qfrag + (size_t)blockIdx.x * QFrag<G>::WORDS, rows, sm);
 }
 
 // ---- 2. stream: INT2 chunks and BF16 pages ------------------------------------------
@@ -466,12 +482,15 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
   }
 
   float o[NT][8][4];
-  float m_run[NT], l_run[NT], u_run[NT];
+  // l and u are kept as two partial sums (tokens gid and gid + 8 of each m-tile)
+  // so that the page's pairs update them with packed fp32 instructions
+  float m_run[NT];
+  float2 l_run[NT], u_run[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     m_run[nt] = -INFINITY;
-    l_run[nt] = 0.0f;
-    u_run[nt] = 0.0f;
+    l_run[nt] = make_float2(0.0f, 0.0f);
+    u_run[nt] = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
@@ -528,32 +547,42 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
                                        ok ? __high2float(vm) : 0.0f);
     }
     __syncwarp();
-    float lg[NT][8], sw[8], zv[8];
+    // logits in the log2 domain, as pairs (token 16 mt + gid, that token + 8)
+    float2 lg[NT][4], sw[4], zv[4];
     auto epilogue = [&](auto full_page) {
       constexpr bool FULL = decltype(full_page)::value;
 #pragma unroll
-      for (int mt = 0; mt < 4; ++mt)
+      for (int mt = 0; mt < 4; ++mt) {
+        const int tok = 16 * mt + gid;
+        const float4 m0 = sm.meta[warp][tok], m1 = sm.meta[warp][tok + 8];
+        sw[mt] = make_float2(m0.z, m1.z);
+        zv[mt] = make_float2(m0.w, m1.w);
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          const int i = 2 * mt + rr;
-          const int tok = 16 * mt + gid + 8 * rr;
-          const float4 mtv = sm.meta[warp][tok];
-          const bool ok = FULL || tok < valid;
-          sw[i] = mtv.z;
-          zv[i] = mtv.w;
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const float v = fmaf(ks[nt] * mtv.x, acc[nt][mt][2 * rr] + acc[nt][mt][2 * rr + 1], kz[nt] * mtv.y);
-            lg[nt][i] = (ok && (4 * nt + 4 <= G || 4 * nt + tid < G)) ? v : -INFINITY;
+        for (int nt = 0; nt < NT; ++nt) {
+          // hi + lo columns, then s_k kscale acc + z_k (scale log2 e sum q_rot)
+          const float2 a = __fadd2_rn(make_float2(acc[nt][mt][0], acc[nt][mt][2]),
+                                      make_float2(acc[nt][mt][1], acc[nt][mt][3]));
+          const float2 sk = __fmul2_rn(make_float2(m0.x, m1.x), make_float2(ks[nt], ks[nt]));
+          const float2 zk = __fmul2_rn(make_float2(m0.y, m1.y), make_float2(kz[nt], kz[nt]));
+          float2 v = __ffma2_rn(sk, a, zk);
+          const bool head_ok = 4 * nt + 4 <= G || 4 * nt + tid < G;
+          if (!FULL || !head_ok) {
+            v.x = (head_ok && tok < valid) ? v.x : -INFINITY;
+            v.y = (head_ok && tok + 8 < valid) ? v.y : -INFINITY;
           }
+          lg[nt][mt] = v;
         }
+      }
     };
     if (valid == PAGE)
       epilogue(std::true_type{});
     else
       epilogue(std::false_type{});
     // ---- online softmax per head (lanes with equal tid share a head); the
-    // weights p s_v 2^ew go to shared memory as fp16 hi / lo halves
+    // weights p s_v 2^ew go to shared memory as fp16 hi / lo halves.  Within each
+    // 16-token group the weight rows hold token 16 g + r at position 16 g + 2 r
+    // (r < 8) or 16 g + 2 (r - 8) + 1, so a lane's pair is one 32-bit store; the
+    // value contraction below takes its k index in the same order.
     uint16_t(*wh)[2][WH_STRIDE];
     if constexpr (kWeightsInRing<G>) {
       wh = reinterpret_cast<uint16_t(*)[2][WH_STRIDE]>(sm.buf.ring[warp][stg] + K_CODES_OFF);
@@ -563,9 +592,9 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      float pm = lg[nt][0];
+      float pm = fmaxf(lg[nt][0].x, lg[nt][0].y);
 #pragma unroll
-      for (int i = 1; i < 8; ++i) pm = fmaxf(pm, lg[nt][i]);
+      for (int mt = 1; mt < 4; ++mt) pm = fmaxf(pm, fmaxf(lg[nt][mt].x, lg[nt][mt].y));
       pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
       pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
       pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
@@ -575,32 +604,34 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
       if (pm > m_run[nt] + LAZY_MAX) {
         const float corr = ex2(m_run[nt] - pm);
         m_run[nt] = pm;
-        l_run[nt] *= corr;
-        u_run[nt] *= corr;
+        l_run[nt] = __fmul2_rn(l_run[nt], make_float2(corr, corr));
+        u_run[nt] = __fmul2_rn(u_run[nt], make_float2(corr, corr));
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) o[nt][mt][e] *= corr;
       }
-      const float m_ref = m_run[nt];
+      const float2 neg_ref = make_float2(-m_run[nt], -m_run[nt]);
       const int h = 4 * nt + tid;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float p = ex2(lg[nt][i] - m_ref);
-        l_run[nt] += p;
-        u_run[nt] = fmaf(p, zv[i], u_run[nt]);
+      for (int mt = 0; mt < 4; ++mt) {
+        const float2 d = __fadd2_rn(lg[nt][mt], neg_ref);
+        const float2 p = make_float2(ex2(d.x), ex2(d.y));
+        l_run[nt] = __fadd2_rn(l_run[nt], p);
+        u_run[nt] = __ffma2_rn(p, zv[mt], u_run[nt]);
         if (h < G) {
-          const float w = p * sw[i];
-          const __half hi = __float2half_rn(w);
-          const __half lo = __float2half_rn(w - __half2float(hi));
-          const int tok = 16 * (i >> 1) + gid + 8 * (i & 1);
-          wh[h][0][tok] = __half_as_ushort(hi);
-          wh[h][1][tok] = __half_as_ushort(lo);
+          const float2 w = __fmul2_rn(p, sw[mt]);
+          const __half2 hi = __float22half2_rn(w);
+          const float2 lo = __ffma2_rn(__half22float2(hi), make_float2(-1.0f, -1.0f), w);
+          const int pos = 16 * mt + 2 * gid;
+          *reinterpret_cast<__half2*>(&wh[h][0][pos]) = hi;
+          *reinterpret_cast<__half2*>(&wh[h][1][pos]) = __float22half2_rn(lo);
         }
       }
     }
     __syncwarp();
-    // ---- values: 8 m-tiles of 16 channels x NT n-tiles, K = 64 tokens
+    // ---- values: 8 m-tiles of 16 channels x NT n-tiles, K = 64 tokens; k index
+    // 2 j + b of step s is token 16 s + j + 8 b
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
       const int ta = 16 * s + 2 * tid;
@@ -616,9 +647,10 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
           bw[nt][0] = bw[nt][1] = 0u;
         }
       }
+      const int tb = 16 * s + tid;
       const uint32_t* vrow = reinterpret_cast<const uint32_t*>(rec + V_CODES_OFF) + gid;
-      const uint32_t wa = vrow[ta * (CODE_BYTES / 4)], wb = vrow[(ta + 1) * (CODE_BYTES / 4)];
-      const uint32_t wc = vrow[(ta + 8) * (CODE_BYTES / 4)], wd = vrow[(ta + 9) * (CODE_BYTES / 4)];
+      const uint32_t wa = vrow[tb * (CODE_BYTES / 4)], wb = vrow[(tb + 8) * (CODE_BYTES / 4)];
+      const uint32_t wc = vrow[(tb + 4) * (CODE_BYTES / 4)], wd = vrow[(tb + 12) * (CODE_BYTES / 4)];
       const uint32_t x1 = __byte_perm(wa, wb, 0x5410), y1 = __byte_perm(wa, wb, 0x7632);
       const uint32_t x2 = __byte_perm(wc, wd, 0x5410), y2 = __byte_perm(wc, wd, 0x7632);
       const uint32_t x1s = x1 >> 10, y1s = y1 >> 10;
@@ -656,7 +688,7 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
   // ---- this warp's state -> shared memory (rotated basis, unscaled, z term added)
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    float l = l_run[nt], u = u_run[nt];
+    float l = l_run[nt].x + l_run[nt].y, u = u_run[nt].x + u_run[nt].y;
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       l += __shfl_xor_sync(0xffffffffu, l, off);
@@ -1018,10 +1050,12 @@ __global__ void __launch_bounds__(FRONT_THREADS) step_front_kernel(DevCache c, i
   }
   const int b = blockIdx.x - app_blocks;
   const int ri = b / (c.Hkv * SLABS), head = (b / SLABS) % c.Hkv, slab = b % SLABS;
+  RotRows<FRONT_THREADS> rows;
+  rotate_load_r(c, layer, head, slab, rows);
   grid_dep_wait();
   grid_dep_launch();
-  rotate_block<G, FRONT_THREADS>(c, layer, f.epoch, f.batch_row[ri], head, slab, q,
-                                 qfrag + ((size_t)ri * c.Hkv + head) * QFrag<G>::WORDS, sm.rot);
+  rotate_block<G, FRONT_THREADS>(c, f.epoch, f.batch_row[ri], head, slab, q,
+                                 qfrag + ((size_t)ri * c.Hkv + head) * QFrag<G>::WORDS, rows, sm.rot);
 }
 
 // Dynamic shared memory opt-in, once per device and kernel.
