@@ -30,6 +30,7 @@ sys.path.insert(0, ROOT)
 METRIC = "decode-attention µs/step & KV HBM GB/s (frac of 8 TB/s) at 100K ctx; demote tok/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 INT2_BYTES_PER_TOKEN_HEAD = 72          # 2 x (32 code bytes + 4 meta bytes)
 BF16_BYTES_PER_TOKEN_HEAD = 512         # K and V rows of 128 bf16
 
@@ -76,6 +77,16 @@ def measured_peak_hbm():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_peak_bf16():
+    """Dense bf16 tensor peak for a kernel timed alone (burst), TFLOP/s."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def committed_traffic(kernel: str):
@@ -380,8 +391,7 @@ def run_gpu(args, log):
 
 
 # ----------------------------------------------------------------------------------------------
-PREFILL_FLOP_PER_TOKEN_HEAD = 2 * 2 * 128 * 128      # K and V rotation, one FMA = 2 flops
-FP32_PEAK_TFLOPS_DERIVED = 152 * 128 * 2 * 2.07e9 / 1e12   # SMs x FP32 lanes x 2 flops x max SM clock
+PREFILL_FLOP_PER_TOKEN_HEAD = 2 * 2 * 128 * 128      # K and V rotation, one multiply-add = 2 flops
 
 
 def run_write(args, log):
@@ -460,6 +470,7 @@ def run_write(args, log):
     pre_avg = float(np.mean(pre_us[1:] if len(pre_us) > 1 else pre_us))
     flops = (T - 320) * hkv * PREFILL_FLOP_PER_TOKEN_HEAD
     achieved = flops / (pre_avg * 1e-6) / 1e12
+    peak, peak_src = measured_peak_bf16()
     pre_bytes = T * hkv * 512 + (T - 320) * hkv * INT2_BYTES_PER_TOKEN_HEAD + 320 * hkv * 512
     return {
         "metric": METRIC, "value": tok_s, "unit": "demoted tok/s (tokens x layers / s)", "n_gpus": world,
@@ -471,10 +482,11 @@ def run_write(args, log):
                          % (pre_bytes / 1e6)},
         "prefill_us_per_layer": pre_avg,
         "prefill_gbs": pre_bytes / (pre_avg * 1e-6) / 1e9,
-        "roofline": {"bound": "alu", "kernel": "prefill_hist_kernel (rotation as an fp32 FMA chain)",
-                     "achieved": achieved, "peak": FP32_PEAK_TFLOPS_DERIVED, "unit": "TFLOP/s",
-                     "frac": achieved / FP32_PEAK_TFLOPS_DERIVED,
-                     "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz", "traffic": None},
+        "roofline": {"bound": "tensor", "kernel": "prefill_hist_kernel (rotation on the tensor cores, exact quantiser)",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_source": peak_src, "flops": "algorithmic: 2 x 128 x 128 per token, kv head and K or V",
+                     "traffic": committed_traffic("prefill_hist_kernel"),
+                     "algorithmic_bytes_per_launch": pre_bytes - 320 * hkv * 512 * 2},
         "e2e": {"value": e2e_tok_s, "unit": "demoted tok/s (tokens x layers / s)",
                 "h2d_bytes_per_step": (kn[0].numel() + vn[0].numel()) * 2, "d2h_bytes_per_step": 4},
         "gpu_launches": K * L,
