@@ -272,11 +272,17 @@ __device__ __forceinline__ void rotate_block(const DevCache& c, unsigned long lo
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
     if (lane == 0) {
+      // e = 15 - 24 - ceil(log2(|q|_2 1.001)), read off the exponent of the
+      // rounded-up norm (a power of two in, the next one up otherwise)
       int e = 0;
-      if (n2 > 0.0f) e = static_cast<int>(floorf(log2f(32768.0f / (sqrtf(n2) * 1.001f)))) - 24;
+      if (n2 > 0.0f) {
+        const uint32_t b = __float_as_uint(__fmul_ru(__fsqrt_ru(n2), 1.001f));
+        const int ceil_log2 = static_cast<int>((b >> 23) & 0xffu) - 127 + ((b & 0x7fffffu) != 0u ? 1 : 0);
+        e = 15 - 24 - ceil_log2;
+      }
       e = max(-60, min(e, 60));
-      sm.qscale[h] = ldexpf(1.0f, e);
-      if (slab == 0) consts[h] = ldexpf(c.scale * LOG2E, -e);
+      sm.qscale[h] = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+      if (slab == 0) consts[h] = c.scale * LOG2E * __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
     }
   }
   if (slab == 0 && t >= G && t < 8) consts[t] = 0.0f;
@@ -320,11 +326,9 @@ __device__ __forceinline__ void rotate_block(const DevCache& c, unsigned long lo
     }
     dst[(size_t)(4 * gid + slab) * QFrag<G>::REGS + k] = word;
   }
+  // the block barrier orders every thread's words before thread 0's release store
   __syncthreads();
-  if (t == 0) {
-    __threadfence();
-    st_release(reinterpret_cast<unsigned long long*>(dst + QFrag<G>::READY) + slab, epoch);
-  }
+  if (t == 0) st_release(reinterpret_cast<unsigned long long*>(dst + QFrag<G>::READY) + slab, epoch);
 }
 
 template <int G>
