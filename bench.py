@@ -390,6 +390,56 @@ def run_gpu(args, log):
     return wl, res
 
 
+def bf16_baseline(wl, r, log, launches: int = 40):
+    """Uncompressed BF16 paged decode (oscar_bf16_decode) over the same lengths, heads
+    and queries, timed like the decode kernels: CUDA events around each call on the
+    launching stream.  Two layers' pools alternate (each larger than L2); values are
+    seeded normal bf16 (the kernel's time does not depend on them)."""
+    import torch
+    b = wl.b
+    lens = [wl.cache.length(q, 0)[0] for q in wl.reqs]
+    n, hkv = wl.batch, wl.hkv
+    pages = [(t + 63) // 64 for t in lens]
+    total = sum(pages)
+    gen = torch.Generator(device="cuda").manual_seed(7)
+    pools, tables = [], []
+    for layer in range(2):
+        pool = torch.randn((total, hkv, 2, 64, 128), generator=gen, device="cuda", dtype=torch.float32)
+        pools.append(pool.to(torch.bfloat16))
+        del pool
+        perm = torch.randperm(total, generator=gen, device="cuda").to(torch.int32)
+        pt = torch.zeros((n, max(pages)), dtype=torch.int32, device="cuda")
+        o = 0
+        for i, np_ in enumerate(pages):
+            pt[i, :np_] = perm[o:o + np_]
+            o += np_
+        tables.append(pt)
+    out = torch.empty((n, wl.hq, 128), dtype=torch.float32, device="cuda")
+    ws = None
+    for i in range(3):
+        ws = b.bf16_decode(pools[i % 2], tables[i % 2], lens, wl.q[i, 0], out, hkv, workspace=ws)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(launches)]
+    for i, (e0, e1) in enumerate(ev):
+        e0.record()
+        b.bf16_decode(pools[i % 2], tables[i % 2], lens, wl.q[i % wl.q.shape[0], 0], out, hkv, workspace=ws)
+        e1.record()
+    torch.cuda.synchronize()
+    if int(ws[:4].view(torch.int32).item()) != 0:
+        raise RuntimeError("bf16 baseline: page id outside the pool")
+    us = float(np.mean([1000.0 * a.elapsed_time(c) for a, c in ev]))
+    nbytes = sum(lens) * hkv * BF16_BYTES_PER_TOKEN_HEAD
+    gbs = nbytes / (us * 1e-6) / 1e9
+    int2_us = r["us_step"] / wl.L
+    log(f"bf16 baseline {us:.1f} us/layer ({gbs:.0f} GB/s); INT2 step {int2_us:.1f} us/layer")
+    del pools
+    return {"kernel": "bf16_stream_kernel + bf16_merge_kernel (oscar_bf16_decode)", "us_per_layer": us,
+            "bytes_per_layer": nbytes, "achieved_gbs": gbs, "frac": gbs / r["peak"], "peak_source": r["peak_kind"],
+            "launches_timed": launches,
+            "int2_step_us_per_layer": int2_us, "speedup_of_int2_step": us / int2_us,
+            "timing": "CUDA events around each call, two alternating layer pools larger than L2"}
+
+
 # ----------------------------------------------------------------------------------------------
 PREFILL_FLOP_PER_TOKEN_HEAD = 2 * 2 * 128 * 128      # K and V rotation, one multiply-add = 2 flops
 
@@ -599,6 +649,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--config", type=int, default=2, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-bf16-baseline", action="store_true",
+                    help="skip the uncompressed BF16 decode comparison")
     ap.add_argument("--layers", type=int, default=0, help="fewer layers (small profiling cases only)")
     ap.add_argument("--separate-calls", action="store_true",
                     help="time oscar_append + oscar_decode_attention per layer instead of oscar_decode_step")
@@ -622,6 +674,7 @@ def main(argv=None):
             print(json.dumps(line), flush=True)
         return
     wl, r = run_gpu(args, log)
+    base16 = bf16_baseline(wl, r, log) if not args.no_bf16_baseline else None
     cpu = par = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu, par = cpu_baseline(wl, r, log)
@@ -671,6 +724,8 @@ def main(argv=None):
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }
+    if base16 is not None:
+        line["bf16_baseline"] = base16
     if cpu is not None:
         line["cpu_baseline"] = cpu
         line["parity"] = par

@@ -77,6 +77,9 @@ _SIGNATURES = {
     "oscar_decode_step": (c_int32, [_P, c_int32, c_int32, POINTER(c_int32), _P, _P, _P, _P, _P, c_size_t, _P]),
     "oscar_cache_check": (c_int32, [_P, _P]),
     "oscar_last_error": (c_char_p, [_P]),
+    "oscar_bf16_decode_workspace_bytes": (c_size_t, [c_int32, POINTER(c_int32), c_int32, c_int32]),
+    "oscar_bf16_decode": (c_int32, [_P, c_int64, _P, c_int32, POINTER(c_int32), c_int32, c_int32, c_int32, c_float,
+                                    _P, _P, _P, c_size_t, _P]),
 }
 
 _lib = None
@@ -286,6 +289,26 @@ class OscarCache:
         n = self.cfg.max_requests * self.cfg.max_pages_per_request
         return self.mem[lay.hist_pt_offset:lay.hist_pt_offset + 4 * n].view(torch.int32).view(
             self.cfg.max_requests, self.cfg.max_pages_per_request)
+
+
+def bf16_decode(kv, page_table, lens, q, out, num_kv_heads: int, scale: float = 0.0, workspace=None, stream=None):
+    """Uncompressed BF16 paged decode attention (the baseline): kv bf16
+    [pages][Hkv][2][64][128], page_table int32 [n][max_pages] (device), lens host
+    ints, q bf16 [n][Hq][128], out fp32 [n][Hq][128].  Returns the workspace."""
+    lib = load()
+    n, hq = q.shape[0], q.shape[1]
+    arr = (c_int32 * n)(*[int(x) for x in lens])
+    need = lib.oscar_bf16_decode_workspace_bytes(n, arr, hq, num_kv_heads)
+    if need == 0:
+        raise OscarError(1, "bf16_decode: arguments outside the supported limits")
+    if workspace is None or workspace.numel() < need:
+        workspace = new_workspace(need)
+    st = lib.oscar_bf16_decode(_ptr(kv), kv.shape[0], _ptr(page_table), page_table.shape[1], arr, n, hq,
+                               num_kv_heads, float(scale), _ptr(q), _ptr(out), _ptr(workspace), workspace.numel(),
+                               _stream_ptr(stream))
+    if st != 0:
+        raise OscarError(st, "oscar_bf16_decode failed")
+    return workspace
 
 
 def new_workspace(nbytes: int, device="cuda"):

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "liboscar_gb300.so")
-SOURCES = ["host.cpp", "write_kernels.cu", "decode_kernels.cu", "decode_scratch.cu"]
+SOURCES = ["host.cpp", "write_kernels.cu", "decode_kernels.cu", "decode_scratch.cu", "bf16_decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

@@ -241,6 +241,32 @@ const char* oscar_last_error(const oscar_cache* cache);
 /* Library version string. */
 const char* oscar_version(void);
 
+/* ---- Uncompressed BF16 baseline -------------------------------------------
+ * Plain softmax attention over a paged BF16 KV cache, the comparison point of
+ * the pages' decode-speed results ([MTP] section "Results": the 2-bit cache
+ * against a BF16 cache of the same context):
+ *   out[i][h] = softmax(q[i][h] K_i^T * scale) V_i   over all lens[i] tokens,
+ * K_i, V_i the tokens of request i in the kv head h / (Hq / Hkv).
+ *   kv          device bf16 [num_pages][Hkv][2][64][128]: per page and kv head,
+ *               64 K rows then 64 V rows; token t of request i sits in page
+ *               page_table[i][t / 64], row t % 64.  Bytes of rows past lens[i]
+ *               are never used.
+ *   page_table  device int32 [n][max_pages].
+ *   lens        host int32 [n], each >= 1 and <= 64 * max_pages.
+ *   q           device bf16 [n][Hq][128]; out device fp32 [n][Hq][128].
+ *   scale       softmax scale; <= 0 selects 1 / sqrt(128).
+ *   workspace   device, >= oscar_bf16_decode_workspace_bytes(); its first 4
+ *               bytes become nonzero if a page id was out of range (that page
+ *               is then read as page 0).
+ * 1 <= n <= 64, Hq / Hkv in {1, 2, 4, 8}; kv, q, out and workspace 16-byte
+ * aligned.  Asynchronous on "stream"; argument errors are returned before any
+ * launch.  The workspace size returned is 0 for arguments outside these limits. */
+size_t oscar_bf16_decode_workspace_bytes(int32_t n, const int32_t* lens, int32_t num_q_heads, int32_t num_kv_heads);
+oscar_status oscar_bf16_decode(const void* kv, int64_t num_pages, const int32_t* page_table, int32_t max_pages,
+                               const int32_t* lens, int32_t n, int32_t num_q_heads, int32_t num_kv_heads,
+                               float scale, const void* q, float* out, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
 #ifdef __cplusplus
 }
 #endif
