@@ -38,6 +38,8 @@ constexpr int BF_PITCH = D + 8;            // bf16 per staged row: ldmatrix with
 constexpr int BF_WPITCH = BF_SUB + 8;      // bf16 per weight column
 constexpr float BF_LAZY = 8.0f;            // the reference max moves only when exceeded by 2^8
 constexpr int BF_MERGE_THREADS = 128;
+constexpr int BF_MERGE_WARPS = BF_MERGE_THREADS / 32;
+constexpr int BF_MERGE_UNROLL = 4;         // chunk partials in flight per merge warp
 constexpr int BF_MAX_REQ = 64;             // requests per launch
 
 struct BfArgs {
@@ -99,6 +101,8 @@ __device__ __forceinline__ uint16_t bf16_bits(float x) {
   return *reinterpret_cast<const uint16_t*>(&h);
 }
 __device__ __forceinline__ float bf16_value(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Chunk c of the pages of (request ri, kv head h): pages [c ppc, (c + 1) ppc).
 // Warp w takes sub-pages w, w + 4, ... of the chunk.  Partial of query head g of
@@ -111,6 +115,8 @@ __global__ void __launch_bounds__(BF_THREADS, 3) bf16_stream_kernel(BfArgs a, co
   constexpr int NT = BfSmem<G>::NT;   // n-tiles of 8 (head, hi / lo) columns
   extern __shared__ __align__(16) uint8_t bf_raw[];
   BfSmem<G>& sm = *reinterpret_cast<BfSmem<G>*>(bf_raw);
+  // the merge grid may be scheduled now; it waits for this grid's completion
+  grid_dep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tid = lane & 3;
   int ri = 0;
   while (ri + 1 < a.n && a.block_start[ri + 1] <= (int)blockIdx.x) ++ri;
@@ -296,28 +302,79 @@ __global__ void __launch_bounds__(BF_THREADS, 3) bf16_stream_kernel(BfArgs a, co
   }
 }
 
-// One block per (request, query head): fold the chunk partials, thread t per channel.
+// One block per (request, query head): fold the chunk partials.  Warp w takes
+// chunks w, w + 4, ..., BF_MERGE_UNROLL at a time with lane l holding channels
+// 4 l .. 4 l + 3; the warps' states are then folded per channel.
 template <int G>
 __global__ void __launch_bounds__(BF_MERGE_THREADS) bf16_merge_kernel(BfArgs a, const float* __restrict__ partials,
                                                                       float* __restrict__ out) {
+  __shared__ float s_m[BF_MERGE_WARPS], s_l[BF_MERGE_WARPS];
+  __shared__ __align__(16) float s_o[BF_MERGE_WARPS][D];
   const int ri = blockIdx.x / a.Hq, hq = blockIdx.x % a.Hq;
   const int head = hq / G, g = hq % G;
   const int nch = a.chunks[ri];
-  const float* base = partials + ((size_t)a.block_start[ri] + (size_t)head * nch) * G * PARTIAL_FLOATS +
-                      (size_t)g * PARTIAL_FLOATS;
-  const int t = threadIdx.x;
-  float M = -INFINITY;
-  for (int c = 0; c < nch; ++c) M = fmaxf(M, __ldg(base + (size_t)c * G * PARTIAL_FLOATS + PARTIAL_M));
-  float acc = 0.0f, L = 0.0f;
-  for (int c = 0; c < nch; ++c) {
-    const float* p = base + (size_t)c * G * PARTIAL_FLOATS;
-    const float m = __ldg(p + PARTIAL_M);
-    if (m == -INFINITY) continue;
-    const float f = exp2f(m - M);
-    acc = fmaf(__ldg(p + t), f, acc);
-    L = fmaf(__ldg(p + PARTIAL_L), f, L);
+  constexpr size_t STRIDE = (size_t)G * PARTIAL_FLOATS;
+  const float* base = partials + ((size_t)a.block_start[ri] + (size_t)head * nch) * STRIDE + (size_t)g * PARTIAL_FLOATS;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dep_wait();   // the stream grid's partials are complete and visible
+  float m = -INFINITY, l = 0.0f;
+  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  for (int c0 = warp; c0 < nch; c0 += BF_MERGE_WARPS * BF_MERGE_UNROLL) {
+    float mv[BF_MERGE_UNROLL], lv[BF_MERGE_UNROLL];
+    float4 ov[BF_MERGE_UNROLL];
+#pragma unroll
+    for (int u = 0; u < BF_MERGE_UNROLL; ++u) {
+      const int c = c0 + BF_MERGE_WARPS * u;
+      mv[u] = -INFINITY;
+      lv[u] = 0.0f;
+      ov[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (c < nch) {
+        const float* p = base + (size_t)c * STRIDE;
+        mv[u] = __ldg(p + PARTIAL_M);
+        lv[u] = __ldg(p + PARTIAL_L);
+        ov[u] = __ldg(reinterpret_cast<const float4*>(p) + lane);
+      }
+    }
+    float mn = m;
+#pragma unroll
+    for (int u = 0; u < BF_MERGE_UNROLL; ++u) mn = fmaxf(mn, mv[u]);
+    if (mn == -INFINITY) continue;   // nothing seen yet (exp2f(-inf) is 0 from here on)
+    const float f = exp2f(m - mn);
+    l *= f;
+    acc.x *= f;
+    acc.y *= f;
+    acc.z *= f;
+    acc.w *= f;
+#pragma unroll
+    for (int u = 0; u < BF_MERGE_UNROLL; ++u) {
+      const float fu = exp2f(mv[u] - mn);
+      l = fmaf(lv[u], fu, l);
+      acc.x = fmaf(ov[u].x, fu, acc.x);
+      acc.y = fmaf(ov[u].y, fu, acc.y);
+      acc.z = fmaf(ov[u].z, fu, acc.z);
+      acc.w = fmaf(ov[u].w, fu, acc.w);
+    }
+    m = mn;
   }
-  out[((size_t)ri * a.Hq + hq) * D + t] = acc / L;
+  if (lane == 0) {
+    s_m[warp] = m;
+    s_l[warp] = l;
+  }
+  reinterpret_cast<float4*>(s_o[warp])[lane] = acc;
+  __syncthreads();
+  const int t = threadIdx.x;   // channel t (BF_MERGE_THREADS == D)
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < BF_MERGE_WARPS; ++w) M = fmaxf(M, s_m[w]);
+  float o = 0.0f, L = 0.0f;
+#pragma unroll
+  for (int w = 0; w < BF_MERGE_WARPS; ++w) {
+    if (s_m[w] == -INFINITY) continue;
+    const float f = exp2f(s_m[w] - M);
+    o = fmaf(s_o[w][t], f, o);
+    L = fmaf(s_l[w], f, L);
+  }
+  out[((size_t)ri * a.Hq + hq) * D + t] = o / L;
 }
 
 template <int G>
@@ -336,34 +393,56 @@ cudaError_t launch_bf16(const BfArgs& a, int blocks, const uint16_t* kv, const i
   bf16_stream_kernel<G><<<blocks, BF_THREADS, sizeof(BfSmem<G>), s>>>(a, kv, pt, q, partials, err);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  bf16_merge_kernel<G><<<a.n * a.Hq, BF_MERGE_THREADS, 0, s>>>(a, partials, out);
-  return cudaGetLastError();
+  // programmatic dependent launch: the merge's launch overlaps the stream grid's tail
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n * a.Hq);
+  cfg.blockDim = dim3(BF_MERGE_THREADS);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, bf16_merge_kernel<G>, a, static_cast<const float*>(partials), out);
 }
 
 constexpr int BF_CTAS_PER_SM = 3;
+constexpr int64_t BF_MAX_CHUNKS = 256;  // chunks per (request, kv head) the plan considers
 constexpr size_t BF_ERR_BYTES = 256;   // the error word, padded
 
-// Chunks per kv head of each request and pages per chunk: about one wave of blocks.
+// Chunks per kv head of each request and pages per chunk.  Blocks are equal in
+// size, so the grid runs in ceil(blocks / slots) rounds of ppc pages each; a
+// block also costs about one page of start-up and partial write.  The plan
+// takes the ppc (one of ceil(max pages / c)) with the least estimated time.
 int bf16_plan(int32_t n, const int32_t* lens, int32_t hkv, int sms, BfArgs& a) {
-  int64_t total = 0;
   int64_t max_np = 1;
-  for (int32_t i = 0; i < n; ++i) {
-    const int64_t np = (lens[i] + PAGE - 1) / PAGE;
-    total += hkv * np;
-    max_np = std::max(max_np, np);
+  for (int32_t i = 0; i < n; ++i) max_np = std::max<int64_t>(max_np, (lens[i] + PAGE - 1) / PAGE);
+  const int64_t slots = (int64_t)sms * BF_CTAS_PER_SM;
+  auto blocks_for = [&](int64_t ppc) {
+    int64_t b = 0;
+    for (int32_t i = 0; i < n; ++i) b += hkv * std::max<int64_t>(1, ((lens[i] + PAGE - 1) / PAGE + ppc - 1) / ppc);
+    return b;
+  };
+  int64_t best_ppc = max_np, best_cost = -1;
+  for (int64_t c = 1; c <= std::min<int64_t>(max_np, BF_MAX_CHUNKS); ++c) {
+    const int64_t ppc = (max_np + c - 1) / c;
+    const int64_t rounds = (blocks_for(ppc) + slots - 1) / slots;
+    const int64_t cost = rounds * (ppc + 1);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_ppc = ppc;
+    }
   }
-  const int64_t target = (int64_t)sms * BF_CTAS_PER_SM;
-  int64_t ppc = std::max<int64_t>(1, (total + target - 1) / target);
   int blocks = 0;
   for (int32_t i = 0; i < n; ++i) {
     const int64_t np = (lens[i] + PAGE - 1) / PAGE;
-    const int ch = static_cast<int>(std::max<int64_t>(1, (np + ppc - 1) / ppc));
+    const int ch = static_cast<int>(std::max<int64_t>(1, (np + best_ppc - 1) / best_ppc));
     a.block_start[i] = blocks;
     a.chunks[i] = ch;
     a.len[i] = lens[i];
     blocks += ch * hkv;
   }
-  a.ppc = static_cast<int>(ppc);
+  a.ppc = static_cast<int>(best_ppc);
   return blocks;
 }
 
