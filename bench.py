@@ -171,14 +171,14 @@ def algorithmic_bytes(tokens: int, hist_end: int, kv_heads: int) -> int:
 class Workload:
     """The cache, its rotations and every input of the timed steps, resident on the GPU."""
 
-    def __init__(self, cfg_id: int, steps_total: int, log, layers: int = 0):
+    def __init__(self, cfg_id: int, steps_total: int, log, layers: int = 0, override=None):
         import torch
         from bit_rotated_kv_decode_gb300 import binding, build, calibrate, synth
         build.build()
         self.torch = torch
         self.b = binding
         self.synth = synth
-        w = WORKLOADS[cfg_id]
+        w = dict(WORKLOADS[cfg_id], **(override or {}))
         self.cfg_id = cfg_id
         self.w = w
         self.L, self.hq, self.hkv, self.batch = w["layers"], w["q_heads"], w["kv_heads"], w["batch"]
@@ -254,6 +254,7 @@ class Workload:
         self.ws = binding.new_workspace(ws_bytes)
         self.step_index = 0
         self.fused = True
+        self.demote_first = False
         # raw C entry points with pre-marshalled arguments (the binding's own calls, minus re-marshalling)
         self.lib = self.cache.lib
         self.h = self.cache.h
@@ -273,6 +274,8 @@ class Workload:
         """One step: every layer appends (with demotion) and decodes."""
         lib, h, n, ra, ws, wl = self.lib, self.h, self.batch, self.reqs_arr, self.ws_ptr, self.ws_len
         append, decode, fused = lib.oscar_append, lib.oscar_decode_attention, lib.oscar_decode_step
+        if self.demote_first and lib.oscar_demote_layers(h, 0, self.L, n, ra, stream):
+            raise RuntimeError(f"demote failed: {lib.oscar_last_error(h).decode()}")
         if dec_events is None:
             for layer, (kp, vp, qp, op) in enumerate(ptrs):
                 if self.fused:
@@ -311,6 +314,7 @@ def run_gpu(args, log):
     ew, ek = 2, max(3, K // 2)
     wl = Workload(args.config, W + 2 * K + ew + ek, log, args.layers)
     wl.fused = not args.separate_calls
+    wl.demote_first = args.demote_first
     stream = wl.stream_ptr()
     L = wl.L
     ptrs = [wl.pointers(s) for s in range(W + 2 * K)]
@@ -385,7 +389,9 @@ def run_gpu(args, log):
         "us_step": us_step, "kv_bytes_step": kv_bytes_step, "dec_avg_us": dec_avg, "app_avg_us": app_avg, "bytes_per_launch": bpl,
         "achieved_gbs": achieved, "peak": peak, "peak_kind": peak_kind, "e2e_us": e2e_us, "h2d": h2d, "d2h": d2h,
         "launch_us": launch_us,
-        "clocks": clk.summary(), "launches": K * L * (3 if wl.fused else 4), "world": world, "rank": rank,
+        "clocks": clk.summary(),
+        "launches": K * (L * (3 if wl.fused else 4) + (-(-L * wl.batch // 96) if wl.demote_first else 0)),
+        "world": world, "rank": rank,
     }
     return wl, res
 
@@ -438,6 +444,59 @@ def bf16_baseline(wl, r, log, launches: int = 40):
             "launches_timed": launches,
             "int2_step_us_per_layer": int2_us, "speedup_of_int2_step": us / int2_us,
             "timing": "CUDA events around each call, two alternating layer pools larger than L2"}
+
+
+def speedup_table(args, log):
+    """INT2 cache vs the uncompressed BF16 baseline at the pages' decode shapes:
+    Qwen3-8B attention (32/8 heads), contexts 30K / 60K / 100K, batch 1 and 32.
+    Two layers per case, alternating (each layer's KV is read once per step, as in
+    a model), CUDA events around the whole loop of K steps."""
+    import torch
+    rows = []
+    K = max(10, min(args.steps, 40))
+    for batch in (1, 32):
+        for ctx in (30000, 60000, 100000):
+            wl = Workload(2, args.warmup + 2 * K, log, layers=2, override={"context": ctx, "batch": batch})
+            stream = wl.stream_ptr()
+            ptrs = [wl.pointers(s) for s in range(args.warmup + 2 * K)]
+            mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+            for s in range(args.warmup):
+                wl.run_step(ptrs[s], stream)
+            torch.cuda.synchronize()
+            a, b = mk(), mk()
+            a.record()
+            for i in range(K):
+                wl.run_step(ptrs[args.warmup + i], stream)
+            b.record()
+            torch.cuda.synchronize()
+            step_us = 1000.0 * a.elapsed_time(b) / (K * wl.L)
+            # decode alone (no append), same layers alternating
+            lib, h, n, ra = wl.lib, wl.h, wl.batch, wl.reqs_arr
+            a, b = mk(), mk()
+            a.record()
+            for i in range(K):
+                for layer, (_, _, qp, op) in enumerate(ptrs[args.warmup + K + i]):
+                    if lib.oscar_decode_attention(h, layer, n, ra, qp, op, wl.ws_ptr, wl.ws_len, stream):
+                        raise RuntimeError(lib.oscar_last_error(h).decode())
+            b.record()
+            torch.cuda.synchronize()
+            wl.cache.check()
+            dec_us = 1000.0 * a.elapsed_time(b) / (K * wl.L)
+            peak, kind = measured_peak_hbm()
+            bf = bf16_baseline(wl, {"us_step": step_us * wl.L, "peak": peak, "peak_kind": kind}, log, launches=K)
+            int2_bytes = np.mean([wl.decode_bytes(layer) for layer in range(wl.L)])
+            rows.append({"context": ctx, "batch": batch, "int2_step_us": step_us, "int2_decode_us": dec_us,
+                         "int2_decode_gbs": int2_bytes / (dec_us * 1e-6) / 1e9, "bf16_decode_us": bf["us_per_layer"],
+                         "bf16_gbs": bf["achieved_gbs"], "speedup_step": bf["us_per_layer"] / step_us,
+                         "speedup_decode": bf["us_per_layer"] / dec_us})
+            log(json.dumps(rows[-1]))
+            del wl
+            torch.cuda.empty_cache()
+    return {"table": "int2_vs_bf16_decode_per_layer", "model": "Qwen3-8B attention shape (32 q / 8 kv heads, d 128)",
+            "layers_alternated": 2, "steps": K, "warmup": args.warmup, "peak_gbs": measured_peak_hbm()[0],
+            "rows": rows,
+            "note": "us per layer; step = oscar_decode_step (append with demote + decode); decode = "
+                    "oscar_decode_attention alone; bf16 = oscar_bf16_decode over the same lengths"}
 
 
 # ----------------------------------------------------------------------------------------------
@@ -651,6 +710,11 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-bf16-baseline", action="store_true",
                     help="skip the uncompressed BF16 decode comparison")
+    ap.add_argument("--demote-first", action="store_true",
+                    help="each step starts with one oscar_demote_layers over all layers; the per-layer steps "
+                         "then only append")
+    ap.add_argument("--speedup-table", action="store_true",
+                    help="INT2 vs BF16 decode per layer at 30K / 60K / 100K, batch 1 and 32 (one JSON line)")
     ap.add_argument("--layers", type=int, default=0, help="fewer layers (small profiling cases only)")
     ap.add_argument("--separate-calls", action="store_true",
                     help="time oscar_append + oscar_decode_attention per layer instead of oscar_decode_step")
@@ -666,6 +730,11 @@ def main(argv=None):
         line = run_reference(args, log)
         if line is not None:
             print(json.dumps(line), flush=True)
+        return
+    if args.speedup_table:
+        import torch
+        torch.cuda.set_device(0)
+        print(json.dumps(speedup_table(args, log)), flush=True)
         return
     w = WORKLOADS[args.config]
     if w.get("write_path"):
@@ -699,9 +768,13 @@ def main(argv=None):
                        min(wl.lens), max(wl.lens), int(np.mean(wl.lens))),
                    "shared_prefix_tokens": wl.prefix, "page_tokens": 64, "page_order": "seeded shuffle",
                    "storage": "INT2 codes + fp16 scale/zero history, BF16 sink/recent",
-                   "step": ("per layer: oscar_decode_step (append with fused demote, then decode attention)"
-                            if not args.separate_calls else
-                            "per layer: oscar_append (fused demote) then oscar_decode_attention"),
+                   "step": (("oscar_demote_layers over all layers, then " if args.demote_first else "") +
+                            ("per layer: oscar_decode_step (append" +
+                             (", then decode attention)" if args.demote_first else
+                              " with fused demote, then decode attention)")
+                             if not args.separate_calls else
+                             "per layer: oscar_append" + ("" if args.demote_first else " (fused demote)") +
+                             " then oscar_decode_attention")),
                    "l2": "inputs larger than L2 (%.2f GB of KV per step vs 129 MB L2)" % (
                        r["bytes_per_launch"] * wl.L / 1e9),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
@@ -710,7 +783,7 @@ def main(argv=None):
         "kv_frac_of_8tbs_step": kv_gbs / NOMINAL_HBM_GBS,
         "decode_us_per_layer": r["dec_avg_us"],
         "append_us_per_layer": r["app_avg_us"],
-        "demote_tok_s": wl.batch * 1e6 / r["app_avg_us"],
+        "demote_tok_s": None if args.demote_first else wl.batch * 1e6 / r["app_avg_us"],
         "roofline": {"bound": "hbm", "kernel": "decode_stream_kernel", "achieved": r["achieved_gbs"], "peak": r["peak"],
                      "unit": "GB/s", "frac": r["achieved_gbs"] / r["peak"], "peak_source": r["peak_kind"],
                      "traffic": traffic, "algorithmic_bytes_per_launch": r["bytes_per_launch"],

@@ -71,6 +71,7 @@ _SIGNATURES = {
     "oscar_prefill_quantize": (c_int32, [_P, c_int32, c_int32, _P, _P, c_int64, _P]),
     "oscar_append": (c_int32, [_P, c_int32, c_int32, POINTER(c_int32), _P, _P, _P]),
     "oscar_demote": (c_int32, [_P, c_int32, c_int32, POINTER(c_int32), _P]),
+    "oscar_demote_layers": (c_int32, [_P, c_int32, c_int32, c_int32, POINTER(c_int32), _P]),
     "oscar_decode_workspace_bytes": (c_int32, [_P, c_int32, POINTER(c_int32), POINTER(c_size_t)]),
     "oscar_decode_attention": (c_int32, [_P, c_int32, c_int32, POINTER(c_int32), _P, _P, _P, c_size_t, _P]),
     "oscar_decode_attention_noalloc": (c_int32, [_P, c_int32, c_int32, POINTER(c_int32), _P, _P, _P]),
@@ -236,6 +237,12 @@ class OscarCache:
         arr = self._reqs(reqs)
         self._check(self.lib.oscar_demote(self.h, layer, len(reqs), arr, None if self.dry else _stream_ptr(stream)),
                     "demote", allow_dry=True)
+
+    def demote_layers(self, layer_begin: int, layer_end: int, reqs, stream=None) -> None:
+        arr = self._reqs(reqs)
+        self._check(self.lib.oscar_demote_layers(self.h, layer_begin, layer_end, len(reqs), arr,
+                                                 None if self.dry else _stream_ptr(stream)),
+                    "demote_layers", allow_dry=True)
 
     # -- decode -------------------------------------------------------------------
     def workspace_bytes(self, reqs) -> int:

@@ -602,6 +602,28 @@ oscar_status oscar_demote(oscar_cache* c, int32_t layer, int32_t n, const int32_
   return write_batch(c, layer, n, reqs, nullptr, nullptr, false, stream);
 }
 
+// Every layer's checks first (a page opened by one layer is reused by the
+// others, so checking each layer against the current free count is enough),
+// then each layer's state change in order, then the launches.
+oscar_status oscar_demote_layers(oscar_cache* c, int32_t layer_begin, int32_t layer_end, int32_t n,
+                                 const int32_t* reqs, void* stream) {
+  if (!c) return OSCAR_ERR_INVALID_ARG;
+  if (layer_begin < 0 || layer_end > c->cfg.num_layers || layer_begin >= layer_end)
+    return c->fail(OSCAR_ERR_INVALID_ARG, "bad layer range");
+  for (int32_t l = layer_begin; l < layer_end; ++l) {
+    const oscar_status st = validate_write(c, l, n, reqs, nullptr, nullptr, false);
+    if (st != OSCAR_OK) return st;
+  }
+  std::vector<DemoteEntry> work;
+  work.reserve((size_t)n * (size_t)(layer_end - layer_begin));
+  for (int32_t l = layer_begin; l < layer_end; ++l)
+    for (const AppendReq& a : apply_write(c, l, n, reqs, false)) work.push_back(DemoteEntry{l, a});
+  if (c->dry) return OSCAR_ERR_DRY_RUN;
+  const cudaError_t err =
+      launch_demote_layers(c->dc, work.data(), static_cast<int>(work.size()), static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? OSCAR_OK : c->cuda_fail(err, "demote launch");
+}
+
 oscar_status oscar_decode_workspace_bytes(const oscar_cache* c, int32_t n, const int32_t* reqs, size_t* bytes) {
   if (!c || !bytes) return OSCAR_ERR_INVALID_ARG;
   oscar_cache* mc = const_cast<oscar_cache*>(c);

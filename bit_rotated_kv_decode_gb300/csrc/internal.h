@@ -99,6 +99,13 @@ struct AppendReq {
 constexpr int APPEND_PER_LAUNCH = 48;
 cudaError_t launch_append(const DevCache& c, int layer, const AppendReq* reqs, int n, const uint16_t* k,
                           const uint16_t* v, cudaStream_t s);
+// Demotion of one (layer, request) in a multi-layer demote launch.
+struct DemoteEntry {
+  int32_t layer;
+  AppendReq r;              // in_row = -1: no new token
+};
+constexpr int DEMOTE_PER_LAUNCH = 96;   // kernel arguments stay under 4 KiB
+cudaError_t launch_demote_layers(const DevCache& c, const DemoteEntry* e, int n, cudaStream_t s);
 
 // ---- decode ---------------------------------------------------------------------
 struct DecodeReq {

@@ -347,6 +347,20 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(DevCache c, int 
   append_block(c, layer, k, v, a.r[blockIdx.x], blockIdx.y, blockIdx.z, sm);
 }
 
+struct DemoteArgs {
+  int n;
+  DemoteEntry e[DEMOTE_PER_LAUNCH];
+};
+
+// Multi-layer demote: block (entry, kv head, K or V), each entry one layer of
+// one request.  Layers write disjoint pool regions, and only the first layer
+// to open a history page writes its page-table entry.
+__global__ void __launch_bounds__(APPEND_THREADS) demote_layers_kernel(DevCache c, DemoteArgs a) {
+  __shared__ AppendSmem sm;
+  const DemoteEntry& e = a.e[blockIdx.x];
+  append_block(c, e.layer, nullptr, nullptr, e.r, blockIdx.y, blockIdx.z, sm);
+}
+
 }  // namespace
 
 cudaError_t launch_pt_update(const DevCache& c, const PtEntry* entries, int n, cudaStream_t s) {
@@ -421,6 +435,26 @@ cudaError_t launch_append(const DevCache& c, int layer, const AppendReq* reqs, i
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, append_kernel, c, layer, k, v, a);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_demote_layers(const DevCache& c, const DemoteEntry* entries, int n, cudaStream_t s) {
+  for (int base = 0; base < n; base += DEMOTE_PER_LAUNCH) {
+    DemoteArgs a;
+    a.n = n - base < DEMOTE_PER_LAUNCH ? n - base : DEMOTE_PER_LAUNCH;
+    for (int i = 0; i < a.n; ++i) a.e[i] = entries[base + i];
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.n), static_cast<unsigned>(c.Hkv), 2);
+    cfg.blockDim = dim3(APPEND_THREADS);
+    cfg.stream = s;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, demote_layers_kernel, c, a);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

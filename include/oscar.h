@@ -173,6 +173,22 @@ oscar_status oscar_append(oscar_cache* cache, int32_t layer, int32_t n, const in
  * shrinks by one).  reqs: host int32 [n], distinct. */
 oscar_status oscar_demote(oscar_cache* cache, int32_t layer, int32_t n, const int32_t* reqs, void* stream);
 
+/* Multi-layer demote: oscar_demote(l, n, reqs) for every layer l in
+ * [layer_begin, layer_end), with the same state changes and cache bytes, as one
+ * launch per 96 (layer, request) pairs.  The token leaving the recent window at
+ * a step is the same position in every layer and already sits in each layer's
+ * ring, so its demotion in all layers can run at the start of the step; the
+ * per-layer appends (or oscar_decode_step calls) that follow find room in the
+ * window and only write the new token ([MTP] section "The Serving System":
+ * write path; [MS] section "OSCAR的设计": the oldest recent token is demoted).
+ *   reqs  host int32 [n], distinct request ids.
+ * Errors: a bad layer range or batch is OSCAR_ERR_INVALID_ARG; a layer whose
+ * recent window is empty is OSCAR_ERR_STATE; too few free INT2 pages is
+ * OSCAR_ERR_OUT_OF_PAGES.  Every layer is checked before any change, so an
+ * error leaves the cache as it was. */
+oscar_status oscar_demote_layers(oscar_cache* cache, int32_t layer_begin, int32_t layer_end, int32_t n,
+                                 const int32_t* reqs, void* stream);
+
 /* Workspace bytes oscar_decode_attention needs for this batch. */
 oscar_status oscar_decode_workspace_bytes(const oscar_cache* cache, int32_t n, const int32_t* reqs,
                                           size_t* bytes);

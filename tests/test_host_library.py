@@ -56,7 +56,7 @@ def test_random_call_sequence_matches_mirror(b, seed):
     lib, mir = _pair(b, layers=2, max_req=4, max_pages=40, pages=120, seed=seed)
     live = []
     for step in range(400):
-        op = rng.integers(0, 10)
+        op = rng.integers(0, 11)
         try:
             if op == 0 and len(live) < 4:
                 r1 = mir.open()
@@ -111,6 +111,24 @@ def test_random_call_sequence_matches_mirror(b, seed):
                         lib.demote(layer, [r])
                     continue
                 lib.demote(layer, [r])
+            elif op == 10 and live:
+                # multi-layer demote: both layers of a batch, all checks before any change
+                batch = [int(r) for r in rng.choice(live, size=int(rng.integers(1, len(live) + 1)), replace=False)]
+                snapshot = {r: ([list(mir.reqs[r].T), list(mir.reqs[r].hist_end)], list(mir.reqs[r].hist_pt))
+                            for r in batch}
+                free0 = (mir.int2.stack[:], list(mir.int2.refs))
+                try:
+                    for layer in range(2):
+                        for r in batch:
+                            mir.demote(r, layer)
+                except (StateError, MemoryError):
+                    for r, ((t, he), pt) in snapshot.items():
+                        mir.reqs[r].T, mir.reqs[r].hist_end, mir.reqs[r].hist_pt = t, he, pt
+                    mir.int2.stack, mir.int2.refs = free0
+                    with pytest.raises(b.OscarError):
+                        lib.demote_layers(0, 2, batch)
+                    continue
+                lib.demote_layers(0, 2, batch)
             elif op == 9 and live and len(live) < 4:
                 par = live[int(rng.integers(len(live)))]
                 prefix = 64 + 64 * int(rng.integers(0, 4))
