@@ -440,6 +440,7 @@ def bf16_baseline(wl, r, log, launches: int = 40):
     log(f"bf16 baseline {us:.1f} us/layer ({gbs:.0f} GB/s); INT2 step {int2_us:.1f} us/layer")
     del pools
     return {"kernel": "bf16_stream_kernel + bf16_merge_kernel (oscar_bf16_decode)", "us_per_layer": us,
+            "traffic_stream_kernel": committed_traffic("bf16_stream_kernel"),
             "bytes_per_layer": nbytes, "achieved_gbs": gbs, "frac": gbs / r["peak"], "peak_source": r["peak_kind"],
             "launches_timed": launches,
             "int2_step_us_per_layer": int2_us, "speedup_of_int2_step": us / int2_us,
