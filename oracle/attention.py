@@ -37,7 +37,7 @@ def segments(total: int, hist_end: int):
 
 
 def reconstruct_head(k: np.ndarray, v: np.ndarray, hist_end: int, rk: np.ndarray, rv: np.ndarray,
-                     tau_k: float, tau_v: float, identity_quantizer: bool = False):
+                     tau_k: float, tau_v: float, identity_quantizer: bool = False, group: int = 128):
     """Keys / values [T][d] float64 as decode sees them, for one kv head."""
     total = k.shape[0]
     kt = np.array(k, dtype=np.float64, copy=True)
@@ -49,8 +49,8 @@ def reconstruct_head(k: np.ndarray, v: np.ndarray, hist_end: int, rk: np.ndarray
             kt[idx] = (k[idx] @ rk) @ rk.T
             vt[idx] = (v[idx] @ rv) @ rv.T
         else:
-            ck, sk, zk, _ = quant.quantize_tokens(k[idx], rk, np.float32(tau_k))
-            cv, sv, zv, _ = quant.quantize_tokens(v[idx], rv, np.float32(tau_v))
+            ck, sk, zk, _ = quant.quantize_tokens(k[idx], rk, np.float32(tau_k), group)
+            cv, sv, zv, _ = quant.quantize_tokens(v[idx], rv, np.float32(tau_v), group)
             kt[idx] = quant.dequantize(ck, sk, zk) @ rk.T
             vt[idx] = quant.dequantize(cv, sv, zv) @ rv.T
     return kt, vt
@@ -67,7 +67,7 @@ def softmax_attention(q: np.ndarray, keys: np.ndarray, values: np.ndarray, scale
 
 def decode(q: np.ndarray, k: np.ndarray, v: np.ndarray, hist_end: int, rk: np.ndarray, rv: np.ndarray,
            tau_k: np.ndarray, tau_v: np.ndarray, scale: float | None = None,
-           identity_quantizer: bool = False, heads=None) -> np.ndarray:
+           identity_quantizer: bool = False, heads=None, group: int = 128) -> np.ndarray:
     """Decode output [H_q][d] float64 of one request.
 
     q [H_q][d], k / v [T][H_kv][d] (float64 holding bf16 values), rk / rv
@@ -84,14 +84,14 @@ def decode(q: np.ndarray, k: np.ndarray, v: np.ndarray, hist_end: int, rk: np.nd
     kv_needed = sorted({h // g for h in want})
     for kvh in kv_needed:
         kt, vt = reconstruct_head(k[:, kvh], v[:, kvh], hist_end, rk[kvh], rv[kvh],
-                                  float(tau_k[kvh]), float(tau_v[kvh]), identity_quantizer)
+                                  float(tau_k[kvh]), float(tau_v[kvh]), identity_quantizer, group)
         for h in want:
             if h // g == kvh:
                 out[h] = softmax_attention(q[h], kt, vt, scale)
     return out
 
 
-def decode_naive(q, k, v, hist_end, rk, rv, tau_k, tau_v, scale=None):
+def decode_naive(q, k, v, hist_end, rk, rv, tau_k, tau_v, scale=None, group=128):
     """Per-token loop version of ``decode`` for tiny inputs."""
     hq, d = q.shape
     hkv = k.shape[1]
@@ -106,13 +106,15 @@ def decode_naive(q, k, v, hist_end, rk, rv, tau_k, tau_v, scale=None):
         vals = []
         for j in range(total):
             if SINK <= j < hist_end:
-                ck, sk, zk, _ = quant.quantize_tokens(k[j:j + 1, kvh], rk[kvh], np.float32(tau_k[kvh]))
-                cv, sv, zv, _ = quant.quantize_tokens(v[j:j + 1, kvh], rv[kvh], np.float32(tau_v[kvh]))
+                ck, sk, zk, _ = quant.quantize_tokens(k[j:j + 1, kvh], rk[kvh], np.float32(tau_k[kvh]), group)
+                cv, sv, zv, _ = quant.quantize_tokens(v[j:j + 1, kvh], rv[kvh], np.float32(tau_v[kvh]), group)
+                sk, zk, sv, zv = (np.reshape(a, (1, -1)) for a in (sk, zk, sv, zv))
                 kj = np.zeros(d)
                 vj = np.zeros(d)
                 for a in range(d):
-                    xk = float(zk[0]) + float(sk[0]) * float(ck[0, a])
-                    xv = float(zv[0]) + float(sv[0]) * float(cv[0, a])
+                    gi = a // group
+                    xk = float(zk[0, gi]) + float(sk[0, gi]) * float(ck[0, a])
+                    xv = float(zv[0, gi]) + float(sv[0, gi]) * float(cv[0, a])
                     for b in range(d):
                         kj[b] += xk * rk[kvh][b, a]
                         vj[b] += xv * rv[kvh][b, a]

@@ -160,17 +160,18 @@ class CacheMirror:
 
 
 def expected_history(k_head: np.ndarray, v_head: np.ndarray, rk: np.ndarray, rv: np.ndarray,
-                     tau_k: float, tau_v: float):
+                     tau_k: float, tau_v: float, group: int = 128):
     """Codes / meta of history tokens of one head (rows of k_head, v_head).
 
-    Returns dict of packed K/V code bytes [n][32], meta bytes [n][4], the raw
-    codes, s, z and the fp32 rotated values (for exemption bands).
+    Returns dict of packed K/V code bytes [n][32], meta bytes [n][4 * groups],
+    the raw codes, s, z and the fp32 rotated values (for exemption bands).
     """
-    ck, sk, zk, xk = quant.quantize_tokens(k_head, rk, np.float32(tau_k))
-    cv, sv, zv, xv = quant.quantize_tokens(v_head, rv, np.float32(tau_v))
+    ck, sk, zk, xk = quant.quantize_tokens(k_head, rk, np.float32(tau_k), group)
+    cv, sv, zv, xv = quant.quantize_tokens(v_head, rv, np.float32(tau_v), group)
+    ng = layout.HEAD_DIM // group
     return {
         "k_packed": layout.pack_codes(ck), "v_packed": layout.pack_codes(cv),
-        "k_meta": layout.meta_bytes(sk, zk), "v_meta": layout.meta_bytes(sv, zv),
+        "k_meta": layout.meta_bytes(sk, zk, ng), "v_meta": layout.meta_bytes(sv, zv, ng),
         "k_codes": ck, "v_codes": cv, "k_s": sk, "k_z": zk, "v_s": sv, "v_z": zv,
         "k_x32": xk, "v_x32": xv,
     }

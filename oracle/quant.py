@@ -4,7 +4,9 @@
 path each token is rotated, clipped to a calibration-derived threshold, then
 quantised with per-token asymmetric INT2.  [MS] section "OSCAR的设计": the read
 side dequantises with a scale and a zero point; [MS] section "快速实践": group
-size 128 (``--kv-cache-quant-group-size 128``), i.e. one group per token-head.
+size 128 (``--kv-cache-quant-group-size 128``), i.e. one group per token-head;
+[MTP] section "What OSCAR Does Differently" names G_K = 64 channels per group
+as the default, i.e. two groups per token-head, each with its own s and z.
 
 Readings (the pages give no formula):
   * x = k . R evaluated exactly, then rounded once to fp32 -- fp32 is the
@@ -15,7 +17,9 @@ Readings (the pages give no formula):
   * z = fp16_rn(min x), s = fp16_rn(fl32(fl32(max x - min x) / 3));
   * code = clamp(rint_half_even(fl32(fl32(x - z) / s)), 0, 3), code = 0 when
     s == 0;
-  * dequantised value x_hat = z + s * code (exact real arithmetic).
+  * dequantised value x_hat = z + s * code (exact real arithmetic);
+  * with G_K = 64, every step above is taken per group of 64 consecutive
+    rotated channels (0..63 and 64..127), independently.
 Every fp32 / fp16 operation above is IEEE round-to-nearest-even.  Pinned by
 closed-form groups, round-half-even ties, brute-force nearest-level search and
 the reconstruction error bound (tests/test_oracle_quant.py).
@@ -78,45 +82,73 @@ def rotate_to_fp32(x: np.ndarray, r: np.ndarray) -> np.ndarray:
     return y32
 
 
-def quantize_groups(x32: np.ndarray, tau: np.float32):
-    """Clip and quantise each row (one 128-channel group) of fp32 values.
+def _split(a: np.ndarray, group: int) -> np.ndarray:
+    """[..., d] -> [..., d // group, group] (consecutive channels per group)."""
+    d = a.shape[-1]
+    if group <= 0 or d % group:
+        raise ValueError("group size must divide the channel count")
+    return a.reshape(a.shape[:-1] + (d // group, group))
 
-    Returns (codes uint8 [..., d], s float16 [...], z float16 [...]).
+
+def _per_group(meta: np.ndarray, codes_shape) -> np.ndarray:
+    """s or z as [..., groups, 1]: one group when meta has one axis fewer than the codes."""
+    meta = np.asarray(meta)
+    if meta.ndim == len(codes_shape) - 1:
+        meta = meta[..., None]
+    return meta[..., None]
+
+
+def quantize_groups(x32: np.ndarray, tau: np.float32, group: int = 128):
+    """Clip and quantise each group of ``group`` consecutive channels of fp32 values.
+
+    Returns (codes uint8 [..., d], s float16, z float16); s and z are [...] when
+    the group is the whole row (d == group), else [..., d // group].
     """
     x32 = np.asarray(x32, dtype=np.float32)
     tau = np.float32(tau)
     xc = (np.minimum(np.maximum(x32, -tau), tau) + np.float32(0.0)).astype(np.float32)
-    mn = xc.min(axis=-1)
-    mx = xc.max(axis=-1)
+    xg = _split(xc, group)
+    mn = xg.min(axis=-1)
+    mx = xg.max(axis=-1)
     z = mn.astype(np.float16)
     rng = (mx - mn).astype(np.float32)
     s = (rng / np.float32(3.0)).astype(np.float32).astype(np.float16)
     zf = z.astype(np.float32)[..., None]
     sf = s.astype(np.float32)[..., None]
     with np.errstate(divide="ignore", invalid="ignore"):
-        t = ((xc - zf).astype(np.float32) / sf).astype(np.float32)
+        t = ((xg - zf).astype(np.float32) / sf).astype(np.float32)
     code = np.clip(np.rint(t), 0, MAX_CODE)
-    code = np.where(sf == 0, 0, code)
+    code = np.where(sf == 0, 0, code).reshape(xc.shape)
+    if xg.shape[-2] == 1:
+        s, z = s[..., 0], z[..., 0]
     return code.astype(np.uint8), s, z
 
 
 def t_values(x32: np.ndarray, tau: np.float32, s: np.ndarray, z: np.ndarray) -> np.ndarray:
-    """The fp32 t = (clip(x) - z) / s each code was rounded from (for exemption bands)."""
+    """The fp32 t = (clip(x) - z) / s each code was rounded from (for exemption bands).
+
+    s, z as returned by quantize_groups (one group per row, or [..., groups])."""
     tau = np.float32(tau)
-    xc = (np.minimum(np.maximum(np.asarray(x32, np.float32), -tau), tau) + np.float32(0.0)).astype(np.float32)
-    zf = z.astype(np.float32)[..., None]
-    sf = s.astype(np.float32)[..., None]
+    x32 = np.asarray(x32, np.float32)
+    xc = (np.minimum(np.maximum(x32, -tau), tau) + np.float32(0.0)).astype(np.float32)
+    zf = _per_group(z, x32.shape).astype(np.float32)
+    sf = _per_group(s, x32.shape).astype(np.float32)
+    xg = _split(xc, x32.shape[-1] // zf.shape[-2])
     with np.errstate(divide="ignore", invalid="ignore"):
-        return ((xc - zf).astype(np.float32) / sf).astype(np.float32)
+        return ((xg - zf).astype(np.float32) / sf).astype(np.float32).reshape(x32.shape)
 
 
 def dequantize(codes: np.ndarray, s: np.ndarray, z: np.ndarray) -> np.ndarray:
-    """x_hat = z + s * code in float64."""
-    return z.astype(np.float64)[..., None] + s.astype(np.float64)[..., None] * codes.astype(np.float64)
+    """x_hat = z + s * code in float64, per group (s, z as from quantize_groups)."""
+    codes = np.asarray(codes)
+    zf = _per_group(z, codes.shape).astype(np.float64)
+    sf = _per_group(s, codes.shape).astype(np.float64)
+    cg = _split(codes.astype(np.float64), codes.shape[-1] // zf.shape[-2])
+    return (zf + sf * cg).reshape(codes.shape)
 
 
-def quantize_tokens(x: np.ndarray, r: np.ndarray, tau: np.float32):
+def quantize_tokens(x: np.ndarray, r: np.ndarray, tau: np.float32, group: int = 128):
     """Rotate (exact, rounded to fp32), clip and quantise token rows of one head."""
     x32 = rotate_to_fp32(x, r)
-    codes, s, z = quantize_groups(x32, tau)
+    codes, s, z = quantize_groups(x32, tau, group)
     return codes, s, z, x32
