@@ -106,8 +106,8 @@ def exported_symbols() -> list[str]:
 
 
 def make_config(num_layers, num_q_heads, num_kv_heads, max_requests, max_pages_per_request, num_int2_pages,
-                num_bf16_pages=0, softmax_scale=0.0, page_perm_seed=0) -> oscar_cache_config:
-    return oscar_cache_config(num_layers, num_q_heads, num_kv_heads, HEAD_DIM, 64, 256, 64, 128, max_requests,
+                num_bf16_pages=0, softmax_scale=0.0, page_perm_seed=0, group_size=128) -> oscar_cache_config:
+    return oscar_cache_config(num_layers, num_q_heads, num_kv_heads, HEAD_DIM, 64, 256, 64, group_size, max_requests,
                               max_pages_per_request, num_int2_pages, num_bf16_pages, softmax_scale, page_perm_seed)
 
 
@@ -278,9 +278,10 @@ class OscarCache:
     # -- views of device memory (for tests and inspection) ------------------------
     def int2_pool(self, layer: int):
         lay = self.layout()
-        n = self.cfg.num_int2_pages * self.cfg.num_kv_heads * RECORD_BYTES
+        rec = lay.int2_record_bytes          # 4608 (group 128) or 5120 (group 64)
+        n = self.cfg.num_int2_pages * self.cfg.num_kv_heads * rec
         base = lay.int2_pool_offset + layer * lay.int2_layer_stride
-        return self.mem[base:base + n].view(self.cfg.num_int2_pages, self.cfg.num_kv_heads, RECORD_BYTES)
+        return self.mem[base:base + n].view(self.cfg.num_int2_pages, self.cfg.num_kv_heads, rec)
 
     def bf16_pool(self, layer: int):
         import torch

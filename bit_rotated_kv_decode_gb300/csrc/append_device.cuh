@@ -19,7 +19,29 @@ __device__ __forceinline__ uint16_t* bf16_row(const DevCache& c, int layer, int 
 }
 
 __device__ __forceinline__ uint8_t* int2_record(const DevCache& c, int layer, int page, int head) {
-  return c.int2 + layer * c.int2_layer_stride + ((size_t)page * c.Hkv + head) * RECORD;
+  return c.int2 + layer * c.int2_layer_stride + ((size_t)page * c.Hkv + head) * c.record;
+}
+
+// The lane's group code into a record at token slot `slot`: code bytes from every
+// lane, then {s, z} from the first lane of each group (lane 0; lanes 0 and 16 at
+// G_K = 64).
+__device__ __forceinline__ void store_group_code(const DevCache& c, uint8_t* rec, int which, int slot,
+                                                 const GroupCode& g) {
+  const int lane = threadIdx.x & 31;
+  rec[(which ? V_CODES_OFF : K_CODES_OFF) + slot * CODE_BYTES + lane] = static_cast<uint8_t>(g.byte);
+  const int lanes_per_group = c.gk / 4;
+  if ((lane & (lanes_per_group - 1)) == 0) {
+    const int mb = meta_bytes_for(c.gk);
+    const int off = which ? v_meta_off_for(c.gk) : k_meta_off_for(c.gk);
+    *reinterpret_cast<uint32_t*>(rec + off + slot * mb + 4 * (lane / lanes_per_group)) =
+        static_cast<uint32_t>(g.s_bits) | (static_cast<uint32_t>(g.z_bits) << 16);
+  }
+}
+
+// quantize_group_warp for the cache's group size (warp-uniform branch)
+__device__ __forceinline__ GroupCode quantize_for(const DevCache& c, float4 x, float4 e, float4 sb, float tau,
+                                                  float4 k4, const float* __restrict__ rt) {
+  return c.gk == 64 ? quantize_group_warp<64>(x, e, sb, tau, k4, rt) : quantize_group_warp<128>(x, e, sb, tau, k4, rt);
 }
 
 constexpr int APPEND_THREADS = 256;
@@ -108,14 +130,9 @@ __device__ __forceinline__ void append_block(const DevCache& c, int layer, const
         const float tau = (which ? c.tau_v : c.tau_k)[lh];
         const float* __restrict__ Rt = (which ? c.rot_vt : c.rot_kt) + lh * D * D;
         const float4 k4 = make_float4(xin[4 * lane], xin[4 * lane + 1], xin[4 * lane + 2], xin[4 * lane + 3]);
-        const GroupCode g = quantize_group_warp(make_float4(x[0], x[1], x[2], x[3]), make_float4(e[0], e[1], e[2], e[3]),
-                                                make_float4(sabs[0], sabs[1], sabs[2], sabs[3]), tau, k4, Rt);
-        uint8_t* rec = int2_record(c, layer, q.hist_page, head);
-        rec[(which ? V_CODES_OFF : K_CODES_OFF) + q.demote_slot * CODE_BYTES + lane] = static_cast<uint8_t>(g.byte);
-        if (lane == 0) {
-          *reinterpret_cast<uint32_t*>(rec + (which ? V_META_OFF : K_META_OFF) + q.demote_slot * META_BYTES) =
-              static_cast<uint32_t>(g.s_bits) | (static_cast<uint32_t>(g.z_bits) << 16);
-        }
+        const GroupCode g = quantize_for(c, make_float4(x[0], x[1], x[2], x[3]), make_float4(e[0], e[1], e[2], e[3]),
+                                         make_float4(sabs[0], sabs[1], sabs[2], sabs[3]), tau, k4, Rt);
+        store_group_code(c, int2_record(c, layer, q.hist_page, head), which, q.demote_slot, g);
       }
       if (q.pt_index >= 0 && head == 0 && which == 0 && t == 0) {
         c.hist_pt[(size_t)q.slot * c.max_pages + q.pt_index] = q.hist_page;

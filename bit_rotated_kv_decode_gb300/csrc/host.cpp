@@ -123,7 +123,7 @@ bool config_ok(const oscar_cache_config* c, std::string* why) {
   if (c->sink_tokens != SINK) return bad("sink_tokens must be 64");
   if (c->recent_tokens != RECENT) return bad("recent_tokens must be 256");
   if (c->page_tokens != PAGE) return bad("page_tokens must be 64");
-  if (c->group_size != D) return bad("group_size must be 128");
+  if (c->group_size != D && c->group_size != 64) return bad("group_size must be 128 or 64");
   if (c->num_layers < 1 || c->num_kv_heads < 1 || c->num_q_heads < 1) return bad("layer / head counts must be >= 1");
   if (c->num_q_heads % c->num_kv_heads != 0) return bad("num_q_heads must be a multiple of num_kv_heads");
   const int g = c->num_q_heads / c->num_kv_heads;
@@ -141,8 +141,8 @@ oscar_cache_layout make_layout(const oscar_cache_config& c) {
   const size_t L = c.num_layers, H = c.num_kv_heads;
   const size_t nb = c.num_bf16_pages == 0 ? (size_t)BF16_PAGES_PER_REQ * c.max_requests : (size_t)c.num_bf16_pages;
   size_t off = 0;
-  l.int2_record_bytes = RECORD;
-  l.int2_page_stride = H * RECORD;
+  l.int2_record_bytes = record_for(c.group_size);
+  l.int2_page_stride = H * l.int2_record_bytes;
   l.int2_layer_stride = align256((size_t)c.num_int2_pages * l.int2_page_stride);
   l.int2_pool_offset = off;
   off += L * l.int2_layer_stride;
@@ -223,6 +223,8 @@ oscar_status oscar_cache_create(const oscar_cache_config* cfg, void* device_mem,
   d.n_int2_pages = c->cfg.num_int2_pages;
   d.n_bf16_pages = c->cfg.num_bf16_pages;
   d.scale = c->cfg.softmax_scale;
+  d.gk = c->cfg.group_size;
+  d.record = record_for(c->cfg.group_size);
   if (c->dry) {
     *out = c;
     return OSCAR_OK;
@@ -583,6 +585,7 @@ size_t decode_bytes_needed(const oscar_cache* c, int32_t layer, int32_t n, const
 
 oscar_status check_decode_batch(oscar_cache* c, int32_t layer, int32_t n, const int32_t* reqs) {
   if (!c->valid_layer(layer) || n < 1 || !reqs) return c->fail(OSCAR_ERR_INVALID_ARG, "bad layer or batch");
+  if (c->cfg.group_size != D) return c->fail(OSCAR_ERR_INVALID_ARG, "decode needs group_size 128");
   for (int32_t i = 0; i < n; ++i) {
     if (!c->valid_req(reqs[i])) return c->fail(OSCAR_ERR_INVALID_ARG, "bad request id");
     if (c->reqs[reqs[i]].T[layer] < 1) return c->fail(OSCAR_ERR_STATE, "request has no cached tokens");

@@ -23,6 +23,13 @@ constexpr int K_META_OFF = 2 * PAGE * CODE_BYTES;          // 4096
 constexpr int V_META_OFF = K_META_OFF + PAGE * META_BYTES; // 4352
 constexpr int RECORD = V_META_OFF + PAGE * META_BYTES;     // 4608
 constexpr int BF16_RECORD_ELEMS = 2 * PAGE * D;            // K rows then V rows
+// INT2 record of a quantisation group size gk (128: the layout above; 64: two
+// {s, z} per token, K meta [4096, 4608), V meta [4608, 5120))
+__host__ __device__ constexpr int meta_bytes_for(int gk) { return META_BYTES * (D / gk); }
+__host__ __device__ constexpr int k_meta_off_for(int) { return 2 * PAGE * CODE_BYTES; }
+__host__ __device__ constexpr int v_meta_off_for(int gk) { return k_meta_off_for(gk) + PAGE * meta_bytes_for(gk); }
+__host__ __device__ constexpr int record_for(int gk) { return v_meta_off_for(gk) + PAGE * meta_bytes_for(gk); }
+static_assert(record_for(128) == RECORD && record_for(64) == 5120, "record sizes");
 constexpr int MAX_G = 8;
 // decode partial per (work item, query head): o[128], m, l, 2 floats of padding
 // (a multiple of 16 bytes so o can be moved with 16-byte vector accesses)
@@ -52,6 +59,8 @@ struct DevCache {
   int32_t* bf16_pt;              // [max_requests][5]
   int32_t* err;
   int32_t L, Hq, Hkv, G, max_pages;
+  int32_t gk;                    // quantisation group size: 128 or 64
+  int32_t record;                // record_for(gk) bytes per (page, kv head)
   int64_t n_int2_pages, n_bf16_pages;
   float scale;
 };

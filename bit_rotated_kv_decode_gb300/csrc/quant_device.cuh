@@ -1,4 +1,7 @@
-// Device-side INT2 quantiser of one 128-channel token-head group.
+// Device-side INT2 quantiser of the groups of one 128-channel token-head: one
+// group of 128 channels, or two of 64 (G_K = 64: channels 0..63 and 64..127,
+// each with its own scale and zero; "Together AI Open-Sources OSCAR"
+// (MarkTechPost), section "What OSCAR Does Differently").
 //
 // Write path of "Together AI Open-Sources OSCAR" (MarkTechPost), section "The
 // Serving System: Mixed-Precision Cache Layout": rotate, clip to the stored
@@ -138,14 +141,20 @@ __device__ __forceinline__ void warp_dot2(float4 k, float4 r, float S, float& lo
   hi = __fadd_ru(__fadd_ru(s, c), E);
 }
 
-// A full warp holds the group: lane l owns channels 4l .. 4l+3 with rotated
+// A full warp holds the token-head: lane l owns channels 4l .. 4l+3 with rotated
 // values x (fast path), their error bounds ev and S >= sum_i |k_i R_i,ch| (sv);
 // k holds the token's input channels 4l .. 4l+3 and rt points at R^T (row ch =
 // column ch of R).  A value whose interval leaves a decision open is narrowed
 // first by warp_dot2 (cheap, fp32) and only then, if still open, computed
-// exactly by warp_exact_dot (fp64).
+// exactly by warp_exact_dot (fp64).  With GK = 64, lanes 0..15 hold group 0 and
+// lanes 16..31 group 1: the min / max reductions stay within a half-warp, each
+// lane's scale and zero are its group's, and the warp-wide narrowing loops run
+// when either group needs them (only that group's values are candidates).
+template <int GK = 128>
 __device__ __forceinline__ GroupCode quantize_group_warp(float4 xv, float4 ev, float4 sv, float tau, float4 k,
                                                          const float* __restrict__ rt) {
+  static_assert(GK == 128 || GK == 64, "group of 128 or 64 channels");
+  constexpr int RED0 = GK / 8;   // first butterfly offset: lanes of one group
   const int lane = threadIdx.x & 31;
   const float x[4] = {xv.x, xv.y, xv.z, xv.w};
   const float er[4] = {ev.x, ev.y, ev.z, ev.w};
@@ -161,12 +170,12 @@ __device__ __forceinline__ GroupCode quantize_group_warp(float4 xv, float4 ev, f
   }
   auto reduce_min = [](float v) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    for (int off = RED0; off > 0; off >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, off));
     return v;
   };
   auto reduce_max = [](float v) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    for (int off = RED0; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
     return v;
   };
   auto exact = [&](int ch) {
@@ -189,15 +198,15 @@ __device__ __forceinline__ GroupCode quantize_group_warp(float4 xv, float4 ev, f
   float mx_hi = reduce_max(fmaxf(fmaxf(hi[0], hi[1]), fmaxf(hi[2], hi[3])));
   bool meta_sure = __half_as_ushort(__float2half_rn(mn_lo)) == __half_as_ushort(__float2half_rn(mn_hi)) &&
                    scale_of(mx_lo, mn_hi) == scale_of(mx_hi, mn_lo);
-  if (!meta_sure) {
-    // (warp-uniform) the group's min or max is too close to an fp16 rounding
-    // boundary: narrow every value that could be the min (its interval reaches
+  if (__any_sync(0xffffffffu, !meta_sure)) {
+    // a group's min or max is too close to an fp16 rounding boundary: narrow
+    // every value of that group that could be the min (its interval reaches
     // below mn_hi) or the max (reaches above mx_lo) and is not already a single
     // point (a clipped value is); then decide again.
     uint32_t cand = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      if (lo[i] != hi[i] && (lo[i] <= mn_hi || hi[i] >= mx_lo)) cand |= 1u << i;
+      if (!meta_sure && lo[i] != hi[i] && (lo[i] <= mn_hi || hi[i] >= mx_lo)) cand |= 1u << i;
     uint32_t todo = __ballot_sync(0xffffffffu, cand != 0);
     while (todo) {
       const int src = __ffs(todo) - 1;
@@ -222,13 +231,13 @@ __device__ __forceinline__ GroupCode quantize_group_warp(float4 xv, float4 ev, f
     meta_sure = __half_as_ushort(__float2half_rn(mn_lo)) == __half_as_ushort(__float2half_rn(mn_hi)) &&
                 scale_of(mx_lo, mn_hi) == scale_of(mx_hi, mn_lo);
   }
-  if (!meta_sure) {
+  if (__any_sync(0xffffffffu, !meta_sure)) {
     // (rare) still open: take exactly every candidate of the min or the max.  The
     // others lie strictly inside, so the extremes become exact.
     uint32_t cand = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      if (lo[i] != hi[i] && (lo[i] <= mn_hi || hi[i] >= mx_lo)) cand |= 1u << i;
+      if (!meta_sure && lo[i] != hi[i] && (lo[i] <= mn_hi || hi[i] >= mx_lo)) cand |= 1u << i;
     uint32_t todo = __ballot_sync(0xffffffffu, cand != 0);
     while (todo) {
       const int src = __ffs(todo) - 1;

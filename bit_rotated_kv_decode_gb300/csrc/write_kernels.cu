@@ -316,8 +316,8 @@ __global__ void __launch_bounds__(PF_THREADS, 2) prefill_hist_kernel(DevCache c,
                                     __uint_as_float(kw.y << 16), __uint_as_float(kw.y & 0xffff0000u));
       const float sbound = __fmul_ru(__fsqrt_ru(__fmul_ru(sm.kn[j], 1.0001f)), colnorm);   // >= sum_i |k_i R_ic|
       const float err = __fmul_ru(sbound, PF_MMA_ERR);
-      const GroupCode g = quantize_group_warp(x, make_float4(err, err, err, err),
-                                              make_float4(sbound, sbound, sbound, sbound), tau, k4, Rt);
+      const GroupCode g = quantize_for(c, x, make_float4(err, err, err, err),
+                                       make_float4(sbound, sbound, sbound, sbound), tau, k4, Rt);
       const int64_t h = t0 + j - SINK;
       const int32_t page = sm.pages[h / PAGE - (t0 - SINK) / PAGE];
       const int row = static_cast<int>(h % PAGE);
@@ -325,12 +325,7 @@ __global__ void __launch_bounds__(PF_THREADS, 2) prefill_hist_kernel(DevCache c,
         if (lane == 0) atomicOr(c.err, ERR_INT2_PAGE);
         continue;
       }
-      uint8_t* rec = int2_record(c, layer, page, head);
-      rec[(which ? V_CODES_OFF : K_CODES_OFF) + row * CODE_BYTES + lane] = static_cast<uint8_t>(g.byte);
-      if (lane == 0) {
-        *reinterpret_cast<uint32_t*>(rec + (which ? V_META_OFF : K_META_OFF) + row * META_BYTES) =
-            static_cast<uint32_t>(g.s_bits) | (static_cast<uint32_t>(g.z_bits) << 16);
-      }
+      store_group_code(c, int2_record(c, layer, page, head), which, row, g);
     }
   }
 }

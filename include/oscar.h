@@ -62,8 +62,13 @@ typedef struct oscar_cache oscar_cache;
 
 /* Geometry of a cache.  The fixed fields follow the pages: head_dim 128,
  * sink 64 and recent 256 tokens ([MTP] section "The Serving System"), group
- * size 128 ([MS] section "快速实践", --kv-cache-quant-group-size 128), and
- * 64-token pages (a reading: the pages name no page size). */
+ * size 128 ([MS] section "快速实践", --kv-cache-quant-group-size 128) or 64
+ * ([MTP] section "What OSCAR Does Differently": G_K = 64 by default), and
+ * 64-token pages (a reading: the pages name no page size).  With group size 64
+ * each token-head has two {fp16 s, fp16 z} pairs (channels 0..63, 64..127)
+ * and a record is 5120 bytes: K codes [0, 2048), V codes [2048, 4096), K meta
+ * [4096, 4608) with token slot r at 4096 + 8 r (group 0's s, z, then group
+ * 1's), V meta [4608, 5120) the same way. */
 typedef struct {
   int32_t num_layers;
   int32_t num_q_heads;             /* multiple of num_kv_heads, G = q/kv <= 8   */
@@ -72,7 +77,7 @@ typedef struct {
   int32_t sink_tokens;             /* must be 64                                */
   int32_t recent_tokens;           /* must be 256                               */
   int32_t page_tokens;             /* must be 64                                */
-  int32_t group_size;              /* must be 128                               */
+  int32_t group_size;              /* 128, or 64 (two groups per token-head)    */
   int32_t max_requests;            /* request slots                             */
   int32_t max_pages_per_request;   /* INT2 pages one request may hold           */
   int64_t num_int2_pages;          /* physical INT2 pages (shared by layers)   */

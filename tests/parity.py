@@ -32,21 +32,25 @@ def near_fp16_midpoint(v32: np.ndarray) -> np.ndarray:
 
 
 def _t_near_boundary(t: np.ndarray) -> np.ndarray:
-    frac = t - np.floor(t)
+    # t is nan / inf in a constant group (s = 0), whose codes are all 0 on both sides
+    with np.errstate(invalid="ignore"):
+        frac = t - np.floor(t)
     return (np.abs(frac - 0.5) <= BAND * np.maximum(1.0, np.abs(t))) & (t > 0) & (t < 3)
 
 
-def compare_groups(gpu_packed, gpu_meta, x32, tau):
-    """Compare GPU code bytes [n][32] and meta [n][4] of one head / K-or-V with the oracle.
+def compare_groups(gpu_packed, gpu_meta, x32, tau, group=128):
+    """Compare GPU code bytes [n][32] and meta [n][4 * groups] of one head / K-or-V
+    with the oracle.
 
-    x32: oracle fp32 rotated values [n][128].  Returns a dict of counts; raises
+    x32: oracle fp32 rotated values [n][128].  With group = 64 every token-head is
+    two groups, compared as rows of their own.  Returns a dict of counts; raises
     AssertionError on any out-of-band difference.
     """
-    x32 = np.asarray(x32, np.float32)
+    x32 = np.asarray(x32, np.float32).reshape(-1, group)
     tau = np.float32(tau)
-    codes_o, s_o, z_o = quant.quantize_groups(x32, tau)
-    s_g, z_g = layout.meta_to_sz(np.asarray(gpu_meta, np.uint8))
-    codes_g = layout.unpack_codes(np.asarray(gpu_packed, np.uint8))
+    codes_o, s_o, z_o = quant.quantize_groups(x32, tau, group)
+    s_g, z_g = layout.meta_to_sz(np.asarray(gpu_meta, np.uint8).reshape(-1, 4))
+    codes_g = layout.unpack_codes(np.asarray(gpu_packed, np.uint8)).reshape(-1, group)
     xc = (np.minimum(np.maximum(x32, -tau), tau) + np.float32(0)).astype(np.float32)
     mn = xc.min(1)
     mx = xc.max(1)

@@ -39,12 +39,13 @@ def rotations(cfg_id, layers, hq, hkv, drift=False):
 
 class Setup:
     def __init__(self, b, cfg_id=0, layers=1, hq=32, hkv=8, max_req=4, max_pages=64, pages=256, seed=0,
-                 drift=False, total_len=0):
+                 drift=False, total_len=0, group=128):
         self.b = b
+        self.group = group
         self.cfg_id, self.L, self.hq, self.hkv = cfg_id, layers, hq, hkv
         self.drift, self.total_len = drift, total_len
         self.rk, self.rv, self.tk, self.tv = rotations(cfg_id, layers, hq, hkv, drift)
-        cfg = b.make_config(layers, hq, hkv, max_req, max_pages, pages, 0, 0.0, seed)
+        cfg = b.make_config(layers, hq, hkv, max_req, max_pages, pages, 0, 0.0, seed, group_size=group)
         self.cache = b.OscarCache(cfg, torch.from_numpy(self.rk).cuda(), torch.from_numpy(self.rv).cuda(),
                                   self.tk, self.tv)
         self.mirror = CacheMirror(layers, hkv, max_req, max_pages, pages, 5 * max_req, seed)
@@ -102,7 +103,7 @@ class Setup:
         he = self.mirror.reqs[r].hist_end[layer]
         return attention.decode(parity.bf16_to_f64(q_row), parity.bf16_to_f64(k), parity.bf16_to_f64(v), he,
                                 self.rk[layer].astype(np.float64), self.rv[layer].astype(np.float64),
-                                self.tk[layer], self.tv[layer])
+                                self.tk[layer], self.tv[layer], group=self.group)
 
     def check_pages(self, r, layer):
         """Page tables exact; every history group within the parity rules; BF16 rows exact."""
@@ -123,14 +124,16 @@ class Setup:
             rows = (pos - 64) % 64
             for h in range(self.hkv):
                 rec = pool[pages, h]
+                lay = layout.record_layout(self.group)
+                mb = lay["meta_bytes"]
                 for which, src, rr, tau in ((0, kf, self.rk, self.tk), (1, vf, self.rv, self.tv)):
-                    off_c = layout.V_CODES_OFF if which else layout.K_CODES_OFF
-                    off_m = layout.V_META_OFF if which else layout.K_META_OFF
+                    off_c = lay["v_codes"] if which else lay["k_codes"]
+                    off_m = lay["v_meta"] if which else lay["k_meta"]
                     codes = np.stack([rec[i, off_c + 32 * rows[i]: off_c + 32 * rows[i] + 32] for i in range(nh)])
-                    meta = np.stack([rec[i, off_m + 4 * rows[i]: off_m + 4 * rows[i] + 4] for i in range(nh)])
+                    meta = np.stack([rec[i, off_m + mb * rows[i]: off_m + mb * rows[i] + mb] for i in range(nh)])
                     from oracle import quant
                     x32 = quant.rotate_to_fp32(src[64:he, h], rr[layer, h].astype(np.float64))
-                    st = parity.compare_groups(codes, meta, x32, tau[layer, h])
+                    st = parity.compare_groups(codes, meta, x32, tau[layer, h], self.group)
                     for key in stats:
                         stats[key] += st[key]
         bfp = self.cache.bf16_pool(layer).cpu()

@@ -161,10 +161,14 @@ def test_invalid_configs_rejected(b):
     good = b.make_config(1, 32, 8, 1, 4, 8)
     assert lib.oscar_cache_device_bytes(ctypes.byref(good)) > 0
     for field, value in [("head_dim", 64), ("sink_tokens", 32), ("recent_tokens", 128), ("page_tokens", 32),
-                         ("group_size", 64), ("num_q_heads", 24), ("num_int2_pages", 0), ("max_requests", 0)]:
+                         ("group_size", 32), ("group_size", 96), ("num_q_heads", 24), ("num_int2_pages", 0),
+                         ("max_requests", 0)]:
         cfg = b.make_config(1, 32, 8, 1, 4, 8)
         setattr(cfg, field, value)
         assert lib.oscar_cache_device_bytes(ctypes.byref(cfg)) == 0, field
+    # G_K = 64 is a valid geometry: 5120-byte INT2 records instead of 4608
+    g64 = b.make_config(1, 32, 8, 1, 4, 8, group_size=64)
+    assert lib.oscar_cache_device_bytes(ctypes.byref(g64)) > lib.oscar_cache_device_bytes(ctypes.byref(good))
 
 
 def test_bad_thresholds_rejected(b):
