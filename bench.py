@@ -32,6 +32,11 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 INT2_BYTES_PER_TOKEN_HEAD = 72          # 2 x (32 code bytes + 4 meta bytes)
+
+
+def int2_bytes_per_token_head(group: int = 128) -> int:
+    """K and V codes (2 x 32 bytes) plus one fp16 {s, z} per group of each."""
+    return 2 * (32 + 4 * (128 // group))
 BF16_BYTES_PER_TOKEN_HEAD = 512         # K and V rows of 128 bf16
 
 WORKLOADS = {
@@ -161,11 +166,11 @@ def pages_for(hist_end: int) -> int:
     return (hist_end - 64 + 63) // 64 if hist_end > 64 else 0
 
 
-def algorithmic_bytes(tokens: int, hist_end: int, kv_heads: int) -> int:
+def algorithmic_bytes(tokens: int, hist_end: int, kv_heads: int, group: int = 128) -> int:
     """Bytes one decode of one request must read: INT2 codes + fp16 meta + BF16 segments."""
     n_hist = max(0, hist_end - 64)
     n_bf16 = min(tokens, 64) + (tokens - hist_end if tokens > 64 else 0)
-    return kv_heads * (n_hist * INT2_BYTES_PER_TOKEN_HEAD + n_bf16 * BF16_BYTES_PER_TOKEN_HEAD)
+    return kv_heads * (n_hist * int2_bytes_per_token_head(group) + n_bf16 * BF16_BYTES_PER_TOKEN_HEAD)
 
 
 class Workload:
@@ -201,8 +206,9 @@ class Workload:
         max_pages = pages_for(self.T0 + steps_total + 64) + 1
         n_pages = sum(pages_for(t + steps_total + 64) + 1 for t in self.lens) + 8
         seed = synth.seed_for(cfg_id, 0, 0, 99) or 1
+        self.group = w.get("group", 128)
         cfg = binding.make_config(self.L, self.hq, self.hkv, self.batch + (1 if self.prefix else 0), max_pages,
-                                  n_pages, 0, 0.0, seed)
+                                  n_pages, 0, 0.0, seed, group_size=self.group)
         self.cache = binding.OscarCache(cfg, torch.from_numpy(self.rk).cuda(), torch.from_numpy(self.rv).cuda(),
                                         self.tk, self.tv)
         t = time.time()
@@ -300,9 +306,9 @@ class Workload:
         tot = 0
         for r in self.reqs:
             t, he = self.cache.length(r, layer)
-            tot += algorithmic_bytes(t, he, self.hkv)
+            tot += algorithmic_bytes(t, he, self.hkv, self.group)
         if unique and self.prefix:
-            tot -= (self.batch - 1) * (self.prefix - 64) * self.hkv * INT2_BYTES_PER_TOKEN_HEAD
+            tot -= (self.batch - 1) * (self.prefix - 64) * self.hkv * int2_bytes_per_token_head(self.group)
         return tot
 
 
@@ -312,7 +318,8 @@ def run_gpu(args, log):
     torch.cuda.set_device(local)
     W, K = args.warmup, args.steps
     ew, ek = 2, max(3, K // 2)
-    wl = Workload(args.config, W + 2 * K + ew + ek, log, args.layers)
+    wl = Workload(args.config, W + 2 * K + ew + ek, log, args.layers,
+                  override={"group": args.group} if args.group != 128 else None)
     wl.fused = not args.separate_calls
     wl.demote_first = args.demote_first
     stream = wl.stream_ptr()
@@ -646,7 +653,7 @@ def cpu_baseline(wl, res, log):
     cores = len(os.sched_getaffinity(0))
     t0 = time.time()
     ref = attention.decode(qf, k, v, he, wl.rk[layer].astype(np.float64), wl.rv[layer].astype(np.float64),
-                           wl.tk[layer], wl.tv[layer])
+                           wl.tk[layer], wl.tv[layer], group=wl.group)
     secs = time.time() - t0
     par = parity.check_output(out[0].cpu().numpy(), ref)
     return {
@@ -711,6 +718,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-bf16-baseline", action="store_true",
                     help="skip the uncompressed BF16 decode comparison")
+    ap.add_argument("--group", type=int, default=128, choices=[128, 64],
+                    help="quantisation group size (64: two {s, z} per token-head, 2.5 bits)")
     ap.add_argument("--demote-first", action="store_true",
                     help="each step starts with one oscar_demote_layers over all layers; the per-layer steps "
                          "then only append")
@@ -769,6 +778,7 @@ def main(argv=None):
                        min(wl.lens), max(wl.lens), int(np.mean(wl.lens))),
                    "shared_prefix_tokens": wl.prefix, "page_tokens": 64, "page_order": "seeded shuffle",
                    "storage": "INT2 codes + fp16 scale/zero history, BF16 sink/recent",
+                   "quant_group": wl.group,
                    "step": (("oscar_demote_layers over all layers, then " if args.demote_first else "") +
                             ("per layer: oscar_decode_step (append" +
                              (", then decode attention)" if args.demote_first else

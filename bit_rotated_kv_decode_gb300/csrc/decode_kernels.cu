@@ -56,9 +56,10 @@ constexpr int WARPS = 4;                 // warps per stream block
 constexpr int THREADS = 32 * WARPS;
 constexpr int MERGE_THREADS = 512;
 // TMA ring depth per warp and resident stream blocks per SM
-template <int G> struct Tune {
+template <int G, int GK = 128> struct Tune {
   static constexpr int STAGES = 2;
-  static constexpr int CTAS = G <= 4 ? 4 : 3;
+  // G_K = 64: larger records, a second meta table and weight rows of their own
+  static constexpr int CTAS = (G <= 4 && GK == 128) ? 4 : 3;
 };
 constexpr int BF16_ITEMS = DECODE_BF16_ITEMS;
 constexpr uint32_t WAIT_LIMIT = 1u << 16;        // mbarrier try_wait rounds, each up to SUSPEND_NS
@@ -152,25 +153,26 @@ __device__ __forceinline__ void split_half(float x, float& hi, float& lo) {
 }
 
 constexpr int WH_STRIDE = PAGE + 8;   // halves per weight row (bank spread)
-// Softmax weights of the page being processed, fp16 [G][hi, lo][WH_STRIDE] per warp.
-// Up to four heads they fit in the page's K-code region, dead once the logits are
-// formed; eight heads get rows of their own.
-template <int G>
-constexpr bool kWeightsInRing = G * 2 * WH_STRIDE * 2 <= PAGE * CODE_BYTES;
-template <int G, bool InRing = kWeightsInRing<G>>
+// Softmax weights of the page being processed, fp16 [G x groups][hi, lo][WH_STRIDE]
+// per warp (row (D / GK) h + g: head h, quantisation group g).  When they fit (up
+// to four heads with one group, two with two) they live in the page's K-code
+// region, dead once the logits are formed; otherwise in rows of their own.
+template <int G, int GK = 128>
+constexpr bool kWeightsInRing = G * (D / GK) * 2 * WH_STRIDE * 2 <= PAGE * CODE_BYTES;
+template <int G, int GK, bool InRing = kWeightsInRing<G, GK>>
 struct WeightRows {
-  __align__(16) uint16_t wh[WARPS][G][2][WH_STRIDE];
+  __align__(16) uint16_t wh[WARPS][G * (D / GK)][2][WH_STRIDE];
 };
-template <int G>
-struct WeightRows<G, true> {};
+template <int G, int GK>
+struct WeightRows<G, GK, true> {};
 
-template <int G>
+template <int G, int GK = 128>
 struct Smem {
   // INT2: per-warp TMA rings; BF16 items: the page's K rows (16-byte chunks
   // XOR-swizzled by row), V rows, q and the logits; after the page loop:
   // per-warp states.
   union {
-    __align__(128) uint8_t ring[WARPS][Tune<G>::STAGES][RECORD];
+    __align__(128) uint8_t ring[WARPS][Tune<G, GK>::STAGES][record_for(GK)];
     struct {
       __align__(16) uint16_t k[PAGE][D];
       __align__(16) uint16_t v[PAGE][D];
@@ -179,9 +181,10 @@ struct Smem {
     } bf;
     float state[WARPS][G][PART];
   } buf;
-  __align__(8) uint64_t bar[WARPS][Tune<G>::STAGES];
+  __align__(8) uint64_t bar[WARPS][Tune<G, GK>::STAGES];
   __align__(16) float4 meta[WARPS][PAGE];   // INT2: per token {s_k, z_k, s_v 2^ew, z_v} of the page
-  WeightRows<G> w;
+  __align__(16) float4 meta2[WARPS][GK == 64 ? PAGE : 1];   // G_K = 64: the same for group 1
+  WeightRows<G, GK> w;
 };
 
 // ---- 1. q_rot = q R_K, delivered as tensor-core operands --------------------------
@@ -197,7 +200,10 @@ struct Smem {
 //   kscale[h] s_k acc + (scale log2(e) sum_slab qsum[slab][h]) z_k.
 // Register r of k-step s for lane (gid, tid) pairs channel 32 tid + 16 (s >> 2) + m
 // (low half) with that channel + 8 (high half), m = 2 (s & 3) + r, as the code
-// registers of the A operand do; so lanes with tid = t only need slab t.
+// registers of the A operand do; so lanes with tid = t only need slab t.  With
+// G_K = 64 the k-steps are group-pure instead: channel 64 (s >> 2) + 16 tid + m
+// (and + 8), so k-steps 0..3 hold group 0 and 4..7 group 1; slab sl then feeds
+// lanes with tid = 2 (sl & 1), 2 (sl & 1) + 1 at k-steps 4 (sl >> 1) ...
 // qscale(h) = 2^e with |q_rot| 2^(e + 24) <= 2^15 taken from |q|_2 >= max |q_rot|
 // (R_K is orthogonal), so each slab block finds it alone.
 template <int G>
@@ -246,7 +252,7 @@ __device__ __forceinline__ void rotate_load_r(const DevCache& c, int layer, int 
   for (int i = 0; i < RotRows<NTH>::ROWS; ++i) rr.r[i] = __ldg(RK + (size_t)(RotRows<NTH>::ROWS * grp + i) * D);
 }
 
-template <int G, int NTH>
+template <int G, int NTH, int GK = 128>
 __device__ __forceinline__ void rotate_block(const DevCache& c, unsigned long long epoch, int batch_row,
                                              int head, int slab, const uint16_t* __restrict__ q,
                                              uint32_t* __restrict__ dst, const RotRows<NTH>& rows,
@@ -309,29 +315,46 @@ __device__ __forceinline__ void rotate_block(const DevCache& c, unsigned long lo
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     if (lane == 0) consts[8 + 8 * slab + h] = sum;
   }
-  // fragment words of the lanes with tid == slab: lane 4 gid + slab, register k
+  // fragment words fed by this slab: 8 QFrag<G>::REGS of them
   for (int wi = t; wi < 8 * QFrag<G>::REGS; wi += NTH) {
-    const int gid = wi / QFrag<G>::REGS, k = wi % QFrag<G>::REGS;
+    int lane_w, k, cl;   // destination lane and register, channel within the slab
+    if constexpr (GK == 128) {
+      // the lanes with tid == slab: lane 4 gid + slab, every register
+      const int gid = wi / QFrag<G>::REGS;
+      k = wi % QFrag<G>::REGS;
+      lane_w = 4 * gid + slab;
+      const int s = (k >> 1) & 7;
+      cl = 16 * (s >> 2) + 2 * (s & 3) + (k & 1);
+    } else {
+      // lanes with tid = 2 (slab & 1) + (j & 1), registers of k-steps 4 (slab >> 1) ..
+      constexpr int HALF = QFrag<G>::REGS / 2;
+      const int j = wi / HALF, kk = wi % HALF;
+      const int tid = 2 * (slab & 1) + (j & 1);
+      lane_w = 4 * (j >> 1) + tid;
+      const int nt = kk >> 3, sl = (kk >> 1) & 3, rr = kk & 1;
+      k = 16 * nt + 2 * (4 * (slab >> 1) + sl) + rr;
+      cl = 16 * (tid & 1) + 2 * sl + rr;
+    }
+    const int gid = lane_w >> 2;
     const int nt = k >> 4, s = (k >> 1) & 7, rr = k & 1;
     const int h = 4 * nt + (gid >> 1);
     uint32_t word = 0u;
     if (h < G) {
       const int m = 2 * (s & 3) + rr;
-      const int cl = 16 * (s >> 2) + m;     // channel within the slab
       const float f = ldexpf(sm.qscale[h], 24 - 2 * code_exp(m));
       float ha, la, hb, lb;
       split_half(sm.red[0][h][cl] * f, ha, la);
       split_half(sm.red[0][h][cl + 8] * f, hb, lb);
       word = (gid & 1) ? pack_half2(la, lb) : pack_half2(ha, hb);
     }
-    dst[(size_t)(4 * gid + slab) * QFrag<G>::REGS + k] = word;
+    dst[(size_t)lane_w * QFrag<G>::REGS + k] = word;
   }
   // the block barrier orders every thread's words before thread 0's release store
   __syncthreads();
   if (t == 0) st_release(reinterpret_cast<unsigned long long*>(dst + QFrag<G>::READY) + slab, epoch);
 }
 
-template <int G>
+template <int G, int GK>
 __global__ void __launch_bounds__(ROT_THREADS) rotate_q_kernel(DevCache c, int layer, DecodeArgs a,
                                                                const uint16_t* __restrict__ q,
                                                                uint32_t* __restrict__ qfrag) {
@@ -343,7 +366,7 @@ __global__ void __launch_bounds__(ROT_THREADS) rotate_q_kernel(DevCache c, int l
   // grid of this decode may start
   grid_dep_wait();
   grid_dep_launch();
-  rotate_block<G, ROT_THREADS>(c, a.epoch, a.r[ri].batch_row, head, slab, q,
+  rotate_block<G, ROT_THREADS, GK>(c, a.epoch, a.r[ri].batch_row, head, slab, q,
                                qfrag + (size_t)blockIdx.x * QFrag<G>::WORDS, rows, sm);
 }
 
@@ -358,12 +381,15 @@ __device__ __forceinline__ float ex2(float x) {
 // (request, kv head)'s q operands.  Warp w of the block takes pages w, w + 4, ...
 // of the chunk.  Leaves the block's partial (rotated basis) for every query head
 // of the group in part_out.
-template <int G>
+template <int G, int GK>
 __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const DecodeReq& R, int head, int chunk,
                                            int ppc, const uint32_t* __restrict__ qf, unsigned long long epoch,
-                                           Smem<G>& sm, float* part_out) {
+                                           Smem<G, GK>& sm, float* part_out) {
   constexpr int NT = QFrag<G>::NT;       // n-tiles of 8 columns = 4 heads x (hi, lo)
-  constexpr int STAGES = Tune<G>::STAGES;
+  constexpr int STAGES = Tune<G, GK>::STAGES;
+  constexpr int REC = record_for(GK);
+  constexpr int NGR = D / GK;            // quantisation groups per token-head
+  constexpr int KMETA = k_meta_off_for(GK), VMETA = v_meta_off_for(GK), MB = meta_bytes_for(GK);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tid = lane & 3;
   const int nhist = R.hist_end - SINK;
@@ -372,8 +398,8 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
   const int pc1 = min(npages, pc0 + ppc);
   const int my_n = (pc1 - pc0 > warp) ? (pc1 - pc0 - warp + WARPS - 1) / WARPS : 0;
   const int32_t* pt = c.hist_pt + (size_t)R.slot * c.max_pages;
-  const uint8_t* base = c.int2 + layer * c.int2_layer_stride + (size_t)head * RECORD;
-  const size_t pstride = (size_t)c.Hkv * RECORD;
+  const uint8_t* base = c.int2 + layer * c.int2_layer_stride + (size_t)head * REC;
+  const size_t pstride = (size_t)c.Hkv * REC;
   bool timed_out = false;
   int issued = 0;   // copies issued by this warp (lane 0's count)
 
@@ -420,8 +446,8 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
   for (int j = 0; j < STAGES; ++j) {
     const uint8_t* src = page_src(j);
     if (lane == 0 && j < my_n) {
-      mbar_expect_tx(&sm.bar[warp][j], RECORD);
-      tma_load_1d(sm.buf.ring[warp][j], src, RECORD, &sm.bar[warp][j]);
+      mbar_expect_tx(&sm.bar[warp][j], REC);
+      tma_load_1d(sm.buf.ring[warp][j], src, REC, &sm.bar[warp][j]);
       ++issued;
     }
   }
@@ -472,16 +498,21 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
       }
     }
   }
-  float ks[NT], kz[NT];
+  // kz[nt][g]: scale log2(e) times the sum of q_rot over group g's channels (its slabs)
+  float ks[NT], kz[NT][NGR];
   {
     const float* consts = reinterpret_cast<const float*>(qf + QFrag<G>::CONSTS);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       ks[nt] = __ldcg(consts + 4 * nt + tid);
-      float sum = 0.0f;
 #pragma unroll
-      for (int sl = 0; sl < SLABS; ++sl) sum += __ldcg(consts + 8 + 8 * sl + 4 * nt + tid);
-      kz[nt] = c.scale * LOG2E * sum;
+      for (int g = 0; g < NGR; ++g) {
+        float sum = 0.0f;
+#pragma unroll
+        for (int sl = g * (SLABS / NGR); sl < (g + 1) * (SLABS / NGR); ++sl)
+          sum += __ldcg(consts + 8 + 8 * sl + 4 * nt + tid);
+        kz[nt][g] = c.scale * LOG2E * sum;
+      }
     }
   }
 
@@ -489,12 +520,13 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
   // l and u are kept as two partial sums (tokens gid and gid + 8 of each m-tile)
   // so that the page's pairs update them with packed fp32 instructions
   float m_run[NT];
-  float2 l_run[NT], u_run[NT];
+  float2 l_run[NT], u_run[NT][NGR];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     m_run[nt] = -INFINITY;
     l_run[nt] = make_float2(0.0f, 0.0f);
-    u_run[nt] = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int g = 0; g < NGR; ++g) u_run[nt][g] = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
@@ -512,18 +544,33 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
     const uint8_t* rec = sm.buf.ring[warp][stg];
     const int valid = min(PAGE, nhist - pi * PAGE);
 
-    // ---- logits: 4 m-tiles of 16 tokens x NT n-tiles, K = 128 channels
-    float acc[NT][4][4];
+    // ---- logits: 4 m-tiles of 16 tokens x NT n-tiles, K = 128 channels; with
+    // G_K = 64 the k-steps of each group accumulate apart (acc[g])
+    float acc[NGR][NT][4][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+    for (int g = 0; g < NGR; ++g)
 #pragma unroll
-      for (int mt = 0; mt < 4; ++mt)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[nt][mt][e] = 0.0f;
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[g][nt][mt][e] = 0.0f;
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt) {
-      const uint2 ka = *reinterpret_cast<const uint2*>(rec + K_CODES_OFF + (16 * mt + gid) * CODE_BYTES + 8 * tid);
-      const uint2 kb = *reinterpret_cast<const uint2*>(rec + K_CODES_OFF + (16 * mt + gid + 8) * CODE_BYTES + 8 * tid);
+      uint2 ka, kb;
+      if constexpr (GK == 128) {
+        // channels 32 tid .. 32 tid + 31 of tokens 16 mt + gid and + 8
+        ka = *reinterpret_cast<const uint2*>(rec + K_CODES_OFF + (16 * mt + gid) * CODE_BYTES + 8 * tid);
+        kb = *reinterpret_cast<const uint2*>(rec + K_CODES_OFF + (16 * mt + gid + 8) * CODE_BYTES + 8 * tid);
+      } else {
+        // channels 16 tid .. 16 tid + 15 of group 0 (.x) and of group 1 (.y)
+        const uint8_t* ra = rec + K_CODES_OFF + (16 * mt + gid) * CODE_BYTES;
+        const uint8_t* rb = ra + 8 * CODE_BYTES;
+        ka = make_uint2(*reinterpret_cast<const uint32_t*>(ra + 4 * tid),
+                        *reinterpret_cast<const uint32_t*>(ra + 16 + 4 * tid));
+        kb = make_uint2(*reinterpret_cast<const uint32_t*>(rb + 4 * tid),
+                        *reinterpret_cast<const uint32_t*>(rb + 16 + 4 * tid));
+      }
       const uint2 kas = make_uint2(ka.x >> 10, ka.y >> 10);
       const uint2 kbs = make_uint2(kb.x >> 10, kb.y >> 10);
 #pragma unroll
@@ -534,7 +581,8 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
         const uint32_t a0 = code_pair2(wa, was, m0), a1 = code_pair2(wb, wbs, m0);
         const uint32_t a2 = code_pair2(wa, was, m0 + 1), a3 = code_pair2(wb, wbs, m0 + 1);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt][mt], a0, a1, a2, a3, bq[nt][s][0], bq[nt][s][1]);
+        for (int nt = 0; nt < NT; ++nt)
+          mma16816(acc[NGR == 2 ? (s >> 2) : 0][nt][mt], a0, a1, a2, a3, bq[nt][s][0], bq[nt][s][1]);
       }
     }
     // token meta of this lane's 8 tokens: 16 mt + gid + 8 rr; a partial page (the
@@ -544,31 +592,53 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int tok = lane + 32 * hh;
-      const __half2 km = *reinterpret_cast<const __half2*>(rec + K_META_OFF + tok * META_BYTES);
-      const __half2 vm = *reinterpret_cast<const __half2*>(rec + V_META_OFF + tok * META_BYTES);
       const bool ok = tok < valid;
-      sm.meta[warp][tok] = make_float4(__low2float(km), __high2float(km), ok ? __low2float(vm) * wscale : 0.0f,
-                                       ok ? __high2float(vm) : 0.0f);
+#pragma unroll
+      for (int g = 0; g < NGR; ++g) {
+        const __half2 km = *reinterpret_cast<const __half2*>(rec + KMETA + tok * MB + 4 * g);
+        const __half2 vm = *reinterpret_cast<const __half2*>(rec + VMETA + tok * MB + 4 * g);
+        const float4 mv = make_float4(__low2float(km), __high2float(km), ok ? __low2float(vm) * wscale : 0.0f,
+                                      ok ? __high2float(vm) : 0.0f);
+        if (g == 0)
+          sm.meta[warp][tok] = mv;
+        else
+          sm.meta2[warp][tok] = mv;
+      }
     }
     __syncwarp();
     // logits in the log2 domain, as pairs (token 16 mt + gid, that token + 8)
-    float2 lg[NT][4], sw[4], zv[4];
+    float2 lg[NT][4], sw[NGR][4], zv[NGR][4];
     auto epilogue = [&](auto full_page) {
       constexpr bool FULL = decltype(full_page)::value;
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt) {
         const int tok = 16 * mt + gid;
         const float4 m0 = sm.meta[warp][tok], m1 = sm.meta[warp][tok + 8];
-        sw[mt] = make_float2(m0.z, m1.z);
-        zv[mt] = make_float2(m0.w, m1.w);
+        sw[0][mt] = make_float2(m0.z, m1.z);
+        zv[0][mt] = make_float2(m0.w, m1.w);
+        float4 n0 = m0, n1 = m1;
+        if constexpr (NGR == 2) {
+          n0 = sm.meta2[warp][tok];
+          n1 = sm.meta2[warp][tok + 8];
+          sw[NGR - 1][mt] = make_float2(n0.z, n1.z);
+          zv[NGR - 1][mt] = make_float2(n0.w, n1.w);
+        }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          // hi + lo columns, then s_k kscale acc + z_k (scale log2 e sum q_rot)
-          const float2 a = __fadd2_rn(make_float2(acc[nt][mt][0], acc[nt][mt][2]),
-                                      make_float2(acc[nt][mt][1], acc[nt][mt][3]));
+          // hi + lo columns, then s_k kscale acc + z_k (scale log2 e sum q_rot), per group
+          const float2 a = __fadd2_rn(make_float2(acc[0][nt][mt][0], acc[0][nt][mt][2]),
+                                      make_float2(acc[0][nt][mt][1], acc[0][nt][mt][3]));
           const float2 sk = __fmul2_rn(make_float2(m0.x, m1.x), make_float2(ks[nt], ks[nt]));
-          const float2 zk = __fmul2_rn(make_float2(m0.y, m1.y), make_float2(kz[nt], kz[nt]));
+          const float2 zk = __fmul2_rn(make_float2(m0.y, m1.y), make_float2(kz[nt][0], kz[nt][0]));
           float2 v = __ffma2_rn(sk, a, zk);
+          if constexpr (NGR == 2) {
+            const float2 a1 = __fadd2_rn(make_float2(acc[NGR - 1][nt][mt][0], acc[NGR - 1][nt][mt][2]),
+                                         make_float2(acc[NGR - 1][nt][mt][1], acc[NGR - 1][nt][mt][3]));
+            const float2 sk1 = __fmul2_rn(make_float2(n0.x, n1.x), make_float2(ks[nt], ks[nt]));
+            const float2 zk1 = __fmul2_rn(make_float2(n0.y, n1.y),
+                                          make_float2(kz[nt][NGR - 1], kz[nt][NGR - 1]));
+            v = __ffma2_rn(sk1, a1, __fadd2_rn(v, zk1));
+          }
           const bool head_ok = 4 * nt + 4 <= G || 4 * nt + tid < G;
           if (!FULL || !head_ok) {
             v.x = (head_ok && tok < valid) ? v.x : -INFINITY;
@@ -588,7 +658,7 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
     // (r < 8) or 16 g + 2 (r - 8) + 1, so a lane's pair is one 32-bit store; the
     // value contraction below takes its k index in the same order.
     uint16_t(*wh)[2][WH_STRIDE];
-    if constexpr (kWeightsInRing<G>) {
+    if constexpr (kWeightsInRing<G, GK>) {
       wh = reinterpret_cast<uint16_t(*)[2][WH_STRIDE]>(sm.buf.ring[warp][stg] + K_CODES_OFF);
       __syncwarp();   // every lane is done reading this page's K codes
     } else {
@@ -609,7 +679,8 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
         const float corr = ex2(m_run[nt] - pm);
         m_run[nt] = pm;
         l_run[nt] = __fmul2_rn(l_run[nt], make_float2(corr, corr));
-        u_run[nt] = __fmul2_rn(u_run[nt], make_float2(corr, corr));
+#pragma unroll
+        for (int g = 0; g < NGR; ++g) u_run[nt][g] = __fmul2_rn(u_run[nt][g], make_float2(corr, corr));
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
@@ -622,14 +693,18 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
         const float2 d = __fadd2_rn(lg[nt][mt], neg_ref);
         const float2 p = make_float2(ex2(d.x), ex2(d.y));
         l_run[nt] = __fadd2_rn(l_run[nt], p);
-        u_run[nt] = __ffma2_rn(p, zv[mt], u_run[nt]);
+#pragma unroll
+        for (int g = 0; g < NGR; ++g) u_run[nt][g] = __ffma2_rn(p, zv[g][mt], u_run[nt][g]);
         if (h < G) {
-          const float2 w = __fmul2_rn(p, sw[mt]);
-          const __half2 hi = __float22half2_rn(w);
-          const float2 lo = __ffma2_rn(__half22float2(hi), make_float2(-1.0f, -1.0f), w);
           const int pos = 16 * mt + 2 * gid;
-          *reinterpret_cast<__half2*>(&wh[h][0][pos]) = hi;
-          *reinterpret_cast<__half2*>(&wh[h][1][pos]) = __float22half2_rn(lo);
+#pragma unroll
+          for (int g = 0; g < NGR; ++g) {
+            const float2 w = __fmul2_rn(p, sw[g][mt]);
+            const __half2 hi = __float22half2_rn(w);
+            const float2 lo = __ffma2_rn(__half22float2(hi), make_float2(-1.0f, -1.0f), w);
+            *reinterpret_cast<__half2*>(&wh[NGR * h + g][0][pos]) = hi;
+            *reinterpret_cast<__half2*>(&wh[NGR * h + g][1][pos]) = __float22half2_rn(lo);
+          }
         }
       }
     }
@@ -639,32 +714,57 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
       const int ta = 16 * s + 2 * tid;
-      uint32_t bw[NT][2];
+      uint32_t bw[NGR][NT][2];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int h = 4 * nt + (gid >> 1);
-        if (h < G) {
-          const uint16_t* row = wh[h][gid & 1];
-          bw[nt][0] = *reinterpret_cast<const uint32_t*>(row + ta);
-          bw[nt][1] = *reinterpret_cast<const uint32_t*>(row + ta + 8);
-        } else {
-          bw[nt][0] = bw[nt][1] = 0u;
+      for (int g = 0; g < NGR; ++g)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int h = 4 * nt + (gid >> 1);
+          if (h < G) {
+            const uint16_t* row = wh[NGR * h + g][gid & 1];
+            bw[g][nt][0] = *reinterpret_cast<const uint32_t*>(row + ta);
+            bw[g][nt][1] = *reinterpret_cast<const uint32_t*>(row + ta + 8);
+          } else {
+            bw[g][nt][0] = bw[g][nt][1] = 0u;
+          }
         }
-      }
       const int tb = 16 * s + tid;
-      const uint32_t* vrow = reinterpret_cast<const uint32_t*>(rec + V_CODES_OFF) + gid;
-      const uint32_t wa = vrow[tb * (CODE_BYTES / 4)], wb = vrow[(tb + 8) * (CODE_BYTES / 4)];
-      const uint32_t wc = vrow[(tb + 4) * (CODE_BYTES / 4)], wd = vrow[(tb + 12) * (CODE_BYTES / 4)];
-      const uint32_t x1 = __byte_perm(wa, wb, 0x5410), y1 = __byte_perm(wa, wb, 0x7632);
-      const uint32_t x2 = __byte_perm(wc, wd, 0x5410), y2 = __byte_perm(wc, wd, 0x7632);
-      const uint32_t x1s = x1 >> 10, y1s = y1 >> 10;
-      const uint32_t x2s = x2 >> 10, y2s = y2 >> 10;
+      if constexpr (GK == 128) {
+        // row gid of m-tile mt: channel 16 gid + mt; row gid + 8: 16 gid + 8 + mt
+        const uint32_t* vrow = reinterpret_cast<const uint32_t*>(rec + V_CODES_OFF) + gid;
+        const uint32_t wa = vrow[tb * (CODE_BYTES / 4)], wb = vrow[(tb + 8) * (CODE_BYTES / 4)];
+        const uint32_t wc = vrow[(tb + 4) * (CODE_BYTES / 4)], wd = vrow[(tb + 12) * (CODE_BYTES / 4)];
+        const uint32_t x1 = __byte_perm(wa, wb, 0x5410), y1 = __byte_perm(wa, wb, 0x7632);
+        const uint32_t x2 = __byte_perm(wc, wd, 0x5410), y2 = __byte_perm(wc, wd, 0x7632);
+        const uint32_t x1s = x1 >> 10, y1s = y1 >> 10;
+        const uint32_t x2s = x2 >> 10, y2s = y2 >> 10;
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const uint32_t a0 = code_pair2(x1, x1s, mt), a1 = code_pair2(y1, y1s, mt);
-        const uint32_t a2 = code_pair2(x2, x2s, mt), a3 = code_pair2(y2, y2s, mt);
+        for (int mt = 0; mt < 8; ++mt) {
+          const uint32_t a0 = code_pair2(x1, x1s, mt), a1 = code_pair2(y1, y1s, mt);
+          const uint32_t a2 = code_pair2(x2, x2s, mt), a3 = code_pair2(y2, y2s, mt);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma16816(o[nt][mt], a0, a1, a2, a3, bw[nt][0], bw[nt][1]);
+          for (int nt = 0; nt < NT; ++nt) mma16816(o[nt][mt], a0, a1, a2, a3, bw[0][nt][0], bw[0][nt][1]);
+        }
+      } else {
+        // group-pure m-tiles: m-tile 4 g + j, row gid holds channel 64 g + 8 gid + j and
+        // row gid + 8 channel 64 g + 8 gid + 4 + j (16-bit half gid & 1 of word 4 g + gid / 2)
+        const uint32_t sel = (gid & 1) ? 0x7632u : 0x5410u;
+#pragma unroll
+        for (int g = 0; g < NGR; ++g) {
+          const uint32_t* vrow = reinterpret_cast<const uint32_t*>(rec + V_CODES_OFF) + 4 * g + (gid >> 1);
+          const uint32_t wa = vrow[tb * (CODE_BYTES / 4)], wb = vrow[(tb + 8) * (CODE_BYTES / 4)];
+          const uint32_t wc = vrow[(tb + 4) * (CODE_BYTES / 4)], wd = vrow[(tb + 12) * (CODE_BYTES / 4)];
+          const uint32_t x1 = __byte_perm(wa, wb, sel), x2 = __byte_perm(wc, wd, sel);
+          const uint32_t x1s = x1 >> 10, x2s = x2 >> 10;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t a0 = code_pair2(x1, x1s, j), a1 = code_pair2(x1, x1s, j + 4);
+            const uint32_t a2 = code_pair2(x2, x2s, j), a3 = code_pair2(x2, x2s, j + 4);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma16816(o[nt][4 * g + j], a0, a1, a2, a3, bw[g][nt][0], bw[g][nt][1]);
+          }
+        }
       }
     }
     __syncwarp();
@@ -672,9 +772,9 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
       const uint8_t* src = page_src(j + STAGES);
       if (lane == 0 && j + STAGES < my_n) {
         // the weights were written to this buffer through the generic proxy
-        if constexpr (kWeightsInRing<G>) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_expect_tx(&sm.bar[warp][stg], RECORD);
-        tma_load_1d(sm.buf.ring[warp][stg], src, RECORD, &sm.bar[warp][stg]);
+        if constexpr (kWeightsInRing<G, GK>) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_expect_tx(&sm.bar[warp][stg], REC);
+        tma_load_1d(sm.buf.ring[warp][stg], src, REC, &sm.bar[warp][stg]);
         ++issued;
       }
     }
@@ -692,20 +792,31 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
   // ---- this warp's state -> shared memory (rotated basis, unscaled, z term added)
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    float l = l_run[nt].x + l_run[nt].y, u = u_run[nt].x + u_run[nt].y;
+    float l = l_run[nt].x + l_run[nt].y, u[NGR];
+#pragma unroll
+    for (int g = 0; g < NGR; ++g) u[g] = u_run[nt][g].x + u_run[nt][g].y;
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       l += __shfl_xor_sync(0xffffffffu, l, off);
-      u += __shfl_xor_sync(0xffffffffu, u, off);
+#pragma unroll
+      for (int g = 0; g < NGR; ++g) u[g] += __shfl_xor_sync(0xffffffffu, u[g], off);
     }
     const int h = 4 * nt + tid;
     if (h < G) {
       float* st = sm.buf.state[warp][h];
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
-        const float f = ldexpf(1.0f, 24 - 2 * code_exp(mt) - ew);
-        st[16 * gid + mt] = fmaf(o[nt][mt][0] + o[nt][mt][1], f, u);
-        st[16 * gid + 8 + mt] = fmaf(o[nt][mt][2] + o[nt][mt][3], f, u);
+        if constexpr (GK == 128) {
+          const float f = ldexpf(1.0f, 24 - 2 * code_exp(mt) - ew);
+          st[16 * gid + mt] = fmaf(o[nt][mt][0] + o[nt][mt][1], f, u[0]);
+          st[16 * gid + 8 + mt] = fmaf(o[nt][mt][2] + o[nt][mt][3], f, u[0]);
+        } else {
+          const int g = mt >> 2, j = mt & 3;
+          const float f0 = ldexpf(1.0f, 24 - 2 * code_exp(j) - ew);
+          const float f1 = ldexpf(1.0f, 24 - 2 * code_exp(j + 4) - ew);
+          st[64 * g + 8 * gid + j] = fmaf(o[nt][mt][0] + o[nt][mt][1], f0, u[g]);
+          st[64 * g + 8 * gid + 4 + j] = fmaf(o[nt][mt][2] + o[nt][mt][3], f1, u[g]);
+        }
       }
       if (gid == 0) {
         st[PARTIAL_M] = m_run[nt];
@@ -740,9 +851,9 @@ __device__ __forceinline__ void int2_chunk(const DevCache& c, int layer, const D
 
 // One BF16 page (the sink page, or one of the four recent-ring pages) of one
 // (request, kv head), with the unrotated q; partial for every query head.
-template <int G>
+template <int G, typename SM>
 __device__ __forceinline__ void bf16_item(const DevCache& c, int layer, const DecodeReq& R, int head, int which,
-                                          Smem<G>& sm, float* part_out) {
+                                          SM& sm, float* part_out) {
   const int t = threadIdx.x;
   const int warp = t >> 5, lane = t & 31;
   const float scale2 = c.scale * LOG2E;
@@ -850,13 +961,13 @@ __device__ __forceinline__ void bf16_item(const DevCache& c, int layer, const De
 // BF16 pages ((request, kv head) major, item minor).  Partial slot of item k of
 // (request i, kv head h): part_start(i) + h * (5 + chunks(i)) + k, k < 5 the BF16
 // items, k >= 5 the chunks.
-template <int G>
-__global__ void __launch_bounds__(THREADS, Tune<G>::CTAS) decode_stream_kernel(DevCache c, int layer, DecodeArgs a,
+template <int G, int GK>
+__global__ void __launch_bounds__(THREADS, Tune<G, GK>::CTAS) decode_stream_kernel(DevCache c, int layer, DecodeArgs a,
                                                                          const uint16_t* __restrict__ q,
                                                                          const uint32_t* __restrict__ qfrag,
                                                                          float* __restrict__ partials) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  Smem<G>& sm = *reinterpret_cast<Smem<G>*>(smem_raw);
+  Smem<G, GK>& sm = *reinterpret_cast<Smem<G, GK>*>(smem_raw);
   const int item = blockIdx.x;
   int ri = 0, head, sub;
   if (item < a.int2_items) {
@@ -888,7 +999,7 @@ __global__ void __launch_bounds__(THREADS, Tune<G>::CTAS) decode_stream_kernel(D
     __syncthreads();
     bf16_item<G>(c, layer, R, head, sub, sm, part);
   } else {
-    int2_chunk<G>(c, layer, R, head, sub - BF16_ITEMS, a.pages_per_chunk,
+    int2_chunk<G, GK>(c, layer, R, head, sub - BF16_ITEMS, a.pages_per_chunk,
                   qfrag + ((size_t)ri * c.Hkv + head) * QFrag<G>::WORDS, a.epoch, sm, part);
   }
   // this grid completes only after rotate_q has (later launches rely on stream order)
@@ -1036,7 +1147,7 @@ struct FrontArgs {
 };
 constexpr int FRONT_THREADS = APPEND_THREADS;
 
-template <int G>
+template <int G, int GK>
 __global__ void __launch_bounds__(FRONT_THREADS) step_front_kernel(DevCache c, int layer, FrontArgs f,
                                                                    const uint16_t* __restrict__ k,
                                                                    const uint16_t* __restrict__ v,
@@ -1058,7 +1169,7 @@ __global__ void __launch_bounds__(FRONT_THREADS) step_front_kernel(DevCache c, i
   rotate_load_r(c, layer, head, slab, rows);
   grid_dep_wait();
   grid_dep_launch();
-  rotate_block<G, FRONT_THREADS>(c, f.epoch, f.batch_row[ri], head, slab, q,
+  rotate_block<G, FRONT_THREADS, GK>(c, f.epoch, f.batch_row[ri], head, slab, q,
                                  qfrag + ((size_t)ri * c.Hkv + head) * QFrag<G>::WORDS, rows, sm.rot);
 }
 
@@ -1089,12 +1200,12 @@ struct PdlLaunch {
 };
 
 // The stream and merge kernels (after rotate_q or the fused front).
-template <int G>
+template <int G, int GK>
 cudaError_t launch_stream_merge(const DevCache& c, int layer, const DecodeArgs& a, int items, const uint16_t* q,
                                 float* out, uint32_t* qfrag, float* partials, cudaStream_t s) {
   static unsigned stream_set = 0, merge_set = 0;
-  const size_t smem = sizeof(Smem<G>);
-  cudaError_t e = set_smem(decode_stream_kernel<G>, smem, stream_set);
+  const size_t smem = sizeof(Smem<G, GK>);
+  cudaError_t e = set_smem(decode_stream_kernel<G, GK>, smem, stream_set);
   if (e == cudaSuccess) e = set_smem(decode_merge_kernel<G>, sizeof(MergeSmem), merge_set);
   if (e != cudaSuccess) return e;
   PdlLaunch L(s);
@@ -1102,7 +1213,7 @@ cudaError_t launch_stream_merge(const DevCache& c, int layer, const DecodeArgs& 
   cfg.gridDim = dim3(static_cast<unsigned>(items));
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = smem;
-  e = cudaLaunchKernelEx(&cfg, decode_stream_kernel<G>, c, layer, a, q, static_cast<const uint32_t*>(qfrag),
+  e = cudaLaunchKernelEx(&cfg, decode_stream_kernel<G, GK>, c, layer, a, q, static_cast<const uint32_t*>(qfrag),
                          partials);
   if (e != cudaSuccess) return e;
 
@@ -1112,27 +1223,40 @@ cudaError_t launch_stream_merge(const DevCache& c, int layer, const DecodeArgs& 
   return cudaLaunchKernelEx(&cfg, decode_merge_kernel<G>, c, layer, a, static_cast<const float*>(partials), out);
 }
 
-template <int G>
-cudaError_t launch_g(const DevCache& c, int layer, const DecodeArgs& a, int items, const uint16_t* q, float* out,
-                     uint32_t* qfrag, float* partials, cudaStream_t s) {
+template <int G, int GK>
+cudaError_t launch_g2(const DevCache& c, int layer, const DecodeArgs& a, int items, const uint16_t* q, float* out,
+                      uint32_t* qfrag, float* partials, cudaStream_t s) {
   PdlLaunch L(s);
   L.cfg.gridDim = dim3(static_cast<unsigned>(a.n * c.Hkv), SLABS);
   L.cfg.blockDim = dim3(ROT_THREADS);
-  const cudaError_t e = cudaLaunchKernelEx(&L.cfg, rotate_q_kernel<G>, c, layer, a, q, qfrag);
+  const cudaError_t e = cudaLaunchKernelEx(&L.cfg, rotate_q_kernel<G, GK>, c, layer, a, q, qfrag);
   if (e != cudaSuccess) return e;
-  return launch_stream_merge<G>(c, layer, a, items, q, out, qfrag, partials, s);
+  return launch_stream_merge<G, GK>(c, layer, a, items, q, out, qfrag, partials, s);
+}
+template <int G>
+cudaError_t launch_g(const DevCache& c, int layer, const DecodeArgs& a, int items, const uint16_t* q, float* out,
+                     uint32_t* qfrag, float* partials, cudaStream_t s) {
+  return c.gk == 64 ? launch_g2<G, 64>(c, layer, a, items, q, out, qfrag, partials, s)
+                    : launch_g2<G, 128>(c, layer, a, items, q, out, qfrag, partials, s);
 }
 
+template <int G, int GK>
+cudaError_t launch_step_g2(const DevCache& c, int layer, const FrontArgs& f, const uint16_t* k, const uint16_t* v,
+                           const DecodeArgs& a, int items, const uint16_t* q, float* out, uint32_t* qfrag,
+                           float* partials, cudaStream_t s) {
+  PdlLaunch L(s);
+  L.cfg.gridDim = dim3(static_cast<unsigned>(f.n_app * c.Hkv * 2 + a.n * c.Hkv * SLABS));
+  L.cfg.blockDim = dim3(FRONT_THREADS);
+  const cudaError_t e = cudaLaunchKernelEx(&L.cfg, step_front_kernel<G, GK>, c, layer, f, k, v, q, qfrag);
+  if (e != cudaSuccess) return e;
+  return launch_stream_merge<G, GK>(c, layer, a, items, q, out, qfrag, partials, s);
+}
 template <int G>
 cudaError_t launch_step_g(const DevCache& c, int layer, const FrontArgs& f, const uint16_t* k, const uint16_t* v,
                           const DecodeArgs& a, int items, const uint16_t* q, float* out, uint32_t* qfrag,
                           float* partials, cudaStream_t s) {
-  PdlLaunch L(s);
-  L.cfg.gridDim = dim3(static_cast<unsigned>(f.n_app * c.Hkv * 2 + a.n * c.Hkv * SLABS));
-  L.cfg.blockDim = dim3(FRONT_THREADS);
-  const cudaError_t e = cudaLaunchKernelEx(&L.cfg, step_front_kernel<G>, c, layer, f, k, v, q, qfrag);
-  if (e != cudaSuccess) return e;
-  return launch_stream_merge<G>(c, layer, a, items, q, out, qfrag, partials, s);
+  return c.gk == 64 ? launch_step_g2<G, 64>(c, layer, f, k, v, a, items, q, out, qfrag, partials, s)
+                    : launch_step_g2<G, 128>(c, layer, f, k, v, a, items, q, out, qfrag, partials, s);
 }
 
 DecodeArgs make_args(const DecodeReq* reqs, const DecodePlan& plan, uint64_t epoch, int front_writes) {
@@ -1183,7 +1307,10 @@ cudaError_t launch_step(const DevCache& c, int layer, const AppendReq* app, int 
   }
 }
 
-int decode_ctas_per_sm(int g) { return g <= 4 ? Tune<4>::CTAS : Tune<8>::CTAS; }
+int decode_ctas_per_sm(int g, int gk) {
+  if (gk == 64) return g <= 4 ? Tune<4, 64>::CTAS : Tune<8, 64>::CTAS;
+  return g <= 4 ? Tune<4>::CTAS : Tune<8>::CTAS;
+}
 
 size_t decode_qfrag_bytes(int g) {
   return (g <= 4 ? QFrag<4>::WORDS : QFrag<8>::WORDS) * sizeof(uint32_t);

@@ -530,7 +530,7 @@ DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int
     total_pages += H * np;
     max_np = std::max(max_np, np);
   }
-  const int64_t target = std::max<int64_t>(1, (int64_t)c->num_sms * decode_ctas_per_sm(c->G()) - reserve);
+  const int64_t target = std::max<int64_t>(1, (int64_t)c->num_sms * decode_ctas_per_sm(c->G(), c->cfg.group_size) - reserve);
   const int64_t bf16 = (int64_t)DECODE_BF16_ITEMS * n * H;
   // the BF16 items are short: they share the first wave when few (one request), and
   // otherwise follow the INT2 blocks rather than shrinking the INT2 split
@@ -585,7 +585,6 @@ size_t decode_bytes_needed(const oscar_cache* c, int32_t layer, int32_t n, const
 
 oscar_status check_decode_batch(oscar_cache* c, int32_t layer, int32_t n, const int32_t* reqs) {
   if (!c->valid_layer(layer) || n < 1 || !reqs) return c->fail(OSCAR_ERR_INVALID_ARG, "bad layer or batch");
-  if (c->cfg.group_size != D) return c->fail(OSCAR_ERR_INVALID_ARG, "decode needs group_size 128");
   for (int32_t i = 0; i < n; ++i) {
     if (!c->valid_req(reqs[i])) return c->fail(OSCAR_ERR_INVALID_ARG, "bad request id");
     if (c->reqs[reqs[i]].T[layer] < 1) return c->fail(OSCAR_ERR_STATE, "request has no cached tokens");
@@ -733,7 +732,7 @@ oscar_status oscar_decode_step(oscar_cache* c, int32_t layer, int32_t n, const i
     // each append block of the front kernel (256 threads) displaces two stream blocks
     // until it ends; leaving their slots out keeps every stream block starting at once
     // (a large batch's front kernel is over before it matters: no reservation)
-    const int64_t slots = (int64_t)c->num_sms * decode_ctas_per_sm(c->G());
+    const int64_t slots = (int64_t)c->num_sms * decode_ctas_per_sm(c->G(), c->cfg.group_size);
     const int64_t app_blocks = (int64_t)m * c->cfg.num_kv_heads * 2;
     const int64_t reserve = 2 * app_blocks <= slots / 8 ? 2 * app_blocks : 0;
     const DecodePlan p = plan_decode(c, layer, m, reqs + b, b, ppc_min, dr, reserve);

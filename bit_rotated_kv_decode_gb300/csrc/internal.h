@@ -131,7 +131,7 @@ struct DecodeReq {
 };
 constexpr int DECODE_PER_LAUNCH = 64;
 constexpr int DECODE_BF16_ITEMS = 1 + RING_PAGES;   // BF16 work items per (request, kv head)
-int decode_ctas_per_sm(int g);                      // resident stream blocks per SM
+int decode_ctas_per_sm(int g, int gk);              // resident stream blocks per SM
 constexpr int MAX_CHUNKS_PER_HEAD = 512;
 // Workspace of one decode launch: the q_rot operands, decode_qfrag_bytes(G) per
 // (request, kv head) in launch order, then the partials fp32 [slot][G][PARTIAL_FLOATS].

@@ -71,3 +71,46 @@ def test_group64_prefill_adversarial(b):
     s.tokens[(r, 0)] = (k, v)
     s.cache.check()
     _exact(s.check_pages(r, 0))
+
+
+@pytest.mark.parametrize("hq", [32, 64, 8, 16])
+def test_group64_decode_matches_oracle(b, hq):
+    # ragged lengths: sink only, sink + part of the window, one partial history page,
+    # several shuffled pages with a ragged tail
+    from tests import parity
+    s = Setup(b, layers=2, hq=hq, hkv=8, max_req=5, max_pages=64, pages=400, seed=0xBEEF, group=64)
+    lengths = [30, 320, 449, 1700, 2600]
+    reqs = [s.open() for _ in lengths]
+    for layer in range(2):
+        for r, n in zip(reqs, lengths):
+            s.prefill(r, layer, n + layer)
+        s.append(reqs, layer, 0)
+    for layer in range(2):
+        q, out = s.decode(reqs, layer)
+        for i, r in enumerate(reqs):
+            parity.check_output(out[i].cpu().numpy(), s.oracle_decode(r, layer, q[i]))
+
+
+def test_group64_fused_step_matches_oracle(b):
+    from bit_rotated_kv_decode_gb300 import synth
+    from tests import parity
+    s = Setup(b, layers=1, hq=32, hkv=8, max_req=3, pages=300, group=64)
+    reqs = [s.open() for _ in range(3)]
+    for r, n in zip(reqs, [64 + 256 + 64 * 2 - 1, 900, 100]):
+        s.prefill(r, 0, n)
+    ws = b.new_workspace(s.cache.workspace_bytes(reqs) + (1 << 16))
+    for step in range(3):
+        k = torch.stack([s.kv(0, s.mirror.reqs[r].T[0], 1, 100 + r)[0][0] for r in reqs])
+        v = torch.stack([s.kv(0, s.mirror.reqs[r].T[0], 1, 100 + r)[1][0] for r in reqs])
+        q = synth.queries(0, 0, 32, len(reqs), step, device="cuda")
+        out = torch.full((len(reqs), 32, 128), float("nan"), dtype=torch.float32, device="cuda")
+        s.cache.step(0, reqs, k, v, q, out, ws)
+        for i, r in enumerate(reqs):
+            s.mirror.append(r, 0)
+            ok, ov = s.tokens[(r, 0)]
+            s.tokens[(r, 0)] = (torch.cat([ok, k[i:i + 1]]), torch.cat([ov, v[i:i + 1]]))
+        s.cache.check()
+        for i, r in enumerate(reqs):
+            parity.check_output(out[i].cpu().numpy(), s.oracle_decode(r, 0, q[i]))
+    for r in reqs:
+        _exact(s.check_pages(r, 0))
