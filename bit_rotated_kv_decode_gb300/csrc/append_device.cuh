@@ -38,6 +38,19 @@ __device__ __forceinline__ void store_group_code(const DevCache& c, uint8_t* rec
   }
 }
 
+// store_group_code with the group size fixed at compile time
+template <int GK>
+__device__ __forceinline__ void store_group_code_t(uint8_t* rec, int which, int slot, const GroupCode& g) {
+  const int lane = threadIdx.x & 31;
+  rec[(which ? V_CODES_OFF : K_CODES_OFF) + slot * CODE_BYTES + lane] = static_cast<uint8_t>(g.byte);
+  constexpr int LPG = GK / 4, MB = meta_bytes_for(GK);
+  if ((lane & (LPG - 1)) == 0) {
+    const int off = which ? v_meta_off_for(GK) : k_meta_off_for(GK);
+    *reinterpret_cast<uint32_t*>(rec + off + slot * MB + 4 * (lane / LPG)) =
+        static_cast<uint32_t>(g.s_bits) | (static_cast<uint32_t>(g.z_bits) << 16);
+  }
+}
+
 // quantize_group_warp for the cache's group size (warp-uniform branch)
 __device__ __forceinline__ GroupCode quantize_for(const DevCache& c, float4 x, float4 e, float4 sb, float tau,
                                                   float4 k4, const float* __restrict__ rt) {

@@ -54,6 +54,12 @@ __device__ __forceinline__ uint32_t code_of(float xc, float z, float s) {
   return static_cast<uint32_t>(fminf(fmaxf(rintf(t), 0.0f), 3.0f));
 }
 
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float scale_of(float mx, float mn) {
   return __half2float(__float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f)));
 }
@@ -261,10 +267,25 @@ __device__ __forceinline__ GroupCode quantize_group_warp(float4 xv, float4 ev, f
   const float s = __half2float(sh);
   uint32_t code[4];
   uint32_t unsure = 0;
+  // Fast decision of a whole interval [lo, hi] with the approximate reciprocal:
+  // q' = fl(d rcp(s)) is within |d / s| 2^-21 of the IEEE quotient fl(d / s)
+  // (rcp.approx: 1 ulp; two roundings of 2^-24), and M = (|q'| + 1) 2^-19 also
+  // covers the roundings of q' -/+ M + 1/2.  If both ends land in one rounding
+  // cell after the clamp, every value of the interval has that code; otherwise
+  // the IEEE quotient decides, as before.
+  const float rs = s == 0.0f ? 0.0f : rcp_approx(s);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    code[i] = code_of(lo[i], z, s);
-    if (code[i] != code_of(hi[i], z, s)) unsure |= 1u << i;
+    const float qa = __fmul_rn(__fsub_rn(lo[i], z), rs), qb = __fmul_rn(__fsub_rn(hi[i], z), rs);
+    const float ma = __fmul_rn(fabsf(qa) + 1.0f, 0x1p-19f), mb = __fmul_rn(fabsf(qb) + 1.0f, 0x1p-19f);
+    const float ca = fminf(fmaxf(floorf(qa - ma + 0.5f), 0.0f), 3.0f);
+    const float cb = fminf(fmaxf(floorf(qb + mb + 0.5f), 0.0f), 3.0f);
+    if (ca == cb) {
+      code[i] = static_cast<uint32_t>(ca);
+    } else {
+      code[i] = code_of(lo[i], z, s);
+      if (code[i] != code_of(hi[i], z, s)) unsure |= 1u << i;
+    }
   }
   // resolve the undecided codes one at a time, the whole warp computing each:
   // narrowed first, exactly only if the narrow interval still straddles a boundary

@@ -171,6 +171,7 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_
 // [x tiles_per_cta, (x + 1) tiles_per_cta) of PF_TILE positions each; the launch
 // sizes the grid to two resident blocks per SM, so R is split and staged once
 // per block.
+template <int GK>
 __global__ void __launch_bounds__(PF_THREADS, 2) prefill_hist_kernel(DevCache c, int layer, int slot,
                                                                   const uint16_t* __restrict__ k,
                                                                   const uint16_t* __restrict__ v,
@@ -316,8 +317,8 @@ __global__ void __launch_bounds__(PF_THREADS, 2) prefill_hist_kernel(DevCache c,
                                     __uint_as_float(kw.y << 16), __uint_as_float(kw.y & 0xffff0000u));
       const float sbound = __fmul_ru(__fsqrt_ru(__fmul_ru(sm.kn[j], 1.0001f)), colnorm);   // >= sum_i |k_i R_ic|
       const float err = __fmul_ru(sbound, PF_MMA_ERR);
-      const GroupCode g = quantize_for(c, x, make_float4(err, err, err, err),
-                                       make_float4(sbound, sbound, sbound, sbound), tau, k4, Rt);
+      const GroupCode g = quantize_group_warp<GK>(x, make_float4(err, err, err, err),
+                                                  make_float4(sbound, sbound, sbound, sbound), tau, k4, Rt);
       const int64_t h = t0 + j - SINK;
       const int32_t page = sm.pages[h / PAGE - (t0 - SINK) / PAGE];
       const int row = static_cast<int>(h % PAGE);
@@ -325,7 +326,8 @@ __global__ void __launch_bounds__(PF_THREADS, 2) prefill_hist_kernel(DevCache c,
         if (lane == 0) atomicOr(c.err, ERR_INT2_PAGE);
         continue;
       }
-      store_group_code(c, int2_record(c, layer, page, head), which, row, g);
+      store_group_code_t<GK>(c.int2 + layer * c.int2_layer_stride + ((size_t)page * c.Hkv + head) * record_for(GK),
+                             which, row, g);
     }
   }
 }
@@ -396,8 +398,11 @@ cudaError_t launch_prefill_hist(const DevCache& c, int layer, int slot, const ui
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 32 || !(attr_done & (1u << dev))) {
-    e = cudaFuncSetAttribute(prefill_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(prefill_hist_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(PREFILL_SMEM));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(prefill_hist_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(PREFILL_SMEM));
     if (e != cudaSuccess) return e;
     if (dev < 32) attr_done |= 1u << dev;
   }
@@ -409,8 +414,12 @@ cudaError_t launch_prefill_hist(const DevCache& c, int layer, int slot, const ui
   const int64_t per_matrix = std::max<int64_t>(1, std::min<int64_t>(tiles, (2 * (int64_t)sms) / (2 * c.Hkv)));
   const int64_t tiles_per_cta = (tiles + per_matrix - 1) / per_matrix;
   dim3 grid(static_cast<unsigned>((tiles + tiles_per_cta - 1) / tiles_per_cta), c.Hkv, 2);
-  prefill_hist_kernel<<<grid, PF_THREADS, PREFILL_SMEM, s>>>(c, layer, slot, k, v, in_base, h0, h1,
-                                                             static_cast<int>(tiles_per_cta));
+  if (c.gk == 64)
+    prefill_hist_kernel<64><<<grid, PF_THREADS, PREFILL_SMEM, s>>>(c, layer, slot, k, v, in_base, h0, h1,
+                                                                   static_cast<int>(tiles_per_cta));
+  else
+    prefill_hist_kernel<128><<<grid, PF_THREADS, PREFILL_SMEM, s>>>(c, layer, slot, k, v, in_base, h0, h1,
+                                                                    static_cast<int>(tiles_per_cta));
   return cudaGetLastError();
 }
 
