@@ -216,3 +216,40 @@ def test_workspace_query(b):
     lib.prefill(r, 1, None, None, n_tokens=100)
     nb = lib.workspace_bytes([r])
     assert nb > 256 and nb % 256 == 0
+
+
+def _bf16_plan_blocks(lens, hkv, sms):
+    """Chunk plan of the BF16 baseline: the ppc (one of ceil(max pages / c)) with the
+    fewest rounds of resident blocks times (ppc + 1); 3 blocks per SM."""
+    nps = [(t + 63) // 64 for t in lens]
+    mx, slots = max(nps), 3 * sms
+    best = None
+    for c in range(1, min(mx, 256) + 1):
+        ppc = -(-mx // c)
+        blocks = sum(hkv * max(1, -(-n // ppc)) for n in nps)
+        cost = -(-blocks // slots) * (ppc + 1)
+        if best is None or cost < best[0]:
+            best = (cost, blocks)
+    return best[1]
+
+
+def test_bf16_baseline_workspace_plan(b):
+    import ctypes
+    import torch
+    lib = b.load()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 152
+
+    def ws(lens, hq, hkv):
+        arr = (ctypes.c_int32 * len(lens))(*lens)
+        return lib.oscar_bf16_decode_workspace_bytes(len(lens), arr, hq, hkv)
+
+    for lens, hq, hkv in [([100000], 32, 8), ([40000] * 32, 32, 8), ([131072] * 8, 64, 8), ([1, 64, 65, 5000], 8, 8)]:
+        g = hq // hkv
+        assert ws(lens, hq, hkv) == 256 + _bf16_plan_blocks(lens, hkv, sms) * g * 132 * 4, (lens[:2], hq)
+    # one wave of equal chunks at 100K on 152 SMs: 56 chunks of 28 pages per kv head
+    if sms == 152:
+        assert _bf16_plan_blocks([100000], 8, 152) == 448
+    assert ws([], 32, 8) == 0
+    assert ws([0], 32, 8) == 0
+    assert ws([100], 20, 8) == 0                       # query heads not a multiple of kv heads
+    assert ws([100] * 65, 32, 8) == 0                  # more than 64 requests per launch
