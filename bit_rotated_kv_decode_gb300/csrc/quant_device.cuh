@@ -174,15 +174,30 @@ __device__ __forceinline__ GroupCode quantize_group_warp(float4 xv, float4 ev, f
     lo[i] = clip_canon(__fsub_rd(x[i], e), tau);
     hi[i] = clip_canon(__fadd_ru(x[i], e), tau);
   }
+  // min / max over the group's lanes: one warp-wide redux.sync (f32, sm_100 family)
+  // for a 128-channel group, a half-warp butterfly for 64 (no -0 or NaN reaches here:
+  // the values are clipped and canonicalised)
   auto reduce_min = [](float v) {
+    if constexpr (GK == 128) {
+      float r;
+      asm volatile("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+      return r;
+    } else {
 #pragma unroll
-    for (int off = RED0; off > 0; off >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, off));
-    return v;
+      for (int off = RED0; off > 0; off >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, off));
+      return v;
+    }
   };
   auto reduce_max = [](float v) {
+    if constexpr (GK == 128) {
+      float r;
+      asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+      return r;
+    } else {
 #pragma unroll
-    for (int off = RED0; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-    return v;
+      for (int off = RED0; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+      return v;
+    }
   };
   auto exact = [&](int ch) {
     const float4 r = __ldg(reinterpret_cast<const float4*>(rt + (size_t)ch * D) + lane);
