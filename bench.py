@@ -102,13 +102,15 @@ def committed_traffic(kernel: str):
             entry = json.load(f)[kernel]
     except Exception:
         return None
-    src = os.path.join(ROOT, "bit_rotated_kv_decode_gb300", "csrc", entry["source"])
     import hashlib
+    h = hashlib.sha256()
     try:
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        # the kernel's file and the headers it includes, in the listed order
+        for name in entry.get("sources", [entry["source"]]):
+            h.update(open(os.path.join(ROOT, "bit_rotated_kv_decode_gb300", "csrc", name), "rb").read())
     except OSError:
         return None
-    return entry["bytes_per_launch"] if digest == entry.get("source_sha256_16") else None
+    return entry["bytes_per_launch"] if h.hexdigest()[:16] == entry.get("source_sha256_16") else None
 
 
 class ClockSampler:
