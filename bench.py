@@ -106,7 +106,7 @@ def committed_traffic(kernel: str):
     h = hashlib.sha256()
     try:
         # the kernel's file and the headers it includes, in the listed order
-        for name in entry.get("sources", [entry["source"]]):
+        for name in entry["sources"] if "sources" in entry else [entry["source"]]:
             h.update(open(os.path.join(ROOT, "bit_rotated_kv_decode_gb300", "csrc", name), "rb").read())
     except OSError:
         return None
