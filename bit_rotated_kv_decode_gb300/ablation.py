@@ -17,6 +17,10 @@ exact attention over the BF16 tokens (float64 on the host) it reports:
   * kl: mean KL(softmax(S) || softmax(S^)) over query heads and queries, all
     tokens (the BF16 segments are exact on both sides);
   * out_rel, out_max_abs: the decode call's outputs.
+The same page says the permuted bit-reversal P_br spreads every importance
+level over the quantisation groups, which only matters with more than one group
+per token-head: the "_nobr" variants drop it (R = H, R = U H) to measure that at
+G_K = 64.
 Usage: ``python -m bit_rotated_kv_decode_gb300.ablation``.
 """
 from __future__ import annotations
@@ -28,15 +32,16 @@ import numpy as np
 from . import calibrate, synth
 
 VARIANTS = ("naive", "hadamard", "oscar")
+BR_VARIANTS = ("hadamard_nobr", "hadamard", "oscar_nobr", "oscar")
 
 
 def rotations(variant: str, q_cal, k_cal, v_cal, hkv: int, clip: float):
     """fp32 R_K, R_V [H_kv][d][d] and tau_K, tau_V [H_kv] of one variant."""
     d = synth.HEAD_DIM
-    if variant == "oscar":
-        return calibrate.calibrate_layer(q_cal, k_cal, v_cal, clip, clip)
-    if variant == "hadamard":
-        r = calibrate.composed_rotation(np.eye(d)).astype(np.float32)
+    if variant in ("oscar", "oscar_nobr"):
+        return calibrate.calibrate_layer(q_cal, k_cal, v_cal, clip, clip, bit_reversal=variant == "oscar")
+    if variant in ("hadamard", "hadamard_nobr"):
+        r = calibrate.composed_rotation(np.eye(d), bit_reversal=variant == "hadamard").astype(np.float32)
     elif variant == "naive":
         r = np.eye(d, dtype=np.float32)
     else:
@@ -63,24 +68,27 @@ def exact_attention(q, k, v, hkv: int):
     return out
 
 
-def dequantised_keys(pool, hist_pages, nhist: int, rk, hkv: int):
-    """K^ [nhist][H_kv][d] (float64) from INT2 records [pages][H_kv][4608] (uint8)."""
+def dequantised_keys(pool, hist_pages, nhist: int, rk, hkv: int, group: int = 128):
+    """K^ [nhist][H_kv][d] (float64) from INT2 records [pages][H_kv][4608 or 5120] (uint8):
+    per group of ``group`` channels, x = z + s c from that group's {s, z}."""
     d = synth.HEAD_DIM
+    ng = d // group
     out = np.empty((nhist, hkv, d))
     shifts = np.array([0, 2, 4, 6], dtype=np.uint8)
     for h in range(nhist):
-        rec = pool[hist_pages[h // 64]]                 # [H_kv][4608]
+        rec = pool[hist_pages[h // 64]]                 # [H_kv][record]
         row = h % 64
         codes = rec[:, 32 * row: 32 * row + 32]         # K codes: channel 4 j + i in bits 2 i of byte j
-        c = ((codes[:, :, None] >> shifts) & 3).reshape(hkv, d).astype(np.float64)
-        meta = rec[:, 4096 + 4 * row: 4096 + 4 * row + 4].copy().view(np.float16).astype(np.float64)   # {s, z}
-        x = meta[:, 1:2] + meta[:, 0:1] * c
+        c = ((codes[:, :, None] >> shifts) & 3).reshape(hkv, ng, group).astype(np.float64)
+        meta = rec[:, 4096 + 4 * ng * row: 4096 + 4 * ng * (row + 1)].copy().view(np.float16).astype(np.float64)
+        meta = meta.reshape(hkv, ng, 2)                 # per group {s, z}
+        x = (meta[:, :, 1:2] + meta[:, :, 0:1] * c).reshape(hkv, d)
         out[h] = np.einsum("hc,hic->hi", x, rk.astype(np.float64))   # x R^T: row i of R times x
     return out
 
 
 def run(cfg_id: int = 0, hq: int = 32, hkv: int = 8, tokens: int = 8192, queries: int = 8, clip: float = 0.9,
-        layer: int = 0) -> dict:
+        layer: int = 0, group: int = 128, variants=VARIANTS) -> dict:
     import torch
 
     from . import binding
@@ -95,15 +103,15 @@ def run(cfg_id: int = 0, hq: int = 32, hkv: int = 8, tokens: int = 8192, queries
     refs = [exact_attention(q[0].float().cpu().numpy().astype(np.float64), kf, vf, hkv) for q in qs]
     pages = (tokens - 320) // 64 + 2
     results = {}
-    for variant in VARIANTS:
+    for variant in variants:
         rk, rv, tk, tv = rotations(variant, q_cal, k_cal, v_cal, hkv, clip)
-        cfg = binding.make_config(1, hq, hkv, 1, pages, pages + 2, 0, 0.0, 0)
+        cfg = binding.make_config(1, hq, hkv, 1, pages, pages + 2, 0, 0.0, 0, group_size=group)
         cache = binding.OscarCache(cfg, torch.from_numpy(rk).cuda(), torch.from_numpy(rv).cuda(), tk, tv)
         r = cache.open()
         cache.prefill(r, 0, k, v)
         ws = binding.new_workspace(cache.workspace_bytes([r]))
         nhist = tokens - 320
-        kq = dequantised_keys(cache.int2_pool(0).cpu().numpy(), cache.pages(r)[0], nhist, rk, hkv)
+        kq = dequantised_keys(cache.int2_pool(0).cpu().numpy(), cache.pages(r)[0], nhist, rk, hkv, group)
         khat = kf.copy()
         khat[64:64 + nhist] = kq
         g = hq // hkv
@@ -134,9 +142,12 @@ def run(cfg_id: int = 0, hq: int = 32, hkv: int = 8, tokens: int = 8192, queries
         results[variant] = {"logit_rel": (lnum / lden) ** 0.5, "kl": kl / (len(qs) * hq),
                             "out_rel": (num / den) ** 0.5, "out_max_abs": max_abs}
     return {"config": {"cfg_id": cfg_id, "q_heads": hq, "kv_heads": hkv, "tokens": tokens, "queries": queries,
-                       "clip": clip, "layer": layer}, "results": results}
+                       "clip": clip, "layer": layer, "group": group}, "results": results}
 
 
 if __name__ == "__main__":
     for clip in (1.0, 0.9):
         print(json.dumps(run(clip=clip)))
+    # the bit-reversal's share, with one group and with two groups per token-head
+    for group in (128, 64):
+        print(json.dumps(run(clip=0.9, group=group, variants=BR_VARIANTS)))

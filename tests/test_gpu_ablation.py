@@ -21,3 +21,16 @@ def test_rotations_beat_naive_int2():
     for variant in ("hadamard", "oscar"):
         assert r[variant]["logit_rel"] < 0.6 * r["naive"]["logit_rel"], r
         assert r[variant]["kl"] < 0.6 * r["naive"]["kl"], r
+
+
+def test_rotations_beat_naive_int2_at_group64():
+    # two {s, z} per token-head: the cache's 5120-byte records are read back per group
+    from bit_rotated_kv_decode_gb300 import ablation, build
+    build.build()
+    r = ablation.run(tokens=2048 + 320, queries=2, clip=0.9, group=64)["results"]
+    for variant in ("hadamard", "oscar"):
+        assert r[variant]["logit_rel"] < 0.6 * r["naive"]["logit_rel"], r
+        assert r[variant]["kl"] < 0.6 * r["naive"]["kl"], r
+    # finer groups: the output error is no worse than half again the 128-group one
+    r128 = ablation.run(tokens=2048 + 320, queries=2, clip=0.9)["results"]
+    assert r["oscar"]["logit_rel"] < 1.5 * r128["oscar"]["logit_rel"], (r, r128)
