@@ -218,6 +218,31 @@ def test_workspace_query(b):
     assert nb > 256 and nb % 256 == 0
 
 
+def test_group64_geometry_and_state_machine(b):
+    # G_K = 64 changes the record (5120 bytes: two {s, z} per token-head) and nothing
+    # in the page tables or lengths: the same calls give the same state as group 128
+    from oracle import layout
+    tau = np.ones((2, 8), np.float32)
+    caches = []
+    for group in (128, 64):
+        cfg = b.make_config(2, 32, 8, 2, 64, 200, 0, 0.0, 7, group_size=group)
+        caches.append(b.OscarCache(cfg, tau_k=tau, tau_v=tau, dry_run=True))
+    l128, l64 = (c.layout() for c in caches)
+    assert l128.int2_record_bytes == layout.record_layout(128)["record"] == 4608
+    assert l64.int2_record_bytes == layout.record_layout(64)["record"] == 5120
+    assert l64.int2_page_stride == 8 * 5120 and l64.int2_layer_stride >= 200 * 8 * 5120
+    assert l64.total_bytes > l128.total_bytes
+    for c in caches:
+        r = c.open()
+        c.prefill(r, 0, None, None, n_tokens=3000)
+        c.prefill(r, 1, None, None, n_tokens=700)
+        c.demote_layers(0, 2, [r])
+        c.demote(1, [r])
+    a, g = caches
+    assert a.pages(0) == g.pages(0)
+    assert [a.length(0, layer) for layer in range(2)] == [g.length(0, layer) for layer in range(2)]
+
+
 def _bf16_plan_blocks(lens, hkv, sms):
     """Chunk plan of the BF16 baseline: the ppc (one of ceil(max pages / c)) with the
     fewest rounds of resident blocks times (ppc + 1); 3 blocks per SM."""
