@@ -123,7 +123,10 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.proc = None
         self.gpu = gpu_index
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # raw samples: a per-process scratch file (or OSCAR_CLOCKS_CSV to keep them)
+        import tempfile
+        self.path = os.environ.get("OSCAR_CLOCKS_CSV") or os.path.join(
+            tempfile.gettempdir(), f"oscar_clocks_rank{gpu_index}_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
