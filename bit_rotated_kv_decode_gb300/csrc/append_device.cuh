@@ -25,20 +25,6 @@ __device__ __forceinline__ uint8_t* int2_record(const DevCache& c, int layer, in
 // The lane's group code into a record at token slot `slot`: code bytes from every
 // lane, then {s, z} from the first lane of each group (lane 0; lanes 0 and 16 at
 // G_K = 64).
-__device__ __forceinline__ void store_group_code(const DevCache& c, uint8_t* rec, int which, int slot,
-                                                 const GroupCode& g) {
-  const int lane = threadIdx.x & 31;
-  rec[(which ? V_CODES_OFF : K_CODES_OFF) + slot * CODE_BYTES + lane] = static_cast<uint8_t>(g.byte);
-  const int lanes_per_group = c.gk / 4;
-  if ((lane & (lanes_per_group - 1)) == 0) {
-    const int mb = meta_bytes_for(c.gk);
-    const int off = which ? v_meta_off_for(c.gk) : k_meta_off_for(c.gk);
-    *reinterpret_cast<uint32_t*>(rec + off + slot * mb + 4 * (lane / lanes_per_group)) =
-        static_cast<uint32_t>(g.s_bits) | (static_cast<uint32_t>(g.z_bits) << 16);
-  }
-}
-
-// store_group_code with the group size fixed at compile time
 template <int GK>
 __device__ __forceinline__ void store_group_code_t(uint8_t* rec, int which, int slot, const GroupCode& g) {
   const int lane = threadIdx.x & 31;
@@ -49,12 +35,6 @@ __device__ __forceinline__ void store_group_code_t(uint8_t* rec, int which, int 
     *reinterpret_cast<uint32_t*>(rec + off + slot * MB + 4 * (lane / LPG)) =
         static_cast<uint32_t>(g.s_bits) | (static_cast<uint32_t>(g.z_bits) << 16);
   }
-}
-
-// quantize_group_warp for the cache's group size (warp-uniform branch)
-__device__ __forceinline__ GroupCode quantize_for(const DevCache& c, float4 x, float4 e, float4 sb, float tau,
-                                                  float4 k4, const float* __restrict__ rt) {
-  return c.gk == 64 ? quantize_group_warp<64>(x, e, sb, tau, k4, rt) : quantize_group_warp<128>(x, e, sb, tau, k4, rt);
 }
 
 constexpr int APPEND_THREADS = 256;
@@ -74,6 +54,7 @@ struct AppendSmem {
   __align__(16) float apart[APPEND_GROUPS][D];
 };
 
+template <int GK>
 __device__ __forceinline__ void append_block(const DevCache& c, int layer, const uint16_t* __restrict__ k,
                                              const uint16_t* __restrict__ v, const AppendReq& q, int head,
                                              int which, AppendSmem& sm) {
@@ -143,9 +124,10 @@ __device__ __forceinline__ void append_block(const DevCache& c, int layer, const
         const float tau = (which ? c.tau_v : c.tau_k)[lh];
         const float* __restrict__ Rt = (which ? c.rot_vt : c.rot_kt) + lh * D * D;
         const float4 k4 = make_float4(xin[4 * lane], xin[4 * lane + 1], xin[4 * lane + 2], xin[4 * lane + 3]);
-        const GroupCode g = quantize_for(c, make_float4(x[0], x[1], x[2], x[3]), make_float4(e[0], e[1], e[2], e[3]),
-                                         make_float4(sabs[0], sabs[1], sabs[2], sabs[3]), tau, k4, Rt);
-        store_group_code(c, int2_record(c, layer, q.hist_page, head), which, q.demote_slot, g);
+        const GroupCode g = quantize_group_warp<GK>(make_float4(x[0], x[1], x[2], x[3]),
+                                                    make_float4(e[0], e[1], e[2], e[3]),
+                                                    make_float4(sabs[0], sabs[1], sabs[2], sabs[3]), tau, k4, Rt);
+        store_group_code_t<GK>(int2_record(c, layer, q.hist_page, head), which, q.demote_slot, g);
       }
       if (q.pt_index >= 0 && head == 0 && which == 0 && t == 0) {
         c.hist_pt[(size_t)q.slot * c.max_pages + q.pt_index] = q.hist_page;

@@ -1160,7 +1160,7 @@ __global__ void __launch_bounds__(FRONT_THREADS) step_front_kernel(DevCache c, i
   const int app_blocks = f.n_app * c.Hkv * 2;
   if ((int)blockIdx.x < app_blocks) {
     const int b = blockIdx.x;
-    append_block(c, layer, k, v, f.app[b / (2 * c.Hkv)], (b / 2) % c.Hkv, b % 2, sm.app);   // waits inside
+    append_block<GK>(c, layer, k, v, f.app[b / (2 * c.Hkv)], (b / 2) % c.Hkv, b % 2, sm.app);   // waits inside
     return;
   }
   const int b = blockIdx.x - app_blocks;

@@ -337,11 +337,12 @@ struct AppendArgs {
   AppendReq r[APPEND_PER_LAUNCH];
 };
 
+template <int GK>
 __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(DevCache c, int layer,
                                                                 const uint16_t* __restrict__ k,
                                                                 const uint16_t* __restrict__ v, AppendArgs a) {
   __shared__ AppendSmem sm;
-  append_block(c, layer, k, v, a.r[blockIdx.x], blockIdx.y, blockIdx.z, sm);
+  append_block<GK>(c, layer, k, v, a.r[blockIdx.x], blockIdx.y, blockIdx.z, sm);
 }
 
 struct DemoteArgs {
@@ -352,10 +353,11 @@ struct DemoteArgs {
 // Multi-layer demote: block (entry, kv head, K or V), each entry one layer of
 // one request.  Layers write disjoint pool regions, and only the first layer
 // to open a history page writes its page-table entry.
+template <int GK>
 __global__ void __launch_bounds__(APPEND_THREADS) demote_layers_kernel(DevCache c, DemoteArgs a) {
   __shared__ AppendSmem sm;
   const DemoteEntry& e = a.e[blockIdx.x];
-  append_block(c, e.layer, nullptr, nullptr, e.r, blockIdx.y, blockIdx.z, sm);
+  append_block<GK>(c, e.layer, nullptr, nullptr, e.r, blockIdx.y, blockIdx.z, sm);
 }
 
 }  // namespace
@@ -438,7 +440,8 @@ cudaError_t launch_append(const DevCache& c, int layer, const AppendReq* reqs, i
     cfg.stream = s;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, append_kernel, c, layer, k, v, a);
+    const cudaError_t e = c.gk == 64 ? cudaLaunchKernelEx(&cfg, append_kernel<64>, c, layer, k, v, a)
+                                     : cudaLaunchKernelEx(&cfg, append_kernel<128>, c, layer, k, v, a);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -458,7 +461,8 @@ cudaError_t launch_demote_layers(const DevCache& c, const DemoteEntry* entries, 
     cfg.stream = s;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, demote_layers_kernel, c, a);
+    const cudaError_t e = c.gk == 64 ? cudaLaunchKernelEx(&cfg, demote_layers_kernel<64>, c, a)
+                                     : cudaLaunchKernelEx(&cfg, demote_layers_kernel<128>, c, a);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
