@@ -31,6 +31,33 @@ def test_closed_form_four_levels_and_byte_order():
     assert np.array_equal(layout.unpack_codes(packed), c)
 
 
+def test_v_codes_channel_major_closed_form():
+    """V code region: channel c owns 16 bytes at 16c, slot r in bits 2(r%4) of byte r//4.
+    Slot r of channel c carries (r + c) % 4 here, so each byte is a fixed closed form:
+    byte j of channel c holds codes (4j + i + c) % 4 at bits 2i."""
+    r = np.arange(64)[:, None]
+    c = np.arange(128)[None, :]
+    codes = ((r + c) % 4).astype(np.uint8)                      # [slot][channel]
+    region = layout.pack_v_codes_page(codes)
+    assert region.shape == (2048,)
+    for ch in (0, 1, 2, 3, 77, 127):
+        want = sum(((i + ch) % 4) << (2 * i) for i in range(4))  # independent of j: 4j = 0 mod 4
+        assert np.all(region[16 * ch: 16 * ch + 16] == want)
+    # round trip per slot, and a brute-force bit read of one entry
+    for slot in (0, 1, 5, 31, 62, 63):
+        assert np.array_equal(layout.v_slot_codes(region, slot), codes[slot])
+    rng = np.random.default_rng(5)
+    rnd = rng.integers(0, 4, size=(64, 128)).astype(np.uint8)
+    reg = layout.pack_v_codes_page(rnd)
+    for slot, ch in ((7, 3), (40, 100), (63, 127)):
+        byte = int(reg[16 * ch + slot // 4])
+        assert (byte >> (2 * (slot % 4))) & 3 == rnd[slot, ch]
+    rec = np.zeros(4608, np.uint8)
+    rec[2048:4096] = reg
+    kc, vc, km, vm = layout.record_slot_fields(rec, 9)
+    assert np.array_equal(layout.unpack_codes(vc), rnd[9])
+
+
 def test_round_half_to_even_ties():
     # z = 0, s = 1 -> t = x; ties at 0.5, 1.5, 2.5 go to 0, 2, 2
     x = _group([0.0, 0.5, 1.5, 2.5, 3.0, 0.49, 1.51, 2.2])
