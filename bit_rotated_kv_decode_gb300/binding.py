@@ -77,6 +77,7 @@ _SIGNATURES = {
     "oscar_decode_attention_noalloc": (c_int32, [_P, c_int32, c_int32, POINTER(c_int32), _P, _P, _P]),
     "oscar_decode_step": (c_int32, [_P, c_int32, c_int32, POINTER(c_int32), _P, _P, _P, _P, _P, c_size_t, _P]),
     "oscar_cache_check": (c_int32, [_P, _P]),
+    "oscar_debug_decode_hooks": (c_int32, [_P, ctypes.c_uint32, c_int32]),
     "oscar_last_error": (c_char_p, [_P]),
     "oscar_bf16_decode_workspace_bytes": (c_size_t, [c_int32, POINTER(c_int32), c_int32, c_int32]),
     "oscar_bf16_decode": (c_int32, [_P, c_int64, _P, c_int32, POINTER(c_int32), c_int32, c_int32, c_int32, c_float,
@@ -274,6 +275,10 @@ class OscarCache:
 
     def check(self, stream=None) -> None:
         self._check(self.lib.oscar_cache_check(self.h, None if self.dry else _stream_ptr(stream)), "device check")
+
+    def debug_decode_hooks(self, wait_limit: int = 100000, hold_pair: int = -1) -> None:
+        """Failure-detection hooks of this cache's decode launches (tests only)."""
+        self._check(self.lib.oscar_debug_decode_hooks(self.h, wait_limit, hold_pair), "decode hooks")
 
     # -- views of device memory (for tests and inspection) ------------------------
     def int2_pool(self, layer: int):

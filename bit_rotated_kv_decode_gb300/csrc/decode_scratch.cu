@@ -9,11 +9,13 @@
 // caller-owned workspace.  Nothing here calls cudaMalloc, cudaFree or any
 // library routine that allocates.
 //
-// The array is one per device.  Set-up, once per device with that device
-// current, takes its address with cudaGetSymbolAddress and zeroes it on the
-// caller's stream (the decode itself needs no initial contents).  Two calls
-// that use the array at the same time on one device -- on different streams,
-// or from different caches -- race.
+// The array is one per device.  Every call takes its address afresh with
+// cudaGetSymbolAddress (with the caller's device current), so a module that was
+// reloaded -- after cudaDeviceReset, say -- is never reached through a stale
+// pointer.  The first call on a device also zeroes the array on the caller's
+// stream; the decode needs no initial contents, so a reload that leaves other
+// contents does no harm.  Two calls that use the array at the same time on one
+// device -- on different streams, or from different caches -- race.
 #include <mutex>
 
 #include "internal.h"
@@ -25,7 +27,7 @@ namespace {
 
 constexpr int MAX_DEVICES = 64;
 std::mutex g_mu;
-void* g_addr[MAX_DEVICES] = {};
+bool g_zeroed[MAX_DEVICES] = {};
 
 }  // namespace
 
@@ -34,16 +36,16 @@ cudaError_t decode_scratch_address(void** ptr, cudaStream_t s) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_decode_scratch);
+  if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_decode_scratch);
-    if (e != cudaSuccess) return e;
+  if (!g_zeroed[dev]) {
     e = cudaMemsetAsync(p, 0, DECODE_SCRATCH_BYTES, s);
     if (e != cudaSuccess) return e;
-    g_addr[dev] = p;
+    g_zeroed[dev] = true;
   }
-  *ptr = g_addr[dev];
+  *ptr = p;
   return cudaSuccess;
 }
 

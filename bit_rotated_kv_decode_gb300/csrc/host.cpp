@@ -93,10 +93,7 @@ struct oscar_cache {
   std::vector<Request> reqs;
   std::string err;
   int num_sms = 152;
-  uint64_t uid = 0;               // process-unique cache id (high half of decode epochs)
-  uint32_t decode_launches = 0;
-
-  uint64_t next_epoch() { return (uid << 32) | ++decode_launches; }
+  DecodeDebug dbg{DECODE_WAIT_LIMIT, -1};   // failure-detection hooks of decode launches
 
   oscar_status fail(oscar_status s, const std::string& msg) {
     err = msg;
@@ -203,8 +200,6 @@ oscar_status oscar_cache_create(const oscar_cache_config* cfg, void* device_mem,
     }
   }
   oscar_cache* c = new oscar_cache();
-  static std::atomic<uint64_t> next_uid{1};
-  c->uid = next_uid.fetch_add(1);
   c->cfg = *cfg;
   if (c->cfg.num_bf16_pages == 0) c->cfg.num_bf16_pages = (int64_t)BF16_PAGES_PER_REQ * cfg->max_requests;
   if (c->cfg.softmax_scale == 0.0f) c->cfg.softmax_scale = 1.0f / std::sqrt(static_cast<float>(D));
@@ -514,71 +509,113 @@ oscar_status write_batch(oscar_cache* c, int32_t layer, int32_t n, const int32_t
   return err == cudaSuccess ? OSCAR_OK : c->cuda_fail(err, append ? "append launch" : "demote launch");
 }
 
-// Work split of one decode launch over reqs[0..n), n <= DECODE_PER_LAUNCH.
-// Per (request, kv head): five BF16 items (sink page, four ring pages) and
-// INT2 chunks of pages_per_chunk pages, sized so the stream launch is about one
-// wave of resident blocks.
-int64_t chunks_for(int64_t np, int64_t ppc) { return np == 0 ? 0 : (np + ppc - 1) / ppc; }
+// BF16 half-pages (32 rows) of one kv head holding a cached token: the sink rows
+// [0, min(T, 64)); ring slot s = 64 (page - 1) + r holds position
+// he + ((s - (he - 64)) mod 256), cached while below T.
+int bf16_half_pages(int64_t T, int64_t he) {
+  int n = 0;
+  for (int hp = 0; hp < 2 * DECODE_BF16_ITEMS; ++hp) {
+    const int which = hp / 2;
+    bool any = false;
+    for (int r = 32 * (hp % 2); r < 32 * (hp % 2) + 32 && !any; ++r) {
+      if (which == 0) {
+        any = r < std::min<int64_t>(T, SINK);
+      } else if (T > SINK) {
+        const int64_t s = PAGE * (which - 1) + r;
+        const int64_t p = he + (((s - (he - SINK)) % RECENT) + RECENT) % RECENT;
+        any = p < T;
+      }
+    }
+    n += any ? 1 : 0;
+  }
+  return n;
+}
 
-// reserve: resident stream-block slots taken by a kernel still running beside it
+constexpr int DECODE_SEGMAX = 16;   // segments one decode CTA may touch (the kernel's table)
+
+// Work split of one decode launch over reqs[0..n), n <= DECODE_PER_LAUNCH: the
+// segments (request, kv head) in order, each its INT2 pages (cost 1) then its BF16
+// block, cut into one contiguous equal-cost range per CTA, one CTA per SM.
 DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int32_t* reqs, int32_t first_row,
-                       int64_t ppc_min, DecodeReq* out, int64_t reserve = 0) {
+                       DecodeReq* out) {
   const int64_t H = c->cfg.num_kv_heads;
-  int64_t total_pages = 0, max_np = 0;
-  for (int32_t i = 0; i < n; ++i) {
-    const int64_t np = pages_for(c->reqs[reqs[i]].he[layer]);
-    total_pages += H * np;
-    max_np = std::max(max_np, np);
-  }
-  const int64_t target = std::max<int64_t>(1, (int64_t)c->num_sms * decode_ctas_per_sm(c->G(), c->cfg.group_size) - reserve);
-  const int64_t bf16 = (int64_t)DECODE_BF16_ITEMS * n * H;
-  // the BF16 items are short: they share the first wave when few (one request), and
-  // otherwise follow the INT2 blocks rather than shrinking the INT2 split
-  const int64_t budget = std::max<int64_t>(n * H, target - std::min<int64_t>(bf16, target / 8));
-  int64_t ppc = std::max<int64_t>({ppc_min, 2, (total_pages + budget - 1) / budget,
-                                   (max_np + MAX_CHUNKS_PER_HEAD - 1) / MAX_CHUNKS_PER_HEAD});
-  for (;;) {
-    int64_t items = 0;
-    for (int32_t i = 0; i < n; ++i) items += H * chunks_for(pages_for(c->reqs[reqs[i]].he[layer]), ppc);
-    if (items <= budget || ppc >= max_np) break;
-    ++ppc;
-  }
-  DecodePlan p{};
-  p.n = n;
-  p.pages_per_chunk = static_cast<int>(std::min<int64_t>(ppc, INT32_MAX));
-  int64_t int2 = 0, parts = 0;
+  int64_t cost = 0;
+  std::vector<int64_t> seg_cost;
+  seg_cost.reserve((size_t)n * H);
   for (int32_t i = 0; i < n; ++i) {
     const Request& r = c->reqs[reqs[i]];
-    const int64_t chunks = chunks_for(pages_for(r.he[layer]), ppc);
+    const int64_t T = r.T[layer], he = r.he[layer];
+    const int64_t np = pages_for(he);
+    const int64_t bf = (int64_t)DECODE_BF16_HALF_COST * bf16_half_pages(T, he);
     if (out) {
       DecodeReq& d = out[i];
       d.slot = reqs[i];
       d.batch_row = first_row + i;
-      d.tokens = static_cast<int32_t>(r.T[layer]);
-      d.hist_end = static_cast<int32_t>(r.he[layer]);
+      d.tokens = static_cast<int32_t>(T);
+      d.hist_end = static_cast<int32_t>(he);
       d.sink_page = r.bf16_pt[0];
       for (int k = 0; k < RING_PAGES; ++k) d.ring_page[k] = r.bf16_pt[1 + k];
-      d.int2_start = static_cast<int32_t>(int2);
-      d.chunks = static_cast<int32_t>(chunks);
-      d.part_start = static_cast<int32_t>(parts);
       d.hot_page = -1;
+      d.npages = static_cast<int32_t>(np);
+      d.cost_start = static_cast<int32_t>(cost);
+      d.bf16_cost = static_cast<int32_t>(bf);
     }
-    int2 += H * chunks;
-    parts += H * (DECODE_BF16_ITEMS + chunks);
+    for (int64_t h = 0; h < H; ++h) seg_cost.push_back(np + bf);
+    cost += H * (np + bf);
   }
-  p.int2_items = static_cast<int>(int2);
-  p.total_items = static_cast<int>(int2 + bf16);
-  p.qrot_bytes = align256((size_t)n * H * decode_qfrag_bytes(c->G()));
-  p.partial_bytes = align256((size_t)parts * c->G() * PARTIAL_FLOATS * sizeof(float));
+  DecodePlan p{};
+  p.n = n;
+  p.total_cost = cost;
+  p.segments = (int64_t)n * H;
+  int64_t ncta = std::max<int64_t>(1, std::min<int64_t>(c->num_sms, cost));
+  // more CTAs (up to four per SM) while one of them would touch more segments than
+  // its table holds; the caller splits the batch if that is not enough
+  p.worst_segments = 0;
+  for (;;) {
+    int64_t worst = 0, si = 0, s0 = 0;
+    for (int64_t k = 0; k < ncta; ++k) {
+      const int64_t u0 = k * cost / ncta, u1 = (k + 1) * cost / ncta;
+      while (si < (int64_t)seg_cost.size() && s0 + seg_cost[si] <= u0) s0 += seg_cost[si++];
+      int64_t cnt = 0, sj = si, t0 = s0;
+      while (sj < (int64_t)seg_cost.size() && t0 < u1) t0 += seg_cost[sj++], ++cnt;
+      worst = std::max(worst, cnt);
+    }
+    p.worst_segments = static_cast<int>(worst);
+    if (worst <= DECODE_SEGMAX || ncta >= cost || 2 * ncta > 4 * (int64_t)c->num_sms) break;
+    ncta = std::min<int64_t>(cost, 2 * ncta);
+  }
+  p.ncta = static_cast<int>(ncta);
+  p.partial_bytes = align256((size_t)(2 * p.segments + ncta) * decode_record_bytes(c->G()));
   return p;
 }
 
-size_t decode_bytes_needed(const oscar_cache* c, int32_t layer, int32_t n, const int32_t* reqs, int64_t ppc_min) {
+// Requests per decode launch: DECODE_PER_LAUNCH, halved while some CTA of a
+// launch would touch more segments than its table holds (very uneven lengths).
+int32_t decode_launch_size(const oscar_cache* c, int32_t layer, int32_t n, const int32_t* reqs) {
+  int32_t per = std::min<int32_t>(n, DECODE_PER_LAUNCH);
+  while (per > 1) {
+    bool ok = true;
+    for (int32_t b = 0; b < n && ok; b += per)
+      ok = plan_decode(c, layer, std::min<int32_t>(per, n - b), reqs + b, b, nullptr).worst_segments <= DECODE_SEGMAX;
+    if (ok) break;
+    per = (per + 1) / 2;
+  }
+  return per;
+}
+
+// Workspace of a decode of n requests, whatever their lengths: per launch two
+// records per (request, kv head) and one per CTA (at most four per SM).
+size_t decode_bytes_bound(const oscar_cache* c, int32_t n) {
+  const int64_t segs = (int64_t)std::min<int32_t>(n, DECODE_PER_LAUNCH) * c->cfg.num_kv_heads;
+  return align256((size_t)(2 * segs + 4 * (int64_t)c->num_sms) * decode_record_bytes(c->G()));
+}
+
+size_t decode_bytes_needed(const oscar_cache* c, int32_t layer, int32_t n, const int32_t* reqs) {
   size_t need = 0;
-  for (int32_t b = 0; b < n; b += DECODE_PER_LAUNCH) {
-    const int32_t m = std::min<int32_t>(DECODE_PER_LAUNCH, n - b);
-    const DecodePlan p = plan_decode(c, layer, m, reqs + b, b, ppc_min, nullptr);
-    need = std::max(need, p.qrot_bytes + p.partial_bytes);
+  const int32_t per = decode_launch_size(c, layer, n, reqs);
+  for (int32_t b = 0; b < n; b += per) {
+    const int32_t m = std::min<int32_t>(per, n - b);
+    need = std::max(need, plan_decode(c, layer, m, reqs + b, b, nullptr).partial_bytes);
   }
   return need;
 }
@@ -629,14 +666,13 @@ oscar_status oscar_demote_layers(oscar_cache* c, int32_t layer_begin, int32_t la
 oscar_status oscar_decode_workspace_bytes(const oscar_cache* c, int32_t n, const int32_t* reqs, size_t* bytes) {
   if (!c || !bytes) return OSCAR_ERR_INVALID_ARG;
   oscar_cache* mc = const_cast<oscar_cache*>(c);
-  size_t need = 0;
   for (int32_t l = 0; l < c->cfg.num_layers; ++l) {
     const oscar_status st = check_decode_batch(mc, l, n, reqs);
     if (st != OSCAR_OK && st != OSCAR_ERR_STATE) return st;
-    if (st == OSCAR_OK) need = std::max(need, decode_bytes_needed(c, l, n, reqs, 0));
   }
-  // room for every layer to grow by one page before the next query
-  *bytes = need + align256((size_t)n * c->cfg.num_kv_heads * c->G() * PARTIAL_FLOATS * sizeof(float));
+  // the records depend only on the batch and the CTA count, not on the lengths:
+  // this size holds after any number of appends
+  *bytes = decode_bytes_bound(c, n);
   return OSCAR_OK;
 }
 
@@ -648,34 +684,28 @@ oscar_status oscar_decode_attention(oscar_cache* c, int32_t layer, int32_t n, co
   if (c->dry) return OSCAR_ERR_DRY_RUN;
   if (!q || !out || !workspace || !aligned16(q) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
     return c->fail(OSCAR_ERR_INVALID_ARG, "null or misaligned q / out / workspace");
-  int64_t ppc_min = 0;
-  int64_t max_pages = 1;
-  for (int32_t i = 0; i < n; ++i) max_pages = std::max<int64_t>(max_pages, pages_for(c->reqs[reqs[i]].he[layer]));
-  while (decode_bytes_needed(c, layer, n, reqs, ppc_min) > ws_bytes) {
-    if (ppc_min >= max_pages) return c->fail(OSCAR_ERR_INVALID_ARG, "workspace too small");
-    ppc_min = ppc_min ? 2 * ppc_min : 4;
-  }
+  if (decode_bytes_needed(c, layer, n, reqs) > ws_bytes) return c->fail(OSCAR_ERR_INVALID_ARG, "workspace too small");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   DecodeReq dr[DECODE_PER_LAUNCH];
-  for (int32_t b = 0; b < n; b += DECODE_PER_LAUNCH) {
-    const int32_t m = std::min<int32_t>(DECODE_PER_LAUNCH, n - b);
-    const DecodePlan p = plan_decode(c, layer, m, reqs + b, b, ppc_min, dr);
-    const cudaError_t err = launch_decode(c->dc, layer, dr, p, q, out, workspace, c->next_epoch(), s);
+  const int32_t per = decode_launch_size(c, layer, n, reqs);
+  for (int32_t b = 0; b < n; b += per) {
+    const int32_t m = std::min<int32_t>(per, n - b);
+    const DecodePlan p = plan_decode(c, layer, m, reqs + b, b, dr);
+    const cudaError_t err = launch_decode(c->dc, layer, dr, p, q, out, workspace, false, c->dbg, s);
     if (err != cudaSuccess) return c->cuda_fail(err, "decode launch");
   }
   return OSCAR_OK;
 }
 
-// Same decode, with the merge tickets and partials in the library's fixed
-// static scratch (decode_scratch.cu) instead of a caller workspace, for callers
-// that cannot allocate device memory around a step.
+// Same decode, with the partial records in the library's fixed static scratch
+// (decode_scratch.cu) instead of a caller workspace, for callers that cannot
+// allocate device memory around a step.
 oscar_status oscar_decode_attention_noalloc(oscar_cache* c, int32_t layer, int32_t n, const int32_t* reqs,
                                             const uint16_t* q, float* out, void* stream) {
   if (!c) return OSCAR_ERR_INVALID_ARG;
   const oscar_status st = check_decode_batch(c, layer, n, reqs);
   if (st != OSCAR_OK) return st;
-  // the smallest plan: one cluster of chunks per (request, kv head)
-  const size_t need = decode_bytes_needed(c, layer, n, reqs, INT32_MAX);
+  const size_t need = decode_bytes_needed(c, layer, n, reqs);
   if (need > DECODE_SCRATCH_BYTES) {
     char msg[192];
     std::snprintf(msg, sizeof msg,
@@ -700,50 +730,35 @@ oscar_status oscar_decode_step(oscar_cache* c, int32_t layer, int32_t n, const i
     return c->fail(OSCAR_ERR_INVALID_ARG, "null or misaligned q / out / workspace");
   oscar_status st = validate_write(c, layer, n, reqs, k, v, true);
   if (st != OSCAR_OK) return st;
-  // smallest workspace the decode can run in after the append (every request with
-  // history gets one chunk per kv head), checked before anything changes
-  {
-    const int64_t H = c->cfg.num_kv_heads;
-    size_t need = 0;
-    for (int32_t b = 0; b < n; b += APPEND_PER_LAUNCH) {
-      const int32_t m = std::min<int32_t>(APPEND_PER_LAUNCH, n - b);
-      int64_t parts = 0;
-      for (int32_t i = b; i < b + m; ++i) {
-        const Request& r = c->reqs[reqs[i]];
-        const int64_t T = r.T[layer], he = r.he[layer];
-        const int64_t he_after = (T >= SINK && T - he == RECENT) ? he + 1 : he;
-        parts += H * (DECODE_BF16_ITEMS + (pages_for(he_after) > 0 ? 1 : 0));
-      }
-      need = std::max(need, align256((size_t)m * H * decode_qfrag_bytes(c->G())) +
-                                align256((size_t)parts * c->G() * PARTIAL_FLOATS * sizeof(float)));
-    }
-    if (!c->dry && need > ws_bytes) return c->fail(OSCAR_ERR_INVALID_ARG, "workspace too small");
-  }
+  // the decode after the append needs one record per (segment, CTA) and the BF16
+  // records: the same count before and after the append, checked before any change
+  for (int32_t i = 0; i < n; ++i)
+    if (c->reqs[reqs[i]].T[layer] + 1 > INT32_MAX) return c->fail(OSCAR_ERR_INVALID_ARG, "request too long");
+  if (!c->dry && decode_bytes_bound(c, std::min<int32_t>(n, APPEND_PER_LAUNCH)) > ws_bytes)
+    return c->fail(OSCAR_ERR_INVALID_ARG, "workspace too small");
   const std::vector<AppendReq> work = apply_write(c, layer, n, reqs, true);
   if (c->dry) return OSCAR_ERR_DRY_RUN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   DecodeReq dr[DECODE_PER_LAUNCH];
-  for (int32_t b = 0; b < n; b += APPEND_PER_LAUNCH) {
-    const int32_t m = std::min<int32_t>(APPEND_PER_LAUNCH, n - b);
-    int64_t ppc_min = 0, max_pages = 1;
-    for (int32_t i = b; i < b + m; ++i) max_pages = std::max<int64_t>(max_pages, pages_for(c->reqs[reqs[i]].he[layer]));
-    while (decode_bytes_needed(c, layer, m, reqs + b, ppc_min) > ws_bytes && ppc_min < max_pages)
-      ppc_min = ppc_min ? 2 * ppc_min : 4;
-    // each append block of the front kernel (256 threads) displaces two stream blocks
-    // until it ends; leaving their slots out keeps every stream block starting at once
-    // (a large batch's front kernel is over before it matters: no reservation)
-    const int64_t slots = (int64_t)c->num_sms * decode_ctas_per_sm(c->G(), c->cfg.group_size);
-    const int64_t app_blocks = (int64_t)m * c->cfg.num_kv_heads * 2;
-    const int64_t reserve = 2 * app_blocks <= slots / 8 ? 2 * app_blocks : 0;
-    const DecodePlan p = plan_decode(c, layer, m, reqs + b, b, ppc_min, dr, reserve);
+  const int32_t per = std::min<int32_t>(APPEND_PER_LAUNCH, decode_launch_size(c, layer, n, reqs));
+  for (int32_t b = 0; b < n; b += per) {
+    const int32_t m = std::min<int32_t>(per, n - b);
+    const DecodePlan p = plan_decode(c, layer, m, reqs + b, b, dr);
     for (int32_t i = 0; i < m; ++i) {
       const AppendReq& a = work[b + i];
       dr[i].hot_page = a.demote_slot >= 0 ? static_cast<int32_t>((c->reqs[reqs[b + i]].he[layer] - 1 - SINK) / PAGE) : -1;
     }
-    const cudaError_t err = launch_step(c->dc, layer, work.data() + b, m, k, v, dr, p, q, out, workspace,
-                                        c->next_epoch(), s);
+    const cudaError_t err = launch_step(c->dc, layer, work.data() + b, m, k, v, dr, p, q, out, workspace, c->dbg, s);
     if (err != cudaSuccess) return c->cuda_fail(err, "decode step launch");
   }
+  return OSCAR_OK;
+}
+
+oscar_status oscar_debug_decode_hooks(oscar_cache* c, uint32_t wait_limit, int32_t hold_pair) {
+  if (!c) return OSCAR_ERR_INVALID_ARG;
+  if (wait_limit < 1 || hold_pair < -1) return c->fail(OSCAR_ERR_INVALID_ARG, "bad hook values");
+  c->dbg.wait_limit = wait_limit;
+  c->dbg.hold_pair = hold_pair;
   return OSCAR_OK;
 }
 
@@ -759,9 +774,12 @@ oscar_status oscar_cache_check(oscar_cache* c, void* stream) {
   if (word != 0) {
     const int32_t zero = 0;
     cudaMemcpy(c->dc.err, &zero, sizeof(zero), cudaMemcpyHostToDevice);
-    char msg[128];
-    std::snprintf(msg, sizeof msg, "device check failed: error bits 0x%x (1 INT2 page, 2 BF16 page, 4 length)", word);
-    return c->fail(OSCAR_ERR_DEVICE_CHECK, msg);
+    char msg[160];
+    std::snprintf(msg, sizeof msg,
+                  "device check failed: error bits 0x%x (1 INT2 page, 2 BF16 page, 4 length, 8 wait timed out, "
+                  "16 decode plan)",
+                  word);
+    return c->fail((word & ERR_TIMEOUT) ? OSCAR_ERR_TIMEOUT : OSCAR_ERR_DEVICE_CHECK, msg);
   }
   return OSCAR_OK;
 }

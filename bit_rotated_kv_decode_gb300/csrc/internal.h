@@ -41,6 +41,8 @@ constexpr int PARTIAL_L = D + 1;
 constexpr int ERR_INT2_PAGE = 1;
 constexpr int ERR_BF16_PAGE = 2;
 constexpr int ERR_LENGTH = 4;
+constexpr int ERR_TIMEOUT = 8;     // a bounded wait gave up
+constexpr int ERR_PLAN = 16;       // a decode CTA met more segments than it can hold
 
 // Plain pointers into the cache's device memory.
 struct DevCache {
@@ -117,42 +119,54 @@ constexpr int DEMOTE_PER_LAUNCH = 96;   // kernel arguments stay under 4 KiB
 cudaError_t launch_demote_layers(const DevCache& c, const DemoteEntry* e, int n, cudaStream_t s);
 
 // ---- decode ---------------------------------------------------------------------
+// One launch covers up to DECODE_PER_LAUNCH requests.  The work is the list of
+// segments (request i, kv head h), i major; segment s = i Hkv + h is npages INT2
+// history pages (cost 1 each) followed by its BF16 block (the sink page and the
+// four ring pages, DECODE_BF16_HALF_COST per 32-row half-page holding a cached
+// token).  CTA c of ncta takes the cost units [c C / ncta, (c + 1) C / ncta).
 struct DecodeReq {
-  int32_t slot;
+  int32_t slot;            // request slot (page-table row)
   int32_t batch_row;       // row of q / out
   int32_t tokens;          // T
   int32_t hist_end;
   int32_t sink_page;
   int32_t ring_page[RING_PAGES];
-  int32_t int2_start;      // first INT2 work item (block) of this request
-  int32_t chunks;          // INT2 chunks per kv head
-  int32_t part_start;      // first partial slot: per kv head, 5 BF16 items then the chunks
-  int32_t hot_page;        // history page the preceding fused append writes (-1: none)
+  int32_t hot_page;        // history page index a preceding fused append writes (-1: none)
+  int32_t npages;          // INT2 history pages of each kv head
+  int32_t cost_start;      // first cost unit of (this request, kv head 0)
+  int32_t bf16_cost;       // cost units of the BF16 block of each kv head
 };
 constexpr int DECODE_PER_LAUNCH = 64;
-constexpr int DECODE_BF16_ITEMS = 1 + RING_PAGES;   // BF16 work items per (request, kv head)
-int decode_ctas_per_sm(int g, int gk);              // resident stream blocks per SM
-constexpr int MAX_CHUNKS_PER_HEAD = 512;
-// Workspace of one decode launch: the q_rot operands, decode_qfrag_bytes(G) per
-// (request, kv head) in launch order, then the partials fp32 [slot][G][PARTIAL_FLOATS].
-size_t decode_qfrag_bytes(int g);
+constexpr int DECODE_BF16_HALF_COST = 3;
+constexpr int DECODE_BF16_ITEMS = 1 + RING_PAGES;   // BF16 pages per (request, kv head)
 struct DecodePlan {
   int n;
-  int pages_per_chunk;
-  int int2_items;          // INT2 blocks
-  int total_items;         // INT2 blocks + BF16 blocks
-  size_t qrot_bytes;
-  size_t partial_bytes;
+  int ncta;                // persistent CTAs, at most one per SM and at most the total cost
+  int64_t total_cost;
+  int64_t segments;        // n Hkv
+  int worst_segments;      // most segments one CTA touches
+  size_t partial_bytes;    // workspace: INT2 records (segments + ncta) then BF16 records (segments)
 };
-// epoch: unique per launch (never repeated for any workspace the launch could use)
+// Partial record of one (segment, CTA) or one segment's BF16 block: per query head
+// of the group o[128], m (log2 domain), l.
+inline size_t decode_record_bytes(int g) { return (size_t)g * PARTIAL_FLOATS * sizeof(float); }
+// Failure-detection hooks of a launch: mbarrier wait rounds before a wait gives up
+// (ERR_TIMEOUT), and a page pair whose copy CTA 0's first warpgroup never issues
+// (-1: none), so that a test can make a wait run out.
+struct DecodeDebug {
+  uint32_t wait_limit;
+  int32_t hold_pair;
+};
+constexpr uint32_t DECODE_WAIT_LIMIT = 100000;   // rounds of up to 10 us each
 cudaError_t launch_decode(const DevCache& c, int layer, const DecodeReq* reqs, const DecodePlan& plan,
-                          const uint16_t* q, float* out, void* workspace, uint64_t epoch, cudaStream_t s);
-// Fused step of up to APPEND_PER_LAUNCH requests: one kernel runs the append of
-// every request and the q rotation, then the decode's stream and merge kernels;
-// reqs[i].hot_page names the history page the append writes.
+                          const uint16_t* q, float* out, void* workspace, bool front_writes, DecodeDebug dbg,
+                          cudaStream_t s);
+// Fused step: the append of every request (demoting into reqs[i].hot_page), then
+// the decode, which copies every page the append does not write while the append
+// still runs.
 cudaError_t launch_step(const DevCache& c, int layer, const AppendReq* app, int n_app, const uint16_t* k,
                         const uint16_t* v, const DecodeReq* reqs, const DecodePlan& plan, const uint16_t* q,
-                        float* out, void* workspace, uint64_t epoch, cudaStream_t s);
+                        float* out, void* workspace, DecodeDebug dbg, cudaStream_t s);
 
 // Fixed decode scratch (one static device array per device) for callers that
 // cannot allocate.  The first call on a device, with that device current,

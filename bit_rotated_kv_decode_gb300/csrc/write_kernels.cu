@@ -127,7 +127,8 @@ struct PrefillSmem {
   __align__(16) uint16_t kb[2][PF_TILE][PF_PITCH];  // the tile as bf16, double-buffered (zero rows past its end)
   __align__(16) float xs[PF_TILE][D + 4];       // rotated values (row pad: no bank conflicts)
   float kn[PF_TILE];                            // |k|^2 of each token, rounded up
-  int32_t pages[2];                             // ids of the (at most two) history pages of the tile
+  __align__(16) uint8_t vb[PF_TILE][CODE_BYTES];  // V: the tile's packed codes (token j, lane l's byte)
+  int32_t page;                                 // id of the history page holding the tile
 };
 constexpr size_t PREFILL_SMEM = sizeof(PrefillSmem);
 
@@ -168,15 +169,17 @@ __device__ __forceinline__ uint16_t bf16_rn_bits(float x) {
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 
 // Block x of the history of one kv head (y), K or V (z): tiles
-// [x tiles_per_cta, (x + 1) tiles_per_cta) of PF_TILE positions each; the launch
-// sizes the grid to two resident blocks per SM, so R is split and staged once
-// per block.
+// [x tiles_per_cta, (x + 1) tiles_per_cta) of the launch.  Tile i covers history
+// slots [PF_TILE (k0 + i), PF_TILE (k0 + i + 1)) -- aligned to PF_TILE, so a tile
+// lies in one page and no two tiles share a byte of channel-major V codes --
+// restricted to the positions [h0, h1) being written.  The launch sizes the grid
+// to two resident blocks per SM, so R is split and staged once per block.
 template <int GK>
 __global__ void __launch_bounds__(PF_THREADS, 2) prefill_hist_kernel(DevCache c, int layer, int slot,
                                                                   const uint16_t* __restrict__ k,
                                                                   const uint16_t* __restrict__ v,
                                                                   int64_t in_base, int64_t h0, int64_t h1,
-                                                                  int tiles_per_cta) {
+                                                                  int64_t k0, int64_t tiles, int tiles_per_cta) {
   extern __shared__ __align__(16) uint8_t pf_raw[];
   PrefillSmem& sm = *reinterpret_cast<PrefillSmem*>(pf_raw);
   const int head = blockIdx.y;
@@ -224,17 +227,18 @@ __global__ void __launch_bounds__(PF_THREADS, 2) prefill_hist_kernel(DevCache c,
   const int mrow = 16 * (warp & 1);
   const int ncol = 32 * (warp >> 1);
   const int64_t tile_begin = (int64_t)blockIdx.x * tiles_per_cta;
-  const int64_t tile_end = min((h1 - h0 + PF_TILE - 1) / PF_TILE, tile_begin + tiles_per_cta);
+  const int64_t tile_end = min(tiles, tile_begin + tiles_per_cta);
   // a tile is PF_TILE tokens x 128 channels of bf16, 16 bytes per copy; the next
-  // tile is copied while the current one is rotated and quantised
+  // tile is copied while the current one is rotated and quantised.  Row j of tile
+  // i is position t0 + j, t0 = SINK + PF_TILE (k0 + i); rows outside [h0, h1) are
+  // zero-filled and skipped
   constexpr int CHUNKS = PF_TILE * D / 8 / PF_THREADS;
   auto copy_tile = [&](int64_t tile, int buf) {
-    const int64_t t0 = h0 + tile * PF_TILE;
-    const int ntok = static_cast<int>(h1 - t0 < PF_TILE ? h1 - t0 : PF_TILE);
+    const int64_t t0 = SINK + PF_TILE * (k0 + tile);
 #pragma unroll
     for (int u = 0; u < CHUNKS; ++u) {
       const int idx = u * PF_THREADS + t, j = idx / (D / 8), part = idx % (D / 8);
-      const bool ok = j < ntok;
+      const bool ok = t0 + j >= h0 && t0 + j < h1;
       const uint16_t* g = src + ((size_t)(ok ? t0 + j - in_base : 0) * c.Hkv + head) * D + 8 * part;
       cp_async16(&sm.kb[buf][j][8 * part], g, ok);
     }
@@ -243,16 +247,13 @@ __global__ void __launch_bounds__(PF_THREADS, 2) prefill_hist_kernel(DevCache c,
   if (tile_begin < tile_end) copy_tile(tile_begin, 0);
   for (int64_t tile = tile_begin; tile < tile_end; ++tile) {
     const int buf = static_cast<int>((tile - tile_begin) & 1);
-    const int64_t t0 = h0 + tile * PF_TILE;
-    const int ntok = static_cast<int>(h1 - t0 < PF_TILE ? h1 - t0 : PF_TILE);
+    const int64_t t0 = SINK + PF_TILE * (k0 + tile);
+    const int jlo = static_cast<int>(h0 - t0 > 0 ? h0 - t0 : 0);
+    const int jhi = static_cast<int>(h1 - t0 < PF_TILE ? h1 - t0 : PF_TILE);
     cp_async_wait_all();
-    __syncthreads();   // this tile has landed; the other buffer and xs are free
+    __syncthreads();   // this tile has landed; the other buffer, xs and vb are free
     if (tile + 1 < tile_end) copy_tile(tile + 1, buf ^ 1);
-    if (t < 2) {
-      // the tile's page ids, loaded now and read after the rotation
-      const int64_t p = (t0 - SINK) / PAGE + t;
-      sm.pages[t] = p <= (t0 + ntok - 1 - SINK) / PAGE ? __ldg(pt + p) : -1;
-    }
+    if (t == 0) sm.page = __ldg(pt + (t0 - SINK) / PAGE);   // read after the rotation
     {
       // |k|^2 of each token, rounded up: 16 consecutive threads share a token
 #pragma unroll
@@ -310,7 +311,7 @@ __global__ void __launch_bounds__(PF_THREADS, 2) prefill_hist_kernel(DevCache c,
     }
     __syncthreads();
 
-    for (int j = warp; j < ntok; j += PF_THREADS / 32) {
+    for (int j = jlo + warp; j < jhi; j += PF_THREADS / 32) {
       const float4 x = *reinterpret_cast<const float4*>(&sm.xs[j][4 * lane]);
       const uint2 kw = *reinterpret_cast<const uint2*>(&sm.kb[buf][j][4 * lane]);
       const float4 k4 = make_float4(__uint_as_float(kw.x << 16), __uint_as_float(kw.x & 0xffff0000u),
@@ -319,15 +320,43 @@ __global__ void __launch_bounds__(PF_THREADS, 2) prefill_hist_kernel(DevCache c,
       const float err = __fmul_ru(sbound, PF_MMA_ERR);
       const GroupCode g = quantize_group_warp<GK>(x, make_float4(err, err, err, err),
                                                   make_float4(sbound, sbound, sbound, sbound), tau, k4, Rt);
-      const int64_t h = t0 + j - SINK;
-      const int32_t page = sm.pages[h / PAGE - (t0 - SINK) / PAGE];
-      const int row = static_cast<int>(h % PAGE);
+      const int row = static_cast<int>((t0 + j - SINK) % PAGE);
+      const int32_t page = sm.page;
       if (page < 0 || page >= c.n_int2_pages) {
         if (lane == 0) atomicOr(c.err, ERR_INT2_PAGE);
         continue;
       }
-      store_group_code_t<GK>(c.int2 + layer * c.int2_layer_stride + ((size_t)page * c.Hkv + head) * record_for(GK),
-                             which, row, g);
+      uint8_t* rec = c.int2 + layer * c.int2_layer_stride + ((size_t)page * c.Hkv + head) * record_for(GK);
+      if (which)
+        sm.vb[j][lane] = static_cast<uint8_t>(g.byte);
+      else
+        rec[K_CODES_OFF + row * CODE_BYTES + lane] = static_cast<uint8_t>(g.byte);
+      store_group_meta<GK>(rec, which, row, g);
+    }
+    if (which) {
+      // channel-major V codes of the tile: thread t -> channel t / 2, slots
+      // 16 (t % 2) .. + 15 of the tile (one word); words the tile covers only in
+      // part keep the other slots' codes
+      __syncthreads();
+      const int32_t page = sm.page;
+      if (page >= 0 && page < c.n_int2_pages) {
+        const int ch = t >> 1, q = t & 1;
+        uint32_t word = 0u, mask = 0u;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int j = 16 * q + i;
+          if (j >= jlo && j < jhi) {
+            word |= ((static_cast<uint32_t>(sm.vb[j][ch >> 2]) >> (2 * (ch & 3))) & 3u) << (2 * i);
+            mask |= 3u << (2 * i);
+          }
+        }
+        if (mask != 0u) {
+          uint8_t* rec = c.int2 + layer * c.int2_layer_stride + ((size_t)page * c.Hkv + head) * record_for(GK);
+          const int slot0 = static_cast<int>((t0 - SINK) % PAGE) + 16 * q;   // a multiple of 16
+          uint32_t* p = reinterpret_cast<uint32_t*>(rec + V_CODES_OFF) + 4 * ch + (slot0 >> 4);
+          *p = mask == 0xffffffffu ? word : ((*p & ~mask) | word);
+        }
+      }
     }
   }
 }
@@ -411,17 +440,19 @@ cudaError_t launch_prefill_hist(const DevCache& c, int layer, int slot, const ui
   int sms = 0;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  // two resident blocks per SM over the 2 Hkv (kv head, K or V) matrices
-  const int64_t tiles = (h1 - h0 + PF_TILE - 1) / PF_TILE;
+  // tiles aligned to PF_TILE history slots; two resident blocks per SM over the
+  // 2 Hkv (kv head, K or V) matrices
+  const int64_t k0 = (h0 - SINK) / PF_TILE;
+  const int64_t tiles = (h1 - SINK + PF_TILE - 1) / PF_TILE - k0;
   const int64_t per_matrix = std::max<int64_t>(1, std::min<int64_t>(tiles, (2 * (int64_t)sms) / (2 * c.Hkv)));
   const int64_t tiles_per_cta = (tiles + per_matrix - 1) / per_matrix;
   dim3 grid(static_cast<unsigned>((tiles + tiles_per_cta - 1) / tiles_per_cta), c.Hkv, 2);
   if (c.gk == 64)
-    prefill_hist_kernel<64><<<grid, PF_THREADS, PREFILL_SMEM, s>>>(c, layer, slot, k, v, in_base, h0, h1,
-                                                                   static_cast<int>(tiles_per_cta));
+    prefill_hist_kernel<64><<<grid, PF_THREADS, PREFILL_SMEM, s>>>(c, layer, slot, k, v, in_base, h0, h1, k0,
+                                                                   tiles, static_cast<int>(tiles_per_cta));
   else
-    prefill_hist_kernel<128><<<grid, PF_THREADS, PREFILL_SMEM, s>>>(c, layer, slot, k, v, in_base, h0, h1,
-                                                                    static_cast<int>(tiles_per_cta));
+    prefill_hist_kernel<128><<<grid, PF_THREADS, PREFILL_SMEM, s>>>(c, layer, slot, k, v, in_base, h0, h1, k0,
+                                                                    tiles, static_cast<int>(tiles_per_cta));
   return cudaGetLastError();
 }
 

@@ -220,18 +220,20 @@ oscar_status oscar_decode_attention(oscar_cache* cache, int32_t layer, int32_t n
  * nothing.  The pages have no counterpart to this call; it exists for callers
  * that cannot allocate device memory around a decode step (a serving engine
  * that gives all free HBM to its KV pools at start-up and owns no per-step
- * allocator, or a plain C host with no allocator to pass).  The merge tickets
- * and partials live in one fixed static device array of 8 MiB per device
- * inside the library.
+ * allocator, or a plain C host with no allocator to pass).  The decode's
+ * scratch (its partial records) lives in one fixed static device array
+ * of 8 MiB per device inside the library.
  *   Arguments, layouts and results are those of oscar_decode_attention.
- *   Size limit: a batch whose smallest plan (one cluster of four INT2 chunks
- *     per request and kv head, per launch of up to 64 requests) needs more
- *     than 8 MiB is rejected with OSCAR_ERR_INVALID_ARG before any work; use
- *     oscar_decode_attention with a caller workspace for it.
- *   Set-up: the first call on each device, made with that device current,
- *     takes the array's address and zeroes it on "stream" (an error there is
- *     OSCAR_ERR_CUDA).  Make that first call before capturing any stream.
- *     No part of the array needs particular contents when a call starts.
+ *   Size limit: a batch whose partial records (per launch of up to 64
+ *     requests: two per request and kv head plus one per SM, G x 528 bytes
+ *     each) need more than 8 MiB is rejected with OSCAR_ERR_INVALID_ARG before
+ *     any work; use oscar_decode_attention with a caller workspace for it.
+ *   Set-up: every call takes the array's address on the current device
+ *     (cudaGetSymbolAddress, so a module reloaded after a device reset is
+ *     found afresh); the first call on each device also zeroes it on "stream"
+ *     (an error there is OSCAR_ERR_CUDA).  Make that first call before
+ *     capturing any stream.  No part of the array needs particular contents
+ *     when a call starts.
  *   Overlap: the array is shared by every cache on the device; two calls
  *     that overlap on the GPU (other streams, other caches) race. */
 oscar_status oscar_decode_attention_noalloc(oscar_cache* cache, int32_t layer, int32_t n, const int32_t* reqs,
@@ -252,6 +254,16 @@ oscar_status oscar_decode_attention_noalloc(oscar_cache* cache, int32_t layer, i
 oscar_status oscar_decode_step(oscar_cache* cache, int32_t layer, int32_t n, const int32_t* reqs,
                                const uint16_t* k, const uint16_t* v, const uint16_t* q, float* out,
                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* Failure-detection hooks of the decode launches of this cache (test use; the
+ * pages have no counterpart).  wait_limit: rounds (up to 10 us each) a bounded
+ * device wait makes before it gives up and reports OSCAR_ERR_TIMEOUT through
+ * oscar_cache_check (default 100000, must be >= 1).  hold_pair: the page pair
+ * (in issue order) of CTA 0's first warpgroup whose copy is never issued, so that
+ * its wait runs out (-1, the default, holds none).  The kernel then drains its
+ * copies in flight, frees its tensor memory and returns; that launch's output is
+ * undefined.  OSCAR_ERR_INVALID_ARG for values out of range. */
+oscar_status oscar_debug_decode_hooks(oscar_cache* cache, uint32_t wait_limit, int32_t hold_pair);
 
 /* Synchronise "stream" and report the sticky device error word (then clear it). */
 oscar_status oscar_cache_check(oscar_cache* cache, void* stream);

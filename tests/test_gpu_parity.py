@@ -124,13 +124,10 @@ class Setup:
             rows = (pos - 64) % 64
             for h in range(self.hkv):
                 rec = pool[pages, h]
-                lay = layout.record_layout(self.group)
-                mb = lay["meta_bytes"]
+                fields = [layout.record_slot_fields(rec[i], int(rows[i]), self.group) for i in range(nh)]
                 for which, src, rr, tau in ((0, kf, self.rk, self.tk), (1, vf, self.rv, self.tv)):
-                    off_c = lay["v_codes"] if which else lay["k_codes"]
-                    off_m = lay["v_meta"] if which else lay["k_meta"]
-                    codes = np.stack([rec[i, off_c + 32 * rows[i]: off_c + 32 * rows[i] + 32] for i in range(nh)])
-                    meta = np.stack([rec[i, off_m + mb * rows[i]: off_m + mb * rows[i] + mb] for i in range(nh)])
+                    codes = np.stack([f[1 if which else 0] for f in fields])
+                    meta = np.stack([f[3 if which else 2] for f in fields])
                     from oracle import quant
                     x32 = quant.rotate_to_fp32(src[64:he, h], rr[layer, h].astype(np.float64))
                     st = parity.compare_groups(codes, meta, x32, tau[layer, h], self.group)
@@ -184,8 +181,7 @@ def test_prefill_equals_sequential_appends(b):
     assert pt == s2.cache.pages(r2)[0]
     for i, p in enumerate(pt):
         rows = min(64, 444 - 64 - 64 * i)
-        for off, width in ((0, 32), (2048, 32), (4096, 4), (4352, 4)):
-            assert torch.equal(a[p, :, off:off + rows * width], bb[p, :, off:off + rows * width])
+        assert np.array_equal(parity.slot_bytes(a[p].numpy(), rows), parity.slot_bytes(bb[p].numpy(), rows))
     s2.check_pages(r2, 0)
 
 
