@@ -35,31 +35,12 @@ __device__ __forceinline__ void store_group_meta(uint8_t* rec, int which, int sl
   }
 }
 
-// The V codes of one token slot, channel-major: channel c's 16 bytes (4 words)
-// start at V_CODES_OFF + 16 c, and slot r sits in bits 2 (r % 16) of word r / 16.
-// Lane l holds channels 4 l .. 4 l + 3 (code i in bits 2 i of `byte`).  Each field
-// is a read-modify-write of its word: only one token of a page is written per
-// launch on this path, so no other thread touches these words meanwhile.
-__device__ __forceinline__ void store_v_codes_rmw(uint8_t* rec, int slot, uint32_t byte) {
-  const int lane = threadIdx.x & 31;
-  uint32_t* w = reinterpret_cast<uint32_t*>(rec + V_CODES_OFF) + (slot >> 4);
-  const int sh = 2 * (slot & 15);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t* p = w + 4 * (4 * lane + i);
-    *p = (*p & ~(3u << sh)) | (((byte >> (2 * i)) & 3u) << sh);
-  }
-}
-
-// The lane's group code of one token into a record: K codes token-major (32 bytes
-// at slot * 32, lane l's byte at l), V codes channel-major, then {s, z}.
+// The lane's group code of one token into a record: 32 code bytes at slot * 32 of
+// the K or V code region (lane l's byte at l), then {s, z}.
 template <int GK>
 __device__ __forceinline__ void store_group_code_t(uint8_t* rec, int which, int slot, const GroupCode& g) {
   const int lane = threadIdx.x & 31;
-  if (which)
-    store_v_codes_rmw(rec, slot, g.byte);
-  else
-    rec[K_CODES_OFF + slot * CODE_BYTES + lane] = static_cast<uint8_t>(g.byte);
+  rec[(which ? V_CODES_OFF : K_CODES_OFF) + slot * CODE_BYTES + lane] = static_cast<uint8_t>(g.byte);
   store_group_meta<GK>(rec, which, slot, g);
 }
 

@@ -1,4 +1,4 @@
-// Three-segment decode attention on the fifth-generation tensor cores.
+// Three-segment decode attention.
 //
 // "TogetherAI开源OSCAR" (ModelScope), section "OSCAR的设计": at decode time the
 // INT2 history is unpacked, dequantised with its scale / zero point and
@@ -7,39 +7,45 @@
 // "Together AI Open-Sources OSCAR" (MarkTechPost), section "The Serving
 // System": the value path is inverse-rotated.
 //
-// Two launches per layer (and per 64 requests), chained with programmatic
-// dependent launch:
+// Two launches per layer (and per launch batch of requests), chained with
+// programmatic dependent launch:
 //   1. decode   one persistent CTA per SM.  The work -- every INT2 history page
-//               and every BF16 half-page of every (request, kv head) segment --
-//               is cut into equal-cost contiguous ranges, one per CTA.  A CTA
-//               rotates q itself (q_rot = q R_K, in its prologue, while the first
-//               page copies are in flight), then its warpgroups stream page pairs
-//               (128 tokens) through per-warpgroup TMA rings and write one partial
-//               (o, m, l) per segment it touched, INT2 part in the rotated basis;
-//   2. merge    one CTA per segment: online-softmax merge of the partials,
-//               R_V^T applied to the INT2 part (staged in shared memory while the
-//               decode grid still runs), out = (O_bf16 + O_hist R_V^T) / L.
-//
-// The INT2 contractions of a page pair run as tcgen05.mma (kind::f16, M = 128,
-// fp32 accumulators in tensor memory, issued by one thread per warpgroup):
-//   logits   D_K[token][col] = sum_k A_K[token][k] Bq[k][col]
-//            A_K: the pair's 128 tokens x 128 K codes, in tensor memory;
-//            Bq:  q_rot split into fp16 hi + lo columns, in shared memory;
-//   values   D_V[chan][col] += sum_k A_V[chan][k] Bw[k][col]
-//            A_V: 128 channels x the pair's 128 V codes, in tensor memory;
-//            Bw:  the softmax weights p s_v (fp16 hi + lo), in shared memory.
-// A 2-bit code masked out of a packed word, with every other bit zero, is the
-// fp16 subnormal code 2^(2e - 24) (e = 0..4 by its bit position): one LOP3 gives
-// two codes, and the factor 2^(8 - 2e) of the row goes into the B operand, so
-// every product is code * b 2^-16 exactly in fp32.  Each thread unpacks one row
-// of A_K (its token: K codes are stored token-major) and one row of A_V (its
-// channel: V codes are stored channel-major) and stores it with tcgen05.st.
-// For a token j with K codes c_j and fp16 (s_j, z_j) per quantisation group:
-//   logit_j = scale (s_j (q_rot . c_j) + z_j sum(q_rot))   (per group),
-//   value_j = s_j c_j + z_j                                 (p s_j c_j, plus sum p z_j).
-// Every wait is bounded and reports ERR_TIMEOUT instead of hanging.
+//               and the BF16 pages of every (request, kv head) segment -- is cut
+//               into equal-cost contiguous ranges, one per CTA.  A CTA rotates q
+//               itself (q_rot = q R_K, into tensor-core operands in shared
+//               memory) while the first page copies are in flight; then each warp
+//               streams its share of the CTA's pages of a segment through its own
+//               TMA ring, and at the end of the segment the warps' partials are
+//               combined into one record (o, m, l; rotated basis).  The CTA that
+//               holds a segment's BF16 pages attends to them last, with the
+//               unrotated q, one record per page;
+//   2. merge    one CTA per (request, query head): online-softmax merge of the
+//               segment's records, R_V^T applied to the INT2 part (staged in
+//               shared memory while the decode grid still runs),
+//               out = (O_bf16 + O_hist R_V^T) / L.
+// For an INT2 token j with codes c_j and fp16 scale / zero (s_j, z_j):
+//   logit_j = scale * (s_j (q_rot . c_j) + z_j sum(q_rot)),
+//   value   = s_j c_j + z_j 1   (accumulated as p_j s_j c_j plus sum p_j z_j).
+// The two contractions over a 64-token page -- q_rot . c (64 tokens x G heads x
+// 128 channels) and sum_j (p_j s_j) c_j (128 channels x G heads x 64 tokens) --
+// run on the tensor cores as warp-level mma.sync m16n8k16 (fp16 operands, fp32
+// accumulate).  These are skinny products (the N side is G heads x two parts),
+// which the warp-level MMA of every sub-partition serves at a lower cost per
+// page than the single-thread-issued tcgen05 MMA, whose per-instruction cost does
+// not shrink with N:
+//   * a 2-bit field masked out of a packed byte word, with every other bit
+//     zero, is the fp16 subnormal code * 2^(2e-24) -- exact, one LOP3 per two
+//     codes; the factor 4^e of its bit position is folded into the other operand;
+//   * q_rot and p s are split into fp16 hi + lo parts (22 significant bits),
+//     occupying the N columns as (head, part) pairs;
+//   * every product is exact in fp32; accumulation is fp32.
+// Pages are staged HBM -> shared memory by TMA bulk copies (cp.async.bulk, one
+// record per page and kv head) into a per-warp ring, completion on mbarriers;
+// every wait is bounded and reports ERR_TIMEOUT instead of hanging.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+
+#include <type_traits>
 
 #include "internal.h"
 
@@ -48,37 +54,29 @@ namespace {
 
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr int PART = PARTIAL_FLOATS;
-constexpr int WGT = 128;           // threads per warpgroup
-constexpr int STAGES = 4;          // page-pair stages of a warpgroup's ring
-constexpr int SEG_PRE = 2;         // segments whose q operands the prologue builds
-constexpr int SEGMAX = 16;         // segments one CTA may touch
-constexpr float LAZY_MAX = 8.0f;   // softmax reference max kept within 2^8 of the true one
-constexpr uint32_t SUSPEND_NS = 10000;
-constexpr int MERGE_THREADS = 256;
+constexpr int STAGES = 2;                // TMA ring depth per warp
+constexpr int SEGMAX = 16;               // segments one CTA may touch
+constexpr uint32_t SUSPEND_NS = 20000;   // a waiting warp sleeps until the phase completes
+constexpr int LAZY_MAX_INT = 8;          // softmax reference max kept within 2^8 of the true one
+constexpr float LAZY_MAX = static_cast<float>(LAZY_MAX_INT);
+constexpr int SLABS = D / 32;
+constexpr int MERGE_THREADS = 512;
+constexpr int BF16_ITEMS = DECODE_BF16_ITEMS;
 
+// Warps per CTA: all sixteen when a warp fits in 128 registers, fewer where the
+// second n-tile (G = 8) or the second quantisation group (G_K = 64) take more
+// registers and shared memory.
 template <int G, int GK>
-struct Cfg {
-  static constexpr int NG = D / GK;                     // quantisation groups per token-head
-  static constexpr int NC = 2 * G * NG;                 // used columns: (group, head, hi | lo)
-  static constexpr int N = NC <= 16 ? 16 : 32;          // MMA N
-  static constexpr int NWG = N == 16 ? 3 : 2;           // warpgroups per CTA (tensor-memory budget)
-  static constexpr int THREADS = NWG * WGT;
-  static constexpr int REC = record_for(GK);
-  static constexpr int STAGE = 2 * REC;
-  static constexpr int BT = D * N * 2;                  // bytes of a 128-row B tile
-  static constexpr int TW = 128 + 2 * N;                // tensor-memory columns per warpgroup
-  static constexpr int KMETA = k_meta_off_for(GK), VMETA = v_meta_off_for(GK), MB = meta_bytes_for(GK);
-  static_assert(NWG * TW <= 512, "tensor memory");
+struct Tune {
+  static constexpr int NW = (G <= 4 && GK == 128) ? 16 : ((G == 8 && GK == 64) ? 8 : 12);
+  static constexpr int THREADS = 32 * NW;
 };
-
-__host__ __device__ constexpr int code_exp(int m) { return m <= 4 ? m : m - 5; }
-__device__ __forceinline__ int col_of(int g, int h, int part, int G) { return 2 * G * g + 2 * h + part; }
 
 struct Seg {
   int ri, head;    // request index in the launch, kv head
   int p0, p1;      // INT2 pages [p0, p1) of this CTA
-  int bf16;        // the segment's BF16 block belongs to this CTA
-  int slot;        // INT2 partial record: segment + CTA
+  int bf16;        // the segment's BF16 pages belong to this CTA
+  int slot;        // INT2 record: segment + CTA
 };
 
 struct DecodeArgs {
@@ -88,42 +86,17 @@ struct DecodeArgs {
   DecodeReq r[DECODE_PER_LAUNCH];
 };
 
-template <int G, int GK>
-struct Smem {
-  using C = Cfg<G, GK>;
-  __align__(128) uint8_t ring[C::NWG][STAGES][C::STAGE];
-  __align__(128) uint8_t bw[C::NWG][C::BT];       // value-side B tiles (BF16 phase: q and logits)
-  __align__(128) uint8_t bq[SEG_PRE][C::BT];      // logit-side B tiles of the first segments
-  union {
-    struct {                                      // prologue: q and the row-part sums of q R_K
-      float q[G][D];
-      float part[C::NWG][G][D];
-      float amax[G];
-    } pro;
-    struct {                                      // end of a segment: one partial per warpgroup
-      float o[C::NWG][G][D];
-      float ml[C::NWG][G][2];
-    } fl;
-  } u;
-  float qc[SEG_PRE][G][1 + C::NG];                // per segment and head: ks, kz[group]
-  int ew[SEG_PRE];                                // value prescale exponent of the segment's head
-  float wmax[C::NWG][4][G];
-  float red[C::NWG][4][G * (1 + C::NG)];
-  int flag[C::NWG][2];
-  __align__(8) uint64_t full[C::NWG][STAGES];
-  __align__(8) uint64_t mk[C::NWG], mv[C::NWG];
-  uint32_t tmem;
-  int abort;
-  int nseg;
-  Seg seg[SEGMAX];
-};
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// ---- PTX helpers ---------------------------------------------------------------------
+// Programmatic dependent launch: wait for the preceding grid (complete, its
+// writes visible); allow the next grid to be scheduled.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
@@ -131,6 +104,7 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
 }
+// 1-D TMA bulk copy global -> shared; completion counted on bar.
 __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -155,134 +129,767 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
 __device__ __forceinline__ void bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-          taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
-template <int NR>
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&f)[NR]);
-template <>
-__device__ __forceinline__ void tmem_ld<8>(uint32_t taddr, float (&f)[8]) {
-  uint32_t r[8];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr)
-               : "memory");
-#pragma unroll
-  for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(r[i]);
-}
-template <>
-__device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, float (&f)[16]) {
-  float a[8], b[8];
-  tmem_ld<8>(taddr, a);
-  tmem_ld<8>(taddr + 8, b);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    f[i] = a[i];
-    f[8 + i] = b[i];
-  }
-}
-template <>
-__device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, float (&f)[32]) {
-  float a[16], b[16];
-  tmem_ld<16>(taddr, a);
-  tmem_ld<16>(taddr + 16, b);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    f[i] = a[i];
-    f[16 + i] = b[i];
-  }
-}
-template <int NR>
-__device__ __forceinline__ void tmem_st_f(uint32_t taddr, const float (&f)[NR]) {
-#pragma unroll
-  for (int c0 = 0; c0 < NR; c0 += 8) {
-    uint32_t r[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) r[i] = __float_as_uint(f[c0 + i]);
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr + c0),
-                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-                 : "memory");
-  }
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Shared-memory matrix descriptor of a B tile: 16-bit elements, N-major without
-// swizzle, core matrices of 8 k-rows x 16 bytes; LBO = 128 (next 8 k-rows),
-// SBO = 2048 (next 8 columns).
-__device__ __forceinline__ uint64_t b_desc(uint32_t saddr) {
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(2048 >> 4) << 32) |
-         ((uint64_t)1 << 46);
+// Pair of 2-bit codes m of each 16-bit half of w (m = 0..7) as an fp16x2 of
+// subnormals code * 2^(2 e(m) - 24), e(m) = m for m <= 4, m - 5 otherwise; the
+// caller supplies ws = w >> 10, so one shift serves three codes.
+__host__ __device__ constexpr int code_exp(int m) { return m <= 4 ? m : m - 5; }
+__device__ __forceinline__ uint32_t code_pair2(uint32_t w, uint32_t ws, int m) {
+  return m <= 4 ? (w & (0x00030003u << (2 * m))) : (ws & (0x00030003u << (2 * (m - 5))));
 }
-// Instruction descriptor: kind::f16, fp16 A and B, fp32 D, A K-major, B N-major, M = 128.
-template <int N>
-__device__ __forceinline__ constexpr uint32_t idesc_f16() {
-  return (1u << 4) | (1u << 16) | ((uint32_t)(N >> 3) << 17) | ((128u >> 4) << 24);
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
-__device__ __forceinline__ void umma(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(
-          d),
-      "r"(a), "l"(bdesc), "r"(idesc), "r"(acc)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
+
+// fp16 hi / lo split of x: hi = fp16_rn(x), lo = fp16_rn(x - hi).
+__device__ __forceinline__ void split_half(float x, float& hi, float& lo) {
+  hi = __half2float(__float2half_rn(x));
+  lo = x - hi;
 }
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-__device__ __forceinline__ float warp_max(float x) {
-  float y;
-  asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
-}
-__device__ __forceinline__ uint32_t h2_bits(__half lo, __half hi) {
-  return static_cast<uint32_t>(__half_as_ushort(lo)) | (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
-}
 
-// The 16 codes of a packed word as eight fp16x2 subnormal pairs: register m holds
-// the codes at bit position m of the low and the high half, code 2^(2 e(m) - 24).
-__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t* r) {
-  const uint32_t ws = w >> 10;
-  r[0] = w & 0x00030003u;
-  r[1] = w & 0x000C000Cu;
-  r[2] = w & 0x00300030u;
-  r[3] = w & 0x00C000C0u;
-  r[4] = w & 0x03000300u;
-  r[5] = ws & 0x00030003u;
-  r[6] = ws & 0x000C000Cu;
-  r[7] = ws & 0x00300030u;
-}
-// Eight packed words -> 64 tensor-memory columns of one row (column 8 w + m).
-__device__ __forceinline__ void store_row(uint32_t taddr, const uint32_t (&w)[8]) {
+// ---- q operands ----------------------------------------------------------------------
+// Per segment the CTA holds QFrag<G>::WORDS 32-bit words in shared memory:
+//   frag[lane][nt][s][r]  fp16x2 B operands of the q_rot . c contraction
+//                         (n-tile nt of (head, hi / lo part) columns, k-step s,
+//                         register r), prescaled by qscale(h) 2^(24 - 2 e(m)) so
+//                         that the fp32 accumulator holds qscale(h) q_rot . c;
+//   kscale[8]             fp32 per query head h: scale log2(e) / qscale(h);
+//   qsum[4][8]            fp32 per 32-channel slab and head: sum of q_rot.
+// The logit in the log2 domain is
+//   kscale[h] s_k acc + (scale log2(e) sum_slab qsum[slab][h]) z_k.
+// Register r of k-step s for lane (gid, tid) pairs channel 32 tid + 16 (s >> 2) + m
+// (low half) with that channel + 8 (high half), m = 2 (s & 3) + r, as the code
+// registers of the A operand do.  With G_K = 64 the k-steps are group-pure instead:
+// channel 64 (s >> 2) + 16 tid + m (and + 8), so k-steps 0..3 hold group 0 and
+// 4..7 group 1.  qscale(h) = 2^e with |q_rot| 2^(e + 24) <= 2^15 taken from
+// |q|_2 >= max |q_rot| (R_K is orthogonal).
+template <int G>
+struct QFrag {
+  static constexpr int NT = (G + 3) / 4;
+  static constexpr int REGS = NT * 16;              // fragment registers per lane
+  static constexpr int CONSTS = 32 * REGS;          // word offset of kscale[8], qsum[4][8]
+  static constexpr int WORDS = CONSTS + 40;
+};
+
+constexpr int WH_STRIDE = PAGE + 8;   // halves per weight row (bank spread)
+// Softmax weights of the page being processed, fp16 [G x groups][hi, lo][WH_STRIDE]
+// per warp (row (D / GK) h + g: head h, quantisation group g).  When they fit (up
+// to four heads with one group, two with two) they live in the page's K-code
+// region, dead once the logits are formed; otherwise in rows of their own.
+template <int G, int GK = 128>
+constexpr bool kWeightsInRing = G * (D / GK) * 2 * WH_STRIDE * 2 <= PAGE * CODE_BYTES;
+template <int G, int GK, int NW, bool InRing = kWeightsInRing<G, GK>>
+struct WeightRows {
+  __align__(16) uint16_t wh[NW][G * (D / GK)][2][WH_STRIDE];
+};
+template <int G, int GK, int NW>
+struct WeightRows<G, GK, NW, true> {};
+
+template <int G, int GK>
+struct Smem {
+  static constexpr int NW = Tune<G, GK>::NW;
+  static constexpr int NPART = Tune<G, GK>::THREADS / D;   // row parts of the q rotation
+  static constexpr int NGRP = NW / 4;                      // four-warp groups (BF16 pages)
+  // INT2: per-warp TMA rings; at the end of a segment (every copy consumed): the
+  // warps' states; BF16 pages: group g's K and V rows in the rings of its warps
+  union {
+    __align__(128) uint8_t ring[NW][STAGES][record_for(GK)];
+    float state[NW][G][PART];
+  } buf;
+  union {
+    struct {
+      float q[G][D];
+      float part[NPART][G][D];
+      float norm[G];
+    } pro;                              // rotation of q
+    float bf[NGRP][G][D + PAGE];        // BF16 pages: q (unrotated), then the page's logits
+  } scr;
+  uint32_t qf[2][QFrag<G>::WORDS];      // q operands of segment e in slot e & 1
+  __align__(8) uint64_t bar[NW][STAGES];
+  __align__(16) float4 meta[NW][PAGE];   // INT2: per token {s_k, z_k, s_v 2^ew, z_v} of the page
+  __align__(16) float4 meta2[NW][GK == 64 ? PAGE : 1];   // G_K = 64: the same for group 1
+  WeightRows<G, GK, NW> w;
+  int nseg;
+  Seg seg[SEGMAX];
+};
+
+// q_rot = q R_K for the G query heads of (request, kv head), written as the q
+// operands of slot `slot` (layout above).  Every thread of the CTA takes part:
+// thread (part p, column c) sums rows [p RP, (p + 1) RP) of column c of R_K.
+template <int G, int GK>
+__device__ void build_qfrag(const DevCache& c, int layer, const DecodeReq& R, int head,
+                            const uint16_t* __restrict__ q, Smem<G, GK>& sm, int slot) {
+  constexpr int NTH = Tune<G, GK>::THREADS, NPART = Smem<G, GK>::NPART;
+  constexpr int RP = (D + NPART - 1) / NPART;
+  constexpr int REGS = QFrag<G>::REGS;
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const uint16_t* qrow = q + ((size_t)R.batch_row * c.Hq + (size_t)head * G) * D;
+  const float* __restrict__ RK = c.rot_k + ((size_t)layer * c.Hkv + head) * D * D;
+  const int ch = t % D, part = t / D;
+  const int r0 = part * RP, r1 = min(D, r0 + RP);
+  float rk[RP];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint32_t r[16];
-    unpack_word(w[2 * q], r);
-    unpack_word(w[2 * q + 1], r + 8);
-    tmem_st16(taddr + 16 * q, r);
+  for (int i = 0; i < RP; ++i) rk[i] = (r0 + i < r1) ? __ldg(RK + (size_t)(r0 + i) * D + ch) : 0.0f;
+  for (int i = t; i < G * D; i += NTH) sm.scr.pro.q[i / D][i % D] = __uint_as_float(static_cast<uint32_t>(qrow[i]) << 16);
+  __syncthreads();
+  float acc[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) acc[h] = 0.0f;
+#pragma unroll
+  for (int i = 0; i < RP; ++i) {
+    if (r0 + i < r1) {
+#pragma unroll
+      for (int h = 0; h < G; ++h) acc[h] = fmaf(sm.scr.pro.q[h][r0 + i], rk[i], acc[h]);
+    }
   }
+#pragma unroll
+  for (int h = 0; h < G; ++h) sm.scr.pro.part[part][h][ch] = acc[h];
+  // |q_h|^2 by the warps of part 0 (warp h), rounded up
+  if (w < G) {
+    const float4 x = *reinterpret_cast<const float4*>(&sm.scr.pro.q[w][4 * lane]);
+    float n2 = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, x.w * x.w)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
+    if (lane == 0) sm.scr.pro.norm[w] = n2;
+  }
+  __syncthreads();
+  if (t < D) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float v = sm.scr.pro.part[0][h][t];
+#pragma unroll
+      for (int p = 1; p < NPART; ++p) v += sm.scr.pro.part[p][h][t];
+      sm.scr.pro.part[0][h][t] = v;
+    }
+  }
+  __syncthreads();
+  // qscale(h) = 2^e, e = 15 - 24 - ceil(log2(|q|_2 1.001)) (read off the exponent of
+  // the rounded-up norm), so |q_rot| qscale 2^24 <= 2^15
+  auto qexp = [&](int h) -> int {
+    const float n2 = sm.scr.pro.norm[h];
+    int e = 0;
+    if (n2 > 0.0f) {
+      const uint32_t b = __float_as_uint(__fmul_ru(__fsqrt_ru(n2), 1.001f));
+      const int ceil_log2 = static_cast<int>((b >> 23) & 0xffu) - 127 + ((b & 0x7fffffu) != 0u ? 1 : 0);
+      e = 15 - 24 - ceil_log2;
+    }
+    return max(-60, min(e, 60));
+  };
+  uint32_t* dst = sm.qf[slot];
+  for (int wi = t; wi < 32 * REGS; wi += NTH) {
+    const int lane_w = wi / REGS, k = wi % REGS;
+    const int gid = lane_w >> 2, tid = lane_w & 3;
+    const int nt = k >> 4, s = (k >> 1) & 7, rr = k & 1;
+    const int h = 4 * nt + (gid >> 1);
+    uint32_t word = 0u;
+    if (h < G) {
+      const int m = 2 * (s & 3) + rr;
+      const int chn = GK == 128 ? 32 * tid + 16 * (s >> 2) + m : 64 * (s >> 2) + 16 * tid + m;
+      const float f = ldexpf(1.0f, qexp(h) + 24 - 2 * code_exp(m));
+      float ha, la, hb, lb;
+      split_half(sm.scr.pro.part[0][h][chn] * f, ha, la);
+      split_half(sm.scr.pro.part[0][h][chn + 8] * f, hb, lb);
+      word = (gid & 1) ? pack_half2(la, lb) : pack_half2(ha, hb);
+    }
+    dst[wi] = word;
+  }
+  float* consts = reinterpret_cast<float*>(dst + QFrag<G>::CONSTS);
+  if (t < 8) consts[t] = t < G ? c.scale * LOG2E * ldexpf(1.0f, -qexp(t)) : 0.0f;
+  // slab sums: warp (slab, head) pairs, lane over the slab's 32 channels
+  for (int pr = w; pr < SLABS * 8; pr += NTH / 32) {
+    const int sl = pr / 8, h = pr % 8;
+    float v = h < G ? sm.scr.pro.part[0][h][32 * sl + lane] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) consts[8 + 8 * sl + h] = v;
+  }
+  __syncthreads();
 }
 
-// ---- the plan ------------------------------------------------------------------------
+// The INT2 pages [p0, p1) of one (request, kv head) segment that this CTA holds:
+// warp w takes pages p0 + w, p0 + w + NW, ... through its TMA ring (copy number
+// nc counts the copies this warp has consumed so far, across segments); qf holds
+// the segment's q operands.  Leaves the CTA's partial (rotated basis) for every
+// query head of the group in part_out.
+template <int G, int GK>
+__device__ __forceinline__ void int2_pages(const DevCache& c, int layer, const DecodeReq& R, int head, int p0,
+                                           int p1, const uint32_t* __restrict__ qf, Smem<G, GK>& sm,
+                                           float* part_out, uint32_t limit, bool front_writes, uint32_t& nc,
+                                           bool& timed_out) {
+  constexpr int NW = Tune<G, GK>::NW;
+  constexpr int NT = QFrag<G>::NT;       // n-tiles of 8 columns = 4 heads x (hi, lo)
+  constexpr int REC = record_for(GK);
+  constexpr int NGR = D / GK;            // quantisation groups per token-head
+  constexpr int KMETA = k_meta_off_for(GK), VMETA = v_meta_off_for(GK), MB = meta_bytes_for(GK);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tid = lane & 3;
+  const int nhist = R.hist_end - SINK;
+  const int my_n = (p1 - p0 > warp) ? (p1 - p0 - warp + NW - 1) / NW : 0;
+  const int32_t* pt = c.hist_pt + (size_t)R.slot * c.max_pages;
+  const uint8_t* base = c.int2 + layer * c.int2_layer_stride + (size_t)head * REC;
+  const size_t pstride = (size_t)c.Hkv * REC;
+  const int hot = front_writes ? R.hot_page : -1;
+
+  // page ids of this warp's pages, read 32 at a time (lane l holds page 32 b + l of
+  // batch b); page_src is called by the whole warp with increasing j
+  int32_t batch_pages = 0;
+  int batch_idx = -1;
+  auto checked = [&](int32_t page) -> int32_t {
+    if (page < 0 || page >= c.n_int2_pages) {
+      atomicOr(c.err, ERR_INT2_PAGE);
+      page = 0;
+    }
+    return page;
+  };
+  // the hot page (written by a preceding fused append) is read only after that
+  // grid has completed: its id is fetched by lane 0 at copy time, after the wait
+  auto page_src = [&](int j) -> const uint8_t* {
+    const int b = j >> 5;
+    if (b != batch_idx) {
+      batch_idx = b;
+      const int jj = 32 * b + lane;
+      const int pj = p0 + warp + NW * jj;
+      int32_t page = 0;
+      if (jj < my_n) page = pj == hot ? -1 : checked(__ldcg(pt + pj));
+      batch_pages = page;
+    }
+    int32_t page = __shfl_sync(0xffffffffu, batch_pages, j & 31);
+    if (page < 0 && lane == 0) {
+      grid_dep_wait();
+      page = checked(__ldcg(pt + hot));
+    }
+    return base + (size_t)max(page, 0) * pstride;
+  };
+  auto issue = [&](int j) {
+    const uint8_t* src = page_src(j);
+    if (lane == 0 && j < my_n) {
+      const int st = (nc + j) % STAGES;
+      mbar_expect_tx(&sm.bar[warp][st], REC);
+      tma_load_1d(sm.buf.ring[warp][st], src, REC, &sm.bar[warp][st]);
+    }
+  };
+#pragma unroll
+  for (int j = 0; j < STAGES; ++j) issue(j);
+  // weights p * s_v are prescaled by 2^ew so the smallest ones stay representable in
+  // fp16: s_v <= fp16(2 tau_V / 3) and p <= 2^LAZY_MAX, so p s_v 2^ew <= 2^15
+  int ew;
+  {
+    const float smax = c.tau_v[(size_t)layer * c.Hkv + head] * (2.0f / 3.0f) * 1.002f;
+    ew = max(-60, min(60, static_cast<int>(floorf(log2f(32768.0f / smax))) - LAZY_MAX_INT));
+  }
+  const float wscale = ldexpf(1.0f, ew);
+
+  // B operands of q_rot . c, and the per-head logit constants of this lane's head
+  uint32_t bq[NT][8][2];
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(qf + (size_t)lane * QFrag<G>::REGS);
+    uint4 v[QFrag<G>::REGS / 4];
+#pragma unroll
+    for (int u = 0; u < QFrag<G>::REGS / 4; ++u) v[u] = src[u];
+#pragma unroll
+    for (int u = 0; u < QFrag<G>::REGS / 4; ++u) {
+      const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int k = 4 * u + e;
+        bq[k >> 4][(k >> 1) & 7][k & 1] = w4[e];
+      }
+    }
+  }
+  // kz[nt][g]: scale log2(e) times the sum of q_rot over group g's channels (its slabs)
+  float ks[NT], kz[NT][NGR];
+  {
+    const float* consts = reinterpret_cast<const float*>(qf + QFrag<G>::CONSTS);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      ks[nt] = consts[4 * nt + tid];
+#pragma unroll
+      for (int g = 0; g < NGR; ++g) {
+        float sum = 0.0f;
+#pragma unroll
+        for (int sl = g * (SLABS / NGR); sl < (g + 1) * (SLABS / NGR); ++sl) sum += consts[8 + 8 * sl + 4 * nt + tid];
+        kz[nt][g] = c.scale * LOG2E * sum;
+      }
+    }
+  }
+
+  float o[NT][8][4];
+  // l and u are kept as two partial sums (tokens gid and gid + 8 of each m-tile)
+  // so that the page's pairs update them with packed fp32 instructions
+  float m_run[NT];
+  float2 l_run[NT], u_run[NT][NGR];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    m_run[nt] = -INFINITY;
+    l_run[nt] = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int g = 0; g < NGR; ++g) u_run[nt][g] = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[nt][mt][e] = 0.0f;
+  }
+
+  int done = 0;   // copies of this segment consumed by this warp
+  for (int j = 0; j < my_n; ++j) {
+    const int stg = (nc + j) % STAGES;
+    const int pi = p0 + warp + NW * j;
+    if (!timed_out && !mbar_wait(&sm.bar[warp][stg], ((nc + j) / STAGES) & 1, limit)) {
+      timed_out = true;
+      if (lane == 0) atomicOr(c.err, ERR_TIMEOUT);
+    }
+    if (timed_out) break;
+    done = j + 1;
+    const uint8_t* rec = sm.buf.ring[warp][stg];
+    const int valid = min(PAGE, nhist - pi * PAGE);
+
+
+    // ---- logits: 4 m-tiles of 16 tokens x NT n-tiles, K = 128 channels; with
+    // G_K = 64 the k-steps of each group accumulate apart (acc[g])
+    float acc[NGR][NT][4][4];
+#pragma unroll
+    for (int g = 0; g < NGR; ++g)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[g][nt][mt][e] = 0.0f;
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      uint2 ka, kb;
+      if constexpr (GK == 128) {
+        // channels 32 tid .. 32 tid + 31 of tokens 16 mt + gid and + 8
+        ka = *reinterpret_cast<const uint2*>(rec + K_CODES_OFF + (16 * mt + gid) * CODE_BYTES + 8 * tid);
+        kb = *reinterpret_cast<const uint2*>(rec + K_CODES_OFF + (16 * mt + gid + 8) * CODE_BYTES + 8 * tid);
+      } else {
+        // channels 16 tid .. 16 tid + 15 of group 0 (.x) and of group 1 (.y)
+        const uint8_t* ra = rec + K_CODES_OFF + (16 * mt + gid) * CODE_BYTES;
+        const uint8_t* rb = ra + 8 * CODE_BYTES;
+        ka = make_uint2(*reinterpret_cast<const uint32_t*>(ra + 4 * tid),
+                        *reinterpret_cast<const uint32_t*>(ra + 16 + 4 * tid));
+        kb = make_uint2(*reinterpret_cast<const uint32_t*>(rb + 4 * tid),
+                        *reinterpret_cast<const uint32_t*>(rb + 16 + 4 * tid));
+      }
+      const uint2 kas = make_uint2(ka.x >> 10, ka.y >> 10);
+      const uint2 kbs = make_uint2(kb.x >> 10, kb.y >> 10);
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t wa = s < 4 ? ka.x : ka.y, was = s < 4 ? kas.x : kas.y;
+        const uint32_t wb = s < 4 ? kb.x : kb.y, wbs = s < 4 ? kbs.x : kbs.y;
+        const int m0 = 2 * (s & 3);
+        const uint32_t a0 = code_pair2(wa, was, m0), a1 = code_pair2(wb, wbs, m0);
+        const uint32_t a2 = code_pair2(wa, was, m0 + 1), a3 = code_pair2(wb, wbs, m0 + 1);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          mma16816(acc[NGR == 2 ? (s >> 2) : 0][nt][mt], a0, a1, a2, a3, bq[nt][s][0], bq[nt][s][1]);
+      }
+    }
+    // token meta of this lane's 8 tokens: 16 mt + gid + 8 rr; a partial page (the
+    // last of the history) masks the rows past its end
+    // the page's metadata converted once per token (lanes l and l + 32), not once
+    // per query head: {s_k, z_k, s_v 2^ew, z_v}, value terms zeroed past the end
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int tok = lane + 32 * hh;
+      const bool ok = tok < valid;
+#pragma unroll
+      for (int g = 0; g < NGR; ++g) {
+        const __half2 km = *reinterpret_cast<const __half2*>(rec + KMETA + tok * MB + 4 * g);
+        const __half2 vm = *reinterpret_cast<const __half2*>(rec + VMETA + tok * MB + 4 * g);
+        const float4 mv = make_float4(__low2float(km), __high2float(km), ok ? __low2float(vm) * wscale : 0.0f,
+                                      ok ? __high2float(vm) : 0.0f);
+        if (g == 0)
+          sm.meta[warp][tok] = mv;
+        else
+          sm.meta2[warp][tok] = mv;
+      }
+    }
+    __syncwarp();
+    // logits in the log2 domain, as pairs (token 16 mt + gid, that token + 8)
+    float2 lg[NT][4], sw[NGR][4], zv[NGR][4];
+    auto epilogue = [&](auto full_page) {
+      constexpr bool FULL = decltype(full_page)::value;
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        const int tok = 16 * mt + gid;
+        const float4 m0 = sm.meta[warp][tok], m1 = sm.meta[warp][tok + 8];
+        sw[0][mt] = make_float2(m0.z, m1.z);
+        zv[0][mt] = make_float2(m0.w, m1.w);
+        float4 n0 = m0, n1 = m1;
+        if constexpr (NGR == 2) {
+          n0 = sm.meta2[warp][tok];
+          n1 = sm.meta2[warp][tok + 8];
+          sw[NGR - 1][mt] = make_float2(n0.z, n1.z);
+          zv[NGR - 1][mt] = make_float2(n0.w, n1.w);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          // hi + lo columns, then s_k kscale acc + z_k (scale log2 e sum q_rot), per group
+          const float2 a = __fadd2_rn(make_float2(acc[0][nt][mt][0], acc[0][nt][mt][2]),
+                                      make_float2(acc[0][nt][mt][1], acc[0][nt][mt][3]));
+          const float2 sk = __fmul2_rn(make_float2(m0.x, m1.x), make_float2(ks[nt], ks[nt]));
+          const float2 zk = __fmul2_rn(make_float2(m0.y, m1.y), make_float2(kz[nt][0], kz[nt][0]));
+          float2 v = __ffma2_rn(sk, a, zk);
+          if constexpr (NGR == 2) {
+            const float2 a1 = __fadd2_rn(make_float2(acc[NGR - 1][nt][mt][0], acc[NGR - 1][nt][mt][2]),
+                                         make_float2(acc[NGR - 1][nt][mt][1], acc[NGR - 1][nt][mt][3]));
+            const float2 sk1 = __fmul2_rn(make_float2(n0.x, n1.x), make_float2(ks[nt], ks[nt]));
+            const float2 zk1 = __fmul2_rn(make_float2(n0.y, n1.y),
+                                          make_float2(kz[nt][NGR - 1], kz[nt][NGR - 1]));
+            v = __ffma2_rn(sk1, a1, __fadd2_rn(v, zk1));
+          }
+          const bool head_ok = 4 * nt + 4 <= G || 4 * nt + tid < G;
+          if (!FULL || !head_ok) {
+            v.x = (head_ok && tok < valid) ? v.x : -INFINITY;
+            v.y = (head_ok && tok + 8 < valid) ? v.y : -INFINITY;
+          }
+          lg[nt][mt] = v;
+        }
+      }
+    };
+    if (valid == PAGE)
+      epilogue(std::true_type{});
+    else
+      epilogue(std::false_type{});
+    // ---- online softmax per head (lanes with equal tid share a head); the
+    // weights p s_v 2^ew go to shared memory as fp16 hi / lo halves.  Within each
+    // 16-token group the weight rows hold token 16 g + r at position 16 g + 2 r
+    // (r < 8) or 16 g + 2 (r - 8) + 1, so a lane's pair is one 32-bit store; the
+    // value contraction below takes its k index in the same order.
+    uint16_t(*wh)[2][WH_STRIDE];
+    if constexpr (kWeightsInRing<G, GK>) {
+      wh = reinterpret_cast<uint16_t(*)[2][WH_STRIDE]>(sm.buf.ring[warp][stg] + K_CODES_OFF);
+      __syncwarp();   // every lane is done reading this page's K codes
+    } else {
+      wh = sm.w.wh[warp];
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float pm = fmaxf(lg[nt][0].x, lg[nt][0].y);
+#pragma unroll
+      for (int mt = 1; mt < 4; ++mt) pm = fmaxf(pm, fmaxf(lg[nt][mt].x, lg[nt][mt].y));
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+      // the reference max m_run moves only when a page exceeds it by more than
+      // LAZY_MAX (log2 units): weights stay below 2^LAZY_MAX and the accumulators
+      // are rescaled on few pages
+      if (pm > m_run[nt] + LAZY_MAX) {
+        const float corr = ex2(m_run[nt] - pm);
+        m_run[nt] = pm;
+        l_run[nt] = __fmul2_rn(l_run[nt], make_float2(corr, corr));
+#pragma unroll
+        for (int g = 0; g < NGR; ++g) u_run[nt][g] = __fmul2_rn(u_run[nt][g], make_float2(corr, corr));
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[nt][mt][e] *= corr;
+      }
+      const float2 neg_ref = make_float2(-m_run[nt], -m_run[nt]);
+      const int h = 4 * nt + tid;
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        const float2 d = __fadd2_rn(lg[nt][mt], neg_ref);
+        const float2 p = make_float2(ex2(d.x), ex2(d.y));
+        l_run[nt] = __fadd2_rn(l_run[nt], p);
+#pragma unroll
+        for (int g = 0; g < NGR; ++g) u_run[nt][g] = __ffma2_rn(p, zv[g][mt], u_run[nt][g]);
+        if (h < G) {
+          const int pos = 16 * mt + 2 * gid;
+#pragma unroll
+          for (int g = 0; g < NGR; ++g) {
+            const float2 w = __fmul2_rn(p, sw[g][mt]);
+            const __half2 hi = __float22half2_rn(w);
+            const float2 lo = __ffma2_rn(__half22float2(hi), make_float2(-1.0f, -1.0f), w);
+            *reinterpret_cast<__half2*>(&wh[NGR * h + g][0][pos]) = hi;
+            *reinterpret_cast<__half2*>(&wh[NGR * h + g][1][pos]) = __float22half2_rn(lo);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    // ---- values: 8 m-tiles of 16 channels x NT n-tiles, K = 64 tokens; k index
+    // 2 j + b of step s is token 16 s + j + 8 b
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int ta = 16 * s + 2 * tid;
+      uint32_t bw[NGR][NT][2];
+#pragma unroll
+      for (int g = 0; g < NGR; ++g)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int h = 4 * nt + (gid >> 1);
+          if (h < G) {
+            const uint16_t* row = wh[NGR * h + g][gid & 1];
+            bw[g][nt][0] = *reinterpret_cast<const uint32_t*>(row + ta);
+            bw[g][nt][1] = *reinterpret_cast<const uint32_t*>(row + ta + 8);
+          } else {
+            bw[g][nt][0] = bw[g][nt][1] = 0u;
+          }
+        }
+      const int tb = 16 * s + tid;
+      if constexpr (GK == 128) {
+        // row gid of m-tile mt: channel 16 gid + mt; row gid + 8: 16 gid + 8 + mt
+        const uint32_t* vrow = reinterpret_cast<const uint32_t*>(rec + V_CODES_OFF) + gid;
+        const uint32_t wa = vrow[tb * (CODE_BYTES / 4)], wb = vrow[(tb + 8) * (CODE_BYTES / 4)];
+        const uint32_t wc = vrow[(tb + 4) * (CODE_BYTES / 4)], wd = vrow[(tb + 12) * (CODE_BYTES / 4)];
+        const uint32_t x1 = __byte_perm(wa, wb, 0x5410), y1 = __byte_perm(wa, wb, 0x7632);
+        const uint32_t x2 = __byte_perm(wc, wd, 0x5410), y2 = __byte_perm(wc, wd, 0x7632);
+        const uint32_t x1s = x1 >> 10, y1s = y1 >> 10;
+        const uint32_t x2s = x2 >> 10, y2s = y2 >> 10;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          const uint32_t a0 = code_pair2(x1, x1s, mt), a1 = code_pair2(y1, y1s, mt);
+          const uint32_t a2 = code_pair2(x2, x2s, mt), a3 = code_pair2(y2, y2s, mt);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma16816(o[nt][mt], a0, a1, a2, a3, bw[0][nt][0], bw[0][nt][1]);
+        }
+      } else {
+        // group-pure m-tiles: m-tile 4 g + j, row gid holds channel 64 g + 8 gid + j and
+        // row gid + 8 channel 64 g + 8 gid + 4 + j (16-bit half gid & 1 of word 4 g + gid / 2)
+        const uint32_t sel = (gid & 1) ? 0x7632u : 0x5410u;
+#pragma unroll
+        for (int g = 0; g < NGR; ++g) {
+          const uint32_t* vrow = reinterpret_cast<const uint32_t*>(rec + V_CODES_OFF) + 4 * g + (gid >> 1);
+          const uint32_t wa = vrow[tb * (CODE_BYTES / 4)], wb = vrow[(tb + 8) * (CODE_BYTES / 4)];
+          const uint32_t wc = vrow[(tb + 4) * (CODE_BYTES / 4)], wd = vrow[(tb + 12) * (CODE_BYTES / 4)];
+          const uint32_t x1 = __byte_perm(wa, wb, sel), x2 = __byte_perm(wc, wd, sel);
+          const uint32_t x1s = x1 >> 10, x2s = x2 >> 10;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t a0 = code_pair2(x1, x1s, j), a1 = code_pair2(x1, x1s, j + 4);
+            const uint32_t a2 = code_pair2(x2, x2s, j), a3 = code_pair2(x2, x2s, j + 4);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma16816(o[nt][4 * g + j], a0, a1, a2, a3, bw[g][nt][0], bw[g][nt][1]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (j + STAGES < my_n) {
+      const uint8_t* src = page_src(j + STAGES);
+      if (lane == 0) {
+        // the weights were written to this buffer through the generic proxy
+        if constexpr (kWeightsInRing<G, GK>) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_expect_tx(&sm.bar[warp][stg], REC);
+        tma_load_1d(sm.buf.ring[warp][stg], src, REC, &sm.bar[warp][stg]);
+      }
+    }
+  }
+  if (timed_out && lane == 0) {
+    // let every copy this warp issued land (bounded) before the buffers are reused:
+    // the copies done .. min(done + STAGES, my_n) - 1 may still be in flight
+    for (int j = done; j < min(done + STAGES, my_n); ++j)
+      mbar_wait(&sm.bar[warp][(nc + j) % STAGES], ((nc + j) / STAGES) & 1, limit);
+  }
+  nc += static_cast<uint32_t>(my_n);
+  __syncthreads();   // every warp is done with every ring before states overwrite them
+
+  // ---- this warp's state -> shared memory (rotated basis, unscaled, z term added)
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    float l = l_run[nt].x + l_run[nt].y, u[NGR];
+#pragma unroll
+    for (int g = 0; g < NGR; ++g) u[g] = u_run[nt][g].x + u_run[nt][g].y;
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l += __shfl_xor_sync(0xffffffffu, l, off);
+#pragma unroll
+      for (int g = 0; g < NGR; ++g) u[g] += __shfl_xor_sync(0xffffffffu, u[g], off);
+    }
+    const int h = 4 * nt + tid;
+    if (h < G) {
+      float* st = sm.buf.state[warp][h];
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        if constexpr (GK == 128) {
+          const float f = ldexpf(1.0f, 24 - 2 * code_exp(mt) - ew);
+          st[16 * gid + mt] = fmaf(o[nt][mt][0] + o[nt][mt][1], f, u[0]);
+          st[16 * gid + 8 + mt] = fmaf(o[nt][mt][2] + o[nt][mt][3], f, u[0]);
+        } else {
+          const int g = mt >> 2, j = mt & 3;
+          const float f0 = ldexpf(1.0f, 24 - 2 * code_exp(j) - ew);
+          const float f1 = ldexpf(1.0f, 24 - 2 * code_exp(j + 4) - ew);
+          st[64 * g + 8 * gid + j] = fmaf(o[nt][mt][0] + o[nt][mt][1], f0, u[g]);
+          st[64 * g + 8 * gid + 4 + j] = fmaf(o[nt][mt][2] + o[nt][mt][3], f1, u[g]);
+        }
+      }
+      if (gid == 0) {
+        st[PARTIAL_M] = m_run[nt];
+        st[PARTIAL_L] = l;
+      }
+    }
+  }
+  __syncthreads();
+  // ---- merge the warps: thread t < 128 owns channel t
+  const int t = threadIdx.x;
+  if (t < D) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, sm.buf.state[w][h][PARTIAL_M]);
+      float acc_o = 0.0f, acc_l = 0.0f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float mw = sm.buf.state[w][h][PARTIAL_M];
+        if (mw == -INFINITY) continue;
+        const float f = exp2f(mw - M);
+        acc_o = fmaf(sm.buf.state[w][h][t], f, acc_o);
+        acc_l = fmaf(sm.buf.state[w][h][PARTIAL_L], f, acc_l);
+      }
+      part_out[h * PART + t] = acc_o;
+      if (t == 0) {
+        part_out[h * PART + PARTIAL_M] = M;
+        part_out[h * PART + PARTIAL_L] = acc_l;
+      }
+    }
+  }
+  __syncthreads();   // states read before the rings take the next segment's copies
+}
+
+// One BF16 page (the sink page, or one of the four recent-ring pages) of one
+// (request, kv head), with the unrotated q, by the four-warp group grp of the CTA:
+// its K and V rows go to the rings of the group's warps, q and the logits to the
+// group's scratch rows.  Partial for every query head of the group.
+template <int G, int GK>
+__device__ __forceinline__ void bf16_item(const DevCache& c, int layer, const DecodeReq& R, int head, int which,
+                                          const uint16_t* __restrict__ q, Smem<G, GK>& sm, int grp,
+                                          float* part_out) {
+  constexpr int THREADS = 128, WARPS = 4;
+  const int t = threadIdx.x - THREADS * grp;
+  const int warp = t >> 5, lane = t & 31;
+  uint16_t (*kr)[D] = reinterpret_cast<uint16_t (*)[D]>(&sm.buf.ring[WARPS * grp][0][0]);
+  uint16_t (*vr)[D] = kr + PAGE;
+  float (*qs)[D + PAGE] = sm.scr.bf[grp];
+  auto group_sync = [&]() { bar_sync(1 + grp, THREADS); };
+  const float scale2 = c.scale * LOG2E;
+  const int T = R.tokens, he = R.hist_end;
+  // select chain, not an indexed load: a dynamic index would put R in local memory
+  int page = which == 0 ? R.sink_page
+           : which == 1 ? R.ring_page[0]
+           : which == 2 ? R.ring_page[1]
+           : which == 3 ? R.ring_page[2]
+                        : R.ring_page[3];
+  if (page < 0 || page >= c.n_bf16_pages) {
+    if (t == 0) atomicOr(c.err, ERR_BF16_PAGE);
+    page = 0;
+  }
+  // validity of row r: sink rows [0, min(T, 64)); ring slot s = 64 (which-1) + r holds
+  // position he + ((s - (he - 64)) mod 256), valid when below T
+  auto row_valid = [&](int r) -> bool {
+    if (which == 0) return r < min(T, SINK);
+    if (T <= SINK) return false;
+    const int s = PAGE * (which - 1) + r;
+    const int p = he + ((s - (he - SINK)) % RECENT + RECENT) % RECENT;
+    return p < T;
+  };
+  {
+    const uint16_t* qrow = q + ((size_t)R.batch_row * c.Hq + (size_t)head * G) * D;
+    for (int i = t; i < G * D; i += THREADS) qs[i / D][i % D] = __uint_as_float(static_cast<uint32_t>(qrow[i]) << 16);
+  }
+  const uint16_t* src = c.bf16 + layer * c.bf16_layer_stride + ((size_t)page * c.Hkv + head) * BF16_RECORD_ELEMS;
+  constexpr int LOADS = PAGE * (D / 8) / THREADS;
+  uint4 kk[LOADS], vv[LOADS];
+#pragma unroll
+  for (int it = 0; it < LOADS; ++it) {
+    const int idx = t + THREADS * it, r = idx / (D / 8), part = idx % (D / 8);
+    kk[it] = __ldcg(reinterpret_cast<const uint4*>(src + (size_t)r * D) + part);
+    vv[it] = __ldcg(reinterpret_cast<const uint4*>(src + (size_t)(PAGE + r) * D) + part);
+  }
+#pragma unroll
+  for (int it = 0; it < LOADS; ++it) {
+    const int idx = t + THREADS * it, r = idx / (D / 8), part = idx % (D / 8);
+    reinterpret_cast<uint4*>(&kr[r][0])[part ^ (r & 15)] = kk[it];
+    reinterpret_cast<uint4*>(&vr[r][0])[part] = vv[it];
+  }
+  group_sync();
+  // logits: thread t -> token t/2, channel half t%2, all G heads
+  {
+    const int r = t >> 1, half = t & 1;
+    float acc[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) acc[h] = 0.0f;
+    const uint4* krow = reinterpret_cast<const uint4*>(&kr[r][0]);
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const int chunk = 8 * half + b;
+      const uint4 w = krow[chunk ^ (r & 15)];
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float k0 = bf16lo(ww[e]), k1 = bf16hi(ww[e]);
+        const int ch = 8 * chunk + 2 * e;
+#pragma unroll
+        for (int h = 0; h < G; ++h) acc[h] = fmaf(qs[h][ch + 1], k1, fmaf(qs[h][ch], k0, acc[h]));
+      }
+    }
+    const bool ok = row_valid(r);
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], 1);
+      if (half == 0) qs[h][D + r] = ok ? acc[h] * scale2 : -INFINITY;
+    }
+  }
+  group_sync();
+  // softmax and values: warp w handles heads w, w + 4; lane owns channels 4 lane .. 4 lane + 3
+  for (int h = warp; h < G; h += WARPS) {
+    const float x0 = qs[h][D + lane], x1 = qs[h][D + lane + 32];
+    float m = fmaxf(x0, x1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float p0 = (x0 == -INFINITY) ? 0.0f : exp2f(x0 - m);
+    const float p1 = (x1 == -INFINITY) ? 0.0f : exp2f(x1 - m);
+    float l = p0 + p1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    __syncwarp();
+    qs[h][D + lane] = p0;
+    qs[h][D + lane + 32] = p1;
+    __syncwarp();
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (m != -INFINITY) {
+      for (int r = 0; r < PAGE; ++r) {
+        const float p = qs[h][D + r];
+        // rows outside the window (p = 0) may hold anything, NaN included: skip them
+        if (p == 0.0f) continue;
+        const uint2 vv = reinterpret_cast<const uint2*>(&vr[r][0])[lane];
+        acc[0] = fmaf(p, bf16lo(vv.x), acc[0]);
+        acc[1] = fmaf(p, bf16hi(vv.x), acc[1]);
+        acc[2] = fmaf(p, bf16lo(vv.y), acc[2]);
+        acc[3] = fmaf(p, bf16hi(vv.y), acc[3]);
+      }
+    }
+    reinterpret_cast<float4*>(part_out + h * PART)[lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    if (lane == 0) {
+      part_out[h * PART + PARTIAL_M] = m;
+      part_out[h * PART + PARTIAL_L] = l;
+    }
+  }
+  // warps with fewer heads (G < 4) must not load the group's next page over rows
+  // and weights the others still read
+  group_sync();
+}
+
+// ---- the decode kernel --------------------------------------------------------------
 __device__ __forceinline__ int64_t cta_begin(int c, int ncta, int64_t total) { return (int64_t)c * total / ncta; }
 
 // Segment containing cost unit u: request index, kv head, its first unit.
@@ -295,150 +902,22 @@ __device__ __forceinline__ void segment_of(const DecodeArgs& a, int Hkv, int64_t
   s0 = a.r[ri].cost_start + (int64_t)h * per;
 }
 
-// Whether BF16 row r of item `which` (0 sink, 1..4 ring pages) holds a cached token:
-// sink rows [0, min(T, 64)); ring slot s = 64 (which - 1) + r holds position
-// he + ((s - (he - 64)) mod 256), cached while below T.
-__device__ __forceinline__ bool bf16_row_valid(const DecodeReq& R, int which, int r) {
-  const int T = R.tokens, he = R.hist_end;
-  if (which == 0) return r < min(T, SINK);
-  if (T <= SINK) return false;
-  const int s = PAGE * (which - 1) + r;
-  const int p = he + ((s - (he - SINK)) % RECENT + RECENT) % RECENT;
-  return p < T;
-}
-
-// ---- q operands of a segment --------------------------------------------------------
-// q_rot = q R_K for the G query heads of (request, kv head), then the logit-side
-// B tile: row k (channel chi(k) = 16 (k >> 4) + 8 (k & 1) + ((k >> 1) & 7), the
-// channel whose codes A_K column k >> 1 holds in half k & 1) carries, in column
-// (group, head, part), part of fp16 hi / lo of q_rot[head][chi] 2^eq(head) 2^(8 - 2e)
-// when chi lies in that group, else 0.  2^eq(h) puts max |q_rot[h]| in (2^6, 2^7],
-// so every entry is below 2^15.  Every thread of the CTA takes part.
+// Records in the workspace: INT2 record of (segment s, CTA c) at slot s + c (the
+// CTAs meeting one segment are consecutive, so the slots are unique), then the
+// BF16 page records of segment s at 5 s + page.
 template <int G, int GK>
-__device__ void build_q_operands(const DevCache& c, int layer, const DecodeReq& R, int head,
-                                 const uint16_t* __restrict__ q, Smem<G, GK>& sm, int slot_b) {
-  using C = Cfg<G, GK>;
-  constexpr int NTH = C::THREADS, NP = C::NWG;
-  constexpr int RP = (D + NP - 1) / NP;   // rows per part
-  const int t = threadIdx.x;
-  const uint16_t* qrow = q + ((size_t)R.batch_row * c.Hq + (size_t)head * G) * D;
-  for (int i = t; i < G * D; i += NTH) sm.u.pro.q[i / D][i % D] = __uint_as_float(static_cast<uint32_t>(qrow[i]) << 16);
-  const float* __restrict__ RK = c.rot_k + ((size_t)layer * c.Hkv + head) * D * D;
-  const int ch = t % D, part = t / D;
-  const int r0 = part * RP, r1 = min(D, r0 + RP);
-  float rk[RP];
-#pragma unroll
-  for (int i = 0; i < RP; ++i) rk[i] = (r0 + i < r1) ? __ldg(RK + (size_t)(r0 + i) * D + ch) : 0.0f;
-  __syncthreads();
-  float acc[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) acc[h] = 0.0f;
-#pragma unroll
-  for (int i = 0; i < RP; ++i) {
-    if (r0 + i < r1) {
-#pragma unroll
-      for (int h = 0; h < G; ++h) acc[h] = fmaf(sm.u.pro.q[h][r0 + i], rk[i], acc[h]);
-    }
-  }
-#pragma unroll
-  for (int h = 0; h < G; ++h) sm.u.pro.part[part][h][ch] = acc[h];
-  __syncthreads();
-  // q_rot into part[0]; per-head max |q_rot| (warp-wide, then per head by lane 0)
-  if (t < D) {
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float v = sm.u.pro.part[0][h][t];
-#pragma unroll
-      for (int p = 1; p < NP; ++p) v += sm.u.pro.part[p][h][t];
-      sm.u.pro.part[0][h][t] = v;
-    }
-  }
-  if (t < G) sm.u.pro.amax[t] = 0.0f;
-  __syncthreads();
-  if (t < D) {
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float m = warp_max(fabsf(sm.u.pro.part[0][h][t]));
-      if ((t & 31) == 0) atomicMax(reinterpret_cast<int*>(&sm.u.pro.amax[h]), __float_as_int(m));
-    }
-  }
-  __syncthreads();
-  // B tile rows (threads 0..127), logit constants (warp per head among the rest)
-  if (t < D) {
-    const int k = t;
-    const int m = (k >> 1) & 7, chi = 16 * (k >> 4) + 8 * (k & 1) + m;
-    const int grp = chi / GK;
-    uint32_t row[C::N / 2];
-#pragma unroll
-    for (int i = 0; i < C::N / 2; ++i) row[i] = 0u;
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float am = sm.u.pro.amax[h];
-      int eq = 0;
-      if (am > 0.0f) {
-        const uint32_t b = __float_as_uint(am);
-        const int ceil_log2 = static_cast<int>((b >> 23) & 0xffu) - 127 + ((b & 0x7fffffu) != 0u ? 1 : 0);
-        eq = max(-100, min(100, 7 - ceil_log2));
-      }
-      const float v = sm.u.pro.part[0][h][chi] * ldexpf(1.0f, eq + 8 - 2 * code_exp(m));
-      const __half hi = __float2half_rn(v);
-      const __half lo = __float2half_rn(v - __half2float(hi));
-      const int cc = col_of(grp, h, 0, G);   // even: hi and lo share one word
-      row[cc >> 1] = h2_bits(hi, lo);
-    }
-    uint8_t* base = sm.bq[slot_b] + (k >> 3) * 128 + (k & 7) * 16;
-#pragma unroll
-    for (int ng = 0; ng < C::N / 8; ++ng)
-      *reinterpret_cast<uint4*>(base + 2048 * ng) =
-          make_uint4(row[4 * ng], row[4 * ng + 1], row[4 * ng + 2], row[4 * ng + 3]);
-  }
-  // logit constants: ks = scale log2(e) 2^16 / 2^eq, kz[group] = scale log2(e) sum q_rot
-  const int w = t >> 5, lane = t & 31;
-  for (int h = w - 4; h >= 0 && h < G; h += C::THREADS / 32 - 4) {
-    const float am = sm.u.pro.amax[h];
-    int eq = 0;
-    if (am > 0.0f) {
-      const uint32_t b = __float_as_uint(am);
-      const int ceil_log2 = static_cast<int>((b >> 23) & 0xffu) - 127 + ((b & 0x7fffffu) != 0u ? 1 : 0);
-      eq = max(-100, min(100, 7 - ceil_log2));
-    }
-    const float s2 = c.scale * LOG2E;
-#pragma unroll
-    for (int g = 0; g < C::NG; ++g) {
-      float sum = 0.0f;
-      for (int i = lane; i < GK; i += 32) sum += sm.u.pro.part[0][h][GK * g + i];
-      sum = warp_sum(sum);
-      if (lane == 0) sm.qc[slot_b][h][1 + g] = s2 * sum;
-    }
-    if (lane == 0) sm.qc[slot_b][h][0] = s2 * ldexpf(1.0f, 16 - eq);
-  }
-  if (t == 0) {
-    // weights p s_v 2^ew with p <= 2^8 and s_v <= fp16(2 tau_V / 3): p s_v 2^ew 2^8 <= 2^15.9
-    const float smax = c.tau_v[(size_t)layer * c.Hkv + head] * (2.0f / 3.0f) * 1.002f;
-    int ew = smax > 0.0f ? static_cast<int>(floorf(log2f(0.93f / smax))) : 0;
-    sm.ew[slot_b] = max(-60, min(60, ew));
-  }
-  fence_async_smem();
-  __syncthreads();
-}
-
-// ---- the decode kernel --------------------------------------------------------------
-template <int G, int GK>
-__global__ void __launch_bounds__(Cfg<G, GK>::THREADS, 1)
+__global__ void __launch_bounds__(Tune<G, GK>::THREADS, 1)
     decode_kernel(DevCache c, int layer, DecodeArgs a, const uint16_t* __restrict__ q, float* __restrict__ recs) {
-  using C = Cfg<G, GK>;
-  constexpr int NG = C::NG, NC = C::NC, N = C::N, NWG = C::NWG, REC = C::REC;
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  constexpr int NGRP = Smem<G, GK>::NGRP;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem<G, GK>& sm = *reinterpret_cast<Smem<G, GK>*>(smem_raw);
-  const int t = threadIdx.x, wg = t / WGT, wt = t % WGT, wiw = wt >> 5, lane = t & 31;
+  const int t = threadIdx.x, warp = t >> 5;
   const int cta = blockIdx.x;
-  const uint32_t limit = a.dbg.wait_limit;
   float* int2_recs = recs;
   float* bf16_recs = recs + ((size_t)a.n * c.Hkv + a.ncta) * G * PART;
 
-  // ---- prologue: plan, tensor memory, barriers
   if (!a.front_writes) grid_dep_wait();   // the cache may have been written by the preceding grid
-  grid_dep_launch();
+  grid_dep_launch();                      // the merge grid may be scheduled; it waits for this one
   if (t == 0) {
     const int64_t u0 = cta_begin(cta, a.ncta, a.total_cost), u1 = cta_begin(cta + 1, a.ncta, a.total_cost);
     int n = 0;
@@ -463,624 +942,58 @@ __global__ void __launch_bounds__(Cfg<G, GK>::THREADS, 1)
       u = end;
     }
     sm.nseg = n;
-    sm.abort = 0;
-    for (int w = 0; w < NWG; ++w) {
-      for (int st = 0; st < STAGES; ++st) mbar_init(&sm.full[w][st], 1);
-      mbar_init(&sm.mk[w], 1);
-      mbar_init(&sm.mv[w], 1);
-      sm.flag[w][0] = sm.flag[w][1] = 0;
-    }
+  }
+  if ((t & 31) == 0) {
+#pragma unroll
+    for (int st = 0; st < STAGES; ++st) mbar_init(&sm.bar[warp][st], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (t < 32) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&sm.tmem))
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
   const int nseg = sm.nseg;
-  const uint32_t tw = sm.tmem + (uint32_t)(wg * C::TW);
-  const uint32_t lane_off = (uint32_t)(32 * wiw) << 16;
-  const uint32_t tAK = tw, tAV = tw + 64, tDK = tw + 128, tDV = tw + 128 + N;
-
-  // ---- page-pair iteration of this warpgroup: pairs j = wg, wg + NWG, ... of each segment
-  auto npairs_of = [&](int e) { return (sm.seg[e].p1 - sm.seg[e].p0 + 1) >> 1; };
-  auto advance = [&](int& e, int& j) {
-    while (e < nseg && j >= npairs_of(e)) {
-      ++e;
-      j = wg;
-    }
-  };
-  // the copies of one pair into stage st; page ids are loaded by the caller
-  auto pair_pages = [&](int e, int j, int& pa, int& pb) {
-    const Seg& s = sm.seg[e];
-    pa = s.p0 + 2 * j;
-    pb = pa + 1 < s.p1 ? pa + 1 : -1;
-  };
-  // a page id as stored (checked at copy time, so the load's latency is hidden)
-  auto page_id_raw = [&](int e, int pi) -> int {
-    return __ldcg(c.hist_pt + (size_t)a.r[sm.seg[e].ri].slot * c.max_pages + pi);
-  };
-  auto checked = [&](int id) -> int {
-    if (id < 0 || id >= c.n_int2_pages) {
-      atomicOr(c.err, ERR_INT2_PAGE);
-      id = 0;
-    }
-    return id;
-  };
-  auto page_id = [&](int e, int pi) -> int { return checked(page_id_raw(e, pi)); };
-  auto is_hot = [&](int e, int pi) { return a.front_writes && pi >= 0 && pi == a.r[sm.seg[e].ri].hot_page; };
-  auto issue = [&](int st, int e, int pa, int pb, int ida, int idb) {
-    const Seg& s = sm.seg[e];
-    const uint8_t* base = c.int2 + layer * c.int2_layer_stride + (size_t)s.head * REC;
-    const size_t pstride = (size_t)c.Hkv * REC;
-    mbar_expect_tx(&sm.full[wg][st], pb >= 0 ? 2 * REC : REC);
-    tma_load_1d(sm.ring[wg][st], base + (size_t)ida * pstride, REC, &sm.full[wg][st]);
-    if (pb >= 0) tma_load_1d(sm.ring[wg][st] + REC, base + (size_t)idb * pstride, REC, &sm.full[wg][st]);
-  };
-  // prefetch cursor (thread wt == 0): the pair to copy next, its page ids loaded one refill ahead
-  int pf_e = 0, pf_j = wg, pf_seq = 0;
-  int nx_pa = -1, nx_pb = -1, nx_ida = 0, nx_idb = 0;
-  bool nx_valid = false, nx_hot = false;
-  uint32_t issued_mask = 0;   // stages with a copy in flight (for the bounded drain on abort)
-  auto load_next_ids = [&]() {
-    advance(pf_e, pf_j);
-    nx_valid = pf_e < nseg;
-    if (!nx_valid) return;
-    pair_pages(pf_e, pf_j, nx_pa, nx_pb);
-    // the hot page's id is read at copy time, after the preceding grid has completed
-    nx_hot = is_hot(pf_e, nx_pa) || is_hot(pf_e, nx_pb);
-    nx_ida = is_hot(pf_e, nx_pa) ? 0 : page_id_raw(pf_e, nx_pa);
-    nx_idb = (nx_pb < 0 || is_hot(pf_e, nx_pb)) ? 0 : page_id_raw(pf_e, nx_pb);
-  };
-  auto issue_next = [&]() {
-    if (!nx_valid) return;
-    const int st = pf_seq % STAGES;
-    if (nx_hot) {
-      grid_dep_wait();
-      if (is_hot(pf_e, nx_pa)) nx_ida = page_id_raw(pf_e, nx_pa);
-      if (is_hot(pf_e, nx_pb)) nx_idb = page_id_raw(pf_e, nx_pb);
-    }
-    nx_ida = checked(nx_ida);
-    if (nx_pb >= 0) nx_idb = checked(nx_idb);
-    const bool held = a.dbg.hold_pair >= 0 && cta == 0 && wg == 0 && pf_seq == a.dbg.hold_pair;
-    if (!held) {
-      issue(st, pf_e, nx_pa, nx_pb, nx_ida, nx_idb);
-      issued_mask |= 1u << st;
-    }
-    ++pf_seq;
-    pf_j += NWG;
-    load_next_ids();
-  };
-  if (wt == 0) {
-    // the first STAGES pairs: all page ids in flight at once, then the copies
-    int pe[STAGES], pj[STAGES], pa[STAGES], pb[STAGES], ia[STAGES], ib[STAGES];
-    int cnt = 0;
-    for (; cnt < STAGES; ++cnt) {
-      advance(pf_e, pf_j);
-      if (pf_e >= nseg) break;
-      pe[cnt] = pf_e;
-      pj[cnt] = pf_j;
-      pair_pages(pf_e, pf_j, pa[cnt], pb[cnt]);
-      pf_j += NWG;
-    }
-    for (int i = 0; i < cnt; ++i) {
-      ia[i] = is_hot(pe[i], pa[i]) ? -1 : page_id(pe[i], pa[i]);
-      ib[i] = pb[i] < 0 ? 0 : (is_hot(pe[i], pb[i]) ? -1 : page_id(pe[i], pb[i]));
-    }
-    for (int i = 0; i < cnt; ++i) {
-      nx_pa = pa[i];
-      nx_pb = pb[i];
-      nx_ida = ia[i];
-      nx_idb = ib[i];
-      nx_valid = true;
-      const int save_e = pf_e, save_j = pf_j;
-      pf_e = pe[i];
-      pf_j = pj[i];
-      const int st = pf_seq % STAGES;
-      if (nx_ida < 0 || (nx_pb >= 0 && nx_idb < 0)) {
-        grid_dep_wait();
-        if (nx_ida < 0) nx_ida = page_id(pf_e, nx_pa);
-        if (nx_pb >= 0 && nx_idb < 0) nx_idb = page_id(pf_e, nx_pb);
-      }
-      const bool held = a.dbg.hold_pair >= 0 && cta == 0 && wg == 0 && pf_seq == a.dbg.hold_pair;
-      if (!held) {
-        issue(st, pf_e, nx_pa, nx_pb, nx_ida, nx_idb);
-        issued_mask |= 1u << st;
-      }
-      ++pf_seq;
-      pf_e = save_e;
-      pf_j = save_j;
-    }
-    load_next_ids();
-  }
-
-  // ---- q operands of the first segments (every thread)
-  for (int e = 0; e < min(nseg, SEG_PRE); ++e)
-    build_q_operands<G, GK>(c, layer, a.r[sm.seg[e].ri], sm.seg[e].head, q, sm, e);
-
-  // ---- the INT2 pairs, segment by segment
-  int seq = 0;           // pairs this warpgroup consumed
-  int mv_count = 0;      // value-side commits of this warpgroup
+  uint32_t nc = 0;          // copies this warp has consumed
+  bool timed_out = false;
+  if (nseg > 0) build_qfrag<G, GK>(c, layer, a.r[sm.seg[0].ri], sm.seg[0].head, q, sm, 0);
   for (int e = 0; e < nseg; ++e) {
     const Seg S = sm.seg[e];
-    const DecodeReq& R = a.r[S.ri];
-    int bslot = e;
-    if (e >= SEG_PRE) {
-      // later segments rebuild the operands in slot (e & 1): every warpgroup is done
-      // with the segment that used that slot (the end-of-segment barriers)
-      bslot = e & 1;
-      build_q_operands<G, GK>(c, layer, R, S.head, q, sm, bslot);
-    }
-    float ks[G], kz[G][NG];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      ks[h] = sm.qc[bslot][h][0];
-#pragma unroll
-      for (int g = 0; g < NG; ++g) kz[h][g] = sm.qc[bslot][h][1 + g];
-    }
-    const float wscale = ldexpf(1.0f, sm.ew[bslot]);
-    const uint32_t bq_addr = smem_u32(sm.bq[bslot]);
-    const uint32_t bw_addr = smem_u32(sm.bw[wg]);
-    const int nhist = R.hist_end - SINK;
-    float m_ref[G], l_acc[G], u_acc[G][NG];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      m_ref[h] = -INFINITY;
-      l_acc[h] = 0.0f;
-#pragma unroll
-      for (int g = 0; g < NG; ++g) u_acc[h][g] = 0.0f;
-    }
-    bool has_acc = false;
-    const int npairs = (S.p1 - S.p0 + 1) >> 1;
-    for (int j = wg; j < npairs; j += NWG, ++seq) {
-      const int st = seq % STAGES;
-      const uint8_t* stage = sm.ring[wg][st];
-      const int pa = S.p0 + 2 * j;
-      const int va = min(PAGE, nhist - PAGE * pa);
-      const int vb = pa + 1 < S.p1 ? min(PAGE, nhist - PAGE * (pa + 1)) : 0;
-      if (!sm.abort && !mbar_wait(&sm.full[wg][st], (seq / STAGES) & 1, limit)) {
-        if (wt == 0) {
-          sm.abort = 1;
-          atomicOr(c.err, ERR_TIMEOUT);
-        }
-      }
-      bar_sync(1 + wg, WGT);
-      const bool ab = sm.abort != 0;
-      if (wt == 0) {
-        if (seq >= 1) sm.flag[wg][(seq + 1) & 1] = 0;   // the flag of the next pair
-        issued_mask &= ~(1u << st);
-      }
-      // -- K side: thread = token wt of the pair
-      const int tp = wt >> 6, tr = wt & 63;
-      const bool valid = tr < (tp ? vb : va);
-      if (!ab) {
-        const uint4* kc = reinterpret_cast<const uint4*>(stage + tp * REC + K_CODES_OFF + CODE_BYTES * tr);
-        const uint4 c0 = kc[0], c1 = kc[1];
-        const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        store_row(tAK + lane_off, w);
-        tc_wait_st();
-      }
-      tc_fence_before();
-      bar_sync(1 + wg, WGT);
-      if (wt == 0 && !ab) {
-        tc_fence_after();
-#pragma unroll
-        for (int s = 0; s < 8; ++s) umma(tDK, tAK + 8 * s, b_desc(bq_addr + 256 * s), idesc_f16<N>(), s > 0 ? 1u : 0u);
-        umma_commit(&sm.mk[wg]);
-      }
-      // -- V side: thread = channel wt; the previous value MMA must have read A_V
-      if (!ab) {
-        if (mv_count > 0 && !mbar_wait(&sm.mv[wg], (mv_count - 1) & 1, limit) && wt == 0) {
-          sm.abort = 1;
-          atomicOr(c.err, ERR_TIMEOUT);
-        }
-        tc_fence_after();
-        const uint4 v0 = *reinterpret_cast<const uint4*>(stage + V_CODES_OFF + 16 * wt);
-        const uint4 v1 = *reinterpret_cast<const uint4*>(stage + REC + V_CODES_OFF + 16 * wt);
-        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-        store_row(tAV + lane_off, w);
-        tc_wait_st();
-      }
-      // -- token meta: {s, z} of K and V per group, value terms zeroed past the end
-      float sk[NG], zk[NG], sv[NG], zv[NG];
-      {
-        const uint8_t* rb = stage + tp * REC;
-#pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          const __half2 km = *reinterpret_cast<const __half2*>(rb + C::KMETA + C::MB * tr + 4 * g);
-          const __half2 vm = *reinterpret_cast<const __half2*>(rb + C::VMETA + C::MB * tr + 4 * g);
-          sk[g] = __low2float(km);
-          zk[g] = __high2float(km);
-          sv[g] = valid ? __low2float(vm) * wscale : 0.0f;
-          zv[g] = valid ? __high2float(vm) : 0.0f;
-        }
-      }
-      // -- logits (log2 domain)
-      float lg[G];
-      if (!ab) {
-        if (!mbar_wait(&sm.mk[wg], seq & 1, limit) && wt == 0) {
-          sm.abort = 1;
-          atomicOr(c.err, ERR_TIMEOUT);
-        }
-        tc_fence_after();
-        float d[NC <= 8 ? 8 : (NC <= 16 ? 16 : 32)];
-        tmem_ld(tDK + lane_off, d);
-        tc_wait_ld();
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float v = 0.0f;
-#pragma unroll
-          for (int g = 0; g < NG; ++g) {
-            const float acc = d[col_of(g, h, 0, G)] + d[col_of(g, h, 1, G)];
-            v = fmaf(ks[h] * sk[g], acc, fmaf(kz[h][g], zk[g], v));
-          }
-          lg[h] = valid ? v : -INFINITY;
-        }
-      } else {
-#pragma unroll
-        for (int h = 0; h < G; ++h) lg[h] = -INFINITY;
-      }
-      // -- softmax: the reference max m_ref moves only when a pair exceeds it by more
-      // than LAZY_MAX; the warps of the warpgroup agree on it through shared memory
-      bool exceed = false;
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float wm = warp_max(lg[h]);
-        exceed |= wm > m_ref[h] + LAZY_MAX;
-        if (lane == 0) sm.wmax[wg][wiw][h] = wm;
-      }
-      if (exceed && lane == 0) sm.flag[wg][seq & 1] = 1;
-      // row of the value-side B tile fed by this token, and its position factor
-      const int kr = 2 * (8 * (4 * tp + (tr >> 4)) + (tr & 7)) + ((tr >> 3) & 1);
-      const float fpos = ldexpf(1.0f, 8 - 2 * code_exp(tr & 7));
-      uint8_t* brow = sm.bw[wg] + (kr >> 3) * 128 + (kr & 7) * 16;
-      float p[G];
-      auto write_weights = [&]() {
-        uint32_t row[N / 2];
-#pragma unroll
-        for (int i = 0; i < N / 2; ++i) row[i] = 0u;
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-          for (int g = 0; g < NG; ++g) {
-            const float v = p[h] * sv[g] * fpos;
-            const __half hi = __float2half_rn(v);
-            const __half lo = __float2half_rn(v - __half2float(hi));
-            row[col_of(g, h, 0, G) >> 1] = h2_bits(hi, lo);
-          }
-#pragma unroll
-        for (int ng = 0; ng < N / 8; ++ng)
-          *reinterpret_cast<uint4*>(brow + 2048 * ng) =
-              make_uint4(row[4 * ng], row[4 * ng + 1], row[4 * ng + 2], row[4 * ng + 3]);
-      };
-#pragma unroll
-      for (int h = 0; h < G; ++h) p[h] = lg[h] == -INFINITY ? 0.0f : ex2(lg[h] - m_ref[h]);
-      write_weights();
-      fence_async_smem();
-      tc_fence_before();
-      bar_sync(1 + wg, WGT);
-      if (sm.flag[wg][seq & 1]) {
-        // a new reference max: recompute this pair's weights, rescale the sums and
-        // the value accumulator (once the previous value MMA has completed)
-        float corr[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float mn = m_ref[h];
-#pragma unroll
-          for (int w = 0; w < 4; ++w) mn = fmaxf(mn, sm.wmax[wg][w][h]);
-          corr[h] = (m_ref[h] == -INFINITY || mn == -INFINITY) ? (mn == -INFINITY ? 1.0f : 0.0f) : ex2(m_ref[h] - mn);
-          m_ref[h] = mn;
-          l_acc[h] *= corr[h];
-#pragma unroll
-          for (int g = 0; g < NG; ++g) u_acc[h][g] *= corr[h];
-          p[h] = lg[h] == -INFINITY ? 0.0f : ex2(lg[h] - m_ref[h]);
-        }
-        write_weights();
-        if (has_acc && !ab) {
-          tc_fence_after();
-          float d[NC <= 8 ? 8 : (NC <= 16 ? 16 : 32)];
-          tmem_ld(tDV + lane_off, d);
-          tc_wait_ld();
-#pragma unroll
-          for (int g = 0; g < NG; ++g)
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-              d[col_of(g, h, 0, G)] *= corr[h];
-              d[col_of(g, h, 1, G)] *= corr[h];
-            }
-          tmem_st_f(tDV + lane_off, d);
-          tc_wait_st();
-        }
-        fence_async_smem();
-        tc_fence_before();
-        bar_sync(1 + wg, WGT);
-      }
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        l_acc[h] += p[h];
-#pragma unroll
-        for (int g = 0; g < NG; ++g) u_acc[h][g] = fmaf(p[h], zv[g], u_acc[h][g]);
-      }
-      if (wt == 0) {
-        if (!ab) {
-          tc_fence_after();
-#pragma unroll
-          for (int s = 0; s < 8; ++s)
-            umma(tDV, tAV + 8 * s, b_desc(bw_addr + 256 * s), idesc_f16<N>(), (has_acc || s > 0) ? 1u : 0u);
-          umma_commit(&sm.mv[wg]);
-        }
-        // every thread has read this stage: refill it with the pair STAGES ahead
-        if (!sm.abort) issue_next();
-      }
-      if (!ab) ++mv_count;
-      has_acc = true;
-    }
-    // ---- end of the segment: this warpgroup's partial, then the CTA's record
-    {
-      float l_tot[G], u_tot[G][NG];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float lw = warp_sum(l_acc[h]);
-        if (lane == 0) sm.red[wg][wiw][h * (1 + NG)] = lw;
-#pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          const float uw = warp_sum(u_acc[h][g]);
-          if (lane == 0) sm.red[wg][wiw][h * (1 + NG) + 1 + g] = uw;
-        }
-      }
-      bar_sync(1 + wg, WGT);
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        l_tot[h] = 0.0f;
-#pragma unroll
-        for (int g = 0; g < NG; ++g) u_tot[h][g] = 0.0f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          l_tot[h] += sm.red[wg][w][h * (1 + NG)];
-#pragma unroll
-          for (int g = 0; g < NG; ++g) u_tot[h][g] += sm.red[wg][w][h * (1 + NG) + 1 + g];
-        }
-      }
-      const bool acc_ok = has_acc && mv_count > 0 && !sm.abort;
-      float d[NC <= 8 ? 8 : (NC <= 16 ? 16 : 32)];
-      if (acc_ok) {
-        if (!mbar_wait(&sm.mv[wg], (mv_count - 1) & 1, limit) && wt == 0) {
-          sm.abort = 1;
-          atomicOr(c.err, ERR_TIMEOUT);
-        }
-        tc_fence_after();
-        tmem_ld(tDV + lane_off, d);
-        tc_wait_ld();
-      }
-      const int g = wt / GK;
-      const float f = ldexpf(1.0f, 16) / wscale;
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float o = 0.0f;
-        if (acc_ok) {
-          if constexpr (NG == 1) {
-            o = fmaf(d[col_of(0, h, 0, G)] + d[col_of(0, h, 1, G)], f, u_tot[h][0]);
-          } else {
-            const float a0 = d[col_of(0, h, 0, G)] + d[col_of(0, h, 1, G)];
-            const float a1 = d[col_of(1, h, 0, G)] + d[col_of(1, h, 1, G)];
-            o = fmaf(g ? a1 : a0, f, g ? u_tot[h][1] : u_tot[h][0]);
-          }
-        }
-        sm.u.fl.o[wg][h][wt] = o;
-      }
-      if (wt < G) {
-        sm.u.fl.ml[wg][wt][0] = acc_ok ? m_ref[wt] : -INFINITY;
-        sm.u.fl.ml[wg][wt][1] = acc_ok ? l_tot[wt] : 0.0f;
-      }
-      tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
-      if (wg == 0) {
-        float* rec = int2_recs + (size_t)S.slot * G * PART;
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float M = -INFINITY;
-#pragma unroll
-          for (int w = 0; w < NWG; ++w) M = fmaxf(M, sm.u.fl.ml[w][h][0]);
-          float o = 0.0f, L = 0.0f;
-#pragma unroll
-          for (int w = 0; w < NWG; ++w) {
-            const float mw = sm.u.fl.ml[w][h][0];
-            if (mw == -INFINITY) continue;
-            const float fw = ex2(mw - M);
-            o = fmaf(sm.u.fl.o[w][h][wt], fw, o);
-            L = fmaf(sm.u.fl.ml[w][h][1], fw, L);
-          }
-          rec[h * PART + wt] = o;
-          if (wt == 0) {
-            rec[h * PART + PARTIAL_M] = M;
-            rec[h * PART + PARTIAL_L] = L;
-          }
-        }
-      }
-      __syncthreads();
-    }
+    int2_pages<G, GK>(c, layer, a.r[S.ri], S.head, S.p0, S.p1, sm.qf[e & 1], sm,
+                      int2_recs + (size_t)S.slot * G * PART, a.dbg.wait_limit, a.front_writes != 0, nc, timed_out);
+    if (e + 1 < nseg) build_qfrag<G, GK>(c, layer, a.r[sm.seg[e + 1].ri], sm.seg[e + 1].head, q, sm, (e + 1) & 1);
   }
-
-  // ---- BF16 blocks: 32-row half-pages in the warpgroups' own ring memory (every
-  // INT2 copy of this CTA has been consumed), unrotated q
-  bool any_bf16 = false;
-  for (int e = 0; e < nseg; ++e) any_bf16 |= sm.seg[e].bf16 != 0;
-  if (any_bf16) {
-    if (a.front_writes) grid_dep_wait();   // the ring pages may hold the token just appended
-    uint32_t phase_bits = 0;               // per stage: parity of its next completion
-    for (int st = 0; st < STAGES; ++st)
-      if (((seq - st + STAGES - 1) / STAGES) & 1) phase_bits |= 1u << st;   // completions so far, per stage
-    for (int e = 0; e < nseg; ++e) {
-      if (!sm.seg[e].bf16) continue;
-      const Seg S = sm.seg[e];
-      const DecodeReq& R = a.r[S.ri];
-      float* qf = reinterpret_cast<float*>(sm.bw[wg]);   // [G][D]
-      const uint16_t* qrow = q + ((size_t)R.batch_row * c.Hq + (size_t)S.head * G) * D;
-      for (int i = wt; i < G * D; i += WGT) qf[i] = __uint_as_float(static_cast<uint32_t>(qrow[i]) << 16);
-      // this warpgroup's half-pages: hp = wg, wg + NWG, ... of the ten, skipping empty ones
-      int hps[10], nh = 0;
-      for (int hp = wg; hp < 10; hp += NWG) {
-        bool any = false;
-        for (int r = 0; r < 32 && !any; ++r) any = bf16_row_valid(R, hp >> 1, 32 * (hp & 1) + r);
-        if (any) hps[nh++] = hp;
-      }
-      auto bf16_src = [&](int hp, int which_kv) -> const uint16_t* {
-        const int which = hp >> 1;
-        int page = which == 0 ? R.sink_page : R.ring_page[which - 1];
-        if (page < 0 || page >= c.n_bf16_pages) {
-          if (wt == 0) atomicOr(c.err, ERR_BF16_PAGE);
-          page = 0;
-        }
-        return c.bf16 + layer * c.bf16_layer_stride + ((size_t)page * c.Hkv + S.head) * BF16_RECORD_ELEMS +
-               (size_t)which_kv * PAGE * D + (size_t)32 * (hp & 1) * D;
-      };
-      // K rows into stage 2 b, V rows into stage 2 b + 1 (8 KB each) for buffer b
-      auto copy_half = [&](int i) {
-        if (wt != 0 || sm.abort) return;
-        const int b = i & 1;
-        mbar_expect_tx(&sm.full[wg][2 * b], 8192);
-        tma_load_1d(sm.ring[wg][2 * b], bf16_src(hps[i], 0), 8192, &sm.full[wg][2 * b]);
-        mbar_expect_tx(&sm.full[wg][2 * b + 1], 8192);
-        tma_load_1d(sm.ring[wg][2 * b + 1], bf16_src(hps[i], 1), 8192, &sm.full[wg][2 * b + 1]);
-        issued_mask |= 3u << (2 * b);
-      };
-      bar_sync(1 + wg, WGT);
-      if (nh > 0) copy_half(0);
-      if (nh > 1) copy_half(1);
-      // online state of heads wiw, wiw + 4 (lane: channels 4 lane .. + 3)
-      float bm[2] = {-INFINITY, -INFINITY}, bl[2] = {0.0f, 0.0f}, bo[2][4] = {};
-      for (int i = 0; i < nh; ++i) {
-        const int b = i & 1, hp = hps[i];
-        bool ok = !sm.abort;
-        if (ok) {
-          ok = mbar_wait(&sm.full[wg][2 * b], (phase_bits >> (2 * b)) & 1, limit) &&
-               mbar_wait(&sm.full[wg][2 * b + 1], (phase_bits >> (2 * b + 1)) & 1, limit);
-          if (!ok && wt == 0) {
-            sm.abort = 1;
-            atomicOr(c.err, ERR_TIMEOUT);
-          }
-        }
-        phase_bits ^= 3u << (2 * b);
-        if (wt == 0) issued_mask &= ~(3u << (2 * b));
-        const uint16_t* kr = reinterpret_cast<const uint16_t*>(sm.ring[wg][2 * b]);
-        const uint16_t* vr = reinterpret_cast<const uint16_t*>(sm.ring[wg][2 * b + 1]);
-        float* lgs = reinterpret_cast<float*>(sm.ring[wg][2 * b] + 8192);   // [G][32]
-        // logits: thread -> row wt / 4, channel quarter wt % 4 (chunks in rotated order)
-        {
-          const int r = wt >> 2, qq = wt & 3;
-          float acc[G];
-#pragma unroll
-          for (int h = 0; h < G; ++h) acc[h] = 0.0f;
-#pragma unroll
-          for (int bb = 0; bb < 4; ++bb) {
-            const int chunk = 4 * qq + ((bb + r) & 3);
-            const uint4 kw = *reinterpret_cast<const uint4*>(kr + (size_t)r * D + 8 * chunk);
-            const uint32_t ww[4] = {kw.x, kw.y, kw.z, kw.w};
-#pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-              const float k0 = __uint_as_float(ww[e2] << 16), k1 = __uint_as_float(ww[e2] & 0xffff0000u);
-              const int chn = 8 * chunk + 2 * e2;
-#pragma unroll
-              for (int h = 0; h < G; ++h) acc[h] = fmaf(qf[h * D + chn + 1], k1, fmaf(qf[h * D + chn], k0, acc[h]));
-            }
-          }
-          const bool okr = ok && bf16_row_valid(R, hp >> 1, 32 * (hp & 1) + r);
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], 1);
-            acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], 2);
-            if (qq == 0) lgs[h * 32 + r] = okr ? acc[h] * (c.scale * LOG2E) : -INFINITY;
-          }
-        }
-        bar_sync(1 + wg, WGT);
-        // softmax and values: warp wiw handles heads wiw, wiw + 4
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int h = wiw + 4 * hh;
-          if (h >= G) continue;
-          const float x = lgs[h * 32 + lane];
-          const float mn = fmaxf(bm[hh], warp_max(x));
-          if (mn == -INFINITY) continue;
-          const float corr = bm[hh] == -INFINITY ? 0.0f : ex2(bm[hh] - mn);
-          const float pv = x == -INFINITY ? 0.0f : ex2(x - mn);
-          bl[hh] = bl[hh] * corr + warp_sum(pv);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) bo[hh][k] *= corr;
-          bm[hh] = mn;
-          for (int r = 0; r < 32; ++r) {
-            const float pr = __shfl_sync(0xffffffffu, pv, r);
-            if (pr == 0.0f) continue;   // rows outside the window may hold anything
-            const uint2 vv = *reinterpret_cast<const uint2*>(vr + (size_t)r * D + 4 * lane);
-            bo[hh][0] = fmaf(pr, __uint_as_float(vv.x << 16), bo[hh][0]);
-            bo[hh][1] = fmaf(pr, __uint_as_float(vv.x & 0xffff0000u), bo[hh][1]);
-            bo[hh][2] = fmaf(pr, __uint_as_float(vv.y << 16), bo[hh][2]);
-            bo[hh][3] = fmaf(pr, __uint_as_float(vv.y & 0xffff0000u), bo[hh][3]);
-          }
-        }
-        bar_sync(1 + wg, WGT);   // every thread is done with buffer b
-        if (i + 2 < nh) copy_half(i + 2);
-      }
-      // this warpgroup's BF16 state -> shared memory; warpgroup 0 combines
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int h = wiw + 4 * hh;
-        if (h >= G) continue;
-        *reinterpret_cast<float4*>(&sm.u.fl.o[wg][h][4 * lane]) = make_float4(bo[hh][0], bo[hh][1], bo[hh][2], bo[hh][3]);
-        if (lane == 0) {
-          sm.u.fl.ml[wg][h][0] = bm[hh];
-          sm.u.fl.ml[wg][h][1] = bl[hh];
-        }
-      }
-      __syncthreads();
-      if (wg == 0) {
-        float* rec = bf16_recs + (size_t)(S.ri * c.Hkv + S.head) * G * PART;
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float M = -INFINITY;
-#pragma unroll
-          for (int w = 0; w < NWG; ++w) M = fmaxf(M, sm.u.fl.ml[w][h][0]);
-          float o = 0.0f, L = 0.0f;
-#pragma unroll
-          for (int w = 0; w < NWG; ++w) {
-            const float mw = sm.u.fl.ml[w][h][0];
-            if (mw == -INFINITY) continue;
-            const float fw = ex2(mw - M);
-            o = fmaf(sm.u.fl.o[w][h][wt], fw, o);
-            L = fmaf(sm.u.fl.ml[w][h][1], fw, L);
-          }
-          rec[h * PART + wt] = o;
-          if (wt == 0) {
-            rec[h * PART + PARTIAL_M] = M;
-            rec[h * PART + PARTIAL_L] = L;
-          }
-        }
-      }
-      __syncthreads();
+  // BF16 pages of the segments whose BF16 block this CTA holds, one four-warp group
+  // per page (every INT2 copy has been consumed: the rings are free)
+  bool any = false;
+  for (int e = 0; e < nseg; ++e) any |= sm.seg[e].bf16 != 0;
+  if (!any) return;
+  if (a.front_writes) grid_dep_wait();   // a ring page may hold the token just appended
+  const int grp = warp / 4;
+  for (int e = 0; e < nseg; ++e) {
+    const Seg S = sm.seg[e];
+    if (!S.bf16) continue;
+    const int s = S.ri * c.Hkv + S.head;
+    if (grp < NGRP) {
+      for (int which = grp; which < BF16_ITEMS; which += NGRP)
+        bf16_item<G, GK>(c, layer, a.r[S.ri], S.head, which, q, sm, grp,
+                         bf16_recs + ((size_t)s * BF16_ITEMS + which) * G * PART);
     }
+    __syncthreads();
   }
-
-  // ---- drain: copies still in flight after an abort land (bounded) before exit
-  if (wt == 0 && sm.abort) {
-    for (int st = 0; st < STAGES; ++st)
-      if (issued_mask & (1u << st)) mbar_wait(&sm.full[wg][st], 0, limit), mbar_wait(&sm.full[wg][st], 1, limit);
-  }
-  if (wt == 0 && mv_count > 0) mbar_wait(&sm.mv[wg], (mv_count - 1) & 1, limit);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (t < 32) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(sm.tmem) : "memory");
 }
 
-// ---- merge: one CTA per segment (request, kv head) --------------------------------------
+// ---- merge: one CTA per (request, query head) -----------------------------------------
+// Warp w folds items w, w + 16, ... (the segment's five BF16 page records, then its
+// INT2 records) into a running (M, L, O_bf16, O_hist) with lane l owning channels
+// 4 l .. 4 l + 3; the warp states are combined, O_hist is rotated back by R_V^T
+// (staged in shared memory before the records are waited for) and the output row
+// written.
+constexpr int MERGE_WARPS = MERGE_THREADS / 32;
+constexpr int MERGE_UNROLL = 8;
 struct MergeSmem {
-  float rvt[D][D];          // R_V^T of the kv head: rvt[j][c] = R_V[c][j]
-  float oh[MAX_G][D];       // merged INT2 part (rotated basis)
-  float ob[MAX_G][D];       // merged BF16 part
-  float L[MAX_G];
+  float rvt[D][D];                     // R_V^T of the kv head: rvt[j][c] = R_V[c][j]
+  __align__(16) float ob[MERGE_WARPS][D];
+  __align__(16) float oh[MERGE_WARPS][D];
+  float m[MERGE_WARPS], l[MERGE_WARPS];
+  float hist[D], bf[D], part[MERGE_THREADS / D][D];
+  float L;
 };
 
 template <int G>
@@ -1088,8 +1001,9 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(DevCache c, int la
                                                               const float* __restrict__ recs, float* __restrict__ out) {
   extern __shared__ __align__(16) uint8_t merge_raw[];
   MergeSmem& sm = *reinterpret_cast<MergeSmem*>(merge_raw);
-  const int s = blockIdx.x, ri = s / c.Hkv, head = s % c.Hkv;
-  const int t = threadIdx.x, ch = t % D, hg = t / D;   // hg: heads hg, hg + 2, ...
+  const int ri = blockIdx.x / c.Hq, hq = blockIdx.x % c.Hq;
+  const int head = hq / G, g = hq % G;
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   {
     // R_V^T is written once at set-up: stage it while the decode grid runs
     const float4* src = reinterpret_cast<const float4*>(c.rot_vt + ((size_t)layer * c.Hkv + head) * D * D);
@@ -1104,7 +1018,8 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(DevCache c, int la
   grid_dep_wait();
   grid_dep_launch();
   const DecodeReq& R = a.r[ri];
-  // the CTAs whose cost ranges meet the segment: c_lo .. c_hi, record slot s + cta
+  const int s = ri * c.Hkv + head;
+  // the CTAs whose cost ranges meet the segment: c_lo .. c_hi
   const int64_t per = (int64_t)R.npages + R.bf16_cost;
   const int64_t s0 = R.cost_start + (int64_t)head * per, s1 = s0 + per;
   int c_lo = static_cast<int>(s0 * a.ncta / a.total_cost);
@@ -1113,37 +1028,97 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(DevCache c, int la
   int c_hi = static_cast<int>((s1 - 1) * a.ncta / a.total_cost);
   while (c_hi > 0 && cta_begin(c_hi, a.ncta, a.total_cost) > s1 - 1) --c_hi;
   while (cta_begin(c_hi + 1, a.ncta, a.total_cost) <= s1 - 1) ++c_hi;
-  const float* int2_recs = recs;
-  const float* bf16_rec = recs + ((size_t)a.n * c.Hkv + a.ncta) * G * PART + (size_t)s * G * PART;
-  for (int h = hg; h < G; h += MERGE_THREADS / D) {
-    float M = -INFINITY;
-    const float mb = __ldcg(bf16_rec + h * PART + PARTIAL_M);
-    M = fmaxf(M, mb);
-    for (int cc = c_lo; cc <= c_hi; ++cc) M = fmaxf(M, __ldcg(int2_recs + ((size_t)(s + cc) * G + h) * PART + PARTIAL_M));
-    float L = 0.0f, oh = 0.0f, ob = 0.0f;
-    if (mb != -INFINITY) {
-      const float f = ex2(mb - M);
-      L = __ldcg(bf16_rec + h * PART + PARTIAL_L) * f;
-      ob = __ldcg(bf16_rec + h * PART + ch) * f;
+  const int items = BF16_ITEMS + (c_hi - c_lo + 1);
+  const float* bf16_recs = recs + ((size_t)a.n * c.Hkv + a.ncta) * G * PART;
+  auto item_ptr = [&](int i) -> const float* {
+    return i < BF16_ITEMS ? bf16_recs + (((size_t)s * BF16_ITEMS + i) * G + g) * PART
+                          : recs + ((size_t)(s + c_lo + i - BF16_ITEMS) * G + g) * PART;
+  };
+  float M = -INFINITY, L = 0.0f;
+  float4 ob = make_float4(0.0f, 0.0f, 0.0f, 0.0f), oh = ob;
+  for (int i0 = w; i0 < items; i0 += MERGE_WARPS * MERGE_UNROLL) {
+    float mv[MERGE_UNROLL], lv[MERGE_UNROLL];
+    float4 ov[MERGE_UNROLL];
+#pragma unroll
+    for (int u = 0; u < MERGE_UNROLL; ++u) {
+      const int i = i0 + MERGE_WARPS * u;
+      if (i < items) {
+        const float* p = item_ptr(i);
+        mv[u] = __ldcg(p + PARTIAL_M);
+        lv[u] = __ldcg(p + PARTIAL_L);
+        ov[u] = __ldcg(reinterpret_cast<const float4*>(p) + lane);
+      } else {
+        mv[u] = -INFINITY;
+        lv[u] = 0.0f;
+        ov[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
     }
-    for (int cc = c_lo; cc <= c_hi; ++cc) {
-      const float* rp = int2_recs + ((size_t)(s + cc) * G + h) * PART;
-      const float m = __ldcg(rp + PARTIAL_M);
-      if (m == -INFINITY) continue;
-      const float f = ex2(m - M);
-      L = fmaf(__ldcg(rp + PARTIAL_L), f, L);
-      oh = fmaf(__ldcg(rp + ch), f, oh);
+    float mn = M;
+#pragma unroll
+    for (int u = 0; u < MERGE_UNROLL; ++u) mn = fmaxf(mn, mv[u]);
+    if (mn > M) {
+      const float f = (M == -INFINITY) ? 0.0f : exp2f(M - mn);
+      L *= f;
+      ob.x *= f; ob.y *= f; ob.z *= f; ob.w *= f;
+      oh.x *= f; oh.y *= f; oh.z *= f; oh.w *= f;
+      M = mn;
     }
-    sm.oh[h][ch] = oh;
-    sm.ob[h][ch] = ob;
-    if (ch == 0) sm.L[h] = L;
+#pragma unroll
+    for (int u = 0; u < MERGE_UNROLL; ++u) {
+      const float f = (mv[u] == -INFINITY) ? 0.0f : exp2f(mv[u] - M);
+      L = fmaf(lv[u], f, L);
+      const bool is_bf = i0 + MERGE_WARPS * u < BF16_ITEMS;
+      const float fb = is_bf ? f : 0.0f, fh = is_bf ? 0.0f : f;
+      ob.x = fmaf(ov[u].x, fb, ob.x);
+      ob.y = fmaf(ov[u].y, fb, ob.y);
+      ob.z = fmaf(ov[u].z, fb, ob.z);
+      ob.w = fmaf(ov[u].w, fb, ob.w);
+      oh.x = fmaf(ov[u].x, fh, oh.x);
+      oh.y = fmaf(ov[u].y, fh, oh.y);
+      oh.z = fmaf(ov[u].z, fh, oh.z);
+      oh.w = fmaf(ov[u].w, fh, oh.w);
+    }
+  }
+  reinterpret_cast<float4*>(sm.ob[w])[lane] = ob;
+  reinterpret_cast<float4*>(sm.oh[w])[lane] = oh;
+  if (lane == 0) {
+    sm.m[w] = M;
+    sm.l[w] = L;
   }
   __syncthreads();
-  for (int h = hg; h < G; h += MERGE_THREADS / D) {
-    float acc = sm.ob[h][ch];
-#pragma unroll 8
-    for (int j = 0; j < D; ++j) acc = fmaf(sm.oh[h][j], sm.rvt[j][ch], acc);
-    out[((size_t)R.batch_row * c.Hq + (size_t)head * G + h) * D + ch] = acc / sm.L[h];
+  if (t < D) {
+    float Mt = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < MERGE_WARPS; ++k) Mt = fmaxf(Mt, sm.m[k]);
+    float Lt = 0.0f, b = 0.0f, h = 0.0f;
+#pragma unroll
+    for (int k = 0; k < MERGE_WARPS; ++k) {
+      const float f = (sm.m[k] == -INFINITY) ? 0.0f : exp2f(sm.m[k] - Mt);
+      Lt = fmaf(sm.l[k], f, Lt);
+      b = fmaf(sm.ob[k][t], f, b);
+      h = fmaf(sm.oh[k][t], f, h);
+    }
+    sm.bf[t] = b;
+    sm.hist[t] = h;
+    if (t == 0) sm.L = Lt;
+  }
+  __syncthreads();
+  {
+    // out_c = O_bf16_c + sum_j O_hist_j R_V^T[j][c]; thread (quarter q, c) sums rows
+    // 32 q .. 32 q + 31
+    constexpr int ROWS = D * D / MERGE_THREADS;
+    const int ch = t & (D - 1), qr = t / D;
+    float acc = 0.0f;
+#pragma unroll
+    for (int j = ROWS * qr; j < ROWS * qr + ROWS; ++j) acc = fmaf(sm.hist[j], sm.rvt[j][ch], acc);
+    sm.part[qr][ch] = acc;
+  }
+  __syncthreads();
+  if (t < D) {
+    float v = 0.0f;
+#pragma unroll
+    for (int k = 0; k < MERGE_THREADS / D; ++k) v += sm.part[k][t];
+    out[((size_t)R.batch_row * c.Hq + hq) * D + t] = (sm.bf[t] + v) / sm.L;
   }
 }
 
@@ -1151,7 +1126,7 @@ template <int G, int GK>
 cudaError_t launch_decode_t(const DevCache& c, int layer, const DecodeReq* reqs, const DecodePlan& p,
                             const uint16_t* q, float* out, void* workspace, bool front_writes, DecodeDebug dbg,
                             cudaStream_t s) {
-  using Cf = Cfg<G, GK>;
+  static_assert(sizeof(Smem<G, GK>) <= 227 * 1024, "shared memory");
   static unsigned attr_done = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1178,14 +1153,14 @@ cudaError_t launch_decode_t(const DevCache& c, int layer, const DecodeReq* reqs,
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.ncta));
-  cfg.blockDim = dim3(Cf::THREADS);
+  cfg.blockDim = dim3(Tune<G, GK>::THREADS);
   cfg.dynamicSmemBytes = sizeof(Smem<G, GK>);
   cfg.stream = s;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, decode_kernel<G, GK>, c, layer, a, q, recs);
   if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3(static_cast<unsigned>(p.segments));
+  cfg.gridDim = dim3(static_cast<unsigned>(p.n * c.Hq));
   cfg.blockDim = dim3(MERGE_THREADS);
   cfg.dynamicSmemBytes = sizeof(MergeSmem);
   return cudaLaunchKernelEx(&cfg, merge_kernel<G>, c, layer, a, static_cast<const float*>(recs), out);

@@ -585,7 +585,7 @@ DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int
     ncta = std::min<int64_t>(cost, 2 * ncta);
   }
   p.ncta = static_cast<int>(ncta);
-  p.partial_bytes = align256((size_t)(2 * p.segments + ncta) * decode_record_bytes(c->G()));
+  p.partial_bytes = align256((size_t)((1 + DECODE_BF16_ITEMS) * p.segments + ncta) * decode_record_bytes(c->G()));
   return p;
 }
 
@@ -603,11 +603,12 @@ int32_t decode_launch_size(const oscar_cache* c, int32_t layer, int32_t n, const
   return per;
 }
 
-// Workspace of a decode of n requests, whatever their lengths: per launch two
-// records per (request, kv head) and one per CTA (at most four per SM).
+// Workspace of a decode of n requests, whatever their lengths: per launch one INT2
+// record and five BF16 page records per (request, kv head), and one INT2 record
+// per CTA (at most four per SM).
 size_t decode_bytes_bound(const oscar_cache* c, int32_t n) {
   const int64_t segs = (int64_t)std::min<int32_t>(n, DECODE_PER_LAUNCH) * c->cfg.num_kv_heads;
-  return align256((size_t)(2 * segs + 4 * (int64_t)c->num_sms) * decode_record_bytes(c->G()));
+  return align256((size_t)((1 + DECODE_BF16_ITEMS) * segs + 4 * (int64_t)c->num_sms) * decode_record_bytes(c->G()));
 }
 
 size_t decode_bytes_needed(const oscar_cache* c, int32_t layer, int32_t n, const int32_t* reqs) {

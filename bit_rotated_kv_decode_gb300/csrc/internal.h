@@ -145,10 +145,10 @@ struct DecodePlan {
   int64_t total_cost;
   int64_t segments;        // n Hkv
   int worst_segments;      // most segments one CTA touches
-  size_t partial_bytes;    // workspace: INT2 records (segments + ncta) then BF16 records (segments)
+  size_t partial_bytes;    // workspace: INT2 records (segments + ncta), then BF16 page records (5 segments)
 };
-// Partial record of one (segment, CTA) or one segment's BF16 block: per query head
-// of the group o[128], m (log2 domain), l.
+// Partial record of one (segment, CTA) or of one BF16 page of a segment: per query
+// head of the group o[128], m (log2 domain), l.
 inline size_t decode_record_bytes(int g) { return (size_t)g * PARTIAL_FLOATS * sizeof(float); }
 // Failure-detection hooks of a launch: mbarrier wait rounds before a wait gives up
 // (ERR_TIMEOUT), and a page pair whose copy CTA 0's first warpgroup never issues

@@ -127,7 +127,6 @@ struct PrefillSmem {
   __align__(16) uint16_t kb[2][PF_TILE][PF_PITCH];  // the tile as bf16, double-buffered (zero rows past its end)
   __align__(16) float xs[PF_TILE][D + 4];       // rotated values (row pad: no bank conflicts)
   float kn[PF_TILE];                            // |k|^2 of each token, rounded up
-  __align__(16) uint8_t vb[PF_TILE][CODE_BYTES];  // V: the tile's packed codes (token j, lane l's byte)
   int32_t page;                                 // id of the history page holding the tile
 };
 constexpr size_t PREFILL_SMEM = sizeof(PrefillSmem);
@@ -171,8 +170,7 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_
 // Block x of the history of one kv head (y), K or V (z): tiles
 // [x tiles_per_cta, (x + 1) tiles_per_cta) of the launch.  Tile i covers history
 // slots [PF_TILE (k0 + i), PF_TILE (k0 + i + 1)) -- aligned to PF_TILE, so a tile
-// lies in one page and no two tiles share a byte of channel-major V codes --
-// restricted to the positions [h0, h1) being written.  The launch sizes the grid
+// lies in one page -- restricted to the positions [h0, h1) being written.  The launch sizes the grid
 // to two resident blocks per SM, so R is split and staged once per block.
 template <int GK>
 __global__ void __launch_bounds__(PF_THREADS, 2) prefill_hist_kernel(DevCache c, int layer, int slot,
@@ -326,37 +324,8 @@ __global__ void __launch_bounds__(PF_THREADS, 2) prefill_hist_kernel(DevCache c,
         if (lane == 0) atomicOr(c.err, ERR_INT2_PAGE);
         continue;
       }
-      uint8_t* rec = c.int2 + layer * c.int2_layer_stride + ((size_t)page * c.Hkv + head) * record_for(GK);
-      if (which)
-        sm.vb[j][lane] = static_cast<uint8_t>(g.byte);
-      else
-        rec[K_CODES_OFF + row * CODE_BYTES + lane] = static_cast<uint8_t>(g.byte);
-      store_group_meta<GK>(rec, which, row, g);
-    }
-    if (which) {
-      // channel-major V codes of the tile: thread t -> channel t / 2, slots
-      // 16 (t % 2) .. + 15 of the tile (one word); words the tile covers only in
-      // part keep the other slots' codes
-      __syncthreads();
-      const int32_t page = sm.page;
-      if (page >= 0 && page < c.n_int2_pages) {
-        const int ch = t >> 1, q = t & 1;
-        uint32_t word = 0u, mask = 0u;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int j = 16 * q + i;
-          if (j >= jlo && j < jhi) {
-            word |= ((static_cast<uint32_t>(sm.vb[j][ch >> 2]) >> (2 * (ch & 3))) & 3u) << (2 * i);
-            mask |= 3u << (2 * i);
-          }
-        }
-        if (mask != 0u) {
-          uint8_t* rec = c.int2 + layer * c.int2_layer_stride + ((size_t)page * c.Hkv + head) * record_for(GK);
-          const int slot0 = static_cast<int>((t0 - SINK) % PAGE) + 16 * q;   // a multiple of 16
-          uint32_t* p = reinterpret_cast<uint32_t*>(rec + V_CODES_OFF) + 4 * ch + (slot0 >> 4);
-          *p = mask == 0xffffffffu ? word : ((*p & ~mask) | word);
-        }
-      }
+      store_group_code_t<GK>(c.int2 + layer * c.int2_layer_stride + ((size_t)page * c.Hkv + head) * record_for(GK),
+                             which, row, g);
     }
   }
 }

@@ -8,7 +8,7 @@ tokens, INT2 history in between, paged like a standard paged KV cache.
 Readings (the pages give no byte layout):
   * a page holds 64 tokens; one INT2 page-head record is 4608 bytes:
       [   0, 2048) K codes, token slot r at r*32 (32 bytes = 128 codes)
-      [2048, 4096) V codes, channel c at 2048 + 16c (channel-major, below)
+      [2048, 4096) V codes, same layout
       [4096, 4352) K meta, slot r at 4096 + 4r: fp16 s then fp16 z
       [4352, 4608) V meta, same layout
     i.e. 72 bytes = 2.25 bits per element per token-head;
@@ -16,13 +16,7 @@ Readings (the pages give no byte layout):
     as above, then K meta [4096, 4608) with slot r at 4096 + 8r holding group
     0's fp16 s, z then group 1's, and V meta [4608, 5120) the same way; 80
     bytes = 2.5 bits per element per token-head;
-  * K codes token-major, in the rotated channel order: a slot's 32 bytes hold
-    channel 4j+i in bits 2i..2i+1 of byte j;
-  * V codes channel-major: rotated channel c owns the 16 bytes at 16c of the V
-    code region, and token slot r sits in bits 2(r%4)..2(r%4)+1 of byte r//4
-    (four token slots of one channel per byte).  The pages fix only "four 2-bit
-    values per byte"; packing V by channel keeps one channel's codes of a page
-    contiguous, which is the order the value contraction consumes them in;
+  * codes in the rotated channel order, channel 4j+i in bits 2i..2i+1 of byte j;
   * BF16 pages hold [2][64][128] bf16 per head (K rows then V rows); the
     recent window is a ring: position p >= 64 lives in ring slot (p-64) mod 256,
     i.e. ring page slot//64, row slot%64; sink position p < 64 in sink row p.
@@ -91,35 +85,13 @@ def meta_bytes(s: np.ndarray, z: np.ndarray, groups: int = 1) -> np.ndarray:
     return out.reshape(out.shape[:-2] + (4 * out.shape[-2],))
 
 
-V_CHANNEL_BYTES = PAGE_TOKENS // 4   # 16 bytes of V codes per channel and page
-
-
-def pack_v_codes_page(codes: np.ndarray) -> np.ndarray:
-    """V codes of one page, uint8 [64 slots][128 channels] in 0..3 -> the 2048-byte
-    channel-major V code region: channel c at 16c, slot r in bits 2(r%4) of byte r//4."""
-    c = np.asarray(codes, dtype=np.uint32).T.reshape(HEAD_DIM, V_CHANNEL_BYTES, 4)
-    b = np.zeros((HEAD_DIM, V_CHANNEL_BYTES), dtype=np.uint32)
-    for i in range(4):
-        b |= c[..., i] << (2 * i)
-    return b.astype(np.uint8).reshape(-1)
-
-
-def v_slot_codes(v_region: np.ndarray, slot: int) -> np.ndarray:
-    """The 128 V codes (channel order) of token slot ``slot`` from a 2048-byte
-    channel-major V code region."""
-    v = np.asarray(v_region, dtype=np.uint8).reshape(HEAD_DIM, V_CHANNEL_BYTES)
-    return ((v[:, slot // 4] >> (2 * (slot % 4))) & 3).astype(np.uint8)
-
-
 def record_slot_fields(record: np.ndarray, slot: int, group: int = 128):
-    """Split one page-head record at token slot -> (kc, vc, kmeta, vmeta).
-
-    kc and vc are the slot's codes packed token-major (32 bytes, channel 4j+i in
-    bits 2i of byte j); vc is gathered from the channel-major V region."""
+    """Split one page-head record at token slot -> (kc, vc, kmeta, vmeta): the
+    slot's packed K and V codes (32 bytes each) and its K and V meta bytes."""
     lay = record_layout(group)
     mb = lay["meta_bytes"]
     kc = record[K_CODES_OFF + slot * CODE_BYTES: K_CODES_OFF + (slot + 1) * CODE_BYTES]
-    vc = pack_codes(v_slot_codes(record[V_CODES_OFF: V_CODES_OFF + PAGE_TOKENS * CODE_BYTES], slot))
+    vc = record[V_CODES_OFF + slot * CODE_BYTES: V_CODES_OFF + (slot + 1) * CODE_BYTES]
     km = record[lay["k_meta"] + slot * mb: lay["k_meta"] + (slot + 1) * mb]
     vm = record[lay["v_meta"] + slot * mb: lay["v_meta"] + (slot + 1) * mb]
     return kc, vc, km, vm

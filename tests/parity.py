@@ -103,20 +103,14 @@ def check_output(got: np.ndarray, ref: np.ndarray):
 
 def slot_bytes(records, rows: int, group: int = 128) -> np.ndarray:
     """What token slots 0..rows-1 of page-head records hold, uint8 [heads][...]:
-    their K codes and K / V meta (token-major regions) and their V codes
-    (gathered from the channel-major region).  Bits of slots past ``rows`` (never
-    written, arbitrary) are left out, so two caches compare equal exactly when
-    their written tokens do."""
+    their K and V codes and K / V meta.  Slots past ``rows`` (never written,
+    arbitrary) are left out, so two caches compare equal exactly when their
+    written tokens do."""
     recs = np.asarray(records, dtype=np.uint8)
-    lay = layout.record_layout(group)
-    mb = lay["meta_bytes"]
     out = []
     for rec in recs.reshape(-1, recs.shape[-1]):
-        v = rec[lay["v_codes"]: lay["v_codes"] + 2048]
-        vcodes = np.stack([layout.v_slot_codes(v, r) for r in range(rows)]) if rows else np.zeros((0, 128), np.uint8)
-        out.append(np.concatenate([rec[lay["k_codes"]: lay["k_codes"] + 32 * rows], vcodes.reshape(-1),
-                                   rec[lay["k_meta"]: lay["k_meta"] + mb * rows],
-                                   rec[lay["v_meta"]: lay["v_meta"] + mb * rows]]))
+        f = [layout.record_slot_fields(rec, r, group) for r in range(rows)]
+        out.append(np.concatenate([np.concatenate(x) for x in zip(*f)]) if rows else np.zeros(0, np.uint8))
     return np.stack(out)
 
 

@@ -231,8 +231,9 @@ def test_fork_shares_prefix_pages(b):
     parity.check_output(out[0].cpu().numpy(), s.oracle_decode(ch, 0, q[0]))
 
 
-@pytest.mark.parametrize("hq", [32, 64])
+@pytest.mark.parametrize("hq", [8, 16, 32, 64])
 def test_ragged_batch_two_layers_shuffled_pages(b, hq):
+    # every GQA group size the cache accepts (1, 2, 4, 8 query heads per kv head)
     s = Setup(b, layers=2, hq=hq, hkv=8, max_req=6, max_pages=64, pages=400, seed=0xC0FFEE)
     lengths = [30, 320, 1700, 449, 2600]
     reqs = [s.open() for _ in lengths]

@@ -31,31 +31,17 @@ def test_closed_form_four_levels_and_byte_order():
     assert np.array_equal(layout.unpack_codes(packed), c)
 
 
-def test_v_codes_channel_major_closed_form():
-    """V code region: channel c owns 16 bytes at 16c, slot r in bits 2(r%4) of byte r//4.
-    Slot r of channel c carries (r + c) % 4 here, so each byte is a fixed closed form:
-    byte j of channel c holds codes (4j + i + c) % 4 at bits 2i."""
-    r = np.arange(64)[:, None]
-    c = np.arange(128)[None, :]
-    codes = ((r + c) % 4).astype(np.uint8)                      # [slot][channel]
-    region = layout.pack_v_codes_page(codes)
-    assert region.shape == (2048,)
-    for ch in (0, 1, 2, 3, 77, 127):
-        want = sum(((i + ch) % 4) << (2 * i) for i in range(4))  # independent of j: 4j = 0 mod 4
-        assert np.all(region[16 * ch: 16 * ch + 16] == want)
-    # round trip per slot, and a brute-force bit read of one entry
-    for slot in (0, 1, 5, 31, 62, 63):
-        assert np.array_equal(layout.v_slot_codes(region, slot), codes[slot])
-    rng = np.random.default_rng(5)
-    rnd = rng.integers(0, 4, size=(64, 128)).astype(np.uint8)
-    reg = layout.pack_v_codes_page(rnd)
-    for slot, ch in ((7, 3), (40, 100), (63, 127)):
-        byte = int(reg[16 * ch + slot // 4])
-        assert (byte >> (2 * (slot % 4))) & 3 == rnd[slot, ch]
-    rec = np.zeros(4608, np.uint8)
-    rec[2048:4096] = reg
+def test_record_slot_fields_offsets():
+    """A slot's fields sit at 32 r (K codes), 2048 + 32 r (V codes), 4096 + 4 r and
+    4352 + 4 r (meta) of a 4608-byte record; with G_K = 64 the meta is 8 bytes per
+    slot at 4096 + 8 r and 4608 + 8 r."""
+    rec = np.arange(4608, dtype=np.int64).astype(np.uint8)
     kc, vc, km, vm = layout.record_slot_fields(rec, 9)
-    assert np.array_equal(layout.unpack_codes(vc), rnd[9])
+    assert np.array_equal(kc, rec[288:320]) and np.array_equal(vc, rec[2048 + 288:2048 + 320])
+    assert np.array_equal(km, rec[4096 + 36:4096 + 40]) and np.array_equal(vm, rec[4352 + 36:4352 + 40])
+    rec64 = np.arange(5120, dtype=np.int64).astype(np.uint8)
+    kc, vc, km, vm = layout.record_slot_fields(rec64, 9, group=64)
+    assert np.array_equal(km, rec64[4096 + 72:4096 + 80]) and np.array_equal(vm, rec64[4608 + 72:4608 + 80])
 
 
 def test_round_half_to_even_ties():
