@@ -42,9 +42,11 @@
 // Pages are staged HBM -> shared memory by TMA bulk copies (cp.async.bulk, one
 // record per page and kv head) into a per-warp ring, completion on mbarriers;
 // every wait is bounded and reports ERR_TIMEOUT instead of hanging.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <type_traits>
 
 #include "internal.h"
@@ -205,9 +207,8 @@ template <int G, int GK>
 struct Smem {
   static constexpr int NW = Tune<G, GK>::NW;
   static constexpr int NPART = Tune<G, GK>::THREADS / D;   // row parts of the q rotation
-  static constexpr int NGRP = NW / 4;                      // four-warp groups (BF16 pages)
   // INT2: per-warp TMA rings; at the end of a segment (every copy consumed): the
-  // warps' states; BF16 pages: group g's K and V rows in the rings of its warps
+  // warps' states; BF16 sub-pages: each warp's K and V rows in its ring
   union {
     __align__(128) uint8_t ring[NW][STAGES][record_for(GK)];
     float state[NW][G][PART];
@@ -218,11 +219,10 @@ struct Smem {
       float part[NPART][G][D];
       float norm[G];
     } pro;                              // rotation of q
-    float bf[NGRP][G][D + PAGE];        // BF16 pages: q (unrotated), then the page's logits
   } scr;
-  uint32_t qf[2][QFrag<G>::WORDS];      // q operands of segment e in slot e & 1
+  __align__(16) uint32_t qf[2][QFrag<G>::WORDS];   // q operands of segment e in slot e & 1 (read as uint4)
   __align__(8) uint64_t bar[NW][STAGES];
-  __align__(16) float4 meta[NW][PAGE];   // INT2: per token {s_k, z_k, s_v 2^ew, z_v} of the page
+  __align__(16) float4 meta[NW][PAGE];   // INT2: per token {s_k, z_k, s_v 2^ew, z_v}; BF16: weights
   __align__(16) float4 meta2[NW][GK == 64 ? PAGE : 1];   // G_K = 64: the same for group 1
   WeightRows<G, GK, NW> w;
   int nseg;
@@ -322,6 +322,43 @@ __device__ void build_qfrag(const DevCache& c, int layer, const DecodeReq& R, in
   __syncthreads();
 }
 
+// The first STAGES page copies of warp w's share of a segment's pages [p0, p1)
+// (pages p0 + w + NW j, j < STAGES), by lane 0, into stages nc + j; the hot page
+// (written by a preceding fused append) only once that grid has completed.
+template <int G, int GK>
+__device__ __forceinline__ void int2_issue_first(const DevCache& c, int layer, const DecodeReq& R, int head, int p0,
+                                                 int p1, Smem<G, GK>& sm, bool front_writes, uint32_t nc) {
+  constexpr int NW = Tune<G, GK>::NW;
+  constexpr int REC = record_for(GK);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane != 0) return;
+  const int32_t* pt = c.hist_pt + (size_t)R.slot * c.max_pages;
+  const uint8_t* base = c.int2 + layer * c.int2_layer_stride + (size_t)head * REC;
+  int32_t ids[STAGES];
+#pragma unroll
+  for (int j = 0; j < STAGES; ++j) {
+    const int pi = p0 + warp + NW * j;
+    ids[j] = (pi < p1 && !(front_writes && pi == R.hot_page)) ? __ldcg(pt + pi) : 0;
+  }
+#pragma unroll
+  for (int j = 0; j < STAGES; ++j) {
+    const int pi = p0 + warp + NW * j;
+    if (pi >= p1) break;
+    int32_t id = ids[j];
+    if (front_writes && pi == R.hot_page) {
+      grid_dep_wait();
+      id = __ldcg(pt + pi);
+    }
+    if (id < 0 || id >= c.n_int2_pages) {
+      atomicOr(c.err, ERR_INT2_PAGE);
+      id = 0;
+    }
+    const int st = (nc + j) % STAGES;
+    mbar_expect_tx(&sm.bar[warp][st], REC);
+    tma_load_1d(sm.buf.ring[warp][st], base + (size_t)id * c.Hkv * REC, REC, &sm.bar[warp][st]);
+  }
+}
+
 // The INT2 pages [p0, p1) of one (request, kv head) segment that this CTA holds:
 // warp w takes pages p0 + w, p0 + w + NW, ... through its TMA ring (copy number
 // nc counts the copies this warp has consumed so far, across segments); qf holds
@@ -331,7 +368,7 @@ template <int G, int GK>
 __device__ __forceinline__ void int2_pages(const DevCache& c, int layer, const DecodeReq& R, int head, int p0,
                                            int p1, const uint32_t* __restrict__ qf, Smem<G, GK>& sm,
                                            float* part_out, uint32_t limit, bool front_writes, uint32_t& nc,
-                                           bool& timed_out) {
+                                           bool& timed_out, bool first_issued) {
   constexpr int NW = Tune<G, GK>::NW;
   constexpr int NT = QFrag<G>::NT;       // n-tiles of 8 columns = 4 heads x (hi, lo)
   constexpr int REC = record_for(GK);
@@ -384,8 +421,10 @@ __device__ __forceinline__ void int2_pages(const DevCache& c, int layer, const D
       tma_load_1d(sm.buf.ring[warp][st], src, REC, &sm.bar[warp][st]);
     }
   };
+  if (!first_issued) {
 #pragma unroll
-  for (int j = 0; j < STAGES; ++j) issue(j);
+    for (int j = 0; j < STAGES; ++j) issue(j);
+  }
   // weights p * s_v are prescaled by 2^ew so the smallest ones stay representable in
   // fp16: s_v <= fp16(2 tau_V / 3) and p <= 2^LAZY_MAX, so p s_v 2^ew <= 2^15
   int ew;
@@ -766,127 +805,234 @@ __device__ __forceinline__ void int2_pages(const DevCache& c, int layer, const D
   __syncthreads();   // states read before the rings take the next segment's copies
 }
 
-// One BF16 page (the sink page, or one of the four recent-ring pages) of one
-// (request, kv head), with the unrotated q, by the four-warp group grp of the CTA:
-// its K and V rows go to the rings of the group's warps, q and the logits to the
-// group's scratch rows.  Partial for every query head of the group.
-template <int G, int GK>
-__device__ __forceinline__ void bf16_item(const DevCache& c, int layer, const DecodeReq& R, int head, int which,
-                                          const uint16_t* __restrict__ q, Smem<G, GK>& sm, int grp,
-                                          float* part_out) {
-  constexpr int THREADS = 128, WARPS = 4;
-  const int t = threadIdx.x - THREADS * grp;
-  const int warp = t >> 5, lane = t & 31;
-  uint16_t (*kr)[D] = reinterpret_cast<uint16_t (*)[D]>(&sm.buf.ring[WARPS * grp][0][0]);
-  uint16_t (*vr)[D] = kr + PAGE;
-  float (*qs)[D + PAGE] = sm.scr.bf[grp];
-  auto group_sync = [&]() { bar_sync(1 + grp, THREADS); };
-  const float scale2 = c.scale * LOG2E;
+// ---- BF16 sink and recent pages ------------------------------------------------------
+constexpr int BF_SUB = 16;                   // rows per sub-page (one k-step of P V)
+constexpr int BF_SUBS = BF16_ITEMS * PAGE / BF_SUB;   // 20 sub-pages per segment
+constexpr int BF_PITCH = D + 8;              // bf16 per staged row: ldmatrix without bank conflicts
+constexpr int BF_WPITCH = BF_SUB + 8;        // bf16 per weight column
+struct BfStage {
+  __align__(16) uint16_t k[BF_SUB][BF_PITCH];
+  __align__(16) uint16_t v[BF_SUB][BF_PITCH];
+};
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  const uint32_t d = smem_u32(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm4_t(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint16_t bf16_bits(float x) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  return *reinterpret_cast<const uint16_t*>(&h);
+}
+
+// Whether BF16 row r of item `which` (0 sink, 1..4 ring pages) holds a cached token:
+// sink rows [0, min(T, 64)); ring slot s = 64 (which - 1) + r holds position
+// he + ((s - (he - 64)) mod 256), cached while below T.
+__device__ __forceinline__ bool bf16_row_valid(const DecodeReq& R, int which, int r) {
   const int T = R.tokens, he = R.hist_end;
-  // select chain, not an indexed load: a dynamic index would put R in local memory
-  int page = which == 0 ? R.sink_page
-           : which == 1 ? R.ring_page[0]
-           : which == 2 ? R.ring_page[1]
-           : which == 3 ? R.ring_page[2]
-                        : R.ring_page[3];
-  if (page < 0 || page >= c.n_bf16_pages) {
-    if (t == 0) atomicOr(c.err, ERR_BF16_PAGE);
-    page = 0;
+  if (which == 0) return r < min(T, SINK);
+  if (T <= SINK) return false;
+  const int s = PAGE * (which - 1) + r;
+  const int p = he + ((s - (he - SINK)) % RECENT + RECENT) % RECENT;
+  return p < T;
+}
+
+// The sink page and the four recent-ring pages of one (request, kv head), with the
+// unrotated q, as 16-row sub-pages spread over the CTA's warps (warp w takes
+// sub-pages w, w + NW, ... of the twenty; a sub-page without a cached row is
+// skipped).  q K^T and P V run on mma.sync m16n8k16 bf16 with fp32 accumulation: q
+// is exact in bf16, P is carried as bf16 hi + lo, so every product is exact.  Rows
+// outside the window are zero-filled by the copies and masked.  The CTA's partial
+// for every query head of the group goes to part_out.  Each warp stages its rows
+// in its own (consumed) TMA ring and its weights in its meta rows.
+template <int G, int GK>
+__device__ void bf16_block(const DevCache& c, int layer, const DecodeReq& R, int head,
+                           const uint16_t* __restrict__ q, Smem<G, GK>& sm, float* part_out) {
+  constexpr int NW = Tune<G, GK>::NW;
+  constexpr int NT = QFrag<G>::NT;
+  static_assert(sizeof(BfStage) <= STAGES * record_for(GK), "BF16 stage in the ring");
+  static_assert(NT * 8 * BF_WPITCH * 2 <= PAGE * sizeof(float4), "BF16 weights in the meta rows");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tid = lane & 3;
+  const float scale2 = c.scale * LOG2E;
+  BfStage& sg = *reinterpret_cast<BfStage*>(sm.buf.ring[warp][0]);
+  uint16_t (*wc)[8][BF_WPITCH] = reinterpret_cast<uint16_t (*)[8][BF_WPITCH]>(&sm.meta[warp][0]);
+  // q as the B operand of K q^T: column n of n-tile nt is query head 4 nt + (n >> 1)
+  // (each head twice), k-step s, registers (b0, b1)
+  uint32_t bq[NT][8][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int g = 4 * nt + (gid >> 1);
+    const uint16_t* qh = q + ((size_t)R.batch_row * c.Hq + (size_t)head * G + (g < G ? g : 0)) * D;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      const uint32_t x0 = *reinterpret_cast<const uint32_t*>(qh + 16 * s + 2 * tid);
+      const uint32_t x1 = *reinterpret_cast<const uint32_t*>(qh + 16 * s + 2 * tid + 8);
+      bq[nt][s][0] = g < G ? x0 : 0u;
+      bq[nt][s][1] = g < G ? x1 : 0u;
+    }
   }
-  // validity of row r: sink rows [0, min(T, 64)); ring slot s = 64 (which-1) + r holds
-  // position he + ((s - (he - 64)) mod 256), valid when below T
-  auto row_valid = [&](int r) -> bool {
-    if (which == 0) return r < min(T, SINK);
-    if (T <= SINK) return false;
-    const int s = PAGE * (which - 1) + r;
-    const int p = he + ((s - (he - SINK)) % RECENT + RECENT) % RECENT;
-    return p < T;
-  };
-  {
-    const uint16_t* qrow = q + ((size_t)R.batch_row * c.Hq + (size_t)head * G) * D;
-    for (int i = t; i < G * D; i += THREADS) qs[i / D][i % D] = __uint_as_float(static_cast<uint32_t>(qrow[i]) << 16);
+  float o[NT][8][4];
+  float m_run[NT], l_run[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    m_run[nt] = -INFINITY;
+    l_run[nt] = 0.0f;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[nt][mt][e] = 0.0f;
   }
-  const uint16_t* src = c.bf16 + layer * c.bf16_layer_stride + ((size_t)page * c.Hkv + head) * BF16_RECORD_ELEMS;
-  constexpr int LOADS = PAGE * (D / 8) / THREADS;
-  uint4 kk[LOADS], vv[LOADS];
+  const int arow = (lane & 7) + 8 * ((lane >> 3) & 1), acol = 8 * (lane >> 4);   // K as A (ldmatrix)
+  const int vrow = (lane & 7) + 8 * (lane >> 4), vcol = 8 * ((lane >> 3) & 1);   // V^T as A (ldmatrix.trans)
+  for (int sp = warp; sp < BF_SUBS; sp += NW) {
+    const int which = sp / (PAGE / BF_SUB), r0 = BF_SUB * (sp % (PAGE / BF_SUB));
+    // rows of this sub-page holding a cached token (bit i: row r0 + i); lanes 0..15 test one row each
+    const uint32_t rows = __ballot_sync(0xffffffffu, lane < BF_SUB && bf16_row_valid(R, which, r0 + lane)) & 0xffffu;
+    if (rows == 0u) continue;
+    int page = which == 0 ? R.sink_page
+             : which == 1 ? R.ring_page[0]
+             : which == 2 ? R.ring_page[1]
+             : which == 3 ? R.ring_page[2]
+                          : R.ring_page[3];
+    if (page < 0 || page >= c.n_bf16_pages) {
+      if (lane == 0) atomicOr(c.err, ERR_BF16_PAGE);
+      page = 0;
+    }
+    const uint16_t* kb = c.bf16 + layer * c.bf16_layer_stride + ((size_t)page * c.Hkv + head) * BF16_RECORD_ELEMS +
+                         (size_t)r0 * D;
+    const uint16_t* vb = kb + (size_t)PAGE * D;
 #pragma unroll
-  for (int it = 0; it < LOADS; ++it) {
-    const int idx = t + THREADS * it, r = idx / (D / 8), part = idx % (D / 8);
-    kk[it] = __ldcg(reinterpret_cast<const uint4*>(src + (size_t)r * D) + part);
-    vv[it] = __ldcg(reinterpret_cast<const uint4*>(src + (size_t)(PAGE + r) * D) + part);
+    for (int u = 0; u < 8; ++u) {
+      const int idx = u * 32 + lane, row = idx >> 4, part = idx & 15;
+      const bool ok = (rows >> row) & 1u;
+      cp_async16(&sg.k[row][8 * part], kb + (ok ? row * D + 8 * part : 0), ok);
+      cp_async16(&sg.v[row][8 * part], vb + (ok ? row * D + 8 * part : 0), ok);
+    }
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+    __syncwarp();
+    // ---- logits: S [16 rows x 8 columns] per n-tile over the 128 channels
+    float s[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[nt][e] = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      uint32_t af[4];
+      ldsm4(af, &sg.k[arow][16 * ks + acol]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_bf16(s[nt], af, bq[nt][ks][0], bq[nt][ks][1]);
+    }
+    // ---- softmax of the lane's head 4 nt + tid over rows gid, gid + 8; the weights
+    // go to the warp's weight columns as bf16 hi (column 2 tid) and lo (2 tid + 1)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const bool hok = 4 * nt + tid < G;
+      const float la = (hok && ((rows >> gid) & 1u)) ? s[nt][0] * scale2 : -INFINITY;
+      const float lb = (hok && ((rows >> (gid + 8)) & 1u)) ? s[nt][2] * scale2 : -INFINITY;
+      float pm = fmaxf(la, lb);
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+      if (pm > m_run[nt] + LAZY_MAX) {
+        const float corr = m_run[nt] == -INFINITY ? 0.0f : ex2(m_run[nt] - pm);
+        m_run[nt] = pm;
+        l_run[nt] *= corr;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[nt][mt][e] *= corr;
+      }
+      const float pa = la == -INFINITY ? 0.0f : ex2(la - m_run[nt]);
+      const float pb = lb == -INFINITY ? 0.0f : ex2(lb - m_run[nt]);
+      l_run[nt] += pa + pb;
+      const uint16_t ha = bf16_bits(pa), hb = bf16_bits(pb);
+      wc[nt][2 * tid][gid] = ha;
+      wc[nt][2 * tid][gid + 8] = hb;
+      wc[nt][2 * tid + 1][gid] = bf16_bits(pa - __uint_as_float(static_cast<uint32_t>(ha) << 16));
+      wc[nt][2 * tid + 1][gid + 8] = bf16_bits(pb - __uint_as_float(static_cast<uint32_t>(hb) << 16));
+    }
+    __syncwarp();
+    // ---- values: O [128 channels x 8 columns] += V^T P over the 16 rows
+    uint32_t bw[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      bw[nt][0] = *reinterpret_cast<const uint32_t*>(&wc[nt][gid][2 * tid]);
+      bw[nt][1] = *reinterpret_cast<const uint32_t*>(&wc[nt][gid][2 * tid + 8]);
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      uint32_t af[4];
+      ldsm4_t(af, &sg.v[vrow][16 * mt + vcol]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_bf16(o[nt][mt], af, bw[nt][0], bw[nt][1]);
+    }
+    __syncwarp();   // the stage and the weights are free
   }
+  // ---- this warp's state -> shared memory (over the rings: every warp is done with
+  // its ring first), then the warps merged per channel
+  __syncthreads();
 #pragma unroll
-  for (int it = 0; it < LOADS; ++it) {
-    const int idx = t + THREADS * it, r = idx / (D / 8), part = idx % (D / 8);
-    reinterpret_cast<uint4*>(&kr[r][0])[part ^ (r & 15)] = kk[it];
-    reinterpret_cast<uint4*>(&vr[r][0])[part] = vv[it];
-  }
-  group_sync();
-  // logits: thread t -> token t/2, channel half t%2, all G heads
-  {
-    const int r = t >> 1, half = t & 1;
-    float acc[G];
+  for (int nt = 0; nt < NT; ++nt) {
+    float l = l_run[nt];
 #pragma unroll
-    for (int h = 0; h < G; ++h) acc[h] = 0.0f;
-    const uint4* krow = reinterpret_cast<const uint4*>(&kr[r][0]);
+    for (int off = 4; off < 32; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+    const int g = 4 * nt + tid;
+    if (g < G) {
+      float* st = sm.buf.state[warp][g];
 #pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      const int chunk = 8 * half + b;
-      const uint4 w = krow[chunk ^ (r & 15)];
-      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float k0 = bf16lo(ww[e]), k1 = bf16hi(ww[e]);
-        const int ch = 8 * chunk + 2 * e;
-#pragma unroll
-        for (int h = 0; h < G; ++h) acc[h] = fmaf(qs[h][ch + 1], k1, fmaf(qs[h][ch], k0, acc[h]));
+      for (int mt = 0; mt < 8; ++mt) {
+        // o rows: channels 16 mt + gid and + 8; columns hi and lo of head g
+        st[16 * mt + gid] = o[nt][mt][0] + o[nt][mt][1];
+        st[16 * mt + gid + 8] = o[nt][mt][2] + o[nt][mt][3];
+      }
+      if (gid == 0) {
+        st[PARTIAL_M] = m_run[nt];
+        st[PARTIAL_L] = l;
       }
     }
-    const bool ok = row_valid(r);
+  }
+  __syncthreads();
+  const int t = threadIdx.x;
+  if (t < D) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], 1);
-      if (half == 0) qs[h][D + r] = ok ? acc[h] * scale2 : -INFINITY;
-    }
-  }
-  group_sync();
-  // softmax and values: warp w handles heads w, w + 4; lane owns channels 4 lane .. 4 lane + 3
-  for (int h = warp; h < G; h += WARPS) {
-    const float x0 = qs[h][D + lane], x1 = qs[h][D + lane + 32];
-    float m = fmaxf(x0, x1);
+      float M = -INFINITY;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const float p0 = (x0 == -INFINITY) ? 0.0f : exp2f(x0 - m);
-    const float p1 = (x1 == -INFINITY) ? 0.0f : exp2f(x1 - m);
-    float l = p0 + p1;
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, sm.buf.state[w][h][PARTIAL_M]);
+      float acc_o = 0.0f, acc_l = 0.0f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-    __syncwarp();
-    qs[h][D + lane] = p0;
-    qs[h][D + lane + 32] = p1;
-    __syncwarp();
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    if (m != -INFINITY) {
-      for (int r = 0; r < PAGE; ++r) {
-        const float p = qs[h][D + r];
-        // rows outside the window (p = 0) may hold anything, NaN included: skip them
-        if (p == 0.0f) continue;
-        const uint2 vv = reinterpret_cast<const uint2*>(&vr[r][0])[lane];
-        acc[0] = fmaf(p, bf16lo(vv.x), acc[0]);
-        acc[1] = fmaf(p, bf16hi(vv.x), acc[1]);
-        acc[2] = fmaf(p, bf16lo(vv.y), acc[2]);
-        acc[3] = fmaf(p, bf16hi(vv.y), acc[3]);
+      for (int w = 0; w < NW; ++w) {
+        const float mw = sm.buf.state[w][h][PARTIAL_M];
+        if (mw == -INFINITY) continue;
+        const float f = exp2f(mw - M);
+        acc_o = fmaf(sm.buf.state[w][h][t], f, acc_o);
+        acc_l = fmaf(sm.buf.state[w][h][PARTIAL_L], f, acc_l);
+      }
+      part_out[h * PART + t] = acc_o;
+      if (t == 0) {
+        part_out[h * PART + PARTIAL_M] = M;
+        part_out[h * PART + PARTIAL_L] = acc_l;
       }
     }
-    reinterpret_cast<float4*>(part_out + h * PART)[lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    if (lane == 0) {
-      part_out[h * PART + PARTIAL_M] = m;
-      part_out[h * PART + PARTIAL_L] = l;
-    }
   }
-  // warps with fewer heads (G < 4) must not load the group's next page over rows
-  // and weights the others still read
-  group_sync();
+  __syncthreads();
 }
 
 // ---- the decode kernel --------------------------------------------------------------
@@ -904,11 +1050,10 @@ __device__ __forceinline__ void segment_of(const DecodeArgs& a, int Hkv, int64_t
 
 // Records in the workspace: INT2 record of (segment s, CTA c) at slot s + c (the
 // CTAs meeting one segment are consecutive, so the slots are unique), then the
-// BF16 page records of segment s at 5 s + page.
+// BF16 record of segment s.
 template <int G, int GK>
 __global__ void __launch_bounds__(Tune<G, GK>::THREADS, 1)
     decode_kernel(DevCache c, int layer, DecodeArgs a, const uint16_t* __restrict__ q, float* __restrict__ recs) {
-  constexpr int NGRP = Smem<G, GK>::NGRP;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem<G, GK>& sm = *reinterpret_cast<Smem<G, GK>*>(smem_raw);
   const int t = threadIdx.x, warp = t >> 5;
@@ -952,36 +1097,36 @@ __global__ void __launch_bounds__(Tune<G, GK>::THREADS, 1)
   const int nseg = sm.nseg;
   uint32_t nc = 0;          // copies this warp has consumed
   bool timed_out = false;
-  if (nseg > 0) build_qfrag<G, GK>(c, layer, a.r[sm.seg[0].ri], sm.seg[0].head, q, sm, 0);
+  // the first segment's first copies go out before q is rotated
+  if (nseg > 0) {
+    int2_issue_first<G, GK>(c, layer, a.r[sm.seg[0].ri], sm.seg[0].head, sm.seg[0].p0, sm.seg[0].p1, sm,
+                            a.front_writes != 0, nc);
+    build_qfrag<G, GK>(c, layer, a.r[sm.seg[0].ri], sm.seg[0].head, q, sm, 0);
+  }
   for (int e = 0; e < nseg; ++e) {
     const Seg S = sm.seg[e];
     int2_pages<G, GK>(c, layer, a.r[S.ri], S.head, S.p0, S.p1, sm.qf[e & 1], sm,
-                      int2_recs + (size_t)S.slot * G * PART, a.dbg.wait_limit, a.front_writes != 0, nc, timed_out);
+                      int2_recs + (size_t)S.slot * G * PART, a.dbg.wait_limit, a.front_writes != 0, nc, timed_out,
+                      e == 0);
     if (e + 1 < nseg) build_qfrag<G, GK>(c, layer, a.r[sm.seg[e + 1].ri], sm.seg[e + 1].head, q, sm, (e + 1) & 1);
   }
-  // BF16 pages of the segments whose BF16 block this CTA holds, one four-warp group
-  // per page (every INT2 copy has been consumed: the rings are free)
+  // BF16 pages of the segments whose BF16 block this CTA holds (every INT2 copy
+  // has been consumed: the rings are free)
   bool any = false;
   for (int e = 0; e < nseg; ++e) any |= sm.seg[e].bf16 != 0;
   if (!any) return;
   if (a.front_writes) grid_dep_wait();   // a ring page may hold the token just appended
-  const int grp = warp / 4;
   for (int e = 0; e < nseg; ++e) {
     const Seg S = sm.seg[e];
-    if (!S.bf16) continue;
-    const int s = S.ri * c.Hkv + S.head;
-    if (grp < NGRP) {
-      for (int which = grp; which < BF16_ITEMS; which += NGRP)
-        bf16_item<G, GK>(c, layer, a.r[S.ri], S.head, which, q, sm, grp,
-                         bf16_recs + ((size_t)s * BF16_ITEMS + which) * G * PART);
-    }
-    __syncthreads();
+    if (S.bf16)
+      bf16_block<G, GK>(c, layer, a.r[S.ri], S.head, q, sm,
+                        bf16_recs + (size_t)(S.ri * c.Hkv + S.head) * G * PART);
   }
 }
 
 // ---- merge: one CTA per (request, query head) -----------------------------------------
-// Warp w folds items w, w + 16, ... (the segment's five BF16 page records, then its
-// INT2 records) into a running (M, L, O_bf16, O_hist) with lane l owning channels
+// Warp w folds items w, w + 16, ... (the segment's BF16 record, then its INT2
+// records) into a running (M, L, O_bf16, O_hist) with lane l owning channels
 // 4 l .. 4 l + 3; the warp states are combined, O_hist is rotated back by R_V^T
 // (staged in shared memory before the records are waited for) and the output row
 // written.
@@ -1028,11 +1173,10 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(DevCache c, int la
   int c_hi = static_cast<int>((s1 - 1) * a.ncta / a.total_cost);
   while (c_hi > 0 && cta_begin(c_hi, a.ncta, a.total_cost) > s1 - 1) --c_hi;
   while (cta_begin(c_hi + 1, a.ncta, a.total_cost) <= s1 - 1) ++c_hi;
-  const int items = BF16_ITEMS + (c_hi - c_lo + 1);
+  const int items = 1 + (c_hi - c_lo + 1);
   const float* bf16_recs = recs + ((size_t)a.n * c.Hkv + a.ncta) * G * PART;
   auto item_ptr = [&](int i) -> const float* {
-    return i < BF16_ITEMS ? bf16_recs + (((size_t)s * BF16_ITEMS + i) * G + g) * PART
-                          : recs + ((size_t)(s + c_lo + i - BF16_ITEMS) * G + g) * PART;
+    return i == 0 ? bf16_recs + ((size_t)s * G + g) * PART : recs + ((size_t)(s + c_lo + i - 1) * G + g) * PART;
   };
   float M = -INFINITY, L = 0.0f;
   float4 ob = make_float4(0.0f, 0.0f, 0.0f, 0.0f), oh = ob;
@@ -1067,7 +1211,7 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(DevCache c, int la
     for (int u = 0; u < MERGE_UNROLL; ++u) {
       const float f = (mv[u] == -INFINITY) ? 0.0f : exp2f(mv[u] - M);
       L = fmaf(lv[u], f, L);
-      const bool is_bf = i0 + MERGE_WARPS * u < BF16_ITEMS;
+      const bool is_bf = i0 + MERGE_WARPS * u == 0;
       const float fb = is_bf ? f : 0.0f, fh = is_bf ? 0.0f : f;
       ob.x = fmaf(ov[u].x, fb, ob.x);
       ob.y = fmaf(ov[u].y, fb, ob.y);
@@ -1127,6 +1271,9 @@ cudaError_t launch_decode_t(const DevCache& c, int layer, const DecodeReq* reqs,
                             const uint16_t* q, float* out, void* workspace, bool front_writes, DecodeDebug dbg,
                             cudaStream_t s) {
   static_assert(sizeof(Smem<G, GK>) <= 227 * 1024, "shared memory");
+  using SM = Smem<G, GK>;
+  static_assert(offsetof(SM, qf) % 16 == 0 && (QFrag<G>::WORDS * 4) % 16 == 0, "q operands: uint4 loads");
+  static_assert(offsetof(SM, meta) % 16 == 0 && offsetof(SM, bar) % 8 == 0, "shared memory alignment");
   static unsigned attr_done = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -509,15 +509,15 @@ oscar_status write_batch(oscar_cache* c, int32_t layer, int32_t n, const int32_t
   return err == cudaSuccess ? OSCAR_OK : c->cuda_fail(err, append ? "append launch" : "demote launch");
 }
 
-// BF16 half-pages (32 rows) of one kv head holding a cached token: the sink rows
+// BF16 sub-pages (16 rows) of one kv head holding a cached token: the sink rows
 // [0, min(T, 64)); ring slot s = 64 (page - 1) + r holds position
 // he + ((s - (he - 64)) mod 256), cached while below T.
-int bf16_half_pages(int64_t T, int64_t he) {
+int bf16_sub_pages(int64_t T, int64_t he) {
   int n = 0;
-  for (int hp = 0; hp < 2 * DECODE_BF16_ITEMS; ++hp) {
-    const int which = hp / 2;
+  for (int sp = 0; sp < DECODE_BF16_ITEMS * PAGE / 16; ++sp) {
+    const int which = sp / 4;
     bool any = false;
-    for (int r = 32 * (hp % 2); r < 32 * (hp % 2) + 32 && !any; ++r) {
+    for (int r = 16 * (sp % 4); r < 16 * (sp % 4) + 16 && !any; ++r) {
       if (which == 0) {
         any = r < std::min<int64_t>(T, SINK);
       } else if (T > SINK) {
@@ -546,7 +546,7 @@ DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int
     const Request& r = c->reqs[reqs[i]];
     const int64_t T = r.T[layer], he = r.he[layer];
     const int64_t np = pages_for(he);
-    const int64_t bf = (int64_t)DECODE_BF16_HALF_COST * bf16_half_pages(T, he);
+    const int64_t bf = (int64_t)DECODE_BF16_SUB_COST * bf16_sub_pages(T, he);
     if (out) {
       DecodeReq& d = out[i];
       d.slot = reqs[i];
@@ -585,7 +585,7 @@ DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int
     ncta = std::min<int64_t>(cost, 2 * ncta);
   }
   p.ncta = static_cast<int>(ncta);
-  p.partial_bytes = align256((size_t)((1 + DECODE_BF16_ITEMS) * p.segments + ncta) * decode_record_bytes(c->G()));
+  p.partial_bytes = align256((size_t)(2 * p.segments + ncta) * decode_record_bytes(c->G()));
   return p;
 }
 
@@ -603,12 +603,12 @@ int32_t decode_launch_size(const oscar_cache* c, int32_t layer, int32_t n, const
   return per;
 }
 
-// Workspace of a decode of n requests, whatever their lengths: per launch one INT2
-// record and five BF16 page records per (request, kv head), and one INT2 record
-// per CTA (at most four per SM).
+// Workspace of a decode of n requests, whatever their lengths: per launch an INT2
+// and a BF16 record per (request, kv head), and one INT2 record per CTA (at most
+// four per SM).
 size_t decode_bytes_bound(const oscar_cache* c, int32_t n) {
   const int64_t segs = (int64_t)std::min<int32_t>(n, DECODE_PER_LAUNCH) * c->cfg.num_kv_heads;
-  return align256((size_t)((1 + DECODE_BF16_ITEMS) * segs + 4 * (int64_t)c->num_sms) * decode_record_bytes(c->G()));
+  return align256((size_t)(2 * segs + 4 * (int64_t)c->num_sms) * decode_record_bytes(c->G()));
 }
 
 size_t decode_bytes_needed(const oscar_cache* c, int32_t layer, int32_t n, const int32_t* reqs) {

@@ -122,7 +122,7 @@ cudaError_t launch_demote_layers(const DevCache& c, const DemoteEntry* e, int n,
 // One launch covers up to DECODE_PER_LAUNCH requests.  The work is the list of
 // segments (request i, kv head h), i major; segment s = i Hkv + h is npages INT2
 // history pages (cost 1 each) followed by its BF16 block (the sink page and the
-// four ring pages, DECODE_BF16_HALF_COST per 32-row half-page holding a cached
+// four ring pages, DECODE_BF16_SUB_COST per 16-row sub-page holding a cached
 // token).  CTA c of ncta takes the cost units [c C / ncta, (c + 1) C / ncta).
 struct DecodeReq {
   int32_t slot;            // request slot (page-table row)
@@ -137,7 +137,7 @@ struct DecodeReq {
   int32_t bf16_cost;       // cost units of the BF16 block of each kv head
 };
 constexpr int DECODE_PER_LAUNCH = 64;
-constexpr int DECODE_BF16_HALF_COST = 3;
+constexpr int DECODE_BF16_SUB_COST = 1;
 constexpr int DECODE_BF16_ITEMS = 1 + RING_PAGES;   // BF16 pages per (request, kv head)
 struct DecodePlan {
   int n;
@@ -145,10 +145,10 @@ struct DecodePlan {
   int64_t total_cost;
   int64_t segments;        // n Hkv
   int worst_segments;      // most segments one CTA touches
-  size_t partial_bytes;    // workspace: INT2 records (segments + ncta), then BF16 page records (5 segments)
+  size_t partial_bytes;    // workspace: INT2 records (segments + ncta), then BF16 records (segments)
 };
-// Partial record of one (segment, CTA) or of one BF16 page of a segment: per query
-// head of the group o[128], m (log2 domain), l.
+// Partial record of one (segment, CTA) or of a segment's BF16 pages: per query head
+// of the group o[128], m (log2 domain), l.
 inline size_t decode_record_bytes(int g) { return (size_t)g * PARTIAL_FLOATS * sizeof(float); }
 // Failure-detection hooks of a launch: mbarrier wait rounds before a wait gives up
 // (ERR_TIMEOUT), and a page pair whose copy CTA 0's first warpgroup never issues

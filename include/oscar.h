@@ -225,7 +225,7 @@ oscar_status oscar_decode_attention(oscar_cache* cache, int32_t layer, int32_t n
  * of 8 MiB per device inside the library.
  *   Arguments, layouts and results are those of oscar_decode_attention.
  *   Size limit: a batch whose partial records (per launch of up to 64
- *     requests: six per request and kv head plus one per decode CTA, G x 528
+ *     requests: two per request and kv head plus one per decode CTA, G x 528
  *     bytes each) need more than 8 MiB is rejected with OSCAR_ERR_INVALID_ARG
  *     before any work; use oscar_decode_attention with a caller workspace.
  *   Set-up: every call takes the array's address on the current device

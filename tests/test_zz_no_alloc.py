@@ -22,9 +22,9 @@ def b():
 
 def test_batch_above_the_fixed_scratch_is_rejected_before_any_work(b):
     # metadata-only cache: the size check comes before any device work.  The
-    # records of one launch of 64 requests x 16 kv heads x 8 query heads per group
-    # (6 per segment plus one per CTA, 8 x 528 bytes each) need about 26 MB
-    layers, hkv, n = 1, 16, 64
+    # records of one launch of 64 requests x 32 kv heads x 8 query heads per group
+    # (2 per segment plus one per CTA, 8 x 528 bytes each) need about 18 MB
+    layers, hkv, n = 1, 32, 64
     cfg = b.make_config(layers, 8 * hkv, hkv, n, 8, 4 * n, 0, 0.0, 0)
     tau = np.ones((layers, hkv), np.float32)
     lib = b.OscarCache(cfg, tau_k=tau, tau_v=tau, dry_run=True)
