@@ -276,9 +276,9 @@ class OscarCache:
     def check(self, stream=None) -> None:
         self._check(self.lib.oscar_cache_check(self.h, None if self.dry else _stream_ptr(stream)), "device check")
 
-    def debug_decode_hooks(self, wait_limit: int = 100000, hold_pair: int = -1) -> None:
+    def debug_decode_hooks(self, wait_limit: int = 100000, hold_copy: int = -1) -> None:
         """Failure-detection hooks of this cache's decode launches (tests only)."""
-        self._check(self.lib.oscar_debug_decode_hooks(self.h, wait_limit, hold_pair), "decode hooks")
+        self._check(self.lib.oscar_debug_decode_hooks(self.h, wait_limit, hold_copy), "decode hooks")
 
     # -- views of device memory (for tests and inspection) ------------------------
     def int2_pool(self, layer: int):

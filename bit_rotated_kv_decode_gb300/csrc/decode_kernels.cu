@@ -246,7 +246,8 @@ __device__ void build_qfrag(const DevCache& c, int layer, const DecodeReq& R, in
   float rk[RP];
 #pragma unroll
   for (int i = 0; i < RP; ++i) rk[i] = (r0 + i < r1) ? __ldg(RK + (size_t)(r0 + i) * D + ch) : 0.0f;
-  for (int i = t; i < G * D; i += NTH) sm.scr.pro.q[i / D][i % D] = __uint_as_float(static_cast<uint32_t>(qrow[i]) << 16);
+  for (int i = t; i < G * D; i += NTH)
+    sm.scr.pro.q[i / D][i % D] = __uint_as_float(static_cast<uint32_t>(qrow[i]) << 16);
   __syncthreads();
   float acc[G];
 #pragma unroll
@@ -324,10 +325,11 @@ __device__ void build_qfrag(const DevCache& c, int layer, const DecodeReq& R, in
 
 // The first STAGES page copies of warp w's share of a segment's pages [p0, p1)
 // (pages p0 + w + NW j, j < STAGES), by lane 0, into stages nc + j; the hot page
-// (written by a preceding fused append) only once that grid has completed.
+// (written by a preceding fused append) only once that grid has completed.  Copy
+// number `hold` of warp 0 is not issued (failure-detection hook; -1: none).
 template <int G, int GK>
 __device__ __forceinline__ void int2_issue_first(const DevCache& c, int layer, const DecodeReq& R, int head, int p0,
-                                                 int p1, Smem<G, GK>& sm, bool front_writes, uint32_t nc) {
+                                                 int p1, Smem<G, GK>& sm, bool front_writes, uint32_t nc, int hold) {
   constexpr int NW = Tune<G, GK>::NW;
   constexpr int REC = record_for(GK);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -353,6 +355,7 @@ __device__ __forceinline__ void int2_issue_first(const DevCache& c, int layer, c
       atomicOr(c.err, ERR_INT2_PAGE);
       id = 0;
     }
+    if (warp == 0 && static_cast<int>(nc + j) == hold) continue;
     const int st = (nc + j) % STAGES;
     mbar_expect_tx(&sm.bar[warp][st], REC);
     tma_load_1d(sm.buf.ring[warp][st], base + (size_t)id * c.Hkv * REC, REC, &sm.bar[warp][st]);
@@ -363,12 +366,15 @@ __device__ __forceinline__ void int2_issue_first(const DevCache& c, int layer, c
 // warp w takes pages p0 + w, p0 + w + NW, ... through its TMA ring (copy number
 // nc counts the copies this warp has consumed so far, across segments); qf holds
 // the segment's q operands.  Leaves the CTA's partial (rotated basis) for every
-// query head of the group in part_out.
+// query head of the group in part_out.  A wait that runs out (limit rounds) sets
+// timed_out for the whole warp: it reports ERR_TIMEOUT, issues no further copy,
+// lets the copies it has in flight land and skips the rest of its pages.  Copy
+// number `hold` of warp 0 is never issued (failure-detection hook; -1: none).
 template <int G, int GK>
 __device__ __forceinline__ void int2_pages(const DevCache& c, int layer, const DecodeReq& R, int head, int p0,
                                            int p1, const uint32_t* __restrict__ qf, Smem<G, GK>& sm,
                                            float* part_out, uint32_t limit, bool front_writes, uint32_t& nc,
-                                           bool& timed_out, bool first_issued) {
+                                           bool& timed_out, bool first_issued, int hold) {
   constexpr int NW = Tune<G, GK>::NW;
   constexpr int NT = QFrag<G>::NT;       // n-tiles of 8 columns = 4 heads x (hi, lo)
   constexpr int REC = record_for(GK);
@@ -384,46 +390,68 @@ __device__ __forceinline__ void int2_pages(const DevCache& c, int layer, const D
   const int hot = front_writes ? R.hot_page : -1;
 
   // page ids of this warp's pages, read 32 at a time (lane l holds page 32 b + l of
-  // batch b); page_src is called by the whole warp with increasing j
+  // batch b); page_src is called by the whole warp with increasing j.  An id is a
+  // page (>= 0), HOT_ID (resolved at copy time) or BAD_ID: out of range, reported;
+  // page 0 is copied in its place (keeping the ring's sequence) and skipped.
+  constexpr int32_t HOT_ID = -1, BAD_ID = -2;
   int32_t batch_pages = 0;
   int batch_idx = -1;
   auto checked = [&](int32_t page) -> int32_t {
     if (page < 0 || page >= c.n_int2_pages) {
       atomicOr(c.err, ERR_INT2_PAGE);
-      page = 0;
+      return BAD_ID;
     }
     return page;
   };
   // the hot page (written by a preceding fused append) is read only after that
   // grid has completed: its id is fetched by lane 0 at copy time, after the wait
-  auto page_src = [&](int j) -> const uint8_t* {
+  auto page_src = [&](int j, bool& skip) -> const uint8_t* {
     const int b = j >> 5;
     if (b != batch_idx) {
       batch_idx = b;
       const int jj = 32 * b + lane;
       const int pj = p0 + warp + NW * jj;
       int32_t page = 0;
-      if (jj < my_n) page = pj == hot ? -1 : checked(__ldcg(pt + pj));
+      if (jj < my_n) page = pj == hot ? HOT_ID : checked(__ldcg(pt + pj));
       batch_pages = page;
     }
     int32_t page = __shfl_sync(0xffffffffu, batch_pages, j & 31);
-    if (page < 0 && lane == 0) {
-      grid_dep_wait();
-      page = checked(__ldcg(pt + hot));
+    if (page == HOT_ID) {   // warp-uniform
+      if (lane == 0) {
+        grid_dep_wait();
+        page = checked(__ldcg(pt + hot));
+      }
+      page = __shfl_sync(0xffffffffu, page, 0);
     }
+    skip = page < 0;
     return base + (size_t)max(page, 0) * pstride;
   };
+  // bit st: the page in stage st is skipped (bad id)
+  uint32_t skip_bits = 0u;
+  auto note = [&](int j, bool skip) {
+    const uint32_t bit = 1u << ((nc + j) % STAGES);
+    skip_bits = skip ? (skip_bits | bit) : (skip_bits & ~bit);
+  };
+  auto held = [&](int j) { return warp == 0 && static_cast<int>(nc + j) == hold; };
   auto issue = [&](int j) {
-    const uint8_t* src = page_src(j);
-    if (lane == 0 && j < my_n) {
+    bool skip;
+    const uint8_t* src = page_src(j, skip);
+    note(j, skip);
+    if (lane == 0 && j < my_n && !timed_out && !held(j)) {
       const int st = (nc + j) % STAGES;
       mbar_expect_tx(&sm.bar[warp][st], REC);
       tma_load_1d(sm.buf.ring[warp][st], src, REC, &sm.bar[warp][st]);
     }
   };
-  if (!first_issued) {
 #pragma unroll
-    for (int j = 0; j < STAGES; ++j) issue(j);
+  for (int j = 0; j < STAGES; ++j) {
+    if (first_issued) {   // copies already out: only the skip flags
+      bool skip;
+      page_src(j, skip);
+      note(j, skip);
+    } else {
+      issue(j);
+    }
   }
   // weights p * s_v are prescaled by 2^ew so the smallest ones stay representable in
   // fp16: s_v <= fp16(2 tau_V / 3) and p <= 2^LAZY_MAX, so p s_v 2^ew <= 2^15
@@ -486,246 +514,253 @@ __device__ __forceinline__ void int2_pages(const DevCache& c, int layer, const D
   }
 
   int done = 0;   // copies of this segment consumed by this warp
-  for (int j = 0; j < my_n; ++j) {
+  bool timed_here = false;
+  for (int j = 0; j < my_n && !timed_out; ++j) {
     const int stg = (nc + j) % STAGES;
     const int pi = p0 + warp + NW * j;
-    if (!timed_out && !mbar_wait(&sm.bar[warp][stg], ((nc + j) / STAGES) & 1, limit)) {
-      timed_out = true;
+    // one decision for the whole warp, so that its lanes never diverge
+    const bool landed = mbar_wait(&sm.bar[warp][stg], ((nc + j) / STAGES) & 1, limit);
+    if (!__all_sync(0xffffffffu, landed)) {
+      timed_out = timed_here = true;
       if (lane == 0) atomicOr(c.err, ERR_TIMEOUT);
+      break;
     }
-    if (timed_out) break;
     done = j + 1;
-    const uint8_t* rec = sm.buf.ring[warp][stg];
-    const int valid = min(PAGE, nhist - pi * PAGE);
+    if (!((skip_bits >> stg) & 1u)) {   // a page with a bad id contributes nothing
+      const uint8_t* rec = sm.buf.ring[warp][stg];
+      const int valid = min(PAGE, nhist - pi * PAGE);
 
 
-    // ---- logits: 4 m-tiles of 16 tokens x NT n-tiles, K = 128 channels; with
-    // G_K = 64 the k-steps of each group accumulate apart (acc[g])
-    float acc[NGR][NT][4][4];
-#pragma unroll
-    for (int g = 0; g < NGR; ++g)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[g][nt][mt][e] = 0.0f;
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-      uint2 ka, kb;
-      if constexpr (GK == 128) {
-        // channels 32 tid .. 32 tid + 31 of tokens 16 mt + gid and + 8
-        ka = *reinterpret_cast<const uint2*>(rec + K_CODES_OFF + (16 * mt + gid) * CODE_BYTES + 8 * tid);
-        kb = *reinterpret_cast<const uint2*>(rec + K_CODES_OFF + (16 * mt + gid + 8) * CODE_BYTES + 8 * tid);
-      } else {
-        // channels 16 tid .. 16 tid + 15 of group 0 (.x) and of group 1 (.y)
-        const uint8_t* ra = rec + K_CODES_OFF + (16 * mt + gid) * CODE_BYTES;
-        const uint8_t* rb = ra + 8 * CODE_BYTES;
-        ka = make_uint2(*reinterpret_cast<const uint32_t*>(ra + 4 * tid),
-                        *reinterpret_cast<const uint32_t*>(ra + 16 + 4 * tid));
-        kb = make_uint2(*reinterpret_cast<const uint32_t*>(rb + 4 * tid),
-                        *reinterpret_cast<const uint32_t*>(rb + 16 + 4 * tid));
-      }
-      const uint2 kas = make_uint2(ka.x >> 10, ka.y >> 10);
-      const uint2 kbs = make_uint2(kb.x >> 10, kb.y >> 10);
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const uint32_t wa = s < 4 ? ka.x : ka.y, was = s < 4 ? kas.x : kas.y;
-        const uint32_t wb = s < 4 ? kb.x : kb.y, wbs = s < 4 ? kbs.x : kbs.y;
-        const int m0 = 2 * (s & 3);
-        const uint32_t a0 = code_pair2(wa, was, m0), a1 = code_pair2(wb, wbs, m0);
-        const uint32_t a2 = code_pair2(wa, was, m0 + 1), a3 = code_pair2(wb, wbs, m0 + 1);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          mma16816(acc[NGR == 2 ? (s >> 2) : 0][nt][mt], a0, a1, a2, a3, bq[nt][s][0], bq[nt][s][1]);
-      }
-    }
-    // token meta of this lane's 8 tokens: 16 mt + gid + 8 rr; a partial page (the
-    // last of the history) masks the rows past its end
-    // the page's metadata converted once per token (lanes l and l + 32), not once
-    // per query head: {s_k, z_k, s_v 2^ew, z_v}, value terms zeroed past the end
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int tok = lane + 32 * hh;
-      const bool ok = tok < valid;
-#pragma unroll
-      for (int g = 0; g < NGR; ++g) {
-        const __half2 km = *reinterpret_cast<const __half2*>(rec + KMETA + tok * MB + 4 * g);
-        const __half2 vm = *reinterpret_cast<const __half2*>(rec + VMETA + tok * MB + 4 * g);
-        const float4 mv = make_float4(__low2float(km), __high2float(km), ok ? __low2float(vm) * wscale : 0.0f,
-                                      ok ? __high2float(vm) : 0.0f);
-        if (g == 0)
-          sm.meta[warp][tok] = mv;
-        else
-          sm.meta2[warp][tok] = mv;
-      }
-    }
-    __syncwarp();
-    // logits in the log2 domain, as pairs (token 16 mt + gid, that token + 8)
-    float2 lg[NT][4], sw[NGR][4], zv[NGR][4];
-    auto epilogue = [&](auto full_page) {
-      constexpr bool FULL = decltype(full_page)::value;
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
-        const int tok = 16 * mt + gid;
-        const float4 m0 = sm.meta[warp][tok], m1 = sm.meta[warp][tok + 8];
-        sw[0][mt] = make_float2(m0.z, m1.z);
-        zv[0][mt] = make_float2(m0.w, m1.w);
-        float4 n0 = m0, n1 = m1;
-        if constexpr (NGR == 2) {
-          n0 = sm.meta2[warp][tok];
-          n1 = sm.meta2[warp][tok + 8];
-          sw[NGR - 1][mt] = make_float2(n0.z, n1.z);
-          zv[NGR - 1][mt] = make_float2(n0.w, n1.w);
-        }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          // hi + lo columns, then s_k kscale acc + z_k (scale log2 e sum q_rot), per group
-          const float2 a = __fadd2_rn(make_float2(acc[0][nt][mt][0], acc[0][nt][mt][2]),
-                                      make_float2(acc[0][nt][mt][1], acc[0][nt][mt][3]));
-          const float2 sk = __fmul2_rn(make_float2(m0.x, m1.x), make_float2(ks[nt], ks[nt]));
-          const float2 zk = __fmul2_rn(make_float2(m0.y, m1.y), make_float2(kz[nt][0], kz[nt][0]));
-          float2 v = __ffma2_rn(sk, a, zk);
-          if constexpr (NGR == 2) {
-            const float2 a1 = __fadd2_rn(make_float2(acc[NGR - 1][nt][mt][0], acc[NGR - 1][nt][mt][2]),
-                                         make_float2(acc[NGR - 1][nt][mt][1], acc[NGR - 1][nt][mt][3]));
-            const float2 sk1 = __fmul2_rn(make_float2(n0.x, n1.x), make_float2(ks[nt], ks[nt]));
-            const float2 zk1 = __fmul2_rn(make_float2(n0.y, n1.y),
-                                          make_float2(kz[nt][NGR - 1], kz[nt][NGR - 1]));
-            v = __ffma2_rn(sk1, a1, __fadd2_rn(v, zk1));
-          }
-          const bool head_ok = 4 * nt + 4 <= G || 4 * nt + tid < G;
-          if (!FULL || !head_ok) {
-            v.x = (head_ok && tok < valid) ? v.x : -INFINITY;
-            v.y = (head_ok && tok + 8 < valid) ? v.y : -INFINITY;
-          }
-          lg[nt][mt] = v;
-        }
-      }
-    };
-    if (valid == PAGE)
-      epilogue(std::true_type{});
-    else
-      epilogue(std::false_type{});
-    // ---- online softmax per head (lanes with equal tid share a head); the
-    // weights p s_v 2^ew go to shared memory as fp16 hi / lo halves.  Within each
-    // 16-token group the weight rows hold token 16 g + r at position 16 g + 2 r
-    // (r < 8) or 16 g + 2 (r - 8) + 1, so a lane's pair is one 32-bit store; the
-    // value contraction below takes its k index in the same order.
-    uint16_t(*wh)[2][WH_STRIDE];
-    if constexpr (kWeightsInRing<G, GK>) {
-      wh = reinterpret_cast<uint16_t(*)[2][WH_STRIDE]>(sm.buf.ring[warp][stg] + K_CODES_OFF);
-      __syncwarp();   // every lane is done reading this page's K codes
-    } else {
-      wh = sm.w.wh[warp];
-    }
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float pm = fmaxf(lg[nt][0].x, lg[nt][0].y);
-#pragma unroll
-      for (int mt = 1; mt < 4; ++mt) pm = fmaxf(pm, fmaxf(lg[nt][mt].x, lg[nt][mt].y));
-      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
-      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
-      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-      // the reference max m_run moves only when a page exceeds it by more than
-      // LAZY_MAX (log2 units): weights stay below 2^LAZY_MAX and the accumulators
-      // are rescaled on few pages
-      if (pm > m_run[nt] + LAZY_MAX) {
-        const float corr = ex2(m_run[nt] - pm);
-        m_run[nt] = pm;
-        l_run[nt] = __fmul2_rn(l_run[nt], make_float2(corr, corr));
-#pragma unroll
-        for (int g = 0; g < NGR; ++g) u_run[nt][g] = __fmul2_rn(u_run[nt][g], make_float2(corr, corr));
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) o[nt][mt][e] *= corr;
-      }
-      const float2 neg_ref = make_float2(-m_run[nt], -m_run[nt]);
-      const int h = 4 * nt + tid;
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
-        const float2 d = __fadd2_rn(lg[nt][mt], neg_ref);
-        const float2 p = make_float2(ex2(d.x), ex2(d.y));
-        l_run[nt] = __fadd2_rn(l_run[nt], p);
-#pragma unroll
-        for (int g = 0; g < NGR; ++g) u_run[nt][g] = __ffma2_rn(p, zv[g][mt], u_run[nt][g]);
-        if (h < G) {
-          const int pos = 16 * mt + 2 * gid;
-#pragma unroll
-          for (int g = 0; g < NGR; ++g) {
-            const float2 w = __fmul2_rn(p, sw[g][mt]);
-            const __half2 hi = __float22half2_rn(w);
-            const float2 lo = __ffma2_rn(__half22float2(hi), make_float2(-1.0f, -1.0f), w);
-            *reinterpret_cast<__half2*>(&wh[NGR * h + g][0][pos]) = hi;
-            *reinterpret_cast<__half2*>(&wh[NGR * h + g][1][pos]) = __float22half2_rn(lo);
-          }
-        }
-      }
-    }
-    __syncwarp();
-    // ---- values: 8 m-tiles of 16 channels x NT n-tiles, K = 64 tokens; k index
-    // 2 j + b of step s is token 16 s + j + 8 b
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      const int ta = 16 * s + 2 * tid;
-      uint32_t bw[NGR][NT][2];
-#pragma unroll
+      // ---- logits: 4 m-tiles of 16 tokens x NT n-tiles, K = 128 channels; with
+      // G_K = 64 the k-steps of each group accumulate apart (acc[g])
+      float acc[NGR][NT][4][4];
+  #pragma unroll
       for (int g = 0; g < NGR; ++g)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int h = 4 * nt + (gid >> 1);
-          if (h < G) {
-            const uint16_t* row = wh[NGR * h + g][gid & 1];
-            bw[g][nt][0] = *reinterpret_cast<const uint32_t*>(row + ta);
-            bw[g][nt][1] = *reinterpret_cast<const uint32_t*>(row + ta + 8);
-          } else {
-            bw[g][nt][0] = bw[g][nt][1] = 0u;
+  #pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+  #pragma unroll
+          for (int mt = 0; mt < 4; ++mt)
+  #pragma unroll
+            for (int e = 0; e < 4; ++e) acc[g][nt][mt][e] = 0.0f;
+  #pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        uint2 ka, kb;
+        if constexpr (GK == 128) {
+          // channels 32 tid .. 32 tid + 31 of tokens 16 mt + gid and + 8
+          ka = *reinterpret_cast<const uint2*>(rec + K_CODES_OFF + (16 * mt + gid) * CODE_BYTES + 8 * tid);
+          kb = *reinterpret_cast<const uint2*>(rec + K_CODES_OFF + (16 * mt + gid + 8) * CODE_BYTES + 8 * tid);
+        } else {
+          // channels 16 tid .. 16 tid + 15 of group 0 (.x) and of group 1 (.y)
+          const uint8_t* ra = rec + K_CODES_OFF + (16 * mt + gid) * CODE_BYTES;
+          const uint8_t* rb = ra + 8 * CODE_BYTES;
+          ka = make_uint2(*reinterpret_cast<const uint32_t*>(ra + 4 * tid),
+                          *reinterpret_cast<const uint32_t*>(ra + 16 + 4 * tid));
+          kb = make_uint2(*reinterpret_cast<const uint32_t*>(rb + 4 * tid),
+                          *reinterpret_cast<const uint32_t*>(rb + 16 + 4 * tid));
+        }
+        const uint2 kas = make_uint2(ka.x >> 10, ka.y >> 10);
+        const uint2 kbs = make_uint2(kb.x >> 10, kb.y >> 10);
+  #pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          const uint32_t wa = s < 4 ? ka.x : ka.y, was = s < 4 ? kas.x : kas.y;
+          const uint32_t wb = s < 4 ? kb.x : kb.y, wbs = s < 4 ? kbs.x : kbs.y;
+          const int m0 = 2 * (s & 3);
+          const uint32_t a0 = code_pair2(wa, was, m0), a1 = code_pair2(wb, wbs, m0);
+          const uint32_t a2 = code_pair2(wa, was, m0 + 1), a3 = code_pair2(wb, wbs, m0 + 1);
+  #pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            mma16816(acc[NGR == 2 ? (s >> 2) : 0][nt][mt], a0, a1, a2, a3, bq[nt][s][0], bq[nt][s][1]);
+        }
+      }
+      // token meta of this lane's 8 tokens: 16 mt + gid + 8 rr; a partial page (the
+      // last of the history) masks the rows past its end
+      // the page's metadata converted once per token (lanes l and l + 32), not once
+      // per query head: {s_k, z_k, s_v 2^ew, z_v}, value terms zeroed past the end
+  #pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int tok = lane + 32 * hh;
+        const bool ok = tok < valid;
+  #pragma unroll
+        for (int g = 0; g < NGR; ++g) {
+          const __half2 km = *reinterpret_cast<const __half2*>(rec + KMETA + tok * MB + 4 * g);
+          const __half2 vm = *reinterpret_cast<const __half2*>(rec + VMETA + tok * MB + 4 * g);
+          const float4 mv = make_float4(__low2float(km), __high2float(km), ok ? __low2float(vm) * wscale : 0.0f,
+                                        ok ? __high2float(vm) : 0.0f);
+          if (g == 0)
+            sm.meta[warp][tok] = mv;
+          else
+            sm.meta2[warp][tok] = mv;
+        }
+      }
+      __syncwarp();
+      // logits in the log2 domain, as pairs (token 16 mt + gid, that token + 8)
+      float2 lg[NT][4], sw[NGR][4], zv[NGR][4];
+      auto epilogue = [&](auto full_page) {
+        constexpr bool FULL = decltype(full_page)::value;
+  #pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+          const int tok = 16 * mt + gid;
+          const float4 m0 = sm.meta[warp][tok], m1 = sm.meta[warp][tok + 8];
+          sw[0][mt] = make_float2(m0.z, m1.z);
+          zv[0][mt] = make_float2(m0.w, m1.w);
+          float4 n0 = m0, n1 = m1;
+          if constexpr (NGR == 2) {
+            n0 = sm.meta2[warp][tok];
+            n1 = sm.meta2[warp][tok + 8];
+            sw[NGR - 1][mt] = make_float2(n0.z, n1.z);
+            zv[NGR - 1][mt] = make_float2(n0.w, n1.w);
+          }
+  #pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            // hi + lo columns, then s_k kscale acc + z_k (scale log2 e sum q_rot), per group
+            const float2 a = __fadd2_rn(make_float2(acc[0][nt][mt][0], acc[0][nt][mt][2]),
+                                        make_float2(acc[0][nt][mt][1], acc[0][nt][mt][3]));
+            const float2 sk = __fmul2_rn(make_float2(m0.x, m1.x), make_float2(ks[nt], ks[nt]));
+            const float2 zk = __fmul2_rn(make_float2(m0.y, m1.y), make_float2(kz[nt][0], kz[nt][0]));
+            float2 v = __ffma2_rn(sk, a, zk);
+            if constexpr (NGR == 2) {
+              const float2 a1 = __fadd2_rn(make_float2(acc[NGR - 1][nt][mt][0], acc[NGR - 1][nt][mt][2]),
+                                           make_float2(acc[NGR - 1][nt][mt][1], acc[NGR - 1][nt][mt][3]));
+              const float2 sk1 = __fmul2_rn(make_float2(n0.x, n1.x), make_float2(ks[nt], ks[nt]));
+              const float2 zk1 = __fmul2_rn(make_float2(n0.y, n1.y),
+                                            make_float2(kz[nt][NGR - 1], kz[nt][NGR - 1]));
+              v = __ffma2_rn(sk1, a1, __fadd2_rn(v, zk1));
+            }
+            const bool head_ok = 4 * nt + 4 <= G || 4 * nt + tid < G;
+            if (!FULL || !head_ok) {
+              v.x = (head_ok && tok < valid) ? v.x : -INFINITY;
+              v.y = (head_ok && tok + 8 < valid) ? v.y : -INFINITY;
+            }
+            lg[nt][mt] = v;
           }
         }
-      const int tb = 16 * s + tid;
-      if constexpr (GK == 128) {
-        // row gid of m-tile mt: channel 16 gid + mt; row gid + 8: 16 gid + 8 + mt
-        const uint32_t* vrow = reinterpret_cast<const uint32_t*>(rec + V_CODES_OFF) + gid;
-        const uint32_t wa = vrow[tb * (CODE_BYTES / 4)], wb = vrow[(tb + 8) * (CODE_BYTES / 4)];
-        const uint32_t wc = vrow[(tb + 4) * (CODE_BYTES / 4)], wd = vrow[(tb + 12) * (CODE_BYTES / 4)];
-        const uint32_t x1 = __byte_perm(wa, wb, 0x5410), y1 = __byte_perm(wa, wb, 0x7632);
-        const uint32_t x2 = __byte_perm(wc, wd, 0x5410), y2 = __byte_perm(wc, wd, 0x7632);
-        const uint32_t x1s = x1 >> 10, y1s = y1 >> 10;
-        const uint32_t x2s = x2 >> 10, y2s = y2 >> 10;
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          const uint32_t a0 = code_pair2(x1, x1s, mt), a1 = code_pair2(y1, y1s, mt);
-          const uint32_t a2 = code_pair2(x2, x2s, mt), a3 = code_pair2(y2, y2s, mt);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma16816(o[nt][mt], a0, a1, a2, a3, bw[0][nt][0], bw[0][nt][1]);
-        }
+      };
+      if (valid == PAGE)
+        epilogue(std::true_type{});
+      else
+        epilogue(std::false_type{});
+      // ---- online softmax per head (lanes with equal tid share a head); the
+      // weights p s_v 2^ew go to shared memory as fp16 hi / lo halves.  Within each
+      // 16-token group the weight rows hold token 16 g + r at position 16 g + 2 r
+      // (r < 8) or 16 g + 2 (r - 8) + 1, so a lane's pair is one 32-bit store; the
+      // value contraction below takes its k index in the same order.
+      uint16_t(*wh)[2][WH_STRIDE];
+      if constexpr (kWeightsInRing<G, GK>) {
+        wh = reinterpret_cast<uint16_t(*)[2][WH_STRIDE]>(sm.buf.ring[warp][stg] + K_CODES_OFF);
+        __syncwarp();   // every lane is done reading this page's K codes
       } else {
-        // group-pure m-tiles: m-tile 4 g + j, row gid holds channel 64 g + 8 gid + j and
-        // row gid + 8 channel 64 g + 8 gid + 4 + j (16-bit half gid & 1 of word 4 g + gid / 2)
-        const uint32_t sel = (gid & 1) ? 0x7632u : 0x5410u;
-#pragma unroll
-        for (int g = 0; g < NGR; ++g) {
-          const uint32_t* vrow = reinterpret_cast<const uint32_t*>(rec + V_CODES_OFF) + 4 * g + (gid >> 1);
+        wh = sm.w.wh[warp];
+      }
+  #pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        float pm = fmaxf(lg[nt][0].x, lg[nt][0].y);
+  #pragma unroll
+        for (int mt = 1; mt < 4; ++mt) pm = fmaxf(pm, fmaxf(lg[nt][mt].x, lg[nt][mt].y));
+        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
+        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
+        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+        // the reference max m_run moves only when a page exceeds it by more than
+        // LAZY_MAX (log2 units): weights stay below 2^LAZY_MAX and the accumulators
+        // are rescaled on few pages
+        if (pm > m_run[nt] + LAZY_MAX) {
+          const float corr = ex2(m_run[nt] - pm);
+          m_run[nt] = pm;
+          l_run[nt] = __fmul2_rn(l_run[nt], make_float2(corr, corr));
+  #pragma unroll
+          for (int g = 0; g < NGR; ++g) u_run[nt][g] = __fmul2_rn(u_run[nt][g], make_float2(corr, corr));
+  #pragma unroll
+          for (int mt = 0; mt < 8; ++mt)
+  #pragma unroll
+            for (int e = 0; e < 4; ++e) o[nt][mt][e] *= corr;
+        }
+        const float2 neg_ref = make_float2(-m_run[nt], -m_run[nt]);
+        const int h = 4 * nt + tid;
+  #pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+          const float2 d = __fadd2_rn(lg[nt][mt], neg_ref);
+          const float2 p = make_float2(ex2(d.x), ex2(d.y));
+          l_run[nt] = __fadd2_rn(l_run[nt], p);
+  #pragma unroll
+          for (int g = 0; g < NGR; ++g) u_run[nt][g] = __ffma2_rn(p, zv[g][mt], u_run[nt][g]);
+          if (h < G) {
+            const int pos = 16 * mt + 2 * gid;
+  #pragma unroll
+            for (int g = 0; g < NGR; ++g) {
+              const float2 w = __fmul2_rn(p, sw[g][mt]);
+              const __half2 hi = __float22half2_rn(w);
+              const float2 lo = __ffma2_rn(__half22float2(hi), make_float2(-1.0f, -1.0f), w);
+              *reinterpret_cast<__half2*>(&wh[NGR * h + g][0][pos]) = hi;
+              *reinterpret_cast<__half2*>(&wh[NGR * h + g][1][pos]) = __float22half2_rn(lo);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      // ---- values: 8 m-tiles of 16 channels x NT n-tiles, K = 64 tokens; k index
+      // 2 j + b of step s is token 16 s + j + 8 b
+  #pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const int ta = 16 * s + 2 * tid;
+        uint32_t bw[NGR][NT][2];
+  #pragma unroll
+        for (int g = 0; g < NGR; ++g)
+  #pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const int h = 4 * nt + (gid >> 1);
+            if (h < G) {
+              const uint16_t* row = wh[NGR * h + g][gid & 1];
+              bw[g][nt][0] = *reinterpret_cast<const uint32_t*>(row + ta);
+              bw[g][nt][1] = *reinterpret_cast<const uint32_t*>(row + ta + 8);
+            } else {
+              bw[g][nt][0] = bw[g][nt][1] = 0u;
+            }
+          }
+        const int tb = 16 * s + tid;
+        if constexpr (GK == 128) {
+          // row gid of m-tile mt: channel 16 gid + mt; row gid + 8: 16 gid + 8 + mt
+          const uint32_t* vrow = reinterpret_cast<const uint32_t*>(rec + V_CODES_OFF) + gid;
           const uint32_t wa = vrow[tb * (CODE_BYTES / 4)], wb = vrow[(tb + 8) * (CODE_BYTES / 4)];
           const uint32_t wc = vrow[(tb + 4) * (CODE_BYTES / 4)], wd = vrow[(tb + 12) * (CODE_BYTES / 4)];
-          const uint32_t x1 = __byte_perm(wa, wb, sel), x2 = __byte_perm(wc, wd, sel);
-          const uint32_t x1s = x1 >> 10, x2s = x2 >> 10;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t a0 = code_pair2(x1, x1s, j), a1 = code_pair2(x1, x1s, j + 4);
-            const uint32_t a2 = code_pair2(x2, x2s, j), a3 = code_pair2(x2, x2s, j + 4);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              mma16816(o[nt][4 * g + j], a0, a1, a2, a3, bw[g][nt][0], bw[g][nt][1]);
+          const uint32_t x1 = __byte_perm(wa, wb, 0x5410), y1 = __byte_perm(wa, wb, 0x7632);
+          const uint32_t x2 = __byte_perm(wc, wd, 0x5410), y2 = __byte_perm(wc, wd, 0x7632);
+          const uint32_t x1s = x1 >> 10, y1s = y1 >> 10;
+          const uint32_t x2s = x2 >> 10, y2s = y2 >> 10;
+  #pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            const uint32_t a0 = code_pair2(x1, x1s, mt), a1 = code_pair2(y1, y1s, mt);
+            const uint32_t a2 = code_pair2(x2, x2s, mt), a3 = code_pair2(y2, y2s, mt);
+  #pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma16816(o[nt][mt], a0, a1, a2, a3, bw[0][nt][0], bw[0][nt][1]);
+          }
+        } else {
+          // group-pure m-tiles: m-tile 4 g + j, row gid holds channel 64 g + 8 gid + j and
+          // row gid + 8 channel 64 g + 8 gid + 4 + j (16-bit half gid & 1 of word 4 g + gid / 2)
+          const uint32_t sel = (gid & 1) ? 0x7632u : 0x5410u;
+  #pragma unroll
+          for (int g = 0; g < NGR; ++g) {
+            const uint32_t* vrow = reinterpret_cast<const uint32_t*>(rec + V_CODES_OFF) + 4 * g + (gid >> 1);
+            const uint32_t wa = vrow[tb * (CODE_BYTES / 4)], wb = vrow[(tb + 8) * (CODE_BYTES / 4)];
+            const uint32_t wc = vrow[(tb + 4) * (CODE_BYTES / 4)], wd = vrow[(tb + 12) * (CODE_BYTES / 4)];
+            const uint32_t x1 = __byte_perm(wa, wb, sel), x2 = __byte_perm(wc, wd, sel);
+            const uint32_t x1s = x1 >> 10, x2s = x2 >> 10;
+  #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t a0 = code_pair2(x1, x1s, j), a1 = code_pair2(x1, x1s, j + 4);
+              const uint32_t a2 = code_pair2(x2, x2s, j), a3 = code_pair2(x2, x2s, j + 4);
+  #pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+                mma16816(o[nt][4 * g + j], a0, a1, a2, a3, bw[g][nt][0], bw[g][nt][1]);
+            }
           }
         }
       }
+      __syncwarp();
     }
-    __syncwarp();
     if (j + STAGES < my_n) {
-      const uint8_t* src = page_src(j + STAGES);
-      if (lane == 0) {
+      bool skip;
+      const uint8_t* src = page_src(j + STAGES, skip);
+      note(j + STAGES, skip);
+      if (lane == 0 && !held(j + STAGES)) {
         // the weights were written to this buffer through the generic proxy
         if constexpr (kWeightsInRing<G, GK>) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         mbar_expect_tx(&sm.bar[warp][stg], REC);
@@ -733,11 +768,11 @@ __device__ __forceinline__ void int2_pages(const DevCache& c, int layer, const D
       }
     }
   }
-  if (timed_out && lane == 0) {
+  if (timed_here && lane == 0) {
     // let every copy this warp issued land (bounded) before the buffers are reused:
     // the copies done .. min(done + STAGES, my_n) - 1 may still be in flight
     for (int j = done; j < min(done + STAGES, my_n); ++j)
-      mbar_wait(&sm.bar[warp][(nc + j) % STAGES], ((nc + j) / STAGES) & 1, limit);
+      if (!held(j)) mbar_wait(&sm.bar[warp][(nc + j) % STAGES], ((nc + j) / STAGES) & 1, DECODE_WAIT_LIMIT);
   }
   nc += static_cast<uint32_t>(my_n);
   __syncthreads();   // every warp is done with every ring before states overwrite them
@@ -1096,18 +1131,19 @@ __global__ void __launch_bounds__(Tune<G, GK>::THREADS, 1)
   __syncthreads();
   const int nseg = sm.nseg;
   uint32_t nc = 0;          // copies this warp has consumed
-  bool timed_out = false;
+  bool timed_out = false;   // a wait of this warp ran out: no further copies
+  const int hold = cta == 0 ? a.dbg.hold_copy : -1;
   // the first segment's first copies go out before q is rotated
   if (nseg > 0) {
     int2_issue_first<G, GK>(c, layer, a.r[sm.seg[0].ri], sm.seg[0].head, sm.seg[0].p0, sm.seg[0].p1, sm,
-                            a.front_writes != 0, nc);
+                            a.front_writes != 0, nc, hold);
     build_qfrag<G, GK>(c, layer, a.r[sm.seg[0].ri], sm.seg[0].head, q, sm, 0);
   }
   for (int e = 0; e < nseg; ++e) {
     const Seg S = sm.seg[e];
     int2_pages<G, GK>(c, layer, a.r[S.ri], S.head, S.p0, S.p1, sm.qf[e & 1], sm,
                       int2_recs + (size_t)S.slot * G * PART, a.dbg.wait_limit, a.front_writes != 0, nc, timed_out,
-                      e == 0);
+                      e == 0, hold);
     if (e + 1 < nseg) build_qfrag<G, GK>(c, layer, a.r[sm.seg[e + 1].ri], sm.seg[e + 1].head, q, sm, (e + 1) & 1);
   }
   // BF16 pages of the segments whose BF16 block this CTA holds (every INT2 copy

@@ -755,11 +755,11 @@ oscar_status oscar_decode_step(oscar_cache* c, int32_t layer, int32_t n, const i
   return OSCAR_OK;
 }
 
-oscar_status oscar_debug_decode_hooks(oscar_cache* c, uint32_t wait_limit, int32_t hold_pair) {
+oscar_status oscar_debug_decode_hooks(oscar_cache* c, uint32_t wait_limit, int32_t hold_copy) {
   if (!c) return OSCAR_ERR_INVALID_ARG;
-  if (wait_limit < 1 || hold_pair < -1) return c->fail(OSCAR_ERR_INVALID_ARG, "bad hook values");
+  if (wait_limit < 1 || hold_copy < -1) return c->fail(OSCAR_ERR_INVALID_ARG, "bad hook values");
   c->dbg.wait_limit = wait_limit;
-  c->dbg.hold_pair = hold_pair;
+  c->dbg.hold_copy = hold_copy;
   return OSCAR_OK;
 }
 

@@ -151,13 +151,13 @@ struct DecodePlan {
 // of the group o[128], m (log2 domain), l.
 inline size_t decode_record_bytes(int g) { return (size_t)g * PARTIAL_FLOATS * sizeof(float); }
 // Failure-detection hooks of a launch: mbarrier wait rounds before a wait gives up
-// (ERR_TIMEOUT), and a page pair whose copy CTA 0's first warpgroup never issues
-// (-1: none), so that a test can make a wait run out.
+// (ERR_TIMEOUT), and the page copy (issue order) that warp 0 of CTA 0 never
+// issues (-1: none), so that a test can make a wait run out.
 struct DecodeDebug {
   uint32_t wait_limit;
-  int32_t hold_pair;
+  int32_t hold_copy;
 };
-constexpr uint32_t DECODE_WAIT_LIMIT = 100000;   // rounds of up to 10 us each
+constexpr uint32_t DECODE_WAIT_LIMIT = 100000;   // rounds of up to 20 us each
 cudaError_t launch_decode(const DevCache& c, int layer, const DecodeReq* reqs, const DecodePlan& plan,
                           const uint16_t* q, float* out, void* workspace, bool front_writes, DecodeDebug dbg,
                           cudaStream_t s);

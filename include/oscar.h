@@ -256,14 +256,17 @@ oscar_status oscar_decode_step(oscar_cache* cache, int32_t layer, int32_t n, con
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /* Failure-detection hooks of the decode launches of this cache (test use; the
- * pages have no counterpart).  wait_limit: rounds (up to 10 us each) a bounded
- * device wait makes before it gives up and reports OSCAR_ERR_TIMEOUT through
- * oscar_cache_check (default 100000, must be >= 1).  hold_pair: the page pair
- * (in issue order) of CTA 0's first warpgroup whose copy is never issued, so that
- * its wait runs out (-1, the default, holds none).  The kernel then drains its
- * copies in flight, frees its tensor memory and returns; that launch's output is
- * undefined.  OSCAR_ERR_INVALID_ARG for values out of range. */
-oscar_status oscar_debug_decode_hooks(oscar_cache* cache, uint32_t wait_limit, int32_t hold_pair);
+ * pages have no counterpart).  wait_limit: rounds (up to 20 us each) a bounded
+ * device wait on a page copy makes before it gives up and reports
+ * OSCAR_ERR_TIMEOUT through oscar_cache_check (default 100000, must be >= 1).
+ * hold_copy: the page copy (numbered in issue order, from 0, across the segments
+ * of the CTA) of warp 0 of decode CTA 0 that is never issued, so that its wait
+ * runs out (-1, the default, holds none).  A warp whose wait ran out issues no
+ * further copy, waits (with the default limit) for the copies it has in flight
+ * and skips its remaining pages; the launch's output is then undefined but the
+ * device stays usable and the next launch starts clean.  OSCAR_ERR_INVALID_ARG
+ * for values out of range. */
+oscar_status oscar_debug_decode_hooks(oscar_cache* cache, uint32_t wait_limit, int32_t hold_copy);
 
 /* Synchronise "stream" and report the sticky device error word (then clear it). */
 oscar_status oscar_cache_check(oscar_cache* cache, void* stream);
