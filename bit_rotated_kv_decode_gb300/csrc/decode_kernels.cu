@@ -7,22 +7,20 @@
 // "Together AI Open-Sources OSCAR" (MarkTechPost), section "The Serving
 // System": the value path is inverse-rotated.
 //
-// Two launches per layer (and per launch batch of requests), chained with
-// programmatic dependent launch:
-//   1. decode   one persistent CTA per SM.  The work -- every INT2 history page
-//               and the BF16 pages of every (request, kv head) segment -- is cut
-//               into equal-cost contiguous ranges, one per CTA.  A CTA rotates q
-//               itself (q_rot = q R_K, into tensor-core operands in shared
-//               memory) while the first page copies are in flight; then each warp
-//               streams its share of the CTA's pages of a segment through its own
-//               TMA ring, and at the end of the segment the warps' partials are
-//               combined into one record (o, m, l; rotated basis).  The CTA that
-//               holds a segment's BF16 pages attends to them last, with the
-//               unrotated q, one record per page;
-//   2. merge    one CTA per (request, query head): online-softmax merge of the
-//               segment's records, R_V^T applied to the INT2 part (staged in
-//               shared memory while the decode grid still runs),
-//               out = (O_bf16 + O_hist R_V^T) / L.
+// One launch per layer (and per batch of up to 64 requests): one persistent CTA
+// per SM.  The first nbc CTAs attend to the BF16 sink and recent pages of the
+// (request, kv head) segments, a whole segment's BF16 pages at a time, with the
+// unrotated q (one record per segment, plain basis).  The other CTAs share the
+// INT2 history pages, cut into equal contiguous ranges that a CTA walks segment
+// by segment:
+//   * q_rot = q R_K into tensor-core operands in shared memory (R_K is read
+//     before the launch waits for the preceding grid, q after);
+//   * the segment's INT2 pages, each warp through its own TMA ring, the warps'
+//     partials combined into one record (o, m, l; rotated basis).
+// A per-(request, kv head) counter in the cache counts the CTAs done with a
+// segment; the one that completes the count merges the segment's records with
+// an online softmax and writes out = (O_bf16 + O_hist R_V^T) / L for its G query
+// heads.
 // For an INT2 token j with codes c_j and fp16 scale / zero (s_j, z_j):
 //   logit_j = scale * (s_j (q_rot . c_j) + z_j sum(q_rot)),
 //   value   = s_j c_j + z_j 1   (accumulated as p_j s_j c_j plus sum p_j z_j).
@@ -57,12 +55,10 @@ namespace {
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr int PART = PARTIAL_FLOATS;
 constexpr int STAGES = 2;                // TMA ring depth per warp
-constexpr int SEGMAX = 16;               // segments one CTA may touch
 constexpr uint32_t SUSPEND_NS = 20000;   // a waiting warp sleeps until the phase completes
 constexpr int LAZY_MAX_INT = 8;          // softmax reference max kept within 2^8 of the true one
 constexpr float LAZY_MAX = static_cast<float>(LAZY_MAX_INT);
 constexpr int SLABS = D / 32;
-constexpr int MERGE_THREADS = 512;
 constexpr int BF16_ITEMS = DECODE_BF16_ITEMS;
 
 // Warps per CTA: all sixteen when a warp fits in 128 registers, fewer where the
@@ -75,16 +71,19 @@ struct Tune {
 };
 
 struct Seg {
+  int valid;
   int ri, head;    // request index in the launch, kv head
   int p0, p1;      // INT2 pages [p0, p1) of this CTA
-  int bf16;        // the segment's BF16 pages belong to this CTA
-  int slot;        // INT2 record: segment + CTA
+  int slot;        // INT2 record: segment + INT2 CTA
+  int c_lo, c_hi;  // the INT2 CTAs whose ranges meet the segment
 };
 
 struct DecodeArgs {
-  int n, ncta, front_writes;
+  int n, ncta, nbc, front_writes;   // nbc: the first nbc CTAs take the BF16 blocks
   int64_t total_cost;
   DecodeDebug dbg;
+  const uint16_t* k_new;   // fused step: the appended token's K / V rows (batch rows), else null
+  const uint16_t* v_new;
   DecodeReq r[DECODE_PER_LAUNCH];
 };
 
@@ -207,47 +206,92 @@ template <int G, int GK>
 struct Smem {
   static constexpr int NW = Tune<G, GK>::NW;
   static constexpr int NPART = Tune<G, GK>::THREADS / D;   // row parts of the q rotation
-  // INT2: per-warp TMA rings; at the end of a segment (every copy consumed): the
-  // warps' states; BF16 sub-pages: each warp's K and V rows in its ring
-  union {
+  // per-warp TMA rings of INT2 page records; while no copy is in flight (the merge
+  // of a segment) the staging of the merged records
+  struct {
     __align__(128) uint8_t ring[NW][STAGES][record_for(GK)];
-    float state[NW][G][PART];
   } buf;
+  __align__(16) float state[NW][G][PART];   // each warp's partial (o, m, l) before the CTA combine
   union {
     struct {
       float q[G][D];
       float part[NPART][G][D];
       float norm[G];
     } pro;                              // rotation of q
+    struct {
+      __align__(16) float hist[G][D];   // O_hist of the merged segment
+      float part[NPART][G][D];          // row parts of O_hist R_V^T
+    } mrg;                              // merge of a segment (last CTA)
   } scr;
-  __align__(16) uint32_t qf[2][QFrag<G>::WORDS];   // q operands of segment e in slot e & 1 (read as uint4)
+  __align__(16) uint32_t qf[QFrag<G>::WORDS];   // q operands of the current segment (read as uint4)
   __align__(8) uint64_t bar[NW][STAGES];
+  uint64_t mbar_m;                       // staging of a merge's records
   __align__(16) float4 meta[NW][PAGE];   // INT2: per token {s_k, z_k, s_v 2^ew, z_v}; BF16: weights
   __align__(16) float4 meta2[NW][GK == 64 ? PAGE : 1];   // G_K = 64: the same for group 1
   WeightRows<G, GK, NW> w;
-  int nseg;
-  Seg seg[SEGMAX];
+  float wf[NW][8];                       // combine: per (warp, head) factor 2^(m_w - M)
+  float mh[8], lh[8];                    // combine: per head M and L
+  Seg seg[2];                            // segment e in slot e & 1
+  int64_t u_next;                        // first cost unit after the last planned segment
+  int last;                              // this CTA merges the segment just finished
 };
 
-// q_rot = q R_K for the G query heads of (request, kv head), written as the q
-// operands of slot `slot` (layout above).  Every thread of the CTA takes part:
-// thread (part p, column c) sums rows [p RP, (p + 1) RP) of column c of R_K.
+// Rows of R_K that thread (part p, column c) of the q rotation uses: rows
+// [p RP, (p + 1) RP) of column c.  R_K is written once, when the cache is
+// created, so it may be read before the launch waits for the preceding grid.
 template <int G, int GK>
-__device__ void build_qfrag(const DevCache& c, int layer, const DecodeReq& R, int head,
-                            const uint16_t* __restrict__ q, Smem<G, GK>& sm, int slot) {
+struct RkRows {
+  static constexpr int NPART = Smem<G, GK>::NPART;
+  static constexpr int RP = (D + NPART - 1) / NPART;
+  float v[RP];
+};
+template <int G, int GK>
+__device__ __forceinline__ void load_rk(const DevCache& c, int layer, int head, RkRows<G, GK>& rk) {
+  constexpr int RP = RkRows<G, GK>::RP;
+  const int t = threadIdx.x, ch = t % D, part = t / D;
+  const int r0 = part * RP, r1 = min(D, r0 + RP);
+  const float* __restrict__ RK = c.rot_k + ((size_t)layer * c.Hkv + head) * D * D;
+#pragma unroll
+  for (int i = 0; i < RP; ++i) rk.v[i] = (r0 + i < r1) ? __ldg(RK + (size_t)(r0 + i) * D + ch) : 0.0f;
+}
+
+// The G query rows of (request, kv head): element t + k NTH of the G x 128 block
+// in qv[k] (loaded ahead of the rotation, so that the load overlaps others).
+template <int G, int GK>
+struct QRows {
+  static constexpr int N = (G * D + Tune<G, GK>::THREADS - 1) / Tune<G, GK>::THREADS;
+  uint16_t v[N];
+};
+template <int G, int GK>
+__device__ __forceinline__ void load_q(const DevCache& c, const DecodeReq& R, int head,
+                                       const uint16_t* __restrict__ q, QRows<G, GK>& qv) {
+  constexpr int NTH = Tune<G, GK>::THREADS;
+  const uint16_t* qrow = q + ((size_t)R.batch_row * c.Hq + (size_t)head * G) * D;
+#pragma unroll
+  for (int k = 0; k < QRows<G, GK>::N; ++k) {
+    const int i = threadIdx.x + k * NTH;
+    qv.v[k] = i < G * D ? qrow[i] : 0;
+  }
+}
+
+// q_rot = q R_K for the G query heads of (request, kv head), written as the q
+// operands (layout above).  Every thread of the CTA takes part: thread (part p,
+// column c) sums rows [p RP, (p + 1) RP) of column c of R_K (held in rk).
+template <int G, int GK>
+__device__ __forceinline__ void build_qfrag(const DevCache& c, const QRows<G, GK>& qv, const RkRows<G, GK>& rkr,
+                                            Smem<G, GK>& sm) {
   constexpr int NTH = Tune<G, GK>::THREADS, NPART = Smem<G, GK>::NPART;
-  constexpr int RP = (D + NPART - 1) / NPART;
+  constexpr int RP = RkRows<G, GK>::RP;
   constexpr int REGS = QFrag<G>::REGS;
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-  const uint16_t* qrow = q + ((size_t)R.batch_row * c.Hq + (size_t)head * G) * D;
-  const float* __restrict__ RK = c.rot_k + ((size_t)layer * c.Hkv + head) * D * D;
   const int ch = t % D, part = t / D;
   const int r0 = part * RP, r1 = min(D, r0 + RP);
-  float rk[RP];
+  const float* rk = rkr.v;
 #pragma unroll
-  for (int i = 0; i < RP; ++i) rk[i] = (r0 + i < r1) ? __ldg(RK + (size_t)(r0 + i) * D + ch) : 0.0f;
-  for (int i = t; i < G * D; i += NTH)
-    sm.scr.pro.q[i / D][i % D] = __uint_as_float(static_cast<uint32_t>(qrow[i]) << 16);
+  for (int k = 0; k < QRows<G, GK>::N; ++k) {
+    const int i = t + k * NTH;
+    if (i < G * D) sm.scr.pro.q[i / D][i % D] = __uint_as_float(static_cast<uint32_t>(qv.v[k]) << 16);
+  }
   __syncthreads();
   float acc[G];
 #pragma unroll
@@ -292,7 +336,7 @@ __device__ void build_qfrag(const DevCache& c, int layer, const DecodeReq& R, in
     }
     return max(-60, min(e, 60));
   };
-  uint32_t* dst = sm.qf[slot];
+  uint32_t* dst = sm.qf;
   for (int wi = t; wi < 32 * REGS; wi += NTH) {
     const int lane_w = wi / REGS, k = wi % REGS;
     const int gid = lane_w >> 2, tid = lane_w & 3;
@@ -323,17 +367,64 @@ __device__ void build_qfrag(const DevCache& c, int layer, const DecodeReq& R, in
   __syncthreads();
 }
 
+// The warps' states in shared memory (sm.state[w][h]: o[128], m, l) combined
+// into one record per query head at part_out (o[128], M, L): warp 0 forms the
+// per-(warp, head) factors 2^(m_w - M), then every thread sums (head, channel)
+// pairs over the warps.
+template <int G, int GK>
+__device__ __forceinline__ void cta_combine(Smem<G, GK>& sm, float* part_out) {
+  constexpr int NW = Tune<G, GK>::NW, NTH = Tune<G, GK>::THREADS;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  static_assert(G <= NW, "one warp per head forms the factors");
+  __syncthreads();   // every warp's state is in shared memory
+  if (warp < G) {
+    // warp h: lane w holds warp w's (m, l) of head h
+    const int h = warp;
+    const float m = lane < NW ? sm.state[lane][h][PARTIAL_M] : -INFINITY;
+    const float lw = lane < NW ? sm.state[lane][h][PARTIAL_L] : 0.0f;
+    float M = m;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float f = m == -INFINITY ? 0.0f : exp2f(m - M);
+    float l = lw * f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    if (lane < NW) sm.wf[lane][h] = f;
+    if (lane == 0) {
+      sm.mh[h] = M;
+      sm.lh[h] = l;
+    }
+  }
+  __syncthreads();
+  for (int i = t; i < G * D; i += NTH) {
+    const int h = i / D, ch = i % D;
+    float acc = 0.0f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) acc = fmaf(sm.state[w][h][ch], sm.wf[w][h], acc);
+    part_out[h * PART + ch] = acc;
+  }
+  if (t < G) {
+    part_out[t * PART + PARTIAL_M] = sm.mh[t];
+    part_out[t * PART + PARTIAL_L] = sm.lh[t];
+  }
+  __syncthreads();   // the states are read before the rings are reused
+}
+
 // The first STAGES page copies of warp w's share of a segment's pages [p0, p1)
 // (pages p0 + w + NW j, j < STAGES), by lane 0, into stages nc + j; the hot page
 // (written by a preceding fused append) only once that grid has completed.  Copy
-// number `hold` of warp 0 is not issued (failure-detection hook; -1: none).
+// number `hold` of warp 0 is not issued (failure-detection hook; -1: none), and a
+// warp whose earlier wait ran out issues nothing (it would never wait for it).
 template <int G, int GK>
 __device__ __forceinline__ void int2_issue_first(const DevCache& c, int layer, const DecodeReq& R, int head, int p0,
-                                                 int p1, Smem<G, GK>& sm, bool front_writes, uint32_t nc, int hold) {
+                                                 int p1, Smem<G, GK>& sm, bool front_writes, uint32_t nc, int hold,
+                                                 bool timed_out) {
   constexpr int NW = Tune<G, GK>::NW;
   constexpr int REC = record_for(GK);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane != 0) return;
+  if (lane != 0 || timed_out) return;
+  // the rings may have been written through the generic proxy since their last copy
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   const int32_t* pt = c.hist_pt + (size_t)R.slot * c.max_pages;
   const uint8_t* base = c.int2 + layer * c.int2_layer_stride + (size_t)head * REC;
   int32_t ids[STAGES];
@@ -374,7 +465,7 @@ template <int G, int GK>
 __device__ __forceinline__ void int2_pages(const DevCache& c, int layer, const DecodeReq& R, int head, int p0,
                                            int p1, const uint32_t* __restrict__ qf, Smem<G, GK>& sm,
                                            float* part_out, uint32_t limit, bool front_writes, uint32_t& nc,
-                                           bool& timed_out, bool first_issued, int hold) {
+                                           bool& timed_out, int hold) {
   constexpr int NW = Tune<G, GK>::NW;
   constexpr int NT = QFrag<G>::NT;       // n-tiles of 8 columns = 4 heads x (hi, lo)
   constexpr int REC = record_for(GK);
@@ -433,25 +524,12 @@ __device__ __forceinline__ void int2_pages(const DevCache& c, int layer, const D
     skip_bits = skip ? (skip_bits | bit) : (skip_bits & ~bit);
   };
   auto held = [&](int j) { return warp == 0 && static_cast<int>(nc + j) == hold; };
-  auto issue = [&](int j) {
-    bool skip;
-    const uint8_t* src = page_src(j, skip);
-    note(j, skip);
-    if (lane == 0 && j < my_n && !timed_out && !held(j)) {
-      const int st = (nc + j) % STAGES;
-      mbar_expect_tx(&sm.bar[warp][st], REC);
-      tma_load_1d(sm.buf.ring[warp][st], src, REC, &sm.bar[warp][st]);
-    }
-  };
+  // the first STAGES copies were issued by int2_issue_first: their skip flags
 #pragma unroll
   for (int j = 0; j < STAGES; ++j) {
-    if (first_issued) {   // copies already out: only the skip flags
-      bool skip;
-      page_src(j, skip);
-      note(j, skip);
-    } else {
-      issue(j);
-    }
+    bool skip;
+    page_src(j, skip);
+    note(j, skip);
   }
   // weights p * s_v are prescaled by 2^ew so the smallest ones stay representable in
   // fp16: s_v <= fp16(2 tau_V / 3) and p <= 2^LAZY_MAX, so p s_v 2^ew <= 2^15
@@ -775,7 +853,6 @@ __device__ __forceinline__ void int2_pages(const DevCache& c, int layer, const D
       if (!held(j)) mbar_wait(&sm.bar[warp][(nc + j) % STAGES], ((nc + j) / STAGES) & 1, DECODE_WAIT_LIMIT);
   }
   nc += static_cast<uint32_t>(my_n);
-  __syncthreads();   // every warp is done with every ring before states overwrite them
 
   // ---- this warp's state -> shared memory (rotated basis, unscaled, z term added)
 #pragma unroll
@@ -791,7 +868,7 @@ __device__ __forceinline__ void int2_pages(const DevCache& c, int layer, const D
     }
     const int h = 4 * nt + tid;
     if (h < G) {
-      float* st = sm.buf.state[warp][h];
+      float* st = sm.state[warp][h];
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         if constexpr (GK == 128) {
@@ -812,68 +889,33 @@ __device__ __forceinline__ void int2_pages(const DevCache& c, int layer, const D
       }
     }
   }
-  __syncthreads();
-  // ---- merge the warps: thread t < 128 owns channel t
-  const int t = threadIdx.x;
-  if (t < D) {
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) M = fmaxf(M, sm.buf.state[w][h][PARTIAL_M]);
-      float acc_o = 0.0f, acc_l = 0.0f;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float mw = sm.buf.state[w][h][PARTIAL_M];
-        if (mw == -INFINITY) continue;
-        const float f = exp2f(mw - M);
-        acc_o = fmaf(sm.buf.state[w][h][t], f, acc_o);
-        acc_l = fmaf(sm.buf.state[w][h][PARTIAL_L], f, acc_l);
-      }
-      part_out[h * PART + t] = acc_o;
-      if (t == 0) {
-        part_out[h * PART + PARTIAL_M] = M;
-        part_out[h * PART + PARTIAL_L] = acc_l;
-      }
-    }
-  }
-  __syncthreads();   // states read before the rings take the next segment's copies
+  cta_combine<G, GK>(sm, part_out);
 }
 
 // ---- BF16 sink and recent pages ------------------------------------------------------
-constexpr int BF_SUB = 16;                   // rows per sub-page (one k-step of P V)
+constexpr int BF_SUB = 16;                            // rows per sub-page (one k-step of P V)
 constexpr int BF_SUBS = BF16_ITEMS * PAGE / BF_SUB;   // 20 sub-pages per segment
-constexpr int BF_PITCH = D + 8;              // bf16 per staged row: ldmatrix without bank conflicts
-constexpr int BF_WPITCH = BF_SUB + 8;        // bf16 per weight column
-struct BfStage {
-  __align__(16) uint16_t k[BF_SUB][BF_PITCH];
-  __align__(16) uint16_t v[BF_SUB][BF_PITCH];
-};
+constexpr int BF_WPITCH = BF_SUB + 8;                 // bf16 per weight column
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
-  const uint32_t d = smem_u32(dst);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(valid ? 16 : 0) : "memory");
-}
-__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(p)));
-}
-__device__ __forceinline__ void ldsm4_t(uint32_t (&r)[4], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(p)));
-}
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 __device__ __forceinline__ uint16_t bf16_bits(float x) {
   const __nv_bfloat16 h = __float2bfloat16_rn(x);
   return *reinterpret_cast<const uint16_t*>(&h);
+}
+__device__ __forceinline__ uint32_t word_of(const uint4 (&v)[4], int w) {
+  const uint4 x = v[w >> 2];
+  return (w & 3) == 0 ? x.x : (w & 3) == 1 ? x.y : (w & 3) == 2 ? x.z : x.w;
+}
+__device__ __forceinline__ uint32_t word_of(const uint4 (&v)[2], int w) {
+  const uint4 x = v[w >> 2];
+  return (w & 3) == 0 ? x.x : (w & 3) == 1 ? x.y : (w & 3) == 2 ? x.z : x.w;
 }
 
 // Whether BF16 row r of item `which` (0 sink, 1..4 ring pages) holds a cached token:
@@ -892,34 +934,49 @@ __device__ __forceinline__ bool bf16_row_valid(const DecodeReq& R, int which, in
 // unrotated q, as 16-row sub-pages spread over the CTA's warps (warp w takes
 // sub-pages w, w + NW, ... of the twenty; a sub-page without a cached row is
 // skipped).  q K^T and P V run on mma.sync m16n8k16 bf16 with fp32 accumulation: q
-// is exact in bf16, P is carried as bf16 hi + lo, so every product is exact.  Rows
-// outside the window are zero-filled by the copies and masked.  The CTA's partial
-// for every query head of the group goes to part_out.  Each warp stages its rows
-// in its own (consumed) TMA ring and its weights in its meta rows.
+// is exact in bf16, P is carried as bf16 hi + lo, so every product is exact.  The
+// K and V rows go from global memory straight into the fragments (no shared
+// memory staging), so the block runs while the segment's INT2 copies land in the
+// rings:
+//   * q K^T: A = K (16 rows x 16 channels per k-step); k index 2 tid + e of step s
+//     is channel 32 tid + 4 s + e and 2 tid + 8 + e is 32 tid + 4 s + 2 + e, so
+//     lane (gid, tid) reads 64 contiguous bytes of rows gid and gid + 8; B = q with
+//     column n = head 4 nt + (n >> 1) (each head twice, the hi / lo pair of P V);
+//   * P V^T: A = V^T (16 channels x 16 tokens); row gid of m-tile mt is channel
+//     16 gid + 2 mt and row gid + 8 is that channel + 1, so lane (gid, tid) reads 32
+//     contiguous bytes of each of its tokens 2 tid, 2 tid + 1, 2 tid + 8, 2 tid + 9
+//     and pairs tokens with byte permutes; B = P, columns (head, hi / lo), through
+//     the warp's weight columns in its meta rows.
+// Rows outside the window are masked (K) or zeroed (V).  After a fused append the
+// row of the appended token is read from that step's input (knew / vnew, the row
+// of this request and kv head) rather than from the ring page the append writes,
+// so no row depends on the append kernel's completion.  The CTA's partial for
+// every query head of the group goes to part_out.
 template <int G, int GK>
 __device__ void bf16_block(const DevCache& c, int layer, const DecodeReq& R, int head,
-                           const uint16_t* __restrict__ q, Smem<G, GK>& sm, float* part_out) {
+                           const uint16_t* __restrict__ q, const uint16_t* knew, const uint16_t* vnew,
+                           Smem<G, GK>& sm, float* part_out) {
   constexpr int NW = Tune<G, GK>::NW;
   constexpr int NT = QFrag<G>::NT;
-  static_assert(sizeof(BfStage) <= STAGES * record_for(GK), "BF16 stage in the ring");
   static_assert(NT * 8 * BF_WPITCH * 2 <= PAGE * sizeof(float4), "BF16 weights in the meta rows");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tid = lane & 3;
   const float scale2 = c.scale * LOG2E;
-  BfStage& sg = *reinterpret_cast<BfStage*>(sm.buf.ring[warp][0]);
-  uint16_t (*wc)[8][BF_WPITCH] = reinterpret_cast<uint16_t (*)[8][BF_WPITCH]>(&sm.meta[warp][0]);
-  // q as the B operand of K q^T: column n of n-tile nt is query head 4 nt + (n >> 1)
-  // (each head twice), k-step s, registers (b0, b1)
+  uint16_t(*wc)[8][BF_WPITCH] = reinterpret_cast<uint16_t(*)[8][BF_WPITCH]>(&sm.meta[warp][0]);
+  // q as the B operand of K q^T
   uint32_t bq[NT][8][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const int g = 4 * nt + (gid >> 1);
-    const uint16_t* qh = q + ((size_t)R.batch_row * c.Hq + (size_t)head * G + (g < G ? g : 0)) * D;
+    const int h = 4 * nt + (gid >> 1);
+    uint4 qw[4];
+    const uint4* qs =
+        reinterpret_cast<const uint4*>(q + ((size_t)R.batch_row * c.Hq + (size_t)head * G + (h < G ? h : 0)) * D +
+                                       32 * tid);
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const uint32_t x0 = *reinterpret_cast<const uint32_t*>(qh + 16 * s + 2 * tid);
-      const uint32_t x1 = *reinterpret_cast<const uint32_t*>(qh + 16 * s + 2 * tid + 8);
-      bq[nt][s][0] = g < G ? x0 : 0u;
-      bq[nt][s][1] = g < G ? x1 : 0u;
+    for (int i = 0; i < 4; ++i) qw[i] = h < G ? __ldg(qs + i) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int st = 0; st < 8; ++st) {
+      bq[nt][st][0] = word_of(qw, 2 * st);
+      bq[nt][st][1] = word_of(qw, 2 * st + 1);
     }
   }
   float o[NT][8][4];
@@ -933,18 +990,25 @@ __device__ void bf16_block(const DevCache& c, int layer, const DecodeReq& R, int
 #pragma unroll
       for (int e = 0; e < 4; ++e) o[nt][mt][e] = 0.0f;
   }
-  const int arow = (lane & 7) + 8 * ((lane >> 3) & 1), acol = 8 * (lane >> 4);   // K as A (ldmatrix)
-  const int vrow = (lane & 7) + 8 * (lane >> 4), vcol = 8 * ((lane >> 3) & 1);   // V^T as A (ldmatrix.trans)
+  // item and row of the appended token (position T - 1), when it is read from the step's input
+  int new_which = -1, new_row = -1;
+  if (knew != nullptr) {
+    const int p = R.tokens - 1;
+    if (p < SINK) {
+      new_which = 0;
+      new_row = p;
+    } else {
+      const int slot = (p - SINK) % RECENT;
+      new_which = 1 + slot / PAGE;
+      new_row = slot % PAGE;
+    }
+  }
   for (int sp = warp; sp < BF_SUBS; sp += NW) {
     const int which = sp / (PAGE / BF_SUB), r0 = BF_SUB * (sp % (PAGE / BF_SUB));
     // rows of this sub-page holding a cached token (bit i: row r0 + i); lanes 0..15 test one row each
     const uint32_t rows = __ballot_sync(0xffffffffu, lane < BF_SUB && bf16_row_valid(R, which, r0 + lane)) & 0xffffu;
     if (rows == 0u) continue;
-    int page = which == 0 ? R.sink_page
-             : which == 1 ? R.ring_page[0]
-             : which == 2 ? R.ring_page[1]
-             : which == 3 ? R.ring_page[2]
-                          : R.ring_page[3];
+    int page = which == 0 ? R.sink_page : R.ring_page[which - 1];
     if (page < 0 || page >= c.n_bf16_pages) {
       if (lane == 0) atomicOr(c.err, ERR_BF16_PAGE);
       page = 0;
@@ -952,35 +1016,53 @@ __device__ void bf16_block(const DevCache& c, int layer, const DecodeReq& R, int
     const uint16_t* kb = c.bf16 + layer * c.bf16_layer_stride + ((size_t)page * c.Hkv + head) * BF16_RECORD_ELEMS +
                          (size_t)r0 * D;
     const uint16_t* vb = kb + (size_t)PAGE * D;
+    const int nrow = which == new_which ? new_row - r0 : -1;   // row of the appended token in this sub-page
+    auto krow = [&](int r) { return r == nrow ? knew : kb + (size_t)r * D; };
+    auto vrow = [&](int r) { return r == nrow ? vnew : vb + (size_t)r * D; };
+    // K rows gid and gid + 8, channels 32 tid .. 32 tid + 31 (a row outside the
+    // window is read all the same -- in bounds -- and its logits are masked)
+    uint4 ka[4], kc[4];
+    {
+      const uint4* pa = reinterpret_cast<const uint4*>(krow(gid) + 32 * tid);
+      const uint4* pc = reinterpret_cast<const uint4*>(krow(gid + 8) + 32 * tid);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int idx = u * 32 + lane, row = idx >> 4, part = idx & 15;
-      const bool ok = (rows >> row) & 1u;
-      cp_async16(&sg.k[row][8 * part], kb + (ok ? row * D + 8 * part : 0), ok);
-      cp_async16(&sg.v[row][8 * part], vb + (ok ? row * D + 8 * part : 0), ok);
+      for (int i = 0; i < 4; ++i) {
+        ka[i] = __ldg(pa + i);
+        kc[i] = __ldg(pc + i);
+      }
     }
-    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-    __syncwarp();
+    // V rows of tokens 2 tid, 2 tid + 1, 2 tid + 8, 2 tid + 9, channels 16 gid .. 16 gid + 15;
+    // zero outside the window (P is zero there, and 0 x NaN would not be)
+    uint4 vv[4][2];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int r = 2 * tid + (k & 1) + 8 * (k >> 1);
+      const bool ok = (rows >> r) & 1u;
+      const uint4* pv = reinterpret_cast<const uint4*>(vrow(r) + 16 * gid);
+      vv[k][0] = ok ? __ldg(pv) : make_uint4(0u, 0u, 0u, 0u);
+      vv[k][1] = ok ? __ldg(pv + 1) : make_uint4(0u, 0u, 0u, 0u);
+    }
     // ---- logits: S [16 rows x 8 columns] per n-tile over the 128 channels
-    float s[NT][4];
+    float sa[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s[nt][e] = 0.0f;
+      for (int e = 0; e < 4; ++e) sa[nt][e] = 0.0f;
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      uint32_t af[4];
-      ldsm4(af, &sg.k[arow][16 * ks + acol]);
+    for (int st = 0; st < 8; ++st) {
+      const uint32_t a0 = word_of(ka, 2 * st), a1 = word_of(kc, 2 * st);
+      const uint32_t a2 = word_of(ka, 2 * st + 1), a3 = word_of(kc, 2 * st + 1);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_bf16(s[nt], af, bq[nt][ks][0], bq[nt][ks][1]);
+      for (int nt = 0; nt < NT; ++nt) mma_bf16(sa[nt], a0, a1, a2, a3, bq[nt][st][0], bq[nt][st][1]);
     }
-    // ---- softmax of the lane's head 4 nt + tid over rows gid, gid + 8; the weights
-    // go to the warp's weight columns as bf16 hi (column 2 tid) and lo (2 tid + 1)
+    // ---- softmax of the lane's head 4 nt + tid over rows gid, gid + 8 (column 2 tid;
+    // column 2 tid + 1 repeats it); the weights go to the warp's weight columns as
+    // bf16 hi (column 2 tid) and lo (2 tid + 1)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const bool hok = 4 * nt + tid < G;
-      const float la = (hok && ((rows >> gid) & 1u)) ? s[nt][0] * scale2 : -INFINITY;
-      const float lb = (hok && ((rows >> (gid + 8)) & 1u)) ? s[nt][2] * scale2 : -INFINITY;
+      const float la = (hok && ((rows >> gid) & 1u)) ? sa[nt][0] * scale2 : -INFINITY;
+      const float lb = (hok && ((rows >> (gid + 8)) & 1u)) ? sa[nt][2] * scale2 : -INFINITY;
       float pm = fmaxf(la, lb);
       pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
       pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
@@ -1013,299 +1095,376 @@ __device__ void bf16_block(const DevCache& c, int layer, const DecodeReq& R, int
     }
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-      uint32_t af[4];
-      ldsm4_t(af, &sg.v[vrow][16 * mt + vcol]);
+      const uint32_t w0 = word_of(vv[0], mt), w1 = word_of(vv[1], mt);
+      const uint32_t w2 = word_of(vv[2], mt), w3 = word_of(vv[3], mt);
+      const uint32_t a0 = __byte_perm(w0, w1, 0x5410), a1 = __byte_perm(w0, w1, 0x7632);
+      const uint32_t a2 = __byte_perm(w2, w3, 0x5410), a3 = __byte_perm(w2, w3, 0x7632);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_bf16(o[nt][mt], af, bw[nt][0], bw[nt][1]);
+      for (int nt = 0; nt < NT; ++nt) mma_bf16(o[nt][mt], a0, a1, a2, a3, bw[nt][0], bw[nt][1]);
     }
-    __syncwarp();   // the stage and the weights are free
+    __syncwarp();   // the weight columns are free
   }
-  // ---- this warp's state -> shared memory (over the rings: every warp is done with
-  // its ring first), then the warps merged per channel
-  __syncthreads();
+  // ---- this warp's state -> shared memory: lane (gid, tid) holds head 4 nt + tid,
+  // channels 16 gid .. 16 gid + 15
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     float l = l_run[nt];
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-    const int g = 4 * nt + tid;
-    if (g < G) {
-      float* st = sm.buf.state[warp][g];
+    const int h = 4 * nt + tid;
+    if (h < G) {
+      float4* st = reinterpret_cast<float4*>(&sm.state[warp][h][16 * gid]);
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        // o rows: channels 16 mt + gid and + 8; columns hi and lo of head g
-        st[16 * mt + gid] = o[nt][mt][0] + o[nt][mt][1];
-        st[16 * mt + gid + 8] = o[nt][mt][2] + o[nt][mt][3];
-      }
+      for (int k = 0; k < 4; ++k)
+        st[k] = make_float4(o[nt][2 * k][0] + o[nt][2 * k][1], o[nt][2 * k][2] + o[nt][2 * k][3],
+                            o[nt][2 * k + 1][0] + o[nt][2 * k + 1][1], o[nt][2 * k + 1][2] + o[nt][2 * k + 1][3]);
       if (gid == 0) {
-        st[PARTIAL_M] = m_run[nt];
-        st[PARTIAL_L] = l;
+        sm.state[warp][h][PARTIAL_M] = m_run[nt];
+        sm.state[warp][h][PARTIAL_L] = l;
       }
     }
   }
-  __syncthreads();
-  const int t = threadIdx.x;
-  if (t < D) {
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) M = fmaxf(M, sm.buf.state[w][h][PARTIAL_M]);
-      float acc_o = 0.0f, acc_l = 0.0f;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float mw = sm.buf.state[w][h][PARTIAL_M];
-        if (mw == -INFINITY) continue;
-        const float f = exp2f(mw - M);
-        acc_o = fmaf(sm.buf.state[w][h][t], f, acc_o);
-        acc_l = fmaf(sm.buf.state[w][h][PARTIAL_L], f, acc_l);
-      }
-      part_out[h * PART + t] = acc_o;
-      if (t == 0) {
-        part_out[h * PART + PARTIAL_M] = M;
-        part_out[h * PART + PARTIAL_L] = acc_l;
-      }
-    }
-  }
-  __syncthreads();
+  cta_combine<G, GK>(sm, part_out);
 }
 
 // ---- the decode kernel --------------------------------------------------------------
 __device__ __forceinline__ int64_t cta_begin(int c, int ncta, int64_t total) { return (int64_t)c * total / ncta; }
 
-// Segment containing cost unit u: request index, kv head, its first unit.
+// Cost units of one segment on the INT2 line: a set-up (the q rotation and the
+// latency of the first pages, paid again by a CTA that enters the segment from
+// another) then its pages; none for a request without history pages.
+__device__ __forceinline__ int64_t seg_units(const DecodeReq& R) {
+  return R.npages > 0 ? (int64_t)R.npages + DECODE_SEGMENT_SETUP_COST : 0;
+}
+
+// Segment containing INT2 cost unit u: request index, kv head, its first unit
+// (requests without history pages hold no unit and are passed over).
 __device__ __forceinline__ void segment_of(const DecodeArgs& a, int Hkv, int64_t u, int& ri, int& h, int64_t& s0) {
   ri = 0;
   while (ri + 1 < a.n && a.r[ri + 1].cost_start <= u) ++ri;
-  const int64_t per = a.r[ri].npages + a.r[ri].bf16_cost;
+  const int64_t per = seg_units(a.r[ri]);
   h = static_cast<int>((u - a.r[ri].cost_start) / per);
   if (h >= Hkv) h = Hkv - 1;
   s0 = a.r[ri].cost_start + (int64_t)h * per;
 }
 
-// Records in the workspace: INT2 record of (segment s, CTA c) at slot s + c (the
-// CTAs meeting one segment are consecutive, so the slots are unique), then the
-// BF16 record of segment s.
+// INT2 CTA (index among the INT2 CTAs) whose cost range holds unit u.
+__device__ __forceinline__ int cta_of(int64_t u, int ncta, int64_t total) {
+  int c = static_cast<int>(u * ncta / total);
+  while (c > 0 && cta_begin(c, ncta, total) > u) --c;
+  while (c + 1 < ncta && cta_begin(c + 1, ncta, total) <= u) ++c;
+  return c;
+}
+
+// The segment holding INT2 cost unit u of this INT2 CTA's range [u0, u1) (invalid
+// once u reaches u1); end receives its first unit past the segment.
+__device__ Seg plan_segment(const DecodeArgs& a, int Hkv, int icta, int64_t u, int64_t u0, int64_t u1,
+                            int64_t& end) {
+  Seg e{};
+  end = u1;
+  if (u >= u1) return e;
+  int ri, h;
+  int64_t s0;
+  segment_of(a, Hkv, u, ri, h, s0);
+  const int64_t np = a.r[ri].npages;
+  const int n2 = a.ncta - a.nbc;
+  end = s0 + seg_units(a.r[ri]);
+  const int64_t f0 = s0 + DECODE_SEGMENT_SETUP_COST;   // unit of page 0
+  e.valid = 1;
+  e.ri = ri;
+  e.head = h;
+  e.p0 = static_cast<int>(u0 > f0 ? (u0 - f0 < np ? u0 - f0 : np) : 0);
+  e.p1 = static_cast<int>(u1 > f0 ? (u1 - f0 < np ? u1 - f0 : np) : 0);
+  if (e.p1 < e.p0) e.p1 = e.p0;
+  e.slot = ri * Hkv + h + icta;
+  e.c_lo = cta_of(s0, n2, a.total_cost);
+  e.c_hi = cta_of(end - 1, n2, a.total_cost);
+  return e;
+}
+
+// Atomic add with release (this CTA's records, made visible to thread 0 by the
+// barrier before it, are visible before the count) and acquire (the records of
+// the CTAs counted before are visible after it) semantics at GPU scope.
+__device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Merge of segment s = (ri, head) by the last CTA to finish it: the INT2 records
+// of its n2 INT2 CTAs c_lo .. c_lo + n2 - 1 and its BF16 record, online-softmax
+// combined per (query head, channel); then out = (O_bf16 + O_hist R_V^T) / L for
+// the G query heads.  The records (consecutive in the workspace) are staged into
+// the rings, which hold no copy at this point, by bulk copies of up to CAP
+// records; while the first copy is in flight every thread loads its rows of
+// R_V^T (coalesced: thread (part p, column c) reads column c of rows
+// [p RP, (p + 1) RP)).
+template <int G, int GK>
+__device__ void merge_segment(const DevCache& c, int layer, const DecodeArgs& a, int ri, int head, int c_lo, int n2,
+                              const float* recs, const float* bf16_recs, float* __restrict__ out, Smem<G, GK>& sm,
+                              uint32_t& mphase) {
+  constexpr int NTH = Tune<G, GK>::THREADS, NPART = Smem<G, GK>::NPART;
+  constexpr int PAIRS = (G * D + NTH - 1) / NTH;          // (head, channel) pairs per thread
+  constexpr int RF = G * PART;                            // floats per record
+  constexpr int CAP = int(sizeof(sm.buf.ring) / (RF * sizeof(float))) - 1;   // records per chunk
+  constexpr int RP = (D + NPART - 1) / NPART;                                // R_V^T rows per part
+  constexpr int U = 4;
+  static_assert(CAP >= 1, "staging");
+  const int t = threadIdx.x;
+  const DecodeReq& R = a.r[ri];
+  const int s = ri * c.Hkv + head;
+  const int items = n2;
+  float* stage = reinterpret_cast<float*>(&sm.buf.ring[0][0][0]);   // [CAP][RF], then the BF16 record
+  auto issue = [&](int j0, int nk) {
+    if (t == 0) {
+      // the rings were last written through the generic proxy (weights)
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_expect_tx(&sm.mbar_m, (nk + (j0 == 0 ? 1 : 0)) * RF * 4);
+      if (nk > 0) tma_load_1d(stage, recs + (size_t)(s + c_lo + j0) * RF, nk * RF * 4, &sm.mbar_m);
+      if (j0 == 0) tma_load_1d(stage + CAP * RF, bf16_recs + (size_t)s * RF, RF * 4, &sm.mbar_m);
+    }
+  };
+  issue(0, min(CAP, items));
+  const int rch = t % D, rpart = t / D, r0 = rpart * RP;
+  float rv[RP];
+  {
+    const float* __restrict__ RVt = c.rot_vt + ((size_t)layer * c.Hkv + head) * D * D + rch;
+#pragma unroll
+    for (int i = 0; i < RP; ++i) rv[i] = r0 + i < D ? __ldg(RVt + (size_t)(r0 + i) * D) : 0.0f;
+  }
+  float M[PAIRS], L[PAIRS], oh[PAIRS], bm[PAIRS], bl[PAIRS], bo[PAIRS];
+#pragma unroll
+  for (int k = 0; k < PAIRS; ++k) {
+    M[k] = bm[k] = -INFINITY;
+    L[k] = oh[k] = bl[k] = bo[k] = 0.0f;
+  }
+  for (int j0 = 0; j0 == 0 || j0 < items; j0 += CAP) {   // the first chunk also brings the BF16 record
+    const int nk = min(CAP, items - j0);
+    if (j0 > 0) issue(j0, nk);
+    if (!mbar_wait(&sm.mbar_m, mphase, DECODE_WAIT_LIMIT) && t == 0) atomicOr(c.err, ERR_TIMEOUT);
+    mphase ^= 1u;
+#pragma unroll
+    for (int k = 0; k < PAIRS; ++k) {
+      const int i = t + k * NTH;
+      if (i < G * D) {
+        const int g = i / D, ch = i % D;
+        const float* r = stage + g * PART;
+        float mn = M[k];
+        for (int j = 0; j < nk; j += U) {
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+            if (j + u < nk) mn = fmaxf(mn, r[(j + u) * RF + PARTIAL_M]);
+        }
+        if (mn > M[k]) {
+          const float f = M[k] == -INFINITY ? 0.0f : exp2f(M[k] - mn);
+          L[k] *= f;
+          oh[k] *= f;
+          M[k] = mn;
+        }
+        for (int j = 0; j < nk; j += U) {
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            if (j + u < nk) {
+              const float* rj = r + (j + u) * RF;
+              const float mj = rj[PARTIAL_M];
+              const float f = mj == -INFINITY ? 0.0f : exp2f(mj - M[k]);
+              L[k] = fmaf(rj[PARTIAL_L], f, L[k]);
+              oh[k] = fmaf(rj[ch], f, oh[k]);
+            }
+          }
+        }
+        if (j0 == 0) {
+          bm[k] = r[CAP * RF + PARTIAL_M];
+          bl[k] = r[CAP * RF + PARTIAL_L];
+          bo[k] = r[CAP * RF + ch];
+        }
+      }
+    }
+    __syncthreads();   // the stage is read before the next chunk (or the next copies) land
+  }
+  float ob[PAIRS], lt[PAIRS];
+#pragma unroll
+  for (int k = 0; k < PAIRS; ++k) {
+    const int i = t + k * NTH;
+    const float Mt = fmaxf(M[k], bm[k]);
+    const float fh = M[k] == -INFINITY ? 0.0f : exp2f(M[k] - Mt);
+    const float fb = bm[k] == -INFINITY ? 0.0f : exp2f(bm[k] - Mt);
+    if (i < G * D) sm.scr.mrg.hist[i / D][i % D] = oh[k] * fh;
+    ob[k] = bo[k] * fb;
+    lt[k] = fmaf(L[k], fh, bl[k] * fb);
+  }
+  __syncthreads();
+  {
+    float acc[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) acc[g] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < RP; ++i) {
+      if (r0 + i < D) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) acc[g] = fmaf(sm.scr.mrg.hist[g][r0 + i], rv[i], acc[g]);
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) sm.scr.mrg.part[rpart][g][rch] = acc[g];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < PAIRS; ++k) {
+    const int i = t + k * NTH;
+    if (i < G * D) {
+      const int g = i / D, ch = i % D;
+      float v = ob[k];
+#pragma unroll
+      for (int p = 0; p < NPART; ++p) v += sm.scr.mrg.part[p][g][ch];
+      out[((size_t)R.batch_row * c.Hq + (size_t)head * G + g) * D + ch] = v / lt[k];
+    }
+  }
+  __syncthreads();   // the scratch is free for the next q rotation
+}
+
+// The BF16 pages of segment (ri, head) into its BF16 record.
+template <int G, int GK>
+__device__ __forceinline__ void bf16_segment(const DevCache& c, int layer, const DecodeArgs& a, int ri, int head,
+                                             const uint16_t* q, Smem<G, GK>& sm, float* bf16_recs) {
+  const DecodeReq& R = a.r[ri];
+  const size_t row = ((size_t)R.batch_row * c.Hkv + head) * D;
+  bf16_block<G, GK>(c, layer, R, head, q, a.k_new ? a.k_new + row : nullptr, a.v_new ? a.v_new + row : nullptr, sm,
+                    bf16_recs + (size_t)(ri * c.Hkv + head) * G * PART);
+}
+
+// This CTA is done with segment (ri, head), whose records come from n2 INT2 CTAs
+// (c_lo ..) and one BF16 CTA: count it in the segment's counter; the CTA that
+// completes the count merges the segment.  The block before ends with a barrier,
+// so every record store of this CTA comes before the count.
+template <int G, int GK>
+__device__ __forceinline__ void count_and_merge(const DevCache& c, int layer, const DecodeArgs& a, int ri, int head,
+                                                int c_lo, int n2, const float* recs, const float* bf16_recs,
+                                                float* out, Smem<G, GK>& sm, uint32_t& mphase) {
+  if (threadIdx.x == 32 * (Tune<G, GK>::NW - 1) + 1) {   // a thread that issues no page copy
+    int* cnt = c.dec_count + (size_t)a.r[ri].slot * c.Hkv + head;
+    const int last = atomic_add_acq_rel(cnt, 1) + 1 == n2 + 1;
+    if (last) atomicExch(cnt, 0);   // ready for the next launch
+    sm.last = last;
+  }
+  __syncthreads();
+  if (sm.last) merge_segment<G, GK>(c, layer, a, ri, head, c_lo, n2, recs, bf16_recs, out, sm, mphase);
+}
+
+// Records in the workspace: INT2 record of (segment s, INT2 CTA c) at slot s + c
+// (the INT2 CTAs meeting one segment are consecutive, so the slots are unique),
+// then the BF16 record of segment s.
 template <int G, int GK>
 __global__ void __launch_bounds__(Tune<G, GK>::THREADS, 1)
-    decode_kernel(DevCache c, int layer, DecodeArgs a, const uint16_t* __restrict__ q, float* __restrict__ recs) {
+    decode_kernel(DevCache c, int layer, DecodeArgs a, const uint16_t* __restrict__ q, float* __restrict__ recs,
+                  float* __restrict__ out) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem<G, GK>& sm = *reinterpret_cast<Smem<G, GK>*>(smem_raw);
   const int t = threadIdx.x, warp = t >> 5;
   const int cta = blockIdx.x;
   float* int2_recs = recs;
   float* bf16_recs = recs + ((size_t)a.n * c.Hkv + a.ncta) * G * PART;
+  const bool fw = a.front_writes != 0;
+  const int n2cta = a.ncta - a.nbc;   // INT2 CTAs
 
-  if (!a.front_writes) grid_dep_wait();   // the cache may have been written by the preceding grid
-  grid_dep_launch();                      // the merge grid may be scheduled; it waits for this one
-  if (t == 0) {
-    const int64_t u0 = cta_begin(cta, a.ncta, a.total_cost), u1 = cta_begin(cta + 1, a.ncta, a.total_cost);
-    int n = 0;
-    for (int64_t u = u0; u < u1;) {
-      int ri, h;
-      int64_t s0;
-      segment_of(a, c.Hkv, u, ri, h, s0);
-      const DecodeReq& R = a.r[ri];
-      const int64_t np = R.npages, end = s0 + np + R.bf16_cost;
-      if (n == SEGMAX) {
-        atomicOr(c.err, ERR_PLAN);
-        break;
-      }
-      Seg& e = sm.seg[n++];
-      e.ri = ri;
-      e.head = h;
-      const int64_t lo = u0 - s0 > 0 ? u0 - s0 : 0, hi = u1 - s0 < np ? u1 - s0 : np;
-      e.p0 = static_cast<int>(lo < np ? lo : np);
-      e.p1 = static_cast<int>(hi > e.p0 ? hi : e.p0);
-      e.bf16 = (R.bf16_cost > 0 && s0 + np >= u0 && s0 + np < u1) ? 1 : 0;
-      e.slot = ri * c.Hkv + h + cta;
-      u = end;
-    }
-    sm.nseg = n;
-  }
   if ((t & 31) == 0) {
 #pragma unroll
     for (int st = 0; st < STAGES; ++st) mbar_init(&sm.bar[warp][st], 1);
+    if (t == 0) mbar_init(&sm.mbar_m, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncthreads();
-  const int nseg = sm.nseg;
-  uint32_t nc = 0;          // copies this warp has consumed
-  bool timed_out = false;   // a wait of this warp ran out: no further copies
-  const int hold = cta == 0 ? a.dbg.hold_copy : -1;
-  // the first segment's first copies go out before q is rotated
-  if (nseg > 0) {
-    int2_issue_first<G, GK>(c, layer, a.r[sm.seg[0].ri], sm.seg[0].head, sm.seg[0].p0, sm.seg[0].p1, sm,
-                            a.front_writes != 0, nc, hold);
-    build_qfrag<G, GK>(c, layer, a.r[sm.seg[0].ri], sm.seg[0].head, q, sm, 0);
-  }
-  for (int e = 0; e < nseg; ++e) {
-    const Seg S = sm.seg[e];
-    int2_pages<G, GK>(c, layer, a.r[S.ri], S.head, S.p0, S.p1, sm.qf[e & 1], sm,
-                      int2_recs + (size_t)S.slot * G * PART, a.dbg.wait_limit, a.front_writes != 0, nc, timed_out,
-                      e == 0, hold);
-    if (e + 1 < nseg) build_qfrag<G, GK>(c, layer, a.r[sm.seg[e + 1].ri], sm.seg[e + 1].head, q, sm, (e + 1) & 1);
-  }
-  // BF16 pages of the segments whose BF16 block this CTA holds (every INT2 copy
-  // has been consumed: the rings are free)
-  bool any = false;
-  for (int e = 0; e < nseg; ++e) any |= sm.seg[e].bf16 != 0;
-  if (!any) return;
-  if (a.front_writes) grid_dep_wait();   // a ring page may hold the token just appended
-  for (int e = 0; e < nseg; ++e) {
-    const Seg S = sm.seg[e];
-    if (S.bf16)
-      bf16_block<G, GK>(c, layer, a.r[S.ri], S.head, q, sm,
-                        bf16_recs + (size_t)(S.ri * c.Hkv + S.head) * G * PART);
-  }
-}
+  uint32_t mphase = 0;        // phase of the merge staging barrier
 
-// ---- merge: one CTA per (request, query head) -----------------------------------------
-// Warp w folds items w, w + 16, ... (the segment's BF16 record, then its INT2
-// records) into a running (M, L, O_bf16, O_hist) with lane l owning channels
-// 4 l .. 4 l + 3; the warp states are combined, O_hist is rotated back by R_V^T
-// (staged in shared memory before the records are waited for) and the output row
-// written.
-constexpr int MERGE_WARPS = MERGE_THREADS / 32;
-constexpr int MERGE_UNROLL = 8;
-struct MergeSmem {
-  float rvt[D][D];                     // R_V^T of the kv head: rvt[j][c] = R_V[c][j]
-  __align__(16) float ob[MERGE_WARPS][D];
-  __align__(16) float oh[MERGE_WARPS][D];
-  float m[MERGE_WARPS], l[MERGE_WARPS];
-  float hist[D], bf[D], part[MERGE_THREADS / D][D];
-  float L;
-};
-
-template <int G>
-__global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(DevCache c, int layer, DecodeArgs a,
-                                                              const float* __restrict__ recs, float* __restrict__ out) {
-  extern __shared__ __align__(16) uint8_t merge_raw[];
-  MergeSmem& sm = *reinterpret_cast<MergeSmem*>(merge_raw);
-  const int ri = blockIdx.x / c.Hq, hq = blockIdx.x % c.Hq;
-  const int head = hq / G, g = hq % G;
-  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-  {
-    // R_V^T is written once at set-up: stage it while the decode grid runs
-    const float4* src = reinterpret_cast<const float4*>(c.rot_vt + ((size_t)layer * c.Hkv + head) * D * D);
-    float4* dst = reinterpret_cast<float4*>(&sm.rvt[0][0]);
-    constexpr int N4 = D * D / 4 / MERGE_THREADS;
-    float4 v[N4];
-#pragma unroll
-    for (int u = 0; u < N4; ++u) v[u] = __ldg(src + u * MERGE_THREADS + t);
-#pragma unroll
-    for (int u = 0; u < N4; ++u) dst[u * MERGE_THREADS + t] = v[u];
-  }
-  grid_dep_wait();
-  grid_dep_launch();
-  const DecodeReq& R = a.r[ri];
-  const int s = ri * c.Hkv + head;
-  // the CTAs whose cost ranges meet the segment: c_lo .. c_hi
-  const int64_t per = (int64_t)R.npages + R.bf16_cost;
-  const int64_t s0 = R.cost_start + (int64_t)head * per, s1 = s0 + per;
-  int c_lo = static_cast<int>(s0 * a.ncta / a.total_cost);
-  while (c_lo > 0 && cta_begin(c_lo, a.ncta, a.total_cost) > s0) --c_lo;
-  while (cta_begin(c_lo + 1, a.ncta, a.total_cost) <= s0) ++c_lo;
-  int c_hi = static_cast<int>((s1 - 1) * a.ncta / a.total_cost);
-  while (c_hi > 0 && cta_begin(c_hi, a.ncta, a.total_cost) > s1 - 1) --c_hi;
-  while (cta_begin(c_hi + 1, a.ncta, a.total_cost) <= s1 - 1) ++c_hi;
-  const int items = 1 + (c_hi - c_lo + 1);
-  const float* bf16_recs = recs + ((size_t)a.n * c.Hkv + a.ncta) * G * PART;
-  auto item_ptr = [&](int i) -> const float* {
-    return i == 0 ? bf16_recs + ((size_t)s * G + g) * PART : recs + ((size_t)(s + c_lo + i - 1) * G + g) * PART;
-  };
-  float M = -INFINITY, L = 0.0f;
-  float4 ob = make_float4(0.0f, 0.0f, 0.0f, 0.0f), oh = ob;
-  for (int i0 = w; i0 < items; i0 += MERGE_WARPS * MERGE_UNROLL) {
-    float mv[MERGE_UNROLL], lv[MERGE_UNROLL];
-    float4 ov[MERGE_UNROLL];
-#pragma unroll
-    for (int u = 0; u < MERGE_UNROLL; ++u) {
-      const int i = i0 + MERGE_WARPS * u;
-      if (i < items) {
-        const float* p = item_ptr(i);
-        mv[u] = __ldcg(p + PARTIAL_M);
-        lv[u] = __ldcg(p + PARTIAL_L);
-        ov[u] = __ldcg(reinterpret_cast<const float4*>(p) + lane);
-      } else {
-        mv[u] = -INFINITY;
-        lv[u] = 0.0f;
-        ov[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  if (cta < a.nbc) {
+    // ---- a BF16 CTA: the BF16 blocks of segments cta, cta + nbc, ... (none of
+    // their rows is written by a fused append: the appended token comes from k / v)
+    __syncthreads();
+    if (!fw) grid_dep_wait();   // q and the cache may have been written by the preceding grid
+    grid_dep_launch();          // the next launch may be scheduled; it waits for this grid to complete
+    for (int s = cta; s < a.n * c.Hkv; s += a.nbc) {
+      const int ri = s / c.Hkv, head = s % c.Hkv;
+      const DecodeReq& R = a.r[ri];
+      if (warp == 0 && (t & 31) < 4) {   // R_V rows of the merge, should this CTA do it
+        const float* rv = c.rot_v + ((size_t)layer * c.Hkv + head) * D * D;
+        prefetch_l2(rv + (size_t)(t & 31) * (D * D / 4), D * D);
       }
+      bf16_segment<G, GK>(c, layer, a, ri, head, q, sm, bf16_recs);
+      int c_lo = 0, n2 = 0;
+      if (R.npages > 0 && n2cta > 0) {
+        const int64_t s0 = R.cost_start + (int64_t)head * seg_units(R);
+        c_lo = cta_of(s0, n2cta, a.total_cost);
+        n2 = cta_of(s0 + seg_units(R) - 1, n2cta, a.total_cost) - c_lo + 1;
+      }
+      count_and_merge<G, GK>(c, layer, a, ri, head, c_lo, n2, int2_recs, bf16_recs, out, sm, mphase);
     }
-    float mn = M;
-#pragma unroll
-    for (int u = 0; u < MERGE_UNROLL; ++u) mn = fmaxf(mn, mv[u]);
-    if (mn > M) {
-      const float f = (M == -INFINITY) ? 0.0f : exp2f(M - mn);
-      L *= f;
-      ob.x *= f; ob.y *= f; ob.z *= f; ob.w *= f;
-      oh.x *= f; oh.y *= f; oh.z *= f; oh.w *= f;
-      M = mn;
-    }
-#pragma unroll
-    for (int u = 0; u < MERGE_UNROLL; ++u) {
-      const float f = (mv[u] == -INFINITY) ? 0.0f : exp2f(mv[u] - M);
-      L = fmaf(lv[u], f, L);
-      const bool is_bf = i0 + MERGE_WARPS * u == 0;
-      const float fb = is_bf ? f : 0.0f, fh = is_bf ? 0.0f : f;
-      ob.x = fmaf(ov[u].x, fb, ob.x);
-      ob.y = fmaf(ov[u].y, fb, ob.y);
-      ob.z = fmaf(ov[u].z, fb, ob.z);
-      ob.w = fmaf(ov[u].w, fb, ob.w);
-      oh.x = fmaf(ov[u].x, fh, oh.x);
-      oh.y = fmaf(ov[u].y, fh, oh.y);
-      oh.z = fmaf(ov[u].z, fh, oh.z);
-      oh.w = fmaf(ov[u].w, fh, oh.w);
-    }
+    return;
   }
-  reinterpret_cast<float4*>(sm.ob[w])[lane] = ob;
-  reinterpret_cast<float4*>(sm.oh[w])[lane] = oh;
-  if (lane == 0) {
-    sm.m[w] = M;
-    sm.l[w] = L;
+
+  // ---- an INT2 CTA: its range [u0, u1) of the INT2 pages, segment by segment
+  const int icta = cta - a.nbc;
+  const int64_t u0 = cta_begin(icta, n2cta, a.total_cost), u1 = cta_begin(icta + 1, n2cta, a.total_cost);
+  if (t == 0) {
+    int64_t end;
+    sm.seg[0] = plan_segment(a, c.Hkv, icta, u0, u0, u1, end);
+    sm.u_next = end;
   }
   __syncthreads();
-  if (t < D) {
-    float Mt = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < MERGE_WARPS; ++k) Mt = fmaxf(Mt, sm.m[k]);
-    float Lt = 0.0f, b = 0.0f, h = 0.0f;
-#pragma unroll
-    for (int k = 0; k < MERGE_WARPS; ++k) {
-      const float f = (sm.m[k] == -INFINITY) ? 0.0f : exp2f(sm.m[k] - Mt);
-      Lt = fmaf(sm.l[k], f, Lt);
-      b = fmaf(sm.ob[k][t], f, b);
-      h = fmaf(sm.oh[k][t], f, h);
-    }
-    sm.bf[t] = b;
-    sm.hist[t] = h;
-    if (t == 0) sm.L = Lt;
-  }
-  __syncthreads();
+  uint32_t nc = 0;            // copies this warp has consumed
+  bool timed_out = false;     // a wait of this warp ran out: no further copies
+  const int hold = a.dbg.hold_copy;   // failure-detection hook: warp 0 of every INT2 CTA
   {
-    // out_c = O_bf16_c + sum_j O_hist_j R_V^T[j][c]; thread (quarter q, c) sums rows
-    // 32 q .. 32 q + 31
-    constexpr int ROWS = D * D / MERGE_THREADS;
-    const int ch = t & (D - 1), qr = t / D;
-    float acc = 0.0f;
-#pragma unroll
-    for (int j = ROWS * qr; j < ROWS * qr + ROWS; ++j) acc = fmaf(sm.hist[j], sm.rvt[j][ch], acc);
-    sm.part[qr][ch] = acc;
+    const Seg S = sm.seg[0];
+    RkRows<G, GK> rk;
+    if (S.valid) load_rk<G, GK>(c, layer, S.head, rk);
+    if (!fw) grid_dep_wait();   // the cache and q may have been written by the preceding grid
+    grid_dep_launch();          // the next launch may be scheduled; it waits for this grid to complete
+    if (S.valid) {
+      QRows<G, GK> qv;
+      load_q<G, GK>(c, a.r[S.ri], S.head, q, qv);   // in flight with the page-id loads of the copies
+      int2_issue_first<G, GK>(c, layer, a.r[S.ri], S.head, S.p0, S.p1, sm, fw, nc, hold, timed_out);
+      build_qfrag<G, GK>(c, qv, rk, sm);
+    }
   }
-  __syncthreads();
-  if (t < D) {
-    float v = 0.0f;
-#pragma unroll
-    for (int k = 0; k < MERGE_THREADS / D; ++k) v += sm.part[k][t];
-    out[((size_t)R.batch_row * c.Hq + hq) * D + t] = (sm.bf[t] + v) / sm.L;
+  // segment e is in slot e & 1; its fields are read from shared memory where they
+  // are needed, so that none stays in registers across the page loop
+  for (int e = 0; sm.seg[e & 1].valid; ++e) {
+    const int cur = e & 1, nxt = cur ^ 1;
+    if (t == 0) {
+      int64_t end;
+      sm.seg[nxt] = plan_segment(a, c.Hkv, icta, sm.u_next, u0, u1, end);
+      sm.u_next = end;
+    }
+    {
+      const Seg& S = sm.seg[cur];
+      int2_pages<G, GK>(c, layer, a.r[S.ri], S.head, S.p0, S.p1, sm.qf, sm, int2_recs + (size_t)S.slot * G * PART,
+                        a.dbg.wait_limit, fw, nc, timed_out, hold);
+    }
+    {
+      const Seg& S = sm.seg[cur];
+      count_and_merge<G, GK>(c, layer, a, S.ri, S.head, S.c_lo, S.c_hi - S.c_lo + 1, int2_recs, bf16_recs, out, sm,
+                             mphase);
+    }
+    // the next segment: first copies, q rotation
+    if (sm.seg[nxt].valid) {
+      const Seg& N = sm.seg[nxt];
+      RkRows<G, GK> rk;
+      QRows<G, GK> qv;
+      load_rk<G, GK>(c, layer, N.head, rk);
+      load_q<G, GK>(c, a.r[N.ri], N.head, q, qv);
+      int2_issue_first<G, GK>(c, layer, a.r[N.ri], N.head, N.p0, N.p1, sm, fw, nc, hold, timed_out);
+      build_qfrag<G, GK>(c, qv, rk, sm);
+    }
   }
 }
 
 template <int G, int GK>
 cudaError_t launch_decode_t(const DevCache& c, int layer, const DecodeReq* reqs, const DecodePlan& p,
-                            const uint16_t* q, float* out, void* workspace, bool front_writes, DecodeDebug dbg,
-                            cudaStream_t s) {
+                            const uint16_t* q, float* out, void* workspace, bool front_writes, const uint16_t* k_new,
+                            const uint16_t* v_new, DecodeDebug dbg, cudaStream_t s) {
   static_assert(sizeof(Smem<G, GK>) <= 227 * 1024, "shared memory");
   using SM = Smem<G, GK>;
   static_assert(offsetof(SM, qf) % 16 == 0 && (QFrag<G>::WORDS * 4) % 16 == 0, "q operands: uint4 loads");
@@ -1317,20 +1476,19 @@ cudaError_t launch_decode_t(const DevCache& c, int layer, const DecodeReq* reqs,
   if (dev >= 32 || !(attr_done & (1u << dev))) {
     e = cudaFuncSetAttribute(decode_kernel<G, GK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(sizeof(Smem<G, GK>)));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(merge_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(sizeof(MergeSmem)));
     if (e != cudaSuccess) return e;
     if (dev < 32) attr_done |= 1u << dev;
   }
   DecodeArgs a;
   a.n = p.n;
   a.ncta = p.ncta;
+  a.nbc = p.nbc;
   a.front_writes = front_writes ? 1 : 0;
   a.total_cost = p.total_cost;
   a.dbg = dbg;
+  a.k_new = front_writes ? k_new : nullptr;
+  a.v_new = front_writes ? v_new : nullptr;
   for (int i = 0; i < p.n; ++i) a.r[i] = reqs[i];
-  float* recs = static_cast<float*>(workspace);
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1341,22 +1499,18 @@ cudaError_t launch_decode_t(const DevCache& c, int layer, const DecodeReq* reqs,
   cfg.stream = s;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, decode_kernel<G, GK>, c, layer, a, q, recs);
-  if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3(static_cast<unsigned>(p.n * c.Hq));
-  cfg.blockDim = dim3(MERGE_THREADS);
-  cfg.dynamicSmemBytes = sizeof(MergeSmem);
-  return cudaLaunchKernelEx(&cfg, merge_kernel<G>, c, layer, a, static_cast<const float*>(recs), out);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<G, GK>, c, layer, a, q, static_cast<float*>(workspace), out);
 }
 
 template <int GK>
 cudaError_t launch_decode_g(const DevCache& c, int layer, const DecodeReq* reqs, const DecodePlan& p,
-                            const uint16_t* q, float* out, void* ws, bool fw, DecodeDebug dbg, cudaStream_t s) {
+                            const uint16_t* q, float* out, void* ws, bool fw, const uint16_t* kn, const uint16_t* vn,
+                            DecodeDebug dbg, cudaStream_t s) {
   switch (c.G) {
-    case 1: return launch_decode_t<1, GK>(c, layer, reqs, p, q, out, ws, fw, dbg, s);
-    case 2: return launch_decode_t<2, GK>(c, layer, reqs, p, q, out, ws, fw, dbg, s);
-    case 4: return launch_decode_t<4, GK>(c, layer, reqs, p, q, out, ws, fw, dbg, s);
-    case 8: return launch_decode_t<8, GK>(c, layer, reqs, p, q, out, ws, fw, dbg, s);
+    case 1: return launch_decode_t<1, GK>(c, layer, reqs, p, q, out, ws, fw, kn, vn, dbg, s);
+    case 2: return launch_decode_t<2, GK>(c, layer, reqs, p, q, out, ws, fw, kn, vn, dbg, s);
+    case 4: return launch_decode_t<4, GK>(c, layer, reqs, p, q, out, ws, fw, kn, vn, dbg, s);
+    case 8: return launch_decode_t<8, GK>(c, layer, reqs, p, q, out, ws, fw, kn, vn, dbg, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1364,11 +1518,13 @@ cudaError_t launch_decode_g(const DevCache& c, int layer, const DecodeReq* reqs,
 }  // namespace
 
 cudaError_t launch_decode(const DevCache& c, int layer, const DecodeReq* reqs, const DecodePlan& p,
-                          const uint16_t* q, float* out, void* workspace, bool front_writes, DecodeDebug dbg,
-                          cudaStream_t s) {
-  if (p.n < 1 || p.n > DECODE_PER_LAUNCH || p.ncta < 1) return cudaErrorInvalidValue;
-  return c.gk == 64 ? launch_decode_g<64>(c, layer, reqs, p, q, out, workspace, front_writes, dbg, s)
-                    : launch_decode_g<128>(c, layer, reqs, p, q, out, workspace, front_writes, dbg, s);
+                          const uint16_t* q, float* out, void* workspace, bool front_writes, const uint16_t* k_new,
+                          const uint16_t* v_new, DecodeDebug dbg, cudaStream_t s) {
+  if (p.n < 1 || p.n > DECODE_PER_LAUNCH || p.nbc < 1 || p.ncta < p.nbc || p.total_cost < p.ncta - p.nbc)
+    return cudaErrorInvalidValue;
+  return c.gk == 64
+             ? launch_decode_g<64>(c, layer, reqs, p, q, out, workspace, front_writes, k_new, v_new, dbg, s)
+             : launch_decode_g<128>(c, layer, reqs, p, q, out, workspace, front_writes, k_new, v_new, dbg, s);
 }
 
 cudaError_t launch_step(const DevCache& c, int layer, const AppendReq* app, int n_app, const uint16_t* k,
@@ -1376,7 +1532,7 @@ cudaError_t launch_step(const DevCache& c, int layer, const AppendReq* app, int 
                         float* out, void* workspace, DecodeDebug dbg, cudaStream_t s) {
   const cudaError_t e = launch_append(c, layer, app, n_app, k, v, s);
   if (e != cudaSuccess) return e;
-  return launch_decode(c, layer, reqs, p, q, out, workspace, true, dbg, s);
+  return launch_decode(c, layer, reqs, p, q, out, workspace, true, k, v, dbg, s);
 }
 
 }  // namespace oscar

@@ -170,6 +170,8 @@ oscar_cache_layout make_layout(const oscar_cache_config& c) {
   off += align256((size_t)c.max_requests * BF16_PAGES_PER_REQ * sizeof(int32_t));
   l.error_word_offset = off;
   off += 256;
+  l.decode_count_offset = off;
+  off += align256((size_t)c.max_requests * H * sizeof(int32_t));
   l.total_bytes = off;
   return l;
 }
@@ -249,6 +251,7 @@ oscar_status oscar_cache_create(const oscar_cache_config* cfg, void* device_mem,
   d.hist_pt = reinterpret_cast<int32_t*>(base + c->lay.hist_pt_offset);
   d.bf16_pt = reinterpret_cast<int32_t*>(base + c->lay.bf16_pt_offset);
   d.err = reinterpret_cast<int32_t*>(base + c->lay.error_word_offset);
+  d.dec_count = reinterpret_cast<int32_t*>(base + c->lay.decode_count_offset);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int dev = 0;
@@ -262,6 +265,8 @@ oscar_status oscar_cache_create(const oscar_cache_config* cfg, void* device_mem,
     e = cudaMemsetAsync(d.hist_pt, 0xff, (size_t)c->cfg.max_requests * c->cfg.max_pages_per_request * 4, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(d.bf16_pt, 0xff, (size_t)c->cfg.max_requests * BF16_PAGES_PER_REQ * 4, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(d.err, 0, 4, s);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(d.dec_count, 0, (size_t)c->cfg.max_requests * c->cfg.num_kv_heads * sizeof(int32_t), s);
   if (e == cudaSuccess) e = launch_rotation_setup(d, rot_k, rot_v, rk, rv, rkt, rvt, rcn, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) {
@@ -512,41 +517,19 @@ oscar_status write_batch(oscar_cache* c, int32_t layer, int32_t n, const int32_t
 // BF16 sub-pages (16 rows) of one kv head holding a cached token: the sink rows
 // [0, min(T, 64)); ring slot s = 64 (page - 1) + r holds position
 // he + ((s - (he - 64)) mod 256), cached while below T.
-int bf16_sub_pages(int64_t T, int64_t he) {
-  int n = 0;
-  for (int sp = 0; sp < DECODE_BF16_ITEMS * PAGE / 16; ++sp) {
-    const int which = sp / 4;
-    bool any = false;
-    for (int r = 16 * (sp % 4); r < 16 * (sp % 4) + 16 && !any; ++r) {
-      if (which == 0) {
-        any = r < std::min<int64_t>(T, SINK);
-      } else if (T > SINK) {
-        const int64_t s = PAGE * (which - 1) + r;
-        const int64_t p = he + (((s - (he - SINK)) % RECENT) + RECENT) % RECENT;
-        any = p < T;
-      }
-    }
-    n += any ? 1 : 0;
-  }
-  return n;
-}
-
-constexpr int DECODE_SEGMAX = 16;   // segments one decode CTA may touch (the kernel's table)
-
-// Work split of one decode launch over reqs[0..n), n <= DECODE_PER_LAUNCH: the
-// segments (request, kv head) in order, each its INT2 pages (cost 1) then its BF16
-// block, cut into one contiguous equal-cost range per CTA, one CTA per SM.
+// Work split of one decode launch over reqs[0..n), n <= DECODE_PER_LAUNCH: nbc
+// CTAs for the segments' BF16 blocks, sized so that their blocks take about one
+// CTA's share of the INT2 pages each (DECODE_BF16_BLOCK_COST), at least one and
+// at most one per segment; the other CTAs (one per SM in all, at most one per
+// INT2 page) split the INT2 pages into contiguous equal ranges.
 DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int32_t* reqs, int32_t first_row,
                        DecodeReq* out) {
   const int64_t H = c->cfg.num_kv_heads;
   int64_t cost = 0;
-  std::vector<int64_t> seg_cost;
-  seg_cost.reserve((size_t)n * H);
   for (int32_t i = 0; i < n; ++i) {
     const Request& r = c->reqs[reqs[i]];
     const int64_t T = r.T[layer], he = r.he[layer];
     const int64_t np = pages_for(he);
-    const int64_t bf = (int64_t)DECODE_BF16_SUB_COST * bf16_sub_pages(T, he);
     if (out) {
       DecodeReq& d = out[i];
       d.slot = reqs[i];
@@ -558,57 +541,34 @@ DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int
       d.hot_page = -1;
       d.npages = static_cast<int32_t>(np);
       d.cost_start = static_cast<int32_t>(cost);
-      d.bf16_cost = static_cast<int32_t>(bf);
     }
-    for (int64_t h = 0; h < H; ++h) seg_cost.push_back(np + bf);
-    cost += H * (np + bf);
+    cost += H * (np > 0 ? np + DECODE_SEGMENT_SETUP_COST : 0);
   }
   DecodePlan p{};
   p.n = n;
   p.total_cost = cost;
   p.segments = (int64_t)n * H;
-  int64_t ncta = std::max<int64_t>(1, std::min<int64_t>(c->num_sms, cost));
-  // more CTAs (up to four per SM) while one of them would touch more segments than
-  // its table holds; the caller splits the batch if that is not enough
-  p.worst_segments = 0;
-  for (;;) {
-    int64_t worst = 0, si = 0, s0 = 0;
-    for (int64_t k = 0; k < ncta; ++k) {
-      const int64_t u0 = k * cost / ncta, u1 = (k + 1) * cost / ncta;
-      while (si < (int64_t)seg_cost.size() && s0 + seg_cost[si] <= u0) s0 += seg_cost[si++];
-      int64_t cnt = 0, sj = si, t0 = s0;
-      while (sj < (int64_t)seg_cost.size() && t0 < u1) t0 += seg_cost[sj++], ++cnt;
-      worst = std::max(worst, cnt);
-    }
-    p.worst_segments = static_cast<int>(worst);
-    if (worst <= DECODE_SEGMAX || ncta >= cost || 2 * ncta > 4 * (int64_t)c->num_sms) break;
-    ncta = std::min<int64_t>(cost, 2 * ncta);
-  }
-  p.ncta = static_cast<int>(ncta);
-  p.partial_bytes = align256((size_t)(2 * p.segments + ncta) * decode_record_bytes(c->G()));
+  const int64_t sms = std::max(2, c->num_sms);
+  const int64_t share = cost / sms + 1;   // INT2 cost per CTA were every CTA on INT2 pages
+  int64_t nbc = (p.segments * DECODE_BF16_BLOCK_COST + share - 1) / share;
+  nbc = std::max<int64_t>(1, std::min<int64_t>({nbc, p.segments, cost > 0 ? sms / 2 : sms}));
+  const int64_t n_int2 = std::min<int64_t>(sms - nbc, cost);
+  p.nbc = static_cast<int>(nbc);
+  p.ncta = static_cast<int>(nbc + n_int2);
+  p.partial_bytes = align256((size_t)(2 * p.segments + p.ncta) * decode_record_bytes(c->G()));
   return p;
 }
 
-// Requests per decode launch: DECODE_PER_LAUNCH, halved while some CTA of a
-// launch would touch more segments than its table holds (very uneven lengths).
-int32_t decode_launch_size(const oscar_cache* c, int32_t layer, int32_t n, const int32_t* reqs) {
-  int32_t per = std::min<int32_t>(n, DECODE_PER_LAUNCH);
-  while (per > 1) {
-    bool ok = true;
-    for (int32_t b = 0; b < n && ok; b += per)
-      ok = plan_decode(c, layer, std::min<int32_t>(per, n - b), reqs + b, b, nullptr).worst_segments <= DECODE_SEGMAX;
-    if (ok) break;
-    per = (per + 1) / 2;
-  }
-  return per;
+// Requests per decode launch.
+int32_t decode_launch_size(const oscar_cache*, int32_t, int32_t n, const int32_t*) {
+  return std::min<int32_t>(n, DECODE_PER_LAUNCH);
 }
 
 // Workspace of a decode of n requests, whatever their lengths: per launch an INT2
-// and a BF16 record per (request, kv head), and one INT2 record per CTA (at most
-// four per SM).
+// and a BF16 record per (request, kv head), and one INT2 record per CTA (one per SM).
 size_t decode_bytes_bound(const oscar_cache* c, int32_t n) {
   const int64_t segs = (int64_t)std::min<int32_t>(n, DECODE_PER_LAUNCH) * c->cfg.num_kv_heads;
-  return align256((size_t)(2 * segs + 4 * (int64_t)c->num_sms) * decode_record_bytes(c->G()));
+  return align256((size_t)(2 * segs + (int64_t)c->num_sms) * decode_record_bytes(c->G()));
 }
 
 size_t decode_bytes_needed(const oscar_cache* c, int32_t layer, int32_t n, const int32_t* reqs) {
@@ -623,8 +583,12 @@ size_t decode_bytes_needed(const oscar_cache* c, int32_t layer, int32_t n, const
 
 oscar_status check_decode_batch(oscar_cache* c, int32_t layer, int32_t n, const int32_t* reqs) {
   if (!c->valid_layer(layer) || n < 1 || !reqs) return c->fail(OSCAR_ERR_INVALID_ARG, "bad layer or batch");
+  std::vector<char> seen(c->cfg.max_requests, 0);
   for (int32_t i = 0; i < n; ++i) {
     if (!c->valid_req(reqs[i])) return c->fail(OSCAR_ERR_INVALID_ARG, "bad request id");
+    // each (request, kv head) of a launch owns one merge counter
+    if (seen[reqs[i]]) return c->fail(OSCAR_ERR_INVALID_ARG, "duplicate request id");
+    seen[reqs[i]] = 1;
     if (c->reqs[reqs[i]].T[layer] < 1) return c->fail(OSCAR_ERR_STATE, "request has no cached tokens");
     if (c->reqs[reqs[i]].T[layer] > INT32_MAX) return c->fail(OSCAR_ERR_INVALID_ARG, "request too long");
   }
@@ -692,7 +656,7 @@ oscar_status oscar_decode_attention(oscar_cache* c, int32_t layer, int32_t n, co
   for (int32_t b = 0; b < n; b += per) {
     const int32_t m = std::min<int32_t>(per, n - b);
     const DecodePlan p = plan_decode(c, layer, m, reqs + b, b, dr);
-    const cudaError_t err = launch_decode(c->dc, layer, dr, p, q, out, workspace, false, c->dbg, s);
+    const cudaError_t err = launch_decode(c->dc, layer, dr, p, q, out, workspace, false, nullptr, nullptr, c->dbg, s);
     if (err != cudaSuccess) return c->cuda_fail(err, "decode launch");
   }
   return OSCAR_OK;
@@ -775,10 +739,12 @@ oscar_status oscar_cache_check(oscar_cache* c, void* stream) {
   if (word != 0) {
     const int32_t zero = 0;
     cudaMemcpy(c->dc.err, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    // a launch that reported an error still counts every segment to the end, but
+    // the merge counters are cleared as well so that no count can carry over
+    cudaMemset(c->dc.dec_count, 0, (size_t)c->cfg.max_requests * c->cfg.num_kv_heads * sizeof(int32_t));
     char msg[160];
     std::snprintf(msg, sizeof msg,
-                  "device check failed: error bits 0x%x (1 INT2 page, 2 BF16 page, 4 length, 8 wait timed out, "
-                  "16 decode plan)",
+                  "device check failed: error bits 0x%x (1 INT2 page, 2 BF16 page, 4 length, 8 wait timed out)",
                   word);
     return c->fail((word & ERR_TIMEOUT) ? OSCAR_ERR_TIMEOUT : OSCAR_ERR_DEVICE_CHECK, msg);
   }

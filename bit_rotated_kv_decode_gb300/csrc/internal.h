@@ -42,7 +42,6 @@ constexpr int ERR_INT2_PAGE = 1;
 constexpr int ERR_BF16_PAGE = 2;
 constexpr int ERR_LENGTH = 4;
 constexpr int ERR_TIMEOUT = 8;     // a bounded wait gave up
-constexpr int ERR_PLAN = 16;       // a decode CTA met more segments than it can hold
 
 // Plain pointers into the cache's device memory.
 struct DevCache {
@@ -60,6 +59,7 @@ struct DevCache {
   int32_t* hist_pt;              // [max_requests][max_pages]
   int32_t* bf16_pt;              // [max_requests][5]
   int32_t* err;
+  int32_t* dec_count;            // [max_requests][Hkv]: decode CTAs done with a segment (0 between launches)
   int32_t L, Hq, Hkv, G, max_pages;
   int32_t gk;                    // quantisation group size: 128 or 64
   int32_t record;                // record_for(gk) bytes per (page, kv head)
@@ -119,11 +119,12 @@ constexpr int DEMOTE_PER_LAUNCH = 96;   // kernel arguments stay under 4 KiB
 cudaError_t launch_demote_layers(const DevCache& c, const DemoteEntry* e, int n, cudaStream_t s);
 
 // ---- decode ---------------------------------------------------------------------
-// One launch covers up to DECODE_PER_LAUNCH requests.  The work is the list of
-// segments (request i, kv head h), i major; segment s = i Hkv + h is npages INT2
-// history pages (cost 1 each) followed by its BF16 block (the sink page and the
-// four ring pages, DECODE_BF16_SUB_COST per 16-row sub-page holding a cached
-// token).  CTA c of ncta takes the cost units [c C / ncta, (c + 1) C / ncta).
+// One launch covers up to DECODE_PER_LAUNCH requests; its segments are the
+// (request i, kv head h) pairs, s = i Hkv + h.  The first nbc CTAs attend to the
+// segments' BF16 pages (the sink page and the four ring pages): CTA b takes the
+// BF16 blocks of segments b, b + nbc, ...  The other CTAs share the INT2 history
+// pages: the segments' pages in order (npages per segment, one cost unit each),
+// cut into one contiguous equal range per CTA.
 struct DecodeReq {
   int32_t slot;            // request slot (page-table row)
   int32_t batch_row;       // row of q / out
@@ -133,37 +134,47 @@ struct DecodeReq {
   int32_t ring_page[RING_PAGES];
   int32_t hot_page;        // history page index a preceding fused append writes (-1: none)
   int32_t npages;          // INT2 history pages of each kv head
-  int32_t cost_start;      // first cost unit of (this request, kv head 0)
-  int32_t bf16_cost;       // cost units of the BF16 block of each kv head
+  int32_t cost_start;      // first INT2 cost unit of (this request, kv head 0); each kv head
+                           // takes DECODE_SEGMENT_SETUP_COST + npages units (none if npages is 0)
 };
 constexpr int DECODE_PER_LAUNCH = 64;
-constexpr int DECODE_BF16_SUB_COST = 1;
+// A BF16 block (up to 20 sub-pages of 16 rows) counted as this many INT2 pages
+// when the BF16 CTAs are sized: about the time it takes one CTA.
+constexpr int DECODE_BF16_BLOCK_COST = 40;
+// Cost units in front of each segment's pages on the INT2 line: the set-up a CTA
+// pays on entering a segment (q rotation, first-page latency), in INT2 pages.
+constexpr int DECODE_SEGMENT_SETUP_COST = 40;
 constexpr int DECODE_BF16_ITEMS = 1 + RING_PAGES;   // BF16 pages per (request, kv head)
 struct DecodePlan {
   int n;
-  int ncta;                // persistent CTAs, at most one per SM and at most the total cost
-  int64_t total_cost;
+  int ncta;                // persistent CTAs (at most one per SM): nbc BF16 CTAs, then the INT2 CTAs
+  int nbc;
+  int64_t total_cost;      // INT2 pages of the launch
   int64_t segments;        // n Hkv
-  int worst_segments;      // most segments one CTA touches
   size_t partial_bytes;    // workspace: INT2 records (segments + ncta), then BF16 records (segments)
 };
 // Partial record of one (segment, CTA) or of a segment's BF16 pages: per query head
 // of the group o[128], m (log2 domain), l.
 inline size_t decode_record_bytes(int g) { return (size_t)g * PARTIAL_FLOATS * sizeof(float); }
 // Failure-detection hooks of a launch: mbarrier wait rounds before a wait gives up
-// (ERR_TIMEOUT), and the page copy (issue order) that warp 0 of CTA 0 never
-// issues (-1: none), so that a test can make a wait run out.
+// (ERR_TIMEOUT), and the page copy (issue order) that warp 0 of every INT2 CTA
+// never issues (-1: none), so that a test can make a wait run out.
 struct DecodeDebug {
   uint32_t wait_limit;
   int32_t hold_copy;
 };
 constexpr uint32_t DECODE_WAIT_LIMIT = 100000;   // rounds of up to 20 us each
+// One launch: the CTAs stream their cost ranges, and the last CTA to finish a
+// segment (counted in dec_count) merges it into out.  front_writes: a fused
+// append precedes this launch (see launch_step); k_new / v_new are then its
+// input rows [n][Hkv][128] bf16 (batch rows), read in place of the ring row the
+// append writes.
 cudaError_t launch_decode(const DevCache& c, int layer, const DecodeReq* reqs, const DecodePlan& plan,
-                          const uint16_t* q, float* out, void* workspace, bool front_writes, DecodeDebug dbg,
-                          cudaStream_t s);
+                          const uint16_t* q, float* out, void* workspace, bool front_writes, const uint16_t* k_new,
+                          const uint16_t* v_new, DecodeDebug dbg, cudaStream_t s);
 // Fused step: the append of every request (demoting into reqs[i].hot_page), then
 // the decode, which copies every page the append does not write while the append
-// still runs.
+// still runs, and takes the appended token itself from the step's k / v.
 cudaError_t launch_step(const DevCache& c, int layer, const AppendReq* app, int n_app, const uint16_t* k,
                         const uint16_t* v, const DecodeReq* reqs, const DecodePlan& plan, const uint16_t* q,
                         float* out, void* workspace, DecodeDebug dbg, cudaStream_t s);

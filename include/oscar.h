@@ -103,6 +103,7 @@ typedef struct {
   size_t rot_colnorm_offset;                                       /* fp32 [2][L][Hkv] */
   size_t tau_k_offset, tau_v_offset;                               /* fp32 [L][Hkv] */
   size_t hist_pt_offset, bf16_pt_offset, error_word_offset;
+  size_t decode_count_offset;      /* int32 [max_requests][Hkv], zero between decode launches */
 } oscar_cache_layout;
 
 /* Bytes of device memory oscar_cache_create() needs for cfg (0 if invalid). */
@@ -204,14 +205,19 @@ oscar_status oscar_decode_workspace_bytes(const oscar_cache* cache, int32_t n, c
  * an online-softmax (max / sum) reduction and apply R_V^T to the history part
  * ([MS] section "OSCAR的设计": unpack, scale/zero dequantise, float
  * accumulate, online-softmax merge; [MTP] section "The Serving System").
- *   reqs       host int32 [n] request ids (each with T >= 1).
+ *   reqs       host int32 [n] distinct request ids (each with T >= 1);
+ *              a repeated id is OSCAR_ERR_INVALID_ARG.
  *   q          device bf16 [n][Hq][128].
  *   out        device fp32 [n][Hq][128].
  *   workspace  device, >= oscar_decode_workspace_bytes(), 256-byte aligned;
  *              no initial contents are needed.  Calls that share a workspace
  *              must not overlap on the GPU.
- * The decode is three kernels chained with programmatic dependent launch; the
- * first waits for everything before it on "stream", as any launch does. */
+ * The decode is one kernel per launch of up to 64 requests: one CTA per SM
+ * streams an equal share of the pages, and the last CTA to finish a (request,
+ * kv head) merges it, counted in the cache's per-(request, kv head) counters
+ * (layout decode_count_offset).  The kernel waits for everything before it on
+ * "stream", as any launch does; decodes of the same request must not overlap
+ * on the GPU (on one stream they never do). */
 oscar_status oscar_decode_attention(oscar_cache* cache, int32_t layer, int32_t n, const int32_t* reqs,
                                     const uint16_t* q, float* out, void* workspace, size_t workspace_bytes,
                                     void* stream);
@@ -225,7 +231,7 @@ oscar_status oscar_decode_attention(oscar_cache* cache, int32_t layer, int32_t n
  * of 8 MiB per device inside the library.
  *   Arguments, layouts and results are those of oscar_decode_attention.
  *   Size limit: a batch whose partial records (per launch of up to 64
- *     requests: two per request and kv head plus one per decode CTA, G x 528
+ *     requests: two per request and kv head plus one per SM, G x 528
  *     bytes each) need more than 8 MiB is rejected with OSCAR_ERR_INVALID_ARG
  *     before any work; use oscar_decode_attention with a caller workspace.
  *   Set-up: every call takes the array's address on the current device
@@ -241,10 +247,11 @@ oscar_status oscar_decode_attention_noalloc(oscar_cache* cache, int32_t layer, i
 
 /* One decode step of one layer: oscar_append(layer, n, reqs, k, v) followed by
  * oscar_decode_attention(layer, n, reqs, q, out, workspace), with identical
- * results, as fewer and overlapping launches: the append and the rotation of q
- * run as one kernel, and the decode streams every history page the append does
- * not touch while that kernel is still running ([MTP] section "The Serving
- * System": the write path and decode attention of a step).
+ * results, as overlapping launches: the decode kernel starts while the append
+ * kernel runs, streams every history page the append does not write, waits for
+ * the append only before the one history page a demotion fills, and reads the
+ * appended token itself from k / v ([MTP] section "The Serving System": the
+ * write path and decode attention of a step).
  *   k, v       device bf16 [n][Hkv][128], the new token of each request.
  *   q, out     as oscar_decode_attention.
  *   workspace  device, >= oscar_decode_workspace_bytes() taken before the step
@@ -260,8 +267,8 @@ oscar_status oscar_decode_step(oscar_cache* cache, int32_t layer, int32_t n, con
  * device wait on a page copy makes before it gives up and reports
  * OSCAR_ERR_TIMEOUT through oscar_cache_check (default 100000, must be >= 1).
  * hold_copy: the page copy (numbered in issue order, from 0, across the segments
- * of the CTA) of warp 0 of decode CTA 0 that is never issued, so that its wait
- * runs out (-1, the default, holds none).  A warp whose wait ran out issues no
+ * of the CTA) of warp 0 of every decode CTA that streams history pages that is
+ * never issued, so that its wait runs out (-1, the default, holds none).  A warp whose wait ran out issues no
  * further copy, waits (with the default limit) for the copies it has in flight
  * and skips its remaining pages; the launch's output is then undefined but the
  * device stays usable and the next launch starts clean.  OSCAR_ERR_INVALID_ARG

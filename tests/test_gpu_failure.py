@@ -8,8 +8,9 @@ kernels turn it into a status the host reads, with the device still usable:
     OSCAR_ERR_TIMEOUT, and the next launch (hooks back at their defaults) gives
     exactly the output of a clean launch;
   * an out-of-range page id written into the device page table: the decode's
-    own bounds check reports OSCAR_ERR_DEVICE_CHECK and reads page 0 instead, so
-    the output stays finite; with the id restored the next launch is exact again.
+    own bounds check reports OSCAR_ERR_DEVICE_CHECK and skips that page (a copy of
+    page 0 keeps the ring's sequence), so the output stays finite; with the id
+    restored the next launch is exact again.
 
 No test here traps, asserts on the device or touches an invalid address.
 """
@@ -50,9 +51,10 @@ def _decode(s, reqs, q):
 @pytest.mark.parametrize("hold", [0, 1])
 def test_held_copy_times_out_then_next_launch_is_clean(b, hold):
     from bit_rotated_kv_decode_gb300 import synth
-    # 20000 tokens x 8 kv heads: about 17 cost units per CTA, so warp 0 of CTA 0
-    # has two page copies (hold 0: the first, with the second in flight; hold 1:
-    # the second, after the first was consumed)
+    # 20000 tokens x 8 kv heads: about 19 cost units per CTA on the history pages,
+    # so warp 0 of most such CTAs has one or two page copies (hold 0: the first,
+    # with the second in flight where there is one; hold 1: the second, after the
+    # first was consumed)
     s, reqs = _setup(b, [20000])
     q = synth.queries(0, 0, s.hq, len(reqs), 0, device="cuda")
     clean = _decode(s, reqs, q)
