@@ -45,7 +45,7 @@ class oscar_cache_layout(ctypes.Structure):
         "bf16_pool_offset", "bf16_layer_stride", "bf16_page_stride", "bf16_record_bytes",
         "rot_k_offset", "rot_v_offset", "rot_kt_offset", "rot_vt_offset", "rot_colnorm_offset",
         "tau_k_offset", "tau_v_offset",
-        "hist_pt_offset", "bf16_pt_offset", "error_word_offset", "decode_count_offset")]
+        "hist_pt_offset", "bf16_pt_offset", "error_word_offset", "decode_count_offset", "decode_flag_offset")]
 
 
 class OscarError(RuntimeError):

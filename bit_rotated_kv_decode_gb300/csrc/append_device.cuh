@@ -61,28 +61,18 @@ struct AppendSmem {
   __align__(16) float apart[APPEND_GROUPS][D];
 };
 
-template <int GK>
-__device__ __forceinline__ void append_block(const DevCache& c, int layer, const uint16_t* __restrict__ k,
-                                             const uint16_t* __restrict__ v, const AppendReq& q, int head,
-                                             int which, AppendSmem& sm) {
+// The work of one (request, kv head, K or V) by a unit of APPEND_THREADS
+// consecutive threads (whole warps): t is the thread's index in the unit and
+// sync() a barrier over the unit.
+template <int GK, typename Sync>
+__device__ __forceinline__ void append_work(const DevCache& c, int layer, const uint16_t* __restrict__ k,
+                                            const uint16_t* __restrict__ v, const AppendReq& q, int head, int which,
+                                            AppendSmem& sm, int t, Sync sync) {
   float* xin = sm.xin;
   float (*part)[D] = sm.part;
   float (*apart)[D] = sm.apart;
-  const int t = threadIdx.x;
   const int lane = t & 31, grp = t >> 5;
   const size_t lh = (size_t)layer * c.Hkv + head;
-
-  // Launched with programmatic dependent launch: R is written once at set-up, so
-  // L2 is warmed with this thread's rows while the preceding grid (which may still
-  // be writing k / v or reading the cache) finishes; nothing is read before the wait.
-  if (q.demote_slot >= 0) {
-    const float* R = (which ? c.rot_v : c.rot_k) + lh * D * D;
-#pragma unroll
-    for (int i = 0; i < APPEND_ROWS; ++i)
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(R + (size_t)(APPEND_ROWS * grp + i) * D + 4 * lane));
-  }
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (q.demote_slot >= 0) {
     const bool ok_src = q.src_page >= 0 && q.src_page < c.n_bf16_pages;
@@ -96,7 +86,7 @@ __device__ __forceinline__ void append_block(const DevCache& c, int layer, const
       for (int i = 0; i < APPEND_ROWS; ++i)
         r[i] = __ldg(reinterpret_cast<const float4*>(R + (size_t)(APPEND_ROWS * grp + i) * D) + lane);
       if (t < D) xin[t] = bf16_bits_to_float(bf16_row(c, layer, q.src_page, head, which, q.src_row)[t]);
-      __syncthreads();
+      sync();
       float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f}, aac[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int i = 0; i < APPEND_ROWS; ++i) {
@@ -113,7 +103,7 @@ __device__ __forceinline__ void append_block(const DevCache& c, int layer, const
       }
       reinterpret_cast<float4*>(part[grp])[lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
       reinterpret_cast<float4*>(apart[grp])[lane] = make_float4(aac[0], aac[1], aac[2], aac[3]);
-      __syncthreads();
+      sync();
       if (grp == 0) {
         float x[4], e[4], sabs[4];
 #pragma unroll
@@ -141,7 +131,7 @@ __device__ __forceinline__ void append_block(const DevCache& c, int layer, const
       }
     }
   }
-  __syncthreads();   // the demoted row has been read before its slot is overwritten
+  sync();   // the demoted row has been read before its slot is overwritten
   if (q.in_row >= 0 && t < D) {
     if (q.dst_page < 0 || q.dst_page >= c.n_bf16_pages) {
       if (t == 0) atomicOr(c.err, ERR_BF16_PAGE);
@@ -150,6 +140,26 @@ __device__ __forceinline__ void append_block(const DevCache& c, int layer, const
     const uint16_t* src = (which ? v : k) + ((size_t)q.in_row * c.Hkv + head) * D;
     bf16_row(c, layer, q.dst_page, head, which, q.dst_row)[t] = src[t];
   }
+}
+
+// One block of APPEND_THREADS threads per (request, kv head, K or V), launched
+// with programmatic dependent launch: R is written once at set-up, so L2 is warmed
+// with this thread's rows while the preceding grid (which may still be writing
+// k / v or reading the cache) finishes; nothing else is read before the wait.
+template <int GK>
+__device__ __forceinline__ void append_block(const DevCache& c, int layer, const uint16_t* __restrict__ k,
+                                             const uint16_t* __restrict__ v, const AppendReq& q, int head,
+                                             int which, AppendSmem& sm) {
+  const int t = threadIdx.x, lane = t & 31, grp = t >> 5;
+  if (q.demote_slot >= 0) {
+    const float* R = (which ? c.rot_v : c.rot_k) + ((size_t)layer * c.Hkv + head) * D * D;
+#pragma unroll
+    for (int i = 0; i < APPEND_ROWS; ++i)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(R + (size_t)(APPEND_ROWS * grp + i) * D + 4 * lane));
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  append_work<GK>(c, layer, k, v, q, head, which, sm, t, [] { __syncthreads(); });
 }
 
 }  // namespace oscar

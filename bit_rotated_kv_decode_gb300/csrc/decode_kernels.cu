@@ -47,6 +47,7 @@
 #include <cstddef>
 #include <type_traits>
 
+#include "append_device.cuh"
 #include "internal.h"
 
 namespace oscar {
@@ -79,7 +80,9 @@ struct Seg {
 };
 
 struct DecodeArgs {
-  int n, ncta, nbc, front_writes;   // nbc: the first nbc CTAs take the BF16 blocks
+  int n, ncta, nbc;                 // nbc: the first nbc CTAs take the BF16 blocks
+  int prefetch;                     // the preceding launch is a decode of this cache (see decode_kernel)
+  uint32_t epoch;                   // a decode step (append first) when non-zero
   int64_t total_cost;
   DecodeDebug dbg;
   const uint16_t* k_new;   // fused step: the appended token's K / V rows (batch rows), else null
@@ -232,7 +235,8 @@ struct Smem {
   float wf[NW][8];                       // combine: per (warp, head) factor 2^(m_w - M)
   float mh[8], lh[8];                    // combine: per head M and L
   Seg seg[2];                            // segment e in slot e & 1
-  int64_t u_next;                        // first cost unit after the last planned segment
+  int64_t u_next;                        // last cost unit before the last planned segment
+  uint32_t skip0[NW];                    // per warp: bit j, the first copy j of the segment skips its page
   int last;                              // this CTA merges the segment just finished
 };
 
@@ -410,15 +414,37 @@ __device__ __forceinline__ void cta_combine(Smem<G, GK>& sm, float* part_out) {
   __syncthreads();   // the states are read before the rings are reused
 }
 
+// Bounded wait (one thread) for the append of (request R, kv head) in this step
+// launch: its BF16 CTA releases dec_flag = epoch once the demoted token is in the
+// hot page (and a new page is in the page table).  False, with ERR_TIMEOUT
+// reported, if it gave up.  The hot page is then read through the async proxy.
+__device__ __noinline__ bool wait_append(const DevCache& c, const DecodeReq& R, int head, uint32_t epoch,
+                                         uint32_t limit) {
+  const uint32_t* f = c.dec_flag + (size_t)R.slot * c.Hkv + head;
+  for (uint32_t it = 0; it < limit; ++it) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    if (v == epoch) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      return true;
+    }
+    __nanosleep(256);
+  }
+  atomicOr(c.err, ERR_TIMEOUT);
+  return false;
+}
+
 // The first STAGES page copies of warp w's share of a segment's pages [p0, p1)
 // (pages p0 + w + NW j, j < STAGES), by lane 0, into stages nc + j; the hot page
-// (written by a preceding fused append) only once that grid has completed.  Copy
+// (written by this step's append, epoch != 0) only once that append is done.  Copy
 // number `hold` of warp 0 is not issued (failure-detection hook; -1: none), and a
 // warp whose earlier wait ran out issues nothing (it would never wait for it).
+// phase 1 issues only the copies of pages below npages - 2 (those no decode step
+// launched just before can be writing), phase 2 the others, phase 0 all.
 template <int G, int GK>
 __device__ __forceinline__ void int2_issue_first(const DevCache& c, int layer, const DecodeReq& R, int head, int p0,
-                                                 int p1, Smem<G, GK>& sm, bool front_writes, uint32_t nc, int hold,
-                                                 bool timed_out) {
+                                                 int p1, Smem<G, GK>& sm, uint32_t epoch, uint32_t limit, uint32_t nc,
+                                                 int hold, bool timed_out, int phase = 0) {
   constexpr int NW = Tune<G, GK>::NW;
   constexpr int REC = record_for(GK);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -431,21 +457,26 @@ __device__ __forceinline__ void int2_issue_first(const DevCache& c, int layer, c
 #pragma unroll
   for (int j = 0; j < STAGES; ++j) {
     const int pi = p0 + warp + NW * j;
-    ids[j] = (pi < p1 && !(front_writes && pi == R.hot_page)) ? __ldcg(pt + pi) : 0;
+    ids[j] = (pi < p1 && !(epoch != 0 && pi == R.hot_page)) ? __ldcg(pt + pi) : 0;
   }
 #pragma unroll
   for (int j = 0; j < STAGES; ++j) {
     const int pi = p0 + warp + NW * j;
     if (pi >= p1) break;
+    if (phase != 0 && (pi < R.npages - 2) != (phase == 1)) continue;
     int32_t id = ids[j];
-    if (front_writes && pi == R.hot_page) {
-      grid_dep_wait();
+    bool bad = false;
+    if (epoch != 0 && pi == R.hot_page) {
+      wait_append(c, R, head, epoch, limit);
       id = __ldcg(pt + pi);
     }
     if (id < 0 || id >= c.n_int2_pages) {
       atomicOr(c.err, ERR_INT2_PAGE);
       id = 0;
+      bad = true;
     }
+    // the page loop skips a bad page (page 0 is copied in its place)
+    sm.skip0[warp] = bad ? (sm.skip0[warp] | (1u << j)) : (sm.skip0[warp] & ~(1u << j));
     if (warp == 0 && static_cast<int>(nc + j) == hold) continue;
     const int st = (nc + j) % STAGES;
     mbar_expect_tx(&sm.bar[warp][st], REC);
@@ -464,7 +495,7 @@ __device__ __forceinline__ void int2_issue_first(const DevCache& c, int layer, c
 template <int G, int GK>
 __device__ __forceinline__ void int2_pages(const DevCache& c, int layer, const DecodeReq& R, int head, int p0,
                                            int p1, const uint32_t* __restrict__ qf, Smem<G, GK>& sm,
-                                           float* part_out, uint32_t limit, bool front_writes, uint32_t& nc,
+                                           float* part_out, uint32_t limit, uint32_t epoch, uint32_t& nc,
                                            bool& timed_out, int hold) {
   constexpr int NW = Tune<G, GK>::NW;
   constexpr int NT = QFrag<G>::NT;       // n-tiles of 8 columns = 4 heads x (hi, lo)
@@ -478,7 +509,7 @@ __device__ __forceinline__ void int2_pages(const DevCache& c, int layer, const D
   const int32_t* pt = c.hist_pt + (size_t)R.slot * c.max_pages;
   const uint8_t* base = c.int2 + layer * c.int2_layer_stride + (size_t)head * REC;
   const size_t pstride = (size_t)c.Hkv * REC;
-  const int hot = front_writes ? R.hot_page : -1;
+  const int hot = epoch != 0 ? R.hot_page : -1;
 
   // page ids of this warp's pages, read 32 at a time (lane l holds page 32 b + l of
   // batch b); page_src is called by the whole warp with increasing j.  An id is a
@@ -494,8 +525,8 @@ __device__ __forceinline__ void int2_pages(const DevCache& c, int layer, const D
     }
     return page;
   };
-  // the hot page (written by a preceding fused append) is read only after that
-  // grid has completed: its id is fetched by lane 0 at copy time, after the wait
+  // the hot page (written by this step's append) is read only after that append
+  // is done: its id is fetched by lane 0 at copy time, after the wait
   auto page_src = [&](int j, bool& skip) -> const uint8_t* {
     const int b = j >> 5;
     if (b != batch_idx) {
@@ -509,7 +540,7 @@ __device__ __forceinline__ void int2_pages(const DevCache& c, int layer, const D
     int32_t page = __shfl_sync(0xffffffffu, batch_pages, j & 31);
     if (page == HOT_ID) {   // warp-uniform
       if (lane == 0) {
-        grid_dep_wait();
+        wait_append(c, R, head, epoch, limit);
         page = checked(__ldcg(pt + hot));
       }
       page = __shfl_sync(0xffffffffu, page, 0);
@@ -524,12 +555,12 @@ __device__ __forceinline__ void int2_pages(const DevCache& c, int layer, const D
     skip_bits = skip ? (skip_bits | bit) : (skip_bits & ~bit);
   };
   auto held = [&](int j) { return warp == 0 && static_cast<int>(nc + j) == hold; };
-  // the first STAGES copies were issued by int2_issue_first: their skip flags
+  // the first STAGES copies were issued by int2_issue_first, which left their skip
+  // flags in skip0 (the page ids of the later copies are read at the first refill)
+  {
+    const uint32_t s0 = sm.skip0[warp];
 #pragma unroll
-  for (int j = 0; j < STAGES; ++j) {
-    bool skip;
-    page_src(j, skip);
-    note(j, skip);
+    for (int j = 0; j < STAGES; ++j) note(j, (s0 >> j) & 1u);
   }
   // weights p * s_v are prescaled by 2^ew so the smallest ones stay representable in
   // fp16: s_v <= fp16(2 tau_V / 3) and p <= 2^LAZY_MAX, so p s_v 2^ew <= 2^15
@@ -1156,19 +1187,23 @@ __device__ __forceinline__ int cta_of(int64_t u, int ncta, int64_t total) {
   return c;
 }
 
-// The segment holding INT2 cost unit u of this INT2 CTA's range [u0, u1) (invalid
-// once u reaches u1); end receives its first unit past the segment.
+// The segment holding INT2 cost unit u of this INT2 CTA's range [u0, u1)
+// (invalid once u drops below u0); prev receives the unit before the segment.  A
+// CTA walks its segments from the last one back: a segment's last page (which a
+// decode step's append may be filling) is then one of the last pages the CTA
+// reads, long after the append is done.
 __device__ Seg plan_segment(const DecodeArgs& a, int Hkv, int icta, int64_t u, int64_t u0, int64_t u1,
-                            int64_t& end) {
+                            int64_t& prev) {
   Seg e{};
-  end = u1;
-  if (u >= u1) return e;
+  prev = u0 - 1;
+  if (u < u0) return e;
   int ri, h;
   int64_t s0;
   segment_of(a, Hkv, u, ri, h, s0);
   const int64_t np = a.r[ri].npages;
   const int n2 = a.ncta - a.nbc;
-  end = s0 + seg_units(a.r[ri]);
+  prev = s0 - 1;
+  const int64_t end = s0 + seg_units(a.r[ri]);
   const int64_t f0 = s0 + DECODE_SEGMENT_SETUP_COST;   // unit of page 0
   e.valid = 1;
   e.ri = ri;
@@ -1236,66 +1271,76 @@ __device__ void merge_segment(const DevCache& c, int layer, const DecodeArgs& a,
 #pragma unroll
     for (int i = 0; i < RP; ++i) rv[i] = r0 + i < D ? __ldg(RVt + (size_t)(r0 + i) * D) : 0.0f;
   }
-  float M[PAIRS], L[PAIRS], oh[PAIRS], bm[PAIRS], bl[PAIRS], bo[PAIRS];
+  // per head g: running max M and sum L (warp g keeps them in registers, lane 0's
+  // copy in sm.mh / sm.lh), and per chunk the records' weights 2^(m_j - M)
+  float* wj = reinterpret_cast<float*>(&sm.meta[0][0]);   // [CAP][G]
+  static_assert(CAP * G * sizeof(float) <= sizeof(sm.meta), "chunk weights in the meta rows");
+  float Mw = -INFINITY, Lw = 0.0f;                          // warp g < G: head g
+  float oh[PAIRS];
 #pragma unroll
-  for (int k = 0; k < PAIRS; ++k) {
-    M[k] = bm[k] = -INFINITY;
-    L[k] = oh[k] = bl[k] = bo[k] = 0.0f;
-  }
+  for (int k = 0; k < PAIRS; ++k) oh[k] = 0.0f;
+  const int warp = t >> 5, lane = t & 31;
   for (int j0 = 0; j0 == 0 || j0 < items; j0 += CAP) {   // the first chunk also brings the BF16 record
     const int nk = min(CAP, items - j0);
     if (j0 > 0) issue(j0, nk);
     if (!mbar_wait(&sm.mbar_m, mphase, DECODE_WAIT_LIMIT) && t == 0) atomicOr(c.err, ERR_TIMEOUT);
     mphase ^= 1u;
+    if (warp < G) {
+      const float* r = stage + warp * PART;
+      float mn = Mw;
+      for (int j = lane; j < nk; j += 32) mn = fmaxf(mn, r[j * RF + PARTIAL_M]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mn = fmaxf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      const float resc = Mw == -INFINITY ? 0.0f : exp2f(Mw - mn);
+      float ls = 0.0f;
+      for (int j = lane; j < nk; j += 32) {
+        const float mj = r[j * RF + PARTIAL_M];
+        const float f = mj == -INFINITY ? 0.0f : exp2f(mj - mn);
+        wj[j * G + warp] = f;
+        ls = fmaf(r[j * RF + PARTIAL_L], f, ls);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+      Mw = mn;
+      Lw = fmaf(Lw, resc, ls);
+      if (lane == 0) {
+        sm.mh[warp] = mn;
+        sm.lh[warp] = Lw;
+        sm.wf[0][warp] = resc;
+      }
+    }
+    __syncthreads();
 #pragma unroll
     for (int k = 0; k < PAIRS; ++k) {
       const int i = t + k * NTH;
       if (i < G * D) {
         const int g = i / D, ch = i % D;
-        const float* r = stage + g * PART;
-        float mn = M[k];
+        const float* r = stage + g * PART + ch;
+        float acc = oh[k] * sm.wf[0][g];
         for (int j = 0; j < nk; j += U) {
 #pragma unroll
           for (int u = 0; u < U; ++u)
-            if (j + u < nk) mn = fmaxf(mn, r[(j + u) * RF + PARTIAL_M]);
+            if (j + u < nk) acc = fmaf(r[(j + u) * RF], wj[(j + u) * G + g], acc);
         }
-        if (mn > M[k]) {
-          const float f = M[k] == -INFINITY ? 0.0f : exp2f(M[k] - mn);
-          L[k] *= f;
-          oh[k] *= f;
-          M[k] = mn;
-        }
-        for (int j = 0; j < nk; j += U) {
-#pragma unroll
-          for (int u = 0; u < U; ++u) {
-            if (j + u < nk) {
-              const float* rj = r + (j + u) * RF;
-              const float mj = rj[PARTIAL_M];
-              const float f = mj == -INFINITY ? 0.0f : exp2f(mj - M[k]);
-              L[k] = fmaf(rj[PARTIAL_L], f, L[k]);
-              oh[k] = fmaf(rj[ch], f, oh[k]);
-            }
-          }
-        }
-        if (j0 == 0) {
-          bm[k] = r[CAP * RF + PARTIAL_M];
-          bl[k] = r[CAP * RF + PARTIAL_L];
-          bo[k] = r[CAP * RF + ch];
-        }
+        oh[k] = acc;
       }
     }
-    __syncthreads();   // the stage is read before the next chunk (or the next copies) land
+    if (j0 + CAP >= items) break;   // the BF16 record is still staged: read below
+    __syncthreads();                // the stage and the weights are read before the next chunk lands
   }
   float ob[PAIRS], lt[PAIRS];
 #pragma unroll
   for (int k = 0; k < PAIRS; ++k) {
     const int i = t + k * NTH;
-    const float Mt = fmaxf(M[k], bm[k]);
-    const float fh = M[k] == -INFINITY ? 0.0f : exp2f(M[k] - Mt);
-    const float fb = bm[k] == -INFINITY ? 0.0f : exp2f(bm[k] - Mt);
-    if (i < G * D) sm.scr.mrg.hist[i / D][i % D] = oh[k] * fh;
-    ob[k] = bo[k] * fb;
-    lt[k] = fmaf(L[k], fh, bl[k] * fb);
+    const int g = i < G * D ? i / D : 0, ch = i % D;
+    const float* rb = stage + CAP * RF + g * PART;   // the BF16 record
+    const float bm = rb[PARTIAL_M], M = sm.mh[g];
+    const float Mt = fmaxf(M, bm);
+    const float fh = M == -INFINITY ? 0.0f : exp2f(M - Mt);
+    const float fb = bm == -INFINITY ? 0.0f : exp2f(bm - Mt);
+    if (i < G * D) sm.scr.mrg.hist[g][ch] = oh[k] * fh;
+    ob[k] = rb[ch] * fb;
+    lt[k] = fmaf(sm.lh[g], fh, rb[PARTIAL_L] * fb);
   }
   __syncthreads();
   {
@@ -1355,6 +1400,62 @@ __device__ __forceinline__ void count_and_merge(const DevCache& c, int layer, co
   if (sm.last) merge_segment<G, GK>(c, layer, a, ri, head, c_lo, n2, recs, bf16_recs, out, sm, mphase);
 }
 
+// The append of the step's new token for (request ri, kv head), K and V: the
+// demotion of the oldest recent token into the hot page where reqs[ri].hot_page is
+// set, then the new rows (the inputs the write path would be given, derived from
+// the post-step lengths), by two units of APPEND_THREADS threads (one after the
+// other when the CTA has fewer than 2 APPEND_THREADS); then dec_flag = epoch is
+// released for the CTA that streams the hot page.
+template <int G, int GK>
+__device__ void step_append(const DevCache& c, int layer, const DecodeArgs& a, int ri, int head, Smem<G, GK>& sm) {
+  constexpr int NTH = Tune<G, GK>::THREADS;
+  static_assert(NTH >= APPEND_THREADS && 2 * sizeof(AppendSmem) <= sizeof(sm.buf.ring), "append units");
+  const DecodeReq& R = a.r[ri];
+  AppendReq q;
+  q.slot = R.slot;
+  q.in_row = R.batch_row;
+  const int p = R.tokens - 1;   // the appended token
+  if (p < SINK) {
+    q.dst_page = R.sink_page;
+    q.dst_row = p;
+  } else {
+    const int sl = (p - SINK) % RECENT;
+    q.dst_page = R.ring_page[sl / PAGE];
+    q.dst_row = sl % PAGE;
+  }
+  q.demote_slot = q.hist_page = q.src_page = q.src_row = q.pt_index = -1;
+  if (R.hot_page >= 0) {
+    const int h = R.hist_end - 1 - SINK;   // history position of the demoted token; its ring slot is h mod 256
+    q.demote_slot = h % PAGE;
+    q.src_page = R.ring_page[(h % RECENT) / PAGE];
+    q.src_row = (h % RECENT) % PAGE;
+    if (R.hot_new >= 0) {
+      q.hist_page = R.hot_new;
+      q.pt_index = R.hot_page;
+    } else {
+      q.hist_page = __ldcg(c.hist_pt + (size_t)R.slot * c.max_pages + R.hot_page);
+    }
+  }
+  AppendSmem* as = reinterpret_cast<AppendSmem*>(&sm.buf.ring[0][0][0]);   // the rings hold no copy here
+  const int t = threadIdx.x;
+  if constexpr (NTH >= 2 * APPEND_THREADS) {
+    const int u = t / APPEND_THREADS;
+    if (u < 2)
+      append_work<GK>(c, layer, a.k_new, a.v_new, q, head, u, as[u], t % APPEND_THREADS,
+                      [u] { bar_sync(1 + u, APPEND_THREADS); });
+  } else {
+    if (t < APPEND_THREADS) {
+      for (int which = 0; which < 2; ++which)
+        append_work<GK>(c, layer, a.k_new, a.v_new, q, head, which, as[0], t, [] { bar_sync(1, APPEND_THREADS); });
+    }
+  }
+  __syncthreads();   // every write of the append is done (and seen by thread 0)
+  if (t == 0) {
+    uint32_t* f = c.dec_flag + (size_t)R.slot * c.Hkv + head;
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(a.epoch) : "memory");
+  }
+}
+
 // Records in the workspace: INT2 record of (segment s, INT2 CTA c) at slot s + c
 // (the INT2 CTAs meeting one segment are consecutive, so the slots are unique),
 // then the BF16 record of segment s.
@@ -1368,7 +1469,7 @@ __global__ void __launch_bounds__(Tune<G, GK>::THREADS, 1)
   const int cta = blockIdx.x;
   float* int2_recs = recs;
   float* bf16_recs = recs + ((size_t)a.n * c.Hkv + a.ncta) * G * PART;
-  const bool fw = a.front_writes != 0;
+  const uint32_t epoch = a.epoch;
   const int n2cta = a.ncta - a.nbc;   // INT2 CTAs
 
   if ((t & 31) == 0) {
@@ -1383,14 +1484,29 @@ __global__ void __launch_bounds__(Tune<G, GK>::THREADS, 1)
     // ---- a BF16 CTA: the BF16 blocks of segments cta, cta + nbc, ... (none of
     // their rows is written by a fused append: the appended token comes from k / v)
     __syncthreads();
-    if (!fw) grid_dep_wait();   // q and the cache may have been written by the preceding grid
-    grid_dep_launch();          // the next launch may be scheduled; it waits for this grid to complete
+    if (epoch != 0 && warp == 0) {
+      // the rotations the appends read (written once, at set-up): into L2 while waiting
+      const int lane = t & 31;
+      for (int s = cta; s < a.n * c.Hkv; s += a.nbc) {
+        if (a.r[s / c.Hkv].hot_page < 0 || lane >= 16) continue;
+        const size_t off = ((size_t)layer * c.Hkv + s % c.Hkv) * D * D;
+        const float* m = lane < 4 ? c.rot_k : lane < 8 ? c.rot_v : lane < 12 ? c.rot_kt : c.rot_vt;
+        prefetch_l2(m + off + (size_t)(lane & 3) * (D * D / 4), D * D);
+      }
+    }
+    grid_dep_wait();    // q, k / v and the cache may have been written by the preceding grid
+    grid_dep_launch();  // the next launch may be scheduled (every CTA of this one is running); it waits for it
+    if (epoch != 0) {
+      // a decode step: the append of this CTA's (request, kv head) pairs first, so
+      // that the hot pages are ready early for the CTAs that stream them
+      for (int s = cta; s < a.n * c.Hkv; s += a.nbc) step_append<G, GK>(c, layer, a, s / c.Hkv, s % c.Hkv, sm);
+    }
     for (int s = cta; s < a.n * c.Hkv; s += a.nbc) {
       const int ri = s / c.Hkv, head = s % c.Hkv;
       const DecodeReq& R = a.r[ri];
-      if (warp == 0 && (t & 31) < 4) {   // R_V rows of the merge, should this CTA do it
-        const float* rv = c.rot_v + ((size_t)layer * c.Hkv + head) * D * D;
-        prefetch_l2(rv + (size_t)(t & 31) * (D * D / 4), D * D);
+      if (warp == 0 && (t & 31) < 4) {   // R_V^T of the merge, should this CTA do it
+        const float* rvt = c.rot_vt + ((size_t)layer * c.Hkv + head) * D * D;
+        prefetch_l2(rvt + (size_t)(t & 31) * (D * D / 4), D * D);
       }
       bf16_segment<G, GK>(c, layer, a, ri, head, q, sm, bf16_recs);
       int c_lo = 0, n2 = 0;
@@ -1408,9 +1524,9 @@ __global__ void __launch_bounds__(Tune<G, GK>::THREADS, 1)
   const int icta = cta - a.nbc;
   const int64_t u0 = cta_begin(icta, n2cta, a.total_cost), u1 = cta_begin(icta + 1, n2cta, a.total_cost);
   if (t == 0) {
-    int64_t end;
-    sm.seg[0] = plan_segment(a, c.Hkv, icta, u0, u0, u1, end);
-    sm.u_next = end;
+    int64_t prev;
+    sm.seg[0] = plan_segment(a, c.Hkv, icta, u1 - 1, u0, u1, prev);
+    sm.u_next = prev;
   }
   __syncthreads();
   uint32_t nc = 0;            // copies this warp has consumed
@@ -1420,12 +1536,19 @@ __global__ void __launch_bounds__(Tune<G, GK>::THREADS, 1)
     const Seg S = sm.seg[0];
     RkRows<G, GK> rk;
     if (S.valid) load_rk<G, GK>(c, layer, S.head, rk);
-    if (!fw) grid_dep_wait();   // the cache and q may have been written by the preceding grid
-    grid_dep_launch();          // the next launch may be scheduled; it waits for this grid to complete
+    // After a decode launch of this cache, the history pages below npages - 2 (and
+    // their page-table entries) are not written by any grid that may still run:
+    // their first copies go out before the wait, while that grid finishes
+    if (S.valid && a.prefetch)
+      int2_issue_first<G, GK>(c, layer, a.r[S.ri], S.head, S.p0, S.p1, sm, epoch, a.dbg.wait_limit, nc, hold,
+                              timed_out, 1);
+    grid_dep_wait();    // the cache and q may have been written by the preceding grid
+    grid_dep_launch();  // the next launch may be scheduled (every CTA of this one is running); it waits for it
     if (S.valid) {
       QRows<G, GK> qv;
       load_q<G, GK>(c, a.r[S.ri], S.head, q, qv);   // in flight with the page-id loads of the copies
-      int2_issue_first<G, GK>(c, layer, a.r[S.ri], S.head, S.p0, S.p1, sm, fw, nc, hold, timed_out);
+      int2_issue_first<G, GK>(c, layer, a.r[S.ri], S.head, S.p0, S.p1, sm, epoch, a.dbg.wait_limit, nc, hold,
+                              timed_out, a.prefetch ? 2 : 0);
       build_qfrag<G, GK>(c, qv, rk, sm);
     }
   }
@@ -1434,14 +1557,14 @@ __global__ void __launch_bounds__(Tune<G, GK>::THREADS, 1)
   for (int e = 0; sm.seg[e & 1].valid; ++e) {
     const int cur = e & 1, nxt = cur ^ 1;
     if (t == 0) {
-      int64_t end;
-      sm.seg[nxt] = plan_segment(a, c.Hkv, icta, sm.u_next, u0, u1, end);
-      sm.u_next = end;
+      int64_t prev;
+      sm.seg[nxt] = plan_segment(a, c.Hkv, icta, sm.u_next, u0, u1, prev);
+      sm.u_next = prev;
     }
     {
       const Seg& S = sm.seg[cur];
       int2_pages<G, GK>(c, layer, a.r[S.ri], S.head, S.p0, S.p1, sm.qf, sm, int2_recs + (size_t)S.slot * G * PART,
-                        a.dbg.wait_limit, fw, nc, timed_out, hold);
+                        a.dbg.wait_limit, epoch, nc, timed_out, hold);
     }
     {
       const Seg& S = sm.seg[cur];
@@ -1455,7 +1578,8 @@ __global__ void __launch_bounds__(Tune<G, GK>::THREADS, 1)
       QRows<G, GK> qv;
       load_rk<G, GK>(c, layer, N.head, rk);
       load_q<G, GK>(c, a.r[N.ri], N.head, q, qv);
-      int2_issue_first<G, GK>(c, layer, a.r[N.ri], N.head, N.p0, N.p1, sm, fw, nc, hold, timed_out);
+      int2_issue_first<G, GK>(c, layer, a.r[N.ri], N.head, N.p0, N.p1, sm, epoch, a.dbg.wait_limit, nc, hold,
+                              timed_out);
       build_qfrag<G, GK>(c, qv, rk, sm);
     }
   }
@@ -1463,8 +1587,8 @@ __global__ void __launch_bounds__(Tune<G, GK>::THREADS, 1)
 
 template <int G, int GK>
 cudaError_t launch_decode_t(const DevCache& c, int layer, const DecodeReq* reqs, const DecodePlan& p,
-                            const uint16_t* q, float* out, void* workspace, bool front_writes, const uint16_t* k_new,
-                            const uint16_t* v_new, DecodeDebug dbg, cudaStream_t s) {
+                            const uint16_t* q, float* out, void* workspace, const uint16_t* k_new,
+                            const uint16_t* v_new, uint32_t epoch, bool prefetch, DecodeDebug dbg, cudaStream_t s) {
   static_assert(sizeof(Smem<G, GK>) <= 227 * 1024, "shared memory");
   using SM = Smem<G, GK>;
   static_assert(offsetof(SM, qf) % 16 == 0 && (QFrag<G>::WORDS * 4) % 16 == 0, "q operands: uint4 loads");
@@ -1483,11 +1607,12 @@ cudaError_t launch_decode_t(const DevCache& c, int layer, const DecodeReq* reqs,
   a.n = p.n;
   a.ncta = p.ncta;
   a.nbc = p.nbc;
-  a.front_writes = front_writes ? 1 : 0;
+  a.prefetch = prefetch ? 1 : 0;
+  a.epoch = k_new != nullptr ? epoch : 0u;
   a.total_cost = p.total_cost;
   a.dbg = dbg;
-  a.k_new = front_writes ? k_new : nullptr;
-  a.v_new = front_writes ? v_new : nullptr;
+  a.k_new = a.epoch != 0 ? k_new : nullptr;
+  a.v_new = a.epoch != 0 ? v_new : nullptr;
   for (int i = 0; i < p.n; ++i) a.r[i] = reqs[i];
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1504,13 +1629,13 @@ cudaError_t launch_decode_t(const DevCache& c, int layer, const DecodeReq* reqs,
 
 template <int GK>
 cudaError_t launch_decode_g(const DevCache& c, int layer, const DecodeReq* reqs, const DecodePlan& p,
-                            const uint16_t* q, float* out, void* ws, bool fw, const uint16_t* kn, const uint16_t* vn,
-                            DecodeDebug dbg, cudaStream_t s) {
+                            const uint16_t* q, float* out, void* ws, const uint16_t* kn, const uint16_t* vn,
+                            uint32_t ep, bool pf, DecodeDebug dbg, cudaStream_t s) {
   switch (c.G) {
-    case 1: return launch_decode_t<1, GK>(c, layer, reqs, p, q, out, ws, fw, kn, vn, dbg, s);
-    case 2: return launch_decode_t<2, GK>(c, layer, reqs, p, q, out, ws, fw, kn, vn, dbg, s);
-    case 4: return launch_decode_t<4, GK>(c, layer, reqs, p, q, out, ws, fw, kn, vn, dbg, s);
-    case 8: return launch_decode_t<8, GK>(c, layer, reqs, p, q, out, ws, fw, kn, vn, dbg, s);
+    case 1: return launch_decode_t<1, GK>(c, layer, reqs, p, q, out, ws, kn, vn, ep, pf, dbg, s);
+    case 2: return launch_decode_t<2, GK>(c, layer, reqs, p, q, out, ws, kn, vn, ep, pf, dbg, s);
+    case 4: return launch_decode_t<4, GK>(c, layer, reqs, p, q, out, ws, kn, vn, ep, pf, dbg, s);
+    case 8: return launch_decode_t<8, GK>(c, layer, reqs, p, q, out, ws, kn, vn, ep, pf, dbg, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1518,21 +1643,14 @@ cudaError_t launch_decode_g(const DevCache& c, int layer, const DecodeReq* reqs,
 }  // namespace
 
 cudaError_t launch_decode(const DevCache& c, int layer, const DecodeReq* reqs, const DecodePlan& p,
-                          const uint16_t* q, float* out, void* workspace, bool front_writes, const uint16_t* k_new,
-                          const uint16_t* v_new, DecodeDebug dbg, cudaStream_t s) {
+                          const uint16_t* q, float* out, void* workspace, const uint16_t* k_new,
+                          const uint16_t* v_new, uint32_t epoch, bool prefetch, DecodeDebug dbg, cudaStream_t s) {
   if (p.n < 1 || p.n > DECODE_PER_LAUNCH || p.nbc < 1 || p.ncta < p.nbc || p.total_cost < p.ncta - p.nbc)
     return cudaErrorInvalidValue;
+  if ((k_new != nullptr) != (v_new != nullptr) || (k_new != nullptr && epoch == 0)) return cudaErrorInvalidValue;
   return c.gk == 64
-             ? launch_decode_g<64>(c, layer, reqs, p, q, out, workspace, front_writes, k_new, v_new, dbg, s)
-             : launch_decode_g<128>(c, layer, reqs, p, q, out, workspace, front_writes, k_new, v_new, dbg, s);
-}
-
-cudaError_t launch_step(const DevCache& c, int layer, const AppendReq* app, int n_app, const uint16_t* k,
-                        const uint16_t* v, const DecodeReq* reqs, const DecodePlan& p, const uint16_t* q,
-                        float* out, void* workspace, DecodeDebug dbg, cudaStream_t s) {
-  const cudaError_t e = launch_append(c, layer, app, n_app, k, v, s);
-  if (e != cudaSuccess) return e;
-  return launch_decode(c, layer, reqs, p, q, out, workspace, true, k, v, dbg, s);
+             ? launch_decode_g<64>(c, layer, reqs, p, q, out, workspace, k_new, v_new, epoch, prefetch, dbg, s)
+             : launch_decode_g<128>(c, layer, reqs, p, q, out, workspace, k_new, v_new, epoch, prefetch, dbg, s);
 }
 
 }  // namespace oscar

@@ -94,6 +94,8 @@ struct oscar_cache {
   std::string err;
   int num_sms = 152;
   DecodeDebug dbg{DECODE_WAIT_LIMIT, -1};   // failure-detection hooks of decode launches
+  uint32_t epoch = 0;                       // decode-step launches so far (never 0 once launched)
+  bool last_decode = false;                 // the last kernel this cache launched is a decode
 
   oscar_status fail(oscar_status s, const std::string& msg) {
     err = msg;
@@ -172,6 +174,8 @@ oscar_cache_layout make_layout(const oscar_cache_config& c) {
   off += 256;
   l.decode_count_offset = off;
   off += align256((size_t)c.max_requests * H * sizeof(int32_t));
+  l.decode_flag_offset = off;
+  off += align256((size_t)c.max_requests * H * sizeof(uint32_t));
   l.total_bytes = off;
   return l;
 }
@@ -252,6 +256,7 @@ oscar_status oscar_cache_create(const oscar_cache_config* cfg, void* device_mem,
   d.bf16_pt = reinterpret_cast<int32_t*>(base + c->lay.bf16_pt_offset);
   d.err = reinterpret_cast<int32_t*>(base + c->lay.error_word_offset);
   d.dec_count = reinterpret_cast<int32_t*>(base + c->lay.decode_count_offset);
+  d.dec_flag = reinterpret_cast<uint32_t*>(base + c->lay.decode_flag_offset);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int dev = 0;
@@ -267,6 +272,8 @@ oscar_status oscar_cache_create(const oscar_cache_config* cfg, void* device_mem,
   if (e == cudaSuccess) e = cudaMemsetAsync(d.err, 0, 4, s);
   if (e == cudaSuccess)
     e = cudaMemsetAsync(d.dec_count, 0, (size_t)c->cfg.max_requests * c->cfg.num_kv_heads * sizeof(int32_t), s);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(d.dec_flag, 0, (size_t)c->cfg.max_requests * c->cfg.num_kv_heads * sizeof(uint32_t), s);
   if (e == cudaSuccess) e = launch_rotation_setup(d, rot_k, rot_v, rk, rv, rkt, rvt, rcn, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) {
@@ -317,6 +324,7 @@ oscar_status oscar_request_open(oscar_cache* c, void* stream, int32_t* req_out) 
   if (c->dry) return OSCAR_OK;
   PtEntry e[BF16_PAGES_PER_REQ];
   for (int i = 0; i < BF16_PAGES_PER_REQ; ++i) e[i] = PtEntry{1, slot * BF16_PAGES_PER_REQ + i, r.bf16_pt[i]};
+  c->last_decode = false;
   cudaError_t err = launch_pt_update(c->dc, e, BF16_PAGES_PER_REQ, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? OSCAR_OK : c->cuda_fail(err, "page-table update");
 }
@@ -356,6 +364,7 @@ oscar_status oscar_request_fork(oscar_cache* c, int32_t parent, int64_t prefix, 
   for (int i = 0; i < BF16_PAGES_PER_REQ; ++i) e.push_back(PtEntry{1, slot * BF16_PAGES_PER_REQ + i, r.bf16_pt[i]});
   for (int64_t i = 0; i < npages; ++i)
     e.push_back(PtEntry{0, static_cast<int32_t>((int64_t)slot * c->cfg.max_pages_per_request + i), r.hist_pt[i]});
+  c->last_decode = false;
   cudaError_t err = launch_pt_update(c->dc, e.data(), static_cast<int>(e.size()), static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? OSCAR_OK : c->cuda_fail(err, "page-table update");
 }
@@ -418,6 +427,7 @@ oscar_status oscar_prefill_quantize(oscar_cache* c, int32_t req, int32_t layer, 
   BF16Dest dst;
   dst.sink_page = r.bf16_pt[0];
   for (int i = 0; i < RING_PAGES; ++i) dst.ring_page[i] = r.bf16_pt[1 + i];
+  c->last_decode = false;
   cudaError_t err = launch_pt_update(c->dc, e.data(), static_cast<int>(e.size()), s);
   if (err == cudaSuccess && t0 < SINK) err = launch_prefill_bf16(c->dc, layer, k, v, t0, t0, std::min<int64_t>(total, SINK), dst, s);
   const int64_t r0 = std::max<int64_t>(he1, SINK);
@@ -510,20 +520,19 @@ oscar_status write_batch(oscar_cache* c, int32_t layer, int32_t n, const int32_t
   if (st != OSCAR_OK) return st;
   const std::vector<AppendReq> work = apply_write(c, layer, n, reqs, append);
   if (c->dry) return OSCAR_ERR_DRY_RUN;
+  c->last_decode = false;
   cudaError_t err = launch_append(c->dc, layer, work.data(), n, k, v, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? OSCAR_OK : c->cuda_fail(err, append ? "append launch" : "demote launch");
 }
 
-// BF16 sub-pages (16 rows) of one kv head holding a cached token: the sink rows
-// [0, min(T, 64)); ring slot s = 64 (page - 1) + r holds position
-// he + ((s - (he - 64)) mod 256), cached while below T.
 // Work split of one decode launch over reqs[0..n), n <= DECODE_PER_LAUNCH: nbc
-// CTAs for the segments' BF16 blocks, sized so that their blocks take about one
-// CTA's share of the INT2 pages each (DECODE_BF16_BLOCK_COST), at least one and
-// at most one per segment; the other CTAs (one per SM in all, at most one per
-// INT2 page) split the INT2 pages into contiguous equal ranges.
+// CTAs for the segments' BF16 blocks (and, in a decode step, their appends),
+// sized so that this work takes about one CTA's share of the INT2 cost each
+// (DECODE_BF16_BLOCK_COST, DECODE_APPEND_COST), at least one and at most one per
+// segment; the other CTAs (one per SM in all, at most one per INT2 cost unit)
+// split the INT2 line into contiguous equal ranges.
 DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int32_t* reqs, int32_t first_row,
-                       DecodeReq* out) {
+                       DecodeReq* out, bool step = false) {
   const int64_t H = c->cfg.num_kv_heads;
   int64_t cost = 0;
   for (int32_t i = 0; i < n; ++i) {
@@ -539,6 +548,7 @@ DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int
       d.sink_page = r.bf16_pt[0];
       for (int k = 0; k < RING_PAGES; ++k) d.ring_page[k] = r.bf16_pt[1 + k];
       d.hot_page = -1;
+      d.hot_new = -1;
       d.npages = static_cast<int32_t>(np);
       d.cost_start = static_cast<int32_t>(cost);
     }
@@ -550,7 +560,9 @@ DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int
   p.segments = (int64_t)n * H;
   const int64_t sms = std::max(2, c->num_sms);
   const int64_t share = cost / sms + 1;   // INT2 cost per CTA were every CTA on INT2 pages
-  int64_t nbc = (p.segments * DECODE_BF16_BLOCK_COST + share - 1) / share;
+  // a decode step's BF16 CTAs also append the new token of each segment first
+  const int64_t per_seg = DECODE_BF16_BLOCK_COST + (step ? DECODE_APPEND_COST : 0);
+  int64_t nbc = (p.segments * per_seg + share - 1) / share;
   nbc = std::max<int64_t>(1, std::min<int64_t>({nbc, p.segments, cost > 0 ? sms / 2 : sms}));
   const int64_t n_int2 = std::min<int64_t>(sms - nbc, cost);
   p.nbc = static_cast<int>(nbc);
@@ -623,6 +635,7 @@ oscar_status oscar_demote_layers(oscar_cache* c, int32_t layer_begin, int32_t la
   for (int32_t l = layer_begin; l < layer_end; ++l)
     for (const AppendReq& a : apply_write(c, l, n, reqs, false)) work.push_back(DemoteEntry{l, a});
   if (c->dry) return OSCAR_ERR_DRY_RUN;
+  c->last_decode = false;
   const cudaError_t err =
       launch_demote_layers(c->dc, work.data(), static_cast<int>(work.size()), static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? OSCAR_OK : c->cuda_fail(err, "demote launch");
@@ -656,7 +669,9 @@ oscar_status oscar_decode_attention(oscar_cache* c, int32_t layer, int32_t n, co
   for (int32_t b = 0; b < n; b += per) {
     const int32_t m = std::min<int32_t>(per, n - b);
     const DecodePlan p = plan_decode(c, layer, m, reqs + b, b, dr);
-    const cudaError_t err = launch_decode(c->dc, layer, dr, p, q, out, workspace, false, nullptr, nullptr, c->dbg, s);
+    const cudaError_t err =
+        launch_decode(c->dc, layer, dr, p, q, out, workspace, nullptr, nullptr, 0u, c->last_decode, c->dbg, s);
+    c->last_decode = err == cudaSuccess;
     if (err != cudaSuccess) return c->cuda_fail(err, "decode launch");
   }
   return OSCAR_OK;
@@ -708,12 +723,18 @@ oscar_status oscar_decode_step(oscar_cache* c, int32_t layer, int32_t n, const i
   const int32_t per = std::min<int32_t>(APPEND_PER_LAUNCH, decode_launch_size(c, layer, n, reqs));
   for (int32_t b = 0; b < n; b += per) {
     const int32_t m = std::min<int32_t>(per, n - b);
-    const DecodePlan p = plan_decode(c, layer, m, reqs + b, b, dr);
+    const DecodePlan p = plan_decode(c, layer, m, reqs + b, b, dr, true);
     for (int32_t i = 0; i < m; ++i) {
       const AppendReq& a = work[b + i];
-      dr[i].hot_page = a.demote_slot >= 0 ? static_cast<int32_t>((c->reqs[reqs[b + i]].he[layer] - 1 - SINK) / PAGE) : -1;
+      if (a.demote_slot >= 0) {
+        dr[i].hot_page = static_cast<int32_t>((c->reqs[reqs[b + i]].he[layer] - 1 - SINK) / PAGE);
+        dr[i].hot_new = a.pt_index >= 0 ? a.hist_page : -1;
+      }
     }
-    const cudaError_t err = launch_step(c->dc, layer, work.data() + b, m, k, v, dr, p, q, out, workspace, c->dbg, s);
+    if (++c->epoch == 0) c->epoch = 1;
+    const cudaError_t err =
+        launch_decode(c->dc, layer, dr, p, q, out, workspace, k, v, c->epoch, c->last_decode, c->dbg, s);
+    c->last_decode = err == cudaSuccess;
     if (err != cudaSuccess) return c->cuda_fail(err, "decode step launch");
   }
   return OSCAR_OK;

@@ -60,6 +60,8 @@ struct DevCache {
   int32_t* bf16_pt;              // [max_requests][5]
   int32_t* err;
   int32_t* dec_count;            // [max_requests][Hkv]: decode CTAs done with a segment (0 between launches)
+  uint32_t* dec_flag;            // [max_requests][Hkv]: epoch of the last step launch whose append of
+                                 // that (request, kv head) is complete
   int32_t L, Hq, Hkv, G, max_pages;
   int32_t gk;                    // quantisation group size: 128 or 64
   int32_t record;                // record_for(gk) bytes per (page, kv head)
@@ -132,7 +134,9 @@ struct DecodeReq {
   int32_t hist_end;
   int32_t sink_page;
   int32_t ring_page[RING_PAGES];
-  int32_t hot_page;        // history page index a preceding fused append writes (-1: none)
+  int32_t hot_page;        // history page index the step's append demotes into (-1: none)
+  int32_t hot_new;         // physical INT2 page that demotion opens (page-table entry written by the
+                           // step), -1: the page is already in the table
   int32_t npages;          // INT2 history pages of each kv head
   int32_t cost_start;      // first INT2 cost unit of (this request, kv head 0); each kv head
                            // takes DECODE_SEGMENT_SETUP_COST + npages units (none if npages is 0)
@@ -140,7 +144,9 @@ struct DecodeReq {
 constexpr int DECODE_PER_LAUNCH = 64;
 // A BF16 block (up to 20 sub-pages of 16 rows) counted as this many INT2 pages
 // when the BF16 CTAs are sized: about the time it takes one CTA.
-constexpr int DECODE_BF16_BLOCK_COST = 40;
+constexpr int DECODE_BF16_BLOCK_COST = 60;
+// The append of one (request, kv head) in a decode step (K and V), likewise.
+constexpr int DECODE_APPEND_COST = 30;
 // Cost units in front of each segment's pages on the INT2 line: the set-up a CTA
 // pays on entering a segment (q rotation, first-page latency), in INT2 pages.
 constexpr int DECODE_SEGMENT_SETUP_COST = 40;
@@ -165,19 +171,16 @@ struct DecodeDebug {
 };
 constexpr uint32_t DECODE_WAIT_LIMIT = 100000;   // rounds of up to 20 us each
 // One launch: the CTAs stream their cost ranges, and the last CTA to finish a
-// segment (counted in dec_count) merges it into out.  front_writes: a fused
-// append precedes this launch (see launch_step); k_new / v_new are then its
-// input rows [n][Hkv][128] bf16 (batch rows), read in place of the ring row the
-// append writes.
+// segment (counted in dec_count) merges it into out.  With k_new / v_new (the
+// step's new token rows [n][Hkv][128] bf16, batch rows) the launch is a whole
+// decode step: its BF16 CTAs first append the new token of each (request, kv
+// head) -- demoting into reqs[i].hot_page where it is set -- and release
+// dec_flag = epoch; the CTA that streams the hot page waits for that flag.
+// prefetch: the kernel launched just before on the stream is a decode of this
+// cache, so the older history pages may be copied before the launch waits for it.
 cudaError_t launch_decode(const DevCache& c, int layer, const DecodeReq* reqs, const DecodePlan& plan,
-                          const uint16_t* q, float* out, void* workspace, bool front_writes, const uint16_t* k_new,
-                          const uint16_t* v_new, DecodeDebug dbg, cudaStream_t s);
-// Fused step: the append of every request (demoting into reqs[i].hot_page), then
-// the decode, which copies every page the append does not write while the append
-// still runs, and takes the appended token itself from the step's k / v.
-cudaError_t launch_step(const DevCache& c, int layer, const AppendReq* app, int n_app, const uint16_t* k,
-                        const uint16_t* v, const DecodeReq* reqs, const DecodePlan& plan, const uint16_t* q,
-                        float* out, void* workspace, DecodeDebug dbg, cudaStream_t s);
+                          const uint16_t* q, float* out, void* workspace, const uint16_t* k_new,
+                          const uint16_t* v_new, uint32_t epoch, bool prefetch, DecodeDebug dbg, cudaStream_t s);
 
 // Fixed decode scratch (one static device array per device) for callers that
 // cannot allocate.  The first call on a device, with that device current,

@@ -104,6 +104,7 @@ typedef struct {
   size_t tau_k_offset, tau_v_offset;                               /* fp32 [L][Hkv] */
   size_t hist_pt_offset, bf16_pt_offset, error_word_offset;
   size_t decode_count_offset;      /* int32 [max_requests][Hkv], zero between decode launches */
+  size_t decode_flag_offset;       /* uint32 [max_requests][Hkv], step epochs (see oscar_decode_step) */
 } oscar_cache_layout;
 
 /* Bytes of device memory oscar_cache_create() needs for cfg (0 if invalid). */
@@ -247,11 +248,13 @@ oscar_status oscar_decode_attention_noalloc(oscar_cache* cache, int32_t layer, i
 
 /* One decode step of one layer: oscar_append(layer, n, reqs, k, v) followed by
  * oscar_decode_attention(layer, n, reqs, q, out, workspace), with identical
- * results, as overlapping launches: the decode kernel starts while the append
- * kernel runs, streams every history page the append does not write, waits for
- * the append only before the one history page a demotion fills, and reads the
- * appended token itself from k / v ([MTP] section "The Serving System": the
- * write path and decode attention of a step).
+ * results, as one kernel per launch of up to 48 requests: its BF16 CTAs first
+ * append the new token of each (request, kv head) -- the demotion of the oldest
+ * recent token into INT2 history included -- and mark it done in the cache's
+ * step flags (layout decode_flag_offset); the CTA that streams the history page
+ * a demotion fills waits for that mark (bounded) before copying it, and the new
+ * token itself is read from k / v ([MTP] section "The Serving System": the write
+ * path and decode attention of a step).
  *   k, v       device bf16 [n][Hkv][128], the new token of each request.
  *   q, out     as oscar_decode_attention.
  *   workspace  device, >= oscar_decode_workspace_bytes() taken before the step
