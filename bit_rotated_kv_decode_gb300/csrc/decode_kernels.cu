@@ -220,6 +220,7 @@ struct Smem {
       float q[G][D];
       float part[NPART][G][D];
       float norm[G];
+      int qe[G];                        // q scale exponents
     } pro;                              // rotation of q
     struct {
       __align__(16) float hist[G][D];   // O_hist of the merged segment
@@ -237,6 +238,7 @@ struct Smem {
   Seg seg[2];                            // segment e in slot e & 1
   int64_t u_next;                        // last cost unit before the last planned segment
   uint32_t skip0[NW];                    // per warp: bit j, the first copy j of the segment skips its page
+  int ew;                                // the current segment's value-weight exponent (see build_qfrag)
   int last;                              // this CTA merges the segment just finished
 };
 
@@ -265,11 +267,13 @@ template <int G, int GK>
 struct QRows {
   static constexpr int N = (G * D + Tune<G, GK>::THREADS - 1) / Tune<G, GK>::THREADS;
   uint16_t v[N];
+  float tau_v;   // the segment's value clip threshold (one thread)
 };
 template <int G, int GK>
-__device__ __forceinline__ void load_q(const DevCache& c, const DecodeReq& R, int head,
+__device__ __forceinline__ void load_q(const DevCache& c, int layer, const DecodeReq& R, int head,
                                        const uint16_t* __restrict__ q, QRows<G, GK>& qv) {
   constexpr int NTH = Tune<G, GK>::THREADS;
+  qv.tau_v = threadIdx.x == D + G ? c.tau_v[(size_t)layer * c.Hkv + head] : 0.0f;
   const uint16_t* qrow = q + ((size_t)R.batch_row * c.Hq + (size_t)head * G) * D;
 #pragma unroll
   for (int k = 0; k < QRows<G, GK>::N; ++k) {
@@ -326,11 +330,10 @@ __device__ __forceinline__ void build_qfrag(const DevCache& c, const QRows<G, GK
       for (int p = 1; p < NPART; ++p) v += sm.scr.pro.part[p][h][t];
       sm.scr.pro.part[0][h][t] = v;
     }
-  }
-  __syncthreads();
-  // qscale(h) = 2^e, e = 15 - 24 - ceil(log2(|q|_2 1.001)) (read off the exponent of
-  // the rounded-up norm), so |q_rot| qscale 2^24 <= 2^15
-  auto qexp = [&](int h) -> int {
+  } else if (t < D + G) {
+    // qscale(h) = 2^e, e = 15 - 24 - ceil(log2(|q|_2 1.001)) (read off the exponent of
+    // the rounded-up norm), so |q_rot| qscale 2^24 <= 2^15
+    const int h = t - D;
     const float n2 = sm.scr.pro.norm[h];
     int e = 0;
     if (n2 > 0.0f) {
@@ -338,8 +341,17 @@ __device__ __forceinline__ void build_qfrag(const DevCache& c, const QRows<G, GK
       const int ceil_log2 = static_cast<int>((b >> 23) & 0xffu) - 127 + ((b & 0x7fffffu) != 0u ? 1 : 0);
       e = 15 - 24 - ceil_log2;
     }
-    return max(-60, min(e, 60));
-  };
+    sm.scr.pro.qe[h] = max(-60, min(e, 60));
+  } else if (t == D + G) {
+    // value weights p s_v are prescaled by 2^ew so the smallest ones stay representable
+    // in fp16: s_v <= fp16(2 tau_V / 3) and p <= 2^LAZY_MAX, so p s_v 2^ew <= 2^15
+    const float smax = qv.tau_v * (2.0f / 3.0f) * 1.002f;
+    sm.ew = max(-60, min(60, static_cast<int>(floorf(log2f(32768.0f / smax))) - LAZY_MAX_INT));
+  }
+  __syncthreads();
+  // 2^e for the small exponents here (normal range): built from its bits
+  auto pow2 = [](int e) { return __int_as_float((e + 127) << 23); };
+  auto qexp = [&](int h) { return sm.scr.pro.qe[h]; };
   uint32_t* dst = sm.qf;
   for (int wi = t; wi < 32 * REGS; wi += NTH) {
     const int lane_w = wi / REGS, k = wi % REGS;
@@ -350,7 +362,7 @@ __device__ __forceinline__ void build_qfrag(const DevCache& c, const QRows<G, GK
     if (h < G) {
       const int m = 2 * (s & 3) + rr;
       const int chn = GK == 128 ? 32 * tid + 16 * (s >> 2) + m : 64 * (s >> 2) + 16 * tid + m;
-      const float f = ldexpf(1.0f, qexp(h) + 24 - 2 * code_exp(m));
+      const float f = pow2(qexp(h) + 24 - 2 * code_exp(m));
       float ha, la, hb, lb;
       split_half(sm.scr.pro.part[0][h][chn] * f, ha, la);
       split_half(sm.scr.pro.part[0][h][chn + 8] * f, hb, lb);
@@ -359,7 +371,7 @@ __device__ __forceinline__ void build_qfrag(const DevCache& c, const QRows<G, GK
     dst[wi] = word;
   }
   float* consts = reinterpret_cast<float*>(dst + QFrag<G>::CONSTS);
-  if (t < 8) consts[t] = t < G ? c.scale * LOG2E * ldexpf(1.0f, -qexp(t)) : 0.0f;
+  if (t < 8) consts[t] = t < G ? c.scale * LOG2E * pow2(-qexp(t)) : 0.0f;
   // slab sums: warp (slab, head) pairs, lane over the slab's 32 channels
   for (int pr = w; pr < SLABS * 8; pr += NTH / 32) {
     const int sl = pr / 8, h = pr % 8;
@@ -562,14 +574,9 @@ __device__ __forceinline__ void int2_pages(const DevCache& c, int layer, const D
 #pragma unroll
     for (int j = 0; j < STAGES; ++j) note(j, (s0 >> j) & 1u);
   }
-  // weights p * s_v are prescaled by 2^ew so the smallest ones stay representable in
-  // fp16: s_v <= fp16(2 tau_V / 3) and p <= 2^LAZY_MAX, so p s_v 2^ew <= 2^15
-  int ew;
-  {
-    const float smax = c.tau_v[(size_t)layer * c.Hkv + head] * (2.0f / 3.0f) * 1.002f;
-    ew = max(-60, min(60, static_cast<int>(floorf(log2f(32768.0f / smax))) - LAZY_MAX_INT));
-  }
-  const float wscale = ldexpf(1.0f, ew);
+  // weights p * s_v are prescaled by 2^ew (formed with the q operands)
+  const int ew = sm.ew;
+  const float wscale = __int_as_float((ew + 127) << 23);
 
   // B operands of q_rot . c, and the per-head logit constants of this lane's head
   uint32_t bq[NT][8][2];
@@ -1235,9 +1242,8 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
 // combined per (query head, channel); then out = (O_bf16 + O_hist R_V^T) / L for
 // the G query heads.  The records (consecutive in the workspace) are staged into
 // the rings, which hold no copy at this point, by bulk copies of up to CAP
-// records; while the first copy is in flight every thread loads its rows of
-// R_V^T (coalesced: thread (part p, column c) reads column c of rows
-// [p RP, (p + 1) RP)).
+// records; the first copy also brings the BF16 record and R_V^T (to the end of
+// the rings), so that everything the merge reads lands after one wait.
 template <int G, int GK>
 __device__ void merge_segment(const DevCache& c, int layer, const DecodeArgs& a, int ri, int head, int c_lo, int n2,
                               const float* recs, const float* bf16_recs, float* __restrict__ out, Smem<G, GK>& sm,
@@ -1245,7 +1251,8 @@ __device__ void merge_segment(const DevCache& c, int layer, const DecodeArgs& a,
   constexpr int NTH = Tune<G, GK>::THREADS, NPART = Smem<G, GK>::NPART;
   constexpr int PAIRS = (G * D + NTH - 1) / NTH;          // (head, channel) pairs per thread
   constexpr int RF = G * PART;                            // floats per record
-  constexpr int CAP = int(sizeof(sm.buf.ring) / (RF * sizeof(float))) - 1;   // records per chunk
+  constexpr int RVB = D * D * int(sizeof(float));                            // R_V^T bytes
+  constexpr int CAP = int((sizeof(sm.buf.ring) - RVB) / (RF * sizeof(float))) - 1;   // records per chunk
   constexpr int RP = (D + NPART - 1) / NPART;                                // R_V^T rows per part
   constexpr int U = 4;
   static_assert(CAP >= 1, "staging");
@@ -1254,23 +1261,23 @@ __device__ void merge_segment(const DevCache& c, int layer, const DecodeArgs& a,
   const int s = ri * c.Hkv + head;
   const int items = n2;
   float* stage = reinterpret_cast<float*>(&sm.buf.ring[0][0][0]);   // [CAP][RF], then the BF16 record
+  float* rvt_s = reinterpret_cast<float*>(&sm.buf.ring[0][0][0] + sizeof(sm.buf.ring) - RVB);   // R_V^T [D][D]
+  // the copies are issued from the last warp, which has no head of its own below
+  // (the issue of a large bulk copy holds up its warp for a while)
   auto issue = [&](int j0, int nk) {
-    if (t == 0) {
+    if (t == NTH - 32) {
       // the rings were last written through the generic proxy (weights)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_expect_tx(&sm.mbar_m, (nk + (j0 == 0 ? 1 : 0)) * RF * 4);
+      mbar_expect_tx(&sm.mbar_m, (nk + (j0 == 0 ? 1 : 0)) * RF * 4 + (j0 == 0 ? RVB : 0));
       if (nk > 0) tma_load_1d(stage, recs + (size_t)(s + c_lo + j0) * RF, nk * RF * 4, &sm.mbar_m);
-      if (j0 == 0) tma_load_1d(stage + CAP * RF, bf16_recs + (size_t)s * RF, RF * 4, &sm.mbar_m);
+      if (j0 == 0) {
+        tma_load_1d(stage + CAP * RF, bf16_recs + (size_t)s * RF, RF * 4, &sm.mbar_m);
+        tma_load_1d(rvt_s, c.rot_vt + ((size_t)layer * c.Hkv + head) * D * D, RVB, &sm.mbar_m);
+      }
     }
   };
   issue(0, min(CAP, items));
   const int rch = t % D, rpart = t / D, r0 = rpart * RP;
-  float rv[RP];
-  {
-    const float* __restrict__ RVt = c.rot_vt + ((size_t)layer * c.Hkv + head) * D * D + rch;
-#pragma unroll
-    for (int i = 0; i < RP; ++i) rv[i] = r0 + i < D ? __ldg(RVt + (size_t)(r0 + i) * D) : 0.0f;
-  }
   // per head g: running max M and sum L (warp g keeps them in registers, lane 0's
   // copy in sm.mh / sm.lh), and per chunk the records' weights 2^(m_j - M)
   float* wj = reinterpret_cast<float*>(&sm.meta[0][0]);   // [CAP][G]
@@ -1283,7 +1290,7 @@ __device__ void merge_segment(const DevCache& c, int layer, const DecodeArgs& a,
   for (int j0 = 0; j0 == 0 || j0 < items; j0 += CAP) {   // the first chunk also brings the BF16 record
     const int nk = min(CAP, items - j0);
     if (j0 > 0) issue(j0, nk);
-    if (!mbar_wait(&sm.mbar_m, mphase, DECODE_WAIT_LIMIT) && t == 0) atomicOr(c.err, ERR_TIMEOUT);
+    if (!mbar_wait(&sm.mbar_m, mphase, DECODE_WAIT_LIMIT) && t == NTH - 32) atomicOr(c.err, ERR_TIMEOUT);
     mphase ^= 1u;
     if (warp < G) {
       const float* r = stage + warp * PART;
@@ -1344,15 +1351,16 @@ __device__ void merge_segment(const DevCache& c, int layer, const DecodeArgs& a,
   }
   __syncthreads();
   {
+    // O_hist R_V^T: thread (part p, column c) sums rows [p RP, (p + 1) RP) of column c
     float acc[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) acc[g] = 0.0f;
+    const int r1 = min(D, r0 + RP);
+#pragma unroll 4
+    for (int j = r0; j < r1; ++j) {
+      const float rv = rvt_s[j * D + rch];
 #pragma unroll
-    for (int i = 0; i < RP; ++i) {
-      if (r0 + i < D) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) acc[g] = fmaf(sm.scr.mrg.hist[g][r0 + i], rv[i], acc[g]);
-      }
+      for (int g = 0; g < G; ++g) acc[g] = fmaf(sm.scr.mrg.hist[g][j], rv, acc[g]);
     }
 #pragma unroll
     for (int g = 0; g < G; ++g) sm.scr.mrg.part[rpart][g][rch] = acc[g];
@@ -1546,7 +1554,7 @@ __global__ void __launch_bounds__(Tune<G, GK>::THREADS, 1)
     grid_dep_launch();  // the next launch may be scheduled (every CTA of this one is running); it waits for it
     if (S.valid) {
       QRows<G, GK> qv;
-      load_q<G, GK>(c, a.r[S.ri], S.head, q, qv);   // in flight with the page-id loads of the copies
+      load_q<G, GK>(c, layer, a.r[S.ri], S.head, q, qv);   // in flight with the page-id loads of the copies
       int2_issue_first<G, GK>(c, layer, a.r[S.ri], S.head, S.p0, S.p1, sm, epoch, a.dbg.wait_limit, nc, hold,
                               timed_out, a.prefetch ? 2 : 0);
       build_qfrag<G, GK>(c, qv, rk, sm);
@@ -1577,7 +1585,7 @@ __global__ void __launch_bounds__(Tune<G, GK>::THREADS, 1)
       RkRows<G, GK> rk;
       QRows<G, GK> qv;
       load_rk<G, GK>(c, layer, N.head, rk);
-      load_q<G, GK>(c, a.r[N.ri], N.head, q, qv);
+      load_q<G, GK>(c, layer, a.r[N.ri], N.head, q, qv);
       int2_issue_first<G, GK>(c, layer, a.r[N.ri], N.head, N.p0, N.p1, sm, epoch, a.dbg.wait_limit, nc, hold,
                               timed_out);
       build_qfrag<G, GK>(c, qv, rk, sm);
