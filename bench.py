@@ -181,7 +181,7 @@ def algorithmic_bytes(tokens: int, hist_end: int, kv_heads: int, group: int = 12
 class Workload:
     """The cache, its rotations and every input of the timed steps, resident on the GPU."""
 
-    def __init__(self, cfg_id: int, steps_total: int, log, layers: int = 0, override=None):
+    def __init__(self, cfg_id: int, steps_total: int, log, layers: int = 0, override=None, reserve: int = 0):
         import torch
         from bit_rotated_kv_decode_gb300 import binding, build, calibrate, synth
         build.build()
@@ -208,8 +208,10 @@ class Workload:
         self.rk, self.rv, self.tk, self.tv = calibrate.calibrate_model(cfg_id, self.L, self.hq, self.hkv,
                                                                        drift=self.drift, layers=fit)
         log(f"calibration {time.time() - t:.1f}s")
-        max_pages = pages_for(self.T0 + steps_total + 64) + 1
-        n_pages = sum(pages_for(t + steps_total + 64) + 1 for t in self.lens) + 8
+        # reserve: extra tokens per request (steps that reuse earlier inputs) the page pool must hold
+        grow = steps_total + reserve
+        max_pages = pages_for(self.T0 + grow + 64) + 1
+        n_pages = sum(pages_for(t + grow + 64) + 1 for t in self.lens) + 8
         seed = synth.seed_for(cfg_id, 0, 0, 99) or 1
         self.group = w.get("group", 128)
         cfg = binding.make_config(self.L, self.hq, self.hkv, self.batch + (1 if self.prefix else 0), max_pages,
@@ -324,7 +326,8 @@ def run_gpu(args, log):
     W, K = args.warmup, args.steps
     ew, ek = 2, max(3, K // 2)
     wl = Workload(args.config, W + 2 * K + ew + ek, log, args.layers,
-                  override={"group": args.group} if args.group != 128 else None)
+                  override={"group": args.group} if args.group != 128 else None,
+                  reserve=0 if args.demote_first else 2 * DEMOTE_STEP_PAIRS)
     wl.fused = not args.separate_calls
     wl.demote_first = args.demote_first
     stream = wl.stream_ptr()
@@ -409,6 +412,106 @@ def run_gpu(args, log):
         "world": world, "rank": rank,
     }
     return wl, res
+
+
+DEMOTE_STEP_PAIRS = 600      # step pairs of the in-step demotion cost (about 1 s at 100K x 32 layers)
+DEMOTE_MIN_MS = 1000.0       # timed region of each oscar_demote_layers rate
+
+
+def demote_record(wl, log):
+    """Demotion throughput, two ways.
+
+    (1) oscar_demote_layers over all layers of the workload's shape at batch 1 and
+        batch 32, as tokens x layers per second.  Each request holds a sink, a full
+        recent window and one history page; a chunk of 192 calls (each demotes one
+        token per request in every layer) is timed with CUDA events, then the
+        requests are closed and refilled outside the timed chunks; chunks repeat
+        until their summed time reaches DEMOTE_MIN_MS.
+    (2) The demotion's cost inside the fused step, on the workload itself: pairs of
+        whole steps (oscar_decode_step in every layer), the first with a full window
+        (every append demotes), the second after one oscar_demote_layers made room
+        (no append demotes); CUDA events around each step and around the
+        oscar_demote_layers call.  The step inputs of earlier steps are reused."""
+    import torch
+    b, L, hq, hkv = wl.b, wl.L, wl.hq, wl.hkv
+    lib, stream = wl.lib, wl.stream_ptr()
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    rec = {}
+    # (1) standalone rates
+    T0, per_chunk = 320 + 64, 192
+    kk = [wl.synth.kv_tokens(wl.cfg_id, l, hkv, "k", range(0, T0), device="cuda", stream_id=5) for l in range(L)]
+    vv = [wl.synth.kv_tokens(wl.cfg_id, l, hkv, "v", range(0, T0), device="cuda", stream_id=5) for l in range(L)]
+    rates = {}
+    for n in (1, 32):
+        max_pages = pages_for(T0 + 64) + 4
+        cfg = b.make_config(L, hq, hkv, n, max_pages, n * max_pages + 8, 0, 0.0, 77, group_size=wl.group)
+        cache = b.OscarCache(cfg, torch.from_numpy(wl.rk).cuda(), torch.from_numpy(wl.rv).cuda(), wl.tk, wl.tv)
+        h = cache.h
+        timed_ms, chunks = 0.0, 0
+        while timed_ms < DEMOTE_MIN_MS:
+            reqs = [cache.open() for _ in range(n)]
+            for l in range(L):
+                for r in reqs:
+                    cache.prefill(r, l, kk[l], vv[l])
+            ra = (ctypes.c_int32 * n)(*reqs)
+            e0, e1 = mk(), mk()
+            torch.cuda.synchronize()
+            e0.record()
+            for _ in range(per_chunk):
+                if lib.oscar_demote_layers(h, 0, L, n, ra, stream):
+                    raise RuntimeError(lib.oscar_last_error(h).decode())
+            e1.record()
+            torch.cuda.synchronize()
+            cache.check()
+            timed_ms += e0.elapsed_time(e1)
+            chunks += 1
+            for r in reqs:
+                cache.close(r)
+        calls = chunks * per_chunk
+        rates[n] = {"tok_layers_per_s": n * L * calls / (timed_ms * 1e-3), "us_per_call": 1000.0 * timed_ms / calls,
+                    "calls": calls, "timed_ms": timed_ms, "launches_per_call": -(-L * n // 96)}
+        log(f"demote_layers batch {n}: {rates[n]['us_per_call']:.2f} us/call over {calls} calls")
+        cache.close_handle()
+        del cache
+    del kk, vv
+    rec["demote_layers"] = {"batch_1": rates[1], "batch_32": rates[32],
+                            "state": f"{T0} tokens per request (64 sink + 64 history + 256 recent); chunks of "
+                                     f"{per_chunk} calls timed with CUDA events, refills between chunks untimed"}
+    # (2) in the fused step
+    if not wl.demote_first:
+        n, ra = wl.batch, wl.reqs_arr
+        P = DEMOTE_STEP_PAIRS
+        ptrs = [wl.pointers(s) for s in range(min(2 * P, wl.k_new.shape[0]))]
+        ev = [[mk() for _ in range(6)] for _ in range(P)]
+        torch.cuda.synchronize()
+        for i in range(P):
+            e = ev[i]
+            e[0].record()
+            wl.run_step(ptrs[(2 * i) % len(ptrs)], stream)
+            e[1].record()
+            e[2].record()
+            if lib.oscar_demote_layers(wl.h, 0, L, n, ra, stream):
+                raise RuntimeError(lib.oscar_last_error(wl.h).decode())
+            e[3].record()
+            e[4].record()
+            wl.run_step(ptrs[(2 * i + 1) % len(ptrs)], stream)
+            e[5].record()
+        torch.cuda.synchronize()
+        wl.cache.check()
+        with_d = float(np.mean([1000.0 * e[0].elapsed_time(e[1]) for e in ev[1:]]))
+        dl = float(np.mean([1000.0 * e[2].elapsed_time(e[3]) for e in ev[1:]]))
+        without = float(np.mean([1000.0 * e[4].elapsed_time(e[5]) for e in ev[1:]]))
+        rec["in_step"] = {
+            "step_us_with_demote": with_d, "step_us_without_demote": without,
+            "demote_cost_us_per_layer": (with_d - without) / L,
+            "demote_layers_us_at_workload_state": dl,
+            "demoted_tok_layers_per_s_in_steps": n * L / (with_d * 1e-6),
+            "pairs": P - 1,
+            "note": "whole steps (every layer's oscar_decode_step), CUDA events around each; the cost is the "
+                    "difference per layer between a step whose appends demote and one whose appends find room"}
+        log(f"in-step demotion: {with_d:.1f} vs {without:.1f} us/step ({(with_d - without) / L:.2f} us/layer); "
+            f"demote_layers {dl:.1f} us")
+    return rec
 
 
 def bf16_baseline(wl, r, log, launches: int = 40):
@@ -596,6 +699,7 @@ def run_write(args, log):
     flops = (T - 320) * hkv * PREFILL_FLOP_PER_TOKEN_HEAD
     achieved = flops / (pre_avg * 1e-6) / 1e12
     peak, peak_src = measured_peak_bf16()
+    hbm_peak, hbm_src = measured_peak_hbm()
     pre_bytes = T * hkv * 512 + (T - 320) * hkv * INT2_BYTES_PER_TOKEN_HEAD + 320 * hkv * 512
     return {
         "metric": METRIC, "value": tok_s, "unit": "demoted tok/s (tokens x layers / s)", "n_gpus": world,
@@ -607,11 +711,20 @@ def run_write(args, log):
                          % (pre_bytes / 1e6)},
         "prefill_us_per_layer": pre_avg,
         "prefill_gbs": pre_bytes / (pre_avg * 1e-6) / 1e9,
-        "roofline": {"bound": "tensor", "kernel": "prefill_hist_kernel (rotation on the tensor cores, exact quantiser)",
-                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                     "peak_source": peak_src, "flops": "algorithmic: 2 x 128 x 128 per token, kv head and K or V",
+        # the prefill moves 154 MB per layer against 17 GFLOP of rotation: HBM is the bound
+        "roofline": {"bound": "hbm", "kernel": "prefill (prefill_hist_kernel + prefill_bf16_kernel, one call)",
+                     "achieved": pre_bytes / (pre_avg * 1e-6) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": pre_bytes / (pre_avg * 1e-6) / 1e9 / hbm_peak, "peak_source": hbm_src,
+                     "bytes": "algorithmic per layer: every token's bf16 K and V read, the history's INT2 codes "
+                              "and meta and the BF16 segments written",
+                     "algorithmic_bytes_per_launch": pre_bytes,
+                     "duration_us_per_launch": pre_avg,
+                     "duration_from": "CUDA events around each layer's oscar_prefill_quantize call",
                      "traffic": committed_traffic("prefill_hist_kernel"),
-                     "algorithmic_bytes_per_launch": pre_bytes - 320 * hkv * 512 * 2},
+                     "traffic_kernel": "prefill_hist_kernel",
+                     "tensor": {"achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                                "peak_source": peak_src,
+                                "flops": "algorithmic: 2 x 128 x 128 per token, kv head and K or V"}},
         "e2e": {"value": e2e_tok_s, "unit": "demoted tok/s (tokens x layers / s)",
                 "h2d_bytes_per_step": (kn[0].numel() + vn[0].numel()) * 2, "d2h_bytes_per_step": 4},
         "gpu_launches": K * L,
@@ -734,6 +847,8 @@ def main(argv=None):
     ap.add_argument("--speedup-table", action="store_true",
                     help="INT2 vs BF16 decode per layer at 30K / 60K / 100K, batch 1 and 32 (one JSON line)")
     ap.add_argument("--layers", type=int, default=0, help="fewer layers (small profiling cases only)")
+    ap.add_argument("--no-demote-record", action="store_true",
+                    help="skip the oscar_demote_layers rates and the in-step demotion cost")
     ap.add_argument("--separate-calls", action="store_true",
                     help="time oscar_append + oscar_decode_attention per layer instead of oscar_decode_step")
     args = ap.parse_args(argv)
@@ -765,6 +880,8 @@ def main(argv=None):
     cpu = par = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu, par = cpu_baseline(wl, r, log)
+    # last: its steps append tokens that reuse earlier inputs, which the oracle check above does not follow
+    demote = demote_record(wl, log) if not args.no_demote_record else None
     traffic = committed_traffic("decode_kernel")
     kv_gbs = r["kv_bytes_step"] / (r["us_step"] * 1e-6) / 1e9
     line = {
@@ -818,6 +935,8 @@ def main(argv=None):
     }
     if base16 is not None:
         line["bf16_baseline"] = base16
+    if demote is not None:
+        line["demote"] = demote
     if cpu is not None:
         line["cpu_baseline"] = cpu
         line["parity"] = par

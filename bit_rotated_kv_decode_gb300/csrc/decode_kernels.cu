@@ -38,7 +38,9 @@
 //     occupying the N columns as (head, part) pairs;
 //   * every product is exact in fp32; accumulation is fp32.
 // Pages are staged HBM -> shared memory by TMA bulk copies (cp.async.bulk, one
-// record per page and kv head) into a per-warp ring, completion on mbarriers;
+// record per page and kv head: 4608 B at quantisation group 128 -- K codes
+// [64][32] B, V codes [64][32] B, K and V {s, z} [64] x 4 B -- and 5120 B at
+// group 64, with two {s, z} per token) into a per-warp ring, completion on mbarriers;
 // every wait is bounded and reports ERR_TIMEOUT instead of hanging.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>

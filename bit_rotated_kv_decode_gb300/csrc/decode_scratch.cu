@@ -1,11 +1,11 @@
 // Fixed, statically allocated decode scratch for oscar_decode_attention_noalloc:
-// q_rot and the partials of the decode kernels.
+// the partial records (o, m, l per query head) of the decode kernel.
 //
 // Some callers cannot allocate device memory around a decode step: a serving
 // engine that hands all free HBM to its KV pools at start-up and owns no
 // allocator it may call per step, or a plain C host that has no allocator to
-// pass at all.  For them q_rot and the partials of the decode kernels
-// live in one file-scope device array, loaded with the module, instead of a
+// pass at all.  For them the partial records of the decode kernel live in one
+// file-scope device array, loaded with the module, instead of a
 // caller-owned workspace.  Nothing here calls cudaMalloc, cudaFree or any
 // library routine that allocates.
 //

@@ -39,12 +39,13 @@ def rotations(cfg_id, layers, hq, hkv, drift=False):
 
 class Setup:
     def __init__(self, b, cfg_id=0, layers=1, hq=32, hkv=8, max_req=4, max_pages=64, pages=256, seed=0,
-                 drift=False, total_len=0, group=128):
+                 drift=False, total_len=0, group=128, rot=None):
         self.b = b
         self.group = group
         self.cfg_id, self.L, self.hq, self.hkv = cfg_id, layers, hq, hkv
         self.drift, self.total_len = drift, total_len
-        self.rk, self.rv, self.tk, self.tv = rotations(cfg_id, layers, hq, hkv, drift)
+        # rot: (rk, rv, tk, tv) in place of the calibrated OSCAR rotations
+        self.rk, self.rv, self.tk, self.tv = rot if rot is not None else rotations(cfg_id, layers, hq, hkv, drift)
         cfg = b.make_config(layers, hq, hkv, max_req, max_pages, pages, 0, 0.0, seed, group_size=group)
         self.cache = b.OscarCache(cfg, torch.from_numpy(self.rk).cuda(), torch.from_numpy(self.rv).cuda(),
                                   self.tk, self.tv)
@@ -105,8 +106,9 @@ class Setup:
                                 self.rk[layer].astype(np.float64), self.rv[layer].astype(np.float64),
                                 self.tk[layer], self.tv[layer], group=self.group)
 
-    def check_pages(self, r, layer):
-        """Page tables exact; every history group within the parity rules; BF16 rows exact."""
+    def check_pages(self, r, layer, pages=None):
+        """Page tables exact; every history group within the parity rules; BF16 rows exact.
+        pages: history page indices to check (default all)."""
         pt, bf = self.cache.pages(r)
         assert pt == self.mirror.reqs[r].hist_pt and bf == self.mirror.reqs[r].bf16_pt
         dev_pt = self.cache.device_page_table()[r, :len(pt)].cpu().tolist()
@@ -120,6 +122,9 @@ class Setup:
         nh = he - 64
         if nh > 0:
             pos = np.arange(64, he)
+            if pages is not None:
+                pos = pos[np.isin((pos - 64) // 64, np.asarray(pages))]
+            nh = pos.size
             pages = np.array(pt)[(pos - 64) // 64]
             rows = (pos - 64) % 64
             for h in range(self.hkv):
@@ -129,7 +134,7 @@ class Setup:
                     codes = np.stack([f[1 if which else 0] for f in fields])
                     meta = np.stack([f[3 if which else 2] for f in fields])
                     from oracle import quant
-                    x32 = quant.rotate_to_fp32(src[64:he, h], rr[layer, h].astype(np.float64))
+                    x32 = quant.rotate_to_fp32(src[pos, h], rr[layer, h].astype(np.float64))
                     st = parity.compare_groups(codes, meta, x32, tau[layer, h], self.group)
                     for key in stats:
                         stats[key] += st[key]

@@ -95,3 +95,21 @@ def test_extreme_scales_and_zero_scale():
     v = np.linspace(-1, 1, 10).astype(F)
     ca, cb = fast_code(v, v, z, s, np.zeros(10, F))
     assert np.all(ca == 0) and np.all(cb == 0) and np.all(ieee_code(v, z, s) == 0)
+
+
+def test_device_rule_is_the_rule_checked_here():
+    """The kernels' decision (quant_device.cuh) uses the constants and forms of
+    fast_code above: an rcp.approx reciprocal, the margin (|q'| + 1) 2^-19, and
+    floor(q' -/+ M + 1/2) clamped to [0, 3] at the two ends of the interval."""
+    import os
+    import re
+    src = open(os.path.join(os.path.dirname(__file__), "..", "bit_rotated_kv_decode_gb300", "csrc",
+                            "quant_device.cuh")).read()
+    assert "rcp.approx.f32" in src
+    assert re.search(r"__fmul_rn\(fabsf\(qa\) \+ 1\.0f, 0x1p-19f\)", src)
+    assert re.search(r"__fmul_rn\(fabsf\(qb\) \+ 1\.0f, 0x1p-19f\)", src)
+    assert re.search(r"fminf\(fmaxf\(floorf\(qa - ma \+ 0\.5f\), 0\.0f\), 3\.0f\)", src)
+    assert re.search(r"fminf\(fmaxf\(floorf\(qb \+ mb \+ 0\.5f\), 0\.0f\), 3\.0f\)", src)
+    # and this file's restatement uses the same margin
+    assert F(2.0 ** -19) == F(float.fromhex("0x1p-19"))
+
