@@ -7,9 +7,8 @@ spreads the outliers; OSCAR's R_K = U_Q H P_br also aligns the grid with the
 query covariance (and R_V = U_S H P_br with the score-weighted values), which
 is what its attention-error tables measure.
 
-For one seeded synthetic layer (K/V with outlier channels, queries from
-N(0, Sigma)), each variant fits its clip thresholds on the same calibration
-set, prefills a cache through the C ABI and decodes the same queries.  Against
+For one seeded synthetic layer, each variant fits its clip thresholds on the
+same calibration set, prefills a cache through the C ABI and decodes the same queries.  Against
 exact attention over the BF16 tokens (float64 on the host) it reports:
   * logit_rel: |S - S^|_F / |S|_F of the scaled scores q k^T / sqrt(d) over the
     INT2 history, with K^ dequantised from the cache's own bytes
@@ -21,6 +20,13 @@ The same page says the permuted bit-reversal P_br spreads every importance
 level over the quantisation groups, which only matters with more than one group
 per token-head: the "_nobr" variants drop it (R = H, R = U H) to measure that at
 G_K = 64.
+Two laws (synth.py): "outliers", the workloads' law (K / V with x20 outlier
+channels, queries from N(0, Sigma) with a full-rank Wishart Sigma), and
+"subspace", where the queries of a GQA group have four dominant eigen-directions
+that the keys share (x5 outlier channels).  On the first a Hadamard rotation
+alone already gives every channel the same query importance (the outliers are
+axis-aligned), so the query eigenbasis has nothing to add; the second is the
+structure the query-covariance alignment is for.
 Usage: ``python -m bit_rotated_kv_decode_gb300.ablation``.
 """
 from __future__ import annotations
@@ -88,18 +94,29 @@ def dequantised_keys(pool, hist_pages, nhist: int, rk, hkv: int, group: int = 12
 
 
 def run(cfg_id: int = 0, hq: int = 32, hkv: int = 8, tokens: int = 8192, queries: int = 8, clip: float = 0.9,
-        layer: int = 0, group: int = 128, variants=VARIANTS) -> dict:
+        layer: int = 0, group: int = 128, variants=VARIANTS, law: str = "outliers") -> dict:
+    """law: "outliers" (the workloads' law: x20 outlier channels, full-rank query
+    covariance) or "subspace" (queries and keys sharing a 4-dimensional dominant
+    subspace, x5 outlier channels)."""
     import torch
 
     from . import binding
     binding.load()
     d = synth.HEAD_DIM
-    q_cal, k_cal, v_cal = synth.calibration_set(cfg_id, layer, hq, hkv, 512)
-    k = synth.kv_tokens(cfg_id, layer, hkv, "k", range(tokens), device="cuda")
-    v = synth.kv_tokens(cfg_id, layer, hkv, "v", range(tokens), device="cuda")
+    if law == "outliers":
+        q_cal, k_cal, v_cal = synth.calibration_set(cfg_id, layer, hq, hkv, 512)
+        k = synth.kv_tokens(cfg_id, layer, hkv, "k", range(tokens), device="cuda")
+        v = synth.kv_tokens(cfg_id, layer, hkv, "v", range(tokens), device="cuda")
+        qs = [synth.queries(cfg_id, layer, hq, 1, step, device="cuda") for step in range(queries)]
+    elif law == "subspace":
+        q_cal, k_cal, v_cal = synth.subspace_calibration_set(cfg_id, layer, hq, hkv, 512)
+        k = synth.subspace_kv(cfg_id, layer, hkv, "k", tokens, device="cuda")
+        v = synth.subspace_kv(cfg_id, layer, hkv, "v", tokens, device="cuda")
+        qs = [synth.subspace_queries(cfg_id, layer, hq, hkv, 1, step, device="cuda") for step in range(queries)]
+    else:
+        raise ValueError(law)
     kf = k.float().cpu().numpy().astype(np.float64)
     vf = v.float().cpu().numpy().astype(np.float64)
-    qs = [synth.queries(cfg_id, layer, hq, 1, step, device="cuda") for step in range(queries)]
     refs = [exact_attention(q[0].float().cpu().numpy().astype(np.float64), kf, vf, hkv) for q in qs]
     pages = (tokens - 320) // 64 + 2
     results = {}
@@ -142,7 +159,7 @@ def run(cfg_id: int = 0, hq: int = 32, hkv: int = 8, tokens: int = 8192, queries
         results[variant] = {"logit_rel": (lnum / lden) ** 0.5, "kl": kl / (len(qs) * hq),
                             "out_rel": (num / den) ** 0.5, "out_max_abs": max_abs}
     return {"config": {"cfg_id": cfg_id, "q_heads": hq, "kv_heads": hkv, "tokens": tokens, "queries": queries,
-                       "clip": clip, "layer": layer, "group": group}, "results": results}
+                       "clip": clip, "layer": layer, "group": group, "law": law}, "results": results}
 
 
 if __name__ == "__main__":
@@ -151,3 +168,6 @@ if __name__ == "__main__":
     # the bit-reversal's share, with one group and with two groups per token-head
     for group in (128, 64):
         print(json.dumps(run(clip=0.9, group=group, variants=BR_VARIANTS)))
+    # queries with a few dominant directions that the keys share
+    for group in (128, 64):
+        print(json.dumps(run(clip=0.9, group=group, variants=BR_VARIANTS + ("naive",), law="subspace")))

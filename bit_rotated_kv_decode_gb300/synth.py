@@ -17,6 +17,14 @@ Workloads follow the shapes of the Qwen3 attention layers the pages evaluate
 * An optional slow drift of the channel means for the 128K workload:
   mu_c(t) = mu0_c + (t / T) * delta_c with mu0, delta ~ N(0, 0.5^2).
 * Calibration sets of 512 tokens per head drawn from the same laws.
+* A second law for the rotation ablation, a shared low-rank subspace: per
+  (layer, kv head) a seeded orthonormal basis u_1..u_4 of a 4-dimensional
+  subspace; keys k = x + 6 sum_i z_i u_i (x ~ N(0, 1) with the four outlier
+  channels scaled by 5 instead of 20, z ~ N(0, 1)); values alike with a basis
+  of their own; the group's queries q = 3 sum_i z_i u_i + 0.3 N(0, I).  Queries
+  then have a few dominant eigen-directions, which keys share ("Together AI
+  Open-Sources OSCAR", MarkTechPost, section "What OSCAR Does Differently":
+  the rotation is aligned with the query covariance's dominant directions).
 
 Seeds: seed(cfg, layer, head, purpose) = splitmix64(cfg<<40 | layer<<24 |
 head<<8 | purpose).  Tensors are drawn with torch generators on the device
@@ -47,6 +55,9 @@ P_APPEND_V = 13
 P_LENGTHS = 14
 P_PREFIX_K = 15
 P_PREFIX_V = 16
+P_SUB_BASIS_K = 17
+P_SUB_BASIS_V = 18
+P_SUB_Z = 19
 
 OUTLIER_CHANNELS = 4
 OUTLIER_SCALE = 20.0
@@ -165,3 +176,68 @@ def request_lengths(cfg: int, batch: int, lo: int, hi: int) -> list[int]:
     """Seeded context lengths drawn uniformly from [lo, hi]."""
     rng = np.random.Generator(np.random.PCG64(seed_for(cfg, 0, 0, P_LENGTHS)))
     return [int(x) for x in rng.integers(lo, hi + 1, size=batch)]
+
+
+# ---- the shared low-rank subspace law of the rotation ablation -------------------------------
+SUBSPACE_RANK = 4
+SUBSPACE_KV_SCALE = 6.0
+SUBSPACE_Q_SCALE = 3.0
+SUBSPACE_Q_NOISE = 0.3
+SUBSPACE_OUTLIER_SCALE = 5.0
+
+
+def subspace_basis(cfg: int, layer: int, kv_head: int, which: str) -> np.ndarray:
+    """float64 [128][SUBSPACE_RANK]: orthonormal columns u_1..u_r of the head's subspace
+    (the Q factor, with a positive R diagonal, of a seeded Gaussian)."""
+    purpose = P_SUB_BASIS_K if which == "k" else P_SUB_BASIS_V
+    rng = np.random.Generator(np.random.PCG64(seed_for(cfg, layer, kv_head, purpose)))
+    a = rng.normal(size=(HEAD_DIM, SUBSPACE_RANK))
+    qf, rf = np.linalg.qr(a)
+    return qf * np.sign(np.diag(rf))[None, :]
+
+
+def _subspace_part(cfg, layer, heads, which_basis, n, scale, seed, device):
+    """[n][len(heads)][128] float32: scale * sum_i z_i u_i per head, z ~ N(0, 1)."""
+    g = _gen(device, seed)
+    z = torch.randn((n, len(heads), SUBSPACE_RANK), generator=g, device=device, dtype=torch.float32)
+    basis = torch.from_numpy(np.stack([subspace_basis(cfg, layer, h, which_basis) for h in heads])).to(
+        device=device, dtype=torch.float32)                       # [heads][128][r]
+    return scale * torch.einsum("nhr,hdr->nhd", z, basis)
+
+
+def subspace_kv(cfg: int, layer: int, num_kv_heads: int, which: str, n: int, device="cpu",
+                calibration: bool = False, stream_id: int = 0) -> torch.Tensor:
+    """bf16 [n][H_kv][128] K or V rows of the shared-subspace law."""
+    if which == "k":
+        purpose = P_CAL_K if calibration else P_K
+    else:
+        purpose = P_CAL_V if calibration else P_V
+    g = _gen(device, seed_for(cfg, layer, stream_id, purpose, step=1))
+    x = torch.randn((n, num_kv_heads, HEAD_DIM), generator=g, device=device, dtype=torch.float32)
+    sc = torch.from_numpy(channel_scale(cfg, layer, num_kv_heads, which)).to(device)
+    x.mul_(torch.where(sc > 1.0, torch.full_like(sc, SUBSPACE_OUTLIER_SCALE), sc))
+    x.add_(_subspace_part(cfg, layer, range(num_kv_heads), which, n, SUBSPACE_KV_SCALE,
+                          seed_for(cfg, layer, stream_id, P_SUB_Z, step=purpose), device))
+    return x.to(torch.bfloat16)
+
+
+def subspace_queries(cfg: int, layer: int, num_q_heads: int, num_kv_heads: int, n: int, step: int,
+                     device="cpu", purpose: int = P_Q) -> torch.Tensor:
+    """bf16 [n][H_q][128] queries of the shared-subspace law: query head h draws in the
+    key subspace of kv head h // (H_q / H_kv)."""
+    g_size = num_q_heads // num_kv_heads
+    heads = [h // g_size for h in range(num_q_heads)]
+    q = _subspace_part(cfg, layer, heads, "k", n, SUBSPACE_Q_SCALE,
+                       seed_for(cfg, layer, 0, purpose, step=step + 1), device)
+    g = _gen(device, seed_for(cfg, layer, 1, purpose, step=step + 1))
+    q.add_(SUBSPACE_Q_NOISE * torch.randn((n, num_q_heads, HEAD_DIM), generator=g, device=device,
+                                          dtype=torch.float32))
+    return q.to(torch.bfloat16).contiguous()
+
+
+def subspace_calibration_set(cfg: int, layer: int, num_q_heads: int, num_kv_heads: int, n: int = 512):
+    """Host float64 calibration tensors of the shared-subspace law (as calibration_set)."""
+    k = subspace_kv(cfg, layer, num_kv_heads, "k", n, calibration=True)
+    v = subspace_kv(cfg, layer, num_kv_heads, "v", n, calibration=True)
+    q = subspace_queries(cfg, layer, num_q_heads, num_kv_heads, n, 0, purpose=P_CAL_Q)
+    return (q.to(torch.float64).numpy(), k.to(torch.float64).numpy(), v.to(torch.float64).numpy())
