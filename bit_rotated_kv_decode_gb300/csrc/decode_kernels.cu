@@ -8,7 +8,7 @@
 // System": the value path is inverse-rotated.
 //
 // One launch per layer (and per batch of up to 64 requests): one persistent CTA
-// per SM.  The first nbc CTAs attend to the BF16 sink and recent pages of the
+// per SM.  nbc of them (the last blocks) attend to the BF16 sink and recent pages of the
 // (request, kv head) segments, a whole segment's BF16 pages at a time, with the
 // unrotated q (one record per segment, plain basis).  The other CTAs share the
 // INT2 history pages, cut into equal contiguous ranges that a CTA walks segment
@@ -232,6 +232,7 @@ struct Smem {
   __align__(16) uint32_t qf[QFrag<G>::WORDS];   // q operands of the current segment (read as uint4)
   __align__(8) uint64_t bar[NW][STAGES];
   uint64_t mbar_m;                       // staging of a merge's records
+  uint64_t mbar_r;                       // staging of a merge's R_V^T
   __align__(16) float4 meta[NW][PAGE];   // INT2: per token {s_k, z_k, s_v 2^ew, z_v}; BF16: weights
   __align__(16) float4 meta2[NW][GK == 64 ? PAGE : 1];   // G_K = 64: the same for group 1
   WeightRows<G, GK, NW> w;
@@ -1196,33 +1197,47 @@ __device__ __forceinline__ int cta_of(int64_t u, int ncta, int64_t total) {
   return c;
 }
 
-// The segment holding INT2 cost unit u of this INT2 CTA's range [u0, u1)
-// (invalid once u drops below u0); prev receives the unit before the segment.  A
-// CTA walks its segments from the last one back: a segment's last page (which a
-// decode step's append may be filling) is then one of the last pages the CTA
+// The INT2 CTAs that hold pages of a segment starting at cost unit s0 with
+// units seg units: those whose ranges meet [page 0's unit, end).  A CTA whose
+// range meets only the segment's set-up units takes no part in it.
+__device__ __forceinline__ void segment_ctas(const DecodeArgs& a, int64_t s0, int64_t units, int& c_lo, int& c_hi) {
+  const int n2 = a.ncta - a.nbc;
+  c_lo = cta_of(s0 + DECODE_SEGMENT_SETUP_COST, n2, a.total_cost);
+  c_hi = cta_of(s0 + units - 1, n2, a.total_cost);
+}
+
+// The segment holding INT2 cost unit u of this INT2 CTA's range [u0, u1), or
+// the one before it where the range meets only u's segment's set-up units
+// (invalid once u drops below u0); prev receives the unit before the segment.
+// A CTA walks its segments from the last one back: a segment's last page (which
+// a decode step's append may be filling) is then one of the last pages the CTA
 // reads, long after the append is done.
 __device__ Seg plan_segment(const DecodeArgs& a, int Hkv, int icta, int64_t u, int64_t u0, int64_t u1,
                             int64_t& prev) {
   Seg e{};
   prev = u0 - 1;
-  if (u < u0) return e;
-  int ri, h;
-  int64_t s0;
-  segment_of(a, Hkv, u, ri, h, s0);
-  const int64_t np = a.r[ri].npages;
-  const int n2 = a.ncta - a.nbc;
-  prev = s0 - 1;
-  const int64_t end = s0 + seg_units(a.r[ri]);
-  const int64_t f0 = s0 + DECODE_SEGMENT_SETUP_COST;   // unit of page 0
-  e.valid = 1;
-  e.ri = ri;
-  e.head = h;
-  e.p0 = static_cast<int>(u0 > f0 ? (u0 - f0 < np ? u0 - f0 : np) : 0);
-  e.p1 = static_cast<int>(u1 > f0 ? (u1 - f0 < np ? u1 - f0 : np) : 0);
-  if (e.p1 < e.p0) e.p1 = e.p0;
-  e.slot = ri * Hkv + h + icta;
-  e.c_lo = cta_of(s0, n2, a.total_cost);
-  e.c_hi = cta_of(end - 1, n2, a.total_cost);
+  while (u >= u0) {
+    int ri, h;
+    int64_t s0;
+    segment_of(a, Hkv, u, ri, h, s0);
+    const int64_t np = a.r[ri].npages;
+    const int64_t f0 = s0 + DECODE_SEGMENT_SETUP_COST;   // unit of page 0
+    const int64_t p0 = u0 > f0 ? (u0 - f0 < np ? u0 - f0 : np) : 0;
+    const int64_t p1 = u1 > f0 ? (u1 - f0 < np ? u1 - f0 : np) : 0;
+    if (p1 <= p0) {   // set-up units only: the next CTA takes this segment
+      u = s0 - 1;
+      continue;
+    }
+    prev = s0 - 1;
+    e.valid = 1;
+    e.ri = ri;
+    e.head = h;
+    e.p0 = static_cast<int>(p0);
+    e.p1 = static_cast<int>(p1);
+    e.slot = ri * Hkv + h + icta;
+    segment_ctas(a, s0, seg_units(a.r[ri]), e.c_lo, e.c_hi);
+    return e;
+  }
   return e;
 }
 
@@ -1239,6 +1254,21 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// The ring tail where a merge stages R_V^T (64 KiB; the records go to the start).
+template <int G, int GK>
+__device__ __forceinline__ float* merge_rvt(Smem<G, GK>& sm) {
+  return reinterpret_cast<float*>(&sm.buf.ring[0][0][0] + sizeof(sm.buf.ring) - D * D * sizeof(float));
+}
+// R_V^T of (layer, kv head) into the ring tail, completion on mbar_r (one thread;
+// the rings hold no copy in flight and were last written through the generic proxy).
+template <int G, int GK>
+__device__ __forceinline__ void issue_rvt(const DevCache& c, int layer, int head, Smem<G, GK>& sm) {
+  constexpr uint32_t RVB = D * D * sizeof(float);
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_expect_tx(&sm.mbar_r, RVB);
+  tma_load_1d(merge_rvt(sm), c.rot_vt + ((size_t)layer * c.Hkv + head) * D * D, RVB, &sm.mbar_r);
+}
+
 // Merge of segment s = (ri, head) by the last CTA to finish it: the INT2 records
 // of its n2 INT2 CTAs c_lo .. c_lo + n2 - 1 and its BF16 record, online-softmax
 // combined per (query head, channel); then out = (O_bf16 + O_hist R_V^T) / L for
@@ -1249,7 +1279,7 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
 template <int G, int GK>
 __device__ void merge_segment(const DevCache& c, int layer, const DecodeArgs& a, int ri, int head, int c_lo, int n2,
                               const float* recs, const float* bf16_recs, float* __restrict__ out, Smem<G, GK>& sm,
-                              uint32_t& mphase) {
+                              uint32_t& mphase, bool rvt_issued = false) {
   constexpr int NTH = Tune<G, GK>::THREADS, NPART = Smem<G, GK>::NPART;
   constexpr int PAIRS = (G * D + NTH - 1) / NTH;          // (head, channel) pairs per thread
   constexpr int RF = G * PART;                            // floats per record
@@ -1263,18 +1293,20 @@ __device__ void merge_segment(const DevCache& c, int layer, const DecodeArgs& a,
   const int s = ri * c.Hkv + head;
   const int items = n2;
   float* stage = reinterpret_cast<float*>(&sm.buf.ring[0][0][0]);   // [CAP][RF], then the BF16 record
-  float* rvt_s = reinterpret_cast<float*>(&sm.buf.ring[0][0][0] + sizeof(sm.buf.ring) - RVB);   // R_V^T [D][D]
+  float* rvt_s = merge_rvt(sm);   // R_V^T [D][D]
   // the copies are issued from the last warp, which has no head of its own below
   // (the issue of a large bulk copy holds up its warp for a while)
   auto issue = [&](int j0, int nk) {
     if (t == NTH - 32) {
-      // the rings were last written through the generic proxy (weights)
+      // the rings were last written through the generic proxy (weights), and the
+      // records by other CTAs' generic stores (acquired through the counter)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_expect_tx(&sm.mbar_m, (nk + (j0 == 0 ? 1 : 0)) * RF * 4 + (j0 == 0 ? RVB : 0));
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      mbar_expect_tx(&sm.mbar_m, (nk + (j0 == 0 ? 1 : 0)) * RF * 4);
       if (nk > 0) tma_load_1d(stage, recs + (size_t)(s + c_lo + j0) * RF, nk * RF * 4, &sm.mbar_m);
       if (j0 == 0) {
         tma_load_1d(stage + CAP * RF, bf16_recs + (size_t)s * RF, RF * 4, &sm.mbar_m);
-        tma_load_1d(rvt_s, c.rot_vt + ((size_t)layer * c.Hkv + head) * D * D, RVB, &sm.mbar_m);
+        if (!rvt_issued) issue_rvt(c, layer, head, sm);
       }
     }
   };
@@ -1292,7 +1324,7 @@ __device__ void merge_segment(const DevCache& c, int layer, const DecodeArgs& a,
   for (int j0 = 0; j0 == 0 || j0 < items; j0 += CAP) {   // the first chunk also brings the BF16 record
     const int nk = min(CAP, items - j0);
     if (j0 > 0) issue(j0, nk);
-    if (!mbar_wait(&sm.mbar_m, mphase, DECODE_WAIT_LIMIT) && t == NTH - 32) atomicOr(c.err, ERR_TIMEOUT);
+    if (!mbar_wait(&sm.mbar_m, mphase & 1u, DECODE_WAIT_LIMIT) && t == NTH - 32) atomicOr(c.err, ERR_TIMEOUT);
     mphase ^= 1u;
     if (warp < G) {
       const float* r = stage + warp * PART;
@@ -1351,6 +1383,8 @@ __device__ void merge_segment(const DevCache& c, int layer, const DecodeArgs& a,
     ob[k] = rb[ch] * fb;
     lt[k] = fmaf(sm.lh[g], fh, rb[PARTIAL_L] * fb);
   }
+  if (!mbar_wait(&sm.mbar_r, (mphase >> 1) & 1u, DECODE_WAIT_LIMIT) && t == NTH - 32) atomicOr(c.err, ERR_TIMEOUT);
+  mphase ^= 2u;
   __syncthreads();
   {
     // O_hist R_V^T: thread (part p, column c) sums rows [p RP, (p + 1) RP) of column c
@@ -1393,21 +1427,51 @@ __device__ __forceinline__ void bf16_segment(const DevCache& c, int layer, const
 }
 
 // This CTA is done with segment (ri, head), whose records come from n2 INT2 CTAs
-// (c_lo ..) and one BF16 CTA: count it in the segment's counter; the CTA that
-// completes the count merges the segment.  The block before ends with a barrier,
-// so every record store of this CTA comes before the count.
+// (c_lo ..) and one BF16 CTA: count it in the segment's counter.  When the BF16
+// CTAs merge (bm: one segment each), an INT2 CTA only counts; otherwise the CTA
+// that completes the count (n2 + 1) merges the segment.  The block before ends
+// with a barrier, so every record store of this CTA comes before the count.
 template <int G, int GK>
 __device__ __forceinline__ void count_and_merge(const DevCache& c, int layer, const DecodeArgs& a, int ri, int head,
                                                 int c_lo, int n2, const float* recs, const float* bf16_recs,
-                                                float* out, Smem<G, GK>& sm, uint32_t& mphase) {
+                                                float* out, Smem<G, GK>& sm, uint32_t& mphase, bool bm) {
   if (threadIdx.x == 32 * (Tune<G, GK>::NW - 1) + 1) {   // a thread that issues no page copy
     int* cnt = c.dec_count + (size_t)a.r[ri].slot * c.Hkv + head;
-    const int last = atomic_add_acq_rel(cnt, 1) + 1 == n2 + 1;
+    const int last = !bm && atomic_add_acq_rel(cnt, 1) + 1 == n2 + 1;
+    if (bm) atomic_add_acq_rel(cnt, 1);
     if (last) atomicExch(cnt, 0);   // ready for the next launch
     sm.last = last;
   }
+  if (bm) return;
   __syncthreads();
   if (sm.last) merge_segment<G, GK>(c, layer, a, ri, head, c_lo, n2, recs, bf16_recs, out, sm, mphase);
+}
+
+// The BF16 CTA of segment (ri, head) merges it (bm): R_V^T is staged while it waits
+// (bounded) for the count of the n2 INT2 CTAs, then the records are merged.
+template <int G, int GK>
+__device__ __forceinline__ void wait_and_merge(const DevCache& c, int layer, const DecodeArgs& a, int ri, int head,
+                                               int c_lo, int n2, const float* recs, const float* bf16_recs,
+                                               float* out, Smem<G, GK>& sm, uint32_t& mphase) {
+  constexpr int NTH = Tune<G, GK>::THREADS;
+  const int t = threadIdx.x;
+  __syncthreads();   // the BF16 record is stored and the rings are free
+  if (t == NTH - 32) issue_rvt(c, layer, head, sm);
+  if (t == 32 * (Tune<G, GK>::NW - 1) + 1) {
+    int* cnt = c.dec_count + (size_t)a.r[ri].slot * c.Hkv + head;
+    bool done = false;
+    // about as long as a page wait of the same limit (rounds of up to 20 us)
+    for (uint32_t it = 0; it < 16u * a.dbg.wait_limit && !done; ++it) {
+      int v;
+      asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+      done = v >= n2;
+      if (!done) __nanosleep(64);
+    }
+    if (!done) atomicOr(c.err, ERR_TIMEOUT);
+    atomicExch(cnt, 0);   // ready for the next launch
+  }
+  __syncthreads();
+  merge_segment<G, GK>(c, layer, a, ri, head, c_lo, n2, recs, bf16_recs, out, sm, mphase, true);
 }
 
 // The append of the step's new token for (request ri, kv head), K and V: the
@@ -1476,16 +1540,24 @@ __global__ void __launch_bounds__(Tune<G, GK>::THREADS, 1)
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem<G, GK>& sm = *reinterpret_cast<Smem<G, GK>*>(smem_raw);
   const int t = threadIdx.x, warp = t >> 5;
-  const int cta = blockIdx.x;
+  // Roles: the last nbc blocks are the BF16 CTAs.  Blocks are placed on SMs in index
+  // order as the preceding launch's CTAs leave them, and the SMs left last are those
+  // that merged; the BF16 CTAs' work is short enough to start there late.
+  const int hi0 = a.ncta - a.nbc;
+  const int cta = (int)blockIdx.x >= hi0 ? (int)blockIdx.x - hi0 : (int)blockIdx.x + a.nbc;
   float* int2_recs = recs;
   float* bf16_recs = recs + ((size_t)a.n * c.Hkv + a.ncta) * G * PART;
   const uint32_t epoch = a.epoch;
   const int n2cta = a.ncta - a.nbc;   // INT2 CTAs
+  const bool bm = a.n * c.Hkv <= a.nbc;   // one segment per BF16 CTA: the BF16 CTAs merge
 
   if ((t & 31) == 0) {
 #pragma unroll
     for (int st = 0; st < STAGES; ++st) mbar_init(&sm.bar[warp][st], 1);
-    if (t == 0) mbar_init(&sm.mbar_m, 1);
+    if (t == 0) {
+      mbar_init(&sm.mbar_m, 1);
+      mbar_init(&sm.mbar_r, 1);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   uint32_t mphase = 0;        // phase of the merge staging barrier
@@ -1502,6 +1574,18 @@ __global__ void __launch_bounds__(Tune<G, GK>::THREADS, 1)
         const size_t off = ((size_t)layer * c.Hkv + s % c.Hkv) * D * D;
         const float* m = lane < 4 ? c.rot_k : lane < 8 ? c.rot_v : lane < 12 ? c.rot_kt : c.rot_vt;
         prefetch_l2(m + off + (size_t)(lane & 3) * (D * D / 4), D * D);
+      }
+    }
+    if (warp == 1) {
+      // q (and k / v of a step) of this CTA's segments into L2: the preceding grid may
+      // still write them, which L2 (the coherence point) then holds when they are read
+      // after the wait
+      const int lane = t & 31;
+      for (int s = cta + (lane >> 2) * a.nbc; s < a.n * c.Hkv; s += 8 * a.nbc) {
+        const size_t row = (size_t)a.r[s / c.Hkv].batch_row;
+        if ((lane & 3) == 0) prefetch_l2(q + (row * c.Hq + (size_t)(s % c.Hkv) * G) * D, G * D * 2);
+        if (epoch != 0 && (lane & 3) == 1) prefetch_l2(a.k_new + (row * c.Hkv + s % c.Hkv) * D, D * 2);
+        if (epoch != 0 && (lane & 3) == 2) prefetch_l2(a.v_new + (row * c.Hkv + s % c.Hkv) * D, D * 2);
       }
     }
     grid_dep_wait();    // q, k / v and the cache may have been written by the preceding grid
@@ -1521,11 +1605,14 @@ __global__ void __launch_bounds__(Tune<G, GK>::THREADS, 1)
       bf16_segment<G, GK>(c, layer, a, ri, head, q, sm, bf16_recs);
       int c_lo = 0, n2 = 0;
       if (R.npages > 0 && n2cta > 0) {
-        const int64_t s0 = R.cost_start + (int64_t)head * seg_units(R);
-        c_lo = cta_of(s0, n2cta, a.total_cost);
-        n2 = cta_of(s0 + seg_units(R) - 1, n2cta, a.total_cost) - c_lo + 1;
+        int c_hi;
+        segment_ctas(a, R.cost_start + (int64_t)head * seg_units(R), seg_units(R), c_lo, c_hi);
+        n2 = c_hi - c_lo + 1;
       }
-      count_and_merge<G, GK>(c, layer, a, ri, head, c_lo, n2, int2_recs, bf16_recs, out, sm, mphase);
+      if (bm)
+        wait_and_merge<G, GK>(c, layer, a, ri, head, c_lo, n2, int2_recs, bf16_recs, out, sm, mphase);
+      else
+        count_and_merge<G, GK>(c, layer, a, ri, head, c_lo, n2, int2_recs, bf16_recs, out, sm, mphase, false);
     }
     return;
   }
@@ -1546,6 +1633,10 @@ __global__ void __launch_bounds__(Tune<G, GK>::THREADS, 1)
     const Seg S = sm.seg[0];
     RkRows<G, GK> rk;
     if (S.valid) load_rk<G, GK>(c, layer, S.head, rk);
+    // q of the first segment into L2 (the preceding grid may still write it; L2 then
+    // holds what it wrote when q is read after the wait)
+    if (S.valid && t == 32)
+      prefetch_l2(q + ((size_t)a.r[S.ri].batch_row * c.Hq + (size_t)S.head * G) * D, G * D * 2);
     // After a decode launch of this cache, the history pages below npages - 2 (and
     // their page-table entries) are not written by any grid that may still run:
     // their first copies go out before the wait, while that grid finishes
@@ -1579,7 +1670,7 @@ __global__ void __launch_bounds__(Tune<G, GK>::THREADS, 1)
     {
       const Seg& S = sm.seg[cur];
       count_and_merge<G, GK>(c, layer, a, S.ri, S.head, S.c_lo, S.c_hi - S.c_lo + 1, int2_recs, bf16_recs, out, sm,
-                             mphase);
+                             mphase, bm);
     }
     // the next segment: first copies, q rotation
     if (sm.seg[nxt].valid) {
