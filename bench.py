@@ -832,7 +832,7 @@ def run_reference(args, log):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)   # a timed region of about a second at 100K x 32 layers
+    ap.add_argument("--steps", type=int, default=1400)   # a timed region of over a second at 100K x 32 layers
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--config", type=int, default=2, choices=sorted(WORKLOADS))

@@ -563,6 +563,9 @@ DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int
   // a decode step's BF16 CTAs also append the new token of each segment first
   const int64_t per_seg = DECODE_BF16_BLOCK_COST + (step ? DECODE_APPEND_COST : 0);
   int64_t nbc = (p.segments * per_seg + share - 1) / share;
+  // few segments: one BF16 CTA each, which then also merges its segment (the
+  // INT2 CTAs only count), however short its BF16 work
+  if (p.segments * 8 <= sms) nbc = std::max(nbc, p.segments);
   nbc = std::max<int64_t>(1, std::min<int64_t>({nbc, p.segments, cost > 0 ? sms / 2 : sms}));
   const int64_t n_int2 = std::min<int64_t>(sms - nbc, cost);
   p.nbc = static_cast<int>(nbc);

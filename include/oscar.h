@@ -214,9 +214,11 @@ oscar_status oscar_decode_workspace_bytes(const oscar_cache* cache, int32_t n, c
  *              no initial contents are needed.  Calls that share a workspace
  *              must not overlap on the GPU.
  * The decode is one kernel per launch of up to 64 requests: one CTA per SM
- * streams an equal share of the pages, and the last CTA to finish a (request,
- * kv head) merges it, counted in the cache's per-(request, kv head) counters
- * (layout decode_count_offset).  The kernel waits for everything before it on
+ * streams an equal share of the pages, and the CTAs that finish a (request, kv
+ * head) are counted in the cache's per-(request, kv head) counters (layout
+ * decode_count_offset); the last one merges it, or, when each (request, kv head)
+ * of the launch has a CTA of its own for the BF16 pages, that CTA waits for the
+ * count and merges.  The kernel waits for everything before it on
  * "stream", as any launch does; decodes of the same request must not overlap
  * on the GPU (on one stream they never do). */
 oscar_status oscar_decode_attention(oscar_cache* cache, int32_t layer, int32_t n, const int32_t* reqs,
