@@ -219,13 +219,13 @@ struct Smem {
   __align__(16) float state[NW][G][PART];   // each warp's partial (o, m, l) before the CTA combine
   union {
     struct {
-      float q[G][D];
+      __align__(16) float q[D][G];      // q as [channel][head]: one row holds the G heads
       float part[NPART][G][D];
       float norm[G];
       int qe[G];                        // q scale exponents
     } pro;                              // rotation of q
     struct {
-      __align__(16) float hist[G][D];   // O_hist of the merged segment
+      __align__(16) float hist[D][G];   // O_hist of the merged segment, [channel][head]
       float part[NPART][G][D];          // row parts of O_hist R_V^T
     } mrg;                              // merge of a segment (last CTA)
   } scr;
@@ -301,24 +301,44 @@ __device__ __forceinline__ void build_qfrag(const DevCache& c, const QRows<G, GK
 #pragma unroll
   for (int k = 0; k < QRows<G, GK>::N; ++k) {
     const int i = t + k * NTH;
-    if (i < G * D) sm.scr.pro.q[i / D][i % D] = __uint_as_float(static_cast<uint32_t>(qv.v[k]) << 16);
+    if (i < G * D) sm.scr.pro.q[i % D][i / D] = __uint_as_float(static_cast<uint32_t>(qv.v[k]) << 16);
   }
   __syncthreads();
+  // the G heads of a row in one load, two heads per packed fma (each an fmaf)
   float acc[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) acc[h] = 0.0f;
 #pragma unroll
   for (int i = 0; i < RP; ++i) {
     if (r0 + i < r1) {
+      const float* qr = sm.scr.pro.q[r0 + i];
+      const float2 r2 = make_float2(rk[i], rk[i]);
+      if constexpr (G % 4 == 0) {
 #pragma unroll
-      for (int h = 0; h < G; ++h) acc[h] = fmaf(sm.scr.pro.q[h][r0 + i], rk[i], acc[h]);
+        for (int h = 0; h < G; h += 4) {
+          const float4 x = *reinterpret_cast<const float4*>(qr + h);
+          const float2 a = __ffma2_rn(make_float2(x.x, x.y), r2, make_float2(acc[h], acc[h + 1]));
+          const float2 b = __ffma2_rn(make_float2(x.z, x.w), r2, make_float2(acc[h + 2], acc[h + 3]));
+          acc[h] = a.x;
+          acc[h + 1] = a.y;
+          acc[h + 2] = b.x;
+          acc[h + 3] = b.y;
+        }
+      } else if constexpr (G == 2) {
+        const float2 a = __ffma2_rn(*reinterpret_cast<const float2*>(qr), r2, make_float2(acc[0], acc[1]));
+        acc[0] = a.x;
+        acc[1] = a.y;
+      } else {
+        acc[0] = fmaf(qr[0], rk[i], acc[0]);
+      }
     }
   }
 #pragma unroll
   for (int h = 0; h < G; ++h) sm.scr.pro.part[part][h][ch] = acc[h];
   // |q_h|^2 by the warps of part 0 (warp h), rounded up
   if (w < G) {
-    const float4 x = *reinterpret_cast<const float4*>(&sm.scr.pro.q[w][4 * lane]);
+    const float4 x = make_float4(sm.scr.pro.q[4 * lane][w], sm.scr.pro.q[4 * lane + 1][w],
+                                 sm.scr.pro.q[4 * lane + 2][w], sm.scr.pro.q[4 * lane + 3][w]);
     float n2 = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, x.w * x.w)));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
@@ -1379,7 +1399,7 @@ __device__ void merge_segment(const DevCache& c, int layer, const DecodeArgs& a,
     const float Mt = fmaxf(M, bm);
     const float fh = M == -INFINITY ? 0.0f : exp2f(M - Mt);
     const float fb = bm == -INFINITY ? 0.0f : exp2f(bm - Mt);
-    if (i < G * D) sm.scr.mrg.hist[g][ch] = oh[k] * fh;
+    if (i < G * D) sm.scr.mrg.hist[ch][g] = oh[k] * fh;
     ob[k] = rb[ch] * fb;
     lt[k] = fmaf(sm.lh[g], fh, rb[PARTIAL_L] * fb);
   }
@@ -1395,8 +1415,27 @@ __device__ void merge_segment(const DevCache& c, int layer, const DecodeArgs& a,
 #pragma unroll 4
     for (int j = r0; j < r1; ++j) {
       const float rv = rvt_s[j * D + rch];
+      const float* hr = sm.scr.mrg.hist[j];
+      const float2 r2 = make_float2(rv, rv);
+      // the G heads of row j in one load, two heads per packed fma (each an fmaf)
+      if constexpr (G % 4 == 0) {
 #pragma unroll
-      for (int g = 0; g < G; ++g) acc[g] = fmaf(sm.scr.mrg.hist[g][j], rv, acc[g]);
+        for (int g = 0; g < G; g += 4) {
+          const float4 x = *reinterpret_cast<const float4*>(hr + g);
+          const float2 a = __ffma2_rn(make_float2(x.x, x.y), r2, make_float2(acc[g], acc[g + 1]));
+          const float2 b = __ffma2_rn(make_float2(x.z, x.w), r2, make_float2(acc[g + 2], acc[g + 3]));
+          acc[g] = a.x;
+          acc[g + 1] = a.y;
+          acc[g + 2] = b.x;
+          acc[g + 3] = b.y;
+        }
+      } else if constexpr (G == 2) {
+        const float2 a = __ffma2_rn(*reinterpret_cast<const float2*>(hr), r2, make_float2(acc[0], acc[1]));
+        acc[0] = a.x;
+        acc[1] = a.y;
+      } else {
+        acc[0] = fmaf(hr[0], rv, acc[0]);
+      }
     }
 #pragma unroll
     for (int g = 0; g < G; ++g) sm.scr.mrg.part[rpart][g][rch] = acc[g];
