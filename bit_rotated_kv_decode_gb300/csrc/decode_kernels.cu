@@ -1696,7 +1696,9 @@ __global__ void __launch_bounds__(Tune<G, GK>::THREADS, 1)
   // are needed, so that none stays in registers across the page loop
   for (int e = 0; sm.seg[e & 1].valid; ++e) {
     const int cur = e & 1, nxt = cur ^ 1;
-    if (t == 0) {
+    // planned by the last warp: warp w takes pages w, w + NW, ... of the segment, so
+    // the last warp has the fewest (one page of slack, where warp 0 has the most)
+    if (t == 32 * (Tune<G, GK>::NW - 1)) {
       int64_t prev;
       sm.seg[nxt] = plan_segment(a, c.Hkv, icta, sm.u_next, u0, u1, prev);
       sm.u_next = prev;
