@@ -113,6 +113,10 @@ def test_built_rotation_orthogonal():
 
 
 def test_logit_error_identity():
+    """The identity |Q K^T - Q K^^T|_F^2 = tr((K - K^) Q^T Q (K - K^)^T) that "Together AI
+    Open-Sources OSCAR" (MarkTechPost), section "What OSCAR Does Differently", builds its
+    objective on.  It holds for any K^, so this checks the page's argument; it pins
+    nothing of the oracle."""
     rng = np.random.default_rng(4)
     q = rng.standard_normal((64, 128))
     k = rng.standard_normal((300, 128))
@@ -124,6 +128,9 @@ def test_logit_error_identity():
 
 
 def test_logit_error_identity_with_oracle_quantiser():
+    """The same identity with K^ from the oracle's quantiser: a check of the page's
+    identity (true for any K^), not a pin of the quantiser, which the brute-force and
+    closed-form tests in test_oracle_quant.py pin."""
     q, k, v = _layer(5)
     rk, rv, tk, tv = rotation.build_layer_rotations(q, k, v, 0.9, 0.9)
     rk32 = rk[0].astype(np.float32).astype(np.float64)
