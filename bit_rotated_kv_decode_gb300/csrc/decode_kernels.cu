@@ -87,6 +87,7 @@ struct DecodeArgs {
   uint32_t epoch;                   // a decode step (append first) when non-zero
   int64_t total_cost;
   DecodeDebug dbg;
+  int32_t cstart[DECODE_MAX_INT2 + 1];   // INT2 CTA c holds cost units [cstart[c], cstart[c + 1])
   const uint16_t* k_new;   // fused step: the appended token's K / V rows (batch rows), else null
   const uint16_t* v_new;
   DecodeReq r[DECODE_PER_LAUNCH];
@@ -1189,7 +1190,9 @@ __device__ void bf16_block(const DevCache& c, int layer, const DecodeReq& R, int
 }
 
 // ---- the decode kernel --------------------------------------------------------------
-__device__ __forceinline__ int64_t cta_begin(int c, int ncta, int64_t total) { return (int64_t)c * total / ncta; }
+// First cost unit of INT2 CTA c: c total / n2 (64-bit), computed on the host at
+// launch so that no CTA runs 64-bit divisions before its first pages.
+__device__ __forceinline__ int64_t cta_begin(const DecodeArgs& a, int c) { return a.cstart[c]; }
 
 // Cost units of one segment on the INT2 line: a set-up (the q rotation and the
 // latency of the first pages, paid again by a CTA that enters the segment from
@@ -1204,26 +1207,30 @@ __device__ __forceinline__ void segment_of(const DecodeArgs& a, int Hkv, int64_t
   ri = 0;
   while (ri + 1 < a.n && a.r[ri + 1].cost_start <= u) ++ri;
   const int64_t per = seg_units(a.r[ri]);
-  h = static_cast<int>((u - a.r[ri].cost_start) / per);
+  h = static_cast<int>(static_cast<int32_t>(u - a.r[ri].cost_start) / static_cast<int32_t>(per));   // < 2^31
   if (h >= Hkv) h = Hkv - 1;
   s0 = a.r[ri].cost_start + (int64_t)h * per;
 }
 
 // INT2 CTA (index among the INT2 CTAs) whose cost range holds unit u.
-__device__ __forceinline__ int cta_of(int64_t u, int ncta, int64_t total) {
-  int c = static_cast<int>(u * ncta / total);
-  while (c > 0 && cta_begin(c, ncta, total) > u) --c;
-  while (c + 1 < ncta && cta_begin(c + 1, ncta, total) <= u) ++c;
-  return c;
+__device__ __forceinline__ int cta_of(const DecodeArgs& a, int64_t u) {
+  int lo = 0, hi = a.ncta - a.nbc - 1;   // the last CTA c with cstart[c] <= u
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.cstart[mid] <= u)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
 }
 
 // The INT2 CTAs that hold pages of a segment starting at cost unit s0 with
 // units seg units: those whose ranges meet [page 0's unit, end).  A CTA whose
 // range meets only the segment's set-up units takes no part in it.
 __device__ __forceinline__ void segment_ctas(const DecodeArgs& a, int64_t s0, int64_t units, int& c_lo, int& c_hi) {
-  const int n2 = a.ncta - a.nbc;
-  c_lo = cta_of(s0 + DECODE_SEGMENT_SETUP_COST, n2, a.total_cost);
-  c_hi = cta_of(s0 + units - 1, n2, a.total_cost);
+  c_lo = cta_of(a, s0 + DECODE_SEGMENT_SETUP_COST);
+  c_hi = cta_of(a, s0 + units - 1);
 }
 
 // The segment holding INT2 cost unit u of this INT2 CTA's range [u0, u1), or
@@ -1658,7 +1665,7 @@ __global__ void __launch_bounds__(Tune<G, GK>::THREADS, 1)
 
   // ---- an INT2 CTA: its range [u0, u1) of the INT2 pages, segment by segment
   const int icta = cta - a.nbc;
-  const int64_t u0 = cta_begin(icta, n2cta, a.total_cost), u1 = cta_begin(icta + 1, n2cta, a.total_cost);
+  const int64_t u0 = cta_begin(a, icta), u1 = cta_begin(a, icta + 1);
   if (t == 0) {
     int64_t prev;
     sm.seg[0] = plan_segment(a, c.Hkv, icta, u1 - 1, u0, u1, prev);
@@ -1753,6 +1760,11 @@ cudaError_t launch_decode_t(const DevCache& c, int layer, const DecodeReq* reqs,
   a.epoch = k_new != nullptr ? epoch : 0u;
   a.total_cost = p.total_cost;
   a.dbg = dbg;
+  {
+    const int n2 = p.ncta - p.nbc;
+    if (n2 > DECODE_MAX_INT2 || p.total_cost > INT32_MAX) return cudaErrorInvalidValue;
+    for (int i = 0; i <= n2; ++i) a.cstart[i] = static_cast<int32_t>((int64_t)i * p.total_cost / (n2 > 0 ? n2 : 1));
+  }
   a.k_new = a.epoch != 0 ? k_new : nullptr;
   a.v_new = a.epoch != 0 ? v_new : nullptr;
   for (int i = 0; i < p.n; ++i) a.r[i] = reqs[i];

@@ -567,7 +567,7 @@ DecodePlan plan_decode(const oscar_cache* c, int32_t layer, int32_t n, const int
   // INT2 CTAs only count), however short its BF16 work
   if (p.segments * 8 <= sms) nbc = std::max(nbc, p.segments);
   nbc = std::max<int64_t>(1, std::min<int64_t>({nbc, p.segments, cost > 0 ? sms / 2 : sms}));
-  const int64_t n_int2 = std::min<int64_t>(sms - nbc, cost);
+  const int64_t n_int2 = std::min<int64_t>({sms - nbc, cost, (int64_t)DECODE_MAX_INT2});
   p.nbc = static_cast<int>(nbc);
   p.ncta = static_cast<int>(nbc + n_int2);
   p.partial_bytes = align256((size_t)(2 * p.segments + p.ncta) * decode_record_bytes(c->G()));

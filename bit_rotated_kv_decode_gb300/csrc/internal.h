@@ -150,6 +150,7 @@ constexpr int DECODE_APPEND_COST = 30;
 // Cost units in front of each segment's pages on the INT2 line: the set-up a CTA
 // pays on entering a segment (q rotation, first-page latency), in INT2 pages.
 constexpr int DECODE_SEGMENT_SETUP_COST = 40;
+constexpr int DECODE_MAX_INT2 = 256;            // INT2 CTAs of a decode launch (at most one per SM)
 constexpr int DECODE_BF16_ITEMS = 1 + RING_PAGES;   // BF16 pages per (request, kv head)
 struct DecodePlan {
   int n;
