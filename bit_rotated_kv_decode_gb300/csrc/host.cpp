@@ -745,7 +745,9 @@ oscar_status oscar_decode_step(oscar_cache* c, int32_t layer, int32_t n, const i
 
 oscar_status oscar_debug_decode_hooks(oscar_cache* c, uint32_t wait_limit, int32_t hold_copy) {
   if (!c) return OSCAR_ERR_INVALID_ARG;
-  if (wait_limit < 1 || hold_copy < -1) return c->fail(OSCAR_ERR_INVALID_ARG, "bad hook values");
+  // the device's other bounded waits take multiples of wait_limit in 32 bits
+  if (wait_limit < 1 || wait_limit > (1u << 24) || hold_copy < -1)
+    return c->fail(OSCAR_ERR_INVALID_ARG, "bad hook values");
   c->dbg.wait_limit = wait_limit;
   c->dbg.hold_copy = hold_copy;
   return OSCAR_OK;

@@ -270,7 +270,8 @@ oscar_status oscar_decode_step(oscar_cache* cache, int32_t layer, int32_t n, con
 /* Failure-detection hooks of the decode launches of this cache (test use; the
  * pages have no counterpart).  wait_limit: rounds (up to 20 us each) a bounded
  * device wait on a page copy makes before it gives up and reports
- * OSCAR_ERR_TIMEOUT through oscar_cache_check (default 100000, must be >= 1).
+ * OSCAR_ERR_TIMEOUT through oscar_cache_check (default 100000, from 1 to
+ * 2^24; the other bounded waits of a decode launch scale with it).
  * hold_copy: the page copy (numbered in issue order, from 0, across the segments
  * of the CTA) of warp 0 of every decode CTA that streams history pages that is
  * never issued, so that its wait runs out (-1, the default, holds none).  A warp whose wait ran out issues no

@@ -80,7 +80,7 @@ def test_held_copy_times_out_then_next_launch_is_clean(b, hold):
 
 def test_hook_values_are_checked(b):
     s, _ = _setup(b, [100])
-    for wl, hold in ((0, -1), (10, -2)):
+    for wl, hold in ((0, -1), (10, -2), ((1 << 24) + 1, -1)):
         with pytest.raises(b.OscarError) as e:
             s.cache.debug_decode_hooks(wait_limit=wl, hold_copy=hold)
         assert e.value.status == b.OSCAR_ERR_INVALID_ARG

@@ -278,3 +278,16 @@ def test_bf16_baseline_workspace_plan(b):
     assert ws([0], 32, 8) == 0
     assert ws([100], 20, 8) == 0                       # query heads not a multiple of kv heads
     assert ws([100] * 65, 32, 8) == 0                  # more than 64 requests per launch
+
+
+def test_decode_hook_values_checked_on_the_host(b):
+    cfg = b.make_config(1, 32, 8, 1, 4, 8)
+    tau = np.ones((1, 8), np.float32)
+    cache = b.OscarCache(cfg, tau_k=tau, tau_v=tau, dry_run=True)
+    cache.debug_decode_hooks(wait_limit=1, hold_copy=-1)
+    cache.debug_decode_hooks(wait_limit=1 << 24, hold_copy=3)
+    for wl, hold in ((0, -1), ((1 << 24) + 1, -1), (100, -2)):
+        with pytest.raises(b.OscarError) as e:
+            cache.debug_decode_hooks(wait_limit=wl, hold_copy=hold)
+        assert e.value.status == b.OSCAR_ERR_INVALID_ARG
+    cache.debug_decode_hooks()
