@@ -93,9 +93,6 @@ struct DecodeArgs {
   DecodeReq r[DECODE_PER_LAUNCH];
 };
 
-__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
 // Programmatic dependent launch: wait for the preceding grid (complete, its
 // writes visible); allow the next grid to be scheduled.
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -743,7 +740,7 @@ __device__ __forceinline__ void int2_pages(const DevCache& c, int layer, const D
           const float4 m0 = sm.meta[warp][tok], m1 = sm.meta[warp][tok + 8];
           sw[0][mt] = make_float2(m0.z, m1.z);
           zv[0][mt] = make_float2(m0.w, m1.w);
-          float4 n0 = m0, n1 = m1;
+          [[maybe_unused]] float4 n0 = m0, n1 = m1;   // group 1's meta (G_K = 64)
           if constexpr (NGR == 2) {
             n0 = sm.meta2[warp][tok];
             n1 = sm.meta2[warp][tok + 8];
